@@ -1,0 +1,449 @@
+#!/usr/bin/env python
+"""Benchmark of the MoE FFN decode layer on GB300.
+
+Default workload: the Large layer (H=7168, 512 routed experts, top-16,
+F=2048, shared expert F=2048, 4-bit affine group-64 experts, 8-bit router)
+decoding B=1 token per step, every expert resident in HBM.  A step is one
+full pass of the layer: router GEMV + softmax/top-k + grouping, gate|up +
+SwiGLU of the 16 routed experts and the shared expert, down projection and
+the weighted combine.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--batch B]
+                  [--impl ours|reference]
+
+One JSON line on rank 0.  `value` is tokens/s over all ranks (each rank runs
+an independent replica of the layer: the path has no cross-GPU exchange).
+`--impl reference` times the fp64 CPU oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer decode tokens/s + achieved HBM GB/s vs ~8 TB/s peak (B=1/4/16)"
+WORKLOAD = "large-decode"
+NOMINAL_HBM_GBS = 8000.0
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "gateup_kernel_large_decode_b1.txt")
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--batch", type=int, default=1)
+    p.add_argument("--pool", type=int, default=64, help="distinct hidden-state batches rotated")
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--no-extras", action="store_true",
+                   help="skip the B=4/16 lines, e2e, per-kernel and CPU-baseline passes")
+    a = p.parse_args()
+    a.warmup = max(a.warmup, 3)
+    return a
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_id}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [v.strip() for v in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        win = [p for t, p in self.samples if t0 - 0.15 <= t <= t1 + 0.15]
+        if not win and self.samples:
+            win = [min(self.samples, key=lambda s: abs(s[0] - t1))[1]]
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+
+        sm = [num(p[1]) for p in win if num(p[1]) is not None]
+        mx = [num(p[2]) for p in win if num(p[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in win for i in range(4) if p[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(win),
+                "power_w_max": max((num(p[3]) or 0.0) for p in win)}
+
+
+# ----------------------------------------------------------------- helpers
+
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, v: float, device) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def record_bytes_unpadded(H, F):
+    return 3 * (F * H // 2) + 3 * (F * H // 64) * 4
+
+
+def layer_step_bytes(s, B, distinct: float, with_f32: bool) -> dict:
+    """Algorithmic bytes of one step: every weight byte of the distinct active
+    experts, the shared expert and the router once, activations once."""
+    rec, sh = record_bytes_unpadded(s.H, s.F), record_bytes_unpadded(s.H, s.Fs) if s.Fs else 0
+    router = s.E * s.H + s.E * (s.H // 64) * 4
+    act = B * s.H * 2 + B * s.H * (2 + (4 if with_f32 else 0)) + B * s.k * 8
+    gateup_w = lambda F: 2 * (F * s.H // 2) + 2 * (F * s.H // 64) * 4
+    pairs = B * s.k
+    gateup = distinct * gateup_w(s.F) + (gateup_w(s.Fs) if s.Fs else 0) + B * s.H * 2 + \
+        (pairs * s.F + B * s.Fs) * 4
+    return {"step": distinct * rec + sh + router + act, "gateup": gateup}
+
+
+def gpu_id_for(device_index: int) -> str:
+    import torch
+    try:
+        p = torch.cuda.get_device_properties(device_index)
+        return f"{p.pci_domain_id:08x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0"
+    except Exception:
+        return str(device_index)
+
+
+def read_traffic():
+    """dram bytes per launch of the gate|up kernel from the committed ncu
+    summary, or None when the kernel source changed since the capture."""
+    try:
+        lines = open(PROFILE_SUMMARY).read().splitlines()
+    except OSError:
+        return None
+    kv = {}
+    for ln in lines:
+        if ":" in ln and not ln.startswith(" "):
+            k, v = ln.split(":", 1)
+            kv[k.strip()] = v.strip()
+    src = os.path.join(ROOT, "quantized_routed_expert_gemv_gb300", "csrc", "decode.cu")
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    if kv.get("decode_cu_sha256_16") != h:
+        return None
+    try:
+        return float(kv["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ----------------------------------------------------------------- reference arm
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    from quantized_routed_expert_gemv_gb300 import synth
+
+    wl = synth.WORKLOADS[WORKLOAD]
+    s = wl.shape
+    rc, rsb = synth.router(wl.weight_seed, 0, s.E, s.H)
+    shared = synth.expert_record(wl.weight_seed, 0, s.E, s.H, s.Fs)
+    orc = oracle.Layer(s.H, s.E, s.k, s.F, s.Fs, {}, shared, rc, rsb)
+    B = args.batch
+
+    def step(i):
+        xs = [synth.hidden(wl.input_seed, 1000 + (i % args.pool), t, s.H) for t in range(B)]
+        for x in xs:                       # untimed: draw the records this token needs
+            _, ids, _ = orc.route(x)
+            for e in ids:
+                if int(e) not in orc._recs:
+                    orc.set_record(int(e), synth.expert_record(wl.weight_seed, 0, int(e), s.H, s.F))
+        t0 = time.perf_counter()
+        for x in xs:
+            orc.token(x)
+        dt = time.perf_counter() - t0
+        for e in list(orc._recs):          # keep host memory bounded
+            orc._recs.pop(e)
+        return dt
+
+    for i in range(args.warmup):
+        step(i)
+    total = sum(step(args.warmup + i) for i in range(args.steps))
+    value = B * args.steps / total
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_dict(s, B),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{args.steps} timed steps of B={B} token(s) through the "
+                                   "single-threaded fp64 C oracle"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def config_dict(s, B):
+    return {"workload": f"{WORKLOAD}: H={s.H} E={s.E} top-{s.k} F={s.F} Fs={s.Fs}, "
+                        f"4-bit affine group-64 experts, 8-bit router, all experts in HBM",
+            "batch": B, "hidden": s.H, "experts": s.E, "top_k": s.k, "ffn": s.F,
+            "shared_ffn": s.Fs,
+            "l2": "inputs larger than L2: >=425 MB of distinct weights per step, hidden "
+                  "states rotated over a pool of distinct batches"}
+
+
+# ----------------------------------------------------------------- our arm
+
+def time_graphs(torch, graphs, K, W, stream, world, device):
+    for i in range(W):
+        graphs[i % len(graphs)].replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(K):
+            graphs[i % len(graphs)].replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    barrier(world)
+    ms = e0.elapsed_time(e1)
+    return max_over_ranks(world, ms, device), t0, t1
+
+
+def run_ours(args, world, rank, local):
+    import numpy as np
+    import torch
+
+    from quantized_routed_expert_gemv_gb300 import moe, synth
+    from quantized_routed_expert_gemv_gb300.device import DeviceLayer, bf16_tensor
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    wl = synth.WORKLOADS[WORKLOAD]
+    s = wl.shape
+    batches = [args.batch] if args.no_extras else sorted({args.batch, 1, 4, 16})
+    maxB = max(batches)
+    dl = DeviceLayer(s, wl.weight_seed, max_tokens=maxB, device=device)
+    stream = torch.cuda.Stream(device)
+
+    def make(B):
+        xs = np.stack([np.stack([synth.hidden(wl.input_seed, 1000 + p, t, s.H) for t in range(B)])
+                       for p in range(args.pool)])
+        x = bf16_tensor(xs, device)
+        outs = dl.outputs(B)
+        graphs = []
+        with torch.cuda.stream(stream):
+            dl.decode(x[0], outs, stream.cuda_stream)  # warm the path before capture
+        torch.cuda.synchronize()
+        distinct = []
+        for p in range(args.pool):
+            with torch.cuda.stream(stream):
+                dl.decode(x[p], outs, stream.cuda_stream)
+            stream.synchronize()
+            distinct.append(len(np.unique(outs[2].cpu().numpy())))
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                dl.decode(x[p], outs, stream.cuda_stream)
+            graphs.append(g)
+        torch.cuda.synchronize()
+        return xs, x, outs, graphs, float(np.mean(distinct))
+
+    results = {}
+    clocks = ClockSampler(gpu_id_for(local))
+    clocks.start()
+    time.sleep(0.3)
+    main = None
+    for B in batches:
+        xs, x, outs, graphs, distinct = make(B)
+        K = args.steps if B == args.batch else min(args.steps, 2000)
+        ms, t0, t1 = time_graphs(torch, graphs, K, args.warmup, stream, world, device)
+        assert dl.check(stream.cuda_stream) == moe.MOE_OK, moe.last_error()
+        nbytes = layer_step_bytes(s, B, distinct, with_f32=True)
+        r = {"tokens_per_s": B * K * world / (ms / 1e3), "ms_per_step": ms / K,
+             "distinct_experts": distinct, "bytes_per_step": nbytes["step"],
+             "layer_gbs": nbytes["step"] / (ms / K / 1e3) / 1e9}
+        r["layer_frac_of_8tbs"] = r["layer_gbs"] / NOMINAL_HBM_GBS
+        results[B] = r
+        if B == args.batch:
+            main = dict(r, K=K, t0=t0, t1=t1, xs=xs, x=x, outs=outs, nbytes=nbytes)
+        del graphs
+    time.sleep(0.2)
+    clocks.stop()
+    clk = clocks.summary(main["t0"], main["t1"])
+
+    out = {"metric": METRIC, "value": main["tokens_per_s"], "unit": "tokens/s", "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": main["ms_per_step"],
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+           "data": "synthetic (seeded SplitMix64 layer and hidden states)",
+           "config": config_dict(s, args.batch), "gpu_launches": 3 * args.steps, "clocks": clk,
+           "layer": {"gbs": main["layer_gbs"], "frac_of_8tbs": main["layer_frac_of_8tbs"],
+                     "bytes_per_step": main["bytes_per_step"],
+                     "distinct_experts": main["distinct_experts"]},
+           "by_batch": {str(b): {k: v for k, v in r.items()} for b, r in results.items()}}
+
+    peaks = {}
+    try:
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except OSError:
+        pass
+    peak = peaks.get("hbm_gbs", 6800.0)
+    peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
+
+    if not args.no_extras:
+        # per-kernel durations: events between the three kernels (no PDL overlap)
+        B = args.batch
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        moe.moe_set_profile_events(dl.handle, [e.cuda_event for e in evs])
+        Kp = min(args.steps, 200)
+        sums = [0.0, 0.0, 0.0]
+        x, outs = main["x"], main["outs"]
+        with torch.cuda.stream(stream):
+            for i in range(Kp + 5):
+                dl.decode(x[i % args.pool], outs, stream.cuda_stream)
+                evs[3].synchronize()
+                if i >= 5:
+                    for j in range(3):
+                        sums[j] += evs[j].elapsed_time(evs[j + 1])
+        moe.moe_set_profile_events(dl.handle, None)
+        per = [v / Kp for v in sums]
+        gateup_s = per[1] / 1e3
+        achieved = main["nbytes"]["gateup"] / gateup_s / 1e9
+        out["roofline"] = {"bound": "hbm", "kernel": "gateup_kernel", "achieved": achieved,
+                           "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                           "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)",
+                           "traffic": read_traffic(),
+                           "algorithmic_bytes_per_launch": main["nbytes"]["gateup"],
+                           "kernel_ms": {"router": per[0], "gateup": per[1], "down": per[2]}}
+
+        # end to end through the host-buffer entry point
+        xs = main["xs"]
+        hx = torch.from_numpy(xs.view(np.int16)).pin_memory()
+        hob = torch.empty((B, s.H), dtype=torch.int16).pin_memory()
+        hids = torch.empty((B, s.k), dtype=torch.int32).pin_memory()
+        hw = torch.empty((B, s.k), dtype=torch.float32).pin_memory()
+        Ke = min(args.steps, 500)
+        for i in range(args.warmup):
+            moe.moe_decode_host(dl.handle, hx[i % args.pool].data_ptr(), B, hob.data_ptr(), None,
+                                hids.data_ptr(), hw.data_ptr(), dl.ws.data_ptr(), dl.ws_bytes,
+                                stream.cuda_stream)
+        barrier(world)
+        t0 = time.perf_counter()
+        for i in range(Ke):
+            moe.moe_decode_host(dl.handle, hx[i % args.pool].data_ptr(), B, hob.data_ptr(), None,
+                                hids.data_ptr(), hw.data_ptr(), dl.ws.data_ptr(), dl.ws_bytes,
+                                stream.cuda_stream)
+        dt = max_over_ranks(world, time.perf_counter() - t0, device)
+        out["e2e"] = {"value": B * Ke * world / dt, "unit": "tokens/s",
+                      "h2d_bytes_per_step": B * s.H * 2,
+                      "d2h_bytes_per_step": B * s.H * 2 + B * s.k * 8, "steps": Ke,
+                      "entry": "moe_decode_host (pinned host buffers, copies + sync per step)"}
+
+        if rank == 0 and world == 1:
+            out["cpu_baseline"] = cpu_baseline(wl, s)
+    dl.close()
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+def cpu_baseline(wl, s, target_s=15.0):
+    import oracle
+    from quantized_routed_expert_gemv_gb300 import synth
+    rc, rsb = synth.router(wl.weight_seed, 0, s.E, s.H)
+    shared = synth.expert_record(wl.weight_seed, 0, s.E, s.H, s.Fs)
+    orc = oracle.Layer(s.H, s.E, s.k, s.F, s.Fs, {}, shared, rc, rsb)
+    total, n = 0.0, 0
+    while total < target_s and n < 32:
+        x = synth.hidden(wl.input_seed, 1000 + n, 0, s.H)
+        _, ids, _ = orc.route(x)
+        for e in ids:
+            if int(e) not in orc._recs:
+                orc.set_record(int(e), synth.expert_record(wl.weight_seed, 0, int(e), s.H, s.F))
+        t0 = time.perf_counter()
+        orc.token(x)
+        total += time.perf_counter() - t0
+        n += 1
+        for e in list(orc._recs):
+            orc._recs.pop(e)
+    return {"value": n / total, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} B=1 tokens of the same workload through the single-threaded fp64 C "
+                      f"oracle ({total:.1f} s of CPU time; record generation untimed)"}
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,181 @@
+/*
+ * moe.h -- C ABI of a GB300 (sm_103a) Mixture-of-Experts FFN layer.
+ *
+ * The layer, per token x (bf16, H values):
+ *   1. router: logits l_e = sum_j W_r[e][j] x_j + beta_e over E experts, W_r
+ *      8-bit affine with one bf16 (scale, bias) per 64 inputs;
+ *   2. top-k by (logit descending, expert id ascending), weights
+ *      p_i = softmax over all experts renormalised over the k chosen ones;
+ *   3. for every chosen expert and the always-resident shared expert:
+ *      h = silu(W_g x) * (W_u x), y = W_d h, with W_g, W_u, W_d 4-bit affine,
+ *      group 64 along the input dimension;
+ *   4. out = y_shared + sum_i p_i y_{e_i}.
+ * Sources: TurboFieldfare page ("Gemma 4 26B'yi 2GB RAM ile çalıştıran açık
+ * kaynak motor"), sections "Belleği azaltan çalışma yapısı" (MLX affine
+ * 4-bit group 64 experts, 8-bit router) and "Token üretim süreci" (router on
+ * the GPU, top-8 ids against a bounded LFU cache, shared expert computed
+ * while misses are read, shared and routed outputs combined, prompt prefill
+ * in chunks of at most 128 tokens so one fetched expert serves several
+ * rows); WASTE page ("Kimi K3'ü 29 GB RAM'de ..."), section "Disk streaming
+ * mimarisi" (gate, up and down adjacent in one 4 KiB-aligned expert record).
+ *
+ * Conventions for every call:
+ *   - Return 0 (MOE_OK) or a negative MOE_ERR_* code; moe_last_error()
+ *     gives a thread-local message for the last failing call.
+ *   - "device" pointers are CUDA global-memory addresses on the current
+ *     device; "host" pointers are CPU addresses (pinned for best copy speed).
+ *   - The caller owns every device and host buffer: weights, activations,
+ *     outputs, workspace and slot pools.  A moe_layer handle stores pointers
+ *     and shapes only; moe_close frees host bookkeeping only.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy stream).
+ *     Device work is asynchronous on it; argument errors are detected on the
+ *     host before any launch.  Errors raised by device code (MOE_ERR_TIMEOUT,
+ *     MOE_ERR_RESIDENCY) are latched in the workspace and returned by
+ *     moe_check().
+ *   - Device pointers must be 16-byte aligned (MOE_ERR_ALIGN otherwise);
+ *     expert records additionally start on 256-byte boundaries.
+ *   - Hidden-state magnitudes must stay below 2^40 (the GEMV kernels pre-
+ *     scale activations by powers of two up to 2^85); NaN/Inf inputs are
+ *     outside the contract.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+    MOE_OK = 0,
+    MOE_ERR_ARG = -1,         /* bad shape, size, null pointer, wrong handle */
+    MOE_ERR_ALIGN = -2,       /* pointer not 16-byte (records: 256-byte) aligned */
+    MOE_ERR_CUDA = -3,        /* a CUDA runtime call failed; see moe_last_error() */
+    MOE_ERR_TIMEOUT = -4,     /* a bounded device-side wait expired */
+    MOE_ERR_RESIDENCY = -5,   /* a slot's expert tag did not match the routed id */
+    MOE_ERR_NOMEM = -6,       /* host bookkeeping allocation failed */
+    MOE_ERR_UNSUPPORTED = -7  /* device is not sm_103 or lacks resources */
+};
+
+/* Shapes and quantisation of one layer.  Limits: hidden H in [64, 8192] and a
+ * multiple of 64; n_experts E in [1, 1024]; top_k in [1, min(E, 32)]; ffn F
+ * and shared_ffn Fs multiples of 64 in [64, 8192] (Fs = 0: no shared
+ * expert); group must be 64, wbits 4, rbits 8; max_tokens in [1, 128] bounds
+ * B for decode and T for prefill chunks. */
+typedef struct moe_layer_desc {
+    int32_t hidden;
+    int32_t n_experts;
+    int32_t top_k;
+    int32_t ffn;
+    int32_t shared_ffn;
+    int32_t group;
+    int32_t wbits;
+    int32_t rbits;
+    int32_t max_tokens;
+} moe_layer_desc;
+
+/* Byte offsets of the regions of one expert record with FFN width F:
+ *   [gate codes F x H/2][up codes F x H/2][down codes H x F/2]
+ *   [gate sb F x H/64][up sb F x H/64][down sb H x F/64]
+ * Codes are row-major [out][in], element j of a row in byte j/2, low nibble
+ * for even j.  One little-endian 32-bit "sb" word per (row, group of 64
+ * inputs): bits 0..15 the bf16 scale s, bits 16..31 the bf16 bias b, so
+ * w = s*q + b.  `stride` is `bytes` rounded up to 4096. */
+typedef struct moe_record_layout {
+    uint64_t gate_codes, up_codes, down_codes;
+    uint64_t gate_sb, up_sb, down_sb;
+    uint64_t bytes;
+    uint64_t stride;
+} moe_record_layout;
+
+/* Device weights of one layer (all caller-owned, read-only to the library).
+ *   expert_records: E records back to back at stride moe_expert_bytes(ffn);
+ *                   may be NULL for a layer used only through the residency
+ *                   API, whose slot pool then holds the records.
+ *   shared_record:  one record with FFN width shared_ffn (NULL iff Fs == 0).
+ *   router_codes:   uint8 [E][H], one 8-bit code per weight.
+ *   router_sb:      uint32 [E][H/64] sb words as in moe_record_layout.
+ *   router_logit_bias: float [E] added to the logits, or NULL for none. */
+typedef struct moe_layer_weights {
+    const void *expert_records;
+    const void *shared_record;
+    const uint8_t *router_codes;
+    const uint32_t *router_sb;
+    const float *router_logit_bias;
+} moe_layer_weights;
+
+typedef struct moe_layer moe_layer;
+
+/* Record layout for hidden H and FFN width F (see moe_record_layout).
+ * Returns MOE_ERR_ARG for shapes outside the limits above. */
+int moe_record_layout_of(int32_t hidden, int32_t ffn, moe_record_layout *out);
+
+/* Stride in bytes of one expert record of width `ffn` (0 on bad shapes). */
+size_t moe_expert_bytes(const moe_layer_desc *desc, int32_t ffn);
+
+/* Validates shapes and pointers, queries the device (must be sm_103) and
+ * returns a handle.  No device allocation, no device work. */
+int moe_open(const moe_layer_desc *desc, const moe_layer_weights *weights, moe_layer **out);
+
+/* Frees the handle (host memory only).  NULL is accepted. */
+void moe_close(moe_layer *layer);
+
+/* Bytes of device workspace that calls with up to `max_tokens` tokens need
+ * (0 on a bad handle or size).  One workspace must not be used by two calls
+ * that overlap on the GPU. */
+size_t moe_workspace_bytes(const moe_layer *layer, int32_t max_tokens);
+
+/* Zero-fills a workspace (cudaMemsetAsync on `stream`).  Required once
+ * before the first call that uses it; the library keeps its counters at
+ * zero between calls afterwards. */
+int moe_workspace_init(const moe_layer *layer, void *workspace, size_t workspace_bytes,
+                       void *stream);
+
+/* Decode step for B tokens (1 <= B <= max_tokens), all experts resident.
+ *   x:        device bf16 [B][H] hidden states.
+ *   out_bf16: device bf16 [B][H], round-to-nearest-even of the fp32 result.
+ *   out_f32:  device float [B][H] or NULL.
+ *   ids:      device int32 [B][k] chosen experts, by (logit desc, id asc).
+ *   weights:  device float [B][k] routing weights (sum to 1 per token).
+ * B == 0 returns MOE_OK and does nothing.  Fully asynchronous: no host sync. */
+int moe_decode(moe_layer *layer, const uint16_t *x, int32_t B, uint16_t *out_bf16,
+               float *out_f32, int32_t *ids, float *weights, void *workspace,
+               size_t workspace_bytes, void *stream);
+
+/* Prefill chunk of T tokens (1 <= T <= min(128, max_tokens)); same buffers and
+ * semantics as moe_decode.  Expert work runs as a grouped GEMM on the 5th-gen
+ * tensor cores (tcgen05, accumulators in tensor memory). */
+int moe_prefill_chunk(moe_layer *layer, const uint16_t *x, int32_t T, uint16_t *out_bf16,
+                      float *out_f32, int32_t *ids, float *weights, void *workspace,
+                      size_t workspace_bytes, void *stream);
+
+/* moe_decode with HOST buffers: copies x in, runs the step, copies every
+ * output back (out_f32_host may be NULL) and synchronises `stream` before it
+ * returns.  Device staging lives in the workspace. */
+int moe_decode_host(moe_layer *layer, const uint16_t *x_host, int32_t B,
+                    uint16_t *out_bf16_host, float *out_f32_host, int32_t *ids_host,
+                    float *weights_host, void *workspace, size_t workspace_bytes,
+                    void *stream);
+
+/* Synchronises `stream`, then reads and clears the error word that device
+ * code latches in `workspace`: MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_RESIDENCY. */
+int moe_check(const moe_layer *layer, void *workspace, void *stream);
+
+/* Profiling hook.  With `events` pointing to four cudaEvent_t (passed as
+ * void*), later moe_decode / moe_prefill_chunk calls on this layer record
+ * events[0] before the router kernel, events[1] before the gate|up (or
+ * grouped-GEMM) kernel, events[2] before the down kernel and events[3] after
+ * it, and launch without programmatic dependent launch so the intervals are
+ * per kernel.  NULL switches the hook off.  The events stay caller-owned. */
+int moe_set_profile_events(moe_layer *layer, void *const *events);
+
+/* Thread-local description of the last error (never NULL). */
+const char *moe_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H */

@@ -1,0 +1,383 @@
+// api.cu -- the C ABI of include/moe.h: argument validation, layer
+// geometry, workspace carving and kernel launch order.  No CPU compute path
+// exists: every step of the layer runs in the kernels of decode.cu /
+// prefill.cu.
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include <cuda_runtime.h>
+
+#include "../../include/moe.h"
+#include "kernels.h"
+
+namespace moe {
+size_t router_smem_bytes(int E);
+size_t gateup_smem_bytes(const LayerArgs& a, int ntok);
+size_t down_smem_bytes(const LayerArgs& a, int ntok);
+cudaError_t set_decode_attributes(int smem_optin);
+cudaError_t launch_decode(const LayerArgs& a, int num_sms, cudaStream_t st);
+cudaError_t set_prefill_attributes(int smem_optin);
+cudaError_t launch_prefill(const LayerArgs& a, int num_sms, cudaStream_t st);
+size_t prefill_workspace_bytes(const LayerArgs& a, int T);
+}  // namespace moe
+
+using moe::LayerArgs;
+using moe::RecordOffsets;
+
+static thread_local char g_err[512] = "no error";
+
+static int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof g_err, fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+static int cuda_fail(cudaError_t e, const char* what) {
+  return fail(MOE_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorString(e), cudaGetErrorName(e));
+}
+
+static constexpr uint32_t kMagic = 0x4D6F4531u;  // "MoE1"
+
+struct moe_layer {
+  uint32_t magic;
+  moe_layer_desc d;
+  moe_layer_weights w;
+  RecordOffsets off_r, off_s;
+  int rth_r, rth_s, rt_down, n_tiles, stage_bytes;
+  int device, num_sms;
+  cudaEvent_t prof[4];
+  int prof_on;
+};
+
+static bool aligned(const void* p, size_t a) {
+  return (reinterpret_cast<uintptr_t>(p) % a) == 0;
+}
+
+static bool dim_ok(int v) { return v >= 64 && v <= moe::kMaxDim && v % 64 == 0; }
+
+static RecordOffsets offsets_of(int H, int F) {
+  RecordOffsets o;
+  const uint64_t h = static_cast<uint64_t>(H), f = static_cast<uint64_t>(F);
+  const uint64_t mc = f * h / 2, msb = f * (h / 64) * 4, dsb = h * (f / 64) * 4;
+  o.gate_codes = 0;
+  o.up_codes = mc;
+  o.down_codes = 2 * mc;
+  o.gate_sb = 3 * mc;
+  o.up_sb = o.gate_sb + msb;
+  o.down_sb = o.up_sb + msb;
+  o.bytes = o.down_sb + dsb;
+  o.stride = (o.bytes + 4095u) / 4096u * 4096u;
+  return o;
+}
+
+extern "C" int moe_record_layout_of(int32_t hidden, int32_t ffn, moe_record_layout* out) {
+  if (!out) return fail(MOE_ERR_ARG, "moe_record_layout_of: out is NULL");
+  if (!dim_ok(hidden) || !dim_ok(ffn))
+    return fail(MOE_ERR_ARG, "moe_record_layout_of: hidden=%d ffn=%d must be multiples of 64 in [64, %d]",
+                hidden, ffn, moe::kMaxDim);
+  const RecordOffsets o = offsets_of(hidden, ffn);
+  out->gate_codes = o.gate_codes, out->up_codes = o.up_codes, out->down_codes = o.down_codes;
+  out->gate_sb = o.gate_sb, out->up_sb = o.up_sb, out->down_sb = o.down_sb;
+  out->bytes = o.bytes, out->stride = o.stride;
+  return MOE_OK;
+}
+
+static int check_desc(const moe_layer_desc* d) {
+  if (!d) return fail(MOE_ERR_ARG, "desc is NULL");
+  if (!dim_ok(d->hidden)) return fail(MOE_ERR_ARG, "hidden=%d: must be a multiple of 64 in [64, %d]", d->hidden, moe::kMaxDim);
+  if (d->n_experts < 1 || d->n_experts > moe::kMaxExperts)
+    return fail(MOE_ERR_ARG, "n_experts=%d: must be in [1, %d]", d->n_experts, moe::kMaxExperts);
+  if (d->top_k < 1 || d->top_k > std::min(d->n_experts, moe::kMaxTopK))
+    return fail(MOE_ERR_ARG, "top_k=%d: must be in [1, min(n_experts, %d)]", d->top_k, moe::kMaxTopK);
+  if (!dim_ok(d->ffn)) return fail(MOE_ERR_ARG, "ffn=%d: must be a multiple of 64 in [64, %d]", d->ffn, moe::kMaxDim);
+  if (d->shared_ffn != 0 && !dim_ok(d->shared_ffn))
+    return fail(MOE_ERR_ARG, "shared_ffn=%d: must be 0 or a multiple of 64 in [64, %d]", d->shared_ffn, moe::kMaxDim);
+  if (d->group != 64) return fail(MOE_ERR_ARG, "group=%d: only 64 is supported", d->group);
+  if (d->wbits != 4) return fail(MOE_ERR_ARG, "wbits=%d: only 4 is supported", d->wbits);
+  if (d->rbits != 8) return fail(MOE_ERR_ARG, "rbits=%d: only 8 is supported", d->rbits);
+  if (d->max_tokens < 1 || d->max_tokens > moe::kMaxTokens)
+    return fail(MOE_ERR_ARG, "max_tokens=%d: must be in [1, %d]", d->max_tokens, moe::kMaxTokens);
+  return MOE_OK;
+}
+
+extern "C" size_t moe_expert_bytes(const moe_layer_desc* desc, int32_t ffn) {
+  if (!desc || !dim_ok(desc->hidden) || !dim_ok(ffn)) return 0;
+  return static_cast<size_t>(offsets_of(desc->hidden, ffn).stride);
+}
+
+// Largest multiple of 4 dividing F whose gate+up stage fits the target.
+static int pick_rth(int H, int F) {
+  const int pair = 2 * (H / 2 + H / 16);
+  for (int r = F; r >= 4; r -= 4)
+    if (F % r == 0 && r * pair <= moe::kStageTarget) return r;
+  return 4;
+}
+
+// Largest multiple of 8 dividing H whose down stage (K = Fmax) fits the target.
+static int pick_rt_down(int H, int Fmax) {
+  const int row = Fmax / 2 + Fmax / 16;
+  for (int r = H; r >= 8; r -= 8)
+    if (H % r == 0 && r * row <= moe::kStageTarget) return r;
+  return 8;
+}
+
+static LayerArgs base_args(const moe_layer* L) {
+  LayerArgs a;
+  std::memset(&a, 0, sizeof a);
+  a.H = L->d.hidden, a.E = L->d.n_experts, a.k = L->d.top_k, a.F = L->d.ffn, a.Fs = L->d.shared_ffn;
+  a.records = static_cast<const uint8_t*>(L->w.expert_records);
+  a.shared = static_cast<const uint8_t*>(L->w.shared_record);
+  a.rcodes = L->w.router_codes;
+  a.rsb = L->w.router_sb;
+  a.beta = L->w.router_logit_bias;
+  a.off_r = L->off_r, a.off_s = L->off_s;
+  a.rth_r = L->rth_r, a.rth_s = L->rth_s, a.rt_down = L->rt_down, a.n_tiles_down = L->n_tiles;
+  a.stage_bytes = L->stage_bytes;
+  a.prof_on = L->prof_on;
+  for (int i = 0; i < 4; ++i) a.prof[i] = L->prof_on ? static_cast<void*>(L->prof[i]) : nullptr;
+  return a;
+}
+
+extern "C" int moe_open(const moe_layer_desc* desc, const moe_layer_weights* w, moe_layer** out) {
+  if (!out) return fail(MOE_ERR_ARG, "moe_open: out is NULL");
+  *out = nullptr;
+  int rc = check_desc(desc);
+  if (rc) return rc;
+  if (!w) return fail(MOE_ERR_ARG, "moe_open: weights is NULL");
+  if (!w->router_codes || !w->router_sb) return fail(MOE_ERR_ARG, "moe_open: router_codes/router_sb are NULL");
+  if ((desc->shared_ffn > 0) != (w->shared_record != nullptr))
+    return fail(MOE_ERR_ARG, "moe_open: shared_record must be non-NULL exactly when shared_ffn > 0");
+  if (!aligned(w->router_codes, 16) || !aligned(w->router_sb, 16) ||
+      !aligned(w->router_logit_bias, 16))
+    return fail(MOE_ERR_ALIGN, "moe_open: router pointers must be 16-byte aligned");
+  if (!aligned(w->expert_records, 256) || !aligned(w->shared_record, 256))
+    return fail(MOE_ERR_ALIGN, "moe_open: expert records must be 256-byte aligned");
+
+  moe_layer* L = new (std::nothrow) moe_layer;
+  if (!L) return fail(MOE_ERR_NOMEM, "moe_open: out of host memory");
+  std::memset(L, 0, sizeof *L);
+  L->magic = kMagic;
+  L->d = *desc;
+  L->w = *w;
+  const int H = desc->hidden, F = desc->ffn, Fs = desc->shared_ffn;
+  L->off_r = offsets_of(H, F);
+  L->off_s = Fs ? offsets_of(H, Fs) : RecordOffsets{};
+  L->rth_r = pick_rth(H, F);
+  L->rth_s = Fs ? pick_rth(H, Fs) : 4;
+  L->rt_down = pick_rt_down(H, std::max(F, Fs));
+  L->n_tiles = H / L->rt_down;
+  int sb = 2 * L->rth_r * (H / 2 + H / 16);
+  if (Fs) sb = std::max(sb, 2 * L->rth_s * (H / 2 + H / 16));
+  sb = std::max(sb, L->rt_down * (std::max(F, Fs) / 2 + std::max(F, Fs) / 16));
+  L->stage_bytes = (sb + 127) / 128 * 128;
+
+  cudaError_t e = cudaGetDevice(&L->device);
+  if (e) {
+    delete L;
+    return cuda_fail(e, "moe_open: cudaGetDevice");
+  }
+  int major = 0, minor = 0, smem_optin = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, L->device);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, L->device);
+  cudaDeviceGetAttribute(&L->num_sms, cudaDevAttrMultiProcessorCount, L->device);
+  cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, L->device);
+  if (major != 10 || minor != 3) {
+    const int dev = L->device;
+    delete L;
+    return fail(MOE_ERR_UNSUPPORTED, "moe_open: device %d is sm_%d%d; this library is built for sm_103a",
+                dev, major, minor);
+  }
+  const LayerArgs a = base_args(L);
+  const size_t need = std::max({moe::gateup_smem_bytes(a, 4), moe::down_smem_bytes(a, 4),
+                                moe::router_smem_bytes(desc->n_experts)});
+  if (need > static_cast<size_t>(smem_optin)) {
+    delete L;
+    return fail(MOE_ERR_UNSUPPORTED, "moe_open: kernels need %zu B of shared memory, device allows %d",
+                need, smem_optin);
+  }
+  if ((e = moe::set_decode_attributes(smem_optin)) || (e = moe::set_prefill_attributes(smem_optin))) {
+    delete L;
+    return cuda_fail(e, "moe_open: cudaFuncSetAttribute");
+  }
+  *out = L;
+  return MOE_OK;
+}
+
+extern "C" void moe_close(moe_layer* L) {
+  if (L && L->magic == kMagic) {
+    L->magic = 0;
+    delete L;
+  }
+}
+
+// ---- workspace -------------------------------------------------------------
+// [control: 64 words][tile counters][logits][grouping][h][h_shared][ypart]
+// [host-entry staging][prefill scratch].  The control block and tile counters
+// persist between calls (kept at zero); everything after them is per-call.
+
+struct Carve {
+  size_t off = 0;
+  size_t take(size_t bytes) {
+    const size_t o = off;
+    off += (bytes + 255) / 256 * 256;
+    return o;
+  }
+};
+
+static size_t carve(const moe_layer* L, int T, moe::Workspace* ws, uint8_t* base,
+                    size_t* prefill_off) {
+  const size_t H = L->d.hidden, E = L->d.n_experts, k = L->d.top_k, F = L->d.ffn,
+               Fs = L->d.shared_ffn, t = static_cast<size_t>(T);
+  Carve c;
+  const size_t o_ctl = c.take(64 * 4 + static_cast<size_t>(L->n_tiles) * 4);
+  const size_t o_log = c.take(t * E * 4);
+  const size_t o_nact = c.take(16);
+  const size_t o_ae = c.take(E * 4), o_ao = c.take(E * 4), o_ac = c.take(E * 4);
+  const size_t o_pt = c.take(t * k * 4), o_ps = c.take(t * k * 4);
+  const size_t o_h = c.take(t * k * F * 4), o_hs = c.take(t * Fs * 4);
+  const size_t o_y = c.take(t * (k + 1) * H * 4);
+  const size_t o_xs = c.take(t * H * 2), o_obs = c.take(t * H * 2), o_ofs = c.take(t * H * 4);
+  const size_t o_ids = c.take(t * k * 4), o_w = c.take(t * k * 4);
+  LayerArgs a = base_args(L);
+  const size_t o_pf = c.take(moe::prefill_workspace_bytes(a, T));
+  if (ws && base) {
+    ws->ctl = reinterpret_cast<unsigned*>(base + o_ctl);
+    ws->tile_cnt = ws->ctl + 64;
+    ws->logits = reinterpret_cast<float*>(base + o_log);
+    ws->n_act = reinterpret_cast<int*>(base + o_nact);
+    ws->act_expert = reinterpret_cast<int*>(base + o_ae);
+    ws->act_off = reinterpret_cast<int*>(base + o_ao);
+    ws->act_cnt = reinterpret_cast<int*>(base + o_ac);
+    ws->pair_token = reinterpret_cast<int*>(base + o_pt);
+    ws->pair_slot = reinterpret_cast<int*>(base + o_ps);
+    ws->h = reinterpret_cast<float*>(base + o_h);
+    ws->h_shared = reinterpret_cast<float*>(base + o_hs);
+    ws->ypart = reinterpret_cast<float*>(base + o_y);
+    ws->x_stage = reinterpret_cast<uint16_t*>(base + o_xs);
+    ws->ob_stage = reinterpret_cast<uint16_t*>(base + o_obs);
+    ws->of_stage = reinterpret_cast<float*>(base + o_ofs);
+    ws->ids_stage = reinterpret_cast<int32_t*>(base + o_ids);
+    ws->w_stage = reinterpret_cast<float*>(base + o_w);
+  }
+  if (prefill_off) *prefill_off = o_pf;
+  return c.off;
+}
+
+static bool valid(const moe_layer* L) { return L && L->magic == kMagic; }
+
+extern "C" size_t moe_workspace_bytes(const moe_layer* L, int32_t max_tokens) {
+  if (!valid(L) || max_tokens < 1 || max_tokens > L->d.max_tokens) return 0;
+  return carve(L, max_tokens, nullptr, nullptr, nullptr);
+}
+
+extern "C" int moe_workspace_init(const moe_layer* L, void* ws, size_t bytes, void* stream) {
+  if (!valid(L)) return fail(MOE_ERR_ARG, "moe_workspace_init: invalid layer handle");
+  if (!ws) return fail(MOE_ERR_ARG, "moe_workspace_init: workspace is NULL");
+  if (!aligned(ws, 256)) return fail(MOE_ERR_ALIGN, "moe_workspace_init: workspace must be 256-byte aligned");
+  cudaError_t e = cudaMemsetAsync(ws, 0, bytes, static_cast<cudaStream_t>(stream));
+  return e ? cuda_fail(e, "moe_workspace_init: cudaMemsetAsync") : MOE_OK;
+}
+
+enum class Path { kDecode, kPrefill };
+
+static int run(moe_layer* L, const uint16_t* x, int32_t T, uint16_t* ob, float* of, int32_t* ids,
+               float* wts, void* ws, size_t ws_bytes, void* stream, Path path, const char* name) {
+  if (!valid(L)) return fail(MOE_ERR_ARG, "%s: invalid layer handle", name);
+  const int cap = path == Path::kPrefill ? std::min(128, (int)L->d.max_tokens) : (int)L->d.max_tokens;
+  if (T < 0 || T > cap) return fail(MOE_ERR_ARG, "%s: token count %d outside [0, %d]", name, T, cap);
+  if (T == 0) return MOE_OK;
+  if (!x || !ob || !ids || !wts || !ws) return fail(MOE_ERR_ARG, "%s: a required pointer is NULL", name);
+  if (!aligned(x, 16) || !aligned(ob, 16) || !aligned(of, 16) || !aligned(ids, 16) || !aligned(wts, 16))
+    return fail(MOE_ERR_ALIGN, "%s: activation/output pointers must be 16-byte aligned", name);
+  if (!aligned(ws, 256)) return fail(MOE_ERR_ALIGN, "%s: workspace must be 256-byte aligned", name);
+  if (!L->w.expert_records) return fail(MOE_ERR_ARG, "%s: layer has no resident expert records", name);
+  size_t pf_off = 0;
+  LayerArgs a = base_args(L);
+  const size_t need = carve(L, T, &a.ws, static_cast<uint8_t*>(ws), &pf_off);
+  if (ws_bytes < need) return fail(MOE_ERR_ARG, "%s: workspace of %zu B is smaller than the %zu B needed", name, ws_bytes, need);
+  a.T = T, a.x = x, a.out_bf16 = ob, a.out_f32 = of, a.ids = ids, a.weights = wts;
+  (void)pf_off;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = path == Path::kPrefill ? moe::launch_prefill(a, L->num_sms, st)
+                                          : moe::launch_decode(a, L->num_sms, st);
+  if (e) return cuda_fail(e, name);
+  return MOE_OK;
+}
+
+extern "C" int moe_decode(moe_layer* L, const uint16_t* x, int32_t B, uint16_t* out_bf16, float* out_f32,
+                          int32_t* ids, float* weights, void* ws, size_t ws_bytes, void* stream) {
+  return run(L, x, B, out_bf16, out_f32, ids, weights, ws, ws_bytes, stream, Path::kDecode, "moe_decode");
+}
+
+extern "C" int moe_prefill_chunk(moe_layer* L, const uint16_t* x, int32_t T, uint16_t* out_bf16,
+                                 float* out_f32, int32_t* ids, float* weights, void* ws, size_t ws_bytes,
+                                 void* stream) {
+  return run(L, x, T, out_bf16, out_f32, ids, weights, ws, ws_bytes, stream, Path::kPrefill,
+             "moe_prefill_chunk");
+}
+
+extern "C" int moe_decode_host(moe_layer* L, const uint16_t* x_host, int32_t B, uint16_t* ob_host,
+                               float* of_host, int32_t* ids_host, float* w_host, void* ws,
+                               size_t ws_bytes, void* stream) {
+  if (!valid(L)) return fail(MOE_ERR_ARG, "moe_decode_host: invalid layer handle");
+  if (B < 0 || B > L->d.max_tokens) return fail(MOE_ERR_ARG, "moe_decode_host: B=%d outside [0, %d]", B, L->d.max_tokens);
+  if (B == 0) return MOE_OK;
+  if (!x_host || !ob_host || !ids_host || !w_host || !ws)
+    return fail(MOE_ERR_ARG, "moe_decode_host: a required pointer is NULL");
+  if (!aligned(ws, 256)) return fail(MOE_ERR_ALIGN, "moe_decode_host: workspace must be 256-byte aligned");
+  moe::Workspace w;
+  const size_t need = carve(L, B, &w, static_cast<uint8_t*>(ws), nullptr);
+  if (ws_bytes < need) return fail(MOE_ERR_ARG, "moe_decode_host: workspace too small (%zu < %zu)", ws_bytes, need);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t H = L->d.hidden, k = L->d.top_k, b = static_cast<size_t>(B);
+  cudaError_t e = cudaMemcpyAsync(w.x_stage, x_host, b * H * 2, cudaMemcpyHostToDevice, st);
+  if (e) return cuda_fail(e, "moe_decode_host: copy in");
+  int rc = moe_decode(L, w.x_stage, B, w.ob_stage, of_host ? w.of_stage : nullptr, w.ids_stage, w.w_stage,
+                      ws, ws_bytes, stream);
+  if (rc) return rc;
+  if ((e = cudaMemcpyAsync(ob_host, w.ob_stage, b * H * 2, cudaMemcpyDeviceToHost, st)) ||
+      (of_host && (e = cudaMemcpyAsync(of_host, w.of_stage, b * H * 4, cudaMemcpyDeviceToHost, st))) ||
+      (e = cudaMemcpyAsync(ids_host, w.ids_stage, b * k * 4, cudaMemcpyDeviceToHost, st)) ||
+      (e = cudaMemcpyAsync(w_host, w.w_stage, b * k * 4, cudaMemcpyDeviceToHost, st)))
+    return cuda_fail(e, "moe_decode_host: copy out");
+  if ((e = cudaStreamSynchronize(st))) return cuda_fail(e, "moe_decode_host: synchronize");
+  return MOE_OK;
+}
+
+extern "C" int moe_check(const moe_layer* L, void* ws, void* stream) {
+  if (!valid(L)) return fail(MOE_ERR_ARG, "moe_check: invalid layer handle");
+  if (!ws) return fail(MOE_ERR_ARG, "moe_check: workspace is NULL");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e) return cuda_fail(e, "moe_check: synchronize");
+  unsigned bits = 0;
+  if ((e = cudaMemcpy(&bits, ws, 4, cudaMemcpyDeviceToHost))) return cuda_fail(e, "moe_check: read error word");
+  if (bits == 0) return MOE_OK;
+  const unsigned zero = 0;
+  if ((e = cudaMemcpy(ws, &zero, 4, cudaMemcpyHostToDevice))) return cuda_fail(e, "moe_check: clear error word");
+  if (bits & moe::kErrTimeout) return fail(MOE_ERR_TIMEOUT, "device code gave up a bounded wait (bits 0x%x)", bits);
+  if (bits & moe::kErrResidency) return fail(MOE_ERR_RESIDENCY, "an expert slot did not hold the routed expert (bits 0x%x)", bits);
+  return fail(MOE_ERR_ARG, "device code clamped an out-of-range routing value (bits 0x%x)", bits);
+}
+
+extern "C" int moe_set_profile_events(moe_layer* L, void* const* events) {
+  if (!valid(L)) return fail(MOE_ERR_ARG, "moe_set_profile_events: invalid layer handle");
+  if (!events) {
+    L->prof_on = 0;
+    return MOE_OK;
+  }
+  for (int i = 0; i < 4; ++i) {
+    if (!events[i]) return fail(MOE_ERR_ARG, "moe_set_profile_events: event %d is NULL", i);
+    L->prof[i] = static_cast<cudaEvent_t>(events[i]);
+  }
+  L->prof_on = 1;
+  return MOE_OK;
+}
+
+extern "C" const char* moe_last_error(void) { return g_err; }

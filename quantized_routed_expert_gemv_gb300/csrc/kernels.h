@@ -1,0 +1,76 @@
+// kernels.h -- argument blocks shared by the host orchestration (api.cu) and
+// the kernels (decode.cu, prefill.cu).  Host+device, no CUDA-only types in
+// the structs themselves.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+namespace moe {
+
+constexpr int kMaxTokens = 128;  // decode B and prefill T cap
+constexpr int kMaxTopK = 32;
+constexpr int kMaxExperts = 1024;
+constexpr int kMaxDim = 8192;    // H, F, Fs
+constexpr int kConsumers = 256;  // consumer threads of the GEMV kernels (8 warps)
+constexpr int kStages = 4;       // bulk-copy pipeline depth
+constexpr int kStageTarget = 36 * 1024;  // bytes of weights per pipeline stage
+
+// Error bits latched in the workspace control block by device code.
+enum : unsigned {
+  kErrTimeout = 1u,    // a bounded wait expired
+  kErrResidency = 2u,  // a slot tag did not name the routed expert
+  kErrRange = 4u,      // a routed id or count was out of range (clamped)
+};
+
+// Region offsets inside one expert record (see include/moe.h).
+struct RecordOffsets {
+  uint64_t gate_codes, up_codes, down_codes, gate_sb, up_sb, down_sb, bytes, stride;
+};
+
+// Device pointers into the caller's workspace (computed on the host).
+struct Workspace {
+  unsigned* ctl;         // [0] error bits, [1] router done counter
+  unsigned* tile_cnt;    // down-projection row-tile arrival counters
+  float* logits;         // [T][E]
+  int* n_act;            // number of distinct routed experts this step
+  int* act_expert;       // [E] active expert ids, ascending
+  int* act_off;          // [E] first pair of each active expert
+  int* act_cnt;          // [E] tokens of each active expert
+  int* pair_token;       // [T*k] token of each (expert, token) pair, grouped by expert
+  int* pair_slot;        // [T*k] t*k + i position of the pair in ids/weights
+  float* h;              // [T*k][F]  SwiGLU activations of routed pairs
+  float* h_shared;       // [T][Fs]   SwiGLU activations of the shared expert
+  float* ypart;          // [T][k+1][H] per-(token, slot) down outputs
+  uint16_t* x_stage;     // host-entry staging: [T][H] bf16
+  uint16_t* ob_stage;    // [T][H] bf16
+  float* of_stage;       // [T][H] f32
+  int32_t* ids_stage;    // [T][k]
+  float* w_stage;        // [T][k]
+};
+
+struct LayerArgs {
+  int H, E, k, F, Fs, T;
+  const uint8_t* records;  // E records at `stride` (or the residency slot pool)
+  const uint8_t* shared;   // shared record or null
+  const uint8_t* rcodes;   // router codes [E][H]
+  const uint32_t* rsb;     // router sb words [E][H/64]
+  const float* beta;       // [E] or null
+  const int32_t* slot_of;  // [E] expert -> slot (residency) or null for identity
+  const int32_t* slot_tag; // [n_slots] expert id held by each slot, or null
+  const uint16_t* x;       // [T][H] bf16
+  uint16_t* out_bf16;      // [T][H]
+  float* out_f32;          // [T][H] or null
+  int32_t* ids;            // [T][k]
+  float* weights;          // [T][k]
+  Workspace ws;
+  RecordOffsets off_r, off_s;  // layouts for F and Fs
+  int rth_r, rth_s;            // gate|up rows per matrix per stage (routed / shared)
+  int rt_down;                 // down rows per stage (common row tiling of H)
+  int n_tiles_down;            // H / rt_down
+  int stage_bytes;             // bytes per pipeline stage
+  int prof_on;                 // record prof[] events between kernels, no PDL
+  void* prof[4];               // cudaEvent_t: before router / gate|up / down, after down
+};
+
+}  // namespace moe

@@ -1,0 +1,107 @@
+"""Device-resident synthetic layers: torch owns the memory, libmoe does the work.
+
+``DeviceLayer`` draws a layer with ``synth`` (in pinned host chunks, copied
+to HBM), opens it through the C ABI and owns a zero-initialised workspace.
+Its ``decode`` / ``prefill`` methods only allocate outputs and marshal
+pointers to ``moe_decode`` / ``moe_prefill_chunk``.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import moe, synth
+
+
+def bf16_tensor(bits: np.ndarray, device) -> torch.Tensor:
+    """bf16 bit patterns (uint16) -> torch.bfloat16 tensor on `device`."""
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+    return t.to(device)
+
+
+def bf16_bits(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+class DeviceLayer:
+    def __init__(self, shape: synth.Shape, weight_seed: int, layer: int = 0, beta=None,
+                 max_tokens: int = 16, device="cuda:0", chunk_records: int = 32,
+                 host_records: np.ndarray | None = None, host_shared: np.ndarray | None = None,
+                 router=None, resident: bool = True):
+        self.shape = s = shape
+        self.device = torch.device(device)
+        self.max_tokens = max_tokens
+        self.stride = synth.record_stride(s.H, s.F)
+        if resident:
+            self.records = torch.empty(s.E * self.stride, dtype=torch.uint8, device=self.device)
+            if host_records is not None:
+                self.records.copy_(torch.from_numpy(np.ascontiguousarray(host_records).reshape(-1)))
+            else:
+                n = min(chunk_records, s.E)
+                pinned = torch.empty(n * self.stride, dtype=torch.uint8, pin_memory=True)
+                view = pinned.numpy()
+                for e0 in range(0, s.E, n):
+                    cnt = min(n, s.E - e0)
+                    synth.fill_records(weight_seed, layer, range(e0, e0 + cnt), s.H, s.F, view)
+                    self.records[e0 * self.stride:(e0 + cnt) * self.stride].copy_(
+                        pinned[:cnt * self.stride])
+        else:
+            self.records = None
+        if s.Fs:
+            sh = host_shared if host_shared is not None else synth.expert_record(
+                weight_seed, layer, s.E, s.H, s.Fs)
+            self.shared = torch.from_numpy(np.ascontiguousarray(sh)).to(self.device)
+        else:
+            self.shared = None
+        rc, rsb = router if router is not None else synth.router(weight_seed, layer, s.E, s.H)
+        self.router_codes = torch.from_numpy(np.ascontiguousarray(rc)).to(self.device)
+        self.router_sb = torch.from_numpy(np.ascontiguousarray(rsb).view(np.int32)).to(self.device)
+        self.beta = None if beta is None else torch.from_numpy(
+            np.ascontiguousarray(beta, np.float32)).to(self.device)
+        self.desc = moe.desc(s.H, s.E, s.k, s.F, s.Fs, max_tokens=max_tokens)
+        self.weights = moe.moe_layer_weights(
+            self.records.data_ptr() if self.records is not None else None,
+            self.shared.data_ptr() if self.shared is not None else None,
+            self.router_codes.data_ptr(), self.router_sb.data_ptr(),
+            self.beta.data_ptr() if self.beta is not None else None)
+        self.handle = moe.moe_open(self.desc, self.weights)
+        self.ws_bytes = moe.moe_workspace_bytes(self.handle, max_tokens)
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=self.device)
+        moe.moe_workspace_init(self.handle, self.ws.data_ptr(), self.ws_bytes,
+                               torch.cuda.current_stream(self.device).cuda_stream)
+
+    def outputs(self, T: int):
+        s, dev = self.shape, self.device
+        return (torch.empty(T, s.H, dtype=torch.bfloat16, device=dev),
+                torch.empty(T, s.H, dtype=torch.float32, device=dev),
+                torch.empty(T, s.k, dtype=torch.int32, device=dev),
+                torch.empty(T, s.k, dtype=torch.float32, device=dev))
+
+    def _call(self, fn, x: torch.Tensor, outs, stream):
+        ob, of, ids, w = outs
+        T = x.shape[0]
+        st = stream if stream is not None else torch.cuda.current_stream(self.device).cuda_stream
+        fn(self.handle, x.data_ptr(), T, ob.data_ptr(), of.data_ptr() if of is not None else None,
+           ids.data_ptr(), w.data_ptr(), self.ws.data_ptr(), self.ws_bytes, st)
+        return ob, of, ids, w
+
+    def decode(self, x: torch.Tensor, outs=None, stream=None):
+        return self._call(moe.moe_decode, x, outs or self.outputs(x.shape[0]), stream)
+
+    def prefill(self, x: torch.Tensor, outs=None, stream=None):
+        return self._call(moe.moe_prefill_chunk, x, outs or self.outputs(x.shape[0]), stream)
+
+    def check(self, stream=None) -> int:
+        st = stream if stream is not None else torch.cuda.current_stream(self.device).cuda_stream
+        return moe.moe_check(self.handle, self.ws.data_ptr(), st)
+
+    def close(self):
+        if self.handle:
+            moe.moe_close(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
