@@ -44,6 +44,8 @@ def parse_args():
     p.add_argument("--batch", type=int, default=1)
     p.add_argument("--pool", type=int, default=64, help="distinct hidden-state batches rotated")
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--experts", type=int, default=0,
+                   help="shrink the routed-expert count (small layers for ncu captures only)")
     p.add_argument("--no-extras", action="store_true",
                    help="skip the B=4/16 lines, e2e, per-kernel and CPU-baseline passes")
     a = p.parse_args()
@@ -285,6 +287,8 @@ def run_ours(args, world, rank, local):
     torch.cuda.set_device(device)
     wl = synth.WORKLOADS[WORKLOAD]
     s = wl.shape
+    if args.experts:
+        s = synth.Shape(s.H, args.experts, s.k, s.F, s.Fs)
     batches = [args.batch] if args.no_extras else sorted({args.batch, 1, 4, 16})
     maxB = max(batches)
     dl = DeviceLayer(s, wl.weight_seed, max_tokens=maxB, device=device)
@@ -357,6 +361,9 @@ def run_ours(args, world, rank, local):
         # per-kernel durations: events between the three kernels (no PDL overlap)
         B = args.batch
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        for e in evs:               # torch creates the CUDA event on its first record
+            e.record(stream)
+        torch.cuda.synchronize()
         moe.moe_set_profile_events(dl.handle, [e.cuda_event for e in evs])
         Kp = min(args.steps, 200)
         sums = [0.0, 0.0, 0.0]

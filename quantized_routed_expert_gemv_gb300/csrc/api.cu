@@ -15,9 +15,8 @@
 #include "kernels.h"
 
 namespace moe {
-size_t router_smem_bytes(int E);
-size_t gateup_smem_bytes(const LayerArgs& a, int ntok);
-size_t down_smem_bytes(const LayerArgs& a, int ntok);
+size_t decode_smem_need(const LayerArgs& a, int num_sms);
+size_t prefill_smem_need(const LayerArgs& a, int num_sms);
 cudaError_t set_decode_attributes(int smem_optin);
 cudaError_t launch_decode(const LayerArgs& a, int num_sms, cudaStream_t st);
 cudaError_t set_prefill_attributes(int smem_optin);
@@ -49,7 +48,6 @@ struct moe_layer {
   moe_layer_desc d;
   moe_layer_weights w;
   RecordOffsets off_r, off_s;
-  int rth_r, rth_s, rt_down, n_tiles, stage_bytes;
   int device, num_sms;
   cudaEvent_t prof[4];
   int prof_on;
@@ -111,22 +109,6 @@ extern "C" size_t moe_expert_bytes(const moe_layer_desc* desc, int32_t ffn) {
   return static_cast<size_t>(offsets_of(desc->hidden, ffn).stride);
 }
 
-// Largest multiple of 4 dividing F whose gate+up stage fits the target.
-static int pick_rth(int H, int F) {
-  const int pair = 2 * (H / 2 + H / 16);
-  for (int r = F; r >= 4; r -= 4)
-    if (F % r == 0 && r * pair <= moe::kStageTarget) return r;
-  return 4;
-}
-
-// Largest multiple of 8 dividing H whose down stage (K = Fmax) fits the target.
-static int pick_rt_down(int H, int Fmax) {
-  const int row = Fmax / 2 + Fmax / 16;
-  for (int r = H; r >= 8; r -= 8)
-    if (H % r == 0 && r * row <= moe::kStageTarget) return r;
-  return 8;
-}
-
 static LayerArgs base_args(const moe_layer* L) {
   LayerArgs a;
   std::memset(&a, 0, sizeof a);
@@ -137,8 +119,6 @@ static LayerArgs base_args(const moe_layer* L) {
   a.rsb = L->w.router_sb;
   a.beta = L->w.router_logit_bias;
   a.off_r = L->off_r, a.off_s = L->off_s;
-  a.rth_r = L->rth_r, a.rth_s = L->rth_s, a.rt_down = L->rt_down, a.n_tiles_down = L->n_tiles;
-  a.stage_bytes = L->stage_bytes;
   a.prof_on = L->prof_on;
   for (int i = 0; i < 4; ++i) a.prof[i] = L->prof_on ? static_cast<void*>(L->prof[i]) : nullptr;
   return a;
@@ -168,14 +148,6 @@ extern "C" int moe_open(const moe_layer_desc* desc, const moe_layer_weights* w, 
   const int H = desc->hidden, F = desc->ffn, Fs = desc->shared_ffn;
   L->off_r = offsets_of(H, F);
   L->off_s = Fs ? offsets_of(H, Fs) : RecordOffsets{};
-  L->rth_r = pick_rth(H, F);
-  L->rth_s = Fs ? pick_rth(H, Fs) : 4;
-  L->rt_down = pick_rt_down(H, std::max(F, Fs));
-  L->n_tiles = H / L->rt_down;
-  int sb = 2 * L->rth_r * (H / 2 + H / 16);
-  if (Fs) sb = std::max(sb, 2 * L->rth_s * (H / 2 + H / 16));
-  sb = std::max(sb, L->rt_down * (std::max(F, Fs) / 2 + std::max(F, Fs) / 16));
-  L->stage_bytes = (sb + 127) / 128 * 128;
 
   cudaError_t e = cudaGetDevice(&L->device);
   if (e) {
@@ -194,9 +166,8 @@ extern "C" int moe_open(const moe_layer_desc* desc, const moe_layer_weights* w, 
                 dev, major, minor);
   }
   const LayerArgs a = base_args(L);
-  const size_t need = std::max({moe::gateup_smem_bytes(a, 4), moe::down_smem_bytes(a, 4),
-                                moe::router_smem_bytes(desc->n_experts)});
-  if (need > static_cast<size_t>(smem_optin)) {
+  const size_t need = std::max(moe::decode_smem_need(a, L->num_sms), moe::prefill_smem_need(a, L->num_sms));
+  if (need + 1024 > static_cast<size_t>(smem_optin)) {
     delete L;
     return fail(MOE_ERR_UNSUPPORTED, "moe_open: kernels need %zu B of shared memory, device allows %d",
                 need, smem_optin);
@@ -217,9 +188,9 @@ extern "C" void moe_close(moe_layer* L) {
 }
 
 // ---- workspace -------------------------------------------------------------
-// [control: 64 words][tile counters][logits][grouping][h][h_shared][ypart]
-// [host-entry staging][prefill scratch].  The control block and tile counters
-// persist between calls (kept at zero); everything after them is per-call.
+// [control: 64 words][logits][grouping][h][h_shared][host-entry staging]
+// [prefill scratch].  The control block persists between calls (its counter
+// is kept at zero); everything after it is per-call scratch.
 
 struct Carve {
   size_t off = 0;
@@ -235,20 +206,18 @@ static size_t carve(const moe_layer* L, int T, moe::Workspace* ws, uint8_t* base
   const size_t H = L->d.hidden, E = L->d.n_experts, k = L->d.top_k, F = L->d.ffn,
                Fs = L->d.shared_ffn, t = static_cast<size_t>(T);
   Carve c;
-  const size_t o_ctl = c.take(64 * 4 + static_cast<size_t>(L->n_tiles) * 4);
+  const size_t o_ctl = c.take(64 * 4);
   const size_t o_log = c.take(t * E * 4);
   const size_t o_nact = c.take(16);
   const size_t o_ae = c.take(E * 4), o_ao = c.take(E * 4), o_ac = c.take(E * 4);
   const size_t o_pt = c.take(t * k * 4), o_ps = c.take(t * k * 4);
   const size_t o_h = c.take(t * k * F * 4), o_hs = c.take(t * Fs * 4);
-  const size_t o_y = c.take(t * (k + 1) * H * 4);
   const size_t o_xs = c.take(t * H * 2), o_obs = c.take(t * H * 2), o_ofs = c.take(t * H * 4);
   const size_t o_ids = c.take(t * k * 4), o_w = c.take(t * k * 4);
   LayerArgs a = base_args(L);
   const size_t o_pf = c.take(moe::prefill_workspace_bytes(a, T));
   if (ws && base) {
     ws->ctl = reinterpret_cast<unsigned*>(base + o_ctl);
-    ws->tile_cnt = ws->ctl + 64;
     ws->logits = reinterpret_cast<float*>(base + o_log);
     ws->n_act = reinterpret_cast<int*>(base + o_nact);
     ws->act_expert = reinterpret_cast<int*>(base + o_ae);
@@ -258,7 +227,6 @@ static size_t carve(const moe_layer* L, int T, moe::Workspace* ws, uint8_t* base
     ws->pair_slot = reinterpret_cast<int*>(base + o_ps);
     ws->h = reinterpret_cast<float*>(base + o_h);
     ws->h_shared = reinterpret_cast<float*>(base + o_hs);
-    ws->ypart = reinterpret_cast<float*>(base + o_y);
     ws->x_stage = reinterpret_cast<uint16_t*>(base + o_xs);
     ws->ob_stage = reinterpret_cast<uint16_t*>(base + o_obs);
     ws->of_stage = reinterpret_cast<float*>(base + o_ofs);

@@ -3,26 +3,36 @@
 //   router_kernel   8-bit affine router GEMV -> fp32 logits; the last CTA to
 //                   finish runs softmax + warp-shuffle top-k per token and
 //                   groups the (token, slot) pairs by expert.
-//   gateup_kernel   4-bit gate|up GEMV + SwiGLU for every active expert and
-//                   the shared expert; each expert's rows are read once per
-//                   step and applied to all of its tokens.
-//   down_kernel     4-bit down GEMV into per-(token, slot) partials; the last
-//                   CTA to finish a row tile combines the tile in fixed slot
-//                   order (weighted routed outputs + shared output).
+//   gateup_kernel   4-bit gate|up GEMV + SwiGLU for the shared expert and
+//                   every active expert; each expert's rows are read once per
+//                   step and applied to all of its tokens.  The shared
+//                   expert's rows need no routing and are streamed while the
+//                   router is still running (programmatic dependent launch).
+//   down_kernel     4-bit down GEMV fused with the combine: a CTA owns a row
+//                   tile of the output and walks every expert of the step in
+//                   a fixed order, accumulating p_i * y_i (and y_shared) in
+//                   shared memory, so no partial results leave the SM.
 //
 // The method follows the TurboFieldfare page, section "Token üretim süreci"
-// (router on resident weights, top-8 ids, shared expert, combine; one
+// (router on resident weights, top-8 ids, shared expert computed while
+// routed weights are fetched, shared and routed outputs combined; one
 // fetched expert serves several rows) and section "Belleği azaltan çalışma
 // yapısı" (affine 4-bit group-64 experts, 8-bit router); the record holds
 // gate, up and down contiguously as on the WASTE page, section "Disk
 // streaming mimarisi".
+//
+// Weight streaming.  One producer warp per CTA moves each work item's rows
+// (codes + scale/bias words, and for `down` the expert's activations) from
+// HBM into a ring of shared-memory stages with 1-D bulk copies
+// (cp.async.bulk, completion on an mbarrier); the consumer warps compute from
+// shared memory and hand the stage back through a second mbarrier.
 //
 // GEMV inner loop.  A code q in bits [4i, 4i+4) of a 32-bit word, isolated
 // by one AND, reads as the fp32 value q * 2^(4i-149) (bit patterns below
 // 2^24 are subnormal or the first binade, both exact multiples of 2^-149).
 // Activations are pre-scaled once per column by 2^(85-4i) so every product
 // is q*x*2^-64 and one packed FMA (fma.rn.f32x2) handles two codes; the
-// factored affine term is y = sum_g (s_g 2^64 dot_g + b_g sum_g x).  No
+// affine term is factored as y = sum_g (s_g 2^64 dot_g + b_g sum_g x).  No
 // integer-to-float conversion and no per-code scale multiply remain.
 // Nibbles 6 and 7 are shifted down by 8 bits first (positions 4 and 5).
 #include <algorithm>
@@ -32,6 +42,8 @@
 #include "kernels.h"
 
 namespace moe {
+
+constexpr unsigned kFull = 0xFFFFFFFFu;
 
 // Pre-scale of the activation multiplying nibble i of a word (i = 0..7).
 __device__ __forceinline__ constexpr float nib_scale(int i) {
@@ -44,26 +56,28 @@ __device__ __forceinline__ constexpr float nib_scale(int i) {
 }
 
 // 32 4-bit codes (16 bytes) against 32 pre-scaled activations: returns
-// sum q_m x_m * 2^-64.
+// sum q_m x_m * 2^-64, as two independent packed-FMA chains.
 __device__ __forceinline__ float dot32(const uint4 q, const float (&X)[32]) {
-  float a0 = 0.f, a1 = 0.f;
+  float a0 = 0.f, a1 = 0.f, c0 = 0.f, c1 = 0.f;
   const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const uint32_t v = w[i], u = v >> 8;
-    ffma2(a0, a1, __uint_as_float(v & 0x0000000Fu), __uint_as_float(v & 0x000000F0u),
+    float& d0 = (i & 1) ? c0 : a0;
+    float& d1 = (i & 1) ? c1 : a1;
+    ffma2(d0, d1, __uint_as_float(v & 0x0000000Fu), __uint_as_float(v & 0x000000F0u),
           X[8 * i + 0], X[8 * i + 1]);
-    ffma2(a0, a1, __uint_as_float(v & 0x00000F00u), __uint_as_float(v & 0x0000F000u),
+    ffma2(d0, d1, __uint_as_float(v & 0x00000F00u), __uint_as_float(v & 0x0000F000u),
           X[8 * i + 2], X[8 * i + 3]);
-    ffma2(a0, a1, __uint_as_float(v & 0x000F0000u), __uint_as_float(v & 0x00F00000u),
+    ffma2(d0, d1, __uint_as_float(v & 0x000F0000u), __uint_as_float(v & 0x00F00000u),
           X[8 * i + 4], X[8 * i + 5]);
-    ffma2(a0, a1, __uint_as_float(u & 0x000F0000u), __uint_as_float(u & 0x00F00000u),
+    ffma2(d0, d1, __uint_as_float(u & 0x000F0000u), __uint_as_float(u & 0x00F00000u),
           X[8 * i + 6], X[8 * i + 7]);
   }
-  return a0 + a1;
+  return (a0 + a1) + (c0 + c1);
 }
 
-// 32 bf16 activations (64 bytes, 64-byte aligned) -> pre-scaled fp32 + sum.
+// 32 bf16 activations (64 bytes) -> pre-scaled fp32 + their plain sum.
 __device__ __forceinline__ void load_x_bf16(const uint16_t* p, float (&X)[32], float& SX) {
   const uint4* v = reinterpret_cast<const uint4*>(p);
   uint32_t w[16];
@@ -82,13 +96,13 @@ __device__ __forceinline__ void load_x_bf16(const uint16_t* p, float (&X)[32], f
   SX = s;
 }
 
-// 32 fp32 activations (128 bytes, written by an earlier kernel).
-__device__ __forceinline__ void load_x_f32(const float* p, float (&X)[32], float& SX) {
+// 32 fp32 activations from shared memory -> pre-scaled + plain sum.
+__device__ __forceinline__ void load_x_f32_smem(const float* p, float (&X)[32], float& SX) {
   const float4* v = reinterpret_cast<const float4*>(p);
   float s = 0.f;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const float4 t = __ldcg(v + i);
+    const float4 t = v[i];
     const float e[4] = {t.x, t.y, t.z, t.w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -102,11 +116,36 @@ __device__ __forceinline__ void load_x_f32(const float* p, float (&X)[32], float
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
   return v;
 }
 
+// Sums four per-lane row partials over the warp.  On return lane L holds the
+// warp total of row ((L >> 4) & 1) * 2 + ((L >> 3) & 1).
+__device__ __forceinline__ float bfly4(float p0, float p1, float p2, float p3, int lane) {
+  const bool hi16 = lane & 16;
+  float k0 = hi16 ? p2 : p0, k1 = hi16 ? p3 : p1;
+  const float s0 = hi16 ? p0 : p2, s1 = hi16 ? p1 : p3;
+  k0 += __shfl_xor_sync(kFull, s0, 16);
+  k1 += __shfl_xor_sync(kFull, s1, 16);
+  const bool hi8 = lane & 8;
+  float k = hi8 ? k1 : k0;
+  const float s = hi8 ? k0 : k1;
+  k += __shfl_xor_sync(kFull, s, 8);
+  k += __shfl_xor_sync(kFull, k, 4);
+  k += __shfl_xor_sync(kFull, k, 2);
+  k += __shfl_xor_sync(kFull, k, 1);
+  return k;
+}
+
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
+
+// Lane 0 waits (bounded) and the result is broadcast to the warp.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int lane) {
+  int ok = 1;
+  if (lane == 0) ok = mbar_wait(bar, parity) ? 1 : 0;
+  return __shfl_sync(kFull, ok, 0) != 0;
+}
 
 // ============================================================================
 // Router: logits, then (last CTA) top-k, weights and grouping by expert.
@@ -120,63 +159,86 @@ __device__ __forceinline__ constexpr float byte_scale(int i) {
 }
 
 __device__ __forceinline__ float dot16_u8(const uint4 q, const float (&X)[16]) {
-  float a0 = 0.f, a1 = 0.f;
+  float a0 = 0.f, a1 = 0.f, c0 = 0.f, c1 = 0.f;
   const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const uint32_t v = w[i];
-    ffma2(a0, a1, __uint_as_float(v & 0x000000FFu), __uint_as_float(v & 0x0000FF00u),
+    float& d0 = (i & 1) ? c0 : a0;
+    float& d1 = (i & 1) ? c1 : a1;
+    ffma2(d0, d1, __uint_as_float(v & 0x000000FFu), __uint_as_float(v & 0x0000FF00u),
           X[4 * i + 0], X[4 * i + 1]);
-    ffma2(a0, a1, __uint_as_float(v & 0x00FF0000u), __uint_as_float((v >> 8) & 0x00FF0000u),
+    ffma2(d0, d1, __uint_as_float(v & 0x00FF0000u), __uint_as_float((v >> 8) & 0x00FF0000u),
           X[4 * i + 2], X[4 * i + 3]);
   }
-  return a0 + a1;
+  return (a0 + a1) + (c0 + c1);
 }
 
+constexpr int kRouterThreads = 512;
+constexpr int kRouterRows = 4;  // rows in flight per iteration
+
+// Thread c owns 16-byte chunk c of every router row (its 16 activations stay
+// in registers); each CTA walks rows 4 at a time with all loads in flight.
 template <int NT>
-__global__ void __launch_bounds__(256) router_kernel(const __grid_constant__ LayerArgs a) {
+__global__ void __launch_bounds__(kRouterThreads) router_kernel(const __grid_constant__ LayerArgs a) {
   extern __shared__ __align__(16) float rsm[];
   pdl_launch_dependents();
   const int H = a.H, E = a.E, T = a.T, k = a.k;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int nchunk = H >> 4;  // 16-byte chunks per router row
-  const int gw = blockIdx.x * 8 + warp, nw = gridDim.x * 8;
+  constexpr int NW = kRouterThreads / 32;
+  const int nchunk = H >> 4;
+  const bool act = tid < nchunk;
+  float* red = rsm;  // [NT][kRouterRows][NW]
 
-  for (int e = gw; e < E; e += nw) {
-    const uint4* crow = reinterpret_cast<const uint4*>(a.rcodes + static_cast<size_t>(e) * H);
-    const uint32_t* srow = a.rsb + static_cast<size_t>(e) * (H >> 6);
-    for (int t0 = 0; t0 < T; t0 += NT) {
-      float acc[NT];
+  for (int t0 = 0; t0 < T; t0 += NT) {
+    float X[NT][16], SX[NT];
 #pragma unroll
-      for (int t = 0; t < NT; ++t) acc[t] = 0.f;
-      for (int c = lane; c < nchunk; c += 32) {
-        const uint4 q = __ldg(crow + c);
-        const uint32_t sbw = __ldg(srow + (c >> 2));
-        const float s = bf16lo(sbw) * 0x1p64f, b = bf16hi(sbw);
+    for (int t = 0; t < NT; ++t) {
+      SX[t] = 0.f;
 #pragma unroll
-        for (int t = 0; t < NT; ++t) {
-          if (t0 + t < T) {
-            const uint4* xp =
-                reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(t0 + t) * H + c * 16);
-            const uint4 x0 = __ldg(xp), x1 = __ldg(xp + 1);
-            const uint32_t xw[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-            float X[16], sx = 0.f;
+      for (int m = 0; m < 16; ++m) X[t][m] = 0.f;
+      if (act && t0 + t < T) {
+        const uint4* xp = reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(t0 + t) * H + tid * 16);
+        const uint4 x0 = __ldg(xp), x1 = __ldg(xp + 1);
+        const uint32_t xw[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
 #pragma unroll
-            for (int m = 0; m < 16; ++m) {
-              const float xv = (m & 1) ? bf16hi(xw[m >> 1]) : bf16lo(xw[m >> 1]);
-              X[m] = xv * byte_scale(m & 3);
-              sx += xv;
-            }
-            acc[t] = fmaf(s, dot16_u8(q, X), fmaf(b, sx, acc[t]));
-          }
+        for (int m = 0; m < 16; ++m) {
+          const float xv = (m & 1) ? bf16hi(xw[m >> 1]) : bf16lo(xw[m >> 1]);
+          X[t][m] = xv * byte_scale(m & 3);
+          SX[t] += xv;
+        }
+      }
+    }
+    for (int e0 = blockIdx.x * kRouterRows; e0 < E; e0 += gridDim.x * kRouterRows) {
+      uint4 q[kRouterRows];
+      uint32_t sbw[kRouterRows];
+#pragma unroll
+      for (int r = 0; r < kRouterRows; ++r) {
+        q[r] = make_uint4(0, 0, 0, 0), sbw[r] = 0;
+        if (act && e0 + r < E) {
+          q[r] = __ldg(reinterpret_cast<const uint4*>(a.rcodes + static_cast<size_t>(e0 + r) * H) + tid);
+          sbw[r] = __ldg(a.rsb + static_cast<size_t>(e0 + r) * (H >> 6) + (tid >> 2));
         }
       }
 #pragma unroll
       for (int t = 0; t < NT; ++t) {
-        const float v = warp_sum(acc[t]);
-        if (lane == 0 && t0 + t < T)
-          a.ws.logits[static_cast<size_t>(t0 + t) * E + e] = v + (a.beta ? __ldg(a.beta + e) : 0.f);
+#pragma unroll
+        for (int r = 0; r < kRouterRows; ++r) {
+          const float p = fmaf(bf16lo(sbw[r]) * 0x1p64f, dot16_u8(q[r], X[t]), bf16hi(sbw[r]) * SX[t]);
+          const float v = warp_sum(p);
+          if (lane == 0) red[(t * kRouterRows + r) * NW + warp] = v;
+        }
       }
+      __syncthreads();
+      if (tid < NT * kRouterRows) {
+        const int t = tid / kRouterRows, r = tid % kRouterRows;
+        if (t0 + t < T && e0 + r < E) {
+          float v = 0.f;
+          for (int w = 0; w < NW; ++w) v += red[tid * NW + w];
+          a.ws.logits[static_cast<size_t>(t0 + t) * E + e0 + r] = v + (a.beta ? __ldg(a.beta + e0 + r) : 0.f);
+        }
+      }
+      __syncthreads();
     }
   }
 
@@ -190,15 +252,15 @@ __global__ void __launch_bounds__(256) router_kernel(const __grid_constant__ Lay
   __threadfence();
 
   float* Lw = rsm + warp * E;                                     // per-warp logits
-  unsigned* sel = reinterpret_cast<unsigned*>(rsm + 8 * E);       // [E][4] token bitmasks
+  unsigned* sel = reinterpret_cast<unsigned*>(rsm + NW * E);      // [E][4] token bitmasks
   int* s_off = reinterpret_cast<int*>(sel + 4 * E);               // [E] pair offsets
   int* s_ids = s_off + E;                                         // [T*k]
-  int* s_scan = s_ids + kMaxTokens * kMaxTopK;                    // [16] scan scratch
+  int* s_scan = s_ids + kMaxTokens * kMaxTopK;                    // [2*NW] scan scratch
 
-  for (int i = tid; i < 4 * E; i += 256) sel[i] = 0u;
+  for (int i = tid; i < 4 * E; i += kRouterThreads) sel[i] = 0u;
   __syncthreads();
 
-  for (int t = warp; t < T; t += 8) {
+  for (int t = warp; t < T; t += NW) {
     for (int e = lane; e < E; e += 32) Lw[e] = __ldcg(a.ws.logits + static_cast<size_t>(t) * E + e);
     __syncwarp();
     float myl = 0.f;
@@ -208,12 +270,12 @@ __global__ void __launch_bounds__(256) router_kernel(const __grid_constant__ Lay
       int bi = E;
       for (int e = lane; e < E; e += 32) {
         const float v = Lw[e];
-        if (v > bv || (v == bv && e < bi)) bv = v, bi = e;
+        if (v > bv) bv = v, bi = e;  // ascending e per lane keeps the lower id on ties
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
-        const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
+        const float ov = __shfl_xor_sync(kFull, bv, o);
+        const int oi = __shfl_xor_sync(kFull, bi, o);
         if (ov > bv || (ov == bv && oi < bi)) bv = ov, bi = oi;
       }
       if (bi >= E) {  // only reachable with non-finite logits (outside the contract)
@@ -225,7 +287,7 @@ __global__ void __launch_bounds__(256) router_kernel(const __grid_constant__ Lay
       if (lane == 0) Lw[bi] = -INFINITY;
       __syncwarp();
     }
-    const float lmax = __shfl_sync(0xFFFFFFFFu, myl, 0);
+    const float lmax = __shfl_sync(kFull, myl, 0);
     const float ex = (lane < k) ? expf(myl - lmax) : 0.f;
     const float z = warp_sum(ex);
     if (lane < k) {
@@ -238,8 +300,8 @@ __global__ void __launch_bounds__(256) router_kernel(const __grid_constant__ Lay
   }
   __syncthreads();
 
-  // counts, exclusive scans over experts (pairs and active experts)
-  const int ept = (E + 255) / 256;
+  // counts and exclusive scans over experts (pairs, active experts)
+  const int ept = (E + kRouterThreads - 1) / kRouterThreads;
   const int e0 = tid * ept, e1 = min(e0 + ept, E);
   int c_loc = 0, a_loc = 0;
   for (int e = e0; e < e1; ++e) {
@@ -251,14 +313,14 @@ __global__ void __launch_bounds__(256) router_kernel(const __grid_constant__ Lay
   int c_inc = c_loc, a_inc = a_loc;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const int cu = __shfl_up_sync(0xFFFFFFFFu, c_inc, o);
-    const int au = __shfl_up_sync(0xFFFFFFFFu, a_inc, o);
+    const int cu = __shfl_up_sync(kFull, c_inc, o);
+    const int au = __shfl_up_sync(kFull, a_inc, o);
     if (lane >= o) c_inc += cu, a_inc += au;
   }
-  if (lane == 31) s_scan[warp] = c_inc, s_scan[8 + warp] = a_inc;
+  if (lane == 31) s_scan[warp] = c_inc, s_scan[NW + warp] = a_inc;
   __syncthreads();
   int c_base = 0, a_base = 0;
-  for (int w = 0; w < warp; ++w) c_base += s_scan[w], a_base += s_scan[8 + w];
+  for (int w = 0; w < warp; ++w) c_base += s_scan[w], a_base += s_scan[NW + w];
   int c_run = c_base + c_inc - c_loc, a_run = a_base + a_inc - a_loc;
   for (int e = e0; e < e1; ++e) {
     const int c = __popc(sel[4 * e]) + __popc(sel[4 * e + 1]) + __popc(sel[4 * e + 2]) +
@@ -272,10 +334,10 @@ __global__ void __launch_bounds__(256) router_kernel(const __grid_constant__ Lay
     }
     c_run += c;
   }
-  if (tid == 255) *a.ws.n_act = a_run;
+  if (tid == kRouterThreads - 1) *a.ws.n_act = a_run;
   __syncthreads();
 
-  for (int p = tid; p < T * k; p += 256) {
+  for (int p = tid; p < T * k; p += kRouterThreads) {
     const int t = p / k, e = s_ids[p];
     int rank = 0;
     for (int w = 0; w < (t >> 5); ++w) rank += __popc(sel[4 * e + w]);
@@ -296,15 +358,16 @@ struct Entry {     // one expert's work this step
   const RecordOffsets* off;  // points into the __grid_constant__ kernel parameter
   int Fe;          // FFN width of this expert (F or Fs)
   int ntok;        // tokens routed to it
-  int pair0;       // first pair (routed) -- h row of token 0
+  int pair0;       // first (expert, token) pair -- its h row
   int shared;      // 1 for the shared expert
+  int expert;      // routed expert id (-1 for the shared expert)
 };
 
-__device__ __forceinline__ Entry get_entry(const LayerArgs& a, int idx, int n_act, int has_sh) {
+__device__ __forceinline__ Entry get_entry(const LayerArgs& a, int idx, int has_sh) {
   Entry en;
   if (has_sh && idx == 0) {
-    en.rec = a.shared, en.off = &a.off_s, en.Fe = a.Fs, en.ntok = a.T, en.pair0 = 0,
-    en.shared = 1;
+    en.rec = a.shared, en.off = &a.off_s, en.Fe = a.Fs, en.ntok = a.T, en.pair0 = 0;
+    en.shared = 1, en.expert = -1;
     return en;
   }
   const int i = idx - has_sh;
@@ -314,124 +377,128 @@ __device__ __forceinline__ Entry get_entry(const LayerArgs& a, int idx, int n_ac
   if (cnt < 0 || cnt > a.T) cnt = 0;
   const int slot = a.slot_of ? a.slot_of[e] : e;
   en.rec = a.records + static_cast<size_t>(slot) * a.off_r.stride;
-  en.off = &a.off_r, en.Fe = a.F, en.ntok = cnt, en.pair0 = a.ws.act_off[i], en.shared = 0;
+  en.off = &a.off_r, en.Fe = a.F, en.ntok = cnt, en.pair0 = a.ws.act_off[i];
+  en.shared = 0, en.expert = e;
   return en;
 }
 
-__device__ __forceinline__ int entry_token(const LayerArgs& a, const Entry& en, int t) {
-  return en.shared ? t : a.ws.pair_token[en.pair0 + t];
+__device__ __forceinline__ int read_n_act(const LayerArgs& a) {
+  const int n = *reinterpret_cast<volatile int*>(a.ws.n_act);
+  return n < 0 ? 0 : (n > a.E ? a.E : n);
 }
 
 // ============================================================================
-// gate|up + SwiGLU.  One item = `rth` gate rows and the same `rth` up rows of
-// one expert; the shared expert's items come first.
+// gate|up + SwiGLU.  Consumer warp w covers 32 consecutive 16-byte columns
+// (wc = w % WC) of row-lane rl = w / WC; every thread owns one column and
+// gate rows {2rl, 2rl+1} plus up rows {2rl, 2rl+1} of the item, so the
+// SwiGLU pairs meet after one cross-warp sum.  Item = rth = 2*NRL gate rows
+// and the same up rows of one expert; the shared expert's items come first.
 // ============================================================================
 
-template <int NTOK>
-__global__ void __launch_bounds__(kConsumers + 32, 1) gateup_kernel(const __grid_constant__ LayerArgs a) {
+template <int NTOK, int NCW>
+__global__ void __launch_bounds__((NCW + 1) * 32, 1) gateup_kernel(const __grid_constant__ LayerArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
-  const int H = a.H, C = H >> 5, NRL = kConsumers / C;
-  const int max_rows = 2 * max(a.rth_r, a.rth_s);
-  float* red = reinterpret_cast<float*>(smem + kStages * a.stage_bytes);  // [NTOK][rows][C]
-  float* yv = red + NTOK * max_rows * C;                                  // [NTOK][rows]
-  uint64_t* full = reinterpret_cast<uint64_t*>(yv + NTOK * max_rows);
-  uint64_t* empty = full + kStages;
-  volatile int* s_abort = reinterpret_cast<volatile int*>(empty + kStages);
+  constexpr int NCT = NCW * 32;
+  const int H = a.H, C = H >> 5, WC = (C + 31) >> 5, NRL = a.gu_nrl, rth = 2 * NRL;
+  const int NST = a.gu_nst, SB = a.gu_stage;
+  float* wsum = reinterpret_cast<float*>(smem + NST * SB);  // [2][NTOK][NCW][4]
+  uint64_t* full = reinterpret_cast<uint64_t*>(wsum + 2 * NTOK * NCW * 4);
+  uint64_t* empty = full + NST;
+  volatile int* s_abort = reinterpret_cast<volatile int*>(empty + NST);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1), mbar_init(&empty[s], kConsumers / 32);
+    for (int s = 0; s < NST; ++s) mbar_init(&full[s], 1), mbar_init(&empty[s], NCW);
     *s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
   pdl_launch_dependents();
-  pdl_wait();  // router outputs (active experts, pairs) are ready past this point
 
   const int has_sh = a.Fs > 0 ? 1 : 0;
-  const int n_act = min(*reinterpret_cast<volatile int*>(a.ws.n_act), a.E);
-  const int tiles_r = a.F / a.rth_r, tiles_s = has_sh ? a.Fs / a.rth_s : 0;
-  const int n_items = tiles_s + n_act * tiles_r;
+  const int tiles_s = has_sh ? a.Fs / rth : 0, tiles_r = a.F / rth;
+  // Item i < tiles_s: shared expert tile i (no routing needed).  Later items
+  // need the router's output; n_items is only known after pdl_wait().
 
-  auto item = [&](int i, int& idx, int& tile) {
-    if (i < tiles_s) idx = 0, tile = i;
-    else idx = has_sh + (i - tiles_s) / tiles_r, tile = (i - tiles_s) % tiles_r;
-  };
-
-  if (warp == kConsumers / 32) {  // ---------------- producer warp
+  if (warp == NCW) {  // ---------------- producer warp
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
-      int it = 0;
-      for (int i = blockIdx.x; i < n_items; i += gridDim.x, ++it) {
-        const int s = it % kStages;
-        if (it >= kStages && !mbar_wait(&empty[s], ((it / kStages) - 1) & 1)) {
+      int it = 0, n_items = tiles_s;
+      bool waited = false;
+      for (int i = blockIdx.x;; i += gridDim.x, ++it) {
+        if (i >= tiles_s && !waited) {
+          pdl_wait();
+          waited = true;
+          n_items = tiles_s + read_n_act(a) * tiles_r;
+        }
+        if (i >= n_items) break;
+        const int s = it % NST;
+        if (it >= NST && !mbar_wait(&empty[s], ((it / NST) - 1) & 1)) {
           latch_error(&a.ws.ctl[0], kErrTimeout);
           break;
         }
-        int idx, tile;
-        item(i, idx, tile);
-        const Entry en = get_entry(a, idx, n_act, has_sh);
-        if (!en.shared && a.slot_tag) {
-          const int e = a.ws.act_expert[idx - has_sh];
-          if (a.slot_tag[a.slot_of[e]] != e) latch_error(&a.ws.ctl[0], kErrResidency);
-        }
-        const int rth = en.shared ? a.rth_s : a.rth_r;
+        const int idx = i < tiles_s ? 0 : has_sh + (i - tiles_s) / tiles_r;
+        const int tile = i < tiles_s ? i : (i - tiles_s) % tiles_r;
+        const Entry en = get_entry(a, idx, has_sh);
+        if (!en.shared && a.slot_tag && a.slot_tag[a.slot_of[en.expert]] != en.expert)
+          latch_error(&a.ws.ctl[0], kErrResidency);
         const size_t j0 = static_cast<size_t>(tile) * rth;
         const uint32_t cb = rth * (H / 2), sbb = rth * (H / 16);
-        uint8_t* st = smem + s * a.stage_bytes;
+        uint8_t* st = smem + s * SB;
         mbar_arrive_expect_tx(&full[s], 2 * cb + 2 * sbb);
         bulk_g2s(st, en.rec + en.off->gate_codes + j0 * (H / 2), cb, &full[s], pol);
         bulk_g2s(st + cb, en.rec + en.off->up_codes + j0 * (H / 2), cb, &full[s], pol);
         bulk_g2s(st + 2 * cb, en.rec + en.off->gate_sb + j0 * (H / 16), sbb, &full[s], pol);
         bulk_g2s(st + 2 * cb + sbb, en.rec + en.off->up_sb + j0 * (H / 16), sbb, &full[s], pol);
       }
-      // every issued copy must land before this CTA may exit
-      for (int j = max(0, it - kStages); j < it; ++j)
-        if (!mbar_wait(&full[j % kStages], (j / kStages) & 1)) latch_error(&a.ws.ctl[0], kErrTimeout);
+      for (int j = max(0, it - NST); j < it; ++j)  // every issued copy lands before exit
+        if (!mbar_wait(&full[j % NST], (j / NST) & 1)) latch_error(&a.ws.ctl[0], kErrTimeout);
     }
     return;
   }
 
   // ---------------------------------------------------- consumer warps
-  const int col = tid % C, rl = tid / C;
-  const bool active = rl < NRL;
+  const int rl = warp / WC, wc = warp % WC, col = wc * 32 + lane;
+  const bool active = (rl < NRL) && (col < C);
   float X[NTOK][32], SX[NTOK];
   const bool single = (a.T == 1);  // every entry's only token is token 0
-  if (single && active) {
-    load_x_bf16(a.x + col * 32, X[0], SX[0]);
+  if (single) {
+    if (active) {
+      load_x_bf16(a.x + col * 32, X[0], SX[0]);
+    } else {
 #pragma unroll
-    for (int t = 1; t < NTOK; ++t) {
-#pragma unroll
-      for (int m = 0; m < 32; ++m) X[t][m] = 0.f;
-      SX[t] = 0.f;
+      for (int m = 0; m < 32; ++m) X[0][m] = 0.f;
+      SX[0] = 0.f;
     }
   }
 
-  int it = 0;
-  for (int i = blockIdx.x; i < n_items; i += gridDim.x, ++it) {
-    const int s = it % kStages;
-    if (!mbar_wait(&full[s], (it / kStages) & 1)) *s_abort = 1;
-    named_bar(1, kConsumers);
-    if (*s_abort) {
-      if (tid == 0) latch_error(&a.ws.ctl[0], kErrTimeout);
-      break;
+  int it = 0, n_items = tiles_s;
+  bool waited = false;
+  for (int i = blockIdx.x;; i += gridDim.x, ++it) {
+    if (i >= tiles_s && !waited) {
+      pdl_wait();
+      waited = true;
+      n_items = tiles_s + read_n_act(a) * tiles_r;
     }
-    int idx, tile;
-    item(i, idx, tile);
-    const Entry en = get_entry(a, idx, n_act, has_sh);
-    const int rth = en.shared ? a.rth_s : a.rth_r;
-    const int rows = 2 * rth;
-    const uint8_t* st = smem + s * a.stage_bytes;
-    const uint8_t* stsb = st + rows * (H / 2);
+    if (i >= n_items) break;
+    const int s = it % NST;
+    if (!warp_wait(&full[s], (it / NST) & 1, lane)) *s_abort = 1;
+    const int idx = i < tiles_s ? 0 : has_sh + (i - tiles_s) / tiles_r;
+    const int tile = i < tiles_s ? i : (i - tiles_s) % tiles_r;
+    const Entry en = get_entry(a, idx, has_sh);
+    const uint8_t* st = smem + s * SB;
+    const uint8_t* stsb = st + 2 * rth * (H / 2);
     float* hout = en.shared ? a.ws.h_shared : a.ws.h;
     const int j0 = tile * rth;
+    const int rows[4] = {2 * rl, 2 * rl + 1, rth + 2 * rl, rth + 2 * rl + 1};
 
     for (int tg = 0; tg < en.ntok; tg += NTOK) {
-      if (!single && active) {
+      const int buf = (it + tg / NTOK) & 1;
+      if (!single) {
 #pragma unroll
         for (int t = 0; t < NTOK; ++t) {
-          if (tg + t < en.ntok) {
-            const int tok = entry_token(a, en, tg + t);
+          if (active && tg + t < en.ntok) {
+            const int tok = en.shared ? tg + t : a.ws.pair_token[en.pair0 + tg + t];
             load_x_bf16(a.x + static_cast<size_t>(tok) * H + col * 32, X[t], SX[t]);
           } else {
 #pragma unroll
@@ -440,219 +507,290 @@ __global__ void __launch_bounds__(kConsumers + 32, 1) gateup_kernel(const __grid
           }
         }
       }
+      float part[NTOK][4];
       if (active) {
-        for (int r = rl; r < rows; r += NRL) {
-          const uint4 q = *reinterpret_cast<const uint4*>(st + r * (H / 2) + col * 16);
-          const uint32_t sbw = *reinterpret_cast<const uint32_t*>(stsb + r * (H / 16) + (col >> 1) * 4);
-          const float sc = bf16lo(sbw) * 0x1p64f, bi = bf16hi(sbw);
+        uint4 q[4];
+        uint32_t sbw[4];
 #pragma unroll
-          for (int t = 0; t < NTOK; ++t)
-            red[(t * rows + r) * C + col] = fmaf(sc, dot32(q, X[t]), bi * SX[t]);
+        for (int r = 0; r < 4; ++r) {
+          q[r] = *reinterpret_cast<const uint4*>(st + rows[r] * (H / 2) + col * 16);
+          sbw[r] = *reinterpret_cast<const uint32_t*>(stsb + rows[r] * (H / 16) + (col >> 1) * 4);
         }
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const float sc = bf16lo(sbw[r]) * 0x1p64f, bi = bf16hi(sbw[r]);
+#pragma unroll
+          for (int t = 0; t < NTOK; ++t) part[t][r] = fmaf(sc, dot32(q[r], X[t]), bi * SX[t]);
+        }
+      } else {
+#pragma unroll
+        for (int t = 0; t < NTOK; ++t)
+#pragma unroll
+          for (int r = 0; r < 4; ++r) part[t][r] = 0.f;
       }
       if (tg + NTOK >= en.ntok) {  // last pass over this stage: hand it back
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
       }
-      named_bar(1, kConsumers);
-      for (int p = warp; p < NTOK * rows; p += kConsumers / 32) {
-        float v = 0.f;
-        for (int c = lane; c < C; c += 32) v += red[p * C + c];
-        v = warp_sum(v);
-        if (lane == 0) yv[p] = v;
+#pragma unroll
+      for (int t = 0; t < NTOK; ++t) {
+        const float v = bfly4(part[t][0], part[t][1], part[t][2], part[t][3], lane);
+        if ((lane & 7) == 0) wsum[((buf * NTOK + t) * NCW + warp) * 4 + (lane >> 3)] = v;
       }
-      named_bar(1, kConsumers);
-      for (int q = tid; q < NTOK * rth; q += kConsumers) {
+      named_bar(1, NCT);
+      if (*s_abort) break;
+      for (int q = tid; q < NTOK * rth; q += NCT) {
         const int t = q / rth, j = q % rth;
         if (tg + t < en.ntok) {
-          const float g = yv[t * rows + j], u = yv[t * rows + rth + j];
+          const int rlj = j >> 1, jj = j & 1;
+          float g = 0.f, u = 0.f;
+          for (int w = 0; w < WC; ++w) {
+            const float* ws = wsum + ((buf * NTOK + t) * NCW + rlj * WC + w) * 4;
+            g += ws[jj];
+            u += ws[2 + jj];
+          }
           const int hrow = en.shared ? (tg + t) : (en.pair0 + tg + t);
           hout[static_cast<size_t>(hrow) * en.Fe + j0 + j] = silu_f(g) * u;
         }
       }
+    }
+    if (*s_abort) {
+      if (tid == 0) latch_error(&a.ws.ctl[0], kErrTimeout);
+      break;
     }
     if (en.ntok == 0) {  // cannot happen for a listed expert; keep the ring consistent
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
     }
   }
+  if (!waited) pdl_wait();
 }
 
 // ============================================================================
-// down + combine.  One item = `rt_down` rows of H of one expert.  Outputs go
-// to ypart[token][slot][row]; the CTA whose arrival completes a row tile
-// combines it: out = sum_i p_i y_i + y_shared, in slot order.
+// down + combine.  A CTA owns row tiles of the output (rt rows of H) and, for
+// each tile, walks the shared expert then every active expert in ascending
+// id order; one item = the tile's rows of one expert for up to NTOK of its
+// tokens, staged together with those tokens' h rows.  The weighted sum
+// out = y_shared + sum_i p_i y_i builds up in shared memory in that fixed
+// order and is written once per tile.
 // ============================================================================
 
-template <int NTOK>
-__global__ void __launch_bounds__(kConsumers + 32, 1) down_kernel(const __grid_constant__ LayerArgs a) {
+template <int NTOK, int NCW>
+__global__ void __launch_bounds__((NCW + 1) * 32, 1) down_kernel(const __grid_constant__ LayerArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
-  const int H = a.H, RT = a.rt_down;
-  const int Cmax = max(a.F, a.Fs) >> 5;
-  float* red = reinterpret_cast<float*>(smem + kStages * a.stage_bytes);  // [NTOK][RT][C]
-  float* yv = red + NTOK * RT * Cmax;                                     // [NTOK][RT]
-  uint64_t* full = reinterpret_cast<uint64_t*>(yv + NTOK * RT);
-  uint64_t* empty = full + kStages;
-  volatile int* s_flags = reinterpret_cast<volatile int*>(empty + kStages);  // [0] abort [1] last
+  constexpr int NCT = NCW * 32;
+  const int H = a.H, RT = a.dn_rt, NST = a.dn_nst, SB = a.dn_stage, T = a.T, k = a.k;
+  float* wsum = reinterpret_cast<float*>(smem + NST * SB);  // [2][NTOK][NCW][4]
+  float* acc = wsum + 2 * NTOK * NCW * 4;                   // [T][RT]
+  uint64_t* full = reinterpret_cast<uint64_t*>(acc + T * RT + ((T * RT) & 1));
+  uint64_t* empty = full + NST;
+  volatile int* s_abort = reinterpret_cast<volatile int*>(empty + NST);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1), mbar_init(&empty[s], kConsumers / 32);
-    s_flags[0] = 0;
+    for (int s = 0; s < NST; ++s) mbar_init(&full[s], 1), mbar_init(&empty[s], NCW);
+    *s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  for (int q = tid; q < T * RT; q += blockDim.x) acc[q] = 0.f;
   __syncthreads();
   pdl_launch_dependents();
   pdl_wait();  // h of every expert is ready past this point
 
   const int has_sh = a.Fs > 0 ? 1 : 0;
-  const int n_act = min(*reinterpret_cast<volatile int*>(a.ws.n_act), a.E);
-  const int n_entries = n_act + has_sh;
-  const int n_tiles = a.n_tiles_down;
-  const int n_items = n_entries * n_tiles;
-  const int k = a.k;
+  const int n_ent = read_n_act(a) + has_sh;
+  const int n_tiles = a.dn_tiles;
 
-  if (warp == kConsumers / 32) {  // ---------------- producer warp
+  if (warp == NCW) {  // ---------------- producer warp
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
       int it = 0;
-      for (int i = blockIdx.x; i < n_items; i += gridDim.x, ++it) {
-        const int s = it % kStages;
-        if (it >= kStages && !mbar_wait(&empty[s], ((it / kStages) - 1) & 1)) {
-          latch_error(&a.ws.ctl[0], kErrTimeout);
-          break;
-        }
-        const int idx = i / n_tiles, tile = i % n_tiles;
-        const Entry en = get_entry(a, idx, n_act, has_sh);
+      bool stop = false;
+      for (int tile = blockIdx.x; tile < n_tiles && !stop; tile += gridDim.x) {
         const size_t r0 = static_cast<size_t>(tile) * RT;
-        const uint32_t cb = RT * (en.Fe / 2), sbb = RT * (en.Fe / 16);
-        uint8_t* st = smem + s * a.stage_bytes;
-        mbar_arrive_expect_tx(&full[s], cb + sbb);
-        bulk_g2s(st, en.rec + en.off->down_codes + r0 * (en.Fe / 2), cb, &full[s], pol);
-        bulk_g2s(st + cb, en.rec + en.off->down_sb + r0 * (en.Fe / 16), sbb, &full[s], pol);
+        for (int idx = 0; idx < n_ent && !stop; ++idx) {
+          const Entry en = get_entry(a, idx, has_sh);
+          if (!en.shared && a.slot_tag && a.slot_tag[a.slot_of[en.expert]] != en.expert)
+            latch_error(&a.ws.ctl[0], kErrResidency);
+          const float* hb = en.shared ? a.ws.h_shared : a.ws.h + static_cast<size_t>(en.pair0) * en.Fe;
+          for (int tg = 0; tg < en.ntok; tg += NTOK, ++it) {
+            const int s = it % NST;
+            if (it >= NST && !mbar_wait(&empty[s], ((it / NST) - 1) & 1)) {
+              latch_error(&a.ws.ctl[0], kErrTimeout);
+              stop = true;
+              break;
+            }
+            const int ntg = min(NTOK, en.ntok - tg);
+            const uint32_t cb = RT * (en.Fe / 2), sbb = RT * (en.Fe / 16), hbytes = ntg * en.Fe * 4;
+            uint8_t* st = smem + s * SB;
+            mbar_arrive_expect_tx(&full[s], cb + sbb + hbytes);
+            bulk_g2s(st, en.rec + en.off->down_codes + r0 * (en.Fe / 2), cb, &full[s], pol);
+            bulk_g2s(st + cb, en.rec + en.off->down_sb + r0 * (en.Fe / 16), sbb, &full[s], pol);
+            bulk_g2s(st + cb + sbb, hb + static_cast<size_t>(tg) * en.Fe, hbytes, &full[s]);
+          }
+        }
       }
-      for (int j = max(0, it - kStages); j < it; ++j)
-        if (!mbar_wait(&full[j % kStages], (j / kStages) & 1)) latch_error(&a.ws.ctl[0], kErrTimeout);
+      for (int j = max(0, it - NST); j < it; ++j)
+        if (!mbar_wait(&full[j % NST], (j / NST) & 1)) latch_error(&a.ws.ctl[0], kErrTimeout);
     }
     return;
   }
 
   // ---------------------------------------------------- consumer warps
-  float X[NTOK][32], SX[NTOK];
   int it = 0;
-  for (int i = blockIdx.x; i < n_items; i += gridDim.x, ++it) {
-    const int s = it % kStages;
-    if (!mbar_wait(&full[s], (it / kStages) & 1)) s_flags[0] = 1;
-    named_bar(1, kConsumers);
-    if (s_flags[0]) {
-      if (tid == 0) latch_error(&a.ws.ctl[0], kErrTimeout);
-      break;
-    }
-    const int idx = i / n_tiles, tile = i % n_tiles;
-    const Entry en = get_entry(a, idx, n_act, has_sh);
-    const int C = en.Fe >> 5, NRL = kConsumers / C;
-    const int col = tid % C, rl = tid / C;
-    const bool active = rl < NRL;
-    const uint8_t* st = smem + s * a.stage_bytes;
-    const uint8_t* stsb = st + RT * (en.Fe / 2);
-    const float* hin = en.shared ? a.ws.h_shared : a.ws.h;
+  bool abort = false;
+  for (int tile = blockIdx.x; tile < n_tiles && !abort; tile += gridDim.x) {
     const int r0 = tile * RT;
-
-    for (int tg = 0; tg < en.ntok; tg += NTOK) {
-      if (active) {
+    for (int idx = 0; idx < n_ent && !abort; ++idx) {
+      const Entry en = get_entry(a, idx, has_sh);
+      const int C = en.Fe >> 5, WC = (C + 31) >> 5;
+      int NRL = NCW / WC;
+      while (NRL & (NRL - 1)) NRL &= NRL - 1;  // power of two
+      const int rl = warp / WC, wc = warp % WC, col = wc * 32 + lane;
+      const bool active = (rl < NRL) && (col < C);
+      for (int tg = 0; tg < en.ntok; tg += NTOK, ++it) {
+        const int s = it % NST, buf = it & 1;
+        if (!warp_wait(&full[s], (it / NST) & 1, lane)) *s_abort = 1;
+        const int ntg = min(NTOK, en.ntok - tg);
+        const uint8_t* st = smem + s * SB;
+        const uint8_t* stsb = st + RT * (en.Fe / 2);
+        const float* sth = reinterpret_cast<const float*>(stsb + RT * (en.Fe / 16));
+        float part[NTOK][4];
 #pragma unroll
-        for (int t = 0; t < NTOK; ++t) {
-          if (tg + t < en.ntok) {
-            const int hrow = en.shared ? (tg + t) : (en.pair0 + tg + t);
-            load_x_f32(hin + static_cast<size_t>(hrow) * en.Fe + col * 32, X[t], SX[t]);
-          } else {
+        for (int t = 0; t < NTOK; ++t)
 #pragma unroll
-            for (int m = 0; m < 32; ++m) X[t][m] = 0.f;
-            SX[t] = 0.f;
+          for (int m = 0; m < 4; ++m) part[t][m] = 0.f;
+        if (active) {
+          float X[NTOK][32], SX[NTOK];
+#pragma unroll
+          for (int t = 0; t < NTOK; ++t) {
+            if (t < ntg) {
+              load_x_f32_smem(sth + t * en.Fe + col * 32, X[t], SX[t]);
+            } else {
+#pragma unroll
+              for (int m = 0; m < 32; ++m) X[t][m] = 0.f;
+              SX[t] = 0.f;
+            }
+          }
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            const int r = rl + NRL * m;
+            if (r < RT) {
+              const uint4 q = *reinterpret_cast<const uint4*>(st + r * (en.Fe / 2) + col * 16);
+              const uint32_t sbw = *reinterpret_cast<const uint32_t*>(stsb + r * (en.Fe / 16) + (col >> 1) * 4);
+              const float sc = bf16lo(sbw) * 0x1p64f, bi = bf16hi(sbw);
+#pragma unroll
+              for (int t = 0; t < NTOK; ++t) part[t][m] = fmaf(sc, dot32(q, X[t]), bi * SX[t]);
+            }
           }
         }
-        for (int r = rl; r < RT; r += NRL) {
-          const uint4 q = *reinterpret_cast<const uint4*>(st + r * (en.Fe / 2) + col * 16);
-          const uint32_t sbw =
-              *reinterpret_cast<const uint32_t*>(stsb + r * (en.Fe / 16) + (col >> 1) * 4);
-          const float sc = bf16lo(sbw) * 0x1p64f, bi = bf16hi(sbw);
-#pragma unroll
-          for (int t = 0; t < NTOK; ++t) red[(t * RT + r) * C + col] = fmaf(sc, dot32(q, X[t]), bi * SX[t]);
-        }
-      }
-      if (tg + NTOK >= en.ntok) {
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
-      }
-      named_bar(1, kConsumers);
-      for (int p = warp; p < NTOK * RT; p += kConsumers / 32) {
-        float v = 0.f;
-        for (int c = lane; c < C; c += 32) v += red[p * C + c];
-        v = warp_sum(v);
-        if (lane == 0) yv[p] = v;
-      }
-      named_bar(1, kConsumers);
-      for (int q = tid; q < NTOK * RT; q += kConsumers) {
-        const int t = q / RT, r = q % RT;
-        if (tg + t < en.ntok) {
-          int tok, slot;
+#pragma unroll
+        for (int t = 0; t < NTOK; ++t) {
+          const float v = bfly4(part[t][0], part[t][1], part[t][2], part[t][3], lane);
+          if ((lane & 7) == 0) wsum[((buf * NTOK + t) * NCW + warp) * 4 + (lane >> 3)] = v;
+        }
+        named_bar(1, NCT);
+        if (*s_abort) {
+          abort = true;
+          break;
+        }
+        // bfly4 leaves the thread's row m (row rl + NRL*m of the tile) at slot m.
+        for (int q = tid; q < ntg * RT; q += NCT) {
+          const int t = q / RT, r = q % RT;
+          const int rlr = r % NRL, m = r / NRL;
+          float y = 0.f;
+          for (int w = 0; w < WC; ++w) y += wsum[((buf * NTOK + t) * NCW + rlr * WC + w) * 4 + m];
+          int tok;
+          float p;
           if (en.shared) {
-            tok = tg + t, slot = k;
+            tok = tg + t, p = 1.f;
           } else {
-            const int p = a.ws.pair_slot[en.pair0 + tg + t];
-            tok = p / k, slot = p % k;
+            const int slot = a.ws.pair_slot[en.pair0 + tg + t];
+            tok = slot / k, p = a.weights[slot];
           }
-          a.ws.ypart[(static_cast<size_t>(tok) * (k + 1) + slot) * H + r0 + r] = yv[q];
+          acc[tok * RT + r] = fmaf(p, y, acc[tok * RT + r]);
         }
       }
     }
-    if (en.ntok == 0) {
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
-    }
-
-    // ---- arrival on the row tile; the last arriving CTA combines it
-    __threadfence();
-    named_bar(1, kConsumers);
-    if (tid == 0) s_flags[1] = (atomicAdd(&a.ws.tile_cnt[tile], 1u) == static_cast<unsigned>(n_entries - 1));
-    named_bar(1, kConsumers);
-    if (s_flags[1]) {
-      __threadfence();
-      for (int q = tid; q < a.T * RT; q += kConsumers) {
-        const int t = q / RT, r = r0 + q % RT;
-        const float* yp = a.ws.ypart + static_cast<size_t>(t) * (k + 1) * H + r;
-        float acc = 0.f;
-        for (int i2 = 0; i2 < k; ++i2) acc = fmaf(__ldcg(a.weights + t * k + i2), __ldcg(yp + static_cast<size_t>(i2) * H), acc);
-        if (has_sh) acc += __ldcg(yp + static_cast<size_t>(k) * H);
-        a.out_bf16[static_cast<size_t>(t) * H + r] = f32_to_bf16_rne(acc);
-        if (a.out_f32) a.out_f32[static_cast<size_t>(t) * H + r] = acc;
-      }
-      if (tid == 0) a.ws.tile_cnt[tile] = 0u;
+    if (abort) break;
+    named_bar(1, NCT);  // every expert of this tile has been added
+    for (int q = tid; q < T * RT; q += NCT) {
+      const int t = q / RT, r = q % RT;
+      const float v = acc[q];
+      a.out_bf16[static_cast<size_t>(t) * H + r0 + r] = f32_to_bf16_rne(v);
+      if (a.out_f32) a.out_f32[static_cast<size_t>(t) * H + r0 + r] = v;
+      acc[q] = 0.f;
     }
   }
+  if (abort && tid == 0) latch_error(&a.ws.ctl[0], kErrTimeout);
 }
 
 // ============================================================================
-// Host-side launchers (called from api.cu).
+// Host side: geometry, shared-memory sizes, launches.
 // ============================================================================
+
+static int pow2_floor(int v) {
+  int p = 1;
+  while (p * 2 <= v) p *= 2;
+  return p;
+}
+
+// Row-lanes of a GEMV whose input width is K, for `ncw` consumer warps.
+static int row_lanes(int K, int ncw) {
+  const int C = K / 32, WC = (C + 31) / 32;
+  return pow2_floor(std::max(1, ncw / WC));
+}
+
+static constexpr int kSmemBudget = 200 * 1024;  // pipeline stages per CTA
+
+// Per-launch geometry: gate|up rows per item and stage count; the down row
+// tile (a multiple of 4 dividing H, at most 4 rows per thread for every
+// expert width, two or more waves of tiles when H allows) and stage count.
+void plan_decode(LayerArgs& a, int num_sms, int ncw_gateup, int ncw_down, int ntok) {
+  const int H = a.H;
+  a.gu_nrl = row_lanes(H, ncw_gateup);
+  const int rth = 2 * a.gu_nrl;
+  a.gu_stage = (2 * rth * (H / 2 + H / 16) + 127) / 128 * 128;
+  a.gu_nst = std::max(2, std::min(8, kSmemBudget / a.gu_stage));
+
+  int nrl_min = row_lanes(a.F, ncw_down);
+  if (a.Fs) nrl_min = std::min(nrl_min, row_lanes(a.Fs, ncw_down));
+  const int rt_cap = 4 * nrl_min;
+  const int Fm = std::max(a.F, a.Fs);
+  // Busiest CTA's bytes: waves of tiles x (rt weight rows + the staged h row).
+  int best = 4;
+  double best_cost = 1e300;
+  for (int rt = 4; rt <= rt_cap; rt += 4) {
+    if (H % rt) continue;
+    const double waves = static_cast<double>((H / rt + num_sms - 1) / num_sms);
+    const double cost = waves * (rt * (Fm / 2.0 + Fm / 16.0) + ntok * Fm * 4.0);
+    if (cost < best_cost) best_cost = cost, best = rt;
+  }
+  a.dn_rt = best;
+  a.dn_tiles = H / best;
+  a.dn_stage = (best * (Fm / 2 + Fm / 16) + ntok * Fm * 4 + 127) / 128 * 128;
+  a.dn_nst = std::max(2, std::min(8, kSmemBudget / a.dn_stage));
+}
 
 size_t router_smem_bytes(int E) {
-  return static_cast<size_t>(8 * E) * 4 + static_cast<size_t>(4 * E) * 4 +
-         static_cast<size_t>(E) * 4 + static_cast<size_t>(kMaxTokens * kMaxTopK) * 4 + 16 * 4;
+  constexpr int NW = kRouterThreads / 32;
+  const size_t red = static_cast<size_t>(4) * kRouterRows * NW * 4;
+  const size_t topk = static_cast<size_t>(NW * E) * 4 + static_cast<size_t>(4 * E) * 4 +
+                      static_cast<size_t>(E) * 4 + static_cast<size_t>(kMaxTokens * kMaxTopK) * 4 +
+                      2 * NW * 4;
+  return std::max(red, topk);
 }
 
-size_t gateup_smem_bytes(const LayerArgs& a, int ntok) {
-  const int max_rows = 2 * std::max(a.rth_r, a.rth_s);
-  return static_cast<size_t>(kStages) * a.stage_bytes +
-         static_cast<size_t>(ntok) * max_rows * (a.H / 32) * 4 + static_cast<size_t>(ntok) * max_rows * 4 +
-         2 * kStages * 8 + 16;
+size_t gateup_smem_bytes(const LayerArgs& a, int ntok, int ncw) {
+  return static_cast<size_t>(a.gu_nst) * a.gu_stage + static_cast<size_t>(2 * ntok * ncw * 4) * 4 +
+         2 * a.gu_nst * 8 + 16;
 }
 
-size_t down_smem_bytes(const LayerArgs& a, int ntok) {
-  const int cmax = std::max(a.F, a.Fs) / 32;
-  return static_cast<size_t>(kStages) * a.stage_bytes +
-         static_cast<size_t>(ntok) * a.rt_down * cmax * 4 + static_cast<size_t>(ntok) * a.rt_down * 4 +
-         2 * kStages * 8 + 16;
+size_t down_smem_bytes(const LayerArgs& a, int ntok, int ncw) {
+  return static_cast<size_t>(a.dn_nst) * a.dn_stage + static_cast<size_t>(2 * ntok * ncw * 4) * 4 +
+         static_cast<size_t>(a.T * a.dn_rt + 2) * 4 + 2 * a.dn_nst * 8 + 16;
 }
 
 static cudaError_t launch_ex(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t st,
@@ -674,34 +812,59 @@ static cudaError_t launch_ex(const void* fn, dim3 grid, dim3 block, size_t smem,
 // Opt every kernel in to the device's full dynamic shared memory once, so
 // layers of different shapes opened in any order all launch.
 cudaError_t set_decode_attributes(int smem_optin) {
-  const void* fns[] = {(const void*)router_kernel<1>, (const void*)router_kernel<4>,
-                       (const void*)gateup_kernel<1>, (const void*)gateup_kernel<4>,
-                       (const void*)down_kernel<1>,   (const void*)down_kernel<4>};
+  const void* fns[] = {(const void*)router_kernel<1>,     (const void*)router_kernel<2>,
+                       (const void*)gateup_kernel<1, 16>, (const void*)gateup_kernel<4, 7>,
+                       (const void*)down_kernel<1, 8>,    (const void*)down_kernel<4, 7>};
   for (const void* f : fns) {
-    cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin);
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, f);
     if (e) return e;
+    const int dyn = smem_optin - static_cast<int>(fa.sharedSizeBytes);
+    if ((e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn))) return e;
   }
   return cudaSuccess;
+}
+
+// Largest dynamic shared memory any decode launch of this layer can need.
+size_t decode_smem_need(const LayerArgs& base, int num_sms) {
+  LayerArgs a = base;
+  a.T = kMaxTokens;
+  size_t need = router_smem_bytes(a.E);
+  plan_decode(a, num_sms, 16, 8, 1);
+  need = std::max({need, gateup_smem_bytes(a, 1, 16), down_smem_bytes(a, 1, 8)});
+  plan_decode(a, num_sms, 7, 7, 4);
+  need = std::max({need, gateup_smem_bytes(a, 4, 7), down_smem_bytes(a, 4, 7)});
+  return need;
 }
 
 static cudaError_t mark(const LayerArgs& a, int i, cudaStream_t st) {
   return a.prof_on ? cudaEventRecord(static_cast<cudaEvent_t>(a.prof[i]), st) : cudaSuccess;
 }
 
-cudaError_t launch_decode(const LayerArgs& a, int num_sms, cudaStream_t st) {
+cudaError_t launch_decode(const LayerArgs& in, int num_sms, cudaStream_t st) {
+  LayerArgs a = in;
   const bool one = (a.T == 1);
   const bool pdl = !a.prof_on;
-  const int rgrid = std::max(1, std::min((a.E + 7) / 8, 2 * num_sms));
+  plan_decode(a, num_sms, one ? 16 : 7, one ? 8 : 7, one ? 1 : 4);
+  const int rgrid = std::max(1, std::min((a.E + kRouterRows - 1) / kRouterRows, 2 * num_sms));
   cudaError_t e;
   if ((e = mark(a, 0, st))) return e;
-  e = launch_ex(one ? (const void*)router_kernel<1> : (const void*)router_kernel<4>, dim3(rgrid),
-                dim3(256), router_smem_bytes(a.E), st, false, a);
+  e = launch_ex(one ? (const void*)router_kernel<1> : (const void*)router_kernel<2>, dim3(rgrid),
+                dim3(kRouterThreads), router_smem_bytes(a.E), st, false, a);
   if (e || (e = mark(a, 1, st))) return e;
-  e = launch_ex(one ? (const void*)gateup_kernel<1> : (const void*)gateup_kernel<4>, dim3(num_sms),
-                dim3(kConsumers + 32), gateup_smem_bytes(a, one ? 1 : 4), st, pdl, a);
+  if (one)
+    e = launch_ex((const void*)gateup_kernel<1, 16>, dim3(num_sms), dim3(17 * 32),
+                  gateup_smem_bytes(a, 1, 16), st, pdl, a);
+  else
+    e = launch_ex((const void*)gateup_kernel<4, 7>, dim3(num_sms), dim3(8 * 32),
+                  gateup_smem_bytes(a, 4, 7), st, pdl, a);
   if (e || (e = mark(a, 2, st))) return e;
-  e = launch_ex(one ? (const void*)down_kernel<1> : (const void*)down_kernel<4>, dim3(num_sms),
-                dim3(kConsumers + 32), down_smem_bytes(a, one ? 1 : 4), st, pdl, a);
+  if (one)
+    e = launch_ex((const void*)down_kernel<1, 8>, dim3(num_sms), dim3(9 * 32),
+                  down_smem_bytes(a, 1, 8), st, pdl, a);
+  else
+    e = launch_ex((const void*)down_kernel<4, 7>, dim3(num_sms), dim3(8 * 32),
+                  down_smem_bytes(a, 4, 7), st, pdl, a);
   if (e) return e;
   return mark(a, 3, st);
 }

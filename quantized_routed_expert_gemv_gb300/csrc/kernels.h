@@ -31,7 +31,6 @@ struct RecordOffsets {
 // Device pointers into the caller's workspace (computed on the host).
 struct Workspace {
   unsigned* ctl;         // [0] error bits, [1] router done counter
-  unsigned* tile_cnt;    // down-projection row-tile arrival counters
   float* logits;         // [T][E]
   int* n_act;            // number of distinct routed experts this step
   int* act_expert;       // [E] active expert ids, ascending
@@ -41,7 +40,6 @@ struct Workspace {
   int* pair_slot;        // [T*k] t*k + i position of the pair in ids/weights
   float* h;              // [T*k][F]  SwiGLU activations of routed pairs
   float* h_shared;       // [T][Fs]   SwiGLU activations of the shared expert
-  float* ypart;          // [T][k+1][H] per-(token, slot) down outputs
   uint16_t* x_stage;     // host-entry staging: [T][H] bf16
   uint16_t* ob_stage;    // [T][H] bf16
   float* of_stage;       // [T][H] f32
@@ -65,10 +63,11 @@ struct LayerArgs {
   float* weights;          // [T][k]
   Workspace ws;
   RecordOffsets off_r, off_s;  // layouts for F and Fs
-  int rth_r, rth_s;            // gate|up rows per matrix per stage (routed / shared)
-  int rt_down;                 // down rows per stage (common row tiling of H)
-  int n_tiles_down;            // H / rt_down
-  int stage_bytes;             // bytes per pipeline stage
+  // per-launch geometry (plan_decode / plan_prefill)
+  int gu_nrl;                  // gate|up row-lanes; an item holds 2*gu_nrl gate + up rows
+  int gu_stage, gu_nst;        // gate|up stage bytes and stage count
+  int dn_rt, dn_tiles;         // down row tile and number of tiles (H / dn_rt)
+  int dn_stage, dn_nst;        // down stage bytes and stage count
   int prof_on;                 // record prof[] events between kernels, no PDL
   void* prof[4];               // cudaEvent_t: before router / gate|up / down, after down
 };

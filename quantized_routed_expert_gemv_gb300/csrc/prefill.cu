@@ -10,6 +10,8 @@ cudaError_t launch_decode(const LayerArgs& a, int num_sms, cudaStream_t st);
 
 size_t prefill_workspace_bytes(const LayerArgs&, int) { return 0; }
 
+size_t prefill_smem_need(const LayerArgs&, int) { return 0; }
+
 cudaError_t set_prefill_attributes(int) { return cudaSuccess; }
 
 cudaError_t launch_prefill(const LayerArgs& a, int num_sms, cudaStream_t st) {
