@@ -18,6 +18,9 @@ namespace moe {
 size_t decode_smem_need(const LayerArgs& a, int num_sms);
 size_t prefill_smem_need(const LayerArgs& a, int num_sms);
 cudaError_t set_decode_attributes(int smem_optin);
+cudaError_t set_b1_attributes(int smem_optin);
+bool plan_b1(LayerArgs& a, int num_sms, int smem_optin);
+cudaError_t launch_decode_b1(const LayerArgs& a, int num_sms, cudaStream_t st);
 cudaError_t launch_decode(const LayerArgs& a, int num_sms, cudaStream_t st);
 cudaError_t set_prefill_attributes(int smem_optin);
 cudaError_t launch_prefill(const LayerArgs& a, int num_sms, cudaStream_t st);
@@ -48,7 +51,7 @@ struct moe_layer {
   moe_layer_desc d;
   moe_layer_weights w;
   RecordOffsets off_r, off_s;
-  int device, num_sms;
+  int device, num_sms, smem_optin;
   cudaEvent_t prof[4];
   int prof_on;
 };
@@ -159,6 +162,7 @@ extern "C" int moe_open(const moe_layer_desc* desc, const moe_layer_weights* w, 
   cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, L->device);
   cudaDeviceGetAttribute(&L->num_sms, cudaDevAttrMultiProcessorCount, L->device);
   cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, L->device);
+  L->smem_optin = smem_optin;
   if (major != 10 || minor != 3) {
     const int dev = L->device;
     delete L;
@@ -172,7 +176,8 @@ extern "C" int moe_open(const moe_layer_desc* desc, const moe_layer_weights* w, 
     return fail(MOE_ERR_UNSUPPORTED, "moe_open: kernels need %zu B of shared memory, device allows %d",
                 need, smem_optin);
   }
-  if ((e = moe::set_decode_attributes(smem_optin)) || (e = moe::set_prefill_attributes(smem_optin))) {
+  if ((e = moe::set_decode_attributes(smem_optin)) || (e = moe::set_b1_attributes(smem_optin)) ||
+      (e = moe::set_prefill_attributes(smem_optin))) {
     delete L;
     return cuda_fail(e, "moe_open: cudaFuncSetAttribute");
   }
@@ -188,9 +193,10 @@ extern "C" void moe_close(moe_layer* L) {
 }
 
 // ---- workspace -------------------------------------------------------------
-// [control: 64 words][logits][grouping][h][h_shared][host-entry staging]
-// [prefill scratch].  The control block persists between calls (its counter
-// is kept at zero); everything after it is per-call scratch.
+// [control: 64 words][h chunk counters][fixed-point h][logits][grouping][h]
+// [h_shared][host-entry staging][prefill scratch].  The control block and the
+// chunk counters persist between calls (kept at zero by the kernels);
+// everything after them is per-call scratch.
 
 struct Carve {
   size_t off = 0;
@@ -207,6 +213,9 @@ static size_t carve(const moe_layer* L, int T, moe::Workspace* ws, uint8_t* base
                Fs = L->d.shared_ffn, t = static_cast<size_t>(T);
   Carve c;
   const size_t o_ctl = c.take(64 * 4);
+  // single-token fixed-point h: k routed rows of F and the shared row of Fs
+  const size_t hchunks = k * (F / 32) + Fs / 32, hpad = (hchunks + 3) / 4 * 4;
+  const size_t o_hx = c.take(hchunks * 64), o_hxs = c.take(hpad * 4), o_hxm = c.take(hpad * 4);
   const size_t o_log = c.take(t * E * 4);
   const size_t o_nact = c.take(16);
   const size_t o_ae = c.take(E * 4), o_ao = c.take(E * 4), o_ac = c.take(E * 4);
@@ -218,6 +227,9 @@ static size_t carve(const moe_layer* L, int T, moe::Workspace* ws, uint8_t* base
   const size_t o_pf = c.take(moe::prefill_workspace_bytes(a, T));
   if (ws && base) {
     ws->ctl = reinterpret_cast<unsigned*>(base + o_ctl);
+    ws->hx = reinterpret_cast<uint4*>(base + o_hx);
+    ws->hx_scale = reinterpret_cast<float*>(base + o_hxs);
+    ws->hx_sum = reinterpret_cast<float*>(base + o_hxm);
     ws->logits = reinterpret_cast<float*>(base + o_log);
     ws->n_act = reinterpret_cast<int*>(base + o_nact);
     ws->act_expert = reinterpret_cast<int*>(base + o_ae);
@@ -272,8 +284,13 @@ static int run(moe_layer* L, const uint16_t* x, int32_t T, uint16_t* ob, float* 
   a.T = T, a.x = x, a.out_bf16 = ob, a.out_f32 = of, a.ids = ids, a.weights = wts;
   (void)pf_off;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = path == Path::kPrefill ? moe::launch_prefill(a, L->num_sms, st)
-                                          : moe::launch_decode(a, L->num_sms, st);
+  cudaError_t e;
+  if (path == Path::kPrefill)
+    e = moe::launch_prefill(a, L->num_sms, st);
+  else if (T == 1 && moe::plan_b1(a, L->num_sms, L->smem_optin))
+    e = moe::launch_decode_b1(a, L->num_sms, st);
+  else
+    e = moe::launch_decode(a, L->num_sms, st);
   if (e) return cuda_fail(e, name);
   return MOE_OK;
 }

@@ -63,6 +63,21 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
+// Position in a ring of `nst` pipeline stages: stage index and the parity of
+// the current lap, advanced without integer division.
+struct RingPos {
+  int s = 0;
+  uint32_t ph = 0;
+  __device__ __forceinline__ void next(int nst) {
+    if (++s == nst) s = 0, ph ^= 1u;
+  }
+};
+
+// Every lane polls (no divergence, no broadcast); the warp agrees on the outcome.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity) {
+  return __all_sync(0xFFFFFFFFu, mbar_wait(bar, parity)) != 0;
+}
+
 // 1-D bulk copy global -> shared, completion counted on `bar` in bytes.
 // dst, src 16-byte aligned; bytes a multiple of 16.  The L2 policy marks
 // the source as evict-first: expert weights are streamed once per step.
@@ -95,6 +110,21 @@ __device__ __forceinline__ void named_bar(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// Named barrier that also ORs a predicate over the participants: every
+// thread gets the same answer, so exits decided on it stay uniform.
+__device__ __forceinline__ bool named_bar_or(int id, int count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %3, 0;\n\t"
+      "bar.red.or.pred q, %1, %2, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(id), "r"(count), "r"(static_cast<uint32_t>(pred))
+      : "memory");
+  return r != 0;
+}
+
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
@@ -116,17 +146,6 @@ __device__ __forceinline__ void pdl_wait() {
 }
 __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
-// Packed fp32 FMA (two lanes per instruction): d = a * b + c elementwise.
-__device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, float b0,
-                                      float b1) {
-  unsigned long long a, b, c;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(a0), "f"(a1));
-  asm("mov.b64 %0, {%1, %2};" : "=l"(b) : "f"(b0), "f"(b1));
-  asm("mov.b64 %0, {%1, %2};" : "=l"(c) : "f"(d0), "f"(d1));
-  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(c) : "l"(a), "l"(b));
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(d0), "=f"(d1) : "l"(c));
 }
 
 }  // namespace moe

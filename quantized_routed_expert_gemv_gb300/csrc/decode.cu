@@ -27,116 +27,15 @@
 // (cp.async.bulk, completion on an mbarrier); the consumer warps compute from
 // shared memory and hand the stage back through a second mbarrier.
 //
-// GEMV inner loop.  A code q in bits [4i, 4i+4) of a 32-bit word, isolated
-// by one AND, reads as the fp32 value q * 2^(4i-149) (bit patterns below
-// 2^24 are subnormal or the first binade, both exact multiples of 2^-149).
-// Activations are pre-scaled once per column by 2^(85-4i) so every product
-// is q*x*2^-64 and one packed FMA (fma.rn.f32x2) handles two codes; the
-// affine term is factored as y = sum_g (s_g 2^64 dot_g + b_g sum_g x).  No
-// integer-to-float conversion and no per-code scale multiply remain.
-// Nibbles 6 and 7 are shifted down by 8 bits first (positions 4 and 5).
+// The GEMV inner loops (float path) are in gemv.cuh.
 #include <algorithm>
 #include <cfloat>
 
 #include "common.cuh"
+#include "gemv.cuh"
 #include "kernels.h"
 
 namespace moe {
-
-constexpr unsigned kFull = 0xFFFFFFFFu;
-
-// Pre-scale of the activation multiplying nibble i of a word (i = 0..7).
-__device__ __forceinline__ constexpr float nib_scale(int i) {
-  return i == 0 ? 0x1p85f
-         : i == 1 ? 0x1p81f
-         : i == 2 ? 0x1p77f
-         : i == 3 ? 0x1p73f
-         : (i == 4 || i == 6) ? 0x1p69f
-                              : 0x1p65f;
-}
-
-// 32 4-bit codes (16 bytes) against 32 pre-scaled activations: returns
-// sum q_m x_m * 2^-64, as two independent packed-FMA chains.
-__device__ __forceinline__ float dot32(const uint4 q, const float (&X)[32]) {
-  float a0 = 0.f, a1 = 0.f, c0 = 0.f, c1 = 0.f;
-  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint32_t v = w[i], u = v >> 8;
-    float& d0 = (i & 1) ? c0 : a0;
-    float& d1 = (i & 1) ? c1 : a1;
-    ffma2(d0, d1, __uint_as_float(v & 0x0000000Fu), __uint_as_float(v & 0x000000F0u),
-          X[8 * i + 0], X[8 * i + 1]);
-    ffma2(d0, d1, __uint_as_float(v & 0x00000F00u), __uint_as_float(v & 0x0000F000u),
-          X[8 * i + 2], X[8 * i + 3]);
-    ffma2(d0, d1, __uint_as_float(v & 0x000F0000u), __uint_as_float(v & 0x00F00000u),
-          X[8 * i + 4], X[8 * i + 5]);
-    ffma2(d0, d1, __uint_as_float(u & 0x000F0000u), __uint_as_float(u & 0x00F00000u),
-          X[8 * i + 6], X[8 * i + 7]);
-  }
-  return (a0 + a1) + (c0 + c1);
-}
-
-// 32 bf16 activations (64 bytes) -> pre-scaled fp32 + their plain sum.
-__device__ __forceinline__ void load_x_bf16(const uint16_t* p, float (&X)[32], float& SX) {
-  const uint4* v = reinterpret_cast<const uint4*>(p);
-  uint32_t w[16];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint4 t = __ldg(v + i);
-    w[4 * i + 0] = t.x, w[4 * i + 1] = t.y, w[4 * i + 2] = t.z, w[4 * i + 3] = t.w;
-  }
-  float s = 0.f;
-#pragma unroll
-  for (int m = 0; m < 32; ++m) {
-    const float x = (m & 1) ? bf16hi(w[m >> 1]) : bf16lo(w[m >> 1]);
-    X[m] = x * nib_scale(m & 7);
-    s += x;
-  }
-  SX = s;
-}
-
-// 32 fp32 activations from shared memory -> pre-scaled + plain sum.
-__device__ __forceinline__ void load_x_f32_smem(const float* p, float (&X)[32], float& SX) {
-  const float4* v = reinterpret_cast<const float4*>(p);
-  float s = 0.f;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const float4 t = v[i];
-    const float e[4] = {t.x, t.y, t.z, t.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int m = 4 * i + j;
-      X[m] = e[j] * nib_scale(m & 7);
-      s += e[j];
-    }
-  }
-  SX = s;
-}
-
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
-  return v;
-}
-
-// Sums four per-lane row partials over the warp.  On return lane L holds the
-// warp total of row ((L >> 4) & 1) * 2 + ((L >> 3) & 1).
-__device__ __forceinline__ float bfly4(float p0, float p1, float p2, float p3, int lane) {
-  const bool hi16 = lane & 16;
-  float k0 = hi16 ? p2 : p0, k1 = hi16 ? p3 : p1;
-  const float s0 = hi16 ? p0 : p2, s1 = hi16 ? p1 : p3;
-  k0 += __shfl_xor_sync(kFull, s0, 16);
-  k1 += __shfl_xor_sync(kFull, s1, 16);
-  const bool hi8 = lane & 8;
-  float k = hi8 ? k1 : k0;
-  const float s = hi8 ? k0 : k1;
-  k += __shfl_xor_sync(kFull, s, 8);
-  k += __shfl_xor_sync(kFull, k, 4);
-  k += __shfl_xor_sync(kFull, k, 2);
-  k += __shfl_xor_sync(kFull, k, 1);
-  return k;
-}
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
 
@@ -150,29 +49,6 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int la
 // ============================================================================
 // Router: logits, then (last CTA) top-k, weights and grouping by expert.
 // ============================================================================
-
-// 16 8-bit codes (16 bytes) against pre-scaled activations: byte i of a word
-// isolated by one AND reads as q * 2^(8i-149) for i = 0..2; byte 3 is shifted
-// down by 8 bits first.  Activation pre-scales 2^85, 2^77, 2^69, 2^69.
-__device__ __forceinline__ constexpr float byte_scale(int i) {
-  return i == 0 ? 0x1p85f : i == 1 ? 0x1p77f : 0x1p69f;
-}
-
-__device__ __forceinline__ float dot16_u8(const uint4 q, const float (&X)[16]) {
-  float a0 = 0.f, a1 = 0.f, c0 = 0.f, c1 = 0.f;
-  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint32_t v = w[i];
-    float& d0 = (i & 1) ? c0 : a0;
-    float& d1 = (i & 1) ? c1 : a1;
-    ffma2(d0, d1, __uint_as_float(v & 0x000000FFu), __uint_as_float(v & 0x0000FF00u),
-          X[4 * i + 0], X[4 * i + 1]);
-    ffma2(d0, d1, __uint_as_float(v & 0x00FF0000u), __uint_as_float((v >> 8) & 0x00FF0000u),
-          X[4 * i + 2], X[4 * i + 3]);
-  }
-  return (a0 + a1) + (c0 + c1);
-}
 
 constexpr int kRouterThreads = 512;
 constexpr int kRouterRows = 4;  // rows in flight per iteration
@@ -191,21 +67,23 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const __grid_con
   float* red = rsm;  // [NT][kRouterRows][NW]
 
   for (int t0 = 0; t0 < T; t0 += NT) {
-    float X[NT][16], SX[NT];
+    float2 X[NT][8];
+    float SX[NT];
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
       SX[t] = 0.f;
 #pragma unroll
-      for (int m = 0; m < 16; ++m) X[t][m] = 0.f;
+      for (int j = 0; j < 8; ++j) X[t][j] = make_float2(0.f, 0.f);
       if (act && t0 + t < T) {
         const uint4* xp = reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(t0 + t) * H + tid * 16);
         const uint4 x0 = __ldg(xp), x1 = __ldg(xp + 1);
         const uint32_t xw[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
 #pragma unroll
-        for (int m = 0; m < 16; ++m) {
-          const float xv = (m & 1) ? bf16hi(xw[m >> 1]) : bf16lo(xw[m >> 1]);
-          X[t][m] = xv * byte_scale(m & 3);
-          SX[t] += xv;
+        for (int j = 0; j < 8; ++j) {
+          const float lo = bf16lo(xw[j]), hi = bf16hi(xw[j]);
+          X[t][j] = make_float2(lo * byte_scale((2 * j) & 3), hi * byte_scale((2 * j + 1) & 3));
+          SX[t] += lo;
+          SX[t] += hi;
         }
       }
     }
@@ -460,20 +338,16 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) gateup_kernel(const __grid_
   // ---------------------------------------------------- consumer warps
   const int rl = warp / WC, wc = warp % WC, col = wc * 32 + lane;
   const bool active = (rl < NRL) && (col < C);
-  float X[NTOK][32], SX[NTOK];
+  float2 X[NTOK][16];
+  float SX[NTOK];
   const bool single = (a.T == 1);  // every entry's only token is token 0
   if (single) {
-    if (active) {
-      load_x_bf16(a.x + col * 32, X[0], SX[0]);
-    } else {
-#pragma unroll
-      for (int m = 0; m < 32; ++m) X[0][m] = 0.f;
-      SX[0] = 0.f;
-    }
+    if (active) load_x_bf16(a.x + col * 32, X[0], SX[0]);
+    else zero_x(X[0], SX[0]);
   }
 
   int it = 0, n_items = tiles_s;
-  bool waited = false;
+  bool waited = false, abort_all = false;
   for (int i = blockIdx.x;; i += gridDim.x, ++it) {
     if (i >= tiles_s && !waited) {
       pdl_wait();
@@ -501,9 +375,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) gateup_kernel(const __grid_
             const int tok = en.shared ? tg + t : a.ws.pair_token[en.pair0 + tg + t];
             load_x_bf16(a.x + static_cast<size_t>(tok) * H + col * 32, X[t], SX[t]);
           } else {
-#pragma unroll
-            for (int m = 0; m < 32; ++m) X[t][m] = 0.f;
-            SX[t] = 0.f;
+            zero_x(X[t], SX[t]);
           }
         }
       }
@@ -537,9 +409,13 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) gateup_kernel(const __grid_
         const float v = bfly4(part[t][0], part[t][1], part[t][2], part[t][3], lane);
         if ((lane & 7) == 0) wsum[((buf * NTOK + t) * NCW + warp) * 4 + (lane >> 3)] = v;
       }
-      named_bar(1, NCT);
-      if (*s_abort) break;
-      for (int q = tid; q < NTOK * rth; q += NCT) {
+      if (named_bar_or(1, NCT, *s_abort != 0)) {
+        abort_all = true;
+        break;
+      }
+      // SwiGLU on the highest-numbered threads: warps past NRL*WC have no
+      // column of their own, so the epilogue costs the busy warps nothing.
+      for (int q = NCT - 1 - tid; q < NTOK * rth; q += NCT) {
         const int t = q / rth, j = q % rth;
         if (tg + t < en.ntok) {
           const int rlj = j >> 1, jj = j & 1;
@@ -550,11 +426,11 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) gateup_kernel(const __grid_
             u += ws[2 + jj];
           }
           const int hrow = en.shared ? (tg + t) : (en.pair0 + tg + t);
-          hout[static_cast<size_t>(hrow) * en.Fe + j0 + j] = silu_f(g) * u;
+          hout[static_cast<size_t>(hrow) * en.Fe + h_index(j0 + j, en.Fe)] = silu_f(g) * u;
         }
       }
     }
-    if (*s_abort) {
+    if (abort_all) {
       if (tid == 0) latch_error(&a.ws.ctl[0], kErrTimeout);
       break;
     }
@@ -661,16 +537,12 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) down_kernel(const __grid_co
 #pragma unroll
           for (int m = 0; m < 4; ++m) part[t][m] = 0.f;
         if (active) {
-          float X[NTOK][32], SX[NTOK];
+          float2 X[NTOK][16];
+          float SX[NTOK];
 #pragma unroll
           for (int t = 0; t < NTOK; ++t) {
-            if (t < ntg) {
-              load_x_f32_smem(sth + t * en.Fe + col * 32, X[t], SX[t]);
-            } else {
-#pragma unroll
-              for (int m = 0; m < 32; ++m) X[t][m] = 0.f;
-              SX[t] = 0.f;
-            }
+            if (t < ntg) load_h_smem(sth + t * en.Fe, C, col, X[t], SX[t]);
+            else zero_x(X[t], SX[t]);
           }
 #pragma unroll
           for (int m = 0; m < 4; ++m) {
@@ -691,8 +563,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) down_kernel(const __grid_co
           const float v = bfly4(part[t][0], part[t][1], part[t][2], part[t][3], lane);
           if ((lane & 7) == 0) wsum[((buf * NTOK + t) * NCW + warp) * 4 + (lane >> 3)] = v;
         }
-        named_bar(1, NCT);
-        if (*s_abort) {
+        if (named_bar_or(1, NCT, *s_abort != 0)) {
           abort = true;
           break;
         }
@@ -714,8 +585,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) down_kernel(const __grid_co
         }
       }
     }
-    if (abort) break;
-    named_bar(1, NCT);  // every expert of this tile has been added
+    if (named_bar_or(1, NCT, abort)) break;  // every expert of this tile has been added
     for (int q = tid; q < T * RT; q += NCT) {
       const int t = q / RT, r = q % RT;
       const float v = acc[q];

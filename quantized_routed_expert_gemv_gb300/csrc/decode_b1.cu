@@ -1,0 +1,861 @@
+// decode_b1.cu -- single-token decode (B = 1), the latency-critical case.
+//
+// Same three steps as decode.cu (router + top-k + grouping, gate|up +
+// SwiGLU, down + combine; TurboFieldfare page, section "Token üretim
+// süreci"), with an inner loop built for one token:
+//
+// Integer dot products (the fixed-point path of gemv.cuh): every 32-value
+// chunk of activations becomes 16-bit fixed point with its own power-of-two
+// exponent and dp4a accumulates the chunk's code x activation products
+// exactly; the affine bias term b * sum_j x_j is added in fp32.  Per 32
+// codes this costs ~35 instructions instead of ~78 for unpack-to-float +
+// FFMA, which keeps the CUDA cores well ahead of HBM.  The router keeps the
+// float path: its top-k must agree with an fp64 evaluation to within a
+// 1e-3 logit margin, and fp32 products of 8-bit codes and bf16 activations
+// are exact.
+//
+// gateup_b1_kernel  each consumer thread converts its chunk of the token's
+//                   hidden state; items are streamed as in decode.cu, and the last
+//                   warp to finish an item (shared-memory counter) applies
+//                   SwiGLU, so consumer warps never meet at a barrier.
+// down_b1_kernel    converts the step's h rows (one per active expert) once
+//                   per CTA into shared memory, then streams the CTA's row
+//                   tiles expert by expert; partial sums stay in registers
+//                   across experts (weighted by p_i), one reduction per tile.
+// router_b1_kernel  8-bit router rows (float path); top-k by repeated warp
+//                   argmax built on redux (max of the logit key, then min of
+//                   the id among the lanes holding it).
+#include <algorithm>
+#include <cfloat>
+
+#include "common.cuh"
+#include "gemv.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+namespace {
+
+constexpr unsigned kAll = kFull;
+
+__device__ __forceinline__ float warp_add(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kAll, v, o);
+  return v;
+}
+
+// Sums eight per-lane row partials over the warp; lane L ends with the total
+// of row L >> 2.
+__device__ __forceinline__ float bfly8(const float (&p)[8], int lane) {
+  const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+  float k[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float keep = b4 ? p[4 + i] : p[i], send = b4 ? p[i] : p[4 + i];
+    k[i] = keep + __shfl_xor_sync(kAll, send, 16);
+  }
+  float k2[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float keep = b3 ? k[2 + i] : k[i], send = b3 ? k[i] : k[2 + i];
+    k2[i] = keep + __shfl_xor_sync(kAll, send, 8);
+  }
+  float v = b2 ? k2[1] : k2[0];
+  const float send = b2 ? k2[0] : k2[1];
+  v += __shfl_xor_sync(kAll, send, 4);
+  v += __shfl_xor_sync(kAll, v, 2);
+  v += __shfl_xor_sync(kAll, v, 1);
+  return v;
+}
+
+// Four-row version: lane L ends with the total of row 2*bit4 + bit3.
+__device__ __forceinline__ float bfly4b(const float (&p)[4], int lane) {
+  const bool b4 = lane & 16, b3 = lane & 8;
+  float k[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float keep = b4 ? p[2 + i] : p[i], send = b4 ? p[i] : p[2 + i];
+    k[i] = keep + __shfl_xor_sync(kAll, send, 16);
+  }
+  float v = b3 ? k[1] : k[0];
+  const float send = b3 ? k[0] : k[1];
+  v += __shfl_xor_sync(kAll, send, 8);
+  v += __shfl_xor_sync(kAll, v, 4);
+  v += __shfl_xor_sync(kAll, v, 2);
+  v += __shfl_xor_sync(kAll, v, 1);
+  return v;
+}
+
+__device__ __forceinline__ float silu1(float g) { return g / (1.0f + expf(-g)); }
+
+__device__ __forceinline__ int clamp_n_act(const LayerArgs& a) {
+  const int n = *reinterpret_cast<volatile int*>(a.ws.n_act);
+  return n < 0 ? 0 : (n > a.E ? a.E : n);
+}
+
+struct B1Entry {
+  const uint8_t* rec;
+  const RecordOffsets* off;
+  int Fe, pair, shared, expert;
+};
+
+__device__ __forceinline__ B1Entry b1_entry(const LayerArgs& a, int idx, int has_sh) {
+  B1Entry en;
+  if (has_sh && idx == 0) {
+    en.rec = a.shared, en.off = &a.off_s, en.Fe = a.Fs, en.pair = 0, en.shared = 1, en.expert = -1;
+    return en;
+  }
+  const int i = idx - has_sh;
+  int e = a.ws.act_expert[i];
+  if (e < 0 || e >= a.E) e = 0;
+  const int slot = a.slot_of ? a.slot_of[e] : e;
+  en.rec = a.records + static_cast<size_t>(slot) * a.off_r.stride;
+  en.off = &a.off_r, en.Fe = a.F, en.pair = a.ws.act_off[i], en.shared = 0, en.expert = e;
+  return en;
+}
+
+}  // namespace
+
+// ============================================================================
+// Router (B = 1): 8-bit rows against the fixed-point token, then top-k.
+// ============================================================================
+
+constexpr int kR1Threads = 512;
+constexpr int kR1Rows = 8;  // rows per CTA pass: 64 CTAs for 512 experts leave most SMs to gate|up
+
+__global__ void __launch_bounds__(kR1Threads) router_b1_kernel(const __grid_constant__ LayerArgs a) {
+  extern __shared__ __align__(16) float rsm[];
+  pdl_launch_dependents();
+  const int H = a.H, E = a.E, k = a.k;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  constexpr int NW = kR1Threads / 32;
+  const int nchunk = H >> 4;  // 16 8-bit codes per chunk
+  const bool act = tid < nchunk;
+  float* red = rsm;  // [kR1Rows][NW]
+
+  uint4 q[kR1Rows];
+  uint32_t sbw[kR1Rows];
+  auto load_rows = [&](int e0) {
+#pragma unroll
+    for (int r = 0; r < kR1Rows; ++r) {
+      q[r] = make_uint4(0, 0, 0, 0), sbw[r] = 0;
+      if (act && e0 + r < E) {
+        q[r] = __ldg(reinterpret_cast<const uint4*>(a.rcodes + static_cast<size_t>(e0 + r) * H) + tid);
+        sbw[r] = __ldg(a.rsb + static_cast<size_t>(e0 + r) * (H >> 6) + (tid >> 2));
+      }
+    }
+  };
+  load_rows(blockIdx.x * kR1Rows);  // weight rows in flight before the activations
+
+  // token chunk: 16 bf16 activations, pre-scaled per byte position
+  float2 X[8];
+  float sx = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) X[j] = make_float2(0.f, 0.f);
+  if (act) {
+    const uint4* xp = reinterpret_cast<const uint4*>(a.x + tid * 16);
+    const uint4 x0 = __ldg(xp), x1 = __ldg(xp + 1);
+    const uint32_t xw[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float lo = bf16lo(xw[j]), hi = bf16hi(xw[j]);
+      X[j] = make_float2(lo * byte_scale((2 * j) & 3), hi * byte_scale((2 * j + 1) & 3));
+      sx += lo;
+      sx += hi;
+    }
+  }
+
+  for (int e0 = blockIdx.x * kR1Rows; e0 < E; e0 += gridDim.x * kR1Rows) {
+    if (e0 != blockIdx.x * kR1Rows) load_rows(e0);
+#pragma unroll
+    for (int r = 0; r < kR1Rows; ++r) {
+      const float p = fmaf(bf16lo(sbw[r]) * 0x1p64f, dot16_u8(q[r], X), bf16hi(sbw[r]) * sx);
+      const float v = warp_add(p);
+      if (lane == 0) red[r * NW + warp] = v;
+    }
+    __syncthreads();
+    if (tid < kR1Rows && e0 + tid < E) {
+      float v = 0.f;
+      for (int w = 0; w < NW; ++w) v += red[tid * NW + w];
+      a.ws.logits[e0 + tid] = v + (a.beta ? __ldg(a.beta + e0 + tid) : 0.f);
+    }
+    __syncthreads();
+  }
+
+  // ---- last CTA: top-k, weights, grouping (one token) ---------------------
+  __shared__ int s_last;
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = (atomicAdd(&a.ws.ctl[1], 1u) == gridDim.x - 1);
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  if (warp != 0) return;
+  // Lane l holds the keys of experts l, l+32, ... in registers; a logit's
+  // key is its IEEE bit pattern mapped to an order-preserving unsigned (all
+  // finite logits map above 0; 0 marks a taken or absent expert).
+  constexpr int KPL = kMaxExperts / 32;
+  uint32_t key[KPL];
+#pragma unroll
+  for (int s2 = 0; s2 < KPL; ++s2) {
+    const int e = s2 * 32 + lane;
+    uint32_t kk = 0u;
+    if (e < E) {
+      const uint32_t u = __float_as_uint(__ldcg(a.ws.logits + e));
+      kk = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    }
+    key[s2] = kk;
+  }
+  float myl = 0.f;
+  int myi = 0;
+  for (int i = 0; i < k; ++i) {
+    uint32_t bk = 0u;
+    int bs = 0;
+#pragma unroll
+    for (int s2 = 0; s2 < KPL; ++s2)  // ascending slot = ascending id: ties keep the lower
+      if (key[s2] > bk) bk = key[s2], bs = s2;
+    const uint32_t top = __reduce_max_sync(kAll, bk);
+    const unsigned win = __reduce_min_sync(kAll, (bk == top && top != 0u) ? static_cast<unsigned>(bs * 32 + lane)
+                                                                         : 0xFFFFFFFFu);
+    int w = static_cast<int>(win);
+    if (w >= E) {  // only with non-finite logits (outside the contract)
+      if (lane == 0) latch_error(&a.ws.ctl[0], kErrRange);
+      w = i;
+    }
+    if (lane == i) {
+      myi = w;
+      myl = __uint_as_float((top & 0x80000000u) ? (top & 0x7FFFFFFFu) : ~top);
+    }
+#pragma unroll
+    for (int s2 = 0; s2 < KPL; ++s2)
+      if (s2 * 32 + lane == w) key[s2] = 0u;
+  }
+  const float lmax = __shfl_sync(kAll, myl, 0);
+  const float ex = (lane < k) ? expf(myl - lmax) : 0.f;
+  const float z = warp_add(ex);
+  if (lane < k) a.ids[lane] = myi, a.weights[lane] = ex / z;
+  // Grouping for one token: active experts in ascending id, one pair each.
+  // Sort the k ids with a rank count (k <= 32).
+  int rank = 0;
+  for (int j = 0; j < k; ++j) {
+    const int oj = __shfl_sync(kAll, myi, j);
+    if (lane < k && oj < myi) ++rank;
+  }
+  if (lane < k) {
+    a.ws.act_expert[rank] = myi;
+    a.ws.act_off[rank] = rank;
+    a.ws.act_cnt[rank] = 1;
+    a.ws.pair_token[rank] = 0;
+    a.ws.pair_slot[rank] = lane;
+  }
+  if (lane == 0) *a.ws.n_act = k, a.ws.ctl[1] = 0u;
+}
+
+size_t router_b1_smem_bytes(int E) {
+  return std::max(static_cast<size_t>(kR1Rows) * (kR1Threads / 32) * 4, static_cast<size_t>(E) * 4);
+}
+
+// ============================================================================
+// gate|up + SwiGLU (B = 1).  Consumer warp w: row-lane rl = w / WC owns
+// gate rows 2rl, 2rl+1 and up rows 2rl, 2rl+1 of the item and column
+// 32*(w % WC) + lane.  An item holds rth = 2*NRL gate rows and the same up
+// rows of one expert (32 KB at H = 7168, so six stages fit); the shared
+// expert's items come first.
+// ============================================================================
+
+constexpr int kG1Warps = 16;
+
+struct G1Smem {  // byte offsets of the dynamic shared-memory carve
+  int wsum, cnt, item, bars, total;
+};
+
+__host__ __device__ inline G1Smem g1_smem(int nst, int stage, int rows) {
+  G1Smem s;
+  s.wsum = nst * stage;
+  s.cnt = s.wsum + nst * kG1Warps * rows * 4;  // [NST] warps done per item
+  s.item = s.cnt + 64;                          // [NST] item index held by the stage
+  s.bars = s.item + 64;
+  s.total = s.bars + 2 * nst * 8 + 16;
+  return s;
+}
+
+// Converts chunk c of a fixed-point h row (lane m holds value m) and
+// publishes its words, scale and sum for the down kernel's shared memory.  The layout matches down_b1's shared-memory copy: uint4 g
+// (eh, el, oh, ol) of chunk c of a row starting at chunk c0 with nc chunks
+// sits at index c0*4 + g*nc + c.
+__device__ __forceinline__ void publish_hchunk(const LayerArgs& a, int c0, int nc, int c, float v, int lane) {
+  const float amax = warp_max(fabsf(v));
+  const float scale = fixed_scale(amax);
+  const int X = to_fixed(v, 1.f / scale);
+  float sum = v;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(kAll, sum, o);
+  // lane L < 16 builds word i = L & 3 of group g = L >> 2: bytes b = 0..3 are
+  // activations 8i + p + 2b (p = parity), high byte for g even, low for g odd
+  const int g = (lane >> 2) & 3, i = lane & 3, par = g >> 1, hi = (g & 1) == 0;
+  int byte[4];
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    const int xv = __shfl_sync(kAll, X, 8 * i + par + 2 * b);
+    byte[b] = hi ? (xv >> 8) : xv;
+  }
+  if (lane < 16) {
+    uint32_t* words = reinterpret_cast<uint32_t*>(a.ws.hx);
+    words[(static_cast<size_t>(c0) * 4 + g * nc + c) * 4 + i] = pack4(byte[0], byte[1], byte[2], byte[3]);
+  }
+  if (lane == 0) a.ws.hx_scale[c0 + c] = scale, a.ws.hx_sum[c0 + c] = sum;
+}
+
+template <int R>  // rows per thread per item: R/2 gate + R/2 up
+__global__ void __launch_bounds__((kG1Warps + 1) * 32, 1) gateup_b1_kernel(const __grid_constant__ LayerArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  constexpr int NCW = kG1Warps;
+  const int H = a.H, C = H >> 5, WC = (C + 31) >> 5, NRL = a.gu_nrl, NAW = NRL * WC;
+  constexpr int RH = R / 2;
+  const int rth = RH * NRL;
+  const int NST = a.gu_nst, SB = a.gu_stage;
+  const G1Smem L = g1_smem(NST, SB, R);
+  float* wsum = reinterpret_cast<float*>(smem + L.wsum);  // [NST][NCW][R]
+  int* s_cnt = reinterpret_cast<int*>(smem + L.cnt);      // [NST]
+  volatile int* s_item = reinterpret_cast<volatile int*>(smem + L.item);  // [NST]
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
+  uint64_t* empty = full + NST;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  if (tid == 0) {
+    for (int s = 0; s < NST; ++s) mbar_init(&full[s], 1), mbar_init(&empty[s], NAW), s_cnt[s] = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  pdl_launch_dependents();
+
+  const int has_sh = a.Fs > 0 ? 1 : 0;
+  const int tiles_s = has_sh ? a.Fs / rth : 0, tiles_r = a.F / rth;
+  // Items 0 .. tiles_s-1: shared expert tiles (no routing needed).  Later
+  // items need the router's output.  CTAs claim items from a global counter,
+  // so CTAs that start late (their SM still ran the router) simply take fewer.
+
+  if (warp == NCW) {  // ---------------- producer warp
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      unsigned* claim = &a.ws.ctl[2];
+      int it = 0, n_items = tiles_s;
+      bool waited = false, marker = false;
+      RingPos pos;
+      int next = static_cast<int>(atomicAdd(claim, 1u));
+      for (;; ++it, pos.next(NST)) {
+        const int i = next;
+        if (i >= tiles_s && !waited) {
+          pdl_wait();
+          waited = true;
+          n_items = tiles_s + clamp_n_act(a) * tiles_r;
+        }
+        const int s = pos.s;
+        if (it >= NST && !mbar_wait(&empty[s], pos.ph ^ 1u)) {
+          latch_error(&a.ws.ctl[0], kErrTimeout);
+          break;
+        }
+        if (i >= n_items) {  // no work left: tell the consumers through the ring
+          s_item[s] = -1;
+          mbar_arrive(&full[s]);
+          marker = true;
+          break;
+        }
+        next = static_cast<int>(atomicAdd(claim, 1u));  // claim ahead, latency overlaps the copy
+        const int idx = i < tiles_s ? 0 : has_sh + (i - tiles_s) / tiles_r;
+        const int tile = i < tiles_s ? i : (i - tiles_s) % tiles_r;
+        const B1Entry en = b1_entry(a, idx, has_sh);
+        if (!en.shared && a.slot_tag && a.slot_tag[a.slot_of[en.expert]] != en.expert)
+          latch_error(&a.ws.ctl[0], kErrResidency);
+        const size_t j0 = static_cast<size_t>(tile) * rth;
+        const uint32_t cb = rth * (H / 2), sbb = rth * (H / 16);
+        uint8_t* st = smem + s * SB;
+        s_item[s] = i;
+        mbar_arrive_expect_tx(&full[s], 2 * cb + 2 * sbb);
+        bulk_g2s(st, en.rec + en.off->gate_codes + j0 * (H / 2), cb, &full[s], pol);
+        bulk_g2s(st + cb, en.rec + en.off->up_codes + j0 * (H / 2), cb, &full[s], pol);
+        bulk_g2s(st + 2 * cb, en.rec + en.off->gate_sb + j0 * (H / 16), sbb, &full[s], pol);
+        bulk_g2s(st + 2 * cb + sbb, en.rec + en.off->up_sb + j0 * (H / 16), sbb, &full[s], pol);
+      }
+      // Copies in flight land before exit.  The end marker re-armed the stage
+      // of item it - NST, whose copies were already consumed (its empty wait
+      // passed), so that one is skipped: its parity would alias.
+      for (int j = max(0, it - NST + (marker ? 1 : 0)); j < it; ++j)
+        if (!mbar_wait(&full[j % NST], (j / NST) & 1)) latch_error(&a.ws.ctl[0], kErrTimeout);
+    }
+    return;
+  }
+
+  // ---------------------------------------------------- consumers
+  const int rl = warp / WC, wc = warp % WC, col = wc * 32 + lane;
+  const bool has_col = col < C;
+  if (warp >= NAW) return;  // no column of this item layout
+  float xv[32], sx = 0.f;
+#pragma unroll
+  for (int m = 0; m < 32; ++m) xv[m] = 0.f;
+  if (has_col) {
+    const uint4* v = reinterpret_cast<const uint4*>(a.x + col * 32);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 t = __ldg(v + i);
+      const uint32_t w4[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) xv[8 * i + 2 * j] = bf16lo(w4[j]), xv[8 * i + 2 * j + 1] = bf16hi(w4[j]);
+    }
+#pragma unroll
+    for (int m = 0; m < 32; ++m) sx += xv[m];
+  }
+  XChunk X;
+  const float scale = make_xchunk_own(xv, X);
+
+  bool waited = false;
+  RingPos pos;
+  for (;; pos.next(NST)) {
+    const int s = pos.s;
+    if (!mbar_wait_warp(&full[s], pos.ph)) {
+      if (lane == 0) latch_error(&a.ws.ctl[0], kErrTimeout);
+      break;
+    }
+    const int i = s_item[s];
+    if (i < 0) break;  // the producer ran out of items
+    const uint8_t* st = smem + s * SB;
+    const uint8_t* stsb = st + 2 * rth * (H / 2);
+    float part[R];
+#pragma unroll
+    for (int m = 0; m < R; ++m) part[m] = 0.f;
+    if (has_col) {
+#pragma unroll
+      for (int m = 0; m < R; ++m) {
+        const int r = (m < RH) ? (RH * rl + m) : (rth + RH * rl + m - RH);
+        const uint4 q = *reinterpret_cast<const uint4*>(st + r * (H / 2) + col * 16);
+        const uint32_t sbw = *reinterpret_cast<const uint32_t*>(stsb + r * (H / 16) + (col >> 1) * 4);
+        part[m] = fmaf(bf16lo(sbw) * scale, static_cast<float>(dot_chunk(q, X)), bf16hi(sbw) * sx);
+      }
+    }
+    constexpr int LPR = 32 / R;  // lanes per row after the butterfly
+    float v;
+    if constexpr (R == 8) v = bfly8(part, lane);
+    else v = bfly4b(part, lane);
+    if ((lane & (LPR - 1)) == 0) wsum[(s * NCW + warp) * R + lane / LPR] = v;
+    __threadfence_block();
+    __syncwarp();
+    int last = 0;
+    if (lane == 0) last = (atomicAdd(&s_cnt[s], 1) == NAW - 1);
+    last = __shfl_sync(kAll, last, 0);
+    if (last) {  // every warp's sums for this item are in: SwiGLU, store h
+      __threadfence_block();
+      if (i >= tiles_s && !waited) pdl_wait(), waited = true;
+      const int idx = i < tiles_s ? 0 : has_sh + (i - tiles_s) / tiles_r;
+      const int tile = i < tiles_s ? i : (i - tiles_s) % tiles_r;
+      const B1Entry en = b1_entry(a, idx, has_sh);
+      float* hout = en.shared ? a.ws.h_shared : a.ws.h + static_cast<size_t>(en.pair) * a.F;
+      for (int j = lane; j < rth; j += 32) {
+        const int rlj = j / RH, mj = j % RH;
+        float g = 0.f, u = 0.f;
+        for (int w = 0; w < WC; ++w) {
+          const float* ws = wsum + (s * NCW + rlj * WC + w) * R;
+          g += ws[mj];
+          u += ws[RH + mj];
+        }
+        hout[tile * rth + j] = silu1(g) * u;
+      }
+      __syncwarp();
+      if (lane == 0) s_cnt[s] = 0;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+  }
+  if (!waited) pdl_wait();
+}
+
+size_t gateup_b1_smem_bytes(const LayerArgs& a, int rows) {
+  return g1_smem(a.gu_nst, a.gu_stage, rows).total;
+}
+
+// ============================================================================
+// down + combine (B = 1).  Prologue: a table of the step's experts (shared
+// expert first, then active experts in ascending id: record, width, h row,
+// routing weight); their h rows become fixed-point chunks (spread over the
+// grid, then a grid-wide barrier) that each CTA copies into shared memory.
+// Main loop: experts outer, this CTA's row tiles of H inner (at most
+// kD1MaxTiles), so a thread loads its activation chunk once per expert.  A
+// thread owns column `col` and rows rl + NRL*m (m < 2) of every tile for
+// each expert width; the weighted sums stay in registers until the end,
+// when one butterfly + one barrier per CTA combine them.
+// ============================================================================
+
+constexpr int kD1Warps = 16;
+constexpr int kD1MaxTiles = 4;  // row tiles per CTA
+constexpr int kD1Rpt = 2;       // rows per thread per tile and expert width
+
+struct D1Entry {        // one expert of the step, as the down kernel uses it
+  const uint8_t* rec;   // record base
+  float p;              // routing weight (1 for the shared expert)
+  int Fe;               // FFN width
+  int c0;               // first fixed-point chunk of its h row
+  int expert;           // expert id (-1: shared)
+};
+
+struct D1Smem {
+  int ent, xform, xsum, xscale, wsum, bars, total;
+};
+
+// rows: h rows of the step; cols_total: sum over rows of F_row / 32.
+__host__ __device__ inline D1Smem d1_smem(int nst, int stage, int rows, int cols_total) {
+  D1Smem s;
+  s.ent = nst * stage;
+  s.xform = s.ent + ((rows * static_cast<int>(sizeof(D1Entry)) + 127) / 128) * 128;
+  const int cpad = (cols_total + 3) / 4 * 4;
+  s.xsum = s.xform + cols_total * 64;          // float per chunk
+  s.xscale = s.xsum + cpad * 4;                // float per chunk
+  s.wsum = s.xscale + cpad * 4;
+  s.bars = s.wsum + kD1MaxTiles * kD1Warps * 4 * 4;  // [tile][warp][4]
+  s.total = s.bars + (2 * nst + 1) * 8 + 16;          // full, empty, fixed-point h
+  return s;
+}
+
+struct D1Geo {  // thread mapping for one expert width
+  int C, WC, NRL, rl, col;
+  bool act;
+};
+
+__device__ __forceinline__ D1Geo d1_geo(int Fe, int warp, int lane) {
+  D1Geo g;
+  g.C = Fe >> 5;
+  g.WC = (g.C + 31) >> 5;
+  int n = kD1Warps / g.WC;
+  while (n & (n - 1)) n &= n - 1;
+  g.NRL = n;
+  g.rl = warp / g.WC;
+  g.col = (warp % g.WC) * 32 + lane;
+  g.act = g.rl < g.NRL && g.col < g.C;
+  return g;
+}
+
+__global__ void __launch_bounds__((kD1Warps + 1) * 32, 1) down_b1_kernel(const __grid_constant__ LayerArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  constexpr int NCW = kD1Warps, NCT = NCW * 32;
+  const int H = a.H, RT = a.dn_rt, NST = a.dn_nst, SB = a.dn_stage, k = a.k;
+  const int has_sh = a.Fs > 0 ? 1 : 0;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int max_rows = k + has_sh;
+  const int max_cols = k * (a.F / 32) + has_sh * (a.Fs / 32);
+  const D1Smem L = d1_smem(NST, SB, max_rows, max_cols);
+  D1Entry* ent = reinterpret_cast<D1Entry*>(smem + L.ent);
+  uint4* xform = reinterpret_cast<uint4*>(smem + L.xform);
+  float* xsum = reinterpret_cast<float*>(smem + L.xsum);
+  float* xscale = reinterpret_cast<float*>(smem + L.xscale);
+  float* wsum = reinterpret_cast<float*>(smem + L.wsum);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
+  uint64_t* empty = full + NST;
+  uint64_t* xbar = empty + NST;  // fixed-point h block landed
+
+  if (tid == 0) {
+    for (int s = 0; s < NST; ++s) mbar_init(&full[s], 1), mbar_init(&empty[s], NCW);
+    mbar_init(xbar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  pdl_launch_dependents();
+  pdl_wait();  // fixed-point h, routing and weights are ready past this point
+  if (blockIdx.x == 0 && tid == 0) a.ws.ctl[2] = 0u;  // gate|up claims: back to zero
+  const int n_ent = min(clamp_n_act(a) + has_sh, max_rows);
+  if (warp == 0) {
+    for (int j = lane; j < n_ent; j += 32) {
+      const B1Entry en = b1_entry(a, j, has_sh);
+      D1Entry d;
+      d.rec = en.rec;
+      d.Fe = en.Fe;
+      d.expert = en.expert;
+      d.p = en.shared ? 1.f : a.weights[a.ws.pair_slot[en.pair]];
+      d.c0 = en.shared ? 0 : has_sh * (a.Fs / 32) + (j - has_sh) * (a.F / 32);
+      ent[j] = d;
+      if (!en.shared && a.slot_tag && a.slot_tag[a.slot_of[en.expert]] != en.expert)
+        latch_error(&a.ws.ctl[0], kErrResidency);
+    }
+  }
+  __syncthreads();
+  // this CTA's tiles: blockIdx.x + t * gridDim.x, t < ntc (<= kD1MaxTiles by plan)
+  const int n_tiles = a.dn_tiles;
+  const int ntc = blockIdx.x < n_tiles ? min(kD1MaxTiles, (n_tiles - 1 - blockIdx.x) / gridDim.x + 1) : 0;
+  const int n_cols = n_ent > 0 ? ent[n_ent - 1].c0 + ent[n_ent - 1].Fe / 32 : 0;
+
+  if (warp == NCW) {  // ---------------- producer warp: expert weights, ahead of h
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      int it = 0;
+      bool stop = false;
+      RingPos pos;
+      for (int j = 0; j < n_ent && !stop; ++j) {
+        const D1Entry d = ent[j];
+        const RecordOffsets& off = d.expert < 0 ? a.off_s : a.off_r;
+        const uint32_t cb = RT * (d.Fe / 2), sbb = RT * (d.Fe / 16);
+        for (int t = 0; t < ntc; ++t, ++it, pos.next(NST)) {
+          const int s = pos.s;
+          if (it >= NST && !mbar_wait(&empty[s], pos.ph ^ 1u)) {
+            latch_error(&a.ws.ctl[0], kErrTimeout);
+            stop = true;
+            break;
+          }
+          const size_t r0 = static_cast<size_t>(blockIdx.x + t * gridDim.x) * RT;
+          uint8_t* st = smem + s * SB;
+          mbar_arrive_expect_tx(&full[s], cb + sbb);
+          bulk_g2s(st, d.rec + off.down_codes + r0 * (d.Fe / 2), cb, &full[s], pol);
+          bulk_g2s(st + cb, d.rec + off.down_sb + r0 * (d.Fe / 16), sbb, &full[s], pol);
+        }
+      }
+      for (int j = max(0, it - NST); j < it; ++j)
+        if (!mbar_wait(&full[j % NST], (j / NST) & 1)) latch_error(&a.ws.ctl[0], kErrTimeout);
+      if (!mbar_wait(xbar, 0)) latch_error(&a.ws.ctl[0], kErrTimeout);
+    }
+    return;
+  }
+
+  // ---- phase 0 (consumer warps): the step's h rows become fixed-point
+  // chunks, one chunk per warp across the grid; then a grid-wide barrier (a
+  // 64-bit arrival counter that only grows: this call's target is the next
+  // multiple of the grid size; every CTA is resident, one per SM, so the
+  // wait is bounded by the slowest CTA's phase 0; on a 2 s timeout the error
+  // is latched); then thread 0 copies the whole fixed-point block into
+  // shared memory.
+  for (int gc = blockIdx.x * NCW + warp; gc < n_cols; gc += gridDim.x * NCW) {
+    int j = 0;
+    while (j + 1 < n_ent && ent[j + 1].c0 <= gc) ++j;
+    const D1Entry d = ent[j];
+    const float* hrow = d.expert < 0 ? a.ws.h_shared : a.ws.h + static_cast<size_t>(j - has_sh) * a.F;
+    const int c = gc - d.c0;
+    publish_hchunk(a, d.c0, d.Fe / 32, c, __ldcg(hrow + c * 32 + lane), lane);
+  }
+  named_bar(2, NCT);
+  if (tid == 0) {
+    __threadfence();
+    unsigned long long* gb = reinterpret_cast<unsigned long long*>(a.ws.ctl + 4);
+    const unsigned long long old = atomicAdd(gb, 1ull);
+    const unsigned long long target = (old / gridDim.x + 1) * gridDim.x;
+    const unsigned long long t0 = global_timer_ns();
+    while (*reinterpret_cast<volatile unsigned long long*>(gb) < target) {
+      if (global_timer_ns() - t0 > kWaitLimitNs) {
+        latch_error(&a.ws.ctl[0], kErrTimeout);
+        break;
+      }
+    }
+    __threadfence();
+    // the chunks were written through the generic proxy; the bulk copy reads
+    // them through the async proxy
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    if (n_cols > 0) {
+      const uint32_t xb = n_cols * 64, sb4 = ((n_cols + 3) / 4) * 16;
+      mbar_arrive_expect_tx(xbar, xb + 2 * sb4);
+      bulk_g2s(xform, a.ws.hx, xb, xbar);
+      bulk_g2s(xscale, a.ws.hx_scale, sb4, xbar);
+      bulk_g2s(xsum, a.ws.hx_sum, sb4, xbar);
+    } else {
+      mbar_arrive(xbar);
+    }
+  }
+
+  // ---- the fixed-point h block lands
+  bool abort = !mbar_wait_warp(xbar, 0);
+  if (abort && lane == 0) latch_error(&a.ws.ctl[0], kErrTimeout);
+  (void)H;
+  // ---- main loop: experts outer, tiles inner
+  const D1Geo gs = d1_geo(has_sh ? a.Fs : a.F, warp, lane), gr = d1_geo(a.F, warp, lane);
+  float acc[kD1MaxTiles][2 * kD1Rpt];  // [tile][shared rows m, routed rows m]
+#pragma unroll
+  for (int t = 0; t < kD1MaxTiles; ++t)
+#pragma unroll
+    for (int m = 0; m < 2 * kD1Rpt; ++m) acc[t][m] = 0.f;
+  RingPos pos;
+  for (int j = 0; j < n_ent; ++j) {  // `abort`: this warp gave up a wait; acted on at the final barrier
+    const D1Entry d = ent[j];
+    const bool sh = d.expert < 0;
+    const D1Geo& g = sh ? gs : gr;
+    XChunk X;
+    float sc = 0.f, psx = 0.f;
+    if (g.act) {
+      const int C = g.C, col = g.col;
+      const uint4 g0 = xform[d.c0 * 4 + 0 * C + col], g1 = xform[d.c0 * 4 + 1 * C + col];
+      const uint4 g2 = xform[d.c0 * 4 + 2 * C + col], g3 = xform[d.c0 * 4 + 3 * C + col];
+      X.eh[0] = g0.x, X.eh[1] = g0.y, X.eh[2] = g0.z, X.eh[3] = g0.w;
+      X.el[0] = g1.x, X.el[1] = g1.y, X.el[2] = g1.z, X.el[3] = g1.w;
+      X.oh[0] = g2.x, X.oh[1] = g2.y, X.oh[2] = g2.z, X.oh[3] = g2.w;
+      X.ol[0] = g3.x, X.ol[1] = g3.y, X.ol[2] = g3.z, X.ol[3] = g3.w;
+      sc = xscale[d.c0 + col] * d.p, psx = d.p * xsum[d.c0 + col];
+    }
+    const int rowb = (d.Fe / 2), sbrow = (d.Fe / 16);
+#pragma unroll
+    for (int t = 0; t < kD1MaxTiles; ++t) {
+      if (t >= ntc) break;
+      const int s = pos.s;
+      const uint32_t ph = pos.ph;
+      pos.next(NST);
+      if (abort) continue;
+      if (!mbar_wait_warp(&full[s], ph)) {
+        if (lane == 0) latch_error(&a.ws.ctl[0], kErrTimeout);
+        abort = true;
+        continue;
+      }
+      if (g.act) {
+        const uint8_t* st = smem + s * SB;
+        const uint8_t* stsb = st + RT * rowb;
+#pragma unroll
+        for (int m = 0; m < kD1Rpt; ++m) {
+          const int r = g.rl + g.NRL * m;
+          if (r < RT) {
+            const uint4 q = *reinterpret_cast<const uint4*>(st + r * rowb + g.col * 16);
+            const uint32_t sbw = *reinterpret_cast<const uint32_t*>(stsb + r * sbrow + (g.col >> 1) * 4);
+            const float v = fmaf(bf16lo(sbw) * sc, static_cast<float>(dot_chunk(q, X)), bf16hi(sbw) * psx);
+            if (sh) acc[t][m] += v;
+            else acc[t][kD1Rpt + m] += v;
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+    }
+  }
+  // ---- combine: per tile, one butterfly; one barrier for the whole CTA
+#pragma unroll
+  for (int t = 0; t < kD1MaxTiles; ++t) {
+    if (t >= ntc) break;
+    const float v = bfly4b(acc[t], lane);  // lane L: value (L >> 3) = [sh m0, sh m1, rt m0, rt m1]
+    if ((lane & 7) == 0) wsum[(t * NCW + warp) * 4 + (lane >> 3)] = v;
+  }
+  if (named_bar_or(1, NCT, abort)) return;  // uniform exit if any warp gave up
+  for (int q = tid; q < ntc * RT; q += NCT) {
+    const int t = q / RT, r = q % RT;
+    float out = 0.f;
+    if (has_sh) {
+      const int rl = r % gs.NRL, m = r / gs.NRL;
+      for (int w = 0; w < gs.WC; ++w) out += wsum[(t * NCW + rl * gs.WC + w) * 4 + m];
+    }
+    {
+      const int rl = r % gr.NRL, m = r / gr.NRL;
+      for (int w = 0; w < gr.WC; ++w) out += wsum[(t * NCW + rl * gr.WC + w) * 4 + kD1Rpt + m];
+    }
+    const size_t o = static_cast<size_t>(blockIdx.x + t * gridDim.x) * RT + r;
+    a.out_bf16[o] = f32_to_bf16_rne(out);
+    if (a.out_f32) a.out_f32[o] = out;
+  }
+}
+
+size_t down_b1_smem_bytes(const LayerArgs& a) {
+  const int has_sh = a.Fs > 0 ? 1 : 0;
+  return d1_smem(a.dn_nst, a.dn_stage, a.k + has_sh, a.k * (a.F / 32) + has_sh * (a.Fs / 32)).total;
+}
+
+// ============================================================================
+// Host side.
+// ============================================================================
+
+static int p2floor(int v) {
+  int p = 1;
+  while (p * 2 <= v) p *= 2;
+  return p;
+}
+
+static int lanes_for(int K, int ncw) {
+  const int C = K / 32, WC = (C + 31) / 32;
+  return p2floor(std::max(1, ncw / WC));
+}
+
+constexpr int kB1SmemBudget = 210 * 1024;
+
+// Geometry of the B = 1 kernels; false when this layer shape needs the
+// general kernels instead (fixed-point h rows too large for shared memory).
+bool plan_b1(LayerArgs& a, int num_sms, int smem_optin) {
+  const int H = a.H;
+  a.gu_nrl = lanes_for(H, kG1Warps);
+  // Eight rows per thread when three such stages fit, else four.
+  int rows = 8;
+  for (;; rows = 4) {
+    const int rth = (rows / 2) * a.gu_nrl;
+    a.gu_stage = (2 * rth * (H / 2 + H / 16) + 127) / 128 * 128;
+    a.gu_nst = std::min(8, (kB1SmemBudget - 4096) / a.gu_stage);
+    if (rows == 4 || a.gu_nst >= 3) break;
+  }
+  a.gu_rows = rows;
+  const int rth = (rows / 2) * a.gu_nrl;
+  if (a.F % rth || (a.Fs && a.Fs % rth)) return false;
+  if (a.gu_nst < 2) return false;
+
+  int nrl_min = lanes_for(a.F, kD1Warps);
+  if (a.Fs) nrl_min = std::min(nrl_min, lanes_for(a.Fs, kD1Warps));
+  const int rt_cap = kD1Rpt * nrl_min;
+  const int Fm = std::max(a.F, a.Fs);
+  int best = 4;
+  double best_cost = 1e300;
+  bool found = false;
+  for (int rt = 4; rt <= rt_cap; rt += 4) {
+    if (H % rt) continue;
+    const int waves = (H / rt + num_sms - 1) / num_sms;
+    if (waves > kD1MaxTiles) continue;
+    const double cost = static_cast<double>(waves) * rt * (Fm / 2.0 + Fm / 16.0);
+    if (cost <= best_cost) best_cost = cost, best = rt, found = true;  // ties: larger tiles
+  }
+  if (!found) return false;
+  a.dn_rt = best;
+  a.dn_tiles = H / best;
+  a.dn_stage = (best * (Fm / 2 + Fm / 16) + 127) / 128 * 128;
+  const int has_sh = a.Fs > 0 ? 1 : 0;
+  const int fixed = d1_smem(0, 0, a.k + has_sh, a.k * (a.F / 32) + has_sh * (a.Fs / 32)).total;
+  a.dn_nst = std::min(8, (kB1SmemBudget - fixed) / a.dn_stage);
+  if (a.dn_nst < 2) return false;
+  if (gateup_b1_smem_bytes(a, rows) + 1024 > static_cast<size_t>(smem_optin)) return false;
+  if (down_b1_smem_bytes(a) + 1024 > static_cast<size_t>(smem_optin)) return false;
+  return true;
+}
+
+cudaError_t set_b1_attributes(int smem_optin) {
+  const void* fns[] = {(const void*)router_b1_kernel, (const void*)gateup_b1_kernel<4>,
+                       (const void*)gateup_b1_kernel<8>, (const void*)down_b1_kernel};
+  for (const void* f : fns) {
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, f);
+    if (e) return e;
+    if ((e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  smem_optin - static_cast<int>(fa.sharedSizeBytes))))
+      return e;
+  }
+  return cudaSuccess;
+}
+
+static cudaError_t launch1(const void* fn, int grid, int block, size_t smem, cudaStream_t st, bool pdl,
+                           const LayerArgs& a) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  void* args[] = {const_cast<LayerArgs*>(&a)};
+  return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+static cudaError_t mark1(const LayerArgs& a, int i, cudaStream_t st) {
+  return a.prof_on ? cudaEventRecord(static_cast<cudaEvent_t>(a.prof[i]), st) : cudaSuccess;
+}
+
+// Launches the B = 1 path; `a` already planned by plan_b1.
+cudaError_t launch_decode_b1(const LayerArgs& a, int num_sms, cudaStream_t st) {
+  const bool pdl = !a.prof_on;
+  const int rgrid = std::max(1, std::min((a.E + kR1Rows - 1) / kR1Rows, 2 * num_sms));
+  cudaError_t e;
+  if ((e = mark1(a, 0, st))) return e;
+  if ((e = launch1((const void*)router_b1_kernel, rgrid, kR1Threads, router_b1_smem_bytes(a.E), st, false, a)))
+    return e;
+  if ((e = mark1(a, 1, st))) return e;
+  const void* gu = a.gu_rows == 8 ? (const void*)gateup_b1_kernel<8> : (const void*)gateup_b1_kernel<4>;
+  if ((e = launch1(gu, num_sms, (kG1Warps + 1) * 32, gateup_b1_smem_bytes(a, a.gu_rows), st, pdl, a)))
+    return e;
+  if ((e = mark1(a, 2, st))) return e;
+  if ((e = launch1((const void*)down_b1_kernel, num_sms, (kD1Warps + 1) * 32, down_b1_smem_bytes(a), st, pdl,
+                   a)))
+    return e;
+  return mark1(a, 3, st);
+}
+
+}  // namespace moe

@@ -30,7 +30,11 @@ struct RecordOffsets {
 
 // Device pointers into the caller's workspace (computed on the host).
 struct Workspace {
-  unsigned* ctl;         // [0] error bits, [1] router done counter
+  unsigned* ctl;         // [0] error bits, [1] router done counter, [2] gate|up item claims,
+                         // [4..5] 64-bit grid-barrier arrivals of the down kernel
+  uint4* hx;             // single token: fixed-point h chunks, [chunk-interleaved][4] words
+  float* hx_scale;       // single token: 2^e of each fixed-point h chunk
+  float* hx_sum;         // single token: plain sum of each h chunk
   float* logits;         // [T][E]
   int* n_act;            // number of distinct routed experts this step
   int* act_expert;       // [E] active expert ids, ascending
@@ -66,6 +70,7 @@ struct LayerArgs {
   // per-launch geometry (plan_decode / plan_prefill)
   int gu_nrl;                  // gate|up row-lanes; an item holds 2*gu_nrl gate + up rows
   int gu_stage, gu_nst;        // gate|up stage bytes and stage count
+  int gu_rows;                 // single-token gate|up: rows per thread per item (4 or 8)
   int dn_rt, dn_tiles;         // down row tile and number of tiles (H / dn_rt)
   int dn_stage, dn_nst;        // down stage bytes and stage count
   int prof_on;                 // record prof[] events between kernels, no PDL

@@ -57,6 +57,13 @@ def test_identity_expert_layer(T):
                      router=(rc, rsb))
     lay = oracle.Layer(H, E, k, H, H, {e: records[e] for e in range(E)}, shared, rc, rsb)
     xs = np.stack([synth.hidden(3, 0, t, H) for t in range(T)])
+    # Every |x| >= 1/16 keeps each 32-value chunk within 2^7 of its largest
+    # magnitude (8), where the single-token kernels' 16-bit fixed-point
+    # activations are exact, so the closed form holds to fp32 rounding.
+    xf = synth.bf16_bits_to_float(xs)
+    small = np.abs(xf) < 0.0625
+    xs[small] = np.where(xf[small] < 0, synth.bf16_from_double(-0.0625),
+                         synth.bf16_from_double(0.0625)).astype(np.uint16)
     xs[:, 0] = synth.bf16_from_double(8.0)
     of, ob, ids, w = run(dl, xs)
     for t in range(T):
@@ -91,6 +98,42 @@ def test_small_layers(shape, T):
         assert_token(t, of, ob, ids, w, ref, rids, rp)
     if shape.k == 1:
         assert np.all(w == 1.0)
+
+
+# Single-token geometries: 2, 3 (with idle warps) and 4 warps per row, no
+# shared expert, and enough items per CTA to wrap the pipeline ring.
+B1_SHAPES = [synth.Shape(2048, 64, 8, 2048, 2048), synth.Shape(3072, 24, 4, 1536, 512),
+             synth.Shape(4096, 32, 4, 1024, 0)]
+
+
+@pytest.mark.parametrize("shape", B1_SHAPES, ids=lambda s: f"H{s.H}F{s.F}Fs{s.Fs}")
+def test_single_token_geometries(shape):
+    hl = HostLayer(shape, seed=41, beta=synth.beta_normal(41, 0, shape.E))
+    orc = hl.oracle()
+    dl = device_from_host(hl)
+    for t in range(2):
+        xs = draw_tokens(orc, 41, 10 + t, 1)
+        of, ob, ids, w = run(dl, xs)
+        ref, rids, rp = orc.token(xs[0])
+        assert_token(0, of, ob, ids, w, ref, rids, rp)
+
+
+@pytest.mark.parametrize("outlier", [64.0, 4096.0])
+def test_activation_outliers(outlier):
+    # One huge activation per token (as real hidden states have): the single-
+    # token path rounds the other activations of that 32-value chunk to
+    # 2^-15 of the outlier; the result must still meet the parity bar.
+    shape = synth.Shape(1024, 40, 6, 448, 320)
+    hl = HostLayer(shape, seed=31)
+    orc = hl.oracle()
+    dl = device_from_host(hl)
+    for t in range(3):
+        x = synth.hidden(31, 7, t, shape.H)
+        x[37 * (t + 1)] = synth.bf16_from_double(outlier * (-1) ** t)
+        xs = x[None]
+        of, ob, ids, w = run(dl, xs)
+        ref, rids, rp = orc.token(xs[0])
+        assert_token(0, of, ob, ids, w, ref, rids, rp)
 
 
 def test_tiny_workload_config0():
