@@ -174,6 +174,45 @@ int moe_set_profile_events(moe_layer *layer, void *const *events);
 /* Thread-local description of the last error (never NULL). */
 const char *moe_last_error(void);
 
+/* ---- Decode without a caller-allocated workspace --------------------------
+ * The pages describe no such call: it exists for callers that cannot
+ * allocate device memory when they run a step -- a plain C host with no
+ * device allocator of its own, or one that must not call cudaMalloc /
+ * cudaFree while serving (both synchronise the whole device and stall every
+ * other stream) or whose allocator has already handed all of HBM to its own
+ * pool.
+ *
+ * moe_decode_noalloc computes exactly what moe_decode computes (same
+ * kernels, same arguments minus the workspace), with the workspace taken
+ * from a static device array of MOE_NOALLOC_SCRATCH_BYTES bytes inside this
+ * library, one per device.  The call itself allocates nothing.
+ *
+ * Limit: moe_workspace_bytes(layer, B) must be <= MOE_NOALLOC_SCRATCH_BYTES
+ * (4 MiB: e.g. H=7168, E=512, top-16, F=Fs=2048 up to B=16); a larger B is
+ * rejected with MOE_ERR_ARG before anything is launched, and moe_last_error()
+ * says to use moe_decode with a caller-allocated workspace.  The layer's
+ * device must be the current device (MOE_ERR_ARG otherwise).
+ *
+ * First call per device: looks up the scratch's device address once (with
+ * that device current) and zeroes the whole scratch on `stream`, ordered
+ * before the step.  The scratch's control words (error word, the router's
+ * completion counter, the gate|up item counter, the down kernel's barrier
+ * counter) must start at zero; every later step leaves them ready for the
+ * next one.  Make this first call before any stream capture begins.
+ *
+ * All calls on one device share the one scratch: calls whose executions
+ * overlap (different streams, different threads or different layers without
+ * an ordering between them) race on it and give undefined results.  Issue
+ * them on one stream, or order them with events.  Errors that device code
+ * latches (a bounded wait that ran out) stay in the private scratch, which
+ * moe_check cannot read; use moe_decode with an own workspace where that
+ * status is needed.
+ *
+ * Pointers, alignment, sizes and return codes otherwise as moe_decode. */
+#define MOE_NOALLOC_SCRATCH_BYTES (4u << 20)
+int moe_decode_noalloc(moe_layer *layer, const uint16_t *x, int32_t B, uint16_t *out_bf16,
+                       float *out_f32, int32_t *ids, float *weights, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -366,3 +366,9 @@ extern "C" int moe_set_profile_events(moe_layer* L, void* const* events) {
 }
 
 extern "C" const char* moe_last_error(void) { return g_err; }
+
+// Internal helpers for entry points defined in other translation units.
+namespace moe {
+int report_error(int code, const char* msg) { return fail(code, "%s", msg); }
+int layer_device(const moe_layer* L) { return valid(L) ? L->device : -1; }
+}  // namespace moe

@@ -80,6 +80,7 @@ SIGNATURES = {
     "moe_residency_slots": (ctypes.c_int, [_vp, _vp, _i32]),
     "moe_residency_set_fault": (ctypes.c_int, [_vp, ctypes.c_int]),
     "moe_residency_close": (None, [_vp]),
+    "moe_decode_noalloc": (ctypes.c_int, [_vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp]),
 }
 
 
@@ -154,6 +155,12 @@ def moe_prefill_chunk(layer, x, T, out_bf16, out_f32, ids, weights, ws, ws_bytes
 def moe_decode_host(layer, x, B, out_bf16, out_f32, ids, weights, ws, ws_bytes, stream=0) -> None:
     check(lib().moe_decode_host(layer, x, B, out_bf16, out_f32, ids, weights, ws, ws_bytes,
                                 stream), "moe_decode_host")
+
+
+def moe_decode_noalloc(layer, x, B, out_bf16, out_f32, ids, weights, stream=0) -> None:
+    """moe_decode with the workspace in the library's static device scratch."""
+    check(lib().moe_decode_noalloc(layer, x, B, out_bf16, out_f32, ids, weights, stream),
+          "moe_decode_noalloc")
 
 
 def moe_set_profile_events(layer: int, events) -> None:
