@@ -33,7 +33,7 @@ sys.path.insert(0, ROOT)
 METRIC = "MoE-layer decode tokens/s + achieved HBM GB/s vs ~8 TB/s peak (B=1/4/16)"
 WORKLOAD = "large-decode"
 NOMINAL_HBM_GBS = 8000.0
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "gateup_kernel_large_decode_b1.txt")
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "gateup_b1_kernel_large_decode_b1.txt")
 
 
 def parse_args():
@@ -186,9 +186,9 @@ def read_traffic():
         if ":" in ln and not ln.startswith(" "):
             k, v = ln.split(":", 1)
             kv[k.strip()] = v.strip()
-    src = os.path.join(ROOT, "quantized_routed_expert_gemv_gb300", "csrc", "decode.cu")
+    src = os.path.join(ROOT, "quantized_routed_expert_gemv_gb300", "csrc", "decode_b1.cu")
     h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    if kv.get("decode_cu_sha256_16") != h:
+    if kv.get("decode_b1_cu_sha256_16") != h:
         return None
     try:
         return float(kv["dram_bytes_per_launch"])
@@ -379,10 +379,11 @@ def run_ours(args, world, rank, local):
         per = [v / Kp for v in sums]
         gateup_s = per[1] / 1e3
         achieved = main["nbytes"]["gateup"] / gateup_s / 1e9
-        out["roofline"] = {"bound": "hbm", "kernel": "gateup_kernel", "achieved": achieved,
+        kname = "gateup_b1_kernel" if B == 1 else "gateup_kernel"
+        out["roofline"] = {"bound": "hbm", "kernel": kname, "achieved": achieved,
                            "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                            "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)",
-                           "traffic": read_traffic(),
+                           "traffic": read_traffic() if B == 1 else None,
                            "algorithmic_bytes_per_launch": main["nbytes"]["gateup"],
                            "kernel_ms": {"router": per[0], "gateup": per[1], "down": per[2]}}
 
