@@ -174,6 +174,81 @@ int moe_set_profile_events(moe_layer *layer, void *const *events);
 /* Thread-local description of the last error (never NULL). */
 const char *moe_last_error(void);
 
+/* ---- Expert residency: a bounded HBM cache of expert records ---------------
+ * TurboFieldfare page, section "Token üretim süreci": the router's chosen ids
+ * are checked against a per-layer LFU cache of bounded size; misses are
+ * filled from the slower tier while the shared expert is computed; shared
+ * and routed outputs are combined when the reads finish.  Here the slow tier
+ * is page-locked host memory holding all E records of the layer (same
+ * record format and stride as moe_record_layout_of), the cache is a pool of
+ * n_slots record slots in HBM, and misses are copied with cudaMemcpyAsync on
+ * a caller-given copy stream.
+ *
+ * Policy: one use count per expert, cumulative over the run (kept after
+ * eviction); all experts of the step are counted and pinned first; a miss
+ * takes the lowest empty slot, else evicts the unpinned resident with the
+ * lowest count, ties to the least recently used, then the lower id; experts
+ * are visited in the order they first appear in the step's ids (token-major,
+ * rank order).  A miss copies one whole record. */
+typedef struct moe_residency moe_residency;
+
+typedef struct {
+    uint64_t steps;      /* moe_residency_decode calls that reached the cache */
+    uint64_t hits;       /* distinct experts of a step already resident */
+    uint64_t misses;     /* distinct experts copied in */
+    uint64_t evictions;  /* misses that replaced a resident expert */
+    uint64_t bytes_h2d;  /* record bytes copied host -> device */
+} moe_residency_stats_t;
+
+/* Host-side fault injection for tests (no device fault is involved). */
+#define MOE_RESIDENCY_FAULT_NONE 0
+#define MOE_RESIDENCY_FAULT_TAG 1   /* next step uploads a wrong tag for one of its slots:
+                                       the kernels latch MOE_ERR_RESIDENCY (moe_check) */
+#define MOE_RESIDENCY_FAULT_COPY 2  /* next step's first miss fails as if its copy had:
+                                       MOE_ERR_CUDA, the slot is left empty */
+
+/* Bytes of the device slot pool for n_slots slots: the records at the layer's
+ * record stride, then the slot tables.  0 for an invalid handle or n_slots
+ * outside [1, n_experts]. */
+size_t moe_residency_pool_bytes(const moe_layer *layer, int32_t n_slots);
+
+/* Opens the cache.  host_records (host, page-locked, 16-byte aligned): the
+ * layer's E expert records at the record stride, read by the copies;
+ * device_pool (device, 256-byte aligned, >= moe_residency_pool_bytes): slot
+ * storage, owned by the caller, written only by this cache.  n_slots in
+ * [top_k, n_experts].  Allocates two small pinned host buffers and two
+ * events, freed by moe_residency_close.  The layer may have been opened with
+ * expert_records = NULL. */
+int moe_residency_open(moe_layer *layer, const void *host_records, int32_t n_slots,
+                       void *device_pool, size_t device_pool_bytes, moe_residency **out);
+
+/* One decode step through the cache: arguments and outputs as moe_decode,
+ * plus the copy stream (cudaStream_t as void*; may equal main_stream, which
+ * then forgoes the overlap).  Order of work: the router on main_stream; the
+ * ids to the host; for B = 1 the shared expert's gate|up on main_stream; the
+ * host waits for the ids (this call blocks until the router has finished),
+ * updates the cache and issues one cudaMemcpyAsync per miss and one for the
+ * slot tables on copy_stream; main_stream waits for them, then runs the
+ * routed experts and the combine.  MOE_ERR_RESIDENCY (returned) if a step
+ * needs more distinct experts than there are slots or the router's ids are
+ * out of range; the cache state is then unchanged.  Device-side tag
+ * mismatches are latched and reported by moe_check. */
+int moe_residency_decode(moe_residency *res, const uint16_t *x, int32_t B, uint16_t *out_bf16,
+                         float *out_f32, int32_t *ids, float *weights, void *workspace,
+                         size_t workspace_bytes, void *main_stream, void *copy_stream);
+
+/* Counters since open. */
+int moe_residency_stats(const moe_residency *res, moe_residency_stats_t *out);
+
+/* The expert held by each slot (-1 = empty), host copy; n >= n_slots. */
+int moe_residency_slots(const moe_residency *res, int32_t *slot_expert, int32_t n);
+
+/* Arms one of the MOE_RESIDENCY_FAULT_* modes for the next step (one-shot). */
+int moe_residency_set_fault(moe_residency *res, int32_t mode);
+
+/* Frees the host bookkeeping (pinned buffers, events); NULL is a no-op. */
+void moe_residency_close(moe_residency *res);
+
 /* ---- Decode without a caller-allocated workspace --------------------------
  * The pages describe no such call: it exists for callers that cannot
  * allocate device memory when they run a step -- a plain C host with no

@@ -266,8 +266,12 @@ extern "C" int moe_workspace_init(const moe_layer* L, void* ws, size_t bytes, vo
 
 enum class Path { kDecode, kPrefill };
 
-static int run(moe_layer* L, const uint16_t* x, int32_t T, uint16_t* ob, float* of, int32_t* ids,
-               float* wts, void* ws, size_t ws_bytes, void* stream, Path path, const char* name) {
+// Validates one call and fills `a` (geometry and workspace; the records are
+// the layer's own unless the caller replaces them).  T == 0 is valid and
+// leaves *a untouched.
+static int prepare(moe_layer* L, const uint16_t* x, int32_t T, uint16_t* ob, float* of, int32_t* ids,
+                   float* wts, void* ws, size_t ws_bytes, Path path, bool need_records, LayerArgs* a,
+                   const char* name) {
   if (!valid(L)) return fail(MOE_ERR_ARG, "%s: invalid layer handle", name);
   const int cap = path == Path::kPrefill ? std::min(128, (int)L->d.max_tokens) : (int)L->d.max_tokens;
   if (T < 0 || T > cap) return fail(MOE_ERR_ARG, "%s: token count %d outside [0, %d]", name, T, cap);
@@ -276,13 +280,22 @@ static int run(moe_layer* L, const uint16_t* x, int32_t T, uint16_t* ob, float* 
   if (!aligned(x, 16) || !aligned(ob, 16) || !aligned(of, 16) || !aligned(ids, 16) || !aligned(wts, 16))
     return fail(MOE_ERR_ALIGN, "%s: activation/output pointers must be 16-byte aligned", name);
   if (!aligned(ws, 256)) return fail(MOE_ERR_ALIGN, "%s: workspace must be 256-byte aligned", name);
-  if (!L->w.expert_records) return fail(MOE_ERR_ARG, "%s: layer has no resident expert records", name);
+  if (need_records && !L->w.expert_records)
+    return fail(MOE_ERR_ARG, "%s: layer has no resident expert records", name);
   size_t pf_off = 0;
-  LayerArgs a = base_args(L);
-  const size_t need = carve(L, T, &a.ws, static_cast<uint8_t*>(ws), &pf_off);
+  *a = base_args(L);
+  const size_t need = carve(L, T, &a->ws, static_cast<uint8_t*>(ws), &pf_off);
   if (ws_bytes < need) return fail(MOE_ERR_ARG, "%s: workspace of %zu B is smaller than the %zu B needed", name, ws_bytes, need);
-  a.T = T, a.x = x, a.out_bf16 = ob, a.out_f32 = of, a.ids = ids, a.weights = wts;
+  a->T = T, a->x = x, a->out_bf16 = ob, a->out_f32 = of, a->ids = ids, a->weights = wts;
   (void)pf_off;
+  return MOE_OK;
+}
+
+static int run(moe_layer* L, const uint16_t* x, int32_t T, uint16_t* ob, float* of, int32_t* ids,
+               float* wts, void* ws, size_t ws_bytes, void* stream, Path path, const char* name) {
+  LayerArgs a;
+  const int rc = prepare(L, x, T, ob, of, ids, wts, ws, ws_bytes, path, true, &a, name);
+  if (rc || T == 0) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (path == Path::kPrefill)
@@ -370,5 +383,24 @@ extern "C" const char* moe_last_error(void) { return g_err; }
 // Internal helpers for entry points defined in other translation units.
 namespace moe {
 int report_error(int code, const char* msg) { return fail(code, "%s", msg); }
+int report_cuda(cudaError_t e, const char* what) { return cuda_fail(e, what); }
 int layer_device(const moe_layer* L) { return valid(L) ? L->device : -1; }
+const moe_layer_desc* layer_desc(const moe_layer* L) { return valid(L) ? &L->d : nullptr; }
+uint64_t layer_record_stride(const moe_layer* L) { return L->off_r.stride; }
+uint64_t layer_record_bytes(const moe_layer* L) { return L->off_r.bytes; }
+
+// A decode call's arguments for the expert cache: validated like moe_decode,
+// with the routed records read through the cache's slot pool.
+int prepare_cached_decode(moe_layer* L, const uint16_t* x, int32_t B, uint16_t* ob, float* of,
+                          int32_t* ids, float* wts, void* ws, size_t ws_bytes, const uint8_t* pool,
+                          const int32_t* slot_of, const int32_t* slot_tag, int n_slots, LayerArgs* a,
+                          bool* single, int* num_sms, const char* name) {
+  int rc = prepare(L, x, B, ob, of, ids, wts, ws, ws_bytes, Path::kDecode, false, a, name);
+  if (rc || B == 0) return rc;
+  a->records = pool, a->slot_of = slot_of, a->slot_tag = slot_tag, a->n_slots = n_slots;
+  a->prof_on = 0;
+  *single = B == 1 && plan_b1(*a, L->num_sms, L->smem_optin);
+  *num_sms = L->num_sms;
+  return MOE_OK;
+}
 }  // namespace moe

@@ -239,13 +239,14 @@ struct Entry {     // one expert's work this step
   int pair0;       // first (expert, token) pair -- its h row
   int shared;      // 1 for the shared expert
   int expert;      // routed expert id (-1 for the shared expert)
+  int slot;        // slot (or expert index) its record is read from
 };
 
 __device__ __forceinline__ Entry get_entry(const LayerArgs& a, int idx, int has_sh) {
   Entry en;
   if (has_sh && idx == 0) {
     en.rec = a.shared, en.off = &a.off_s, en.Fe = a.Fs, en.ntok = a.T, en.pair0 = 0;
-    en.shared = 1, en.expert = -1;
+    en.shared = 1, en.expert = -1, en.slot = -1;
     return en;
   }
   const int i = idx - has_sh;
@@ -253,10 +254,15 @@ __device__ __forceinline__ Entry get_entry(const LayerArgs& a, int idx, int has_
   int cnt = a.ws.act_cnt[i];
   if (e < 0 || e >= a.E) e = 0;
   if (cnt < 0 || cnt > a.T) cnt = 0;
-  const int slot = a.slot_of ? a.slot_of[e] : e;
+  int slot = e;
+  if (a.slot_of) {  // residency: a slot outside the pool is never read
+    slot = a.slot_of[e];
+    if (slot < 0 || slot >= a.n_slots) latch_error(&a.ws.ctl[0], kErrResidency), slot = 0;
+  }
   en.rec = a.records + static_cast<size_t>(slot) * a.off_r.stride;
   en.off = &a.off_r, en.Fe = a.F, en.ntok = cnt, en.pair0 = a.ws.act_off[i];
   en.shared = 0, en.expert = e;
+  en.slot = slot;
   return en;
 }
 
@@ -318,7 +324,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) gateup_kernel(const __grid_
         const int idx = i < tiles_s ? 0 : has_sh + (i - tiles_s) / tiles_r;
         const int tile = i < tiles_s ? i : (i - tiles_s) % tiles_r;
         const Entry en = get_entry(a, idx, has_sh);
-        if (!en.shared && a.slot_tag && a.slot_tag[a.slot_of[en.expert]] != en.expert)
+        if (!en.shared && a.slot_tag && a.slot_tag[en.slot] != en.expert)
           latch_error(&a.ws.ctl[0], kErrResidency);
         const size_t j0 = static_cast<size_t>(tile) * rth;
         const uint32_t cb = rth * (H / 2), sbb = rth * (H / 16);
@@ -486,7 +492,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) down_kernel(const __grid_co
         const size_t r0 = static_cast<size_t>(tile) * RT;
         for (int idx = 0; idx < n_ent && !stop; ++idx) {
           const Entry en = get_entry(a, idx, has_sh);
-          if (!en.shared && a.slot_tag && a.slot_tag[a.slot_of[en.expert]] != en.expert)
+          if (!en.shared && a.slot_tag && a.slot_tag[en.slot] != en.expert)
             latch_error(&a.ws.ctl[0], kErrResidency);
           const float* hb = en.shared ? a.ws.h_shared : a.ws.h + static_cast<size_t>(en.pair0) * en.Fe;
           for (int tg = 0; tg < en.ntok; tg += NTOK, ++it) {
@@ -711,17 +717,16 @@ static cudaError_t mark(const LayerArgs& a, int i, cudaStream_t st) {
   return a.prof_on ? cudaEventRecord(static_cast<cudaEvent_t>(a.prof[i]), st) : cudaSuccess;
 }
 
-cudaError_t launch_decode(const LayerArgs& in, int num_sms, cudaStream_t st) {
-  LayerArgs a = in;
+static cudaError_t launch_router_g(const LayerArgs& a, int num_sms, cudaStream_t st) {
   const bool one = (a.T == 1);
-  const bool pdl = !a.prof_on;
-  plan_decode(a, num_sms, one ? 16 : 7, one ? 8 : 7, one ? 1 : 4);
   const int rgrid = std::max(1, std::min((a.E + kRouterRows - 1) / kRouterRows, 2 * num_sms));
+  return launch_ex(one ? (const void*)router_kernel<1> : (const void*)router_kernel<2>, dim3(rgrid),
+                   dim3(kRouterThreads), router_smem_bytes(a.E), st, false, a);
+}
+
+static cudaError_t launch_experts_g(LayerArgs& a, int num_sms, cudaStream_t st, bool pdl) {
+  const bool one = (a.T == 1);
   cudaError_t e;
-  if ((e = mark(a, 0, st))) return e;
-  e = launch_ex(one ? (const void*)router_kernel<1> : (const void*)router_kernel<2>, dim3(rgrid),
-                dim3(kRouterThreads), router_smem_bytes(a.E), st, false, a);
-  if (e || (e = mark(a, 1, st))) return e;
   if (one)
     e = launch_ex((const void*)gateup_kernel<1, 16>, dim3(num_sms), dim3(17 * 32),
                   gateup_smem_bytes(a, 1, 16), st, pdl, a);
@@ -735,7 +740,32 @@ cudaError_t launch_decode(const LayerArgs& in, int num_sms, cudaStream_t st) {
   else
     e = launch_ex((const void*)down_kernel<4, 7>, dim3(num_sms), dim3(8 * 32),
                   down_smem_bytes(a, 4, 7), st, pdl, a);
-  if (e) return e;
+  return e;
+}
+
+// The router alone, then (after the expert cache is updated) everything
+// else: the general path's split for the expert cache.
+cudaError_t launch_decode_router(const LayerArgs& a, int num_sms, cudaStream_t st) {
+  return launch_router_g(a, num_sms, st);
+}
+
+cudaError_t launch_decode_experts(const LayerArgs& in, int num_sms, cudaStream_t st) {
+  LayerArgs a = in;
+  const bool one = (a.T == 1);
+  plan_decode(a, num_sms, one ? 16 : 7, one ? 8 : 7, one ? 1 : 4);
+  return launch_experts_g(a, num_sms, st, false);
+}
+
+cudaError_t launch_decode(const LayerArgs& in, int num_sms, cudaStream_t st) {
+  LayerArgs a = in;
+  const bool one = (a.T == 1);
+  const bool pdl = !a.prof_on;
+  plan_decode(a, num_sms, one ? 16 : 7, one ? 8 : 7, one ? 1 : 4);
+  cudaError_t e;
+  if ((e = mark(a, 0, st))) return e;
+  e = launch_router_g(a, num_sms, st);
+  if (e || (e = mark(a, 1, st))) return e;
+  if ((e = launch_experts_g(a, num_sms, st, pdl))) return e;
   return mark(a, 3, st);
 }
 

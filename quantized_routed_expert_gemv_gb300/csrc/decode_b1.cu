@@ -96,21 +96,26 @@ __device__ __forceinline__ int clamp_n_act(const LayerArgs& a) {
 struct B1Entry {
   const uint8_t* rec;
   const RecordOffsets* off;
-  int Fe, pair, shared, expert;
+  int Fe, pair, shared, expert, slot;
 };
 
 __device__ __forceinline__ B1Entry b1_entry(const LayerArgs& a, int idx, int has_sh) {
   B1Entry en;
   if (has_sh && idx == 0) {
-    en.rec = a.shared, en.off = &a.off_s, en.Fe = a.Fs, en.pair = 0, en.shared = 1, en.expert = -1;
+    en.rec = a.shared, en.off = &a.off_s, en.Fe = a.Fs, en.pair = 0, en.shared = 1, en.expert = -1, en.slot = -1;
     return en;
   }
   const int i = idx - has_sh;
   int e = a.ws.act_expert[i];
   if (e < 0 || e >= a.E) e = 0;
-  const int slot = a.slot_of ? a.slot_of[e] : e;
+  int slot = e;
+  if (a.slot_of) {  // residency: a slot outside the pool is never read
+    slot = a.slot_of[e];
+    if (slot < 0 || slot >= a.n_slots) latch_error(&a.ws.ctl[0], kErrResidency), slot = 0;
+  }
   en.rec = a.records + static_cast<size_t>(slot) * a.off_r.stride;
   en.off = &a.off_r, en.Fe = a.F, en.pair = a.ws.act_off[i], en.shared = 0, en.expert = e;
+  en.slot = slot;
   return en;
 }
 
@@ -126,6 +131,7 @@ constexpr int kR1Rows = 8;  // rows per CTA pass: 64 CTAs for 512 experts leave 
 __global__ void __launch_bounds__(kR1Threads) router_b1_kernel(const __grid_constant__ LayerArgs a) {
   extern __shared__ __align__(16) float rsm[];
   pdl_launch_dependents();
+  if (blockIdx.x == 0 && threadIdx.x == 0) a.ws.ctl[3] = 0u;  // shared-only gate|up claims
   const int H = a.H, E = a.E, k = a.k;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   constexpr int NW = kR1Threads / 32;
@@ -338,14 +344,19 @@ __global__ void __launch_bounds__((kG1Warps + 1) * 32, 1) gateup_b1_kernel(const
   if (warp == NCW) {  // ---------------- producer warp
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
-      unsigned* claim = &a.ws.ctl[2];
+      // part 1 (shared expert only) counts its claims in ctl[3], which the
+      // router of the next step clears; parts 0 and 2 in ctl[2], cleared by
+      // the down kernel.  Part 2 starts after the shared items.
+      const int part = a.gu_part;
+      unsigned* claim = &a.ws.ctl[part == 1 ? 3 : 2];
+      const int base = part == 2 ? tiles_s : 0;
       int it = 0, n_items = tiles_s;
       bool waited = false, marker = false;
       RingPos pos;
-      int next = static_cast<int>(atomicAdd(claim, 1u));
+      int next = base + static_cast<int>(atomicAdd(claim, 1u));
       for (;; ++it, pos.next(NST)) {
         const int i = next;
-        if (i >= tiles_s && !waited) {
+        if (i >= tiles_s && !waited && part != 1) {
           pdl_wait();
           waited = true;
           n_items = tiles_s + clamp_n_act(a) * tiles_r;
@@ -361,11 +372,11 @@ __global__ void __launch_bounds__((kG1Warps + 1) * 32, 1) gateup_b1_kernel(const
           marker = true;
           break;
         }
-        next = static_cast<int>(atomicAdd(claim, 1u));  // claim ahead, latency overlaps the copy
+        next = base + static_cast<int>(atomicAdd(claim, 1u));  // claim ahead, latency overlaps the copy
         const int idx = i < tiles_s ? 0 : has_sh + (i - tiles_s) / tiles_r;
         const int tile = i < tiles_s ? i : (i - tiles_s) % tiles_r;
         const B1Entry en = b1_entry(a, idx, has_sh);
-        if (!en.shared && a.slot_tag && a.slot_tag[a.slot_of[en.expert]] != en.expert)
+        if (!en.shared && a.slot_tag && a.slot_tag[en.slot] != en.expert)
           latch_error(&a.ws.ctl[0], kErrResidency);
         const size_t j0 = static_cast<size_t>(tile) * rth;
         const uint32_t cb = rth * (H / 2), sbb = rth * (H / 16);
@@ -569,7 +580,7 @@ __global__ void __launch_bounds__((kD1Warps + 1) * 32, 1) down_b1_kernel(const _
       d.p = en.shared ? 1.f : a.weights[a.ws.pair_slot[en.pair]];
       d.c0 = en.shared ? 0 : has_sh * (a.Fs / 32) + (j - has_sh) * (a.F / 32);
       ent[j] = d;
-      if (!en.shared && a.slot_tag && a.slot_tag[a.slot_of[en.expert]] != en.expert)
+      if (!en.shared && a.slot_tag && a.slot_tag[en.slot] != en.expert)
         latch_error(&a.ws.ctl[0], kErrResidency);
     }
   }
@@ -839,23 +850,50 @@ static cudaError_t mark1(const LayerArgs& a, int i, cudaStream_t st) {
   return a.prof_on ? cudaEventRecord(static_cast<cudaEvent_t>(a.prof[i]), st) : cudaSuccess;
 }
 
+static cudaError_t launch_router1(const LayerArgs& a, int num_sms, cudaStream_t st) {
+  const int rgrid = std::max(1, std::min((a.E + kR1Rows - 1) / kR1Rows, 2 * num_sms));
+  return launch1((const void*)router_b1_kernel, rgrid, kR1Threads, router_b1_smem_bytes(a.E), st, false, a);
+}
+
+static cudaError_t launch_gateup1(const LayerArgs& a, int part, int num_sms, cudaStream_t st, bool pdl) {
+  LayerArgs b = a;
+  b.gu_part = part;
+  const void* gu = b.gu_rows == 8 ? (const void*)gateup_b1_kernel<8> : (const void*)gateup_b1_kernel<4>;
+  return launch1(gu, num_sms, (kG1Warps + 1) * 32, gateup_b1_smem_bytes(b, b.gu_rows), st, pdl, b);
+}
+
+static cudaError_t launch_down1(const LayerArgs& a, int num_sms, cudaStream_t st, bool pdl) {
+  return launch1((const void*)down_b1_kernel, num_sms, (kD1Warps + 1) * 32, down_b1_smem_bytes(a), st, pdl, a);
+}
+
 // Launches the B = 1 path; `a` already planned by plan_b1.
 cudaError_t launch_decode_b1(const LayerArgs& a, int num_sms, cudaStream_t st) {
   const bool pdl = !a.prof_on;
-  const int rgrid = std::max(1, std::min((a.E + kR1Rows - 1) / kR1Rows, 2 * num_sms));
   cudaError_t e;
   if ((e = mark1(a, 0, st))) return e;
-  if ((e = launch1((const void*)router_b1_kernel, rgrid, kR1Threads, router_b1_smem_bytes(a.E), st, false, a)))
-    return e;
+  if ((e = launch_router1(a, num_sms, st))) return e;
   if ((e = mark1(a, 1, st))) return e;
-  const void* gu = a.gu_rows == 8 ? (const void*)gateup_b1_kernel<8> : (const void*)gateup_b1_kernel<4>;
-  if ((e = launch1(gu, num_sms, (kG1Warps + 1) * 32, gateup_b1_smem_bytes(a, a.gu_rows), st, pdl, a)))
-    return e;
+  if ((e = launch_gateup1(a, 0, num_sms, st, pdl))) return e;
   if ((e = mark1(a, 2, st))) return e;
-  if ((e = launch1((const void*)down_b1_kernel, num_sms, (kD1Warps + 1) * 32, down_b1_smem_bytes(a), st, pdl,
-                   a)))
-    return e;
+  if ((e = launch_down1(a, num_sms, st, pdl))) return e;
   return mark1(a, 3, st);
+}
+
+// The same step in three parts, for the expert cache: the router; the shared
+// expert's gate|up (which runs while the host updates the cache and copies
+// the missing records); then the routed experts' gate|up and the down +
+// combine kernel.
+cudaError_t launch_b1_router(const LayerArgs& a, int num_sms, cudaStream_t st) {
+  return launch_router1(a, num_sms, st);
+}
+
+cudaError_t launch_b1_shared(const LayerArgs& a, int num_sms, cudaStream_t st) {
+  return launch_gateup1(a, 1, num_sms, st, false);
+}
+
+cudaError_t launch_b1_routed(const LayerArgs& a, int num_sms, cudaStream_t st) {
+  cudaError_t e = launch_gateup1(a, 2, num_sms, st, false);
+  return e ? e : launch_down1(a, num_sms, st, true);
 }
 
 }  // namespace moe

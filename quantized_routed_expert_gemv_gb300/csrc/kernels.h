@@ -31,7 +31,8 @@ struct RecordOffsets {
 // Device pointers into the caller's workspace (computed on the host).
 struct Workspace {
   unsigned* ctl;         // [0] error bits, [1] router done counter, [2] gate|up item claims,
-                         // [4..5] 64-bit grid-barrier arrivals of the down kernel
+                         // [3] shared-only gate|up claims, [4..5] 64-bit grid-barrier
+                         // arrivals of the down kernel
   uint4* hx;             // single token: fixed-point h chunks, [chunk-interleaved][4] words
   float* hx_scale;       // single token: 2^e of each fixed-point h chunk
   float* hx_sum;         // single token: plain sum of each h chunk
@@ -60,6 +61,7 @@ struct LayerArgs {
   const float* beta;       // [E] or null
   const int32_t* slot_of;  // [E] expert -> slot (residency) or null for identity
   const int32_t* slot_tag; // [n_slots] expert id held by each slot, or null
+  int n_slots;             // slots of the pool when slot_of is set
   const uint16_t* x;       // [T][H] bf16
   uint16_t* out_bf16;      // [T][H]
   float* out_f32;          // [T][H] or null
@@ -71,6 +73,8 @@ struct LayerArgs {
   int gu_nrl;                  // gate|up row-lanes; an item holds 2*gu_nrl gate + up rows
   int gu_stage, gu_nst;        // gate|up stage bytes and stage count
   int gu_rows;                 // single-token gate|up: rows per thread per item (4 or 8)
+  int gu_part;                 // single-token gate|up items: 0 all, 1 shared expert only,
+                               // 2 routed experts only
   int dn_rt, dn_tiles;         // down row tile and number of tiles (H / dn_rt)
   int dn_stage, dn_nst;        // down stage bytes and stage count
   int prof_on;                 // record prof[] events between kernels, no PDL

@@ -105,3 +105,59 @@ class DeviceLayer:
             self.close()
         except Exception:
             pass
+
+
+def pinned_records(shape: synth.Shape, weight_seed: int, layer: int = 0,
+                   host_records: np.ndarray | None = None) -> torch.Tensor:
+    """All E expert records of a layer in page-locked host memory."""
+    stride = synth.record_stride(shape.H, shape.F)
+    t = torch.empty(shape.E * stride, dtype=torch.uint8, pin_memory=True)
+    if host_records is not None:
+        t.copy_(torch.from_numpy(np.ascontiguousarray(host_records).reshape(-1)))
+    else:
+        synth.fill_records(weight_seed, layer, range(shape.E), shape.H, shape.F, t.numpy())
+    return t
+
+
+class CachedLayer:
+    """A layer whose routed experts are read through the HBM expert cache
+    (moe_residency_*): host records pinned, n_slots record slots on the GPU."""
+
+    def __init__(self, dl: DeviceLayer, host_records: torch.Tensor, n_slots: int):
+        self.dl = dl
+        self.host = host_records
+        self.n_slots = n_slots
+        self.pool_bytes = moe.moe_residency_pool_bytes(dl.handle, n_slots)
+        self.pool = torch.empty(self.pool_bytes, dtype=torch.uint8, device=dl.device)
+        self.handle = moe.moe_residency_open(dl.handle, host_records.data_ptr(), n_slots,
+                                             self.pool.data_ptr(), self.pool_bytes)
+        self.copy_stream = torch.cuda.Stream(dl.device)
+
+    def decode(self, x: torch.Tensor, outs=None, stream=None):
+        ob, of, ids, w = outs or self.dl.outputs(x.shape[0])
+        st = stream if stream is not None else torch.cuda.current_stream(self.dl.device).cuda_stream
+        moe.moe_residency_decode(self.handle, x.data_ptr(), x.shape[0], ob.data_ptr(),
+                                 of.data_ptr() if of is not None else None, ids.data_ptr(),
+                                 w.data_ptr(), self.dl.ws.data_ptr(), self.dl.ws_bytes, st,
+                                 self.copy_stream.cuda_stream)
+        return ob, of, ids, w
+
+    def stats(self) -> dict:
+        return moe.moe_residency_stats(self.handle)
+
+    def slots(self):
+        return moe.moe_residency_slots(self.handle, self.n_slots)
+
+    def set_fault(self, mode: int) -> None:
+        moe.moe_residency_set_fault(self.handle, mode)
+
+    def close(self):
+        if self.handle:
+            moe.moe_residency_close(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

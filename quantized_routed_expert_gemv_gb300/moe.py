@@ -73,12 +73,13 @@ SIGNATURES = {
     "moe_check": (ctypes.c_int, [_vp, _vp, _vp]),
     "moe_last_error": (ctypes.c_char_p, []),
     "moe_set_profile_events": (ctypes.c_int, [_vp, ctypes.POINTER(_vp)]),
-    "moe_residency_open": (ctypes.c_int, [_vp, _vp, _i32, _vp, _sz, _vp, ctypes.POINTER(_vp)]),
+    "moe_residency_pool_bytes": (_sz, [_vp, _i32]),
+    "moe_residency_open": (ctypes.c_int, [_vp, _vp, _i32, _vp, _sz, ctypes.POINTER(_vp)]),
     "moe_residency_decode": (ctypes.c_int, [_vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _sz, _vp,
                                             _vp]),
     "moe_residency_stats": (ctypes.c_int, [_vp, ctypes.POINTER(moe_residency_stats_t)]),
     "moe_residency_slots": (ctypes.c_int, [_vp, _vp, _i32]),
-    "moe_residency_set_fault": (ctypes.c_int, [_vp, ctypes.c_int]),
+    "moe_residency_set_fault": (ctypes.c_int, [_vp, _i32]),
     "moe_residency_close": (None, [_vp]),
     "moe_decode_noalloc": (ctypes.c_int, [_vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp]),
 }
@@ -167,6 +168,46 @@ def moe_set_profile_events(layer: int, events) -> None:
     """events: four cudaEvent_t handles (ints) or None to switch the hook off."""
     arr = None if events is None else (_vp * 4)(*events)
     check(lib().moe_set_profile_events(layer, arr), "moe_set_profile_events")
+
+
+MOE_RESIDENCY_FAULT_NONE, MOE_RESIDENCY_FAULT_TAG, MOE_RESIDENCY_FAULT_COPY = 0, 1, 2
+
+
+def moe_residency_pool_bytes(layer: int, n_slots: int) -> int:
+    return int(lib().moe_residency_pool_bytes(layer, n_slots))
+
+
+def moe_residency_open(layer: int, host_records: int, n_slots: int, pool: int, pool_bytes: int) -> int:
+    h = _vp()
+    check(lib().moe_residency_open(layer, host_records, n_slots, pool, pool_bytes, ctypes.byref(h)),
+          "moe_residency_open")
+    return h.value
+
+
+def moe_residency_decode(res, x, B, out_bf16, out_f32, ids, weights, ws, ws_bytes, main_stream=0,
+                         copy_stream=0) -> None:
+    check(lib().moe_residency_decode(res, x, B, out_bf16, out_f32, ids, weights, ws, ws_bytes,
+                                     main_stream, copy_stream), "moe_residency_decode")
+
+
+def moe_residency_stats(res: int) -> dict:
+    out = moe_residency_stats_t()
+    check(lib().moe_residency_stats(res, ctypes.byref(out)), "moe_residency_stats")
+    return {n: int(getattr(out, n)) for n, _ in moe_residency_stats_t._fields_}
+
+
+def moe_residency_slots(res: int, n_slots: int):
+    arr = (ctypes.c_int32 * n_slots)()
+    check(lib().moe_residency_slots(res, arr, n_slots), "moe_residency_slots")
+    return list(arr)
+
+
+def moe_residency_set_fault(res: int, mode: int) -> None:
+    check(lib().moe_residency_set_fault(res, mode), "moe_residency_set_fault")
+
+
+def moe_residency_close(res: int) -> None:
+    lib().moe_residency_close(res)
 
 
 def moe_check(layer: int, ws: int, stream: int = 0) -> int:

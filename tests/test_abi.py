@@ -117,6 +117,26 @@ def test_calls_reject_invalid_handles(L):
     assert isinstance(moe.last_error(), str)
 
 
+def test_residency_and_noalloc_calls_reject_invalid_handles(L):
+    fake = (ctypes.c_uint8 * 4096)()
+    p = ctypes.addressof(fake)
+    assert L.moe_residency_pool_bytes(None, 4) == 0
+    assert L.moe_residency_pool_bytes(p, 4) == 0
+    h = ctypes.c_void_p()
+    assert L.moe_residency_open(None, p, 4, p, 1 << 20, ctypes.byref(h)) == moe.MOE_ERR_ARG
+    assert L.moe_residency_open(p, p, 4, p, 1 << 20, ctypes.byref(h)) == moe.MOE_ERR_ARG
+    assert h.value is None
+    for r in (None, p):
+        assert L.moe_residency_decode(r, 0, 1, 0, 0, 0, 0, 0, 0, None, None) == moe.MOE_ERR_ARG
+        st = moe.moe_residency_stats_t()
+        assert L.moe_residency_stats(r, ctypes.byref(st)) == moe.MOE_ERR_ARG
+        assert L.moe_residency_slots(r, (ctypes.c_int32 * 4)(), 4) == moe.MOE_ERR_ARG
+        assert L.moe_residency_set_fault(r, 1) == moe.MOE_ERR_ARG
+        L.moe_residency_close(r)  # ignored
+        assert L.moe_decode_noalloc(r, 0, 1, 0, 0, 0, 0, None) == moe.MOE_ERR_ARG
+    assert "invalid" in moe.last_error()
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(moe, "_lib", None)
     monkeypatch.setattr(moe, "LIB_PATH", str(tmp_path / "missing.so"))

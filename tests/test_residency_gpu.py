@@ -1,0 +1,175 @@
+"""The HBM expert cache (moe_residency_*) through the C ABI.
+
+* The hand-worked LFU trace (tests/golden/lfu_trace.txt) replayed on the GPU
+  path: the router is steered to the trace's ids by a large per-expert logit
+  offset; slot contents and hit/miss counts must follow the trace exactly.
+* Zipf-biased streams at B=1 (single-token kernels split around the cache
+  update) and B=4 (general kernels): hits, misses and slot contents equal
+  the oracle's LFU replay of the ids the GPU chose; outputs equal
+  moe_decode's with every expert resident, and the fp64 oracle's within the
+  parity bar.
+* Host-side fault injection: a wrong slot tag is caught by the kernels
+  (MOE_ERR_RESIDENCY through moe_check); a failed copy returns MOE_ERR_CUDA,
+  leaves the slot empty, and the next step recovers.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from layers import HostLayer, hidden_with_margin
+from quantized_routed_expert_gemv_gb300 import moe, synth
+from quantized_routed_expert_gemv_gb300.device import (CachedLayer, DeviceLayer, bf16_bits,
+                                                       bf16_tensor, pinned_records)
+
+pytestmark = pytest.mark.gpu
+
+TOL_REL, TOL_ABS, P_TOL = 2e-3, 1e-4, 1e-5
+DEV = "cuda:0"
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def host(outs):
+    ob, of, ids, w = outs
+    torch.cuda.synchronize()
+    return bf16_bits(ob), of.cpu().numpy(), ids.cpu().numpy(), w.cpu().numpy()
+
+
+def assert_close(got, ref):
+    gb, gf, gi, gw = got
+    rb, rf, ri, rw = ref
+    assert np.array_equal(gi, ri)
+    assert np.abs(gw.astype(np.float64) - rw).max() <= P_TOL
+    for t in range(gf.shape[0]):
+        err = np.abs(gf[t].astype(np.float64) - rf[t]).max()
+        assert err <= TOL_REL * np.abs(rf[t].astype(np.float64)).max() + TOL_ABS
+    assert np.array_equal(gb, synth.float_to_bf16_bits(gf))
+
+
+def assert_oracle(got, t, ref_out, ref_ids, ref_p):
+    gb, gf, gi, gw = got
+    assert np.array_equal(gi[t], ref_ids)
+    assert np.abs(gw[t].astype(np.float64) - ref_p).max() <= P_TOL
+    err = np.abs(gf[t].astype(np.float64) - ref_out).max()
+    assert err <= TOL_REL * np.abs(ref_out).max() + TOL_ABS
+
+
+def make(shape, seed, beta, n_slots, max_tokens=4):
+    hl = HostLayer(shape, seed, beta=beta)
+    dl = DeviceLayer(shape, seed, beta=beta, max_tokens=max_tokens, device=DEV,
+                     host_records=hl.records, host_shared=hl.shared,
+                     router=(hl.router_codes, hl.router_sb))
+    cl = CachedLayer(dl, pinned_records(shape, seed, host_records=hl.records), n_slots)
+    return hl, dl, cl
+
+
+def first_appearance(ids):
+    seen, order = set(), []
+    for e in np.asarray(ids).reshape(-1):
+        if int(e) not in seen:
+            seen.add(int(e))
+            order.append(int(e))
+    return np.array(order, np.int32)
+
+
+def test_hand_trace_on_gpu():
+    rows = [l.split("|") for l in open(os.path.join(GOLDEN, "lfu_trace.txt"))
+            if l.strip() and not l.startswith("#")]
+    shape = synth.Shape(64, 6, 2, 64, 64)
+    hl, dl, cl = make(shape, 5, np.zeros(6, np.float32), 3, max_tokens=1)
+    x = bf16_tensor(synth.hidden(5, 0, 0, 64)[None], DEV)
+    prev = cl.stats()
+    for r in rows:
+        ids = [int(t) for t in r[1].split()]
+        hits = [int(t) for t in r[2].split()]
+        beta = np.zeros(6, np.float32)
+        beta[ids[0]], beta[ids[1]] = 200.0, 100.0
+        dl.beta.copy_(torch.from_numpy(beta))
+        got = host(cl.decode(x))
+        assert list(got[2][0]) == ids
+        assert cl.slots() == [int(t) for t in r[4].split()]
+        st = cl.stats()
+        assert st["hits"] - prev["hits"] == sum(hits)
+        assert st["misses"] - prev["misses"] == len(ids) - sum(hits)
+        prev = st
+        ref = host(dl.decode(x))
+        assert_close(got, ref)
+    assert dl.check() == moe.MOE_OK, moe.last_error()
+    assert prev["steps"] == len(rows)
+    assert prev["bytes_h2d"] == prev["misses"] * oracle.record_layout(64, 64)["bytes"]
+    cl.close()
+    dl.close()
+
+
+@pytest.mark.parametrize("B,steps,n_slots", [(1, 40, 8), (4, 16, 16)])
+def test_zipf_stream_matches_lfu_replay_and_oracle(B, steps, n_slots):
+    shape = synth.Shape(256, 64, 4, 128, 256)
+    beta = synth.beta_zipf(4, 0, 64)
+    hl, dl, cl = make(shape, 7, beta, n_slots, max_tokens=B)
+    orc = hl.oracle()
+    lfu = oracle.LFU(n_slots, 64)
+    prev = cl.stats()
+    for s in range(steps):
+        xs = np.stack([hidden_with_margin(orc, 9, s, t) for t in range(B)])
+        x = bf16_tensor(xs, DEV)
+        got = host(cl.decode(x))
+        hit, _, m = lfu.step(first_appearance(got[2]))
+        st = cl.stats()
+        assert st["misses"] - prev["misses"] == m
+        assert st["hits"] - prev["hits"] == int(hit.sum())
+        assert cl.slots() == list(lfu.slot_expert)
+        prev = st
+        assert_close(got, host(dl.decode(x)))
+        if s % 8 == 0 or s == steps - 1:
+            for t in range(B):
+                assert_oracle(got, t, *orc.token(xs[t]))
+    assert dl.check() == moe.MOE_OK, moe.last_error()
+    assert prev["evictions"] > 0 and prev["hits"] > 0
+    cl.close()
+    dl.close()
+
+
+def test_faults_are_caught_and_recovered():
+    shape = synth.Shape(256, 16, 2, 128, 256)
+    hl, dl, cl = make(shape, 3, None, 4, max_tokens=2)
+    orc = hl.oracle()
+    xs = [np.stack([hidden_with_margin(orc, 13, s, 0)]) for s in range(4)]
+    # a copy that fails: MOE_ERR_CUDA, its slot left empty, nothing counted twice
+    cl.set_fault(moe.MOE_RESIDENCY_FAULT_COPY)
+    with pytest.raises(moe.MoEError) as ei:
+        cl.decode(bf16_tensor(xs[0], DEV))
+    assert ei.value.code == moe.MOE_ERR_CUDA
+    torch.cuda.synchronize()
+    assert cl.slots().count(-1) >= 3
+    got = host(cl.decode(bf16_tensor(xs[0], DEV)))
+    assert dl.check() == moe.MOE_OK, moe.last_error()
+    assert_oracle(got, 0, *orc.token(xs[0][0]))
+    # a wrong slot tag: the kernels refuse the slot and latch MOE_ERR_RESIDENCY
+    cl.set_fault(moe.MOE_RESIDENCY_FAULT_TAG)
+    cl.decode(bf16_tensor(xs[1], DEV))
+    assert dl.check() == moe.MOE_ERR_RESIDENCY
+    got = host(cl.decode(bf16_tensor(xs[2], DEV)))
+    assert dl.check() == moe.MOE_OK, moe.last_error()
+    assert_oracle(got, 0, *orc.token(xs[2][0]))
+    cl.close()
+    # more distinct experts in a step than slots (2 slots, 2 tokens of top-2):
+    # refused, state unchanged
+    small = CachedLayer(dl, cl.host, 2)
+    host(small.decode(bf16_tensor(xs[3], DEV)))
+    before, slots = small.stats(), small.slots()
+    for s in range(8):
+        x2 = np.stack([hidden_with_margin(orc, 14, s, t) for t in range(2)])
+        ids = host(dl.decode(bf16_tensor(x2, DEV)))[2]
+        if len(set(ids.reshape(-1).tolist())) > 2:
+            break
+    else:
+        pytest.fail("no pair of tokens with more than 2 distinct experts")
+    with pytest.raises(moe.MoEError) as ei:
+        small.decode(bf16_tensor(x2, DEV))
+    assert ei.value.code == moe.MOE_ERR_RESIDENCY
+    torch.cuda.synchronize()
+    assert small.stats() == before and small.slots() == slots
+    small.close()
+    dl.close()
