@@ -246,6 +246,7 @@ static size_t carve(const moe_layer* L, int T, moe::Workspace* ws, uint8_t* base
     ws->w_stage = reinterpret_cast<float*>(base + o_w);
   }
   if (prefill_off) *prefill_off = o_pf;
+  if (ws && base) ws->pf = moe::prefill_workspace_bytes(a, T) ? base + o_pf : nullptr;
   return c.off;
 }
 

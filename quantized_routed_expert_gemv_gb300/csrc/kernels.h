@@ -50,6 +50,34 @@ struct Workspace {
   float* of_stage;       // [T][H] f32
   int32_t* ids_stage;    // [T][k]
   float* w_stage;        // [T][k]
+  uint8_t* pf;           // prefill chunk scratch (tensor-core path), or null
+};
+
+// One token block of the prefill path: up to 64 tokens of one expert (or of
+// the shared expert), padded to a multiple of 16 rows.
+struct PBlk {
+  int expert;  // routed expert id, -1 for the shared expert
+  int len;     // tokens in the block
+  int np;      // len rounded up to a multiple of 16
+  int xrow;    // first packed row of the block (activation blocks, group sums)
+  int tok0;    // first pair position (routed) or first token (shared)
+  int hoff;    // first element of the block's packed h (hi and lo arrays)
+  int entry;   // 0.. (shared expert first, then active experts ascending)
+  int pad;
+};
+
+// Prefill scratch carved from Workspace::pf (device pointers).
+struct PrefillPtrs {
+  int* hdr;          // [0] blocks, [1] shared-expert blocks
+  PBlk* blk;         // block table
+  uint16_t* xc;      // packed activations, core-matrix order, K permuted
+  float* sx;         // per block: [H/64 groups][np] sums of x over each group
+  uint16_t* hc_hi;   // packed SwiGLU outputs, bf16 high part
+  uint16_t* hc_lo;   // bf16 low part (h - hi)
+  float* sh;         // per block: [F/64 groups][np] sums of h over each group
+  float* y_pair;     // [T*k][H] routed expert outputs, grouped pair order
+  float* y_sh;       // [T][H] shared expert outputs
+  int* inv;          // [T*k] grouped pair position of (token, rank)
 };
 
 struct LayerArgs {
@@ -77,6 +105,7 @@ struct LayerArgs {
                                // 2 routed experts only
   int dn_rt, dn_tiles;         // down row tile and number of tiles (H / dn_rt)
   int dn_stage, dn_nst;        // down stage bytes and stage count
+  PrefillPtrs pf;              // prefill chunk scratch (tensor-core path)
   int prof_on;                 // record prof[] events between kernels, no PDL
   void* prof[4];               // cudaEvent_t: before router / gate|up / down, after down
 };

@@ -1,21 +1,708 @@
-// prefill.cu -- prefill chunk (T <= 128 tokens).
+// prefill.cu -- a prefill chunk (T <= 128 tokens) on the fifth-generation
+// tensor cores.
+//
+// TurboFieldfare page, section "Token üretim süreci": prompt prefill runs in
+// chunks of at most 128 tokens so that one fetched expert serves several
+// rows.  With up to 128 tokens per expert the expert FFN is a small dense
+// contraction: each expert's 4-bit weights are read from HBM once per chunk
+// and multiplied against all of its tokens on the tensor cores.
+//
+// Kernels, in stream order (T >= kPrefillTcMin and H, F, Fs multiples of 128;
+// other chunks run the decode kernels):
+//   router          decode.cu's router for T tokens: logits, top-k, weights,
+//                   grouping by expert.
+//   pf_pack_kernel  one CTA per entry (shared expert, then active experts):
+//                   splits the entry's tokens into blocks of <= 64, writes the
+//                   block table, the activations in the tensor core's
+//                   core-matrix order (see below) and their per-group sums.
+//   pf_gemm_kernel<0>  gate|up: items = (block, 64 gate rows + the same 64 up
+//                   rows); D = [W_g; W_u] x^T, then SwiGLU, h packed as bf16
+//                   hi + lo for the down GEMM.
+//   pf_gemm_kernel<1>  down: items = (block, 128 rows of H); y = W_d h.
+//   pf_combine_kernel  out = y_shared + sum_i p_i y_{e_i}, fixed order.
+//
+// Exact 4-bit weights on the tensor cores.  A weight is s*q + b (s, b bf16
+// per group of 64 along K, q in 0..15).  The A operand holds the code q
+// itself as bf16: four masks turn a 32-bit word of 8 codes into bf16 pairs
+// 128 + q (bits 0x4300 | q), and one exact bf16x2 FMA per pair removes the
+// 128.  Each group of 64 K-values accumulates into its own TMEM columns, and
+// the epilogue applies  s * D_g + b * X_g  with X_g the group sum of the
+// activations (fp32), so no weight is rounded.  The masks yield the codes of
+// a word in the order 0,4,1,5,2,6,3,7; the activations are packed in the
+// same order, so the contraction is unchanged.
+// The down GEMM's h is fp32; it is split into bf16 hi + lo (two MMAs into
+// the same accumulator), error about 2^-17 relative.
+//
+// Operand layout (no swizzle, K-major): core matrices of 8 rows x 16 bytes;
+// within a 128-K chunk, core (k8, r8) sits at (k8 * R8 + r8) * 128 bytes
+// (R8 = rows / 8).  The descriptor's leading offset is the K-direction core
+// stride (R8 * 128), its stride offset the 8-row stride (128).
+//
+// Warp roles of pf_gemm_kernel (16 warps, one CTA per SM, persistent over
+// items): warps 0-7 epilogue (TMEM lanes 32*(w%4).., column half w/4),
+// warps 8-13 dequantise codes into A, warp 14 streams codes (bulk copies,
+// 64 B per row per chunk), warp 15 allocates TMEM and issues the MMAs.
 #include <algorithm>
 
 #include "common.cuh"
 #include "kernels.h"
+#include "tcgen05.cuh"
 
 namespace moe {
 
 cudaError_t launch_decode(const LayerArgs& a, int num_sms, cudaStream_t st);
+cudaError_t launch_decode_router(const LayerArgs& a, int num_sms, cudaStream_t st);
 
-size_t prefill_workspace_bytes(const LayerArgs&, int) { return 0; }
+constexpr int kPrefillTcMin = 32;  // smaller chunks: the decode kernels
+constexpr unsigned kAllLanes = 0xFFFFFFFFu;
+constexpr int kBlkTokens = 64;     // tokens per block (N of the MMA <= 64)
 
-size_t prefill_smem_need(const LayerArgs&, int) { return 0; }
+__host__ __device__ inline int round16(int v) { return (v + 15) & ~15; }
+__host__ __device__ inline int blocks_of(int cnt) { return (cnt + kBlkTokens - 1) / kBlkTokens; }
+__host__ __device__ inline int rows_of(int cnt) {  // packed rows of an entry with cnt tokens
+  return (cnt / kBlkTokens) * kBlkTokens + round16(cnt % kBlkTokens);
+}
 
-cudaError_t set_prefill_attributes(int) { return cudaSuccess; }
+bool prefill_tc_ok(const LayerArgs& a, int T) {
+  return T >= kPrefillTcMin && T <= kMaxTokens && a.H % 128 == 0 && a.F % 128 == 0 && a.Fs % 128 == 0;
+}
 
-cudaError_t launch_prefill(const LayerArgs& a, int num_sms, cudaStream_t st) {
-  return launch_decode(a, num_sms, st);
+// ---------------------------------------------------------------------------
+// scratch layout
+// ---------------------------------------------------------------------------
+struct PfLayout {
+  size_t hdr, blk, xc, sx, hc_hi, hc_lo, sh, y_pair, y_sh, inv, total;
+  int rows_cap, blk_cap;
+};
+
+static PfLayout pf_layout(const LayerArgs& a, int T) {
+  PfLayout L{};
+  const size_t H = a.H, k = a.k, Fm = std::max(a.F, a.Fs);
+  const int pairs = T * a.k, has_sh = a.Fs > 0;
+  const int nact = std::min(a.E, pairs);
+  L.rows_cap = (has_sh ? rows_of(T) : 0) + pairs + 15 * nact;
+  L.blk_cap = (has_sh ? blocks_of(T) : 0) + nact + pairs / kBlkTokens + 1;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += (bytes + 255) / 256 * 256;
+    return o;
+  };
+  const size_t rows = L.rows_cap;
+  L.hdr = take(256);
+  L.blk = take(static_cast<size_t>(L.blk_cap) * sizeof(PBlk));
+  L.xc = take(rows * H * 2);
+  L.sx = take(rows * (H / 64) * 4);
+  L.hc_hi = take(rows * Fm * 2);
+  L.hc_lo = take(rows * Fm * 2);
+  L.sh = take(rows * (Fm / 64) * 4);
+  L.y_pair = take(static_cast<size_t>(pairs) * H * 4);
+  L.y_sh = take(has_sh ? static_cast<size_t>(T) * H * 4 : 0);
+  L.inv = take(static_cast<size_t>(pairs) * 4);
+  (void)k;
+  L.total = off;
+  return L;
+}
+
+size_t prefill_workspace_bytes(const LayerArgs& a, int T) {
+  return prefill_tc_ok(a, T) ? pf_layout(a, T).total : 0;
+}
+
+// ---------------------------------------------------------------------------
+// pack: block table, activations in core-matrix order, group sums
+// ---------------------------------------------------------------------------
+constexpr int kPackThreads = 256;
+
+__device__ __forceinline__ int clamp_nact(const LayerArgs& a) {
+  const int n = *reinterpret_cast<volatile int*>(a.ws.n_act);
+  return n < 0 ? 0 : (n > a.E ? a.E : n);
+}
+
+__device__ __forceinline__ int entry_cnt(const LayerArgs& a, int i, int has_sh) {
+  if (has_sh && i == 0) return a.T;
+  const int c = a.ws.act_cnt[i - has_sh];
+  return c < 0 ? 0 : (c > a.T ? a.T : c);
+}
+
+__global__ void __launch_bounds__(kPackThreads) pf_pack_kernel(const __grid_constant__ LayerArgs a) {
+  const int has_sh = a.Fs > 0 ? 1 : 0;
+  const int n_ent = has_sh + clamp_nact(a);
+  const int j = blockIdx.x;
+  if (j >= n_ent) return;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, H = a.H;
+  const bool shared = has_sh && j == 0;
+  const int Fj = shared ? a.Fs : a.F;
+
+  // prefix over the entries before j: blocks, packed rows, packed h elements
+  __shared__ long long s_red[3][kPackThreads / 32];
+  long long nb = 0, rows = 0, helem = 0;
+  for (int i = tid; i < j; i += kPackThreads) {
+    const int c = entry_cnt(a, i, has_sh);
+    nb += blocks_of(c);
+    rows += rows_of(c);
+    helem += static_cast<long long>(rows_of(c)) * ((has_sh && i == 0) ? a.Fs : a.F);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    nb += __shfl_xor_sync(kAllLanes, nb, o);
+    rows += __shfl_xor_sync(kAllLanes, rows, o);
+    helem += __shfl_xor_sync(kAllLanes, helem, o);
+  }
+  if (lane == 0) s_red[0][warp] = nb, s_red[1][warp] = rows, s_red[2][warp] = helem;
+  __syncthreads();
+  long long nb0 = 0, row0 = 0, h0 = 0;
+  for (int w = 0; w < kPackThreads / 32; ++w) nb0 += s_red[0][w], row0 += s_red[1][w], h0 += s_red[2][w];
+
+  const int cnt = entry_cnt(a, j, has_sh);
+  const int nbj = blocks_of(cnt);
+  const int expert = shared ? -1 : a.ws.act_expert[j - has_sh];
+  const int pair0 = shared ? 0 : a.ws.act_off[j - has_sh];
+  if (tid < nbj) {
+    const int b = tid;
+    PBlk p;
+    p.expert = expert;
+    p.len = min(kBlkTokens, cnt - b * kBlkTokens);
+    p.np = round16(p.len);
+    p.xrow = static_cast<int>(row0) + b * kBlkTokens;
+    p.tok0 = pair0 + b * kBlkTokens;
+    p.hoff = static_cast<int>(h0) + b * kBlkTokens * Fj;
+    p.entry = j;
+    p.pad = 0;
+    a.pf.blk[nb0 + b] = p;
+  }
+  if (j == n_ent - 1 && tid == 0) {
+    a.pf.hdr[0] = static_cast<int>(nb0) + nbj;
+    a.pf.hdr[1] = has_sh ? blocks_of(a.T) : 0;
+  }
+  if (!shared)
+    for (int n = tid; n < cnt; n += kPackThreads) {
+      const int p = pair0 + n;
+      const int slot = a.ws.pair_slot[p];
+      if (slot >= 0 && slot < a.T * a.k) a.pf.inv[slot] = p;
+    }
+
+  // packed rows: one warp per row; a lane handles 8 consecutive K values
+  const int nrows = rows_of(cnt), units = H / 8;
+  for (int n = warp; n < nrows; n += kPackThreads / 32) {
+    const int b = n / kBlkTokens, nn = n % kBlkTokens;
+    const int len = min(kBlkTokens, cnt - b * kBlkTokens), np = round16(len);
+    const int xrow = static_cast<int>(row0) + b * kBlkTokens;
+    int tok = -1;
+    if (nn < len) tok = shared ? b * kBlkTokens + nn : a.ws.pair_token[pair0 + b * kBlkTokens + nn];
+    if (tok < 0 || tok >= a.T) tok = -1;
+    uint16_t* xb = a.pf.xc + static_cast<size_t>(xrow) * H;
+    float* sxb = a.pf.sx + static_cast<size_t>(xrow) * (H / 64);
+    for (int u0 = 0; u0 < units; u0 += 32) {
+      const int u = u0 + lane;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      float s = 0.f;
+      if (u < units && tok >= 0) {
+        v = __ldg(reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(tok) * H) + u);
+        s = bf16lo(v.x) + bf16hi(v.x) + bf16lo(v.y) + bf16hi(v.y) + bf16lo(v.z) + bf16hi(v.z) + bf16lo(v.w) +
+            bf16hi(v.w);
+      }
+      // group sum over the 8 lanes (64 values) of this lane's group
+      s += __shfl_xor_sync(kAllLanes, s, 1);
+      s += __shfl_xor_sync(kAllLanes, s, 2);
+      s += __shfl_xor_sync(kAllLanes, s, 4);
+      if (u < units) {
+        // K order inside the core row: 0,4,1,5,2,6,3,7
+        uint4 w;
+        w.x = __byte_perm(v.x, v.z, 0x5410);
+        w.y = __byte_perm(v.x, v.z, 0x7632);
+        w.z = __byte_perm(v.y, v.w, 0x5410);
+        w.w = __byte_perm(v.y, v.w, 0x7632);
+        const int c = u >> 4, k8 = u & 15;
+        const size_t e = static_cast<size_t>(c) * np * 128 + (k8 * (np >> 3) + (nn >> 3)) * 64 + (nn & 7) * 8;
+        *reinterpret_cast<uint4*>(xb + e) = w;
+        if ((lane & 7) == 0) sxb[(u >> 3) * np + nn] = s;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// grouped GEMM on the tensor cores
+// ---------------------------------------------------------------------------
+constexpr int kPgThreads = 512;
+constexpr int kEpiWarps = 8, kDqWarps = 6, kProdWarp = 14, kMmaWarp = 15;
+constexpr int kNSC = 8;                  // code stages
+constexpr int kNSA = 2;                  // A / B stages
+constexpr int kCodesStage = 128 * 64;    // 128 rows x 64 B (128 codes)
+constexpr int kAStage = 128 * 128 * 2;   // 128 rows x 128 bf16
+constexpr int kTmemCols = 256;           // 2 buffers x 2 groups x 64 columns
+constexpr int kXPitch = 65;              // floats per row of the SwiGLU exchange (no bank conflicts)
+
+struct PgSmem {
+  int codes, a, b, xchg, bars, total, bstage;
+};
+
+__host__ __device__ inline PgSmem pg_smem(int mode) {
+  PgSmem L;
+  int off = 0;
+  L.codes = off;
+  off += kNSC * kCodesStage;
+  L.a = off;
+  off += kNSA * kAStage;
+  L.bstage = kBlkTokens * 256 * (mode == 1 ? 2 : 1);
+  L.b = off;
+  off += kNSA * L.bstage;
+  L.xchg = off;
+  off += mode == 0 ? 64 * kXPitch * 4 : 0;
+  L.bars = off;
+  off += 256;
+  L.total = off;
+  return L;
+}
+
+struct PgItem {
+  PBlk blk;
+  int tile, K, nch;
+  const uint8_t* rec;
+  const RecordOffsets* off;
+  int Fe;
+};
+
+template <int MODE>
+__device__ __forceinline__ bool pg_item(const LayerArgs& a, int it, int nblk, int nsb, PgItem& I) {
+  const int has_sh = a.Fs > 0 ? 1 : 0;
+  int b, tile;
+  if (MODE == 0) {
+    const int Ts = a.Fs / 64, Tr = a.F / 64;
+    if (it < nsb * Ts) b = it / Ts, tile = it % Ts;
+    else b = nsb + (it - nsb * Ts) / Tr, tile = (it - nsb * Ts) % Tr;
+  } else {
+    const int Th = a.H / 128;
+    b = it / Th, tile = it % Th;
+  }
+  if (b >= nblk) return false;
+  I.blk = a.pf.blk[b];
+  I.tile = tile;
+  const bool shared = has_sh && I.blk.expert < 0;
+  I.Fe = shared ? a.Fs : a.F;
+  I.K = MODE == 0 ? a.H : I.Fe;
+  I.nch = I.K / 128;
+  if (shared) {
+    I.rec = a.shared, I.off = &a.off_s;
+  } else {
+    int e = I.blk.expert;
+    if (e < 0 || e >= a.E) e = 0;
+    I.rec = a.records + static_cast<size_t>(e) * a.off_r.stride;
+    I.off = &a.off_r;
+  }
+  int np = I.blk.np;
+  I.blk.np = np < 16 ? 16 : (np > kBlkTokens ? kBlkTokens : np);
+  return true;
+}
+
+// Waits for a phase; gives up (and tells every other role through `abort`)
+// after the bounded limit or when another role already gave up.
+__device__ __forceinline__ bool pg_wait(uint64_t* bar, uint32_t parity, volatile int* abort, unsigned* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_timer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63u) == 0) {
+      if (*abort) return false;
+      if (global_timer_ns() - t0 > kWaitLimitNs) {
+        *abort = 1;
+        latch_error(err, kErrTimeout);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ bool pg_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort, unsigned* err) {
+  return __all_sync(kAllLanes, pg_wait(bar, parity, abort, err)) != 0;
+}
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
+
+// Two bf16 lanes holding 128 + q (bits 0x4300 | q) -> q, exactly:
+// (128 + q) * 1 - 128 needs no rounding.
+__device__ __forceinline__ uint32_t codes_bf16x2(uint32_t v) {
+  uint32_t r;
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(v), "r"(0x3F803F80u), "r"(0xC300C300u));
+  return r;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kPgThreads, 1) pf_gemm_kernel(const __grid_constant__ LayerArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const PgSmem L = pg_smem(MODE);
+  uint8_t* s_codes = smem + L.codes;
+  uint8_t* s_a = smem + L.a;
+  uint8_t* s_b = smem + L.b;
+  float* s_x = reinterpret_cast<float*>(smem + L.xchg);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
+  uint64_t* codes_full = bars;
+  uint64_t* codes_empty = codes_full + kNSC;
+  uint64_t* a_full = codes_empty + kNSC;
+  uint64_t* a_empty = a_full + kNSA;
+  uint64_t* b_full = a_empty + kNSA;
+  uint64_t* tm_full = b_full + kNSA;
+  uint64_t* tm_empty = tm_full + 2;
+  uint32_t* s_taddr = reinterpret_cast<uint32_t*>(tm_empty + 2);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(s_taddr + 1);
+  unsigned* err = &a.ws.ctl[0];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    for (int i = 0; i < kNSC; ++i) mbar_init(&codes_full[i], 1), mbar_init(&codes_empty[i], kDqWarps);
+    for (int i = 0; i < kNSA; ++i) mbar_init(&a_full[i], kDqWarps), mbar_init(&a_empty[i], 1), mbar_init(&b_full[i], 1);
+    for (int i = 0; i < 2; ++i) mbar_init(&tm_full[i], 1), mbar_init(&tm_empty[i], kEpiWarps);
+    *s_abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == kMmaWarp) tmem_alloc(smem_u32(s_taddr), kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t taddr = *s_taddr;
+
+  int nblk = a.pf.hdr[0], nsb = a.pf.hdr[1];
+  nblk = max(0, nblk);
+  nsb = min(max(0, nsb), nblk);
+  const int H = a.H;
+  const int n_items = MODE == 0 ? nsb * (a.Fs / 64) + (nblk - nsb) * (a.F / 64) : nblk * (H / 128);
+
+  if (warp == kProdWarp) {
+    // ------------------------------------------------------------ codes
+    const uint64_t pol = policy_evict_first();
+    RingPos pc;
+    int issued = 0;
+    bool stop = false;
+    for (int it = blockIdx.x; it < n_items && !stop; it += gridDim.x) {
+      PgItem I;
+      if (!pg_item<MODE>(a, it, nblk, nsb, I)) break;
+      for (int c = 0; c < I.nch; ++c, pc.next(kNSC)) {
+        if (issued >= kNSC && !pg_wait_warp(&codes_empty[pc.s], pc.ph ^ 1u, s_abort, err)) {
+          stop = true;
+          break;
+        }
+        if (lane == 0) mbar_arrive_expect_tx(&codes_full[pc.s], kCodesStage);
+        __syncwarp();
+        uint8_t* dst = s_codes + pc.s * kCodesStage;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int r = lane * 4 + i;
+          const uint8_t* src;
+          if (MODE == 0)
+            src = I.rec + (r < 64 ? I.off->gate_codes : I.off->up_codes) +
+                  static_cast<size_t>(I.tile * 64 + (r & 63)) * (H / 2) + c * 64;
+          else
+            src = I.rec + I.off->down_codes + static_cast<size_t>(I.tile * 128 + r) * (I.Fe / 2) + c * 64;
+          bulk_g2s(dst + r * 64, src, 64, &codes_full[pc.s], pol);
+        }
+        ++issued;
+      }
+    }
+    // copies in flight land before the CTA leaves
+    for (int j = max(0, issued - kNSC); j < issued; ++j)
+      if (!mbar_wait(&codes_full[j % kNSC], (j / kNSC) & 1)) latch_error(err, kErrTimeout);
+  } else if (warp >= kEpiWarps && warp < kEpiWarps + kDqWarps) {
+    // ------------------------------------------------------------ dequantise
+    const int dw = warp - kEpiWarps, t = dw * 32 + lane;
+    RingPos pc, pa;
+    int cc = 0, b_issued = 0;
+    for (int it = blockIdx.x; it < n_items && !*s_abort; it += gridDim.x) {
+      PgItem I;
+      if (!pg_item<MODE>(a, it, nblk, nsb, I)) break;
+      const int np = I.blk.np;
+      bool stop = false;
+      for (int c = 0; c < I.nch; ++c, ++cc, pc.next(kNSC), pa.next(kNSA)) {
+        if (cc >= kNSA && !pg_wait_warp(&a_empty[pa.s], pa.ph ^ 1u, s_abort, err)) {
+          stop = true;
+          break;
+        }
+        if (dw == 0 && lane == 0) {  // this chunk's B operand
+          uint8_t* bdst = s_b + pa.s * L.bstage;
+          const uint32_t part = np * 256;
+          if (MODE == 0) {
+            mbar_arrive_expect_tx(&b_full[pa.s], part);
+            bulk_g2s(bdst, a.pf.xc + static_cast<size_t>(I.blk.xrow) * H + static_cast<size_t>(c) * np * 128, part,
+                     &b_full[pa.s]);
+          } else {
+            const size_t e = static_cast<size_t>(I.blk.hoff) + static_cast<size_t>(c) * np * 128;
+            mbar_arrive_expect_tx(&b_full[pa.s], 2 * part);
+            bulk_g2s(bdst, a.pf.hc_hi + e, part, &b_full[pa.s]);
+            bulk_g2s(bdst + part, a.pf.hc_lo + e, part, &b_full[pa.s]);
+          }
+          ++b_issued;
+        }
+        if (!pg_wait_warp(&codes_full[pc.s], pc.ph, s_abort, err)) {
+          stop = true;
+          break;
+        }
+        const uint8_t* src = s_codes + pc.s * kCodesStage;
+        uint8_t* dst = s_a + pa.s * kAStage;
+        for (int u = t; u < 512; u += kDqWarps * 32) {
+          const int r = u >> 2, c4 = u & 3;
+          const uint4 q = *reinterpret_cast<const uint4*>(src + r * 64 + c4 * 16);
+          const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            const uint32_t v = w4[w];
+            uint4 o;
+            o.x = codes_bf16x2((v & 0x000F000Fu) | 0x43004300u);
+            o.y = codes_bf16x2(((v >> 4) & 0x000F000Fu) | 0x43004300u);
+            o.z = codes_bf16x2(((v >> 8) & 0x000F000Fu) | 0x43004300u);
+            o.w = codes_bf16x2(((v >> 12) & 0x000F000Fu) | 0x43004300u);
+            const int k8 = c4 * 4 + w;
+            *reinterpret_cast<uint4*>(dst + (k8 * 16 + (r >> 3)) * 128 + (r & 7) * 16) = o;
+          }
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&a_full[pa.s]);
+          mbar_arrive(&codes_empty[pc.s]);
+        }
+      }
+      if (stop) break;
+    }
+    if (dw == 0 && lane == 0)
+      for (int j = max(0, b_issued - kNSA); j < b_issued; ++j)
+        if (!mbar_wait(&b_full[j % kNSA], (j / kNSA) & 1)) latch_error(err, kErrTimeout);
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issue
+    if (lane == 0) {
+      RingPos pa, pt;
+      int cc = 0;
+      bool stop = false;
+      for (int it = blockIdx.x; it < n_items && !stop; it += gridDim.x) {
+        PgItem I;
+        if (!pg_item<MODE>(a, it, nblk, nsb, I)) break;
+        const int np = I.blk.np;
+        const uint32_t idesc = idesc_bf16_f32(128, np);
+        for (int c = 0; c < I.nch; ++c, ++cc, pa.next(kNSA), pt.next(2)) {
+          if (!pg_wait(&a_full[pa.s], pa.ph, s_abort, err) || !pg_wait(&b_full[pa.s], pa.ph, s_abort, err) ||
+              (cc >= 2 && !pg_wait(&tm_empty[pt.s], pt.ph ^ 1u, s_abort, err))) {
+            stop = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(s_a + pa.s * kAStage), b0 = smem_u32(s_b + pa.s * L.bstage);
+#pragma unroll
+          for (int gi = 0; gi < 2; ++gi) {
+            const uint32_t d = taddr + pt.s * 128 + gi * 64;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const int kq = gi * 4 + kk;
+              const uint64_t ad = smem_desc(a0 + kq * 4096, 2048, 128);
+              mma_bf16(d, ad, smem_desc(b0 + kq * np * 32, np * 16, 128), idesc, kk > 0 ? 1u : 0u);
+              if (MODE == 1) mma_bf16(d, ad, smem_desc(b0 + np * 256 + kq * np * 32, np * 16, 128), idesc, 1u);
+            }
+          }
+          mma_commit(smem_u32(&a_empty[pa.s]));
+          mma_commit(smem_u32(&tm_full[pt.s]));
+        }
+      }
+      // the last commits have landed before TMEM is released
+      if (cc > 0 && !mbar_wait(&tm_full[(cc - 1) & 1], ((cc - 1) >> 1) & 1)) latch_error(err, kErrTimeout);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3, hh = warp >> 2;
+    const int row = q * 32 + lane;  // TMEM lane = A row of the item
+    RingPos pt;
+    bool stop = false;
+    for (int it = blockIdx.x; it < n_items && !stop; it += gridDim.x) {
+      PgItem I;
+      if (!pg_item<MODE>(a, it, nblk, nsb, I)) break;
+      const int np = I.blk.np, half = np >> 1;
+      const int G = I.K / 64;
+      // this row's scale/bias words and the block's group sums
+      const uint32_t* sbrow;
+      const float* gsum;
+      if (MODE == 0) {
+        const uint64_t o = row < 64 ? I.off->gate_sb : I.off->up_sb;
+        sbrow = reinterpret_cast<const uint32_t*>(I.rec + o) + static_cast<size_t>(I.tile * 64 + (row & 63)) * G;
+        gsum = a.pf.sx + static_cast<size_t>(I.blk.xrow) * G;
+      } else {
+        sbrow = reinterpret_cast<const uint32_t*>(I.rec + I.off->down_sb) + static_cast<size_t>(I.tile * 128 + row) * G;
+        gsum = a.pf.sh + I.blk.hoff / 64;
+      }
+      float acc[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) acc[j] = 0.f;
+      for (int c = 0; c < I.nch; ++c, pt.next(2)) {
+        uint32_t sbw[2];
+        sbw[0] = __ldg(sbrow + 2 * c);
+        sbw[1] = __ldg(sbrow + 2 * c + 1);
+        // the 8 epilogue warps decide together, so the barriers below stay uniform
+        const bool ok = pg_wait_warp(&tm_full[pt.s], pt.ph, s_abort, err);
+        if (named_bar_or(2, kEpiWarps * 32, !ok)) {
+          stop = true;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int gi = 0; gi < 2; ++gi) {
+          uint32_t d[32];
+          const uint32_t base = taddr + (static_cast<uint32_t>(q * 32) << 16) + pt.s * 128 + gi * 64 + hh * half;
+#pragma unroll
+          for (int p = 0; p < 4; ++p)
+            if (p * 8 < half) {
+              uint32_t r8[8];
+              tmem_ld8(base + p * 8, r8);
+#pragma unroll
+              for (int j = 0; j < 8; ++j) d[p * 8 + j] = r8[j];
+            }
+          tmem_wait();
+          const float s = bf16lo(sbw[gi]), b = bf16hi(sbw[gi]);
+          const float* gs = gsum + (2 * c + gi) * np + hh * half;
+#pragma unroll
+          for (int p = 0; p < 4; ++p)
+            if (p * 8 < half) {
+              const float4 x0 = *reinterpret_cast<const float4*>(gs + p * 8);
+              const float4 x1 = *reinterpret_cast<const float4*>(gs + p * 8 + 4);
+              const float xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                acc[p * 8 + j] = fmaf(s, __uint_as_float(d[p * 8 + j]), fmaf(b, xs[j], acc[p * 8 + j]));
+            }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tm_empty[pt.s]);
+      }
+      if (stop) break;
+      if (MODE == 0) {
+        // SwiGLU: up rows (64..127) hand their values to the gate rows
+        if (q >= 2) {
+          float* xr = s_x + ((q - 2) * 32 + lane) * kXPitch + hh * half;
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j < half) xr[j] = acc[j];
+        }
+        named_bar(1, kEpiWarps * 32);
+        if (q < 2) {
+          const int f = I.tile * 64 + row;  // row of h (F index)
+          const int cf = f >> 7, k8 = (f & 127) >> 3, pos = ((f & 7) >> 2) | ((f & 3) << 1);
+          float* xr = s_x + row * kXPitch + hh * half;
+          const size_t e0 = static_cast<size_t>(I.blk.hoff) + static_cast<size_t>(cf) * np * 128 + k8 * (np >> 3) * 64 + pos;
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j < half) {
+              const int n = hh * half + j;
+              const float h = silu_f(acc[j]) * xr[j];
+              xr[j] = h;
+              const uint16_t hi = f32_to_bf16_rne(h);
+              const uint16_t lo = f32_to_bf16_rne(h - __uint_as_float(static_cast<uint32_t>(hi) << 16));
+              const size_t e = e0 + (n >> 3) * 64 + (n & 7) * 8;
+              a.pf.hc_hi[e] = hi;
+              a.pf.hc_lo[e] = lo;
+            }
+        }
+        named_bar(1, kEpiWarps * 32);
+        // group sums of h over the tile's 64 rows (one group of the down GEMM)
+        if (tid < np) {
+          float sum = 0.f;
+          for (int r = 0; r < 64; ++r) sum += s_x[r * kXPitch + tid];
+          a.pf.sh[I.blk.hoff / 64 + I.tile * np + tid] = sum;
+        }
+        named_bar(1, kEpiWarps * 32);
+      } else {
+        const int r = I.tile * 128 + row;
+        const bool shared = a.Fs > 0 && I.blk.expert < 0;
+        float* y = shared ? a.pf.y_sh : a.pf.y_pair;
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (j < half) {
+            const int n = hh * half + j;
+            if (n < I.blk.len) y[static_cast<size_t>(I.blk.tok0 + n) * H + r] = acc[j];
+          }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(taddr, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// combine: out = y_shared + sum_i p_i y_{e_i}
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) pf_combine_kernel(const __grid_constant__ LayerArgs a) {
+  const int t = blockIdx.x, H = a.H, k = a.k;
+  const bool has_sh = a.Fs > 0;
+  for (int r4 = threadIdx.x; r4 < H / 4; r4 += blockDim.x) {
+    float4 acc = has_sh ? reinterpret_cast<const float4*>(a.pf.y_sh + static_cast<size_t>(t) * H)[r4]
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i = 0; i < k; ++i) {
+      int p = a.pf.inv[t * k + i];
+      if (p < 0 || p >= a.T * k) p = 0;
+      const float w = a.weights[t * k + i];
+      const float4 y = reinterpret_cast<const float4*>(a.pf.y_pair + static_cast<size_t>(p) * H)[r4];
+      acc.x = fmaf(w, y.x, acc.x), acc.y = fmaf(w, y.y, acc.y);
+      acc.z = fmaf(w, y.z, acc.z), acc.w = fmaf(w, y.w, acc.w);
+    }
+    const size_t o = static_cast<size_t>(t) * H + r4 * 4;
+    if (a.out_f32) *reinterpret_cast<float4*>(a.out_f32 + o) = acc;
+    uint2 b;
+    b.x = static_cast<uint32_t>(f32_to_bf16_rne(acc.x)) | (static_cast<uint32_t>(f32_to_bf16_rne(acc.y)) << 16);
+    b.y = static_cast<uint32_t>(f32_to_bf16_rne(acc.z)) | (static_cast<uint32_t>(f32_to_bf16_rne(acc.w)) << 16);
+    *reinterpret_cast<uint2*>(a.out_bf16 + o) = b;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host
+// ---------------------------------------------------------------------------
+size_t prefill_smem_need(const LayerArgs&, int) { return pg_smem(1).total; }
+
+cudaError_t set_prefill_attributes(int smem_optin) {
+  const void* fns[] = {(const void*)pf_gemm_kernel<0>, (const void*)pf_gemm_kernel<1>};
+  for (const void* f : fns) {
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, f);
+    if (e) return e;
+    if ((e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  smem_optin - static_cast<int>(fa.sharedSizeBytes))))
+      return e;
+  }
+  return cudaSuccess;
+}
+
+static cudaError_t markp(const LayerArgs& a, int i, cudaStream_t st) {
+  return a.prof_on ? cudaEventRecord(static_cast<cudaEvent_t>(a.prof[i]), st) : cudaSuccess;
+}
+
+cudaError_t launch_prefill(const LayerArgs& in, int num_sms, cudaStream_t st) {
+  if (!prefill_tc_ok(in, in.T) || !in.ws.pf) return launch_decode(in, num_sms, st);
+  LayerArgs a = in;
+  const PfLayout L = pf_layout(a, a.T);
+  uint8_t* base = a.ws.pf;
+  a.pf.hdr = reinterpret_cast<int*>(base + L.hdr);
+  a.pf.blk = reinterpret_cast<PBlk*>(base + L.blk);
+  a.pf.xc = reinterpret_cast<uint16_t*>(base + L.xc);
+  a.pf.sx = reinterpret_cast<float*>(base + L.sx);
+  a.pf.hc_hi = reinterpret_cast<uint16_t*>(base + L.hc_hi);
+  a.pf.hc_lo = reinterpret_cast<uint16_t*>(base + L.hc_lo);
+  a.pf.sh = reinterpret_cast<float*>(base + L.sh);
+  a.pf.y_pair = reinterpret_cast<float*>(base + L.y_pair);
+  a.pf.y_sh = reinterpret_cast<float*>(base + L.y_sh);
+  a.pf.inv = reinterpret_cast<int*>(base + L.inv);
+  cudaError_t e;
+  if ((e = markp(a, 0, st))) return e;
+  if ((e = launch_decode_router(a, num_sms, st))) return e;
+  pf_pack_kernel<<<a.E + (a.Fs > 0 ? 1 : 0), kPackThreads, 0, st>>>(a);
+  if ((e = cudaGetLastError())) return e;
+  if ((e = markp(a, 1, st))) return e;
+  pf_gemm_kernel<0><<<num_sms, kPgThreads, pg_smem(0).total, st>>>(a);
+  if ((e = cudaGetLastError())) return e;
+  if ((e = markp(a, 2, st))) return e;
+  pf_gemm_kernel<1><<<num_sms, kPgThreads, pg_smem(1).total, st>>>(a);
+  if ((e = cudaGetLastError())) return e;
+  pf_combine_kernel<<<a.T, 256, 0, st>>>(a);
+  if ((e = cudaGetLastError())) return e;
+  return markp(a, 3, st);
 }
 
 }  // namespace moe

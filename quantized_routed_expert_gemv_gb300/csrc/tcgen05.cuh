@@ -1,0 +1,77 @@
+// tcgen05.cuh -- fifth-generation tensor-core primitives (sm_100 family):
+// tensor-memory allocation, shared-memory matrix descriptors, the MMA
+// instruction descriptor for bf16 inputs with fp32 accumulation, commit to
+// an mbarrier, and tensor-memory loads.  Inline PTX only.
+#pragma once
+
+#include <cstdint>
+
+namespace moe {
+
+// ---- tensor memory (TMEM) ---------------------------------------------------
+// One warp allocates `ncols` (a power of two >= 32) columns of the SM's
+// tensor memory; the base address is written to shared memory at `slot`.
+__device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem), "r"(ncols));
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::);
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols));
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Makes this thread's generic-proxy shared-memory writes visible to the
+// tensor core's (async proxy) reads.
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// ---- descriptors --------------------------------------------------------------
+// Shared-memory matrix descriptor, no swizzle, K-major operand made of "core
+// matrices" of 8 rows x 16 bytes (128 contiguous bytes, row i at +16 i).
+//   lbo: byte distance between core matrices adjacent along K
+//   sbo: byte distance between core matrices adjacent along M (or N)
+// Bits: start address >> 4 in [0,14), lbo >> 4 in [16,30), sbo >> 4 in
+// [32,46), descriptor version 1 in [46,48), base offset 0, swizzle 0.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= 1ull << 46;
+  return d;
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, both
+// K-major, N in [16, 256] multiple of 16 and M = 128 for one CTA.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
+
+// The mbarrier at `bar_smem` receives one arrival when every tcgen05
+// operation this thread issued so far has completed.
+__device__ __forceinline__ void mma_commit(uint32_t bar_smem) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar_smem)
+               : "memory");
+}
+
+// Eight consecutive 32-bit columns of this warp's 32 TMEM lanes (lane i of
+// the warp reads TMEM lane (taddr >> 16) + i).  Asynchronous until tmem_wait.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+}  // namespace moe
