@@ -13,6 +13,7 @@
 
 #include "../../include/moe.h"
 #include "kernels.h"
+#include "tma.cuh"
 
 namespace moe {
 size_t decode_smem_need(const LayerArgs& a, int num_sms);
@@ -23,7 +24,8 @@ bool plan_b1(LayerArgs& a, int num_sms, int smem_optin);
 cudaError_t launch_decode_b1(const LayerArgs& a, int num_sms, cudaStream_t st);
 cudaError_t launch_decode(const LayerArgs& a, int num_sms, cudaStream_t st);
 cudaError_t set_prefill_attributes(int smem_optin);
-cudaError_t launch_prefill(const LayerArgs& a, int num_sms, cudaStream_t st);
+cudaError_t launch_prefill(const LayerArgs& a, const LayerMaps* maps, int num_sms, cudaStream_t st);
+cudaError_t build_layer_maps(const LayerArgs& a, LayerMaps* out);
 size_t prefill_workspace_bytes(const LayerArgs& a, int T);
 }  // namespace moe
 
@@ -54,6 +56,7 @@ struct moe_layer {
   int device, num_sms, smem_optin;
   cudaEvent_t prof[4];
   int prof_on;
+  moe::LayerMaps maps;  // tiled-load descriptors of the code matrices (prefill)
 };
 
 static bool aligned(const void* p, size_t a) {
@@ -181,6 +184,10 @@ extern "C" int moe_open(const moe_layer_desc* desc, const moe_layer_weights* w, 
     delete L;
     return cuda_fail(e, "moe_open: cudaFuncSetAttribute");
   }
+  if ((e = moe::build_layer_maps(a, &L->maps))) {
+    delete L;
+    return cuda_fail(e, "moe_open: tensor maps of the code matrices");
+  }
   *out = L;
   return MOE_OK;
 }
@@ -300,7 +307,7 @@ static int run(moe_layer* L, const uint16_t* x, int32_t T, uint16_t* ob, float* 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (path == Path::kPrefill)
-    e = moe::launch_prefill(a, L->num_sms, st);
+    e = moe::launch_prefill(a, &L->maps, L->num_sms, st);
   else if (T == 1 && moe::plan_b1(a, L->num_sms, L->smem_optin))
     e = moe::launch_decode_b1(a, L->num_sms, st);
   else

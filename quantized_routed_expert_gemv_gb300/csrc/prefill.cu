@@ -40,13 +40,15 @@
 //
 // Warp roles of pf_gemm_kernel (16 warps, one CTA per SM, persistent over
 // items): warps 0-7 epilogue (TMEM lanes 32*(w%4).., column half w/4),
-// warps 8-13 dequantise codes into A, warp 14 streams codes (bulk copies,
-// 64 B per row per chunk), warp 15 allocates TMEM and issues the MMAs.
+// warps 8-11 dequantise codes into A (warp 12 idles), warp 13 streams the activation (B)
+// chunks, warp 14 streams codes (tiled TMA loads) and group sums, warp 15
+// allocates TMEM and issues the MMAs.
 #include <algorithm>
 
 #include "common.cuh"
 #include "kernels.h"
 #include "tcgen05.cuh"
+#include "tma.cuh"
 
 namespace moe {
 
@@ -225,32 +227,45 @@ __global__ void __launch_bounds__(kPackThreads) pf_pack_kernel(const __grid_cons
 // grouped GEMM on the tensor cores
 // ---------------------------------------------------------------------------
 constexpr int kPgThreads = 512;
-constexpr int kEpiWarps = 8, kDqWarps = 6, kProdWarp = 14, kMmaWarp = 15;
-constexpr int kNSC = 8;                  // code stages
+constexpr int kEpiWarps = 8, kDqWarps = 4, kBWarp = 13, kProdWarp = 14, kMmaWarp = 15;
+constexpr int kDqWarp0 = kEpiWarps;  // dequantise warps: kDqWarp0 .. kDqWarp0 + kDqWarps - 1; warp 12 idles
+static_assert(kEpiWarps == 8, "the epilogue's named barriers count 8 warps (256 threads)");
+static_assert(kDqWarp0 + kDqWarps <= kBWarp && kBWarp < kProdWarp && kProdWarp < kMmaWarp &&
+                  kMmaWarp == kPgThreads / 32 - 1,
+              "warp roles must not overlap");
+static_assert(kDqWarps * 32 == 128, "one dequantising thread per A row");
+template <int MODE>
+constexpr int kNSC = MODE == 0 ? 8 : 6;  // code stages (8 KB each)
+template <int MODE>
+constexpr int kNSB = MODE == 0 ? 4 : 3;  // activation (B) stages
 constexpr int kNSA = 2;                  // A / B stages
 constexpr int kCodesStage = 128 * 64;    // 128 rows x 64 B (128 codes)
 constexpr int kAStage = 128 * 128 * 2;   // 128 rows x 128 bf16
-constexpr int kTmemCols = 256;           // 2 buffers x 2 groups x 64 columns
+constexpr int kTmemBufs = 4;             // accumulator buffers: 2 groups x 64 columns each
+constexpr int kTmemCols = 512;
+constexpr int kNSG = 16;                 // group-sum stages (2 groups x 64 floats)
 constexpr int kXPitch = 65;              // floats per row of the SwiGLU exchange (no bank conflicts)
 
 struct PgSmem {
-  int codes, a, b, xchg, bars, total, bstage;
+  int codes, a, b, gs, xchg, bars, total, bstage;
 };
 
 __host__ __device__ inline PgSmem pg_smem(int mode) {
   PgSmem L;
   int off = 0;
   L.codes = off;
-  off += kNSC * kCodesStage;
+  off += (mode == 0 ? kNSC<0> : kNSC<1>) * kCodesStage;
   L.a = off;
   off += kNSA * kAStage;
   L.bstage = kBlkTokens * 256 * (mode == 1 ? 2 : 1);
   L.b = off;
-  off += kNSA * L.bstage;
+  off += (mode == 0 ? kNSB<0> : kNSB<1>) * L.bstage;
+  L.gs = off;
+  off += kNSG * 2 * kBlkTokens * 4;
   L.xchg = off;
   off += mode == 0 ? 64 * kXPitch * 4 : 0;
   L.bars = off;
-  off += 256;
+  off += 1024;  // mbarriers, the TMEM address and the abort flag
   L.total = off;
   return L;
 }
@@ -287,6 +302,7 @@ __device__ __forceinline__ bool pg_item(const LayerArgs& a, int it, int nblk, in
   } else {
     int e = I.blk.expert;
     if (e < 0 || e >= a.E) e = 0;
+    I.blk.expert = e;
     I.rec = a.records + static_cast<size_t>(e) * a.off_r.stride;
     I.off = &a.off_r;
   }
@@ -300,15 +316,13 @@ __device__ __forceinline__ bool pg_item(const LayerArgs& a, int it, int nblk, in
 __device__ __forceinline__ bool pg_wait(uint64_t* bar, uint32_t parity, volatile int* abort, unsigned* err) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_timer_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63u) == 0) {
-      if (*abort) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
-        *abort = 1;
-        latch_error(err, kErrTimeout);
-        return false;
-      }
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
+    if (*abort) return false;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      *abort = 1;
+      latch_error(err, kErrTimeout);
+      return false;
     }
   }
 }
@@ -319,6 +333,30 @@ __device__ __forceinline__ bool pg_wait_warp(uint64_t* bar, uint32_t parity, vol
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
 
+// Asks L2 to fetch [p, p + bytes) (16-byte aligned, a multiple of 16 bytes).
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// An item's weight rows are contiguous runs in the record (the code rows and
+// their scale/bias rows); the tiled loads then read them from L2 instead of
+// visiting each DRAM page once per 128-wide chunk.
+template <int MODE>
+__device__ __forceinline__ void prefetch_item(const PgItem& I, int H) {
+  if (MODE == 0) {
+    const size_t r0 = static_cast<size_t>(I.tile) * 64;
+    const uint32_t cb = 64 * (H / 2), sb = 64 * (H / 16);
+    prefetch_l2(I.rec + I.off->gate_codes + r0 * (H / 2), cb);
+    prefetch_l2(I.rec + I.off->up_codes + r0 * (H / 2), cb);
+    prefetch_l2(I.rec + I.off->gate_sb + r0 * (H / 16), sb);
+    prefetch_l2(I.rec + I.off->up_sb + r0 * (H / 16), sb);
+  } else {
+    const size_t r0 = static_cast<size_t>(I.tile) * 128;
+    prefetch_l2(I.rec + I.off->down_codes + r0 * (I.Fe / 2), 128 * (I.Fe / 2));
+    prefetch_l2(I.rec + I.off->down_sb + r0 * (I.Fe / 16), 128 * (I.Fe / 16));
+  }
+}
+
 // Two bf16 lanes holding 128 + q (bits 0x4300 | q) -> q, exactly:
 // (128 + q) * 1 - 128 needs no rounding.
 __device__ __forceinline__ uint32_t codes_bf16x2(uint32_t v) {
@@ -328,30 +366,37 @@ __device__ __forceinline__ uint32_t codes_bf16x2(uint32_t v) {
 }
 
 template <int MODE>
-__global__ void __launch_bounds__(kPgThreads, 1) pf_gemm_kernel(const __grid_constant__ LayerArgs a) {
+__global__ void __launch_bounds__(kPgThreads, 1)
+    pf_gemm_kernel(const __grid_constant__ LayerArgs a, const __grid_constant__ PfMaps maps) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const PgSmem L = pg_smem(MODE);
   uint8_t* s_codes = smem + L.codes;
   uint8_t* s_a = smem + L.a;
   uint8_t* s_b = smem + L.b;
   float* s_x = reinterpret_cast<float*>(smem + L.xchg);
+  float* s_gs = reinterpret_cast<float*>(smem + L.gs);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* codes_full = bars;
-  uint64_t* codes_empty = codes_full + kNSC;
-  uint64_t* a_full = codes_empty + kNSC;
+  uint64_t* codes_empty = codes_full + kNSC<MODE>;
+  uint64_t* a_full = codes_empty + kNSC<MODE>;
   uint64_t* a_empty = a_full + kNSA;
   uint64_t* b_full = a_empty + kNSA;
-  uint64_t* tm_full = b_full + kNSA;
-  uint64_t* tm_empty = tm_full + 2;
-  uint32_t* s_taddr = reinterpret_cast<uint32_t*>(tm_empty + 2);
+  uint64_t* b_empty = b_full + kNSB<MODE>;
+  uint64_t* tm_full = b_empty + kNSB<MODE>;
+  uint64_t* tm_empty = tm_full + kTmemBufs;
+  uint64_t* gs_full = tm_empty + kTmemBufs;
+  uint64_t* gs_empty = gs_full + kNSG;
+  uint32_t* s_taddr = reinterpret_cast<uint32_t*>(gs_empty + kNSG);
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_taddr + 1);
   unsigned* err = &a.ws.ctl[0];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
-    for (int i = 0; i < kNSC; ++i) mbar_init(&codes_full[i], 1), mbar_init(&codes_empty[i], kDqWarps);
-    for (int i = 0; i < kNSA; ++i) mbar_init(&a_full[i], kDqWarps), mbar_init(&a_empty[i], 1), mbar_init(&b_full[i], 1);
-    for (int i = 0; i < 2; ++i) mbar_init(&tm_full[i], 1), mbar_init(&tm_empty[i], kEpiWarps);
+    for (int i = 0; i < kNSC<MODE>; ++i) mbar_init(&codes_full[i], 1), mbar_init(&codes_empty[i], kDqWarps);
+    for (int i = 0; i < kNSA; ++i) mbar_init(&a_full[i], kDqWarps), mbar_init(&a_empty[i], 1);
+    for (int i = 0; i < kNSB<MODE>; ++i) mbar_init(&b_full[i], 1), mbar_init(&b_empty[i], 1);
+    for (int i = 0; i < kTmemBufs; ++i) mbar_init(&tm_full[i], 1), mbar_init(&tm_empty[i], kEpiWarps);
+    for (int i = 0; i < kNSG; ++i) mbar_init(&gs_full[i], 1), mbar_init(&gs_empty[i], kEpiWarps);
     *s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -370,76 +415,85 @@ __global__ void __launch_bounds__(kPgThreads, 1) pf_gemm_kernel(const __grid_con
   if (warp == kProdWarp) {
     // ------------------------------------------------------------ codes
     const uint64_t pol = policy_evict_first();
-    RingPos pc;
+    RingPos pc, pg;
     int issued = 0;
     bool stop = false;
     for (int it = blockIdx.x; it < n_items && !stop; it += gridDim.x) {
       PgItem I;
       if (!pg_item<MODE>(a, it, nblk, nsb, I)) break;
-      for (int c = 0; c < I.nch; ++c, pc.next(kNSC)) {
-        if (issued >= kNSC && !pg_wait_warp(&codes_empty[pc.s], pc.ph ^ 1u, s_abort, err)) {
+      if (lane == 0) {  // this item's rows (first item only) and the next item's, into L2
+        PgItem J;
+        if (it == blockIdx.x) prefetch_item<MODE>(I, H);
+        if (it + static_cast<int>(gridDim.x) < n_items && pg_item<MODE>(a, it + gridDim.x, nblk, nsb, J))
+          prefetch_item<MODE>(J, H);
+      }
+      const int np = I.blk.np;
+      const float* gsum = MODE == 0 ? a.pf.sx + static_cast<size_t>(I.blk.xrow) * (H / 64) : a.pf.sh + I.blk.hoff / 64;
+      for (int c = 0; c < I.nch; ++c, pc.next(kNSC<MODE>), pg.next(kNSG)) {
+        if (issued >= kNSC<MODE> && !pg_wait_warp(&codes_empty[pc.s], pc.ph ^ 1u, s_abort, err)) {
           stop = true;
           break;
         }
-        if (lane == 0) mbar_arrive_expect_tx(&codes_full[pc.s], kCodesStage);
-        __syncwarp();
-        uint8_t* dst = s_codes + pc.s * kCodesStage;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int r = lane * 4 + i;
-          const uint8_t* src;
-          if (MODE == 0)
-            src = I.rec + (r < 64 ? I.off->gate_codes : I.off->up_codes) +
-                  static_cast<size_t>(I.tile * 64 + (r & 63)) * (H / 2) + c * 64;
-          else
-            src = I.rec + I.off->down_codes + static_cast<size_t>(I.tile * 128 + r) * (I.Fe / 2) + c * 64;
-          bulk_g2s(dst + r * 64, src, 64, &codes_full[pc.s], pol);
+        if (issued >= kNSG && !pg_wait_warp(&gs_empty[pg.s], pg.ph ^ 1u, s_abort, err)) {
+          stop = true;
+          break;
         }
+        if (lane == 0) {  // this chunk's two group sums of the block's tokens
+          mbar_arrive_expect_tx(&gs_full[pg.s], 2 * np * 4);
+          bulk_g2s(s_gs + pg.s * 2 * kBlkTokens, gsum + static_cast<size_t>(2 * c) * np, 2 * np * 4, &gs_full[pg.s]);
+        }
+        if (lane == 0) {  // the chunk's 128 rows x 64 B of codes: one or two tiled loads
+          uint8_t* dst = s_codes + pc.s * kCodesStage;
+          const bool sh = I.rec == a.shared;
+          const CUtensorMap* m = sh ? maps.shared : maps.routed;
+          const int z = sh ? 0 : I.blk.expert;
+          mbar_arrive_expect_tx(&codes_full[pc.s], kCodesStage);
+          if (MODE == 0) {
+            tma_load_3d(dst, &m[0], c * 64, I.tile * 64, z, &codes_full[pc.s], pol);
+            tma_load_3d(dst + 64 * 64, &m[1], c * 64, I.tile * 64, z, &codes_full[pc.s], pol);
+          } else {
+            tma_load_3d(dst, &m[0], c * 64, I.tile * 128, z, &codes_full[pc.s], pol);
+          }
+        }
+        __syncwarp();
         ++issued;
       }
     }
     // copies in flight land before the CTA leaves
-    for (int j = max(0, issued - kNSC); j < issued; ++j)
-      if (!mbar_wait(&codes_full[j % kNSC], (j / kNSC) & 1)) latch_error(err, kErrTimeout);
-  } else if (warp >= kEpiWarps && warp < kEpiWarps + kDqWarps) {
+    for (int j = max(0, issued - kNSC<MODE>); j < issued; ++j)
+      if (!mbar_wait(&codes_full[j % kNSC<MODE>], (j / kNSC<MODE>) & 1)) latch_error(err, kErrTimeout);
+    for (int j = max(0, issued - kNSG); j < issued; ++j)
+      if (!mbar_wait(&gs_full[j % kNSG], (j / kNSG) & 1)) latch_error(err, kErrTimeout);
+  } else if (warp >= kDqWarp0 && warp < kDqWarp0 + kDqWarps) {
     // ------------------------------------------------------------ dequantise
-    const int dw = warp - kEpiWarps, t = dw * 32 + lane;
+    const int dw = warp - kDqWarp0, t = dw * 32 + lane;
     RingPos pc, pa;
-    int cc = 0, b_issued = 0;
+    int cc = 0;
     for (int it = blockIdx.x; it < n_items && !*s_abort; it += gridDim.x) {
       PgItem I;
       if (!pg_item<MODE>(a, it, nblk, nsb, I)) break;
-      const int np = I.blk.np;
       bool stop = false;
-      for (int c = 0; c < I.nch; ++c, ++cc, pc.next(kNSC), pa.next(kNSA)) {
+      for (int c = 0; c < I.nch; ++c, ++cc, pc.next(kNSC<MODE>), pa.next(kNSA)) {
         if (cc >= kNSA && !pg_wait_warp(&a_empty[pa.s], pa.ph ^ 1u, s_abort, err)) {
           stop = true;
           break;
-        }
-        if (dw == 0 && lane == 0) {  // this chunk's B operand
-          uint8_t* bdst = s_b + pa.s * L.bstage;
-          const uint32_t part = np * 256;
-          if (MODE == 0) {
-            mbar_arrive_expect_tx(&b_full[pa.s], part);
-            bulk_g2s(bdst, a.pf.xc + static_cast<size_t>(I.blk.xrow) * H + static_cast<size_t>(c) * np * 128, part,
-                     &b_full[pa.s]);
-          } else {
-            const size_t e = static_cast<size_t>(I.blk.hoff) + static_cast<size_t>(c) * np * 128;
-            mbar_arrive_expect_tx(&b_full[pa.s], 2 * part);
-            bulk_g2s(bdst, a.pf.hc_hi + e, part, &b_full[pa.s]);
-            bulk_g2s(bdst + part, a.pf.hc_lo + e, part, &b_full[pa.s]);
-          }
-          ++b_issued;
         }
         if (!pg_wait_warp(&codes_full[pc.s], pc.ph, s_abort, err)) {
           stop = true;
           break;
         }
-        const uint8_t* src = s_codes + pc.s * kCodesStage;
-        uint8_t* dst = s_a + pa.s * kAStage;
-        for (int u = t; u < 512; u += kDqWarps * 32) {
-          const int r = u >> 2, c4 = u & 3;
-          const uint4 q = *reinterpret_cast<const uint4*>(src + r * 64 + c4 * 16);
+        // One row per thread (t = row).  A 16-byte core row's bank depends
+        // only on row & 7, so 8 consecutive rows per quarter-warp store
+        // without conflicts; each row starts at a different 16-byte column
+        // of its 64 code bytes ((row >> 1) & 3), so the loads are also free
+        // of conflicts.
+        const uint8_t* src = s_codes + pc.s * kCodesStage + t * 64;
+        uint8_t* dst = s_a + pa.s * kAStage + (t >> 3) * 128 + (t & 7) * 16;
+        const int rot = (t >> 1) & 3;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int c4 = (j + rot) & 3;
+          const uint4 q = *reinterpret_cast<const uint4*>(src + c4 * 16);
           const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
           for (int w = 0; w < 4; ++w) {
@@ -449,8 +503,7 @@ __global__ void __launch_bounds__(kPgThreads, 1) pf_gemm_kernel(const __grid_con
             o.y = codes_bf16x2(((v >> 4) & 0x000F000Fu) | 0x43004300u);
             o.z = codes_bf16x2(((v >> 8) & 0x000F000Fu) | 0x43004300u);
             o.w = codes_bf16x2(((v >> 12) & 0x000F000Fu) | 0x43004300u);
-            const int k8 = c4 * 4 + w;
-            *reinterpret_cast<uint4*>(dst + (k8 * 16 + (r >> 3)) * 128 + (r & 7) * 16) = o;
+            *reinterpret_cast<uint4*>(dst + (c4 * 4 + w) * 2048) = o;
           }
         }
         fence_async_smem();
@@ -462,13 +515,44 @@ __global__ void __launch_bounds__(kPgThreads, 1) pf_gemm_kernel(const __grid_con
       }
       if (stop) break;
     }
-    if (dw == 0 && lane == 0)
-      for (int j = max(0, b_issued - kNSA); j < b_issued; ++j)
-        if (!mbar_wait(&b_full[j % kNSA], (j / kNSA) & 1)) latch_error(err, kErrTimeout);
+  } else if (warp == kBWarp) {
+    // ------------------------------------------------------------ B operand
+    if (lane == 0) {
+      RingPos pb;
+      int issued = 0;
+      bool stop = false;
+      for (int it = blockIdx.x; it < n_items && !stop; it += gridDim.x) {
+        PgItem I;
+        if (!pg_item<MODE>(a, it, nblk, nsb, I)) break;
+        const int np = I.blk.np;
+        for (int c = 0; c < I.nch; ++c, pb.next(kNSB<MODE>)) {
+          if (issued >= kNSB<MODE> && !pg_wait(&b_empty[pb.s], pb.ph ^ 1u, s_abort, err)) {
+            stop = true;
+            break;
+          }
+          uint8_t* bdst = s_b + pb.s * L.bstage;
+          const uint32_t part = np * 256;
+          if (MODE == 0) {
+            mbar_arrive_expect_tx(&b_full[pb.s], part);
+            bulk_g2s(bdst, a.pf.xc + static_cast<size_t>(I.blk.xrow) * H + static_cast<size_t>(c) * np * 128, part,
+                     &b_full[pb.s]);
+          } else {
+            const size_t e = static_cast<size_t>(I.blk.hoff) + static_cast<size_t>(c) * np * 128;
+            mbar_arrive_expect_tx(&b_full[pb.s], 2 * part);
+            bulk_g2s(bdst, a.pf.hc_hi + e, part, &b_full[pb.s]);
+            bulk_g2s(bdst + part, a.pf.hc_lo + e, part, &b_full[pb.s]);
+          }
+          ++issued;
+        }
+      }
+      for (int j = max(0, issued - kNSB<MODE>); j < issued; ++j)
+        if (!mbar_wait(&b_full[j % kNSB<MODE>], (j / kNSB<MODE>) & 1)) latch_error(err, kErrTimeout);
+    }
+    __syncwarp();
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issue
     if (lane == 0) {
-      RingPos pa, pt;
+      RingPos pa, pb, pt;
       int cc = 0;
       bool stop = false;
       for (int it = blockIdx.x; it < n_items && !stop; it += gridDim.x) {
@@ -476,14 +560,14 @@ __global__ void __launch_bounds__(kPgThreads, 1) pf_gemm_kernel(const __grid_con
         if (!pg_item<MODE>(a, it, nblk, nsb, I)) break;
         const int np = I.blk.np;
         const uint32_t idesc = idesc_bf16_f32(128, np);
-        for (int c = 0; c < I.nch; ++c, ++cc, pa.next(kNSA), pt.next(2)) {
-          if (!pg_wait(&a_full[pa.s], pa.ph, s_abort, err) || !pg_wait(&b_full[pa.s], pa.ph, s_abort, err) ||
-              (cc >= 2 && !pg_wait(&tm_empty[pt.s], pt.ph ^ 1u, s_abort, err))) {
+        for (int c = 0; c < I.nch; ++c, ++cc, pa.next(kNSA), pb.next(kNSB<MODE>), pt.next(kTmemBufs)) {
+          if (!pg_wait(&a_full[pa.s], pa.ph, s_abort, err) || !pg_wait(&b_full[pb.s], pb.ph, s_abort, err) ||
+              (cc >= kTmemBufs && !pg_wait(&tm_empty[pt.s], pt.ph ^ 1u, s_abort, err))) {
             stop = true;
             break;
           }
           tc_fence_after();
-          const uint32_t a0 = smem_u32(s_a + pa.s * kAStage), b0 = smem_u32(s_b + pa.s * L.bstage);
+          const uint32_t a0 = smem_u32(s_a + pa.s * kAStage), b0 = smem_u32(s_b + pb.s * L.bstage);
 #pragma unroll
           for (int gi = 0; gi < 2; ++gi) {
             const uint32_t d = taddr + pt.s * 128 + gi * 64;
@@ -496,44 +580,44 @@ __global__ void __launch_bounds__(kPgThreads, 1) pf_gemm_kernel(const __grid_con
             }
           }
           mma_commit(smem_u32(&a_empty[pa.s]));
+          mma_commit(smem_u32(&b_empty[pb.s]));
           mma_commit(smem_u32(&tm_full[pt.s]));
         }
       }
       // the last commits have landed before TMEM is released
-      if (cc > 0 && !mbar_wait(&tm_full[(cc - 1) & 1], ((cc - 1) >> 1) & 1)) latch_error(err, kErrTimeout);
+      if (cc > 0 && !mbar_wait(&tm_full[(cc - 1) % kTmemBufs], ((cc - 1) / kTmemBufs) & 1))
+        latch_error(err, kErrTimeout);
     }
     __syncwarp();
-  } else {
+  } else if (warp < kEpiWarps) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3, hh = warp >> 2;
     const int row = q * 32 + lane;  // TMEM lane = A row of the item
-    RingPos pt;
+    RingPos pt, pg;
     bool stop = false;
     for (int it = blockIdx.x; it < n_items && !stop; it += gridDim.x) {
       PgItem I;
       if (!pg_item<MODE>(a, it, nblk, nsb, I)) break;
       const int np = I.blk.np, half = np >> 1;
       const int G = I.K / 64;
-      // this row's scale/bias words and the block's group sums
+      // this row's scale/bias words (the next chunk's pair is loaded one chunk ahead)
       const uint32_t* sbrow;
-      const float* gsum;
       if (MODE == 0) {
         const uint64_t o = row < 64 ? I.off->gate_sb : I.off->up_sb;
         sbrow = reinterpret_cast<const uint32_t*>(I.rec + o) + static_cast<size_t>(I.tile * 64 + (row & 63)) * G;
-        gsum = a.pf.sx + static_cast<size_t>(I.blk.xrow) * G;
       } else {
         sbrow = reinterpret_cast<const uint32_t*>(I.rec + I.off->down_sb) + static_cast<size_t>(I.tile * 128 + row) * G;
-        gsum = a.pf.sh + I.blk.hoff / 64;
       }
       float acc[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) acc[j] = 0.f;
-      for (int c = 0; c < I.nch; ++c, pt.next(2)) {
-        uint32_t sbw[2];
-        sbw[0] = __ldg(sbrow + 2 * c);
-        sbw[1] = __ldg(sbrow + 2 * c + 1);
+      uint2 sb_next = __ldg(reinterpret_cast<const uint2*>(sbrow));
+      for (int c = 0; c < I.nch; ++c, pt.next(kTmemBufs), pg.next(kNSG)) {
+        const uint32_t sbw[2] = {sb_next.x, sb_next.y};
+        if (c + 1 < I.nch) sb_next = __ldg(reinterpret_cast<const uint2*>(sbrow + 2 * c + 2));
         // the 8 epilogue warps decide together, so the barriers below stay uniform
-        const bool ok = pg_wait_warp(&tm_full[pt.s], pt.ph, s_abort, err);
+        const bool ok = pg_wait_warp(&tm_full[pt.s], pt.ph, s_abort, err) &&
+                        pg_wait_warp(&gs_full[pg.s], pg.ph, s_abort, err);
         if (named_bar_or(2, kEpiWarps * 32, !ok)) {
           stop = true;
           break;
@@ -553,7 +637,7 @@ __global__ void __launch_bounds__(kPgThreads, 1) pf_gemm_kernel(const __grid_con
             }
           tmem_wait();
           const float s = bf16lo(sbw[gi]), b = bf16hi(sbw[gi]);
-          const float* gs = gsum + (2 * c + gi) * np + hh * half;
+          const float* gs = s_gs + pg.s * 2 * kBlkTokens + gi * np + hh * half;
 #pragma unroll
           for (int p = 0; p < 4; ++p)
             if (p * 8 < half) {
@@ -567,7 +651,7 @@ __global__ void __launch_bounds__(kPgThreads, 1) pf_gemm_kernel(const __grid_con
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&tm_empty[pt.s]);
+        if (lane == 0) mbar_arrive(&tm_empty[pt.s]), mbar_arrive(&gs_empty[pg.s]);
       }
       if (stop) break;
       if (MODE == 0) {
@@ -655,7 +739,7 @@ __global__ void __launch_bounds__(256) pf_combine_kernel(const __grid_constant__
 // ---------------------------------------------------------------------------
 // host
 // ---------------------------------------------------------------------------
-size_t prefill_smem_need(const LayerArgs&, int) { return pg_smem(1).total; }
+size_t prefill_smem_need(const LayerArgs&, int) { return std::max(pg_smem(0).total, pg_smem(1).total); }
 
 cudaError_t set_prefill_attributes(int smem_optin) {
   const void* fns[] = {(const void*)pf_gemm_kernel<0>, (const void*)pf_gemm_kernel<1>};
@@ -674,8 +758,54 @@ static cudaError_t markp(const LayerArgs& a, int i, cudaStream_t st) {
   return a.prof_on ? cudaEventRecord(static_cast<cudaEvent_t>(a.prof[i]), st) : cudaSuccess;
 }
 
-cudaError_t launch_prefill(const LayerArgs& in, int num_sms, cudaStream_t st) {
-  if (!prefill_tc_ok(in, in.T) || !in.ws.pf) return launch_decode(in, num_sms, st);
+// Tensor maps of a layer's code matrices (routed records and the shared
+// record) for the tiled loads of the prefill kernels.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static bool encode_codes(EncodeTiledFn enc, CUtensorMap* m, const uint8_t* base, uint64_t row_bytes, uint64_t rows,
+                         uint64_t n_rec, uint64_t rec_stride, uint32_t box_rows) {
+  const cuuint64_t dim[3] = {row_bytes, rows, n_rec};
+  const cuuint64_t stride[2] = {row_bytes, rec_stride};
+  const cuuint32_t box[3] = {64, box_rows, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(base), dim, stride, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Fills `out` (valid = 1) when the layer can take the tensor-core prefill
+// path; valid = 0 otherwise (no records, or shapes the path does not take).
+cudaError_t build_layer_maps(const LayerArgs& a, LayerMaps* out) {
+  out->valid = 0;
+  if (!a.records || a.H % 128 || a.F % 128 || a.Fs % 128) return cudaSuccess;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+  if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) return e ? e : cudaErrorNotSupported;
+  EncodeTiledFn enc = reinterpret_cast<EncodeTiledFn>(fn);
+  const uint64_t H = a.H, F = a.F, Fs = a.Fs, E = a.E;
+  bool ok = encode_codes(enc, &out->gateup.routed[0], a.records + a.off_r.gate_codes, H / 2, F, E, a.off_r.stride, 64) &&
+            encode_codes(enc, &out->gateup.routed[1], a.records + a.off_r.up_codes, H / 2, F, E, a.off_r.stride, 64) &&
+            encode_codes(enc, &out->down.routed[0], a.records + a.off_r.down_codes, F / 2, H, E, a.off_r.stride, 128);
+  out->down.routed[1] = out->down.routed[0];
+  if (ok && a.shared) {
+    ok = encode_codes(enc, &out->gateup.shared[0], a.shared + a.off_s.gate_codes, H / 2, Fs, 1, a.off_s.stride, 64) &&
+         encode_codes(enc, &out->gateup.shared[1], a.shared + a.off_s.up_codes, H / 2, Fs, 1, a.off_s.stride, 64) &&
+         encode_codes(enc, &out->down.shared[0], a.shared + a.off_s.down_codes, Fs / 2, H, 1, a.off_s.stride, 128);
+    out->down.shared[1] = out->down.shared[0];
+  } else if (ok) {
+    out->gateup.shared[0] = out->gateup.shared[1] = out->gateup.routed[0];
+    out->down.shared[0] = out->down.shared[1] = out->down.routed[0];
+  }
+  if (!ok) return cudaErrorInvalidValue;
+  out->valid = 1;
+  return cudaSuccess;
+}
+
+cudaError_t launch_prefill(const LayerArgs& in, const LayerMaps* maps, int num_sms, cudaStream_t st) {
+  if (!prefill_tc_ok(in, in.T) || !in.ws.pf || !maps || !maps->valid) return launch_decode(in, num_sms, st);
   LayerArgs a = in;
   const PfLayout L = pf_layout(a, a.T);
   uint8_t* base = a.ws.pf;
@@ -695,10 +825,10 @@ cudaError_t launch_prefill(const LayerArgs& in, int num_sms, cudaStream_t st) {
   pf_pack_kernel<<<a.E + (a.Fs > 0 ? 1 : 0), kPackThreads, 0, st>>>(a);
   if ((e = cudaGetLastError())) return e;
   if ((e = markp(a, 1, st))) return e;
-  pf_gemm_kernel<0><<<num_sms, kPgThreads, pg_smem(0).total, st>>>(a);
+  pf_gemm_kernel<0><<<num_sms, kPgThreads, pg_smem(0).total, st>>>(a, maps->gateup);
   if ((e = cudaGetLastError())) return e;
   if ((e = markp(a, 2, st))) return e;
-  pf_gemm_kernel<1><<<num_sms, kPgThreads, pg_smem(1).total, st>>>(a);
+  pf_gemm_kernel<1><<<num_sms, kPgThreads, pg_smem(1).total, st>>>(a, maps->down);
   if ((e = cudaGetLastError())) return e;
   pf_combine_kernel<<<a.T, 256, 0, st>>>(a);
   if ((e = cudaGetLastError())) return e;
