@@ -33,14 +33,16 @@
 // The down GEMM's h is fp32; it is split into bf16 hi + lo (two MMAs into
 // the same accumulator), error about 2^-17 relative.
 //
-// Operand layout (no swizzle, K-major): core matrices of 8 rows x 16 bytes;
-// within a 128-K chunk, core (k8, r8) sits at (k8 * R8 + r8) * 128 bytes
-// (R8 = rows / 8).  The descriptor's leading offset is the K-direction core
-// stride (R8 * 128), its stride offset the 8-row stride (128).
+// Operands: A (the dequantised codes) lives in TMEM, row m in lane m, two
+// bf16 per 32-bit column in K order; B (activations) in shared memory, no
+// swizzle, K-major core matrices of 8 rows x 16 bytes: within a 128-K chunk,
+// core (k8, r8) sits at (k8 * R8 + r8) * 128 bytes (R8 = rows / 8), so the
+// descriptor's leading offset is the K-direction core stride (R8 * 128) and
+// its stride offset the 8-row stride (128).
 //
 // Warp roles of pf_gemm_kernel (16 warps, one CTA per SM, persistent over
 // items): warps 0-7 epilogue (TMEM lanes 32*(w%4).., column half w/4),
-// warps 8-11 dequantise codes into A (warp 12 idles), warp 13 streams the activation (B)
+// warps 8-11 dequantise codes into TMEM (warp 12 idles), warp 13 streams the activation (B)
 // chunks, warp 14 streams codes (tiled TMA loads) and group sums, warp 15
 // allocates TMEM and issues the MMAs.
 #include <algorithm>
@@ -235,19 +237,21 @@ static_assert(kDqWarp0 + kDqWarps <= kBWarp && kBWarp < kProdWarp && kProdWarp <
               "warp roles must not overlap");
 static_assert(kDqWarps * 32 == 128, "one dequantising thread per A row");
 template <int MODE>
-constexpr int kNSC = MODE == 0 ? 8 : 6;  // code stages (8 KB each)
+constexpr int kNSC = MODE == 0 ? 12 : 10;  // code stages (8 KB each)
 template <int MODE>
-constexpr int kNSB = MODE == 0 ? 4 : 3;  // activation (B) stages
-constexpr int kNSA = 2;                  // A / B stages
+constexpr int kNSB = MODE == 0 ? 6 : 4;    // activation (B) stages
+constexpr int kNSA = 2;                  // A stages (in TMEM)
 constexpr int kCodesStage = 128 * 64;    // 128 rows x 64 B (128 codes)
-constexpr int kAStage = 128 * 128 * 2;   // 128 rows x 128 bf16
-constexpr int kTmemBufs = 4;             // accumulator buffers: 2 groups x 64 columns each
+constexpr int kACols = 64;               // TMEM columns of one A stage: 128 bf16 per row
+constexpr int kTmemBufs = 3;             // accumulator buffers: 2 groups x 64 columns each
+constexpr int kACol0 = kTmemBufs * 128;  // A stages follow the accumulators
 constexpr int kTmemCols = 512;
+static_assert(kACol0 + kNSA * kACols <= kTmemCols, "TMEM columns");
 constexpr int kNSG = 16;                 // group-sum stages (2 groups x 64 floats)
 constexpr int kXPitch = 65;              // floats per row of the SwiGLU exchange (no bank conflicts)
 
 struct PgSmem {
-  int codes, a, b, gs, xchg, bars, total, bstage;
+  int codes, b, gs, xchg, bars, total, bstage;
 };
 
 __host__ __device__ inline PgSmem pg_smem(int mode) {
@@ -255,8 +259,6 @@ __host__ __device__ inline PgSmem pg_smem(int mode) {
   int off = 0;
   L.codes = off;
   off += (mode == 0 ? kNSC<0> : kNSC<1>) * kCodesStage;
-  L.a = off;
-  off += kNSA * kAStage;
   L.bstage = kBlkTokens * 256 * (mode == 1 ? 2 : 1);
   L.b = off;
   off += (mode == 0 ? kNSB<0> : kNSB<1>) * L.bstage;
@@ -371,7 +373,6 @@ __global__ void __launch_bounds__(kPgThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem[];
   const PgSmem L = pg_smem(MODE);
   uint8_t* s_codes = smem + L.codes;
-  uint8_t* s_a = smem + L.a;
   uint8_t* s_b = smem + L.b;
   float* s_x = reinterpret_cast<float*>(smem + L.xchg);
   float* s_gs = reinterpret_cast<float*>(smem + L.gs);
@@ -482,31 +483,31 @@ __global__ void __launch_bounds__(kPgThreads, 1)
           stop = true;
           break;
         }
-        // One row per thread (t = row).  A 16-byte core row's bank depends
-        // only on row & 7, so 8 consecutive rows per quarter-warp store
-        // without conflicts; each row starts at a different 16-byte column
-        // of its 64 code bytes ((row >> 1) & 3), so the loads are also free
-        // of conflicts.
+        // One row per thread: row = TMEM lane.  The code tile lands with the
+        // 64-byte swizzle (16-byte chunk j of row r at chunk j ^ ((r >> 1) & 3)),
+        // so 8 consecutive rows reading the same logical chunk hit distinct
+        // banks.  Word k8 of the row (8 codes) becomes TMEM columns 4k8..4k8+3.
+        tc_fence_after();
         const uint8_t* src = s_codes + pc.s * kCodesStage + t * 64;
-        uint8_t* dst = s_a + pa.s * kAStage + (t >> 3) * 128 + (t & 7) * 16;
-        const int rot = (t >> 1) & 3;
+        const int sw = (t >> 1) & 3;
+        const uint32_t ta = taddr + (static_cast<uint32_t>(dw * 32) << 16) + kACol0 + pa.s * kACols;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const int c4 = (j + rot) & 3;
-          const uint4 q = *reinterpret_cast<const uint4*>(src + c4 * 16);
+          const uint4 q = *reinterpret_cast<const uint4*>(src + ((j ^ sw) << 4));
           const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+          uint32_t v[16];
 #pragma unroll
           for (int w = 0; w < 4; ++w) {
-            const uint32_t v = w4[w];
-            uint4 o;
-            o.x = codes_bf16x2((v & 0x000F000Fu) | 0x43004300u);
-            o.y = codes_bf16x2(((v >> 4) & 0x000F000Fu) | 0x43004300u);
-            o.z = codes_bf16x2(((v >> 8) & 0x000F000Fu) | 0x43004300u);
-            o.w = codes_bf16x2(((v >> 12) & 0x000F000Fu) | 0x43004300u);
-            *reinterpret_cast<uint4*>(dst + (c4 * 4 + w) * 2048) = o;
+            const uint32_t x = w4[w];
+            v[4 * w + 0] = codes_bf16x2((x & 0x000F000Fu) | 0x43004300u);
+            v[4 * w + 1] = codes_bf16x2(((x >> 4) & 0x000F000Fu) | 0x43004300u);
+            v[4 * w + 2] = codes_bf16x2(((x >> 8) & 0x000F000Fu) | 0x43004300u);
+            v[4 * w + 3] = codes_bf16x2(((x >> 12) & 0x000F000Fu) | 0x43004300u);
           }
+          tmem_st16(ta + j * 16, v);
         }
-        fence_async_smem();
+        tmem_wait_st();
+        tc_fence_before();
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(&a_full[pa.s]);
@@ -567,16 +568,16 @@ __global__ void __launch_bounds__(kPgThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a0 = smem_u32(s_a + pa.s * kAStage), b0 = smem_u32(s_b + pb.s * L.bstage);
+          const uint32_t a0 = taddr + kACol0 + pa.s * kACols, b0 = smem_u32(s_b + pb.s * L.bstage);
 #pragma unroll
           for (int gi = 0; gi < 2; ++gi) {
             const uint32_t d = taddr + pt.s * 128 + gi * 64;
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-              const int kq = gi * 4 + kk;
-              const uint64_t ad = smem_desc(a0 + kq * 4096, 2048, 128);
-              mma_bf16(d, ad, smem_desc(b0 + kq * np * 32, np * 16, 128), idesc, kk > 0 ? 1u : 0u);
-              if (MODE == 1) mma_bf16(d, ad, smem_desc(b0 + np * 256 + kq * np * 32, np * 16, 128), idesc, 1u);
+              const int kq = gi * 4 + kk;  // K = 16 per MMA: 8 TMEM columns of A
+              mma_bf16_ta(d, a0 + kq * 8, smem_desc(b0 + kq * np * 32, np * 16, 128), idesc, kk > 0 ? 1u : 0u);
+              if (MODE == 1)
+                mma_bf16_ta(d, a0 + kq * 8, smem_desc(b0 + np * 256 + kq * np * 32, np * 16, 128), idesc, 1u);
             }
           }
           mma_commit(smem_u32(&a_empty[pa.s]));
@@ -771,7 +772,7 @@ static bool encode_codes(EncodeTiledFn enc, CUtensorMap* m, const uint8_t* base,
   const cuuint32_t box[3] = {64, box_rows, 1};
   const cuuint32_t es[3] = {1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(base), dim, stride, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
