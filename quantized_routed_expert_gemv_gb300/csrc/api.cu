@@ -299,6 +299,13 @@ static int prepare(moe_layer* L, const uint16_t* x, int32_t T, uint16_t* ob, flo
   return MOE_OK;
 }
 
+// Decode batches whose tokens are expected to share almost no routed expert
+// (B * top_k <= E / 2: with uniform routing at most ~1/4 of a token's
+// experts are expected to repeat) run one single-token pass per token.
+static bool per_token_decode(const moe_layer* L, int T) {
+  return T > 1 && T <= 16 && static_cast<long>(T) * L->d.top_k * 2 <= L->d.n_experts;
+}
+
 static int run(moe_layer* L, const uint16_t* x, int32_t T, uint16_t* ob, float* of, int32_t* ids,
                float* wts, void* ws, size_t ws_bytes, void* stream, Path path, const char* name) {
   LayerArgs a;
@@ -306,12 +313,26 @@ static int run(moe_layer* L, const uint16_t* x, int32_t T, uint16_t* ob, float* 
   if (rc || T == 0) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
-  if (path == Path::kPrefill)
+  if (path == Path::kPrefill) {
     e = moe::launch_prefill(a, &L->maps, L->num_sms, st);
-  else if (T == 1 && moe::plan_b1(a, L->num_sms, L->smem_optin))
+  } else if (T == 1 && moe::plan_b1(a, L->num_sms, L->smem_optin)) {
     e = moe::launch_decode_b1(a, L->num_sms, st);
-  else
+  } else if (per_token_decode(L, T) && moe::plan_b1(a, L->num_sms, L->smem_optin)) {
+    // Few tokens over many experts: the tokens share almost no expert, so a
+    // grouped pass reads nearly the same weight bytes as one single-token
+    // pass per token, and the single-token kernels stream them faster.
+    e = cudaSuccess;
+    for (int t = 0; t < T && e == cudaSuccess; ++t) {
+      LayerArgs b = a;
+      const size_t H = L->d.hidden, k = L->d.top_k;
+      b.T = 1, b.x = x + t * H, b.out_bf16 = ob + t * H, b.out_f32 = of ? of + t * H : nullptr;
+      b.ids = ids + t * k, b.weights = wts + t * k;
+      b.prof_on = t == 0 ? a.prof_on : 0;  // the profiling hook times the first token's kernels
+      e = moe::launch_decode_b1(b, L->num_sms, st);
+    }
+  } else {
     e = moe::launch_decode(a, L->num_sms, st);
+  }
   if (e) return cuda_fail(e, name);
   return MOE_OK;
 }

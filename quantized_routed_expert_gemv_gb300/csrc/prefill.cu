@@ -237,13 +237,15 @@ static_assert(kDqWarp0 + kDqWarps <= kBWarp && kBWarp < kProdWarp && kProdWarp <
               "warp roles must not overlap");
 static_assert(kDqWarps * 32 == 128, "one dequantising thread per A row");
 template <int MODE>
-constexpr int kNSC = MODE == 0 ? 12 : 10;  // code stages (8 KB each)
+constexpr int kNSC = MODE == 0 ? 16 : 14;  // code stages (8 KB each)
 template <int MODE>
-constexpr int kNSB = MODE == 0 ? 6 : 4;    // activation (B) stages
+constexpr int kNSB = 3;  // activation (B) stages: stage c % 3 is free once chunk c - 3 is done
 constexpr int kNSA = 2;                  // A stages (in TMEM)
 constexpr int kCodesStage = 128 * 64;    // 128 rows x 64 B (128 codes)
 constexpr int kACols = 64;               // TMEM columns of one A stage: 128 bf16 per row
 constexpr int kTmemBufs = 3;             // accumulator buffers: 2 groups x 64 columns each
+static_assert(kNSB<0> == kTmemBufs && kNSB<1> == kTmemBufs && kNSA < kTmemBufs,
+              "operand stages are released by the accumulator-full barrier of an earlier chunk");
 constexpr int kACol0 = kTmemBufs * 128;  // A stages follow the accumulators
 constexpr int kTmemCols = 512;
 static_assert(kACol0 + kNSA * kACols <= kTmemCols, "TMEM columns");
@@ -380,10 +382,8 @@ __global__ void __launch_bounds__(kPgThreads, 1)
   uint64_t* codes_full = bars;
   uint64_t* codes_empty = codes_full + kNSC<MODE>;
   uint64_t* a_full = codes_empty + kNSC<MODE>;
-  uint64_t* a_empty = a_full + kNSA;
-  uint64_t* b_full = a_empty + kNSA;
-  uint64_t* b_empty = b_full + kNSB<MODE>;
-  uint64_t* tm_full = b_empty + kNSB<MODE>;
+  uint64_t* b_full = a_full + kNSA;
+  uint64_t* tm_full = b_full + kNSB<MODE>;
   uint64_t* tm_empty = tm_full + kTmemBufs;
   uint64_t* gs_full = tm_empty + kTmemBufs;
   uint64_t* gs_empty = gs_full + kNSG;
@@ -394,8 +394,8 @@ __global__ void __launch_bounds__(kPgThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
     for (int i = 0; i < kNSC<MODE>; ++i) mbar_init(&codes_full[i], 1), mbar_init(&codes_empty[i], kDqWarps);
-    for (int i = 0; i < kNSA; ++i) mbar_init(&a_full[i], kDqWarps), mbar_init(&a_empty[i], 1);
-    for (int i = 0; i < kNSB<MODE>; ++i) mbar_init(&b_full[i], 1), mbar_init(&b_empty[i], 1);
+    for (int i = 0; i < kNSA; ++i) mbar_init(&a_full[i], kDqWarps);
+    for (int i = 0; i < kNSB<MODE>; ++i) mbar_init(&b_full[i], 1);
     for (int i = 0; i < kTmemBufs; ++i) mbar_init(&tm_full[i], 1), mbar_init(&tm_empty[i], kEpiWarps);
     for (int i = 0; i < kNSG; ++i) mbar_init(&gs_full[i], 1), mbar_init(&gs_empty[i], kEpiWarps);
     *s_abort = 0;
@@ -475,7 +475,9 @@ __global__ void __launch_bounds__(kPgThreads, 1)
       if (!pg_item<MODE>(a, it, nblk, nsb, I)) break;
       bool stop = false;
       for (int c = 0; c < I.nch; ++c, ++cc, pc.next(kNSC<MODE>), pa.next(kNSA)) {
-        if (cc >= kNSA && !pg_wait_warp(&a_empty[pa.s], pa.ph ^ 1u, s_abort, err)) {
+        // A stage cc % 2 is free once chunk cc - 2's MMAs completed (its
+        // accumulator-full phase; chunk cc + 1 cannot have completed yet)
+        if (cc >= kNSA && !pg_wait_warp(&tm_full[(cc - kNSA) % kTmemBufs], ((cc - kNSA) / kTmemBufs) & 1u, s_abort, err)) {
           stop = true;
           break;
         }
@@ -527,7 +529,9 @@ __global__ void __launch_bounds__(kPgThreads, 1)
         if (!pg_item<MODE>(a, it, nblk, nsb, I)) break;
         const int np = I.blk.np;
         for (int c = 0; c < I.nch; ++c, pb.next(kNSB<MODE>)) {
-          if (issued >= kNSB<MODE> && !pg_wait(&b_empty[pb.s], pb.ph ^ 1u, s_abort, err)) {
+          // B stage issued % 3 is free once chunk issued - 3 completed
+          if (issued >= kNSB<MODE> &&
+              !pg_wait(&tm_full[(issued - kNSB<MODE>) % kTmemBufs], ((issued - kNSB<MODE>) / kTmemBufs) & 1u, s_abort, err)) {
             stop = true;
             break;
           }
@@ -580,9 +584,7 @@ __global__ void __launch_bounds__(kPgThreads, 1)
                 mma_bf16_ta(d, a0 + kq * 8, smem_desc(b0 + np * 256 + kq * np * 32, np * 16, 128), idesc, 1u);
             }
           }
-          mma_commit(smem_u32(&a_empty[pa.s]));
-          mma_commit(smem_u32(&b_empty[pb.s]));
-          mma_commit(smem_u32(&tm_full[pt.s]));
+          mma_commit(smem_u32(&tm_full[pt.s]));  // also frees this chunk's A and B stages
         }
       }
       // the last commits have landed before TMEM is released
