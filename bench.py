@@ -27,6 +27,8 @@ import sys
 import threading
 import time
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
@@ -201,10 +203,92 @@ def read_traffic():
 
 # ----------------------------------------------------------------- reference arm
 
+class _OracleSlices:
+    """One token of the layer through the fp64 oracle, cut into bounded
+    slices: the router, then per selected expert (and the shared expert)
+    128-row blocks of its gate and up rows (SwiGLU after the last block) and
+    448-row blocks of its down rows, added into the output with the routing
+    weight.  Every slice is the oracle's own arithmetic (route, gemv4, silu)
+    on a part of the token; a token is complete after all its slices."""
+
+    GU_ROWS, DN_ROWS = 128, 448
+
+    def __init__(self, orc, oracle, synth, wl, s):
+        self.orc, self.oracle, self.synth, self.wl, self.s = orc, oracle, synth, wl, s
+        self.L = {F: oracle.record_layout(s.H, F) for F in {s.F, s.Fs} if F}
+        self.tokens_done = 0
+        self.plan = []
+
+    def _new_token(self, x_bits):
+        s, orc = self.s, self.orc
+        self.x_bits = x_bits
+        self.x = self.synth.bf16_bits_to_float(x_bits).astype(np.float64)
+        self.out = np.zeros(s.H)
+        self.plan = [("route", None)]
+
+    def _expert_slices(self, rec, F, p):
+        s = self.s
+        L = self.L[F]
+        g = np.zeros(F)
+        u = np.zeros(F)
+        st = {"h": None}
+        sl = []
+        gc = rec[L["gate_codes"]:L["up_codes"]]
+        uc = rec[L["up_codes"]:L["down_codes"]]
+        dc = rec[L["down_codes"]:L["gate_sb"]]
+        gs = rec[L["gate_sb"]:L["up_sb"]].view(np.uint32)
+        us = rec[L["up_sb"]:L["down_sb"]].view(np.uint32)
+        ds = rec[L["down_sb"]:L["bytes"]].view(np.uint32)
+        H, G = s.H, s.H // 64
+        for r0 in range(0, F, self.GU_ROWS):
+            r1 = min(F, r0 + self.GU_ROWS)
+
+            def gu(r0=r0, r1=r1):
+                n = r1 - r0
+                g[r0:r1] = self.oracle.gemv4(gc[r0 * H // 2:r1 * H // 2], gs[r0 * G:r1 * G], n, H, self.x)
+                u[r0:r1] = self.oracle.gemv4(uc[r0 * H // 2:r1 * H // 2], us[r0 * G:r1 * G], n, H, self.x)
+                if r1 == F:
+                    st["h"] = np.array([self.oracle.silu(float(v)) for v in g]) * u
+            sl.append(gu)
+        Gd = F // 64
+        for r0 in range(0, H, self.DN_ROWS):
+            r1 = min(H, r0 + self.DN_ROWS)
+
+            def dn(r0=r0, r1=r1):
+                y = self.oracle.gemv4(dc[r0 * F // 2:r1 * F // 2], ds[r0 * Gd:r1 * Gd], r1 - r0, F, st["h"])
+                self.out[r0:r1] += p * y
+            sl.append(dn)
+        return sl
+
+    def prepare(self, x_bits):
+        """Untimed: records the next slice needs (a new token routes first)."""
+        if not self.plan:
+            self._new_token(x_bits)
+
+    def step(self):
+        """Runs one slice (timed by the caller); returns True when a token finished."""
+        kind, fn = self.plan.pop(0)
+        if kind == "route":
+            _, ids, p = self.orc.route(self.x_bits)
+            work = []
+            for e, pe in zip(ids, p):
+                rec = self.synth.expert_record(self.wl.weight_seed, 0, int(e), self.s.H, self.s.F)
+                work += self._expert_slices(rec, self.s.F, float(pe))
+            if self.s.Fs:
+                work += self._expert_slices(self.orc._shared, self.s.Fs, 1.0)
+            self.plan = [("slice", f) for f in work]
+            self._n_slices = len(self.plan) + 1
+            return False
+        fn()
+        if not self.plan:
+            self.tokens_done += 1
+            return True
+        return False
+
+
 def run_reference(args, world, rank):
     if rank != 0:
         return
-    import numpy as np
     import oracle
     from quantized_routed_expert_gemv_gb300 import synth
 
@@ -214,26 +298,23 @@ def run_reference(args, world, rank):
     shared = synth.expert_record(wl.weight_seed, 0, s.E, s.H, s.Fs)
     orc = oracle.Layer(s.H, s.E, s.k, s.F, s.Fs, {}, shared, rc, rsb)
     B = args.batch
+    sl = _OracleSlices(orc, oracle, synth, wl, s)
+    tok = [0]
 
-    def step(i):
-        xs = [synth.hidden(wl.input_seed, 1000 + (i % args.pool), t, s.H) for t in range(B)]
-        for x in xs:                       # untimed: draw the records this token needs
-            _, ids, _ = orc.route(x)
-            for e in ids:
-                if int(e) not in orc._recs:
-                    orc.set_record(int(e), synth.expert_record(wl.weight_seed, 0, int(e), s.H, s.F))
+    def one_step():
+        if not sl.plan:
+            sl.prepare(synth.hidden(wl.input_seed, 1000 + (tok[0] // B) % args.pool, tok[0] % B, s.H))
+            tok[0] += 1
         t0 = time.perf_counter()
-        for x in xs:
-            orc.token(x)
-        dt = time.perf_counter() - t0
-        for e in list(orc._recs):          # keep host memory bounded
-            orc._recs.pop(e)
-        return dt
+        sl.step()
+        return time.perf_counter() - t0
 
-    for i in range(args.warmup):
-        step(i)
-    total = sum(step(args.warmup + i) for i in range(args.steps))
-    value = B * args.steps / total
+    for _ in range(args.warmup):
+        one_step()
+    done0, frac0 = sl.tokens_done, _frac(sl)
+    total = sum(one_step() for _ in range(args.steps))
+    tokens = (sl.tokens_done - done0) + (_frac(sl) - frac0)
+    value = tokens / total
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -241,11 +322,19 @@ def run_reference(args, world, rank):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": config_dict(s, B),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{args.steps} timed steps of B={B} token(s) through the "
-                                   "single-threaded fp64 C oracle"},
+                         "sample": f"{args.steps} timed slices (router, 128-row gate|up blocks, "
+                                   f"448-row down blocks) of B={B} token(s), {tokens:.3f} tokens of "
+                                   "work, single-threaded fp64 C oracle"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }), flush=True)
+
+
+def _frac(sl):
+    """Fraction of the current token's slices already done."""
+    if not sl.plan or not hasattr(sl, "_n_slices"):
+        return 0.0
+    return 1.0 - len(sl.plan) / sl._n_slices
 
 
 def config_dict(s, B):
