@@ -128,6 +128,7 @@ __device__ __forceinline__ B1Entry b1_entry(const LayerArgs& a, int idx, int has
 constexpr int kR1Threads = 512;
 constexpr int kR1Rows = 8;  // rows per CTA pass: 64 CTAs for 512 experts leave most SMs to gate|up
 
+template <int KPL>  // logit slots per lane of the top-k warp: KPL * 32 >= E
 __global__ void __launch_bounds__(kR1Threads) router_b1_kernel(const __grid_constant__ LayerArgs a) {
   extern __shared__ __align__(16) float rsm[];
   pdl_launch_dependents();
@@ -199,8 +200,9 @@ __global__ void __launch_bounds__(kR1Threads) router_b1_kernel(const __grid_cons
   if (warp != 0) return;
   // Lane l holds the keys of experts l, l+32, ... in registers; a logit's
   // key is its IEEE bit pattern mapped to an order-preserving unsigned (all
-  // finite logits map above 0; 0 marks a taken or absent expert).
-  constexpr int KPL = kMaxExperts / 32;
+  // finite logits map above 0; 0 marks a taken or absent expert).  Each lane
+  // keeps its best key; a round takes the warp's maximum (ties: the lower
+  // id), and only the lane that owned the winner rescans its keys.
   uint32_t key[KPL];
 #pragma unroll
   for (int s2 = 0; s2 < KPL; ++s2) {
@@ -212,14 +214,14 @@ __global__ void __launch_bounds__(kR1Threads) router_b1_kernel(const __grid_cons
     }
     key[s2] = kk;
   }
+  uint32_t bk = 0u;
+  int bs = 0;
+#pragma unroll
+  for (int s2 = 0; s2 < KPL; ++s2)  // ascending slot = ascending id: ties keep the lower
+    if (key[s2] > bk) bk = key[s2], bs = s2;
   float myl = 0.f;
   int myi = 0;
   for (int i = 0; i < k; ++i) {
-    uint32_t bk = 0u;
-    int bs = 0;
-#pragma unroll
-    for (int s2 = 0; s2 < KPL; ++s2)  // ascending slot = ascending id: ties keep the lower
-      if (key[s2] > bk) bk = key[s2], bs = s2;
     const uint32_t top = __reduce_max_sync(kAll, bk);
     const unsigned win = __reduce_min_sync(kAll, (bk == top && top != 0u) ? static_cast<unsigned>(bs * 32 + lane)
                                                                          : 0xFFFFFFFFu);
@@ -232,9 +234,15 @@ __global__ void __launch_bounds__(kR1Threads) router_b1_kernel(const __grid_cons
       myi = w;
       myl = __uint_as_float((top & 0x80000000u) ? (top & 0x7FFFFFFFu) : ~top);
     }
+    if ((w & 31) == lane) {  // the winner's lane drops it and finds its next best
+      const int ws = w >> 5;
+      bk = 0u, bs = 0;
 #pragma unroll
-    for (int s2 = 0; s2 < KPL; ++s2)
-      if (s2 * 32 + lane == w) key[s2] = 0u;
+      for (int s2 = 0; s2 < KPL; ++s2) {
+        if (s2 == ws) key[s2] = 0u;
+        if (key[s2] > bk) bk = key[s2], bs = s2;
+      }
+    }
   }
   const float lmax = __shfl_sync(kAll, myl, 0);
   const float ex = (lane < k) ? expf(myl - lmax) : 0.f;
@@ -817,7 +825,9 @@ bool plan_b1(LayerArgs& a, int num_sms, int smem_optin) {
 }
 
 cudaError_t set_b1_attributes(int smem_optin) {
-  const void* fns[] = {(const void*)router_b1_kernel, (const void*)gateup_b1_kernel<4>,
+  const void* fns[] = {(const void*)router_b1_kernel<4>, (const void*)router_b1_kernel<8>,
+                       (const void*)router_b1_kernel<16>, (const void*)router_b1_kernel<32>,
+                       (const void*)gateup_b1_kernel<4>,
                        (const void*)gateup_b1_kernel<8>, (const void*)down_b1_kernel};
   for (const void* f : fns) {
     cudaFuncAttributes fa;
@@ -850,9 +860,16 @@ static cudaError_t mark1(const LayerArgs& a, int i, cudaStream_t st) {
   return a.prof_on ? cudaEventRecord(static_cast<cudaEvent_t>(a.prof[i]), st) : cudaSuccess;
 }
 
+static const void* router1_fn(int E) {
+  if (E <= 128) return (const void*)router_b1_kernel<4>;
+  if (E <= 256) return (const void*)router_b1_kernel<8>;
+  if (E <= 512) return (const void*)router_b1_kernel<16>;
+  return (const void*)router_b1_kernel<32>;
+}
+
 static cudaError_t launch_router1(const LayerArgs& a, int num_sms, cudaStream_t st) {
   const int rgrid = std::max(1, std::min((a.E + kR1Rows - 1) / kR1Rows, 2 * num_sms));
-  return launch1((const void*)router_b1_kernel, rgrid, kR1Threads, router_b1_smem_bytes(a.E), st, false, a);
+  return launch1(router1_fn(a.E), rgrid, kR1Threads, router_b1_smem_bytes(a.E), st, false, a);
 }
 
 static cudaError_t launch_gateup1(const LayerArgs& a, int part, int num_sms, cudaStream_t st, bool pdl) {
