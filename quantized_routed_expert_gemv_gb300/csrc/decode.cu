@@ -55,7 +55,7 @@ constexpr int kRouterRows = 4;  // rows in flight per iteration
 
 // Thread c owns 16-byte chunk c of every router row (its 16 activations stay
 // in registers); each CTA walks rows 4 at a time with all loads in flight.
-template <int NT>
+template <int NT, int KPL>  // KPL: logit slots per lane of a top-k warp, KPL * 32 >= E
 __global__ void __launch_bounds__(kRouterThreads) router_kernel(const __grid_constant__ LayerArgs a) {
   extern __shared__ __align__(16) float rsm[];
   pdl_launch_dependents();
@@ -66,7 +66,29 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const __grid_con
   const bool act = tid < nchunk;
   float* red = rsm;  // [NT][kRouterRows][NW]
 
-  for (int t0 = 0; t0 < T; t0 += NT) {
+  // The grid is (row blocks of kRouterRows experts) x (token blocks): a CTA
+  // loads its router rows once and walks its share of the token pairs.
+  const int RB = (E + kRouterRows - 1) / kRouterRows;
+  const int TB = max(1, static_cast<int>(gridDim.x) / RB);
+  const int rb = blockIdx.x % RB, tb = blockIdx.x / RB;
+  const int er0 = rb * kRouterRows;
+  const int npair = (T + NT - 1) / NT, ppb = (npair + TB - 1) / TB;
+  const int p_lo = tb * ppb, p_hi = min(npair, p_lo + ppb);
+  uint4 q[kRouterRows];
+  uint32_t sbw[kRouterRows];
+#pragma unroll
+  for (int r = 0; r < kRouterRows; ++r) {
+    q[r] = make_uint4(0, 0, 0, 0), sbw[r] = 0;
+    if (act && er0 + r < E && tb < TB) {
+      q[r] = __ldg(reinterpret_cast<const uint4*>(a.rcodes + static_cast<size_t>(er0 + r) * H) + tid);
+      sbw[r] = __ldg(a.rsb + static_cast<size_t>(er0 + r) * (H >> 6) + (tid >> 2));
+    }
+  }
+  float beta_r = 0.f;
+  if (tid < NT * kRouterRows && a.beta && er0 + tid % kRouterRows < E) beta_r = __ldg(a.beta + er0 + tid % kRouterRows);
+
+  for (int pi = p_lo; pi < p_hi; ++pi) {
+    const int t0 = pi * NT;
     float2 X[NT][8];
     float SX[NT];
 #pragma unroll
@@ -87,37 +109,25 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const __grid_con
         }
       }
     }
-    for (int e0 = blockIdx.x * kRouterRows; e0 < E; e0 += gridDim.x * kRouterRows) {
-      uint4 q[kRouterRows];
-      uint32_t sbw[kRouterRows];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
 #pragma unroll
       for (int r = 0; r < kRouterRows; ++r) {
-        q[r] = make_uint4(0, 0, 0, 0), sbw[r] = 0;
-        if (act && e0 + r < E) {
-          q[r] = __ldg(reinterpret_cast<const uint4*>(a.rcodes + static_cast<size_t>(e0 + r) * H) + tid);
-          sbw[r] = __ldg(a.rsb + static_cast<size_t>(e0 + r) * (H >> 6) + (tid >> 2));
-        }
+        const float p = fmaf(bf16lo(sbw[r]) * 0x1p64f, dot16_u8(q[r], X[t]), bf16hi(sbw[r]) * SX[t]);
+        const float v = warp_sum(p);
+        if (lane == 0) red[(t * kRouterRows + r) * NW + warp] = v;
       }
-#pragma unroll
-      for (int t = 0; t < NT; ++t) {
-#pragma unroll
-        for (int r = 0; r < kRouterRows; ++r) {
-          const float p = fmaf(bf16lo(sbw[r]) * 0x1p64f, dot16_u8(q[r], X[t]), bf16hi(sbw[r]) * SX[t]);
-          const float v = warp_sum(p);
-          if (lane == 0) red[(t * kRouterRows + r) * NW + warp] = v;
-        }
-      }
-      __syncthreads();
-      if (tid < NT * kRouterRows) {
-        const int t = tid / kRouterRows, r = tid % kRouterRows;
-        if (t0 + t < T && e0 + r < E) {
-          float v = 0.f;
-          for (int w = 0; w < NW; ++w) v += red[tid * NW + w];
-          a.ws.logits[static_cast<size_t>(t0 + t) * E + e0 + r] = v + (a.beta ? __ldg(a.beta + e0 + r) : 0.f);
-        }
-      }
-      __syncthreads();
     }
+    __syncthreads();
+    if (tid < NT * kRouterRows) {
+      const int t = tid / kRouterRows, r = tid % kRouterRows;
+      if (t0 + t < T && er0 + r < E) {
+        float v = 0.f;
+        for (int w = 0; w < NW; ++w) v += red[tid * NW + w];
+        a.ws.logits[static_cast<size_t>(t0 + t) * E + er0 + r] = v + beta_r;
+      }
+    }
+    __syncthreads();
   }
 
   // ---- last CTA: top-k, weights, grouping --------------------------------
@@ -129,7 +139,6 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const __grid_con
   if (!s_last) return;
   __threadfence();
 
-  float* Lw = rsm + warp * E;                                     // per-warp logits
   unsigned* sel = reinterpret_cast<unsigned*>(rsm + NW * E);      // [E][4] token bitmasks
   int* s_off = reinterpret_cast<int*>(sel + 4 * E);               // [E] pair offsets
   int* s_ids = s_off + E;                                         // [T*k]
@@ -138,32 +147,48 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const __grid_con
   for (int i = tid; i < 4 * E; i += kRouterThreads) sel[i] = 0u;
   __syncthreads();
 
+  // One warp per token.  Lane l holds the keys of experts l, l+32, ... in
+  // registers (a logit's IEEE bits mapped to an order-preserving unsigned;
+  // 0 marks a taken or absent expert) and its best key; a round takes the
+  // warp's maximum (ties: the lower id) and only the winner's lane rescans.
   for (int t = warp; t < T; t += NW) {
-    for (int e = lane; e < E; e += 32) Lw[e] = __ldcg(a.ws.logits + static_cast<size_t>(t) * E + e);
-    __syncwarp();
+    uint32_t key[KPL];
+#pragma unroll
+    for (int s2 = 0; s2 < KPL; ++s2) {
+      const int e = s2 * 32 + lane;
+      uint32_t kk = 0u;
+      if (e < E) {
+        const uint32_t u = __float_as_uint(__ldcg(a.ws.logits + static_cast<size_t>(t) * E + e));
+        kk = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+      }
+      key[s2] = kk;
+    }
+    uint32_t bk = 0u;
+    int bs = 0;
+#pragma unroll
+    for (int s2 = 0; s2 < KPL; ++s2)
+      if (key[s2] > bk) bk = key[s2], bs = s2;
     float myl = 0.f;
     int myi = 0;
     for (int i = 0; i < k; ++i) {
-      float bv = -FLT_MAX;
-      int bi = E;
-      for (int e = lane; e < E; e += 32) {
-        const float v = Lw[e];
-        if (v > bv) bv = v, bi = e;  // ascending e per lane keeps the lower id on ties
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(kFull, bv, o);
-        const int oi = __shfl_xor_sync(kFull, bi, o);
-        if (ov > bv || (ov == bv && oi < bi)) bv = ov, bi = oi;
-      }
+      const uint32_t top = __reduce_max_sync(kFull, bk);
+      const unsigned win = __reduce_min_sync(
+          kFull, (bk == top && top != 0u) ? static_cast<unsigned>(bs * 32 + lane) : 0xFFFFFFFFu);
+      int bi = static_cast<int>(win);
       if (bi >= E) {  // only reachable with non-finite logits (outside the contract)
         if (lane == 0) latch_error(&a.ws.ctl[0], kErrRange);
         bi = i;
       }
-      if (lane == i) myl = bv, myi = bi;
-      __syncwarp();
-      if (lane == 0) Lw[bi] = -INFINITY;
-      __syncwarp();
+      if (lane == i) myi = bi, myl = __uint_as_float((top & 0x80000000u) ? (top & 0x7FFFFFFFu) : ~top);
+      if ((bi & 31) == lane) {
+        const int ws = bi >> 5;
+        bk = 0u, bs = 0;
+#pragma unroll
+        for (int s2 = 0; s2 < KPL; ++s2) {
+          if (s2 == ws) key[s2] = 0u;
+          if (key[s2] > bk) bk = key[s2], bs = s2;
+        }
+      }
     }
     const float lmax = __shfl_sync(kFull, myl, 0);
     const float ex = (lane < k) ? expf(myl - lmax) : 0.f;
@@ -688,7 +713,10 @@ static cudaError_t launch_ex(const void* fn, dim3 grid, dim3 block, size_t smem,
 // Opt every kernel in to the device's full dynamic shared memory once, so
 // layers of different shapes opened in any order all launch.
 cudaError_t set_decode_attributes(int smem_optin) {
-  const void* fns[] = {(const void*)router_kernel<1>,     (const void*)router_kernel<2>,
+  const void* fns[] = {(const void*)router_kernel<1, 4>,  (const void*)router_kernel<1, 8>,
+                       (const void*)router_kernel<1, 16>, (const void*)router_kernel<1, 32>,
+                       (const void*)router_kernel<2, 4>,  (const void*)router_kernel<2, 8>,
+                       (const void*)router_kernel<2, 16>, (const void*)router_kernel<2, 32>,
                        (const void*)gateup_kernel<1, 16>, (const void*)gateup_kernel<4, 7>,
                        (const void*)down_kernel<1, 8>,    (const void*)down_kernel<4, 7>};
   for (const void* f : fns) {
@@ -719,9 +747,19 @@ static cudaError_t mark(const LayerArgs& a, int i, cudaStream_t st) {
 
 static cudaError_t launch_router_g(const LayerArgs& a, int num_sms, cudaStream_t st) {
   const bool one = (a.T == 1);
-  const int rgrid = std::max(1, std::min((a.E + kRouterRows - 1) / kRouterRows, 2 * num_sms));
-  return launch_ex(one ? (const void*)router_kernel<1> : (const void*)router_kernel<2>, dim3(rgrid),
-                   dim3(kRouterThreads), router_smem_bytes(a.E), st, false, a);
+  const int nt = one ? 1 : 2;
+  const int rb = (a.E + kRouterRows - 1) / kRouterRows;
+  const int tb = std::max(1, std::min((a.T + nt - 1) / nt, (2 * num_sms) / rb));
+  const int rgrid = rb * tb;  // row blocks x token blocks
+  const int kpl = a.E <= 128 ? 4 : a.E <= 256 ? 8 : a.E <= 512 ? 16 : 32;
+  const void* fn;
+  if (one)
+    fn = kpl == 4 ? (const void*)router_kernel<1, 4> : kpl == 8 ? (const void*)router_kernel<1, 8>
+       : kpl == 16 ? (const void*)router_kernel<1, 16> : (const void*)router_kernel<1, 32>;
+  else
+    fn = kpl == 4 ? (const void*)router_kernel<2, 4> : kpl == 8 ? (const void*)router_kernel<2, 8>
+       : kpl == 16 ? (const void*)router_kernel<2, 16> : (const void*)router_kernel<2, 32>;
+  return launch_ex(fn, dim3(rgrid), dim3(kRouterThreads), router_smem_bytes(a.E), st, false, a);
 }
 
 static cudaError_t launch_experts_g(LayerArgs& a, int num_sms, cudaStream_t st, bool pdl) {

@@ -11,7 +11,7 @@
 // other chunks run the decode kernels):
 //   router          decode.cu's router for T tokens: logits, top-k, weights,
 //                   grouping by expert.
-//   pf_pack_kernel  one CTA per entry (shared expert, then active experts):
+//   pf_pack_kernel  CTAs over (entry, 16 packed rows) (shared expert, then active experts):
 //                   splits the entry's tokens into blocks of <= 64, writes the
 //                   block table, the activations in the tensor core's
 //                   core-matrix order (see below) and their per-group sums.
@@ -116,6 +116,7 @@ size_t prefill_workspace_bytes(const LayerArgs& a, int T) {
 // pack: block table, activations in core-matrix order, group sums
 // ---------------------------------------------------------------------------
 constexpr int kPackThreads = 256;
+constexpr int kPackSlices = kMaxTokens / 16;  // CTAs per entry: 16 packed rows each
 
 __device__ __forceinline__ int clamp_nact(const LayerArgs& a) {
   const int n = *reinterpret_cast<volatile int*>(a.ws.n_act);
@@ -131,7 +132,7 @@ __device__ __forceinline__ int entry_cnt(const LayerArgs& a, int i, int has_sh) 
 __global__ void __launch_bounds__(kPackThreads) pf_pack_kernel(const __grid_constant__ LayerArgs a) {
   const int has_sh = a.Fs > 0 ? 1 : 0;
   const int n_ent = has_sh + clamp_nact(a);
-  const int j = blockIdx.x;
+  const int j = blockIdx.x / kPackSlices, slice = blockIdx.x % kPackSlices;  // entry, row slice
   if (j >= n_ent) return;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, H = a.H;
   const bool shared = has_sh && j == 0;
@@ -161,7 +162,7 @@ __global__ void __launch_bounds__(kPackThreads) pf_pack_kernel(const __grid_cons
   const int nbj = blocks_of(cnt);
   const int expert = shared ? -1 : a.ws.act_expert[j - has_sh];
   const int pair0 = shared ? 0 : a.ws.act_off[j - has_sh];
-  if (tid < nbj) {
+  if (slice == 0 && tid < nbj) {
     const int b = tid;
     PBlk p;
     p.expert = expert;
@@ -174,20 +175,21 @@ __global__ void __launch_bounds__(kPackThreads) pf_pack_kernel(const __grid_cons
     p.pad = 0;
     a.pf.blk[nb0 + b] = p;
   }
-  if (j == n_ent - 1 && tid == 0) {
+  if (slice == 0 && j == n_ent - 1 && tid == 0) {
     a.pf.hdr[0] = static_cast<int>(nb0) + nbj;
     a.pf.hdr[1] = has_sh ? blocks_of(a.T) : 0;
   }
-  if (!shared)
+  if (!shared && slice == 0)
     for (int n = tid; n < cnt; n += kPackThreads) {
       const int p = pair0 + n;
       const int slot = a.ws.pair_slot[p];
       if (slot >= 0 && slot < a.T * a.k) a.pf.inv[slot] = p;
     }
 
-  // packed rows: one warp per row; a lane handles 8 consecutive K values
-  const int nrows = rows_of(cnt), units = H / 8;
-  for (int n = warp; n < nrows; n += kPackThreads / 32) {
+  // packed rows: one warp per row (this CTA's slice of 16 rows); a lane
+  // handles 8 consecutive K values
+  const int nrows = min(rows_of(cnt), (slice + 1) * 16), units = H / 8;
+  for (int n = slice * 16 + warp; n < nrows; n += kPackThreads / 32) {
     const int b = n / kBlkTokens, nn = n % kBlkTokens;
     const int len = min(kBlkTokens, cnt - b * kBlkTokens), np = round16(len);
     const int xrow = static_cast<int>(row0) + b * kBlkTokens;
@@ -825,7 +827,7 @@ cudaError_t launch_prefill(const LayerArgs& in, const LayerMaps* maps, int num_s
   cudaError_t e;
   if ((e = markp(a, 0, st))) return e;
   if ((e = launch_decode_router(a, num_sms, st))) return e;
-  pf_pack_kernel<<<a.E + (a.Fs > 0 ? 1 : 0), kPackThreads, 0, st>>>(a);
+  pf_pack_kernel<<<(a.E + (a.Fs > 0 ? 1 : 0)) * kPackSlices, kPackThreads, 0, st>>>(a);
   if ((e = cudaGetLastError())) return e;
   if ((e = markp(a, 1, st))) return e;
   pf_gemm_kernel<0><<<num_sms, kPgThreads, pg_smem(0).total, st>>>(a, maps->gateup);
