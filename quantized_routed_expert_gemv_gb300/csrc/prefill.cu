@@ -40,11 +40,11 @@
 // descriptor's leading offset is the K-direction core stride (R8 * 128) and
 // its stride offset the 8-row stride (128).
 //
-// Warp roles of pf_gemm_kernel (16 warps, one CTA per SM, persistent over
-// items): warps 0-7 epilogue (TMEM lanes 32*(w%4).., column half w/4),
-// warps 8-11 dequantise codes into TMEM (warp 12 idles), warp 13 streams the activation (B)
-// chunks, warp 14 streams codes (tiled TMA loads) and group sums, warp 15
-// allocates TMEM and issues the MMAs.
+// Warp roles of pf_gemm_kernel (11 warps, one CTA per SM, persistent over
+// items): warps 0-3 epilogue (TMEM lanes 32*w.., all of a block's columns),
+// warps 4-7 dequantise codes into TMEM (lanes 32*(w-4)..), warp 8 streams
+// the activation (B) chunks, warp 9 streams codes (tiled TMA loads) and
+// group sums, warp 10 allocates TMEM and issues the MMAs.
 #include <algorithm>
 
 #include "common.cuh"
@@ -230,10 +230,10 @@ __global__ void __launch_bounds__(kPackThreads) pf_pack_kernel(const __grid_cons
 // ---------------------------------------------------------------------------
 // grouped GEMM on the tensor cores
 // ---------------------------------------------------------------------------
-constexpr int kPgThreads = 512;
-constexpr int kEpiWarps = 8, kDqWarps = 4, kBWarp = 13, kProdWarp = 14, kMmaWarp = 15;
-constexpr int kDqWarp0 = kEpiWarps;  // dequantise warps: kDqWarp0 .. kDqWarp0 + kDqWarps - 1; warp 12 idles
-static_assert(kEpiWarps == 8, "the epilogue's named barriers count 8 warps (256 threads)");
+constexpr int kPgThreads = 352;  // 11 warps
+constexpr int kEpiWarps = 4, kDqWarps = 4, kBWarp = 8, kProdWarp = 9, kMmaWarp = 10;
+constexpr int kDqWarp0 = kEpiWarps;  // dequantise warps: kDqWarp0 .. kDqWarp0 + kDqWarps - 1
+static_assert(kEpiWarps == 4 && kDqWarps == 4, "one epilogue and one dequantising warp per TMEM lane quarter");
 static_assert(kDqWarp0 + kDqWarps <= kBWarp && kBWarp < kProdWarp && kProdWarp < kMmaWarp &&
                   kMmaWarp == kPgThreads / 32 - 1,
               "warp roles must not overlap");
@@ -371,8 +371,9 @@ __device__ __forceinline__ uint32_t codes_bf16x2(uint32_t v) {
   return r;
 }
 
+// 11 warps put three warps on some SM sub-partitions: 168 registers each.
 template <int MODE>
-__global__ void __launch_bounds__(kPgThreads, 1)
+__global__ void __maxnreg__(168)
     pf_gemm_kernel(const __grid_constant__ LayerArgs a, const __grid_constant__ PfMaps maps) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const PgSmem L = pg_smem(MODE);
@@ -575,15 +576,18 @@ __global__ void __launch_bounds__(kPgThreads, 1)
           }
           tc_fence_after();
           const uint32_t a0 = taddr + kACol0 + pa.s * kACols, b0 = smem_u32(s_b + pb.s * L.bstage);
+          // descriptor of the chunk's first K step; each next step adds
+          // np * 32 bytes to the start address field (units of 16 bytes)
+          const uint64_t bd0 = smem_desc(b0, np * 16, 128), bstep = static_cast<uint64_t>(np * 2);
+          const uint64_t bd_lo = smem_desc(b0 + np * 256, np * 16, 128);
 #pragma unroll
           for (int gi = 0; gi < 2; ++gi) {
             const uint32_t d = taddr + pt.s * 128 + gi * 64;
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
               const int kq = gi * 4 + kk;  // K = 16 per MMA: 8 TMEM columns of A
-              mma_bf16_ta(d, a0 + kq * 8, smem_desc(b0 + kq * np * 32, np * 16, 128), idesc, kk > 0 ? 1u : 0u);
-              if (MODE == 1)
-                mma_bf16_ta(d, a0 + kq * 8, smem_desc(b0 + np * 256 + kq * np * 32, np * 16, 128), idesc, 1u);
+              mma_bf16_ta(d, a0 + kq * 8, bd0 + kq * bstep, idesc, kk > 0 ? 1u : 0u);
+              if (MODE == 1) mma_bf16_ta(d, a0 + kq * 8, bd_lo + kq * bstep, idesc, 1u);
             }
           }
           mma_commit(smem_u32(&tm_full[pt.s]));  // also frees this chunk's A and B stages
@@ -596,14 +600,14 @@ __global__ void __launch_bounds__(kPgThreads, 1)
     __syncwarp();
   } else if (warp < kEpiWarps) {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3, hh = warp >> 2;
-    const int row = q * 32 + lane;  // TMEM lane = A row of the item
+    const int q = warp;              // TMEM lane quarter
+    const int row = q * 32 + lane;   // TMEM lane = A row of the item
     RingPos pt, pg;
     bool stop = false;
     for (int it = blockIdx.x; it < n_items && !stop; it += gridDim.x) {
       PgItem I;
       if (!pg_item<MODE>(a, it, nblk, nsb, I)) break;
-      const int np = I.blk.np, half = np >> 1;
+      const int np = I.blk.np;
       const int G = I.K / 64;
       // this row's scale/bias words (the next chunk's pair is loaded one chunk ahead)
       const uint32_t* sbrow;
@@ -613,14 +617,14 @@ __global__ void __launch_bounds__(kPgThreads, 1)
       } else {
         sbrow = reinterpret_cast<const uint32_t*>(I.rec + I.off->down_sb) + static_cast<size_t>(I.tile * 128 + row) * G;
       }
-      float acc[32];
+      float acc[kBlkTokens];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) acc[j] = 0.f;
+      for (int j = 0; j < kBlkTokens; ++j) acc[j] = 0.f;
       uint2 sb_next = __ldg(reinterpret_cast<const uint2*>(sbrow));
       for (int c = 0; c < I.nch; ++c, pt.next(kTmemBufs), pg.next(kNSG)) {
         const uint32_t sbw[2] = {sb_next.x, sb_next.y};
         if (c + 1 < I.nch) sb_next = __ldg(reinterpret_cast<const uint2*>(sbrow + 2 * c + 2));
-        // the 8 epilogue warps decide together, so the barriers below stay uniform
+        // the epilogue warps decide together, so the barriers below stay uniform
         const bool ok = pg_wait_warp(&tm_full[pt.s], pt.ph, s_abort, err) &&
                         pg_wait_warp(&gs_full[pg.s], pg.ph, s_abort, err);
         if (named_bar_or(2, kEpiWarps * 32, !ok)) {
@@ -630,28 +634,27 @@ __global__ void __launch_bounds__(kPgThreads, 1)
         tc_fence_after();
 #pragma unroll
         for (int gi = 0; gi < 2; ++gi) {
-          uint32_t d[32];
-          const uint32_t base = taddr + (static_cast<uint32_t>(q * 32) << 16) + pt.s * 128 + gi * 64 + hh * half;
-#pragma unroll
-          for (int p = 0; p < 4; ++p)
-            if (p * 8 < half) {
-              uint32_t r8[8];
-              tmem_ld8(base + p * 8, r8);
-#pragma unroll
-              for (int j = 0; j < 8; ++j) d[p * 8 + j] = r8[j];
-            }
-          tmem_wait();
+          const uint32_t base = taddr + (static_cast<uint32_t>(q * 32) << 16) + pt.s * 128 + gi * 64;
           const float s = bf16lo(sbw[gi]), b = bf16hi(sbw[gi]);
-          const float* gs = s_gs + pg.s * 2 * kBlkTokens + gi * np + hh * half;
+          const float* gs = s_gs + pg.s * 2 * kBlkTokens + gi * np;
 #pragma unroll
-          for (int p = 0; p < 4; ++p)
-            if (p * 8 < half) {
-              const float4 x0 = *reinterpret_cast<const float4*>(gs + p * 8);
-              const float4 x1 = *reinterpret_cast<const float4*>(gs + p * 8 + 4);
-              const float xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+          for (int p = 0; p < kBlkTokens / 16; ++p)  // 16 columns per TMEM round trip
+            if (p * 16 < np) {
+              uint32_t d0[8], d1[8];
+              tmem_ld8(base + p * 16, d0);
+              tmem_ld8(base + p * 16 + 8, d1);
+              tmem_wait();
+              const float4 x0 = *reinterpret_cast<const float4*>(gs + p * 16);
+              const float4 x1 = *reinterpret_cast<const float4*>(gs + p * 16 + 4);
+              const float4 x2 = *reinterpret_cast<const float4*>(gs + p * 16 + 8);
+              const float4 x3 = *reinterpret_cast<const float4*>(gs + p * 16 + 12);
+              const float xs[16] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w,
+                                    x2.x, x2.y, x2.z, x2.w, x3.x, x3.y, x3.z, x3.w};
 #pragma unroll
-              for (int j = 0; j < 8; ++j)
-                acc[p * 8 + j] = fmaf(s, __uint_as_float(d[p * 8 + j]), fmaf(b, xs[j], acc[p * 8 + j]));
+              for (int j = 0; j < 8; ++j) {
+                acc[p * 16 + j] = fmaf(s, __uint_as_float(d0[j]), fmaf(b, xs[j], acc[p * 16 + j]));
+                acc[p * 16 + 8 + j] = fmaf(s, __uint_as_float(d1[j]), fmaf(b, xs[8 + j], acc[p * 16 + 8 + j]));
+              }
             }
         }
         tc_fence_before();
@@ -660,25 +663,24 @@ __global__ void __launch_bounds__(kPgThreads, 1)
       }
       if (stop) break;
       if (MODE == 0) {
-        // SwiGLU: up rows (64..127) hand their values to the gate rows
+        // SwiGLU: up rows (64..127, warps 2-3) hand their values to the gate rows
         if (q >= 2) {
-          float* xr = s_x + ((q - 2) * 32 + lane) * kXPitch + hh * half;
+          float* xr = s_x + ((q - 2) * 32 + lane) * kXPitch;
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (j < half) xr[j] = acc[j];
+          for (int j = 0; j < kBlkTokens; ++j)
+            if (j < np) xr[j] = acc[j];
         }
         named_bar(1, kEpiWarps * 32);
         if (q < 2) {
           const int f = I.tile * 64 + row;  // row of h (F index)
           const int cf = f >> 7, k8 = (f & 127) >> 3, pos = ((f & 7) >> 2) | ((f & 3) << 1);
-          float* xr = s_x + row * kXPitch + hh * half;
+          float* xr = s_x + row * kXPitch;
           const size_t e0 = static_cast<size_t>(I.blk.hoff) + static_cast<size_t>(cf) * np * 128 + k8 * (np >> 3) * 64 + pos;
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (j < half) {
-              const int n = hh * half + j;
-              const float h = silu_f(acc[j]) * xr[j];
-              xr[j] = h;
+          for (int n = 0; n < kBlkTokens; ++n)
+            if (n < np) {
+              const float h = silu_f(acc[n]) * xr[n];
+              xr[n] = h;
               const uint16_t hi = f32_to_bf16_rne(h);
               const uint16_t lo = f32_to_bf16_rne(h - __uint_as_float(static_cast<uint32_t>(hi) << 16));
               const size_t e = e0 + (n >> 3) * 64 + (n & 7) * 8;
@@ -699,11 +701,8 @@ __global__ void __launch_bounds__(kPgThreads, 1)
         const bool shared = a.Fs > 0 && I.blk.expert < 0;
         float* y = shared ? a.pf.y_sh : a.pf.y_pair;
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (j < half) {
-            const int n = hh * half + j;
-            if (n < I.blk.len) y[static_cast<size_t>(I.blk.tok0 + n) * H + r] = acc[j];
-          }
+        for (int n = 0; n < kBlkTokens; ++n)
+          if (n < I.blk.len) y[static_cast<size_t>(I.blk.tok0 + n) * H + r] = acc[n];
       }
     }
   }
