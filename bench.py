@@ -50,6 +50,8 @@ def parse_args():
                    help="shrink the routed-expert count (small layers for ncu captures only)")
     p.add_argument("--no-extras", action="store_true",
                    help="skip the B=4/16 lines, e2e, per-kernel and CPU-baseline passes")
+    p.add_argument("--prefill-only", action="store_true",
+                   help="only the prefill-chunk measurement (mid-prefill, T=128), one JSON object")
     p.add_argument("--streamed", action="store_true",
                    help="add the streamed-cache workload (4 large layers, experts in pinned host "
                         "memory, 64 HBM slots per layer, 256 B=1 steps); needs ~51 GB of host RAM")
@@ -369,7 +371,6 @@ def time_graphs(torch, graphs, K, W, stream, world, device):
 
 
 def run_ours(args, world, rank, local):
-    import numpy as np
     import torch
 
     from quantized_routed_expert_gemv_gb300 import moe, synth
@@ -377,6 +378,13 @@ def run_ours(args, world, rank, local):
 
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
+    if args.prefill_only:
+        peaks = _peaks()
+        stream = torch.cuda.Stream(device)
+        res = run_prefill(args, device, stream, peaks.get("hbm_gbs", 6800.0), peaks.get("bf16_tflops", 1900.0))
+        if rank == 0:
+            print(json.dumps({"prefill": res}), flush=True)
+        return
     wl = synth.WORKLOADS[WORKLOAD]
     s = wl.shape
     if args.experts:
@@ -441,11 +449,7 @@ def run_ours(args, world, rank, local):
                      "distinct_experts": main["distinct_experts"]},
            "by_batch": {str(b): {k: v for k, v in r.items()} for b, r in results.items()}}
 
-    peaks = {}
-    try:
-        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
-    except OSError:
-        pass
+    peaks = _peaks()
     peak = peaks.get("hbm_gbs", 6800.0)
     peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
 
@@ -505,10 +509,83 @@ def run_ours(args, world, rank, local):
         if rank == 0 and world == 1:
             out["cpu_baseline"] = cpu_baseline(wl, s)
     dl.close()
+    if not args.no_extras:
+        out["prefill"] = run_prefill(args, device, stream, peak, peaks.get("bf16_tflops", 1900.0))
     if args.streamed:
         out["streamed"] = run_streamed(args, device, stream, peak)
     if rank == 0:
         print(json.dumps(out), flush=True)
+
+
+def _peaks() -> dict:
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except OSError:
+        return {}
+
+
+def run_prefill(args, device, stream, hbm_peak, bf16_peak):
+    """Prefill chunks of the mid-prefill workload (H=2048, E=128, top-8,
+    F=768, Fs=2048, per-expert logit offsets ~ N(0,1)): T=128 tokens per
+    chunk on the tensor-core path, 8 distinct chunks replayed as CUDA graphs.
+    Algorithmic bytes: every distinct selected expert's record, the shared
+    record and the router once, plus the activations; flops: 2 x 3 x F x H
+    per (token, expert) pair and 2 x 3 x Fs x H per token."""
+    import torch
+
+    from quantized_routed_expert_gemv_gb300 import moe, synth
+    from quantized_routed_expert_gemv_gb300.device import DeviceLayer, bf16_tensor
+
+    wl = synth.WORKLOADS["mid-prefill"]
+    s, T = wl.shape, 128
+    dl = DeviceLayer(s, wl.weight_seed, beta=synth.beta_for(wl), max_tokens=T, device=device)
+    pool = 8
+    xs = [bf16_tensor(np.stack([synth.hidden(wl.input_seed, 2000 + p, t, s.H) for t in range(T)]), device)
+          for p in range(pool)]
+    outs = dl.outputs(T)
+    graphs, distinct = [], []
+    with torch.cuda.stream(stream):
+        dl.prefill(xs[0], outs, stream.cuda_stream)
+    torch.cuda.synchronize()
+    for p in range(pool):
+        with torch.cuda.stream(stream):
+            dl.prefill(xs[p], outs, stream.cuda_stream)
+        stream.synchronize()
+        distinct.append(len(np.unique(outs[2].cpu().numpy())))
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            dl.prefill(xs[p], outs, stream.cuda_stream)
+        graphs.append(g)
+    K = min(args.steps, 200)
+    ms, _, _ = time_graphs(torch, graphs, K, args.warmup, stream, 1, device)
+    assert dl.check(stream.cuda_stream) == moe.MOE_OK, moe.last_error()
+    d = float(np.mean(distinct))
+    rec = record_bytes_unpadded(s.H, s.F)
+    nbytes = d * rec + record_bytes_unpadded(s.H, s.Fs) + s.E * s.H + s.E * (s.H // 64) * 4 + T * s.H * 8
+    flops = 2.0 * 3 * s.F * s.H * T * s.k + 2.0 * 3 * s.Fs * s.H * T
+    sec = ms / K / 1e3
+    # per-phase split: events around router+pack, gate|up, down+combine
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    for e in evs:
+        e.record(stream)
+    torch.cuda.synchronize()
+    moe.moe_set_profile_events(dl.handle, [e.cuda_event for e in evs])
+    sums = [0.0, 0.0, 0.0]
+    with torch.cuda.stream(stream):
+        for i in range(20):
+            dl.prefill(xs[i % pool], outs, stream.cuda_stream)
+            evs[3].synchronize()
+            for j in range(3):
+                sums[j] += evs[j].elapsed_time(evs[j + 1])
+    moe.moe_set_profile_events(dl.handle, None)
+    dl.close()
+    return {"workload": f"mid-prefill: T={T} token chunks, H={s.H} E={s.E} top-{s.k} F={s.F} Fs={s.Fs}, "
+                        "per-expert logit offsets ~ N(0,1)",
+            "tokens_per_s": T / sec, "ms_per_chunk": sec * 1e3, "distinct_experts": d,
+            "bytes_per_chunk": nbytes, "gbs": nbytes / sec / 1e9, "frac_of_measured_hbm": nbytes / sec / 1e9 / hbm_peak,
+            "tflops": flops / sec / 1e12, "frac_of_bf16_peak": flops / sec / 1e12 / bf16_peak,
+            "phase_ms": {"router_pack": sums[0] / 20, "gateup": sums[1] / 20, "down_combine": sums[2] / 20},
+            "l2": "inputs larger than L2: ~344 MB of distinct weights per chunk"}
 
 
 def h2d_bandwidth(torch, device, nbytes=1 << 30, reps=5) -> float:
