@@ -40,11 +40,12 @@
 // descriptor's leading offset is the K-direction core stride (R8 * 128) and
 // its stride offset the 8-row stride (128).
 //
-// Warp roles of pf_gemm_kernel (11 warps, one CTA per SM, persistent over
+// Warp roles of pf_gemm_kernel (12 warps, one CTA per SM, persistent over
 // items): warps 0-3 epilogue (TMEM lanes 32*w.., all of a block's columns),
 // warps 4-7 dequantise codes into TMEM (lanes 32*(w-4)..), warp 8 streams
 // the activation (B) chunks, warp 9 streams codes (tiled TMA loads) and
-// group sums, warp 10 allocates TMEM and issues the MMAs.
+// group sums, warps 10-11 issue the MMAs (alternate chunks; warp 10 also
+// allocates TMEM).
 #include <algorithm>
 
 #include "common.cuh"
@@ -230,24 +231,24 @@ __global__ void __launch_bounds__(kPackThreads) pf_pack_kernel(const __grid_cons
 // ---------------------------------------------------------------------------
 // grouped GEMM on the tensor cores
 // ---------------------------------------------------------------------------
-constexpr int kPgThreads = 352;  // 11 warps
+constexpr int kPgThreads = 384;  // 12 warps
 constexpr int kEpiWarps = 4, kDqWarps = 4, kBWarp = 8, kProdWarp = 9, kMmaWarp = 10;
+constexpr int kMmaWarps = 2;  // MMA issuers: warp kMmaWarp + i issues the chunks with index % 2 == i
 constexpr int kDqWarp0 = kEpiWarps;  // dequantise warps: kDqWarp0 .. kDqWarp0 + kDqWarps - 1
 static_assert(kEpiWarps == 4 && kDqWarps == 4, "one epilogue and one dequantising warp per TMEM lane quarter");
 static_assert(kDqWarp0 + kDqWarps <= kBWarp && kBWarp < kProdWarp && kProdWarp < kMmaWarp &&
-                  kMmaWarp == kPgThreads / 32 - 1,
+                  kMmaWarp + kMmaWarps == kPgThreads / 32,
               "warp roles must not overlap");
 static_assert(kDqWarps * 32 == 128, "one dequantising thread per A row");
 template <int MODE>
-constexpr int kNSC = MODE == 0 ? 16 : 14;  // code stages (8 KB each)
+constexpr int kNSC = MODE == 0 ? 16 : 10;  // code stages (8 KB each)
 template <int MODE>
-constexpr int kNSB = 3;  // activation (B) stages: stage c % 3 is free once chunk c - 3 is done
-constexpr int kNSA = 2;                  // A stages (in TMEM)
+constexpr int kNSB = 4;  // activation (B) stages
+constexpr int kNSA = 4;                  // A stages (in TMEM)
+
 constexpr int kCodesStage = 128 * 64;    // 128 rows x 64 B (128 codes)
 constexpr int kACols = 64;               // TMEM columns of one A stage: 128 bf16 per row
-constexpr int kTmemBufs = 3;             // accumulator buffers: 2 groups x 64 columns each
-static_assert(kNSB<0> == kTmemBufs && kNSB<1> == kTmemBufs && kNSA < kTmemBufs,
-              "operand stages are released by the accumulator-full barrier of an earlier chunk");
+constexpr int kTmemBufs = 2;             // accumulator buffers: 2 groups x 64 columns each
 constexpr int kACol0 = kTmemBufs * 128;  // A stages follow the accumulators
 constexpr int kTmemCols = 512;
 static_assert(kACol0 + kNSA * kACols <= kTmemCols, "TMEM columns");
@@ -371,7 +372,7 @@ __device__ __forceinline__ uint32_t codes_bf16x2(uint32_t v) {
   return r;
 }
 
-// 11 warps put three warps on some SM sub-partitions: 168 registers each.
+// 12 warps put three warps on each SM sub-partition: 168 registers each.
 template <int MODE>
 __global__ void __maxnreg__(168)
     pf_gemm_kernel(const __grid_constant__ LayerArgs a, const __grid_constant__ PfMaps maps) {
@@ -385,8 +386,10 @@ __global__ void __maxnreg__(168)
   uint64_t* codes_full = bars;
   uint64_t* codes_empty = codes_full + kNSC<MODE>;
   uint64_t* a_full = codes_empty + kNSC<MODE>;
-  uint64_t* b_full = a_full + kNSA;
-  uint64_t* tm_full = b_full + kNSB<MODE>;
+  uint64_t* a_empty = a_full + kNSA;
+  uint64_t* b_full = a_empty + kNSA;
+  uint64_t* b_empty = b_full + kNSB<MODE>;
+  uint64_t* tm_full = b_empty + kNSB<MODE>;
   uint64_t* tm_empty = tm_full + kTmemBufs;
   uint64_t* gs_full = tm_empty + kTmemBufs;
   uint64_t* gs_empty = gs_full + kNSG;
@@ -397,8 +400,8 @@ __global__ void __maxnreg__(168)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
     for (int i = 0; i < kNSC<MODE>; ++i) mbar_init(&codes_full[i], 1), mbar_init(&codes_empty[i], kDqWarps);
-    for (int i = 0; i < kNSA; ++i) mbar_init(&a_full[i], kDqWarps);
-    for (int i = 0; i < kNSB<MODE>; ++i) mbar_init(&b_full[i], 1);
+    for (int i = 0; i < kNSA; ++i) mbar_init(&a_full[i], kDqWarps), mbar_init(&a_empty[i], 1);
+    for (int i = 0; i < kNSB<MODE>; ++i) mbar_init(&b_full[i], 1), mbar_init(&b_empty[i], 1);
     for (int i = 0; i < kTmemBufs; ++i) mbar_init(&tm_full[i], 1), mbar_init(&tm_empty[i], kEpiWarps);
     for (int i = 0; i < kNSG; ++i) mbar_init(&gs_full[i], 1), mbar_init(&gs_empty[i], kEpiWarps);
     *s_abort = 0;
@@ -478,9 +481,7 @@ __global__ void __maxnreg__(168)
       if (!pg_item<MODE>(a, it, nblk, nsb, I)) break;
       bool stop = false;
       for (int c = 0; c < I.nch; ++c, ++cc, pc.next(kNSC<MODE>), pa.next(kNSA)) {
-        // A stage cc % 2 is free once chunk cc - 2's MMAs completed (its
-        // accumulator-full phase; chunk cc + 1 cannot have completed yet)
-        if (cc >= kNSA && !pg_wait_warp(&tm_full[(cc - kNSA) % kTmemBufs], ((cc - kNSA) / kTmemBufs) & 1u, s_abort, err)) {
+        if (cc >= kNSA && !pg_wait_warp(&a_empty[pa.s], pa.ph ^ 1u, s_abort, err)) {
           stop = true;
           break;
         }
@@ -532,9 +533,7 @@ __global__ void __maxnreg__(168)
         if (!pg_item<MODE>(a, it, nblk, nsb, I)) break;
         const int np = I.blk.np;
         for (int c = 0; c < I.nch; ++c, pb.next(kNSB<MODE>)) {
-          // B stage issued % 3 is free once chunk issued - 3 completed
-          if (issued >= kNSB<MODE> &&
-              !pg_wait(&tm_full[(issued - kNSB<MODE>) % kTmemBufs], ((issued - kNSB<MODE>) / kTmemBufs) & 1u, s_abort, err)) {
+          if (issued >= kNSB<MODE> && !pg_wait(&b_empty[pb.s], pb.ph ^ 1u, s_abort, err)) {
             stop = true;
             break;
           }
@@ -557,11 +556,15 @@ __global__ void __maxnreg__(168)
         if (!mbar_wait(&b_full[j % kNSB<MODE>], (j / kNSB<MODE>) & 1)) latch_error(err, kErrTimeout);
     }
     __syncwarp();
-  } else if (warp == kMmaWarp) {
+  } else if (warp >= kMmaWarp) {
     // ------------------------------------------------------------ MMA issue
+    // Two issuing threads: one thread can issue a tcgen05.mma only every
+    // ~50 cycles, two together about every 30.  Issuer mi takes the chunks
+    // with index % 2 == mi; both track every ring.
+    const int mi = warp - kMmaWarp;
     if (lane == 0) {
       RingPos pa, pb, pt;
-      int cc = 0;
+      int cc = 0, last = -1;
       bool stop = false;
       for (int it = blockIdx.x; it < n_items && !stop; it += gridDim.x) {
         PgItem I;
@@ -569,6 +572,7 @@ __global__ void __maxnreg__(168)
         const int np = I.blk.np;
         const uint32_t idesc = idesc_bf16_f32(128, np);
         for (int c = 0; c < I.nch; ++c, ++cc, pa.next(kNSA), pb.next(kNSB<MODE>), pt.next(kTmemBufs)) {
+          if ((cc % kMmaWarps) != mi) continue;
           if (!pg_wait(&a_full[pa.s], pa.ph, s_abort, err) || !pg_wait(&b_full[pb.s], pb.ph, s_abort, err) ||
               (cc >= kTmemBufs && !pg_wait(&tm_empty[pt.s], pt.ph ^ 1u, s_abort, err))) {
             stop = true;
@@ -590,11 +594,16 @@ __global__ void __maxnreg__(168)
               if (MODE == 1) mma_bf16_ta(d, a0 + kq * 8, bd_lo + kq * bstep, idesc, 1u);
             }
           }
-          mma_commit(smem_u32(&tm_full[pt.s]));  // also frees this chunk's A and B stages
+          mma_commit(smem_u32(&a_empty[pa.s]));
+          mma_commit(smem_u32(&b_empty[pb.s]));
+          mma_commit(smem_u32(&tm_full[pt.s]));
+          last = cc;
         }
       }
-      // the last commits have landed before TMEM is released
-      if (cc > 0 && !mbar_wait(&tm_full[(cc - 1) % kTmemBufs], ((cc - 1) / kTmemBufs) & 1))
+      // Normally the epilogue has consumed every accumulator (so every MMA
+      // completed) before the final barrier; after an abort, this issuer's
+      // last chunk lands before TMEM is released.
+      if (*s_abort && last >= 0 && !mbar_wait(&tm_full[last % kTmemBufs], (last / kTmemBufs) & 1))
         latch_error(err, kErrTimeout);
     }
     __syncwarp();
