@@ -26,6 +26,7 @@ cudaError_t launch_decode(const LayerArgs& a, int num_sms, cudaStream_t st);
 cudaError_t set_prefill_attributes(int smem_optin);
 cudaError_t launch_prefill(const LayerArgs& a, const LayerMaps* maps, int num_sms, cudaStream_t st);
 cudaError_t build_layer_maps(const LayerArgs& a, LayerMaps* out);
+bool prefill_tc_ok(const LayerArgs& a, int T);
 size_t prefill_workspace_bytes(const LayerArgs& a, int T);
 }  // namespace moe
 
@@ -299,11 +300,13 @@ static int prepare(moe_layer* L, const uint16_t* x, int32_t T, uint16_t* ob, flo
   return MOE_OK;
 }
 
-// Decode batches whose tokens are expected to share almost no routed expert
-// (B * top_k <= E / 2: with uniform routing at most ~1/4 of a token's
-// experts are expected to repeat) run one single-token pass per token.
+// Decode batches with B * top_k <= E (with uniform routing fewer than ~40%
+// of the pairs repeat an expert) run one single-token pass per token: the
+// single-token kernels stream weights several times faster than the grouped
+// ones, which outweighs the repeated reads.  Measured at H=7168, E=512,
+// top-16: B=32 per token 2.9 ms vs 4.3 ms on the tensor-core kernels.
 static bool per_token_decode(const moe_layer* L, int T) {
-  return T > 1 && T <= 16 && static_cast<long>(T) * L->d.top_k * 2 <= L->d.n_experts;
+  return T > 1 && T <= 64 && static_cast<long>(T) * L->d.top_k <= L->d.n_experts;
 }
 
 static int run(moe_layer* L, const uint16_t* x, int32_t T, uint16_t* ob, float* of, int32_t* ids,
@@ -330,6 +333,10 @@ static int run(moe_layer* L, const uint16_t* x, int32_t T, uint16_t* ob, float* 
       b.prof_on = t == 0 ? a.prof_on : 0;  // the profiling hook times the first token's kernels
       e = moe::launch_decode_b1(b, L->num_sms, st);
     }
+  } else if (moe::prefill_tc_ok(a, T) && L->maps.valid) {
+    // Larger batches: the tensor-core kernels of the prefill chunk compute
+    // the same layer with each expert's weights read once for all its tokens.
+    e = moe::launch_prefill(a, &L->maps, L->num_sms, st);
   } else {
     e = moe::launch_decode(a, L->num_sms, st);
   }

@@ -200,7 +200,7 @@ def mid():
     return wl, hl, hl.oracle(), device_from_host(hl, max_tokens=128)
 
 
-@pytest.mark.parametrize("B", [1, 4, 16])
+@pytest.mark.parametrize("B", [1, 4, 16, 32, 64])
 def test_mid_decode(mid, B):
     wl, hl, orc, dl = mid
     xs = draw_tokens(orc, wl.input_seed, 100 + B, B)
@@ -255,7 +255,7 @@ def _oracle_with_records(orc, wl, ids):
             orc.set_record(e, synth.expert_record(wl.weight_seed, 0, e, s.H, s.F))
 
 
-@pytest.mark.parametrize("B,sample", [(1, [0]), (4, [0, 3]), (16, [0, 9, 15])])
+@pytest.mark.parametrize("B,sample", [(1, [0]), (4, [0, 3]), (16, [0, 9, 15]), (32, [0, 31]), (64, [5, 63])])
 def test_large_decode(large, B, sample):
     wl, dl, orc = large
     xs = draw_tokens(orc, wl.input_seed, 200 + B, B)
