@@ -221,9 +221,10 @@ static size_t carve(const moe_layer* L, int T, moe::Workspace* ws, uint8_t* base
                Fs = L->d.shared_ffn, t = static_cast<size_t>(T);
   Carve c;
   const size_t o_ctl = c.take(64 * 4);
-  // single-token fixed-point h: k routed rows of F and the shared row of Fs
-  const size_t hchunks = k * (F / 32) + Fs / 32, hpad = (hchunks + 3) / 4 * 4;
-  const size_t o_hx = c.take(hchunks * 64), o_hxs = c.take(hpad * 4), o_hxm = c.take(hpad * 4);
+  // single-token fixed-point h: k routed rows of F and the shared row of Fs;
+  // per 32-value chunk 64 bytes of words and 4 group scales and sums
+  const size_t hchunks = k * (F / 32) + Fs / 32;
+  const size_t o_hx = c.take(hchunks * 64), o_hxs = c.take(hchunks * 16), o_hxm = c.take(hchunks * 16);
   const size_t o_log = c.take(t * E * 4);
   const size_t o_nact = c.take(16);
   const size_t o_ae = c.take(E * 4), o_ao = c.take(E * 4), o_ac = c.take(E * 4);

@@ -15,11 +15,13 @@
 // are exact.
 //
 // gateup_b1_kernel  each consumer thread converts its chunk of the token's
-//                   hidden state; items are streamed as in decode.cu, and the last
-//                   warp to finish an item (shared-memory counter) applies
-//                   SwiGLU, so consumer warps never meet at a barrier.
-// down_b1_kernel    converts the step's h rows (one per active expert) once
-//                   per CTA into shared memory, then streams the CTA's row
+//                   hidden state; items are streamed as in decode.cu.  An
+//                   epilogue warp gathers each item's row sums, applies
+//                   SwiGLU and writes the item's h values as fixed-point
+//                   8-value groups, each with its own exponent, so consumer
+//                   warps never meet at a barrier or wait on an epilogue.
+// down_b1_kernel    copies each expert's fixed-point h block into a small
+//                   ring ahead of its weight tiles and streams the CTA's row
 //                   tiles expert by expert; partial sums stay in registers
 //                   across experts (weighted by p_i), one reduction per tile.
 // router_b1_kernel  8-bit router rows (float path); top-k by repeated warp
@@ -279,49 +281,63 @@ size_t router_b1_smem_bytes(int E) {
 
 constexpr int kG1Warps = 16;
 
+constexpr int kG1Threads = (kG1Warps + 2) * 32;  // consumers, producer, epilogue warp
+
 struct G1Smem {  // byte offsets of the dynamic shared-memory carve
-  int wsum, cnt, item, bars, total;
+  int wsum, item, bars, total;
 };
 
 __host__ __device__ inline G1Smem g1_smem(int nst, int stage, int rows) {
   G1Smem s;
   s.wsum = nst * stage;
-  s.cnt = s.wsum + nst * kG1Warps * rows * 4;  // [NST] warps done per item
-  s.item = s.cnt + 64;                          // [NST] item index held by the stage
+  s.item = s.wsum + nst * kG1Warps * rows * 4;  // [NST] item index held by the stage
   s.bars = s.item + 64;
-  s.total = s.bars + 2 * nst * 8 + 16;
+  s.total = s.bars + 3 * nst * 8 + 16;          // full, empty, partial sums done
   return s;
 }
 
-// Converts chunk c of a fixed-point h row (lane m holds value m) and
-// publishes its words, scale and sum for the down kernel's shared memory.  The layout matches down_b1's shared-memory copy: uint4 g
-// (eh, el, oh, ol) of chunk c of a row starting at chunk c0 with nc chunks
-// sits at index c0*4 + g*nc + c.
-__device__ __forceinline__ void publish_hchunk(const LayerArgs& a, int c0, int nc, int c, float v, int lane) {
-  const float amax = warp_max(fabsf(v));
-  const float scale = fixed_scale(amax);
-  const int X = to_fixed(v, 1.f / scale);
-  float sum = v;
+// Writes the fixed-point form of one 8-value group of an h row.  The warp's
+// 8-lane segments hold groups: lane 8g + p holds element f (f = 8 * (group)
+// + p) of the row with value v (0 where `act` is false).  The row's chunks
+// start at chunk c0 and number nc.  Layout, as the down kernel copies it:
+// the word of kind K (0: high bytes of the even elements, 1: their low
+// bytes, 2 and 3: the same for the odd elements) of group i of chunk c sits
+// at 32-bit word ((c0 * 4 + K * nc + c) * 4 + i); the group's 2^e and plain
+// sum at float (c0 + c) * 4 + i of hx_scale and hx_sum.
+__device__ __forceinline__ void publish_hgroup(const LayerArgs& a, int c0, int nc, int f, float v, bool act,
+                                               int lane) {
+  float amax = fabsf(v), sum = v;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(kAll, sum, o);
-  // lane L < 16 builds word i = L & 3 of group g = L >> 2: bytes b = 0..3 are
-  // activations 8i + p + 2b (p = parity), high byte for g even, low for g odd
-  const int g = (lane >> 2) & 3, i = lane & 3, par = g >> 1, hi = (g & 1) == 0;
+  for (int o = 4; o > 0; o >>= 1) {
+    amax = fmaxf(amax, __shfl_xor_sync(kAll, amax, o));
+    sum += __shfl_xor_sync(kAll, sum, o);
+  }
+  // 2^e with amax / 2^e < 2^15 and its inverse, straight from amax's
+  // exponent field (the same 2^e as fixed_scale for amax >= 2^-112; below
+  // that, 2^-126, which keeps |v| / 2^e < 2^15)
+  const int eb = max(static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu), 15);
+  const float scale = __uint_as_float(static_cast<uint32_t>(eb - 14) << 23);
+  const float inv = __uint_as_float(static_cast<uint32_t>(268 - eb) << 23);
+  const int X = min(max(__float2int_rn(v * inv), -32767), 32767);
+  // lane p < 4 of the segment builds the word of kind p from elements
+  // par + 2b (b = 0..3) of the group, par = p >> 1
+  const int base = lane & ~7, p = lane & 7, par = (p >> 1) & 1, hi = (p & 1) == 0;
   int byte[4];
 #pragma unroll
   for (int b = 0; b < 4; ++b) {
-    const int xv = __shfl_sync(kAll, X, 8 * i + par + 2 * b);
+    const int xv = __shfl_sync(kAll, X, base + par + 2 * b);
     byte[b] = hi ? (xv >> 8) : xv;
   }
-  if (lane < 16) {
+  if (act && p < 4) {
+    const int c = f >> 5, i = (f >> 3) & 3;
     uint32_t* words = reinterpret_cast<uint32_t*>(a.ws.hx);
-    words[(static_cast<size_t>(c0) * 4 + g * nc + c) * 4 + i] = pack4(byte[0], byte[1], byte[2], byte[3]);
+    words[(static_cast<size_t>(c0) * 4 + p * nc + c) * 4 + i] = pack4(byte[0], byte[1], byte[2], byte[3]);
+    if (p == 0) a.ws.hx_scale[(c0 + c) * 4 + i] = scale, a.ws.hx_sum[(c0 + c) * 4 + i] = sum;
   }
-  if (lane == 0) a.ws.hx_scale[c0 + c] = scale, a.ws.hx_sum[c0 + c] = sum;
 }
 
 template <int R>  // rows per thread per item: R/2 gate + R/2 up
-__global__ void __launch_bounds__((kG1Warps + 1) * 32, 1) gateup_b1_kernel(const __grid_constant__ LayerArgs a) {
+__global__ void __launch_bounds__(kG1Threads, 1) gateup_b1_kernel(const __grid_constant__ LayerArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr int NCW = kG1Warps;
   const int H = a.H, C = H >> 5, WC = (C + 31) >> 5, NRL = a.gu_nrl, NAW = NRL * WC;
@@ -330,14 +346,14 @@ __global__ void __launch_bounds__((kG1Warps + 1) * 32, 1) gateup_b1_kernel(const
   const int NST = a.gu_nst, SB = a.gu_stage;
   const G1Smem L = g1_smem(NST, SB, R);
   float* wsum = reinterpret_cast<float*>(smem + L.wsum);  // [NST][NCW][R]
-  int* s_cnt = reinterpret_cast<int*>(smem + L.cnt);      // [NST]
   volatile int* s_item = reinterpret_cast<volatile int*>(smem + L.item);  // [NST]
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
-  uint64_t* empty = full + NST;
+  uint64_t* empty = full + NST;  // consumers and the epilogue warp are done with a stage
+  uint64_t* pdone = empty + NST;  // every consumer's partial sums of the stage's item are in
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
-    for (int s = 0; s < NST; ++s) mbar_init(&full[s], 1), mbar_init(&empty[s], NAW), s_cnt[s] = 0;
+    for (int s = 0; s < NST; ++s) mbar_init(&full[s], 1), mbar_init(&empty[s], NAW + 1), mbar_init(&pdone[s], NAW);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
@@ -405,6 +421,55 @@ __global__ void __launch_bounds__((kG1Warps + 1) * 32, 1) gateup_b1_kernel(const
     return;
   }
 
+  if (warp == NCW + 1) {  // ---------------- epilogue warp
+    // Per item, in ring order: gather the gate and up sums of the item's
+    // rows (at most 64: two per lane), release the stage, then SwiGLU and
+    // the fixed-point h groups, off the consumers' path.
+    RingPos pos;
+    for (;; pos.next(NST)) {
+      const int s = pos.s;
+      if (!mbar_wait_warp(&full[s], pos.ph)) {
+        if (lane == 0) latch_error(&a.ws.ctl[0], kErrTimeout);
+        break;
+      }
+      const int i = s_item[s];
+      if (i < 0) break;  // the producer ran out of items
+      if (!mbar_wait_warp(&pdone[s], pos.ph)) {
+        if (lane == 0) latch_error(&a.ws.ctl[0], kErrTimeout);
+        break;
+      }
+      float gs[2] = {0.f, 0.f}, us[2] = {0.f, 0.f};
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int j = q * 32 + lane;
+        if (j < rth) {
+          const int rlj = j / RH, mj = j % RH;
+          for (int w = 0; w < WC; ++w) {
+            const float* ws = wsum + (s * NCW + rlj * WC + w) * R;
+            gs[q] += ws[mj];
+            us[q] += ws[RH + mj];
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+      // entry idx of the step (shared expert first, then the active experts
+      // in ascending id) owns h chunks c0 .. c0 + nc - 1; the item's rth
+      // rows (a multiple of 8) are whole groups
+      const int idx = i < tiles_s ? 0 : has_sh + (i - tiles_s) / tiles_r;
+      const int tile = i < tiles_s ? i : (i - tiles_s) % tiles_r;
+      const bool sh_row = has_sh && idx == 0;
+      const int nc = (sh_row ? a.Fs : a.F) >> 5;
+      const int c0 = sh_row ? 0 : has_sh * (a.Fs >> 5) + (idx - has_sh) * (a.F >> 5);
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int j = q * 32 + lane;
+        if (q * 32 < rth) publish_hgroup(a, c0, nc, tile * rth + j, silu1(gs[q]) * us[q], j < rth, lane);
+      }
+    }
+    return;
+  }
+
   // ---------------------------------------------------- consumers
   const int rl = warp / WC, wc = warp % WC, col = wc * 32 + lane;
   const bool has_col = col < C;
@@ -427,7 +492,6 @@ __global__ void __launch_bounds__((kG1Warps + 1) * 32, 1) gateup_b1_kernel(const
   XChunk X;
   const float scale = make_xchunk_own(xv, X);
 
-  bool waited = false;
   RingPos pos;
   for (;; pos.next(NST)) {
     const int s = pos.s;
@@ -456,35 +520,10 @@ __global__ void __launch_bounds__((kG1Warps + 1) * 32, 1) gateup_b1_kernel(const
     if constexpr (R == 8) v = bfly8(part, lane);
     else v = bfly4b(part, lane);
     if ((lane & (LPR - 1)) == 0) wsum[(s * NCW + warp) * R + lane / LPR] = v;
-    __threadfence_block();
-    __syncwarp();
-    int last = 0;
-    if (lane == 0) last = (atomicAdd(&s_cnt[s], 1) == NAW - 1);
-    last = __shfl_sync(kAll, last, 0);
-    if (last) {  // every warp's sums for this item are in: SwiGLU, store h
-      __threadfence_block();
-      if (i >= tiles_s && !waited) pdl_wait(), waited = true;
-      const int idx = i < tiles_s ? 0 : has_sh + (i - tiles_s) / tiles_r;
-      const int tile = i < tiles_s ? i : (i - tiles_s) % tiles_r;
-      const B1Entry en = b1_entry(a, idx, has_sh);
-      float* hout = en.shared ? a.ws.h_shared : a.ws.h + static_cast<size_t>(en.pair) * a.F;
-      for (int j = lane; j < rth; j += 32) {
-        const int rlj = j / RH, mj = j % RH;
-        float g = 0.f, u = 0.f;
-        for (int w = 0; w < WC; ++w) {
-          const float* ws = wsum + (s * NCW + rlj * WC + w) * R;
-          g += ws[mj];
-          u += ws[RH + mj];
-        }
-        hout[tile * rth + j] = silu1(g) * u;
-      }
-      __syncwarp();
-      if (lane == 0) s_cnt[s] = 0;
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
+    __syncwarp();  // the lanes' sums before lane 0's arrivals (release at CTA scope)
+    if (lane == 0) mbar_arrive(&pdone[s]), mbar_arrive(&empty[s]);
   }
-  if (!waited) pdl_wait();
+  pdl_wait();  // the grid completes after the router's, which the down kernel relies on
 }
 
 size_t gateup_b1_smem_bytes(const LayerArgs& a, int rows) {
@@ -492,11 +531,14 @@ size_t gateup_b1_smem_bytes(const LayerArgs& a, int rows) {
 }
 
 // ============================================================================
-// down + combine (B = 1).  Prologue: a table of the step's experts (shared
-// expert first, then active experts in ascending id: record, width, h row,
-// routing weight); their h rows become fixed-point chunks (spread over the
-// grid, then a grid-wide barrier) that each CTA copies into shared memory.
-// Main loop: experts outer, this CTA's row tiles of H inner (at most
+// down + combine (B = 1).  Prologue: the producer streams the shared
+// expert's first tiles before the dependency on gate|up (its weights need no
+// routing); then a table of the step's experts (shared expert first, then
+// active experts in ascending id: record, width, fixed-point h chunks,
+// routing weight).  Each expert's fixed-point h block (written by gate|up, a
+// few KB) is bulk-copied into a small ring of its own ahead of the expert's
+// weight tiles, so the weight ring gets nearly all of shared memory.  Main
+// loop: experts outer, this CTA's row tiles of H inner (at most
 // kD1MaxTiles), so a thread loads its activation chunk once per expert.  A
 // thread owns column `col` and rows rl + NRL*m (m < 2) of every tile for
 // each expert width; the weighted sums stay in registers until the end,
@@ -506,6 +548,8 @@ size_t gateup_b1_smem_bytes(const LayerArgs& a, int rows) {
 constexpr int kD1Warps = 16;
 constexpr int kD1MaxTiles = 4;  // row tiles per CTA
 constexpr int kD1Rpt = 2;       // rows per thread per tile and expert width
+constexpr int kD1XSlots = 3;    // fixed-point h blocks in flight
+constexpr int kD1MaxStages = 16;
 
 struct D1Entry {        // one expert of the step, as the down kernel uses it
   const uint8_t* rec;   // record base
@@ -516,20 +560,20 @@ struct D1Entry {        // one expert of the step, as the down kernel uses it
 };
 
 struct D1Smem {
-  int ent, xform, xsum, xscale, wsum, bars, total;
+  int ent, xring, xslot, wsum, bars, total;
 };
 
-// rows: h rows of the step; cols_total: sum over rows of F_row / 32.
-__host__ __device__ inline D1Smem d1_smem(int nst, int stage, int rows, int cols_total) {
+// rows: h rows of the step; ncmax: chunks of the widest h row.  An h slot
+// holds [4 kinds][nc] uint4 words, then nc float4 group scales at
+// 64 * ncmax, then nc float4 group sums at 80 * ncmax.
+__host__ __device__ inline D1Smem d1_smem(int nst, int stage, int rows, int ncmax) {
   D1Smem s;
   s.ent = nst * stage;
-  s.xform = s.ent + ((rows * static_cast<int>(sizeof(D1Entry)) + 127) / 128) * 128;
-  const int cpad = (cols_total + 3) / 4 * 4;
-  s.xsum = s.xform + cols_total * 64;          // float per chunk
-  s.xscale = s.xsum + cpad * 4;                // float per chunk
-  s.wsum = s.xscale + cpad * 4;
+  s.xring = s.ent + ((rows * static_cast<int>(sizeof(D1Entry)) + 127) / 128) * 128;
+  s.xslot = (96 * ncmax + 127) / 128 * 128;
+  s.wsum = s.xring + kD1XSlots * s.xslot;
   s.bars = s.wsum + kD1MaxTiles * kD1Warps * 4 * 4;  // [tile][warp][4]
-  s.total = s.bars + (2 * nst + 1) * 8 + 16;          // full, empty, fixed-point h
+  s.total = s.bars + (2 * nst + 2 * kD1XSlots) * 8 + 16;  // full, empty, h full, h empty
   return s;
 }
 
@@ -553,28 +597,44 @@ __device__ __forceinline__ D1Geo d1_geo(int Fe, int warp, int lane) {
 
 __global__ void __launch_bounds__((kD1Warps + 1) * 32, 1) down_b1_kernel(const __grid_constant__ LayerArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
-  constexpr int NCW = kD1Warps, NCT = NCW * 32;
-  const int H = a.H, RT = a.dn_rt, NST = a.dn_nst, SB = a.dn_stage, k = a.k;
+  constexpr int NCW = kD1Warps, NCT = NCW * 32, NX = kD1XSlots;
+  const int RT = a.dn_rt, NST = a.dn_nst, SB = a.dn_stage, k = a.k;
   const int has_sh = a.Fs > 0 ? 1 : 0;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int max_rows = k + has_sh;
-  const int max_cols = k * (a.F / 32) + has_sh * (a.Fs / 32);
-  const D1Smem L = d1_smem(NST, SB, max_rows, max_cols);
+  const int ncmax = max(a.F, a.Fs) >> 5;
+  const D1Smem L = d1_smem(NST, SB, max_rows, ncmax);
   D1Entry* ent = reinterpret_cast<D1Entry*>(smem + L.ent);
-  uint4* xform = reinterpret_cast<uint4*>(smem + L.xform);
-  float* xsum = reinterpret_cast<float*>(smem + L.xsum);
-  float* xscale = reinterpret_cast<float*>(smem + L.xscale);
+  uint8_t* xring = smem + L.xring;
   float* wsum = reinterpret_cast<float*>(smem + L.wsum);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* empty = full + NST;
-  uint64_t* xbar = empty + NST;  // fixed-point h block landed
+  uint64_t* xfull = empty + NST;  // fixed-point h block of an expert landed
+  uint64_t* xempty = xfull + NX;  // ... and read by every consumer warp
 
   if (tid == 0) {
     for (int s = 0; s < NST; ++s) mbar_init(&full[s], 1), mbar_init(&empty[s], NCW);
-    mbar_init(xbar, 1);
+    for (int s = 0; s < NX; ++s) mbar_init(&xfull[s], 1), mbar_init(&xempty[s], NCW);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  __syncthreads();
   pdl_launch_dependents();
+  // this CTA's tiles: blockIdx.x + t * gridDim.x, t < ntc (<= kD1MaxTiles by plan)
+  const int n_tiles = a.dn_tiles;
+  const int ntc = blockIdx.x < n_tiles ? min(kD1MaxTiles, (n_tiles - 1 - blockIdx.x) / gridDim.x + 1) : 0;
+  const uint64_t pol = policy_evict_first();
+  // the shared expert's tiles (entry 0) go out before the dependency wait
+  const int pre = has_sh ? min(ntc, NST) : 0;
+  if (warp == NCW && lane == 0) {
+    const uint32_t cb = RT * (a.Fs / 2), sbb = RT * (a.Fs / 16);
+    for (int t = 0; t < pre; ++t) {
+      const size_t r0 = static_cast<size_t>(blockIdx.x + t * gridDim.x) * RT;
+      uint8_t* st = smem + t * SB;
+      mbar_arrive_expect_tx(&full[t], cb + sbb);
+      bulk_g2s(st, a.shared + a.off_s.down_codes + r0 * (a.Fs / 2), cb, &full[t], pol);
+      bulk_g2s(st + cb, a.shared + a.off_s.down_sb + r0 * (a.Fs / 16), sbb, &full[t], pol);
+    }
+  }
   pdl_wait();  // fixed-point h, routing and weights are ready past this point
   if (blockIdx.x == 0 && tid == 0) a.ws.ctl[2] = 0u;  // gate|up claims: back to zero
   const int n_ent = min(clamp_n_act(a) + has_sh, max_rows);
@@ -593,22 +653,33 @@ __global__ void __launch_bounds__((kD1Warps + 1) * 32, 1) down_b1_kernel(const _
     }
   }
   __syncthreads();
-  // this CTA's tiles: blockIdx.x + t * gridDim.x, t < ntc (<= kD1MaxTiles by plan)
-  const int n_tiles = a.dn_tiles;
-  const int ntc = blockIdx.x < n_tiles ? min(kD1MaxTiles, (n_tiles - 1 - blockIdx.x) / gridDim.x + 1) : 0;
-  const int n_cols = n_ent > 0 ? ent[n_ent - 1].c0 + ent[n_ent - 1].Fe / 32 : 0;
 
-  if (warp == NCW) {  // ---------------- producer warp: expert weights, ahead of h
+  if (warp == NCW) {  // ---------------- producer warp: h blocks and expert weights
     if (lane == 0) {
-      const uint64_t pol = policy_evict_first();
-      int it = 0;
+      // the h words were written by the gate|up grid through the generic
+      // proxy; the bulk copies read them through the async proxy
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      int it = 0, jx = 0;
       bool stop = false;
       RingPos pos;
       for (int j = 0; j < n_ent && !stop; ++j) {
         const D1Entry d = ent[j];
+        const int xs = j % NX, nc = d.Fe / 32;
+        if (j >= NX && !mbar_wait(&xempty[xs], ((j / NX) & 1) ^ 1u)) {
+          latch_error(&a.ws.ctl[0], kErrTimeout);
+          break;
+        }
+        uint8_t* xb = xring + xs * L.xslot;
+        mbar_arrive_expect_tx(&xfull[xs], 96 * nc);
+        // every CTA reads these blocks: no evict-first hint
+        bulk_g2s(xb, a.ws.hx + static_cast<size_t>(d.c0) * 4, 64 * nc, &xfull[xs]);
+        bulk_g2s(xb + 64 * ncmax, a.ws.hx_scale + static_cast<size_t>(d.c0) * 4, 16 * nc, &xfull[xs]);
+        bulk_g2s(xb + 80 * ncmax, a.ws.hx_sum + static_cast<size_t>(d.c0) * 4, 16 * nc, &xfull[xs]);
+        jx = j + 1;
         const RecordOffsets& off = d.expert < 0 ? a.off_s : a.off_r;
         const uint32_t cb = RT * (d.Fe / 2), sbb = RT * (d.Fe / 16);
         for (int t = 0; t < ntc; ++t, ++it, pos.next(NST)) {
+          if (j == 0 && t < pre) continue;  // issued before the dependency wait
           const int s = pos.s;
           if (it >= NST && !mbar_wait(&empty[s], pos.ph ^ 1u)) {
             latch_error(&a.ws.ctl[0], kErrTimeout);
@@ -622,84 +693,51 @@ __global__ void __launch_bounds__((kD1Warps + 1) * 32, 1) down_b1_kernel(const _
           bulk_g2s(st + cb, d.rec + off.down_sb + r0 * (d.Fe / 16), sbb, &full[s], pol);
         }
       }
+      // copies in flight land before exit
       for (int j = max(0, it - NST); j < it; ++j)
         if (!mbar_wait(&full[j % NST], (j / NST) & 1)) latch_error(&a.ws.ctl[0], kErrTimeout);
-      if (!mbar_wait(xbar, 0)) latch_error(&a.ws.ctl[0], kErrTimeout);
+      for (int j = max(0, jx - NX); j < jx; ++j)
+        if (!mbar_wait(&xfull[j % NX], (j / NX) & 1)) latch_error(&a.ws.ctl[0], kErrTimeout);
     }
     return;
   }
 
-  // ---- phase 0 (consumer warps): the step's h rows become fixed-point
-  // chunks, one chunk per warp across the grid; then a grid-wide barrier (a
-  // 64-bit arrival counter that only grows: this call's target is the next
-  // multiple of the grid size; every CTA is resident, one per SM, so the
-  // wait is bounded by the slowest CTA's phase 0; on a 2 s timeout the error
-  // is latched); then thread 0 copies the whole fixed-point block into
-  // shared memory.
-  for (int gc = blockIdx.x * NCW + warp; gc < n_cols; gc += gridDim.x * NCW) {
-    int j = 0;
-    while (j + 1 < n_ent && ent[j + 1].c0 <= gc) ++j;
-    const D1Entry d = ent[j];
-    const float* hrow = d.expert < 0 ? a.ws.h_shared : a.ws.h + static_cast<size_t>(j - has_sh) * a.F;
-    const int c = gc - d.c0;
-    publish_hchunk(a, d.c0, d.Fe / 32, c, __ldcg(hrow + c * 32 + lane), lane);
-  }
-  named_bar(2, NCT);
-  if (tid == 0) {
-    __threadfence();
-    unsigned long long* gb = reinterpret_cast<unsigned long long*>(a.ws.ctl + 4);
-    const unsigned long long old = atomicAdd(gb, 1ull);
-    const unsigned long long target = (old / gridDim.x + 1) * gridDim.x;
-    const unsigned long long t0 = global_timer_ns();
-    while (*reinterpret_cast<volatile unsigned long long*>(gb) < target) {
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
-        latch_error(&a.ws.ctl[0], kErrTimeout);
-        break;
-      }
-    }
-    __threadfence();
-    // the chunks were written through the generic proxy; the bulk copy reads
-    // them through the async proxy
-    asm volatile("fence.proxy.async.global;" ::: "memory");
-    if (n_cols > 0) {
-      const uint32_t xb = n_cols * 64, sb4 = ((n_cols + 3) / 4) * 16;
-      mbar_arrive_expect_tx(xbar, xb + 2 * sb4);
-      bulk_g2s(xform, a.ws.hx, xb, xbar);
-      bulk_g2s(xscale, a.ws.hx_scale, sb4, xbar);
-      bulk_g2s(xsum, a.ws.hx_sum, sb4, xbar);
-    } else {
-      mbar_arrive(xbar);
-    }
-  }
-
-  // ---- the fixed-point h block lands
-  bool abort = !mbar_wait_warp(xbar, 0);
-  if (abort && lane == 0) latch_error(&a.ws.ctl[0], kErrTimeout);
-  (void)H;
-  // ---- main loop: experts outer, tiles inner
+  // ---- main loop (consumer warps): experts outer, tiles inner
   const D1Geo gs = d1_geo(has_sh ? a.Fs : a.F, warp, lane), gr = d1_geo(a.F, warp, lane);
   float acc[kD1MaxTiles][2 * kD1Rpt];  // [tile][shared rows m, routed rows m]
 #pragma unroll
   for (int t = 0; t < kD1MaxTiles; ++t)
 #pragma unroll
     for (int m = 0; m < 2 * kD1Rpt; ++m) acc[t][m] = 0.f;
+  bool abort = false;  // this warp gave up a wait; acted on at the final barrier
   RingPos pos;
-  for (int j = 0; j < n_ent; ++j) {  // `abort`: this warp gave up a wait; acted on at the final barrier
+  for (int j = 0; j < n_ent; ++j) {
     const D1Entry d = ent[j];
     const bool sh = d.expert < 0;
     const D1Geo& g = sh ? gs : gr;
     XChunk X;
-    float sc = 0.f, psx = 0.f;
-    if (g.act) {
+    float scp[4] = {0.f, 0.f, 0.f, 0.f}, psx = 0.f;
+    const int xs = j % NX;
+    if (!abort && !mbar_wait_warp(&xfull[xs], (j / NX) & 1)) {
+      if (lane == 0) latch_error(&a.ws.ctl[0], kErrTimeout);
+      abort = true;
+    }
+    if (!abort && g.act) {
       const int C = g.C, col = g.col;
-      const uint4 g0 = xform[d.c0 * 4 + 0 * C + col], g1 = xform[d.c0 * 4 + 1 * C + col];
-      const uint4 g2 = xform[d.c0 * 4 + 2 * C + col], g3 = xform[d.c0 * 4 + 3 * C + col];
+      const uint8_t* xb = xring + xs * L.xslot;
+      const uint4* xw = reinterpret_cast<const uint4*>(xb);
+      const uint4 g0 = xw[0 * C + col], g1 = xw[1 * C + col], g2 = xw[2 * C + col], g3 = xw[3 * C + col];
       X.eh[0] = g0.x, X.eh[1] = g0.y, X.eh[2] = g0.z, X.eh[3] = g0.w;
       X.el[0] = g1.x, X.el[1] = g1.y, X.el[2] = g1.z, X.el[3] = g1.w;
       X.oh[0] = g2.x, X.oh[1] = g2.y, X.oh[2] = g2.z, X.oh[3] = g2.w;
       X.ol[0] = g3.x, X.ol[1] = g3.y, X.ol[2] = g3.z, X.ol[3] = g3.w;
-      sc = xscale[d.c0 + col] * d.p, psx = d.p * xsum[d.c0 + col];
+      const float4 sc4 = reinterpret_cast<const float4*>(xb + 64 * ncmax)[col];
+      const float4 sm4 = reinterpret_cast<const float4*>(xb + 80 * ncmax)[col];
+      scp[0] = sc4.x * d.p, scp[1] = sc4.y * d.p, scp[2] = sc4.z * d.p, scp[3] = sc4.w * d.p;
+      psx = d.p * ((sm4.x + sm4.y) + (sm4.z + sm4.w));
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&xempty[xs]);
     const int rowb = (d.Fe / 2), sbrow = (d.Fe / 16);
 #pragma unroll
     for (int t = 0; t < kD1MaxTiles; ++t) {
@@ -722,7 +760,7 @@ __global__ void __launch_bounds__((kD1Warps + 1) * 32, 1) down_b1_kernel(const _
           if (r < RT) {
             const uint4 q = *reinterpret_cast<const uint4*>(st + r * rowb + g.col * 16);
             const uint32_t sbw = *reinterpret_cast<const uint32_t*>(stsb + r * sbrow + (g.col >> 1) * 4);
-            const float v = fmaf(bf16lo(sbw) * sc, static_cast<float>(dot_chunk(q, X)), bf16hi(sbw) * psx);
+            const float v = fmaf(bf16lo(sbw), dot_chunk_g(q, X, scp), bf16hi(sbw) * psx);
             if (sh) acc[t][m] += v;
             else acc[t][kD1Rpt + m] += v;
           }
@@ -759,7 +797,7 @@ __global__ void __launch_bounds__((kD1Warps + 1) * 32, 1) down_b1_kernel(const _
 
 size_t down_b1_smem_bytes(const LayerArgs& a) {
   const int has_sh = a.Fs > 0 ? 1 : 0;
-  return d1_smem(a.dn_nst, a.dn_stage, a.k + has_sh, a.k * (a.F / 32) + has_sh * (a.Fs / 32)).total;
+  return d1_smem(a.dn_nst, a.dn_stage, a.k + has_sh, std::max(a.F, a.Fs) / 32).total;
 }
 
 // ============================================================================
@@ -794,7 +832,9 @@ bool plan_b1(LayerArgs& a, int num_sms, int smem_optin) {
   }
   a.gu_rows = rows;
   const int rth = (rows / 2) * a.gu_nrl;
-  if (a.F % rth || (a.Fs && a.Fs % rth)) return false;
+  // an item's h values are whole 8-value groups of the fixed-point h, at
+  // most two per lane of the warp that writes them
+  if (rth % 8 || rth > 64 || a.F % rth || (a.Fs && a.Fs % rth)) return false;
   if (a.gu_nst < 2) return false;
 
   int nrl_min = lanes_for(a.F, kD1Warps);
@@ -816,8 +856,8 @@ bool plan_b1(LayerArgs& a, int num_sms, int smem_optin) {
   a.dn_tiles = H / best;
   a.dn_stage = (best * (Fm / 2 + Fm / 16) + 127) / 128 * 128;
   const int has_sh = a.Fs > 0 ? 1 : 0;
-  const int fixed = d1_smem(0, 0, a.k + has_sh, a.k * (a.F / 32) + has_sh * (a.Fs / 32)).total;
-  a.dn_nst = std::min(8, (kB1SmemBudget - fixed) / a.dn_stage);
+  const int fixed = d1_smem(0, 0, a.k + has_sh, std::max(a.F, a.Fs) / 32).total;
+  a.dn_nst = std::min(kD1MaxStages, (kB1SmemBudget - fixed) / a.dn_stage);
   if (a.dn_nst < 2) return false;
   if (gateup_b1_smem_bytes(a, rows) + 1024 > static_cast<size_t>(smem_optin)) return false;
   if (down_b1_smem_bytes(a) + 1024 > static_cast<size_t>(smem_optin)) return false;
@@ -876,7 +916,7 @@ static cudaError_t launch_gateup1(const LayerArgs& a, int part, int num_sms, cud
   LayerArgs b = a;
   b.gu_part = part;
   const void* gu = b.gu_rows == 8 ? (const void*)gateup_b1_kernel<8> : (const void*)gateup_b1_kernel<4>;
-  return launch1(gu, num_sms, (kG1Warps + 1) * 32, gateup_b1_smem_bytes(b, b.gu_rows), st, pdl, b);
+  return launch1(gu, num_sms, kG1Threads, gateup_b1_smem_bytes(b, b.gu_rows), st, pdl, b);
 }
 
 static cudaError_t launch_down1(const LayerArgs& a, int num_sms, cudaStream_t st, bool pdl) {

@@ -17,6 +17,11 @@
 // A bf16 activation is represented exactly unless it is more than 2^7 below
 // its chunk's largest magnitude; the rounding then stays below 2^-15 of
 // that magnitude.
+//
+// Grouped variant (the single-token down's h rows): each 8-value group, i.e.
+// word i of every kind below, carries its own exponent, so the producer of
+// the group needs no other group's values.  The dot keeps four exact integer
+// sums, one per group, each scaled by its own 2^e.
 #pragma once
 
 #include <cstdint>
@@ -227,6 +232,21 @@ __device__ __forceinline__ int dot_chunk(const uint4 q, const XChunk& X) {
   return ah * 256 + al;
 }
 
+
+// sum_i sc[i] * (exact sum over group i of q_m X_m): the grouped form.
+__device__ __forceinline__ float dot_chunk_g(const uint4 q, const XChunk& X, const float (&sc)[4]) {
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+  float r = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t ev = w[i] & 0x0F0F0F0Fu, od = (w[i] >> 4) & 0x0F0F0F0Fu;
+    int ah = dp4a_us(ev, X.eh[i], 0), al = dp4a_uu(ev, X.el[i], 0);
+    ah = dp4a_us(od, X.oh[i], ah);
+    al = dp4a_uu(od, X.ol[i], al);
+    r = fmaf(sc[i], static_cast<float>(ah * 256 + al), r);
+  }
+  return r;
+}
 
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll

@@ -31,11 +31,11 @@ struct RecordOffsets {
 // Device pointers into the caller's workspace (computed on the host).
 struct Workspace {
   unsigned* ctl;         // [0] error bits, [1] router done counter, [2] gate|up item claims,
-                         // [3] shared-only gate|up claims, [4..5] 64-bit grid-barrier
-                         // arrivals of the down kernel
-  uint4* hx;             // single token: fixed-point h chunks, [chunk-interleaved][4] words
-  float* hx_scale;       // single token: 2^e of each fixed-point h chunk
-  float* hx_sum;         // single token: plain sum of each h chunk
+                         // [3] shared-only gate|up claims
+  uint4* hx;             // single token: fixed-point h, per row [4 kinds][chunks] uint4 words
+                         // (word i of a uint4 = 8-value group i of the chunk)
+  float* hx_scale;       // single token: 2^e of each 8-value group, 4 per chunk
+  float* hx_sum;         // single token: plain sum of each 8-value group, 4 per chunk
   float* logits;         // [T][E]
   int* n_act;            // number of distinct routed experts this step
   int* act_expert;       // [E] active expert ids, ascending
