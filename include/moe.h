@@ -159,8 +159,11 @@ int moe_decode_host(moe_layer *layer, const uint16_t *x_host, int32_t B,
                     float *weights_host, void *workspace, size_t workspace_bytes,
                     void *stream);
 
-/* Synchronises `stream`, then reads and clears the error word that device
- * code latches in `workspace`: MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_RESIDENCY. */
+/* Synchronises `stream`, then reads the error word that device code latches
+ * in `workspace`: MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_RESIDENCY.  After an
+ * error it zeroes the workspace's persistent control block (error word and
+ * the claim and completion counters a step that gave up may leave mid-count),
+ * so the workspace is ready for the next call. */
 int moe_check(const moe_layer *layer, void *workspace, void *stream);
 
 /* Profiling hook.  With `events` pointing to four cudaEvent_t (passed as
@@ -271,9 +274,10 @@ void moe_residency_close(moe_residency *res);
  * First call per device: looks up the scratch's device address once (with
  * that device current) and zeroes the whole scratch on `stream`, ordered
  * before the step.  The scratch's control words (error word, the router's
- * completion counter, the gate|up item counter, the down kernel's barrier
- * counter) must start at zero; every later step leaves them ready for the
- * next one.  Make this first call before any stream capture begins.
+ * completion counter, item claim counters, per-expert and per-row-tile
+ * completion counters) must start at zero; every later step leaves them
+ * ready for the next one.  Make this first call before any stream capture
+ * begins.
  *
  * All calls on one device share the one scratch: calls whose executions
  * overlap (different streams, different threads or different layers without

@@ -201,10 +201,14 @@ extern "C" void moe_close(moe_layer* L) {
 }
 
 // ---- workspace -------------------------------------------------------------
-// [control: 64 words][h chunk counters][fixed-point h][logits][grouping][h]
-// [h_shared][host-entry staging][prefill scratch].  The control block and the
-// chunk counters persist between calls (kept at zero by the kernels);
-// everything after them is per-call scratch.
+// [control: 64 words][entry counters][row-tile counters][fixed-point h]
+// [down partial outputs][logits][grouping][h][h_shared][host-entry staging]
+// [prefill scratch].  The control block and the counters persist between
+// calls (kept at zero by the kernels, cleared by moe_check after a device
+// error); everything after them is per-call scratch.
+
+// Bytes at the start of a workspace that persist between calls.
+constexpr size_t kPersistentBytes = 64 * 4 + 64 * 4 + moe::kMaxDim / 8 * 4;
 
 struct Carve {
   size_t off = 0;
@@ -220,11 +224,14 @@ static size_t carve(const moe_layer* L, int T, moe::Workspace* ws, uint8_t* base
   const size_t H = L->d.hidden, E = L->d.n_experts, k = L->d.top_k, F = L->d.ffn,
                Fs = L->d.shared_ffn, t = static_cast<size_t>(T);
   Carve c;
-  const size_t o_ctl = c.take(64 * 4);
+  // persistent control block: 64 control words, per-entry h counters, per
+  // down row tile counters (at most H / 8 tiles)
+  const size_t o_ctl = c.take(64 * 4), o_hcnt = c.take(64 * 4), o_tcnt = c.take(moe::kMaxDim / 8 * 4);
   // single-token fixed-point h: k routed rows of F and the shared row of Fs;
   // per 32-value chunk 64 bytes of words and 4 group scales and sums
   const size_t hchunks = k * (F / 32) + Fs / 32;
   const size_t o_hx = c.take(hchunks * 64), o_hxs = c.take(hchunks * 16), o_hxm = c.take(hchunks * 16);
+  const size_t o_yp = c.take((k + 1) * H * 4);
   const size_t o_log = c.take(t * E * 4);
   const size_t o_nact = c.take(16);
   const size_t o_ae = c.take(E * 4), o_ao = c.take(E * 4), o_ac = c.take(E * 4);
@@ -236,6 +243,9 @@ static size_t carve(const moe_layer* L, int T, moe::Workspace* ws, uint8_t* base
   const size_t o_pf = c.take(moe::prefill_workspace_bytes(a, T));
   if (ws && base) {
     ws->ctl = reinterpret_cast<unsigned*>(base + o_ctl);
+    ws->hcnt = reinterpret_cast<unsigned*>(base + o_hcnt);
+    ws->tcnt = reinterpret_cast<unsigned*>(base + o_tcnt);
+    ws->ypart = reinterpret_cast<float*>(base + o_yp);
     ws->hx = reinterpret_cast<uint4*>(base + o_hx);
     ws->hx_scale = reinterpret_cast<float*>(base + o_hxs);
     ws->hx_sum = reinterpret_cast<float*>(base + o_hxm);
@@ -394,8 +404,9 @@ extern "C" int moe_check(const moe_layer* L, void* ws, void* stream) {
   unsigned bits = 0;
   if ((e = cudaMemcpy(&bits, ws, 4, cudaMemcpyDeviceToHost))) return cuda_fail(e, "moe_check: read error word");
   if (bits == 0) return MOE_OK;
-  const unsigned zero = 0;
-  if ((e = cudaMemcpy(ws, &zero, 4, cudaMemcpyHostToDevice))) return cuda_fail(e, "moe_check: clear error word");
+  // a step that gave up may leave claim and completion counters mid-count:
+  // the whole persistent block goes back to zero with the error word
+  if ((e = cudaMemset(ws, 0, kPersistentBytes))) return cuda_fail(e, "moe_check: clear control block");
   if (bits & moe::kErrTimeout) return fail(MOE_ERR_TIMEOUT, "device code gave up a bounded wait (bits 0x%x)", bits);
   if (bits & moe::kErrResidency) return fail(MOE_ERR_RESIDENCY, "an expert slot did not hold the routed expert (bits 0x%x)", bits);
   return fail(MOE_ERR_ARG, "device code clamped an out-of-range routing value (bits 0x%x)", bits);

@@ -78,6 +78,19 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
+// As mbar_wait, but while the phase is incomplete the thread sleeps in
+// hardware (up to hint_ns per try, woken as soon as the phase completes)
+// instead of spinning, so waiting warps leave their issue slots to warps
+// with work.  Gives up after kWaitLimitNs and returns false.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns = 20000u) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_timer_ns();
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity, hint_ns)) return true;
+    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
 // Position in a ring of `nst` pipeline stages: stage index and the parity of
 // the current lap, advanced without integer division.
 struct RingPos {
@@ -91,6 +104,10 @@ struct RingPos {
 // Every lane polls (no divergence, no broadcast); the warp agrees on the outcome.
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity) {
   return __all_sync(0xFFFFFFFFu, mbar_wait(bar, parity)) != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_sleep_warp(uint64_t* bar, uint32_t parity) {
+  return __all_sync(0xFFFFFFFFu, mbar_wait_sleep(bar, parity)) != 0;
 }
 
 // 1-D bulk copy global -> shared, completion counted on `bar` in bytes.
@@ -152,6 +169,23 @@ __device__ __forceinline__ uint16_t f32_to_bf16_rne(float f) {
 
 __device__ __forceinline__ void latch_error(unsigned* err, unsigned bits) {
   atomicOr(err, bits);
+}
+
+// Counters shared between CTAs of one grid.  A release add orders every
+// write this thread made (or observed, e.g. through __syncwarp) before it
+// at GPU scope; an acquire load orders later reads after the value it saw.
+__device__ __forceinline__ void red_add_release_gpu(unsigned* p, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned* p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
 }
 
 // Programmatic dependent launch: wait for the previous grid's results /

@@ -428,13 +428,13 @@ __global__ void __launch_bounds__(kG1Threads, 1) gateup_b1_kernel(const __grid_c
     RingPos pos;
     for (;; pos.next(NST)) {
       const int s = pos.s;
-      if (!mbar_wait_warp(&full[s], pos.ph)) {
+      if (!mbar_wait_sleep_warp(&full[s], pos.ph)) {
         if (lane == 0) latch_error(&a.ws.ctl[0], kErrTimeout);
         break;
       }
       const int i = s_item[s];
       if (i < 0) break;  // the producer ran out of items
-      if (!mbar_wait_warp(&pdone[s], pos.ph)) {
+      if (!mbar_wait_sleep_warp(&pdone[s], pos.ph)) {
         if (lane == 0) latch_error(&a.ws.ctl[0], kErrTimeout);
         break;
       }
@@ -495,7 +495,7 @@ __global__ void __launch_bounds__(kG1Threads, 1) gateup_b1_kernel(const __grid_c
   RingPos pos;
   for (;; pos.next(NST)) {
     const int s = pos.s;
-    if (!mbar_wait_warp(&full[s], pos.ph)) {
+    if (!mbar_wait_sleep_warp(&full[s], pos.ph)) {
       if (lane == 0) latch_error(&a.ws.ctl[0], kErrTimeout);
       break;
     }
@@ -718,7 +718,7 @@ __global__ void __launch_bounds__((kD1Warps + 1) * 32, 1) down_b1_kernel(const _
     XChunk X;
     float scp[4] = {0.f, 0.f, 0.f, 0.f}, psx = 0.f;
     const int xs = j % NX;
-    if (!abort && !mbar_wait_warp(&xfull[xs], (j / NX) & 1)) {
+    if (!abort && !mbar_wait_sleep_warp(&xfull[xs], (j / NX) & 1)) {
       if (lane == 0) latch_error(&a.ws.ctl[0], kErrTimeout);
       abort = true;
     }
@@ -746,7 +746,7 @@ __global__ void __launch_bounds__((kD1Warps + 1) * 32, 1) down_b1_kernel(const _
       const uint32_t ph = pos.ph;
       pos.next(NST);
       if (abort) continue;
-      if (!mbar_wait_warp(&full[s], ph)) {
+      if (!mbar_wait_sleep_warp(&full[s], ph)) {
         if (lane == 0) latch_error(&a.ws.ctl[0], kErrTimeout);
         abort = true;
         continue;
@@ -801,6 +801,466 @@ size_t down_b1_smem_bytes(const LayerArgs& a) {
 }
 
 // ============================================================================
+// Fused gate|up + down (B = 1): one persistent kernel, one HBM stream.
+//
+// The step's work is one list of items claimed from a global counter: gate|up
+// items (rth gate + rth up rows of one expert, as in gateup_b1_kernel) and
+// down items (RTD rows of H of one expert's down matrix, with the expert's
+// fixed-point h block copied in the same stage).  The list runs
+//   G(shared) D(shared) G(1) ... G(n) interleaved with D(1) ... D(n),
+// with the routed experts' down items kF1Lag experts behind their gate|up
+// items (G(1) .. G(kF1Lag + 1), D(1), G(kF1Lag + 2), D(2), ...), so a CTA
+// reaches an expert's down items several ring depths after that expert's
+// last gate|up item was claimed and its h is normally complete; the
+// producer checks a per-expert completion counter before it issues a down
+// item.  The lighter gate|up arithmetic and
+// the heavier down arithmetic share the consumer warps, and the stream never
+// stops at a kernel boundary.
+//
+// Warps: NCW consumers, one producer, two epilogue warps that take ring
+// positions in turn.  For a gate|up item the epilogue applies SwiGLU and
+// writes the fixed-point h groups, then counts the item for its expert
+// (release).  For a down item it writes the item's weighted row sums to
+// ypart[expert] and counts the expert for the row tile (acquire-release);
+// the epilogue that completes a tile sums its rows over the experts in
+// entry order (the same order whichever CTAs did the work) and writes the
+// output.  Every counter is back at zero when the step ends: the row-tile
+// counters by the tile's summing epilogue, the claim and per-expert counters
+// by the last producer to finish claiming.
+// ============================================================================
+
+constexpr int kF1Warps = 16;                     // consumer warps
+constexpr int kF1Threads = (kF1Warps + 3) * 32;  // + producer + two epilogue warps
+constexpr int kF1SmemBudget = 222 * 1024;
+constexpr int kF1MaxStages = 16;
+constexpr int kF1Lag = 3;  // routed experts between an expert's gate|up and down items
+
+struct F1Smem {
+  int wsum, info, ent, bars, total;
+};
+
+struct F1Ent {          // one expert of the step, as the fused producer uses it
+  const uint8_t* rec;   // record base
+  float p;              // routing weight (1 for the shared expert)
+  int c0;               // first fixed-point chunk of its h row
+  unsigned need;        // gate|up items that complete its h
+  int pad;
+};
+
+__host__ __device__ inline F1Smem f1_smem(int nst, int stage) {
+  F1Smem s;
+  s.wsum = nst * stage;                      // [NST][NCW][8] per-warp row sums
+  s.info = s.wsum + nst * kF1Warps * 8 * 4;  // [16] item codes, [16] routing weights
+  s.ent = s.info + 2 * kF1MaxStages * 4;     // [kMaxTopK + 1] expert table
+  s.bars = s.ent + (kMaxTopK + 1) * static_cast<int>(sizeof(F1Ent));
+  s.total = s.bars + 3 * nst * 8 + 16;       // full, empty, partial sums done
+  return s;
+}
+
+// n / d for n * d < 2^40 as one 64-bit multiply: m = ceil(2^40 / d).
+struct F1Div {
+  unsigned long long m;
+  int d;
+};
+__device__ __forceinline__ F1Div f1_div(int d) {
+  F1Div r;
+  r.d = d;
+  r.m = ((1ull << 40) + static_cast<unsigned long long>(d) - 1) / static_cast<unsigned long long>(d);
+  return r;
+}
+__device__ __forceinline__ int f1_q(int n, const F1Div& v) {
+  return static_cast<int>((static_cast<unsigned long long>(n) * v.m) >> 40);
+}
+
+// Item code in shared memory: entry << 20 | tile << 1 | gate (-1: end).
+__device__ __forceinline__ int f1_code(int gate, int entry, int tile) { return (entry << 20) | (tile << 1) | gate; }
+
+// Claim index -> (gate, entry, tile) for a list with the shared expert's
+// items first (tiles_s gate|up, then ndn down) and n_act routed experts:
+// G(1..m) with m = min(kF1Lag, n_act), then the pairs G(r) D(r - kF1Lag)
+// for r = kF1Lag + 1 .. n_act, then the last m experts' down items.
+// Routed expert r (1-based) is entry has_sh + r - 1.
+// The divisions use the reciprocals dr (tiles_r), dn (ndn), dp (tiles_r + ndn).
+__device__ __forceinline__ int f1_item(int i, int has_sh, int tiles_s, int n_act, const F1Div& dr,
+                                       const F1Div& dn, const F1Div& dp) {
+  const int tiles_r = dr.d, ndn = dn.d;
+  if (has_sh) {
+    if (i < tiles_s) return f1_code(1, 0, i);
+    i -= tiles_s;
+    if (i < ndn) return f1_code(0, 0, i);
+    i -= ndn;
+  }
+  const int e0 = has_sh - 1;  // entry of routed expert r is e0 + r
+  const int m = min(kF1Lag, n_act), head = m * tiles_r;
+  if (i < head) {
+    const int q = f1_q(i, dr);
+    return f1_code(1, e0 + 1 + q, i - q * tiles_r);
+  }
+  const int j = i - head, per = dp.d, pairs = n_act - m, body = pairs * per;
+  if (j < body) {
+    const int p = f1_q(j, dp), off = j - p * per;
+    return off < tiles_r ? f1_code(1, e0 + kF1Lag + 1 + p, off) : f1_code(0, e0 + 1 + p, off - tiles_r);
+  }
+  const int t = j - body, q = f1_q(t, dn);
+  return f1_code(0, e0 + n_act - m + 1 + q, t - q * ndn);
+}
+
+// Waits (bounded) until *cnt >= need; acquire.
+__device__ __forceinline__ bool wait_count(const unsigned* cnt, unsigned need) {
+  if (ld_acquire_gpu(cnt) >= need) return true;
+  const unsigned long long t0 = global_timer_ns();
+  for (;;) {
+    __nanosleep(64);
+    if (ld_acquire_gpu(cnt) >= need) return true;
+    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+template <int R>  // gate|up rows per thread per item: R/2 gate + R/2 up
+__global__ void __launch_bounds__(kF1Threads, 1) ffn_b1_kernel(const __grid_constant__ LayerArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  constexpr int NCW = kF1Warps;
+  const int H = a.H, C = H >> 5, WC = (C + 31) >> 5, NRL = a.gu_nrl, NAW = NRL * WC;
+  constexpr int RH = R / 2;
+  const int rth = RH * NRL;
+  const int NST = a.f1_nst, SB = a.f1_stage, RTD = a.f1_rt;
+  const F1Smem L = f1_smem(NST, SB);
+  float* wsum = reinterpret_cast<float*>(smem + L.wsum);
+  volatile int* s_code = reinterpret_cast<volatile int*>(smem + L.info);
+  volatile float* s_p = reinterpret_cast<volatile float*>(smem + L.info + kF1MaxStages * 4);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
+  uint64_t* empty = full + NST;   // consumers and the position's epilogue warp are done
+  uint64_t* pdone = empty + NST;  // every consumer's row sums of the position are in
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  if (tid == 0) {
+    for (int s = 0; s < NST; ++s) mbar_init(&full[s], 1), mbar_init(&empty[s], NCW + 1), mbar_init(&pdone[s], NCW);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+
+  const int has_sh = a.Fs > 0 ? 1 : 0;
+  const int tiles_s = has_sh ? a.Fs / rth : 0, tiles_r = a.F / rth, ndn = H / RTD;
+  const int n_pre = has_sh ? tiles_s + ndn : 0;  // items that need no routing
+
+  if (warp == NCW) {  // ---------------- producer warp (lane 0 issues; the warp builds the table)
+    F1Ent* tab = reinterpret_cast<F1Ent*>(smem + L.ent);
+    const uint64_t pol = policy_evict_first();
+    unsigned* claim = &a.ws.ctl[2];
+    const F1Div dr = f1_div(tiles_r), dn = f1_div(ndn), dp = f1_div(tiles_r + ndn);
+    int it = 0, n_items = n_pre, n_ent = has_sh, checked = -1, cur = 0, nxt = 0;
+    bool ok = true;
+    RingPos pos;
+    if (has_sh && lane == 0) {  // the shared expert needs no routing
+      F1Ent t;
+      t.rec = a.shared, t.p = 1.f, t.c0 = 0, t.need = tiles_s;
+      tab[0] = t;
+    }
+    if (lane == 0) {
+      // claims run two items ahead, so a claim's round trip has a whole
+      // item to complete before its index is needed
+      cur = static_cast<int>(atomicAdd(claim, 1u));
+      nxt = static_cast<int>(atomicAdd(claim, 1u));
+    }
+    for (int phase = 0; phase < 2 && ok; ++phase) {
+      if (phase == 1) {
+        // routed items: wait for the router, then the whole warp looks the
+        // step's experts up once (lane j: routed expert j) into shared memory
+        pdl_wait();
+        const int n_act = clamp_n_act(a);
+        for (int j = lane; j < n_act; j += 32) {
+          const B1Entry en = b1_entry(a, has_sh + j, has_sh);
+          if (a.slot_tag && a.slot_tag[en.slot] != en.expert) latch_error(&a.ws.ctl[0], kErrResidency);
+          F1Ent t;
+          t.rec = en.rec, t.p = a.weights[a.ws.pair_slot[en.pair]], t.c0 = has_sh * (a.Fs / 32) + j * (a.F / 32);
+          t.need = tiles_r;
+          tab[has_sh + j] = t;
+        }
+        __syncwarp();
+        n_items = n_pre + n_act * (tiles_r + ndn);
+        n_ent = has_sh + n_act;
+      }
+      if (lane == 0) {
+        for (;; ++it, pos.next(NST)) {
+          const int i = cur;
+          if (phase == 0 && i >= n_pre) break;  // routed from here on: phase 1
+          if (i >= n_items) break;
+          cur = nxt;
+          nxt = static_cast<int>(atomicAdd(claim, 1u));
+          const int code = f1_item(i, has_sh, tiles_s, n_ent - has_sh, dr, dn, dp);
+          const int gate = code & 1, e = code >> 20, tile = (code >> 1) & 0x7FFFF;
+          const bool sh = has_sh && e == 0;
+          const RecordOffsets& off = sh ? a.off_s : a.off_r;
+          const F1Ent t = tab[e];
+          // the completion check goes before the wait for a free stage, so
+          // its latency overlaps it
+          if (!gate && e != checked) {  // the expert's h must be complete before its block is copied
+            if (!wait_count(&a.ws.hcnt[e], t.need)) {
+              latch_error(&a.ws.ctl[0], kErrTimeout);
+              ok = false;
+              break;
+            }
+            checked = e;
+            // h was written through the generic proxy; the bulk copy reads it
+            // through the async proxy
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+          }
+          const int s = pos.s;
+          if (it >= NST && !mbar_wait(&empty[s], pos.ph ^ 1u)) {
+            latch_error(&a.ws.ctl[0], kErrTimeout);
+            ok = false;
+            break;
+          }
+          uint8_t* st = smem + s * SB;
+          s_code[s] = code;
+          if (gate) {
+            const size_t j0 = static_cast<size_t>(tile) * rth;
+            const uint32_t cb = rth * (H / 2), sbb = rth * (H / 16);
+            mbar_arrive_expect_tx(&full[s], 2 * cb + 2 * sbb);
+            bulk_g2s(st, t.rec + off.gate_codes + j0 * (H / 2), cb, &full[s], pol);
+            bulk_g2s(st + cb, t.rec + off.up_codes + j0 * (H / 2), cb, &full[s], pol);
+            bulk_g2s(st + 2 * cb, t.rec + off.gate_sb + j0 * (H / 16), sbb, &full[s], pol);
+            bulk_g2s(st + 2 * cb + sbb, t.rec + off.up_sb + j0 * (H / 16), sbb, &full[s], pol);
+          } else {
+            const int Fe = sh ? a.Fs : a.F, nc = Fe / 32;
+            const uint32_t cb = RTD * (Fe / 2), sbb = RTD * (Fe / 16), xw = 64 * nc, xq = 16 * nc;
+            const size_t r0 = static_cast<size_t>(tile) * RTD;
+            s_p[s] = t.p;
+            mbar_arrive_expect_tx(&full[s], cb + sbb + xw + 2 * xq);
+            bulk_g2s(st, t.rec + off.down_codes + r0 * (Fe / 2), cb, &full[s], pol);
+            bulk_g2s(st + cb, t.rec + off.down_sb + r0 * (Fe / 16), sbb, &full[s], pol);
+            // every CTA reads the h blocks: no evict-first hint
+            bulk_g2s(st + cb + sbb, a.ws.hx + static_cast<size_t>(t.c0) * 4, xw, &full[s]);
+            bulk_g2s(st + cb + sbb + xw, a.ws.hx_scale + static_cast<size_t>(t.c0) * 4, xq, &full[s]);
+            bulk_g2s(st + cb + sbb + xw + xq, a.ws.hx_sum + static_cast<size_t>(t.c0) * 4, xq, &full[s]);
+          }
+        }
+      }
+      ok = __shfl_sync(kAll, ok ? 1 : 0, 0) != 0;
+    }
+    if (lane == 0) {
+      // copies in flight land before the end markers re-arm their stages
+      for (int j = max(0, it - NST); j < it; ++j)
+        if (!mbar_wait(&full[j % NST], (j / NST) & 1)) latch_error(&a.ws.ctl[0], kErrTimeout), ok = false;
+      // one end marker per epilogue warp (positions it, it + 1); consumers
+      // stop at the first
+      for (int m = 0; m < 2; ++m, ++it, pos.next(NST)) {
+        const int s = pos.s;
+        if (it >= NST && !mbar_wait(&empty[s], pos.ph ^ 1u)) {
+          latch_error(&a.ws.ctl[0], kErrTimeout);
+          ok = false;
+          break;
+        }
+        s_code[s] = -1;
+        mbar_arrive(&full[s]);
+      }
+      // The last producer to get here resets the claim and per-expert
+      // counters: every claim of the step is made and every down item's
+      // completion check has passed, so every gate|up count is final.
+      if (ok) {
+        __threadfence();
+        if (atomicAdd(&a.ws.ctl[8], 1u) == gridDim.x - 1) {
+          a.ws.ctl[2] = 0u;
+          for (int j = 0; j < n_ent; ++j) a.ws.hcnt[j] = 0u;
+          a.ws.ctl[8] = 0u;
+          __threadfence();
+        }
+      }
+    }
+    return;
+  }
+
+  if (warp > NCW) {  // ---------------- epilogue warps: ring positions q, q + 2, ...
+    const int q = warp - NCW - 1;
+    const D1Geo gs = d1_geo(has_sh ? a.Fs : a.F, 0, 0), gr = d1_geo(a.F, 0, 0);
+    int n_ent = -1;  // known once the router's output is needed
+    for (int it = q;; it += 2) {
+      const int s = it % NST;
+      const uint32_t ph = (it / NST) & 1;
+      if (!mbar_wait_sleep_warp(&full[s], ph)) {
+        if (lane == 0) latch_error(&a.ws.ctl[0], kErrTimeout);
+        break;
+      }
+      const int code = s_code[s];
+      if (code < 0) break;
+      if (!mbar_wait_sleep_warp(&pdone[s], ph)) {
+        if (lane == 0) latch_error(&a.ws.ctl[0], kErrTimeout);
+        break;
+      }
+      const int gate = code & 1, e = code >> 20, tile = (code >> 1) & 0x7FFFF;
+      const bool sh_row = has_sh && e == 0;
+      float v0 = 0.f, v1 = 0.f, w0 = 0.f, w1 = 0.f;
+      if (gate) {  // gate and up sums of the item's rows (at most 64: two per lane)
+#pragma unroll
+        for (int k2 = 0; k2 < 2; ++k2) {
+          const int j = k2 * 32 + lane;
+          if (j < rth) {
+            const int rlj = j / RH, mj = j % RH;
+            float g = 0.f, u = 0.f;
+            for (int w = 0; w < WC; ++w) {
+              const float* ws = wsum + (s * NCW + rlj * WC + w) * 8;
+              g += ws[mj];
+              u += ws[RH + mj];
+            }
+            if (k2 == 0) v0 = g, w0 = u;
+            else v1 = g, w1 = u;
+          }
+        }
+      } else {  // the item's RTD row sums (at most 64: two per lane)
+        const D1Geo& g = sh_row ? gs : gr;
+#pragma unroll
+        for (int k2 = 0; k2 < 2; ++k2) {
+          const int r = k2 * 32 + lane;
+          if (r < RTD) {
+            const int rl = r % g.NRL, m = r / g.NRL;
+            float y = 0.f;
+            for (int w = 0; w < g.WC; ++w) y += wsum[(s * NCW + rl * g.WC + w) * 8 + m];
+            if (k2 == 0) v0 = y;
+            else v1 = y;
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);  // the stage is free; the rest is off the ring's path
+      if (gate) {
+        const int nc = (sh_row ? a.Fs : a.F) >> 5;
+        const int c0 = sh_row ? 0 : has_sh * (a.Fs >> 5) + (e - has_sh) * (a.F >> 5);
+        publish_hgroup(a, c0, nc, tile * rth + lane, silu1(v0) * w0, lane < rth, lane);
+        if (rth > 32) publish_hgroup(a, c0, nc, tile * rth + 32 + lane, silu1(v1) * w1, 32 + lane < rth, lane);
+        __syncwarp();
+        if (lane == 0) red_add_release_gpu(&a.ws.hcnt[e], 1u);
+      } else {
+        float* yp = a.ws.ypart + static_cast<size_t>(e) * H + static_cast<size_t>(tile) * RTD;
+        if (lane < RTD) yp[lane] = v0;
+        if (32 + lane < RTD) yp[32 + lane] = v1;
+        __syncwarp();
+        unsigned old = 0;
+        if (lane == 0) old = atom_add_acq_rel_gpu(&a.ws.tcnt[tile], 1u);
+        old = __shfl_sync(kAll, old, 0);
+        // a shared-expert item with old == 0 cannot be the tile's last (every
+        // step has routed experts); otherwise the router is done: read n_act
+        if (!sh_row || old > 0) {
+          if (n_ent < 0) {
+            pdl_wait();
+            n_ent = has_sh + clamp_n_act(a);
+          }
+          if (old + 1 == static_cast<unsigned>(n_ent)) {  // every expert's rows of this tile are in
+#pragma unroll
+            for (int k2 = 0; k2 < 2; ++k2) {
+              const int r = k2 * 32 + lane;
+              if (r < RTD) {
+                const size_t row = static_cast<size_t>(tile) * RTD + r;
+                float out = 0.f;
+                for (int j = 0; j < n_ent; ++j) out += __ldcg(a.ws.ypart + static_cast<size_t>(j) * H + row);
+                a.out_bf16[row] = f32_to_bf16_rne(out);
+                if (a.out_f32) a.out_f32[row] = out;
+              }
+            }
+            if (lane == 0) a.ws.tcnt[tile] = 0u;
+          }
+        }
+      }
+    }
+    return;
+  }
+
+  // ---------------------------------------------------- consumers
+  const int rl = warp / WC, wc = warp % WC, col = wc * 32 + lane;
+  const bool gact = warp < NAW && col < C;  // this lane's column of a gate|up item
+  float xv[32], sx = 0.f;
+#pragma unroll
+  for (int m = 0; m < 32; ++m) xv[m] = 0.f;
+  if (gact) {
+    const uint4* v = reinterpret_cast<const uint4*>(a.x + col * 32);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 t = __ldg(v + i);
+      const uint32_t w4[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) xv[8 * i + 2 * j] = bf16lo(w4[j]), xv[8 * i + 2 * j + 1] = bf16hi(w4[j]);
+    }
+#pragma unroll
+    for (int m = 0; m < 32; ++m) sx += xv[m];
+  }
+  XChunk X;
+  const float scale = make_xchunk_own(xv, X);
+  const D1Geo gs = d1_geo(has_sh ? a.Fs : a.F, warp, lane), gr = d1_geo(a.F, warp, lane);
+
+  RingPos pos;
+  for (;; pos.next(NST)) {
+    const int s = pos.s;
+    if (!mbar_wait_sleep_warp(&full[s], pos.ph)) {
+      if (lane == 0) latch_error(&a.ws.ctl[0], kErrTimeout);
+      break;
+    }
+    const int code = s_code[s];
+    if (code < 0) break;  // the producer ran out of items
+    const uint8_t* st = smem + s * SB;
+    float* ws = wsum + (s * NCW + warp) * 8;
+    if (code & 1) {  // gate|up item
+      const uint8_t* stsb = st + 2 * rth * (H / 2);
+      float part[R];
+#pragma unroll
+      for (int m = 0; m < R; ++m) part[m] = 0.f;
+      if (gact) {
+#pragma unroll
+        for (int m = 0; m < R; ++m) {
+          const int r = (m < RH) ? (RH * rl + m) : (rth + RH * rl + m - RH);
+          const uint4 qv = *reinterpret_cast<const uint4*>(st + r * (H / 2) + col * 16);
+          const uint32_t sbw = *reinterpret_cast<const uint32_t*>(stsb + r * (H / 16) + (col >> 1) * 4);
+          part[m] = fmaf(bf16lo(sbw) * scale, static_cast<float>(dot_chunk(qv, X)), bf16hi(sbw) * sx);
+        }
+      }
+      constexpr int LPR = 32 / R;  // lanes per row after the butterfly
+      float v;
+      if constexpr (R == 8) v = bfly8(part, lane);
+      else v = bfly4b(part, lane);
+      if ((lane & (LPR - 1)) == 0) ws[lane / LPR] = v;
+    } else {  // down item: RTD rows of one expert, its h block after the weights
+      const bool sh = has_sh && (code >> 20) == 0;
+      const D1Geo& g = sh ? gs : gr;
+      const int Fe = sh ? a.Fs : a.F, nc = Fe >> 5, rowb = Fe / 2, sbrow = Fe / 16;
+      const int RR = RTD / g.NRL;  // rows per thread
+      float part[8];
+#pragma unroll
+      for (int m = 0; m < 8; ++m) part[m] = 0.f;
+      if (g.act) {
+        const uint8_t* stsb = st + RTD * rowb;
+        const uint8_t* xb = stsb + RTD * sbrow;
+        const uint4* xw = reinterpret_cast<const uint4*>(xb);
+        XChunk Xh;
+        const uint4 g0 = xw[0 * nc + g.col], g1 = xw[1 * nc + g.col], g2 = xw[2 * nc + g.col],
+                    g3 = xw[3 * nc + g.col];
+        Xh.eh[0] = g0.x, Xh.eh[1] = g0.y, Xh.eh[2] = g0.z, Xh.eh[3] = g0.w;
+        Xh.el[0] = g1.x, Xh.el[1] = g1.y, Xh.el[2] = g1.z, Xh.el[3] = g1.w;
+        Xh.oh[0] = g2.x, Xh.oh[1] = g2.y, Xh.oh[2] = g2.z, Xh.oh[3] = g2.w;
+        Xh.ol[0] = g3.x, Xh.ol[1] = g3.y, Xh.ol[2] = g3.z, Xh.ol[3] = g3.w;
+        const float p = s_p[s];
+        const float4 sc4 = reinterpret_cast<const float4*>(xb + 64 * nc)[g.col];
+        const float4 sm4 = reinterpret_cast<const float4*>(xb + 80 * nc)[g.col];
+        const float scp[4] = {sc4.x * p, sc4.y * p, sc4.z * p, sc4.w * p};
+        const float psx = p * ((sm4.x + sm4.y) + (sm4.z + sm4.w));
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+          if (m < RR) {
+            const int r = g.rl + g.NRL * m;
+            const uint4 qv = *reinterpret_cast<const uint4*>(st + r * rowb + g.col * 16);
+            const uint32_t sbw = *reinterpret_cast<const uint32_t*>(stsb + r * sbrow + (g.col >> 1) * 4);
+            part[m] = fmaf(bf16lo(sbw), dot_chunk_g(qv, Xh, scp), bf16hi(sbw) * psx);
+          }
+        }
+      }
+      const float v = bfly8(part, lane);  // lane L: row (L >> 2) of the warp's column block
+      if ((lane & 3) == 0) ws[lane >> 2] = v;
+    }
+    __syncwarp();  // the lanes' sums before lane 0's arrivals (release at CTA scope)
+    if (lane == 0) mbar_arrive(&pdone[s]), mbar_arrive(&empty[s]);
+  }
+}
+
+size_t ffn_b1_smem_bytes(const LayerArgs& a) { return f1_smem(a.f1_nst, a.f1_stage).total; }
+
+// ============================================================================
 // Host side.
 // ============================================================================
 
@@ -816,6 +1276,36 @@ static int lanes_for(int K, int ncw) {
 }
 
 constexpr int kB1SmemBudget = 210 * 1024;
+
+// Row-lanes of the down mapping for an h row of width Fe (as d1_geo).
+static int d1_nrl(int Fe) {
+  const int C = Fe / 32, WC = (C + 31) / 32;
+  return p2floor(std::max(1, kD1Warps / WC));
+}
+
+// Geometry of the fused kernel: the largest down item (RTD rows, at most 64,
+// a divisor of H and a multiple of 4 and of both widths' row-lanes, at most
+// 8 rows per thread) whose stage still leaves a ring of three.  f1_nst = 0
+// when none fits (the three-kernel path runs instead).
+static void plan_f1(LayerArgs& a, int rth, int smem_optin) {
+  a.f1_nst = 0;
+  const int H = a.H, Fm = std::max(a.F, a.Fs);
+  const int nr = d1_nrl(a.F), ns = a.Fs ? d1_nrl(a.Fs) : nr;
+  const int gst = 2 * rth * (H / 2 + H / 16);
+  const int budget = std::min(kF1SmemBudget, smem_optin - 1024);
+  for (int rt = 64; rt >= 4; --rt) {
+    if (H % rt || rt % 4 || rt % nr || rt % ns || rt / nr > 8 || rt / ns > 8) continue;
+    if (H / rt > kMaxDim / 8) break;
+    const int dst = rt * (Fm / 2 + Fm / 16) + 96 * (Fm / 32);
+    const int sb = (std::max(gst, dst) + 127) / 128 * 128;
+    // per stage: the stage, its warps' row sums and three barriers
+    const int per = sb + (f1_smem(1, 0).total - f1_smem(0, 0).total);
+    const int nst = std::min(kF1MaxStages, (budget - f1_smem(0, 0).total) / per);
+    if (nst < 3) continue;
+    a.f1_rt = rt, a.f1_stage = sb, a.f1_nst = nst;
+    return;
+  }
+}
 
 // Geometry of the B = 1 kernels; false when this layer shape needs the
 // general kernels instead (fixed-point h rows too large for shared memory).
@@ -861,6 +1351,7 @@ bool plan_b1(LayerArgs& a, int num_sms, int smem_optin) {
   if (a.dn_nst < 2) return false;
   if (gateup_b1_smem_bytes(a, rows) + 1024 > static_cast<size_t>(smem_optin)) return false;
   if (down_b1_smem_bytes(a) + 1024 > static_cast<size_t>(smem_optin)) return false;
+  plan_f1(a, rth, smem_optin);
   return true;
 }
 
@@ -868,7 +1359,8 @@ cudaError_t set_b1_attributes(int smem_optin) {
   const void* fns[] = {(const void*)router_b1_kernel<4>, (const void*)router_b1_kernel<8>,
                        (const void*)router_b1_kernel<16>, (const void*)router_b1_kernel<32>,
                        (const void*)gateup_b1_kernel<4>,
-                       (const void*)gateup_b1_kernel<8>, (const void*)down_b1_kernel};
+                       (const void*)gateup_b1_kernel<8>, (const void*)down_b1_kernel,
+                       (const void*)ffn_b1_kernel<4>, (const void*)ffn_b1_kernel<8>};
   for (const void* f : fns) {
     cudaFuncAttributes fa;
     cudaError_t e = cudaFuncGetAttributes(&fa, f);
@@ -923,10 +1415,23 @@ static cudaError_t launch_down1(const LayerArgs& a, int num_sms, cudaStream_t st
   return launch1((const void*)down_b1_kernel, num_sms, (kD1Warps + 1) * 32, down_b1_smem_bytes(a), st, pdl, a);
 }
 
-// Launches the B = 1 path; `a` already planned by plan_b1.
+static cudaError_t launch_ffn1(const LayerArgs& a, int num_sms, cudaStream_t st, bool pdl) {
+  const void* fn = a.gu_rows == 8 ? (const void*)ffn_b1_kernel<8> : (const void*)ffn_b1_kernel<4>;
+  return launch1(fn, num_sms, kF1Threads, ffn_b1_smem_bytes(a), st, pdl, a);
+}
+
+// Launches the B = 1 path; `a` already planned by plan_b1.  The router, then
+// the fused gate|up + down kernel where it is planned (profile events: the
+// router, the fused kernel, nothing), else gate|up and down.
 cudaError_t launch_decode_b1(const LayerArgs& a, int num_sms, cudaStream_t st) {
   const bool pdl = !a.prof_on;
   cudaError_t e;
+  if (a.f1_nst > 0 && !a.slot_of) {
+    if ((e = mark1(a, 0, st)) || (e = launch_router1(a, num_sms, st)) || (e = mark1(a, 1, st)) ||
+        (e = launch_ffn1(a, num_sms, st, pdl)) || (e = mark1(a, 2, st)))
+      return e;
+    return mark1(a, 3, st);
+  }
   if ((e = mark1(a, 0, st))) return e;
   if ((e = launch_router1(a, num_sms, st))) return e;
   if ((e = mark1(a, 1, st))) return e;

@@ -30,12 +30,16 @@ struct RecordOffsets {
 
 // Device pointers into the caller's workspace (computed on the host).
 struct Workspace {
-  unsigned* ctl;         // [0] error bits, [1] router done counter, [2] gate|up item claims,
-                         // [3] shared-only gate|up claims
+  unsigned* ctl;         // [0] error bits, [1] router done counter, [2] gate|up (or fused
+                         // single-token) item claims, [3] shared-only gate|up claims,
+                         // [8] fused single-token producers done claiming
+  unsigned* hcnt;        // single token, fused kernel: gate|up items done per expert entry
+  unsigned* tcnt;        // single token, fused kernel: experts done per down row tile
   uint4* hx;             // single token: fixed-point h, per row [4 kinds][chunks] uint4 words
                          // (word i of a uint4 = 8-value group i of the chunk)
   float* hx_scale;       // single token: 2^e of each 8-value group, 4 per chunk
   float* hx_sum;         // single token: plain sum of each 8-value group, 4 per chunk
+  float* ypart;          // single token, fused kernel: [entry][H] weighted down outputs
   float* logits;         // [T][E]
   int* n_act;            // number of distinct routed experts this step
   int* act_expert;       // [E] active expert ids, ascending
@@ -105,6 +109,8 @@ struct LayerArgs {
                                // 2 routed experts only
   int dn_rt, dn_tiles;         // down row tile and number of tiles (H / dn_rt)
   int dn_stage, dn_nst;        // down stage bytes and stage count
+  int f1_rt, f1_stage, f1_nst; // fused single-token kernel: down rows per item, stage bytes
+                               // and count (f1_nst == 0: not planned)
   PrefillPtrs pf;              // prefill chunk scratch (tensor-core path)
   int prof_on;                 // record prof[] events between kernels, no PDL
   void* prof[4];               // cudaEvent_t: before router / gate|up / down, after down
