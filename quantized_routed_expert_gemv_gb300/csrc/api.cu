@@ -228,9 +228,9 @@ static size_t carve(const moe_layer* L, int T, moe::Workspace* ws, uint8_t* base
   // down row tile counters (at most H / 8 tiles)
   const size_t o_ctl = c.take(64 * 4), o_hcnt = c.take(64 * 4), o_tcnt = c.take(moe::kMaxDim / 8 * 4);
   // single-token fixed-point h: k routed rows of F and the shared row of Fs;
-  // per 32-value chunk 64 bytes of words and 4 group scales and sums
+  // per 32-value chunk 64 bytes of words and 4 group scales and sums (96 B)
   const size_t hchunks = k * (F / 32) + Fs / 32;
-  const size_t o_hx = c.take(hchunks * 64), o_hxs = c.take(hchunks * 16), o_hxm = c.take(hchunks * 16);
+  const size_t o_hx = c.take(hchunks * 96);
   const size_t o_yp = c.take((k + 1) * H * 4);
   const size_t o_log = c.take(t * E * 4);
   const size_t o_nact = c.take(16);
@@ -246,9 +246,7 @@ static size_t carve(const moe_layer* L, int T, moe::Workspace* ws, uint8_t* base
     ws->hcnt = reinterpret_cast<unsigned*>(base + o_hcnt);
     ws->tcnt = reinterpret_cast<unsigned*>(base + o_tcnt);
     ws->ypart = reinterpret_cast<float*>(base + o_yp);
-    ws->hx = reinterpret_cast<uint4*>(base + o_hx);
-    ws->hx_scale = reinterpret_cast<float*>(base + o_hxs);
-    ws->hx_sum = reinterpret_cast<float*>(base + o_hxm);
+    ws->hx = base + o_hx;
     ws->logits = reinterpret_cast<float*>(base + o_log);
     ws->n_act = reinterpret_cast<int*>(base + o_nact);
     ws->act_expert = reinterpret_cast<int*>(base + o_ae);

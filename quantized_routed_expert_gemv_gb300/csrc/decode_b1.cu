@@ -127,6 +127,79 @@ __device__ __forceinline__ B1Entry b1_entry(const LayerArgs& a, int idx, int has
 // Router (B = 1): 8-bit rows against the fixed-point token, then top-k.
 // ============================================================================
 
+// Top-k of one token's E logits (logit(e) reads one), softmax over the
+// chosen logits, and the single-token grouping; run by one whole warp.
+template <int KPL, typename Logit>
+__device__ __forceinline__ void topk_group_b1(const LayerArgs& a, int lane, Logit logit) {
+  const int E = a.E, k = a.k;
+  // Lane l holds the keys of experts l, l+32, ... in registers; a logit's
+  // key is its IEEE bit pattern mapped to an order-preserving unsigned (all
+  // finite logits map above 0; 0 marks a taken or absent expert).  Each lane
+  // keeps its best key; a round takes the warp's maximum (ties: the lower
+  // id), and only the lane that owned the winner rescans its keys.
+  uint32_t key[KPL];
+#pragma unroll
+  for (int s2 = 0; s2 < KPL; ++s2) {
+    const int e = s2 * 32 + lane;
+    uint32_t kk = 0u;
+    if (e < E) {
+      const uint32_t u = __float_as_uint(logit(e));
+      kk = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    }
+    key[s2] = kk;
+  }
+  uint32_t bk = 0u;
+  int bs = 0;
+#pragma unroll
+  for (int s2 = 0; s2 < KPL; ++s2)  // ascending slot = ascending id: ties keep the lower
+    if (key[s2] > bk) bk = key[s2], bs = s2;
+  float myl = 0.f;
+  int myi = 0;
+  for (int i = 0; i < k; ++i) {
+    const uint32_t top = __reduce_max_sync(kAll, bk);
+    const unsigned win = __reduce_min_sync(kAll, (bk == top && top != 0u) ? static_cast<unsigned>(bs * 32 + lane)
+                                                                         : 0xFFFFFFFFu);
+    int w = static_cast<int>(win);
+    if (w >= E) {  // only with non-finite logits (outside the contract)
+      if (lane == 0) latch_error(&a.ws.ctl[0], kErrRange);
+      w = i;
+    }
+    if (lane == i) {
+      myi = w;
+      myl = __uint_as_float((top & 0x80000000u) ? (top & 0x7FFFFFFFu) : ~top);
+    }
+    if ((w & 31) == lane) {  // the winner's lane drops it and finds its next best
+      const int ws = w >> 5;
+      bk = 0u, bs = 0;
+#pragma unroll
+      for (int s2 = 0; s2 < KPL; ++s2) {
+        if (s2 == ws) key[s2] = 0u;
+        if (key[s2] > bk) bk = key[s2], bs = s2;
+      }
+    }
+  }
+  const float lmax = __shfl_sync(kAll, myl, 0);
+  const float ex = (lane < k) ? expf(myl - lmax) : 0.f;
+  const float z = warp_add(ex);
+  if (lane < k) a.ids[lane] = myi, a.weights[lane] = ex / z;
+  // Grouping for one token: active experts in ascending id, one pair each.
+  // Sort the k ids with a rank count (k <= 32).
+  int rank = 0;
+  for (int j = 0; j < k; ++j) {
+    const int oj = __shfl_sync(kAll, myi, j);
+    if (lane < k && oj < myi) ++rank;
+  }
+  if (lane < k) {
+    a.ws.act_expert[rank] = myi;
+    a.ws.act_off[rank] = rank;
+    a.ws.act_cnt[rank] = 1;
+    a.ws.pair_token[rank] = 0;
+    a.ws.pair_slot[rank] = lane;
+  }
+  if (lane == 0) *a.ws.n_act = k;
+}
+
+
 constexpr int kR1Threads = 512;
 constexpr int kR1Rows = 8;  // rows per CTA pass: 64 CTAs for 512 experts leave most SMs to gate|up
 
@@ -200,71 +273,8 @@ __global__ void __launch_bounds__(kR1Threads) router_b1_kernel(const __grid_cons
   if (!s_last) return;
   __threadfence();
   if (warp != 0) return;
-  // Lane l holds the keys of experts l, l+32, ... in registers; a logit's
-  // key is its IEEE bit pattern mapped to an order-preserving unsigned (all
-  // finite logits map above 0; 0 marks a taken or absent expert).  Each lane
-  // keeps its best key; a round takes the warp's maximum (ties: the lower
-  // id), and only the lane that owned the winner rescans its keys.
-  uint32_t key[KPL];
-#pragma unroll
-  for (int s2 = 0; s2 < KPL; ++s2) {
-    const int e = s2 * 32 + lane;
-    uint32_t kk = 0u;
-    if (e < E) {
-      const uint32_t u = __float_as_uint(__ldcg(a.ws.logits + e));
-      kk = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-    }
-    key[s2] = kk;
-  }
-  uint32_t bk = 0u;
-  int bs = 0;
-#pragma unroll
-  for (int s2 = 0; s2 < KPL; ++s2)  // ascending slot = ascending id: ties keep the lower
-    if (key[s2] > bk) bk = key[s2], bs = s2;
-  float myl = 0.f;
-  int myi = 0;
-  for (int i = 0; i < k; ++i) {
-    const uint32_t top = __reduce_max_sync(kAll, bk);
-    const unsigned win = __reduce_min_sync(kAll, (bk == top && top != 0u) ? static_cast<unsigned>(bs * 32 + lane)
-                                                                         : 0xFFFFFFFFu);
-    int w = static_cast<int>(win);
-    if (w >= E) {  // only with non-finite logits (outside the contract)
-      if (lane == 0) latch_error(&a.ws.ctl[0], kErrRange);
-      w = i;
-    }
-    if (lane == i) {
-      myi = w;
-      myl = __uint_as_float((top & 0x80000000u) ? (top & 0x7FFFFFFFu) : ~top);
-    }
-    if ((w & 31) == lane) {  // the winner's lane drops it and finds its next best
-      const int ws = w >> 5;
-      bk = 0u, bs = 0;
-#pragma unroll
-      for (int s2 = 0; s2 < KPL; ++s2) {
-        if (s2 == ws) key[s2] = 0u;
-        if (key[s2] > bk) bk = key[s2], bs = s2;
-      }
-    }
-  }
-  const float lmax = __shfl_sync(kAll, myl, 0);
-  const float ex = (lane < k) ? expf(myl - lmax) : 0.f;
-  const float z = warp_add(ex);
-  if (lane < k) a.ids[lane] = myi, a.weights[lane] = ex / z;
-  // Grouping for one token: active experts in ascending id, one pair each.
-  // Sort the k ids with a rank count (k <= 32).
-  int rank = 0;
-  for (int j = 0; j < k; ++j) {
-    const int oj = __shfl_sync(kAll, myi, j);
-    if (lane < k && oj < myi) ++rank;
-  }
-  if (lane < k) {
-    a.ws.act_expert[rank] = myi;
-    a.ws.act_off[rank] = rank;
-    a.ws.act_cnt[rank] = 1;
-    a.ws.pair_token[rank] = 0;
-    a.ws.pair_slot[rank] = lane;
-  }
-  if (lane == 0) *a.ws.n_act = k, a.ws.ctl[1] = 0u;
+  topk_group_b1<KPL>(a, lane, [&](int e) { return __ldcg(a.ws.logits + e); });
+  if (lane == 0) a.ws.ctl[1] = 0u;
 }
 
 size_t router_b1_smem_bytes(int E) {
@@ -299,11 +309,12 @@ __host__ __device__ inline G1Smem g1_smem(int nst, int stage, int rows) {
 // Writes the fixed-point form of one 8-value group of an h row.  The warp's
 // 8-lane segments hold groups: lane 8g + p holds element f (f = 8 * (group)
 // + p) of the row with value v (0 where `act` is false).  The row's chunks
-// start at chunk c0 and number nc.  Layout, as the down kernel copies it:
+// start at chunk c0 and number nc; its block of 96 * nc bytes starts at byte
+// 96 * c0 of hx, so the down kernels copy it in one piece.  In the block:
 // the word of kind K (0: high bytes of the even elements, 1: their low
 // bytes, 2 and 3: the same for the odd elements) of group i of chunk c sits
-// at 32-bit word ((c0 * 4 + K * nc + c) * 4 + i); the group's 2^e and plain
-// sum at float (c0 + c) * 4 + i of hx_scale and hx_sum.
+// at 32-bit word (K * nc + c) * 4 + i; the group's 2^e at float
+// 16 * nc + c * 4 + i and its plain sum at float 20 * nc + c * 4 + i.
 __device__ __forceinline__ void publish_hgroup(const LayerArgs& a, int c0, int nc, int f, float v, bool act,
                                                int lane) {
   float amax = fabsf(v), sum = v;
@@ -330,9 +341,13 @@ __device__ __forceinline__ void publish_hgroup(const LayerArgs& a, int c0, int n
   }
   if (act && p < 4) {
     const int c = f >> 5, i = (f >> 3) & 3;
-    uint32_t* words = reinterpret_cast<uint32_t*>(a.ws.hx);
-    words[(static_cast<size_t>(c0) * 4 + p * nc + c) * 4 + i] = pack4(byte[0], byte[1], byte[2], byte[3]);
-    if (p == 0) a.ws.hx_scale[(c0 + c) * 4 + i] = scale, a.ws.hx_sum[(c0 + c) * 4 + i] = sum;
+    uint32_t* blk = reinterpret_cast<uint32_t*>(a.ws.hx + static_cast<size_t>(c0) * 96);
+    blk[(p * nc + c) * 4 + i] = pack4(byte[0], byte[1], byte[2], byte[3]);
+    if (p == 0) {
+      float* f = reinterpret_cast<float*>(blk);
+      f[16 * nc + c * 4 + i] = scale;
+      f[20 * nc + c * 4 + i] = sum;
+    }
   }
 }
 
@@ -564,8 +579,8 @@ struct D1Smem {
 };
 
 // rows: h rows of the step; ncmax: chunks of the widest h row.  An h slot
-// holds [4 kinds][nc] uint4 words, then nc float4 group scales at
-// 64 * ncmax, then nc float4 group sums at 80 * ncmax.
+// holds one expert's h block: [4 kinds][nc] uint4 words, then nc float4
+// group scales at 64 * nc, then nc float4 group sums at 80 * nc.
 __host__ __device__ inline D1Smem d1_smem(int nst, int stage, int rows, int ncmax) {
   D1Smem s;
   s.ent = nst * stage;
@@ -672,9 +687,7 @@ __global__ void __launch_bounds__((kD1Warps + 1) * 32, 1) down_b1_kernel(const _
         uint8_t* xb = xring + xs * L.xslot;
         mbar_arrive_expect_tx(&xfull[xs], 96 * nc);
         // every CTA reads these blocks: no evict-first hint
-        bulk_g2s(xb, a.ws.hx + static_cast<size_t>(d.c0) * 4, 64 * nc, &xfull[xs]);
-        bulk_g2s(xb + 64 * ncmax, a.ws.hx_scale + static_cast<size_t>(d.c0) * 4, 16 * nc, &xfull[xs]);
-        bulk_g2s(xb + 80 * ncmax, a.ws.hx_sum + static_cast<size_t>(d.c0) * 4, 16 * nc, &xfull[xs]);
+        bulk_g2s(xb, a.ws.hx + static_cast<size_t>(d.c0) * 96, 96 * nc, &xfull[xs]);
         jx = j + 1;
         const RecordOffsets& off = d.expert < 0 ? a.off_s : a.off_r;
         const uint32_t cb = RT * (d.Fe / 2), sbb = RT * (d.Fe / 16);
@@ -731,8 +744,8 @@ __global__ void __launch_bounds__((kD1Warps + 1) * 32, 1) down_b1_kernel(const _
       X.el[0] = g1.x, X.el[1] = g1.y, X.el[2] = g1.z, X.el[3] = g1.w;
       X.oh[0] = g2.x, X.oh[1] = g2.y, X.oh[2] = g2.z, X.oh[3] = g2.w;
       X.ol[0] = g3.x, X.ol[1] = g3.y, X.ol[2] = g3.z, X.ol[3] = g3.w;
-      const float4 sc4 = reinterpret_cast<const float4*>(xb + 64 * ncmax)[col];
-      const float4 sm4 = reinterpret_cast<const float4*>(xb + 80 * ncmax)[col];
+      const float4 sc4 = reinterpret_cast<const float4*>(xb + 64 * C)[col];
+      const float4 sm4 = reinterpret_cast<const float4*>(xb + 80 * C)[col];
       scp[0] = sc4.x * d.p, scp[1] = sc4.y * d.p, scp[2] = sc4.z * d.p, scp[3] = sc4.w * d.p;
       psx = d.p * ((sm4.x + sm4.y) + (sm4.z + sm4.w));
     }
@@ -945,7 +958,7 @@ __global__ void __launch_bounds__(kF1Threads, 1) ffn_b1_kernel(const __grid_cons
 
   if (warp == NCW) {  // ---------------- producer warp (lane 0 issues; the warp builds the table)
     F1Ent* tab = reinterpret_cast<F1Ent*>(smem + L.ent);
-    const uint64_t pol = policy_evict_first();
+    const uint64_t pol = policy_evict_first(), pol_h = policy_evict_last();
     unsigned* claim = &a.ws.ctl[2];
     const F1Div dr = f1_div(tiles_r), dn = f1_div(ndn), dp = f1_div(tiles_r + ndn);
     int it = 0, n_items = n_pre, n_ent = has_sh, checked = -1, cur = 0, nxt = 0;
@@ -1023,16 +1036,14 @@ __global__ void __launch_bounds__(kF1Threads, 1) ffn_b1_kernel(const __grid_cons
             bulk_g2s(st + 2 * cb + sbb, t.rec + off.up_sb + j0 * (H / 16), sbb, &full[s], pol);
           } else {
             const int Fe = sh ? a.Fs : a.F, nc = Fe / 32;
-            const uint32_t cb = RTD * (Fe / 2), sbb = RTD * (Fe / 16), xw = 64 * nc, xq = 16 * nc;
+            const uint32_t cb = RTD * (Fe / 2), sbb = RTD * (Fe / 16), xb = 96 * nc;
             const size_t r0 = static_cast<size_t>(tile) * RTD;
             s_p[s] = t.p;
-            mbar_arrive_expect_tx(&full[s], cb + sbb + xw + 2 * xq);
+            mbar_arrive_expect_tx(&full[s], cb + sbb + xb);
             bulk_g2s(st, t.rec + off.down_codes + r0 * (Fe / 2), cb, &full[s], pol);
             bulk_g2s(st + cb, t.rec + off.down_sb + r0 * (Fe / 16), sbb, &full[s], pol);
-            // every CTA reads the h blocks: no evict-first hint
-            bulk_g2s(st + cb + sbb, a.ws.hx + static_cast<size_t>(t.c0) * 4, xw, &full[s]);
-            bulk_g2s(st + cb + sbb + xw, a.ws.hx_scale + static_cast<size_t>(t.c0) * 4, xq, &full[s]);
-            bulk_g2s(st + cb + sbb + xw + xq, a.ws.hx_sum + static_cast<size_t>(t.c0) * 4, xq, &full[s]);
+            // the expert's h block, which every CTA reads: kept in L2
+            bulk_g2s(st + cb + sbb, a.ws.hx + static_cast<size_t>(t.c0) * 96, xb, &full[s], pol_h);
           }
         }
       }

@@ -35,10 +35,10 @@ struct Workspace {
                          // [8] fused single-token producers done claiming
   unsigned* hcnt;        // single token, fused kernel: gate|up items done per expert entry
   unsigned* tcnt;        // single token, fused kernel: experts done per down row tile
-  uint4* hx;             // single token: fixed-point h, per row [4 kinds][chunks] uint4 words
-                         // (word i of a uint4 = 8-value group i of the chunk)
-  float* hx_scale;       // single token: 2^e of each 8-value group, 4 per chunk
-  float* hx_sum;         // single token: plain sum of each 8-value group, 4 per chunk
+  uint8_t* hx;           // single token: fixed-point h, one block of 96 * nc bytes per
+                         // expert entry (nc chunks, starting at byte 96 * c0): [4 kinds]
+                         // [nc] uint4 words (word i of a uint4 = 8-value group i of the
+                         // chunk), then [nc] float4 group 2^e, then [nc] float4 group sums
   float* ypart;          // single token, fused kernel: [entry][H] weighted down outputs
   float* logits;         // [T][E]
   int* n_act;            // number of distinct routed experts this step
