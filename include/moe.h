@@ -166,10 +166,20 @@ int moe_decode_host(moe_layer *layer, const uint16_t *x_host, int32_t B,
  * so the workspace is ready for the next call. */
 int moe_check(const moe_layer *layer, void *workspace, void *stream);
 
+/* Number of kernels one moe_decode call with B tokens launches on this
+ * layer, as its dispatch would choose them (with a workspace sized for B):
+ * 2 for one token on the fused single-token kernel (router, fused gate|up +
+ * down), 3 where the single-token kernels are not fused, B times that for
+ * batches run one token at a time, 5 for the tensor-core chunk kernels and 3
+ * for the grouped kernels.  0 for B = 0; -1 on a bad handle or B outside
+ * [0, max_tokens].  Host-only: no device work. */
+int32_t moe_decode_kernels(const moe_layer *layer, int32_t B);
+
 /* Profiling hook.  With `events` pointing to four cudaEvent_t (passed as
  * void*), later moe_decode / moe_prefill_chunk calls on this layer record
  * events[0] before the router kernel, events[1] before the gate|up (or
- * grouped-GEMM) kernel, events[2] before the down kernel and events[3] after
+ * grouped-GEMM, or fused single-token) kernel, events[2] before the down
+ * kernel (right after the fused kernel, which has none) and events[3] after
  * it, and launch without programmatic dependent launch so the intervals are
  * per kernel.  NULL switches the hook off.  The events stay caller-owned. */
 int moe_set_profile_events(moe_layer *layer, void *const *events);

@@ -393,6 +393,18 @@ extern "C" int moe_decode_host(moe_layer* L, const uint16_t* x_host, int32_t B, 
   return MOE_OK;
 }
 
+extern "C" int32_t moe_decode_kernels(const moe_layer* L, int32_t B) {
+  if (!valid(L) || B < 0 || B > L->d.max_tokens) return -1;
+  if (B == 0) return 0;
+  LayerArgs a = base_args(L);
+  a.T = B;
+  const int b1 = moe::plan_b1(a, L->num_sms, L->smem_optin) ? (a.f1_nst > 0 ? 2 : 3) : 0;
+  if (B == 1 && b1) return b1;
+  if (per_token_decode(L, B) && b1) return B * b1;
+  if (moe::prefill_tc_ok(a, B) && L->maps.valid) return 5;
+  return 3;
+}
+
 extern "C" int moe_check(const moe_layer* L, void* ws, void* stream) {
   if (!valid(L)) return fail(MOE_ERR_ARG, "moe_check: invalid layer handle");
   if (!ws) return fail(MOE_ERR_ARG, "moe_check: workspace is NULL");

@@ -282,3 +282,17 @@ def test_large_prefill_chunk(large):
         _oracle_with_records(orc, wl, ids[t])
         ref, rids, rp = orc.token(xs[t])
         assert_token(t, of, ob, ids, w, ref, rids, rp)
+
+
+def test_decode_kernel_counts(large):
+    """moe_decode_kernels follows the dispatch: one token runs the router and
+    the fused gate|up + down kernel; 16 tokens over 512 experts run 16 such
+    passes; 64 tokens (64 * 16 > 512) the five tensor-core chunk kernels."""
+    _, dl, _ = large
+    L = moe.lib()
+    assert L.moe_decode_kernels(dl.handle, 0) == 0
+    assert L.moe_decode_kernels(dl.handle, 1) == 2
+    assert L.moe_decode_kernels(dl.handle, 16) == 32
+    assert L.moe_decode_kernels(dl.handle, 64) == 5
+    assert L.moe_decode_kernels(dl.handle, 129) == -1
+    assert L.moe_decode_kernels(None, 1) == -1
