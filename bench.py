@@ -351,12 +351,20 @@ def config_dict(s, B):
             "batch": B, "hidden": s.H, "experts": s.E, "top_k": s.k, "ffn": s.F,
             "shared_ffn": s.Fs,
             "l2": "inputs larger than L2: >=425 MB of distinct weights per step, hidden "
-                  "states rotated over a pool of distinct batches"}
+                  "states rotated over a pool of distinct batches",
+            "graphs": f"{GRAPH_STEPS} consecutive steps per CUDA graph replay (the remainder "
+                      "of K as one-step graphs); every step is a full layer call"}
 
 
 # ----------------------------------------------------------------- our arm
 
-def time_graphs(torch, graphs, K, W, stream, world, device):
+GRAPH_STEPS = 16  # consecutive steps captured in one CUDA graph
+
+
+def time_graphs(torch, graphs, chunks, K, W, stream, world, device):
+    """W warm-up steps, then exactly K timed steps: K // GRAPH_STEPS replays
+    of the multi-step graphs (rotating over the pool) and the remainder as
+    single-step graphs."""
     for i in range(W):
         graphs[i % len(graphs)].replay()
     torch.cuda.synchronize()
@@ -366,7 +374,9 @@ def time_graphs(torch, graphs, K, W, stream, world, device):
     t0 = time.time()
     with torch.cuda.stream(stream):
         e0.record(stream)
-        for i in range(K):
+        for i in range(K // GRAPH_STEPS):
+            chunks[i % len(chunks)].replay()
+        for i in range(K % GRAPH_STEPS):
             graphs[i % len(graphs)].replay()
         e1.record(stream)
     torch.cuda.synchronize()
@@ -419,8 +429,17 @@ def run_ours(args, world, rank, local):
             with torch.cuda.graph(g, stream=stream):
                 dl.decode(x[p], outs, stream.cuda_stream)
             graphs.append(g)
+        # multi-step graphs: GRAPH_STEPS consecutive steps over consecutive
+        # pool batches each, as a decode loop captures many layer calls at once
+        chunks = []
+        for c0 in range(0, max(1, args.pool - GRAPH_STEPS + 1), GRAPH_STEPS):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for p in range(c0, c0 + GRAPH_STEPS):
+                    dl.decode(x[p % args.pool], outs, stream.cuda_stream)
+            chunks.append(g)
         torch.cuda.synchronize()
-        return xs, x, outs, graphs, float(np.mean(distinct))
+        return xs, x, outs, graphs, chunks, float(np.mean(distinct))
 
     results = {}
     clocks = ClockSampler(gpu_id_for(local))
@@ -428,9 +447,9 @@ def run_ours(args, world, rank, local):
     time.sleep(0.3)
     main = None
     for B in batches:
-        xs, x, outs, graphs, distinct = make(B)
+        xs, x, outs, graphs, chunks, distinct = make(B)
         K = args.steps if B == args.batch else min(args.steps, 2000)
-        ms, t0, t1 = time_graphs(torch, graphs, K, args.warmup, stream, world, device)
+        ms, t0, t1 = time_graphs(torch, graphs, chunks, K, args.warmup, stream, world, device)
         assert dl.check(stream.cuda_stream) == moe.MOE_OK, moe.last_error()
         nbytes = layer_step_bytes(s, B, distinct, with_f32=True)
         r = {"tokens_per_s": B * K * world / (ms / 1e3), "ms_per_step": ms / K,
@@ -440,7 +459,7 @@ def run_ours(args, world, rank, local):
         results[B] = r
         if B == args.batch:
             main = dict(r, K=K, t0=t0, t1=t1, xs=xs, x=x, outs=outs, nbytes=nbytes)
-        del graphs
+        del graphs, chunks
     time.sleep(0.2)
     clocks.stop()
     clk = clocks.summary(main["t0"], main["t1"])

@@ -201,7 +201,7 @@ __device__ __forceinline__ void topk_group_b1(const LayerArgs& a, int lane, Logi
 
 
 constexpr int kR1Threads = 512;
-constexpr int kR1Rows = 8;  // rows per CTA pass: 64 CTAs for 512 experts leave most SMs to gate|up
+constexpr int kR1Rows = 16;  // rows per CTA pass: 32 CTAs for 512 experts leave most SMs to the fused kernel
 
 template <int KPL>  // logit slots per lane of the top-k warp: KPL * 32 >= E
 __global__ void __launch_bounds__(kR1Threads) router_b1_kernel(const __grid_constant__ LayerArgs a) {
