@@ -364,7 +364,7 @@ GRAPH_STEPS = 16  # consecutive steps captured in one CUDA graph
 def time_graphs(torch, graphs, chunks, K, W, stream, world, device):
     """W warm-up steps, then exactly K timed steps: K // GRAPH_STEPS replays
     of the multi-step graphs (rotating over the pool) and the remainder as
-    single-step graphs."""
+    single-step graphs; without multi-step graphs, K single-step replays."""
     for i in range(W):
         graphs[i % len(graphs)].replay()
     torch.cuda.synchronize()
@@ -374,9 +374,10 @@ def time_graphs(torch, graphs, chunks, K, W, stream, world, device):
     t0 = time.time()
     with torch.cuda.stream(stream):
         e0.record(stream)
-        for i in range(K // GRAPH_STEPS):
+        n_multi = K // GRAPH_STEPS if chunks else 0
+        for i in range(n_multi):
             chunks[i % len(chunks)].replay()
-        for i in range(K % GRAPH_STEPS):
+        for i in range(K - n_multi * GRAPH_STEPS):
             graphs[i % len(graphs)].replay()
         e1.record(stream)
     torch.cuda.synchronize()
@@ -587,7 +588,7 @@ def run_prefill(args, device, stream, hbm_peak, bf16_peak):
             dl.prefill(xs[p], outs, stream.cuda_stream)
         graphs.append(g)
     K = min(args.steps, 200)
-    ms, _, _ = time_graphs(torch, graphs, K, args.warmup, stream, 1, device)
+    ms, _, _ = time_graphs(torch, graphs, [], K, args.warmup, stream, 1, device)
     assert dl.check(stream.cuda_stream) == moe.MOE_OK, moe.last_error()
     d = float(np.mean(distinct))
     rec = record_bytes_unpadded(s.H, s.F)

@@ -24,9 +24,9 @@
 //                   ring ahead of its weight tiles and streams the CTA's row
 //                   tiles expert by expert; partial sums stay in registers
 //                   across experts (weighted by p_i), one reduction per tile.
-// router_b1_kernel  8-bit router rows (float path); top-k by repeated warp
-//                   argmax built on redux (max of the logit key, then min of
-//                   the id among the lanes holding it).
+// router_b1_kernel  8-bit router rows (float path); the last CTA takes the
+//                   top-k with bitonic sorts and merges across its 16 warps
+//                   on (logit, id) keys.
 #include <algorithm>
 #include <cfloat>
 
@@ -127,74 +127,112 @@ __device__ __forceinline__ B1Entry b1_entry(const LayerArgs& a, int idx, int has
 // Router (B = 1): 8-bit rows against the fixed-point token, then top-k.
 // ============================================================================
 
-// Top-k of one token's E logits (logit(e) reads one), softmax over the
-// chosen logits, and the single-token grouping; run by one whole warp.
-template <int KPL, typename Logit>
-__device__ __forceinline__ void topk_group_b1(const LayerArgs& a, int lane, Logit logit) {
-  const int E = a.E, k = a.k;
-  // Lane l holds the keys of experts l, l+32, ... in registers; a logit's
-  // key is its IEEE bit pattern mapped to an order-preserving unsigned (all
-  // finite logits map above 0; 0 marks a taken or absent expert).  Each lane
-  // keeps its best key; a round takes the warp's maximum (ties: the lower
-  // id), and only the lane that owned the winner rescans its keys.
-  uint32_t key[KPL];
+// ---- block-wide top-k ------------------------------------------------------
+// A candidate is one 64-bit key: the logit's IEEE bits mapped to an
+// order-preserving unsigned in the high word (every finite logit maps above
+// 0), 0xFFFFFFFF - id in the low word, so a larger key is a larger logit and,
+// on a tie, the lower id.  0 marks an absent candidate.
+__device__ __forceinline__ uint64_t tk_key(float l, int e) {
+  const uint32_t u = __float_as_uint(l + 0.0f);  // -0 and +0 compare equal: one key
+  const uint32_t k = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return (static_cast<uint64_t>(k) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(e));
+}
+
+__device__ __forceinline__ float tk_logit(uint64_t key) {
+  const uint32_t k = static_cast<uint32_t>(key >> 32);
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+__device__ __forceinline__ uint64_t shfl_xor64(uint64_t v, int m) {
+  const uint32_t lo = __shfl_xor_sync(kAll, static_cast<uint32_t>(v), m);
+  const uint32_t hi = __shfl_xor_sync(kAll, static_cast<uint32_t>(v >> 32), m);
+  return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+
+// Bitonic sort of the warp's 32 keys, largest in lane 0.
+__device__ __forceinline__ uint64_t warp_sort_desc(uint64_t v, int lane) {
 #pragma unroll
-  for (int s2 = 0; s2 < KPL; ++s2) {
-    const int e = s2 * 32 + lane;
-    uint32_t kk = 0u;
-    if (e < E) {
-      const uint32_t u = __float_as_uint(logit(e));
-      kk = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  for (int k2 = 2; k2 <= 32; k2 <<= 1)
+#pragma unroll
+    for (int j = k2 >> 1; j > 0; j >>= 1) {
+      const uint64_t o = shfl_xor64(v, j);
+      const bool keep_max = ((lane & j) == 0) == ((lane & k2) == 0);
+      v = keep_max ? (v > o ? v : o) : (v < o ? v : o);
     }
-    key[s2] = kk;
+  return v;
+}
+
+// Top 32 of two descending lists held one key per lane (a) and (b), returned
+// descending: max(a[i], b[31 - i]) is bitonic and holds the 32 largest; the
+// half-cleaners sort it.
+__device__ __forceinline__ uint64_t warp_merge_desc(uint64_t a, uint64_t b_rev, int lane) {
+  uint64_t v = a > b_rev ? a : b_rev;
+#pragma unroll
+  for (int j = 16; j > 0; j >>= 1) {
+    const uint64_t o = shfl_xor64(v, j);
+    v = ((lane & j) == 0) ? (v > o ? v : o) : (v < o ? v : o);
   }
-  uint32_t bk = 0u;
-  int bs = 0;
+  return v;
+}
+
+// Bitonic sort of the warp's 32 values, smallest in lane 0.
+__device__ __forceinline__ uint32_t warp_sort_asc32(uint32_t v, int lane) {
 #pragma unroll
-  for (int s2 = 0; s2 < KPL; ++s2)  // ascending slot = ascending id: ties keep the lower
-    if (key[s2] > bk) bk = key[s2], bs = s2;
-  float myl = 0.f;
-  int myi = 0;
-  for (int i = 0; i < k; ++i) {
-    const uint32_t top = __reduce_max_sync(kAll, bk);
-    const unsigned win = __reduce_min_sync(kAll, (bk == top && top != 0u) ? static_cast<unsigned>(bs * 32 + lane)
-                                                                         : 0xFFFFFFFFu);
-    int w = static_cast<int>(win);
-    if (w >= E) {  // only with non-finite logits (outside the contract)
-      if (lane == 0) latch_error(&a.ws.ctl[0], kErrRange);
-      w = i;
-    }
-    if (lane == i) {
-      myi = w;
-      myl = __uint_as_float((top & 0x80000000u) ? (top & 0x7FFFFFFFu) : ~top);
-    }
-    if ((w & 31) == lane) {  // the winner's lane drops it and finds its next best
-      const int ws = w >> 5;
-      bk = 0u, bs = 0;
+  for (int k2 = 2; k2 <= 32; k2 <<= 1)
 #pragma unroll
-      for (int s2 = 0; s2 < KPL; ++s2) {
-        if (s2 == ws) key[s2] = 0u;
-        if (key[s2] > bk) bk = key[s2], bs = s2;
-      }
+    for (int j = k2 >> 1; j > 0; j >>= 1) {
+      const uint32_t o = __shfl_xor_sync(kAll, v, j);
+      const bool keep_min = ((lane & j) == 0) == ((lane & k2) == 0);
+      v = keep_min ? min(v, o) : max(v, o);
     }
+  return v;
+}
+
+// Top-k of one token's E <= 1024 logits (logit(e) reads one) by the whole
+// 16-warp block, then the softmax over the chosen logits and the
+// single-token grouping.  Warp w sorts candidates 32w .. 32w + 31 (and, for
+// E > 512, merges in 512 + 32w ..); a tree of warp merges halves the lists
+// four times, so warp 0 ends with the 32 largest keys in order.  The result
+// is the selection by (logit descending, id ascending), as the repeated
+// argmax defines it.  `lists` is [16][32] keys of shared memory.
+template <typename Logit>
+__device__ __forceinline__ void topk_block_b1(const LayerArgs& a, uint64_t (*lists)[32], Logit logit) {
+  const int E = a.E, k = a.k, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  int e = warp * 32 + lane;
+  uint64_t v = warp_sort_desc(e < E ? tk_key(logit(e), e) : 0ull, lane);
+  e += 512;
+  if (E > 512) {
+    const uint64_t w2 = warp_sort_desc(e < E ? tk_key(logit(e), e) : 0ull, lane);
+    v = warp_merge_desc(v, shfl_xor64(w2, 31), lane);
+  }
+  lists[warp][lane] = v;
+  __syncthreads();
+#pragma unroll
+  for (int n = 8; n >= 1; n >>= 1) {
+    if (warp < n) lists[warp][lane] = warp_merge_desc(lists[warp][lane], lists[warp + n][31 - lane], lane);
+    __syncthreads();
+  }
+  if (warp != 0) return;
+  const uint64_t key = lists[0][lane];
+  int myi = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(key));
+  float myl = tk_logit(key);
+  if (lane < k && (key == 0ull || myi >= E)) {  // only with non-finite logits (outside the contract)
+    latch_error(&a.ws.ctl[0], kErrRange);
+    myi = lane, myl = 0.f;
   }
   const float lmax = __shfl_sync(kAll, myl, 0);
   const float ex = (lane < k) ? expf(myl - lmax) : 0.f;
   const float z = warp_add(ex);
   if (lane < k) a.ids[lane] = myi, a.weights[lane] = ex / z;
-  // Grouping for one token: active experts in ascending id, one pair each.
-  // Sort the k ids with a rank count (k <= 32).
-  int rank = 0;
-  for (int j = 0; j < k; ++j) {
-    const int oj = __shfl_sync(kAll, myi, j);
-    if (lane < k && oj < myi) ++rank;
-  }
+  // grouping for one token: active experts in ascending id, one pair each;
+  // the sort carries each expert's position in ids[] in the low 5 bits
+  const uint32_t s = warp_sort_asc32(lane < k ? (static_cast<uint32_t>(myi) << 5) | lane : 0xFFFFFFFFu, lane);
   if (lane < k) {
-    a.ws.act_expert[rank] = myi;
-    a.ws.act_off[rank] = rank;
-    a.ws.act_cnt[rank] = 1;
-    a.ws.pair_token[rank] = 0;
-    a.ws.pair_slot[rank] = lane;
+    a.ws.act_expert[lane] = static_cast<int>(s >> 5);
+    a.ws.act_off[lane] = lane;
+    a.ws.act_cnt[lane] = 1;
+    a.ws.pair_token[lane] = 0;
+    a.ws.pair_slot[lane] = static_cast<int>(s & 31u);
   }
   if (lane == 0) *a.ws.n_act = k;
 }
@@ -203,7 +241,6 @@ __device__ __forceinline__ void topk_group_b1(const LayerArgs& a, int lane, Logi
 constexpr int kR1Threads = 512;
 constexpr int kR1Rows = 16;  // rows per CTA pass: 32 CTAs for 512 experts leave most SMs to the fused kernel
 
-template <int KPL>  // logit slots per lane of the top-k warp: KPL * 32 >= E
 __global__ void __launch_bounds__(kR1Threads) router_b1_kernel(const __grid_constant__ LayerArgs a) {
   extern __shared__ __align__(16) float rsm[];
   pdl_launch_dependents();
@@ -272,9 +309,9 @@ __global__ void __launch_bounds__(kR1Threads) router_b1_kernel(const __grid_cons
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  if (warp != 0) return;
-  topk_group_b1<KPL>(a, lane, [&](int e) { return __ldcg(a.ws.logits + e); });
-  if (lane == 0) a.ws.ctl[1] = 0u;
+  __shared__ uint64_t lists[16][32];
+  topk_block_b1(a, lists, [&](int e) { return __ldcg(a.ws.logits + e); });
+  if (tid == 0) a.ws.ctl[1] = 0u;
 }
 
 size_t router_b1_smem_bytes(int E) {
@@ -820,9 +857,9 @@ size_t down_b1_smem_bytes(const LayerArgs& a) {
 // items (rth gate + rth up rows of one expert, as in gateup_b1_kernel) and
 // down items (RTD rows of H of one expert's down matrix, with the expert's
 // fixed-point h block copied in the same stage).  The list runs
-//   G(shared) D(shared) G(1) ... G(n) interleaved with D(1) ... D(n),
-// with the routed experts' down items kF1Lag experts behind their gate|up
-// items (G(1) .. G(kF1Lag + 1), D(1), G(kF1Lag + 2), D(2), ...), so a CTA
+//   G(0) ... G(n - 1) interleaved with D(0) ... D(n - 1),
+// with every expert's down items kF1Lag experts behind its gate|up items
+// (G(0) G(1) G(2) G(3) D(0) G(4) D(1) ...; entry 0 the shared expert), so a CTA
 // reaches an expert's down items several ring depths after that expert's
 // last gate|up item was claimed and its h is normally complete; the
 // producer checks a per-expert completion counter before it issues a down
@@ -846,7 +883,7 @@ constexpr int kF1Warps = 16;                     // consumer warps
 constexpr int kF1Threads = (kF1Warps + 3) * 32;  // + producer + two epilogue warps
 constexpr int kF1SmemBudget = 222 * 1024;
 constexpr int kF1MaxStages = 16;
-constexpr int kF1Lag = 3;  // routed experts between an expert's gate|up and down items
+constexpr int kF1Lag = 3;  // experts between an expert's gate|up and down items
 
 struct F1Smem {
   int wsum, info, ent, bars, total;
@@ -864,7 +901,7 @@ __host__ __device__ inline F1Smem f1_smem(int nst, int stage) {
   F1Smem s;
   s.wsum = nst * stage;                      // [NST][NCW][8] per-warp row sums
   s.info = s.wsum + nst * kF1Warps * 8 * 4;  // [16] item codes, [16] routing weights
-  s.ent = s.info + 2 * kF1MaxStages * 4;     // [kMaxTopK + 1] expert table
+  s.ent = s.info + 2 * kF1MaxStages * 4 + 16;  // (+16: the step's expert count) expert table
   s.bars = s.ent + (kMaxTopK + 1) * static_cast<int>(sizeof(F1Ent));
   s.total = s.bars + 3 * nst * 8 + 16;       // full, empty, partial sums done
   return s;
@@ -888,34 +925,30 @@ __device__ __forceinline__ int f1_q(int n, const F1Div& v) {
 // Item code in shared memory: entry << 20 | tile << 1 | gate (-1: end).
 __device__ __forceinline__ int f1_code(int gate, int entry, int tile) { return (entry << 20) | (tile << 1) | gate; }
 
-// Claim index -> (gate, entry, tile) for a list with the shared expert's
-// items first (tiles_s gate|up, then ndn down) and n_act routed experts:
-// G(1..m) with m = min(kF1Lag, n_act), then the pairs G(r) D(r - kF1Lag)
-// for r = kF1Lag + 1 .. n_act, then the last m experts' down items.
-// Routed expert r (1-based) is entry has_sh + r - 1.
-// The divisions use the reciprocals dr (tiles_r), dn (ndn), dp (tiles_r + ndn).
-__device__ __forceinline__ int f1_item(int i, int has_sh, int tiles_s, int n_act, const F1Div& dr,
+// Claim index -> (gate, entry, tile) for the n_ent experts of the step
+// (entry 0 the shared expert when there is one, its gate|up block tiles_s
+// items; every other gate|up block tiles_r items, every down block ndn
+// items): G(0) .. G(m - 1) with m = min(kF1Lag, n_ent), then the pairs
+// G(m + p) D(p), then the last m experts' down items.  Only G(0) of the
+// shared expert comes before the router's output is needed.  The divisions
+// use the reciprocals dr (tiles_r), dn (ndn), dp (tiles_r + ndn).
+__device__ __forceinline__ int f1_item(int i, int has_sh, int tiles_s, int n_ent, const F1Div& dr,
                                        const F1Div& dn, const F1Div& dp) {
-  const int tiles_r = dr.d, ndn = dn.d;
-  if (has_sh) {
-    if (i < tiles_s) return f1_code(1, 0, i);
-    i -= tiles_s;
-    if (i < ndn) return f1_code(0, 0, i);
-    i -= ndn;
-  }
-  const int e0 = has_sh - 1;  // entry of routed expert r is e0 + r
-  const int m = min(kF1Lag, n_act), head = m * tiles_r;
+  const int tiles_r = dr.d, ndn = dn.d, m = min(kF1Lag, n_ent);
+  const int g0 = has_sh ? tiles_s : tiles_r;
+  if (i < g0) return f1_code(1, 0, i);
+  const int head = g0 + (m - 1) * tiles_r;
   if (i < head) {
-    const int q = f1_q(i, dr);
-    return f1_code(1, e0 + 1 + q, i - q * tiles_r);
+    const int j = i - g0, q = f1_q(j, dr);
+    return f1_code(1, 1 + q, j - q * tiles_r);
   }
-  const int j = i - head, per = dp.d, pairs = n_act - m, body = pairs * per;
+  const int j = i - head, per = dp.d, body = (n_ent - m) * per;
   if (j < body) {
     const int p = f1_q(j, dp), off = j - p * per;
-    return off < tiles_r ? f1_code(1, e0 + kF1Lag + 1 + p, off) : f1_code(0, e0 + 1 + p, off - tiles_r);
+    return off < tiles_r ? f1_code(1, m + p, off) : f1_code(0, p, off - tiles_r);
   }
   const int t = j - body, q = f1_q(t, dn);
-  return f1_code(0, e0 + n_act - m + 1 + q, t - q * ndn);
+  return f1_code(0, n_ent - m + q, t - q * ndn);
 }
 
 // Waits (bounded) until *cnt >= need; acquire.
@@ -941,6 +974,7 @@ __global__ void __launch_bounds__(kF1Threads, 1) ffn_b1_kernel(const __grid_cons
   float* wsum = reinterpret_cast<float*>(smem + L.wsum);
   volatile int* s_code = reinterpret_cast<volatile int*>(smem + L.info);
   volatile float* s_p = reinterpret_cast<volatile float*>(smem + L.info + kF1MaxStages * 4);
+  volatile int* s_nent = reinterpret_cast<volatile int*>(smem + L.info + 2 * kF1MaxStages * 4);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* empty = full + NST;   // consumers and the position's epilogue warp are done
   uint64_t* pdone = empty + NST;  // every consumer's row sums of the position are in
@@ -954,7 +988,7 @@ __global__ void __launch_bounds__(kF1Threads, 1) ffn_b1_kernel(const __grid_cons
 
   const int has_sh = a.Fs > 0 ? 1 : 0;
   const int tiles_s = has_sh ? a.Fs / rth : 0, tiles_r = a.F / rth, ndn = H / RTD;
-  const int n_pre = has_sh ? tiles_s + ndn : 0;  // items that need no routing
+  const int n_pre = has_sh ? tiles_s : 0;  // items that need no routing: the shared gate|up
 
   if (warp == NCW) {  // ---------------- producer warp (lane 0 issues; the warp builds the table)
     F1Ent* tab = reinterpret_cast<F1Ent*>(smem + L.ent);
@@ -990,8 +1024,9 @@ __global__ void __launch_bounds__(kF1Threads, 1) ffn_b1_kernel(const __grid_cons
           tab[has_sh + j] = t;
         }
         __syncwarp();
-        n_items = n_pre + n_act * (tiles_r + ndn);
+        n_items = n_pre + n_act * tiles_r + (has_sh + n_act) * ndn;
         n_ent = has_sh + n_act;
+        if (lane == 0) *s_nent = n_ent;  // for the epilogue warps, before any routed item is issued
       }
       if (lane == 0) {
         for (;; ++it, pos.next(NST)) {
@@ -1000,7 +1035,7 @@ __global__ void __launch_bounds__(kF1Threads, 1) ffn_b1_kernel(const __grid_cons
           if (i >= n_items) break;
           cur = nxt;
           nxt = static_cast<int>(atomicAdd(claim, 1u));
-          const int code = f1_item(i, has_sh, tiles_s, n_ent - has_sh, dr, dn, dp);
+          const int code = f1_item(i, has_sh, tiles_s, n_ent, dr, dn, dp);
           const int gate = code & 1, e = code >> 20, tile = (code >> 1) & 0x7FFFF;
           const bool sh = has_sh && e == 0;
           const RecordOffsets& off = sh ? a.off_s : a.off_r;
@@ -1148,27 +1183,22 @@ __global__ void __launch_bounds__(kF1Threads, 1) ffn_b1_kernel(const __grid_cons
         unsigned old = 0;
         if (lane == 0) old = atom_add_acq_rel_gpu(&a.ws.tcnt[tile], 1u);
         old = __shfl_sync(kAll, old, 0);
-        // a shared-expert item with old == 0 cannot be the tile's last (every
-        // step has routed experts); otherwise the router is done: read n_act
-        if (!sh_row || old > 0) {
-          if (n_ent < 0) {
-            pdl_wait();
-            n_ent = has_sh + clamp_n_act(a);
-          }
-          if (old + 1 == static_cast<unsigned>(n_ent)) {  // every expert's rows of this tile are in
+        // the producer wrote the step's expert count before it issued any
+        // down item (every down item comes after the routing)
+        if (n_ent < 0) n_ent = *s_nent;
+        if (old + 1 == static_cast<unsigned>(n_ent)) {  // every expert's rows of this tile are in
 #pragma unroll
-            for (int k2 = 0; k2 < 2; ++k2) {
-              const int r = k2 * 32 + lane;
-              if (r < RTD) {
-                const size_t row = static_cast<size_t>(tile) * RTD + r;
-                float out = 0.f;
-                for (int j = 0; j < n_ent; ++j) out += __ldcg(a.ws.ypart + static_cast<size_t>(j) * H + row);
-                a.out_bf16[row] = f32_to_bf16_rne(out);
-                if (a.out_f32) a.out_f32[row] = out;
-              }
+          for (int k2 = 0; k2 < 2; ++k2) {
+            const int r = k2 * 32 + lane;
+            if (r < RTD) {
+              const size_t row = static_cast<size_t>(tile) * RTD + r;
+              float out = 0.f;
+              for (int j = 0; j < n_ent; ++j) out += __ldcg(a.ws.ypart + static_cast<size_t>(j) * H + row);
+              a.out_bf16[row] = f32_to_bf16_rne(out);
+              if (a.out_f32) a.out_f32[row] = out;
             }
-            if (lane == 0) a.ws.tcnt[tile] = 0u;
           }
+          if (lane == 0) a.ws.tcnt[tile] = 0u;
         }
       }
     }
@@ -1367,8 +1397,7 @@ bool plan_b1(LayerArgs& a, int num_sms, int smem_optin) {
 }
 
 cudaError_t set_b1_attributes(int smem_optin) {
-  const void* fns[] = {(const void*)router_b1_kernel<4>, (const void*)router_b1_kernel<8>,
-                       (const void*)router_b1_kernel<16>, (const void*)router_b1_kernel<32>,
+  const void* fns[] = {(const void*)router_b1_kernel,
                        (const void*)gateup_b1_kernel<4>,
                        (const void*)gateup_b1_kernel<8>, (const void*)down_b1_kernel,
                        (const void*)ffn_b1_kernel<4>, (const void*)ffn_b1_kernel<8>};
@@ -1403,16 +1432,10 @@ static cudaError_t mark1(const LayerArgs& a, int i, cudaStream_t st) {
   return a.prof_on ? cudaEventRecord(static_cast<cudaEvent_t>(a.prof[i]), st) : cudaSuccess;
 }
 
-static const void* router1_fn(int E) {
-  if (E <= 128) return (const void*)router_b1_kernel<4>;
-  if (E <= 256) return (const void*)router_b1_kernel<8>;
-  if (E <= 512) return (const void*)router_b1_kernel<16>;
-  return (const void*)router_b1_kernel<32>;
-}
 
 static cudaError_t launch_router1(const LayerArgs& a, int num_sms, cudaStream_t st) {
   const int rgrid = std::max(1, std::min((a.E + kR1Rows - 1) / kR1Rows, 2 * num_sms));
-  return launch1(router1_fn(a.E), rgrid, kR1Threads, router_b1_smem_bytes(a.E), st, false, a);
+  return launch1((const void*)router_b1_kernel, rgrid, kR1Threads, router_b1_smem_bytes(a.E), st, false, a);
 }
 
 static cudaError_t launch_gateup1(const LayerArgs& a, int part, int num_sms, cudaStream_t st, bool pdl) {
