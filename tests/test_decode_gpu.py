@@ -296,3 +296,30 @@ def test_decode_kernel_counts(large):
     assert L.moe_decode_kernels(dl.handle, 64) == 5
     assert L.moe_decode_kernels(dl.handle, 129) == -1
     assert L.moe_decode_kernels(None, 1) == -1
+
+
+def test_router_exact_ties_over_512_experts():
+    """Router rows repeat every 40 experts, so each logit value is shared by
+    15 experts.  The selection by (logit descending, id ascending) must take
+    the lowest ids of the tied classes, over E = 600 > 512 candidates (two
+    candidates per thread in the top-k's first sorts) and k = 32."""
+    shape = synth.Shape(256, 600, 32, 64, 0)
+    hl = HostLayer(shape, seed=61)
+    for e in range(40, shape.E):
+        hl.router_codes[e] = hl.router_codes[e % 40]
+        hl.router_sb[e] = hl.router_sb[e % 40]
+    orc = hl.oracle()
+    for attempt in range(64):  # distinct classes at least 1e-3 apart
+        x = synth.hidden(61, 0, 0, shape.H, attempt=attempt)
+        lg = orc.route(x)[0]
+        if np.diff(np.sort(lg[:40])).min() >= 1e-3:
+            break
+    else:
+        raise RuntimeError("no hidden state with separated logit classes")
+    dl = device_from_host(hl, max_tokens=1)
+    of, ob, ids, w = run(dl, x[None])
+    ref, rids, rp = orc.token(x)
+    assert_token(0, of, ob, ids, w, ref, rids, rp)
+    chosen = set(int(i) for i in ids[0])
+    for i in chosen:  # every lower id of the same class is chosen too
+        assert all(j in chosen for j in range(i % 40, i, 40))
