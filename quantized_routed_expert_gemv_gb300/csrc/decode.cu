@@ -87,6 +87,20 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const __grid_con
   float beta_r = 0.f;
   if (tid < NT * kRouterRows && a.beta && er0 + tid % kRouterRows < E) beta_r = __ldg(a.beta + er0 + tid % kRouterRows);
 
+  // The activations of the next token pass are loaded while this one is
+  // computed: raw bf16 words, two uint4 per token.
+  uint4 xr[NT][2];
+  auto load_x = [&](int pi) {
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      xr[t][0] = xr[t][1] = make_uint4(0, 0, 0, 0);
+      if (act && pi < p_hi && pi * NT + t < T) {
+        const uint4* xp = reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(pi * NT + t) * H + tid * 16);
+        xr[t][0] = __ldg(xp), xr[t][1] = __ldg(xp + 1);
+      }
+    }
+  };
+  load_x(p_lo);
   for (int pi = p_lo; pi < p_hi; ++pi) {
     const int t0 = pi * NT;
     float2 X[NT][8];
@@ -97,9 +111,8 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const __grid_con
 #pragma unroll
       for (int j = 0; j < 8; ++j) X[t][j] = make_float2(0.f, 0.f);
       if (act && t0 + t < T) {
-        const uint4* xp = reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(t0 + t) * H + tid * 16);
-        const uint4 x0 = __ldg(xp), x1 = __ldg(xp + 1);
-        const uint32_t xw[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+        const uint32_t xw[8] = {xr[t][0].x, xr[t][0].y, xr[t][0].z, xr[t][0].w,
+                                xr[t][1].x, xr[t][1].y, xr[t][1].z, xr[t][1].w};
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const float lo = bf16lo(xw[j]), hi = bf16hi(xw[j]);
@@ -109,6 +122,7 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const __grid_con
         }
       }
     }
+    load_x(pi + 1);  // in flight while this pass is computed
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
 #pragma unroll
@@ -151,6 +165,16 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const __grid_con
   // registers (a logit's IEEE bits mapped to an order-preserving unsigned;
   // 0 marks a taken or absent expert) and its best key; a round takes the
   // warp's maximum (ties: the lower id) and only the winner's lane rescans.
+  // The warp's next token's logits are loaded while this one is selected.
+  float lnext[KPL];
+  auto load_logits = [&](int t) {
+#pragma unroll
+    for (int s2 = 0; s2 < KPL; ++s2) {
+      const int e = s2 * 32 + lane;
+      lnext[s2] = (t < T && e < E) ? __ldcg(a.ws.logits + static_cast<size_t>(t) * E + e) : 0.f;
+    }
+  };
+  load_logits(warp);
   for (int t = warp; t < T; t += NW) {
     uint32_t key[KPL];
 #pragma unroll
@@ -158,11 +182,12 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const __grid_con
       const int e = s2 * 32 + lane;
       uint32_t kk = 0u;
       if (e < E) {
-        const uint32_t u = __float_as_uint(__ldcg(a.ws.logits + static_cast<size_t>(t) * E + e));
+        const uint32_t u = __float_as_uint(lnext[s2]);
         kk = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
       }
       key[s2] = kk;
     }
+    load_logits(t + NW);
     uint32_t bk = 0u;
     int bs = 0;
 #pragma unroll

@@ -199,30 +199,40 @@ __global__ void __launch_bounds__(kPackThreads) pf_pack_kernel(const __grid_cons
     if (tok < 0 || tok >= a.T) tok = -1;
     uint16_t* xb = a.pf.xc + static_cast<size_t>(xrow) * H;
     float* sxb = a.pf.sx + static_cast<size_t>(xrow) * (H / 64);
-    for (int u0 = 0; u0 < units; u0 += 32) {
-      const int u = u0 + lane;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      float s = 0.f;
-      if (u < units && tok >= 0) {
-        v = __ldg(reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(tok) * H) + u);
-        s = bf16lo(v.x) + bf16hi(v.x) + bf16lo(v.y) + bf16hi(v.y) + bf16lo(v.z) + bf16hi(v.z) + bf16lo(v.w) +
-            bf16hi(v.w);
+    // batches of 8 units per lane: every load of a batch is in flight
+    // before the first one is used
+    constexpr int kBatch = 8;
+    for (int u0 = 0; u0 < units; u0 += 32 * kBatch) {
+      uint4 vb[kBatch];
+#pragma unroll
+      for (int q = 0; q < kBatch; ++q) {
+        const int u = u0 + q * 32 + lane;
+        vb[q] = make_uint4(0, 0, 0, 0);
+        if (u < units && tok >= 0) vb[q] = __ldg(reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(tok) * H) + u);
       }
-      // group sum over the 8 lanes (64 values) of this lane's group
-      s += __shfl_xor_sync(kAllLanes, s, 1);
-      s += __shfl_xor_sync(kAllLanes, s, 2);
-      s += __shfl_xor_sync(kAllLanes, s, 4);
-      if (u < units) {
-        // K order inside the core row: 0,4,1,5,2,6,3,7
-        uint4 w;
-        w.x = __byte_perm(v.x, v.z, 0x5410);
-        w.y = __byte_perm(v.x, v.z, 0x7632);
-        w.z = __byte_perm(v.y, v.w, 0x5410);
-        w.w = __byte_perm(v.y, v.w, 0x7632);
-        const int c = u >> 4, k8 = u & 15;
-        const size_t e = static_cast<size_t>(c) * np * 128 + (k8 * (np >> 3) + (nn >> 3)) * 64 + (nn & 7) * 8;
-        *reinterpret_cast<uint4*>(xb + e) = w;
-        if ((lane & 7) == 0) sxb[(u >> 3) * np + nn] = s;
+#pragma unroll
+      for (int q = 0; q < kBatch; ++q) {
+        const int u = u0 + q * 32 + lane;
+        if (u0 + q * 32 >= units) break;  // the same on every lane
+        const uint4 v = vb[q];
+        float s = bf16lo(v.x) + bf16hi(v.x) + bf16lo(v.y) + bf16hi(v.y) + bf16lo(v.z) + bf16hi(v.z) +
+                  bf16lo(v.w) + bf16hi(v.w);
+        // group sum over the 8 lanes (64 values) of this lane's group
+        s += __shfl_xor_sync(kAllLanes, s, 1);
+        s += __shfl_xor_sync(kAllLanes, s, 2);
+        s += __shfl_xor_sync(kAllLanes, s, 4);
+        if (u < units) {
+          // K order inside the core row: 0,4,1,5,2,6,3,7
+          uint4 w;
+          w.x = __byte_perm(v.x, v.z, 0x5410);
+          w.y = __byte_perm(v.x, v.z, 0x7632);
+          w.z = __byte_perm(v.y, v.w, 0x5410);
+          w.w = __byte_perm(v.y, v.w, 0x7632);
+          const int c = u >> 4, k8 = u & 15;
+          const size_t e = static_cast<size_t>(c) * np * 128 + (k8 * (np >> 3) + (nn >> 3)) * 64 + (nn & 7) * 8;
+          *reinterpret_cast<uint4*>(xb + e) = w;
+          if ((lane & 7) == 0) sxb[(u >> 3) * np + nn] = s;
+        }
       }
     }
   }
