@@ -53,8 +53,16 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int la
 constexpr int kRouterThreads = 512;
 constexpr int kRouterRows = 4;  // rows in flight per iteration
 
-// Thread c owns 16-byte chunk c of every router row (its 16 activations stay
-// in registers); each CTA walks rows 4 at a time with all loads in flight.
+// Warp groups: a group of WPR = ceil(H / 512) warps covers a router row (its
+// thread c owns 16-byte chunk c, 16 activations); the block's G = 16 / WPR
+// groups take different tokens of a pass, so small H keeps every warp busy.
+__host__ __device__ inline int router_groups(int H) {
+  const int wpr = ((H >> 4) + 31) / 32;
+  return (kRouterThreads / 32) / wpr;
+}
+
+// Each CTA holds kRouterRows router rows in registers (all loads in flight at
+// once) and walks its token passes of NT tokens per group.
 template <int NT, int KPL>  // KPL: logit slots per lane of a top-k warp, KPL * 32 >= E
 __global__ void __launch_bounds__(kRouterThreads) router_kernel(const __grid_constant__ LayerArgs a) {
   extern __shared__ __align__(16) float rsm[];
@@ -62,30 +70,33 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const __grid_con
   const int H = a.H, E = a.E, T = a.T, k = a.k;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   constexpr int NW = kRouterThreads / 32;
-  const int nchunk = H >> 4;
-  const bool act = tid < nchunk;
-  float* red = rsm;  // [NT][kRouterRows][NW]
+  const int nchunk = H >> 4, WPR = (nchunk + 31) / 32, G = NW / WPR;
+  const int g = warp / WPR, wi = warp - g * WPR, c = tid - g * WPR * 32;
+  const bool act = g < G && c < nchunk;
+  float* red = rsm;  // [G][NT][kRouterRows][WPR]
 
   // The grid is (row blocks of kRouterRows experts) x (token blocks): a CTA
-  // loads its router rows once and walks its share of the token pairs.
+  // loads its router rows once and walks its share of the token passes.
   const int RB = (E + kRouterRows - 1) / kRouterRows;
   const int TB = max(1, static_cast<int>(gridDim.x) / RB);
   const int rb = blockIdx.x % RB, tb = blockIdx.x / RB;
   const int er0 = rb * kRouterRows;
-  const int npair = (T + NT - 1) / NT, ppb = (npair + TB - 1) / TB;
-  const int p_lo = tb * ppb, p_hi = min(npair, p_lo + ppb);
+  const int TP = NT * G;  // tokens per pass
+  const int npass = (T + TP - 1) / TP, ppb = (npass + TB - 1) / TB;
+  const int p_lo = tb * ppb, p_hi = min(npass, p_lo + ppb);
   uint4 q[kRouterRows];
   uint32_t sbw[kRouterRows];
 #pragma unroll
   for (int r = 0; r < kRouterRows; ++r) {
     q[r] = make_uint4(0, 0, 0, 0), sbw[r] = 0;
     if (act && er0 + r < E && tb < TB) {
-      q[r] = __ldg(reinterpret_cast<const uint4*>(a.rcodes + static_cast<size_t>(er0 + r) * H) + tid);
-      sbw[r] = __ldg(a.rsb + static_cast<size_t>(er0 + r) * (H >> 6) + (tid >> 2));
+      q[r] = __ldg(reinterpret_cast<const uint4*>(a.rcodes + static_cast<size_t>(er0 + r) * H) + c);
+      sbw[r] = __ldg(a.rsb + static_cast<size_t>(er0 + r) * (H >> 6) + (c >> 2));
     }
   }
+  const int nout = G * NT * kRouterRows;  // logits per pass, one per thread tid < nout
   float beta_r = 0.f;
-  if (tid < NT * kRouterRows && a.beta && er0 + tid % kRouterRows < E) beta_r = __ldg(a.beta + er0 + tid % kRouterRows);
+  if (tid < nout && a.beta && er0 + tid % kRouterRows < E) beta_r = __ldg(a.beta + er0 + tid % kRouterRows);
 
   // The activations of the next token pass are loaded while this one is
   // computed: raw bf16 words, two uint4 per token.
@@ -94,15 +105,16 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const __grid_con
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
       xr[t][0] = xr[t][1] = make_uint4(0, 0, 0, 0);
-      if (act && pi < p_hi && pi * NT + t < T) {
-        const uint4* xp = reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(pi * NT + t) * H + tid * 16);
+      const int tok = pi * TP + g * NT + t;
+      if (act && pi < p_hi && tok < T) {
+        const uint4* xp = reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(tok) * H + c * 16);
         xr[t][0] = __ldg(xp), xr[t][1] = __ldg(xp + 1);
       }
     }
   };
   load_x(p_lo);
   for (int pi = p_lo; pi < p_hi; ++pi) {
-    const int t0 = pi * NT;
+    const int t0 = pi * TP + g * NT;  // this group's first token of the pass
     float2 X[NT][8];
     float SX[NT];
 #pragma unroll
@@ -129,16 +141,17 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const __grid_con
       for (int r = 0; r < kRouterRows; ++r) {
         const float p = fmaf(bf16lo(sbw[r]) * 0x1p64f, dot16_u8(q[r], X[t]), bf16hi(sbw[r]) * SX[t]);
         const float v = warp_sum(p);
-        if (lane == 0) red[(t * kRouterRows + r) * NW + warp] = v;
+        if (lane == 0 && g < G) red[((g * NT + t) * kRouterRows + r) * WPR + wi] = v;
       }
     }
     __syncthreads();
-    if (tid < NT * kRouterRows) {
-      const int t = tid / kRouterRows, r = tid % kRouterRows;
-      if (t0 + t < T && er0 + r < E) {
+    if (tid < nout) {  // tid = (group, token, row)
+      const int gg = tid / (NT * kRouterRows), t = (tid / kRouterRows) % NT, r = tid % kRouterRows;
+      const int tok = pi * TP + gg * NT + t;
+      if (tok < T && er0 + r < E) {
         float v = 0.f;
-        for (int w = 0; w < NW; ++w) v += red[tid * NW + w];
-        a.ws.logits[static_cast<size_t>(t0 + t) * E + er0 + r] = v + beta_r;
+        for (int w = 0; w < WPR; ++w) v += red[tid * WPR + w];
+        a.ws.logits[static_cast<size_t>(tok) * E + er0 + r] = v + beta_r;
       }
     }
     __syncthreads();
@@ -774,7 +787,8 @@ static cudaError_t launch_router_g(const LayerArgs& a, int num_sms, cudaStream_t
   const bool one = (a.T == 1);
   const int nt = one ? 1 : 2;
   const int rb = (a.E + kRouterRows - 1) / kRouterRows;
-  const int tb = std::max(1, std::min((a.T + nt - 1) / nt, (2 * num_sms) / rb));
+  const int tp = nt * router_groups(a.H);  // tokens per pass of a CTA
+  const int tb = std::max(1, std::min((a.T + tp - 1) / tp, (2 * num_sms) / rb));
   const int rgrid = rb * tb;  // row blocks x token blocks
   const int kpl = a.E <= 128 ? 4 : a.E <= 256 ? 8 : a.E <= 512 ? 16 : 32;
   const void* fn;
