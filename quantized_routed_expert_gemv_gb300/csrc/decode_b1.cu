@@ -14,6 +14,17 @@
 // 1e-3 logit margin, and fp32 products of 8-bit codes and bf16 activations
 // are exact.
 //
+// router_b1_kernel  8-bit router rows (float path); the last CTA takes the
+//                   top-k with bitonic sorts and merges across its 16 warps
+//                   on (logit, id) keys.
+// ffn_b1_kernel     the step's gate|up and down work as one claimed item list
+//                   in one persistent kernel (the layer's usual path): gate|up
+//                   items publish fixed-point h groups, down items (three
+//                   experts behind) copy the expert's h block with their
+//                   weights, and per row tile the last expert's epilogue sums
+//                   the experts' rows in a fixed order.
+// The expert cache runs the same step as separate kernels, so the shared
+// expert's gate|up can run while missing records are copied:
 // gateup_b1_kernel  each consumer thread converts its chunk of the token's
 //                   hidden state; items are streamed as in decode.cu.  An
 //                   epilogue warp gathers each item's row sums, applies
@@ -24,9 +35,6 @@
 //                   ring ahead of its weight tiles and streams the CTA's row
 //                   tiles expert by expert; partial sums stay in registers
 //                   across experts (weighted by p_i), one reduction per tile.
-// router_b1_kernel  8-bit router rows (float path); the last CTA takes the
-//                   top-k with bitonic sorts and merges across its 16 warps
-//                   on (logit, id) keys.
 #include <algorithm>
 #include <cfloat>
 
