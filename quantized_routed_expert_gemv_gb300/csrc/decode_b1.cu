@@ -247,7 +247,7 @@ __device__ __forceinline__ void topk_block_b1(const LayerArgs& a, uint64_t (*lis
 
 
 constexpr int kR1Threads = 512;
-constexpr int kR1Rows = 16;  // rows per CTA pass: 32 CTAs for 512 experts leave most SMs to the fused kernel
+constexpr int kR1Rows = 4;  // rows per CTA pass: 128 CTAs for 512 experts (the router's latency is on the critical path)
 
 __global__ void __launch_bounds__(kR1Threads) router_b1_kernel(const __grid_constant__ LayerArgs a) {
   extern __shared__ __align__(16) float rsm[];
