@@ -19,10 +19,10 @@
 //                   on (logit, id) keys.
 // ffn_b1_kernel     the step's gate|up and down work as one claimed item list
 //                   in one persistent kernel (the layer's usual path): gate|up
-//                   items publish fixed-point h groups, down items (three
-//                   experts behind) copy the expert's h block with their
-//                   weights, and per row tile the last expert's epilogue sums
-//                   the experts' rows in a fixed order.
+//                   items publish fixed-point h groups, then down items copy
+//                   the expert's h block with their weights, and per row tile
+//                   the last expert's epilogue sums the experts' rows in a
+//                   fixed order.
 // The expert cache runs the same step as separate kernels, so the shared
 // expert's gate|up can run while missing records are copied:
 // gateup_b1_kernel  each consumer thread converts its chunk of the token's
@@ -865,15 +865,12 @@ size_t down_b1_smem_bytes(const LayerArgs& a) {
 // items (rth gate + rth up rows of one expert, as in gateup_b1_kernel) and
 // down items (RTD rows of H of one expert's down matrix, with the expert's
 // fixed-point h block copied in the same stage).  The list runs
-//   G(0) ... G(n - 1) interleaved with D(0) ... D(n - 1),
-// with every expert's down items kF1Lag experts behind its gate|up items
-// (G(0) G(1) G(2) G(3) D(0) G(4) D(1) ...; entry 0 the shared expert), so a CTA
-// reaches an expert's down items several ring depths after that expert's
-// last gate|up item was claimed and its h is normally complete; the
-// producer checks a per-expert completion counter before it issues a down
-// item.  The lighter gate|up arithmetic and
-// the heavier down arithmetic share the consumer warps, and the stream never
-// stops at a kernel boundary.
+//   G(0) ... G(n - 1) D(0) ... D(n - 1)
+// (entry 0 the shared expert): every gate|up item, then every down item, so
+// a CTA reaches an expert's down items long after that expert's last
+// gate|up item was claimed and its h is complete; the producer still checks
+// a per-expert completion counter before it issues a down item.  The stream
+// never stops at a kernel boundary between the two halves.
 //
 // Warps: NCW consumers, one producer, two epilogue warps that take ring
 // positions in turn.  For a gate|up item the epilogue applies SwiGLU and
@@ -891,7 +888,6 @@ constexpr int kF1Warps = 16;                     // consumer warps
 constexpr int kF1Threads = (kF1Warps + 3) * 32;  // + producer + two epilogue warps
 constexpr int kF1SmemBudget = 222 * 1024;
 constexpr int kF1MaxStages = 16;
-constexpr int kF1Lag = 3;  // experts between an expert's gate|up and down items
 
 struct F1Smem {
   int wsum, info, ent, bars, total;
@@ -936,27 +932,21 @@ __device__ __forceinline__ int f1_code(int gate, int entry, int tile) { return (
 // Claim index -> (gate, entry, tile) for the n_ent experts of the step
 // (entry 0 the shared expert when there is one, its gate|up block tiles_s
 // items; every other gate|up block tiles_r items, every down block ndn
-// items): G(0) .. G(m - 1) with m = min(kF1Lag, n_ent), then the pairs
-// G(m + p) D(p), then the last m experts' down items.  Only G(0) of the
-// shared expert comes before the router's output is needed.  The divisions
-// use the reciprocals dr (tiles_r), dn (ndn), dp (tiles_r + ndn).
+// items): every gate|up item, expert by expert, then every down item.  Only
+// the shared expert's gate|up comes before the router's output is needed.
+// The divisions use the reciprocals dr (tiles_r) and dn (ndn).
 __device__ __forceinline__ int f1_item(int i, int has_sh, int tiles_s, int n_ent, const F1Div& dr,
-                                       const F1Div& dn, const F1Div& dp) {
-  const int tiles_r = dr.d, ndn = dn.d, m = min(kF1Lag, n_ent);
+                                       const F1Div& dn) {
+  const int tiles_r = dr.d, ndn = dn.d;
   const int g0 = has_sh ? tiles_s : tiles_r;
   if (i < g0) return f1_code(1, 0, i);
-  const int head = g0 + (m - 1) * tiles_r;
-  if (i < head) {
+  const int gates = g0 + (n_ent - 1) * tiles_r;
+  if (i < gates) {
     const int j = i - g0, q = f1_q(j, dr);
     return f1_code(1, 1 + q, j - q * tiles_r);
   }
-  const int j = i - head, per = dp.d, body = (n_ent - m) * per;
-  if (j < body) {
-    const int p = f1_q(j, dp), off = j - p * per;
-    return off < tiles_r ? f1_code(1, m + p, off) : f1_code(0, p, off - tiles_r);
-  }
-  const int t = j - body, q = f1_q(t, dn);
-  return f1_code(0, n_ent - m + q, t - q * ndn);
+  const int t = i - gates, q = f1_q(t, dn);
+  return f1_code(0, q, t - q * ndn);
 }
 
 // Waits (bounded) until *cnt >= need; acquire.
@@ -1002,7 +992,7 @@ __global__ void __launch_bounds__(kF1Threads, 1) ffn_b1_kernel(const __grid_cons
     F1Ent* tab = reinterpret_cast<F1Ent*>(smem + L.ent);
     const uint64_t pol = policy_evict_first(), pol_h = policy_evict_last();
     unsigned* claim = &a.ws.ctl[2];
-    const F1Div dr = f1_div(tiles_r), dn = f1_div(ndn), dp = f1_div(tiles_r + ndn);
+    const F1Div dr = f1_div(tiles_r), dn = f1_div(ndn);
     int it = 0, n_items = n_pre, n_ent = has_sh, checked = -1, cur = 0, nxt = 0;
     bool ok = true;
     RingPos pos;
@@ -1043,7 +1033,7 @@ __global__ void __launch_bounds__(kF1Threads, 1) ffn_b1_kernel(const __grid_cons
           if (i >= n_items) break;
           cur = nxt;
           nxt = static_cast<int>(atomicAdd(claim, 1u));
-          const int code = f1_item(i, has_sh, tiles_s, n_ent, dr, dn, dp);
+          const int code = f1_item(i, has_sh, tiles_s, n_ent, dr, dn);
           const int gate = code & 1, e = code >> 20, tile = (code >> 1) & 0x7FFFF;
           const bool sh = has_sh && e == 0;
           const RecordOffsets& off = sh ? a.off_s : a.off_r;
