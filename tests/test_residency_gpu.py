@@ -150,6 +150,11 @@ def test_faults_are_caught_and_recovered():
     cl.set_fault(moe.MOE_RESIDENCY_FAULT_TAG)
     cl.decode(bf16_tensor(xs[1], DEV))
     assert dl.check() == moe.MOE_ERR_RESIDENCY
+    # moe_check cleared the workspace's persistent counters with the error:
+    # the single-token kernels of a plain decode run on the same workspace
+    got = host(dl.decode(bf16_tensor(xs[1], DEV)))
+    assert dl.check() == moe.MOE_OK, moe.last_error()
+    assert_oracle(got, 0, *orc.token(xs[1][0]))
     got = host(cl.decode(bf16_tensor(xs[2], DEV)))
     assert dl.check() == moe.MOE_OK, moe.last_error()
     assert_oracle(got, 0, *orc.token(xs[2][0]))
