@@ -253,7 +253,7 @@ __global__ void __launch_bounds__(kR1Threads) router_b1_kernel(const __grid_cons
   extern __shared__ __align__(16) float rsm[];
   pdl_launch_dependents();
   if (blockIdx.x == 0 && threadIdx.x == 0) a.ws.ctl[3] = 0u;  // shared-only gate|up claims
-  const int H = a.H, E = a.E, k = a.k;
+  const int H = a.H, E = a.E;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   constexpr int NW = kR1Threads / 32;
   const int nchunk = H >> 4;  // 16 8-bit codes per chunk
