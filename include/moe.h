@@ -259,6 +259,25 @@ int moe_residency_slots(const moe_residency *res, int32_t *slot_expert, int32_t 
 /* Arms one of the MOE_RESIDENCY_FAULT_* modes for the next step (one-shot). */
 int moe_residency_set_fault(moe_residency *res, int32_t mode);
 
+/* Optional payload check of the host records (WASTE page, section "Disk
+ * streaming mimarisi": a crc32 of each record, off by default, worth running
+ * once on records whose copy cannot be trusted).
+ *   crc: host uint32 [n_experts], the expected moe_crc32 of each record's
+ *        payload: its first `bytes` bytes (moe_record_layout_of(hidden, ffn);
+ *        the padding up to the stride is not covered), copied; NULL switches
+ *        the check off.
+ * While on, a record is checked on the host before its first upload; a
+ * mismatch makes moe_residency_decode return MOE_ERR_RESIDENCY with the
+ * cache state unchanged (the message names the expert).  Records already
+ * resident are checked by this call (MOE_ERR_RESIDENCY, check left off, on
+ * a mismatch).  Each record is checked once per handle. */
+int moe_residency_verify(moe_residency *res, const uint32_t *crc);
+
+/* CRC-32 as in IEEE 802.3 and zlib (reflected polynomial 0xEDB88320,
+ * all-ones preset, complemented result) of `bytes` host bytes at `data`.
+ * moe_crc32("123456789", 9) == 0xCBF43926.  Host only; no device work. */
+uint32_t moe_crc32(const void *data, size_t bytes);
+
 /* Frees the host bookkeeping (pinned buffers, events); NULL is a no-op. */
 void moe_residency_close(moe_residency *res);
 

@@ -26,8 +26,16 @@
 //   M: waits for C's event -> routed gate|up -> down + combine
 // Every kernel that reads a routed record checks the slot's tag against the
 // expert it wants and latches MOE_ERR_RESIDENCY on a mismatch (moe_check).
+//
+// Optional payload check (WASTE page, section "Disk streaming mimarisi": a
+// crc32 of each record, off by default, worth running once on records of
+// uncertain origin): with moe_residency_verify, a record's CRC-32 is
+// computed on the host before its first upload and compared with the
+// caller's value; a mismatch refuses the step, cache state unchanged.
 #include <cstdint>
+#include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <vector>
 
@@ -63,7 +71,46 @@ size_t tables_offset(uint64_t stride, int n_slots) { return round256(static_cast
 
 size_t tables_bytes(int E, int n_slots) { return round256(static_cast<size_t>(E + n_slots) * 4); }
 
+// CRC-32 as in IEEE 802.3 / zlib: reflected polynomial 0xEDB88320, register
+// preset to all ones, result complemented.  Eight bytes per step with eight
+// 256-entry tables: t[0] is the one-byte table, t[j][i] the remainder of byte
+// i followed by j zero bytes.
+uint32_t g_crc[8][256];
+std::once_flag g_crc_once;
+
+void crc_tables() {
+  for (uint32_t i = 0; i < 256; ++i) {
+    uint32_t c = i;
+    for (int b = 0; b < 8; ++b) c = (c & 1u) ? (c >> 1) ^ 0xEDB88320u : c >> 1;
+    g_crc[0][i] = c;
+  }
+  for (int j = 1; j < 8; ++j)
+    for (uint32_t i = 0; i < 256; ++i) g_crc[j][i] = (g_crc[j - 1][i] >> 8) ^ g_crc[0][g_crc[j - 1][i] & 0xFFu];
+}
+
+uint32_t crc32_update(uint32_t crc, const uint8_t* p, size_t n) {
+  std::call_once(g_crc_once, crc_tables);
+  uint32_t c = ~crc;
+  while (n >= 8) {
+    // little-endian by construction: the bytes are combined explicitly
+    const uint32_t lo = c ^ (static_cast<uint32_t>(p[0]) | static_cast<uint32_t>(p[1]) << 8 |
+                             static_cast<uint32_t>(p[2]) << 16 | static_cast<uint32_t>(p[3]) << 24);
+    const uint32_t hi = static_cast<uint32_t>(p[4]) | static_cast<uint32_t>(p[5]) << 8 |
+                        static_cast<uint32_t>(p[6]) << 16 | static_cast<uint32_t>(p[7]) << 24;
+    c = g_crc[7][lo & 0xFFu] ^ g_crc[6][(lo >> 8) & 0xFFu] ^ g_crc[5][(lo >> 16) & 0xFFu] ^ g_crc[4][lo >> 24] ^
+        g_crc[3][hi & 0xFFu] ^ g_crc[2][(hi >> 8) & 0xFFu] ^ g_crc[1][(hi >> 16) & 0xFFu] ^ g_crc[0][hi >> 24];
+    p += 8, n -= 8;
+  }
+  while (n--) c = (c >> 8) ^ g_crc[0][(c ^ *p++) & 0xFFu];
+  return ~c;
+}
+
 }  // namespace
+
+extern "C" uint32_t moe_crc32(const void* data, size_t bytes) {
+  if (!data && bytes) return 0u;
+  return crc32_update(0u, static_cast<const uint8_t*>(data), bytes);
+}
 
 struct moe_residency {
   uint32_t magic;
@@ -85,6 +132,8 @@ struct moe_residency {
   int64_t step;
   moe_residency_stats_t stats;
   int fault;
+  std::vector<uint32_t> crc_expect;  // [E] caller's CRC-32 per record; empty: no check
+  std::vector<uint8_t> crc_checked;  // [E] the record passed its check
 };
 
 static bool res_valid(const moe_residency* R) { return R && R->magic == kResMagic; }
@@ -212,6 +261,23 @@ extern "C" int moe_residency_decode(moe_residency* R, const uint16_t* x, int32_t
     for (int32_t ex : R->order) R->pinned_at[ex] = R->step;  // leave the state as it was
     return moe::report_error(MOE_ERR_RESIDENCY, "moe_residency_decode: the step needs more distinct experts than the cache has slots");
   }
+  // optional payload check of records about to be uploaded for the first
+  // time; a mismatch refuses the step before any state changes
+  if (!R->crc_expect.empty()) {
+    for (int32_t ex : R->order) {
+      if (R->slot_of[ex] >= 0 || R->crc_checked[ex]) continue;
+      const uint32_t got = moe_crc32(R->host + static_cast<size_t>(ex) * R->stride, R->rec_bytes);
+      if (got != R->crc_expect[ex]) {
+        for (int32_t e2 : R->order) R->pinned_at[e2] = R->step;  // leave the state as it was
+        char msg[160];
+        std::snprintf(msg, sizeof msg,
+                      "moe_residency_decode: host record of expert %d fails its CRC-32 check (0x%08x, expected 0x%08x)",
+                      static_cast<int>(ex), got, R->crc_expect[ex]);
+        return moe::report_error(MOE_ERR_RESIDENCY, msg);
+      }
+      R->crc_checked[ex] = 1;
+    }
+  }
   R->step = step;
   for (int32_t ex : R->order) R->count[ex] += 1, R->last_use[ex] = step;
 
@@ -276,6 +342,27 @@ extern "C" int moe_residency_slots(const moe_residency* R, int32_t* slot_expert,
   if (!res_valid(R) || !slot_expert || n < R->n_slots)
     return moe::report_error(MOE_ERR_ARG, "moe_residency_slots: invalid arguments (n must be >= n_slots)");
   for (int s = 0; s < R->n_slots; ++s) slot_expert[s] = R->slot_expert[s];
+  return MOE_OK;
+}
+
+extern "C" int moe_residency_verify(moe_residency* R, const uint32_t* crc) {
+  if (!res_valid(R)) return moe::report_error(MOE_ERR_ARG, "moe_residency_verify: invalid residency handle");
+  if (!crc) {
+    R->crc_expect.clear(), R->crc_checked.clear();
+    return MOE_OK;
+  }
+  R->crc_expect.assign(crc, crc + R->E);
+  R->crc_checked.assign(R->E, 0);
+  // records already resident were uploaded unchecked: each is checked now
+  for (int s = 0; s < R->n_slots; ++s) {
+    const int ex = R->slot_expert[s];
+    if (ex < 0) continue;
+    if (moe_crc32(R->host + static_cast<size_t>(ex) * R->stride, R->rec_bytes) != R->crc_expect[ex]) {
+      R->crc_expect.clear(), R->crc_checked.clear();
+      return moe::report_error(MOE_ERR_RESIDENCY, "moe_residency_verify: a resident record fails its CRC-32 check");
+    }
+    R->crc_checked[ex] = 1;
+  }
   return MOE_OK;
 }
 

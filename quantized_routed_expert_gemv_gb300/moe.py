@@ -83,6 +83,8 @@ SIGNATURES = {
     "moe_residency_close": (None, [_vp]),
     "moe_decode_noalloc": (ctypes.c_int, [_vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp]),
     "moe_decode_kernels": (_i32, [_vp, _i32]),
+    "moe_residency_verify": (ctypes.c_int, [_vp, _vp]),
+    "moe_crc32": (ctypes.c_uint32, [_vp, _sz]),
 }
 
 

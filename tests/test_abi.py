@@ -132,9 +132,27 @@ def test_residency_and_noalloc_calls_reject_invalid_handles(L):
         assert L.moe_residency_stats(r, ctypes.byref(st)) == moe.MOE_ERR_ARG
         assert L.moe_residency_slots(r, (ctypes.c_int32 * 4)(), 4) == moe.MOE_ERR_ARG
         assert L.moe_residency_set_fault(r, 1) == moe.MOE_ERR_ARG
+        assert L.moe_residency_verify(r, None) == moe.MOE_ERR_ARG
+        assert L.moe_decode_kernels(r, 1) == -1
         L.moe_residency_close(r)  # ignored
         assert L.moe_decode_noalloc(r, 0, 1, 0, 0, 0, 0, None) == moe.MOE_ERR_ARG
     assert "invalid" in moe.last_error()
+
+
+def test_crc32_check_value_and_zlib(L):
+    """moe_crc32 is the IEEE 802.3 / zlib CRC-32: the published check value of
+    "123456789" and zlib's own routine on random data of many lengths and
+    start alignments (the eight-byte steps and the byte tail)."""
+    import zlib
+    msg = b"123456789"
+    assert L.moe_crc32(msg, len(msg)) == 0xCBF43926
+    assert L.moe_crc32(None, 0) == 0
+    rng = np.random.default_rng(5)
+    data = rng.integers(0, 256, 1 << 20, dtype=np.uint8)
+    base = data.ctypes.data
+    for off, n in [(0, 1), (1, 7), (3, 8), (5, 9), (0, 63), (7, 1000), (0, 1 << 20)]:
+        n = min(n, data.size - off)
+        assert L.moe_crc32(base + off, n) == zlib.crc32(data[off:off + n].tobytes()), (off, n)
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):

@@ -11,7 +11,10 @@
 * Host-side fault injection: a wrong slot tag is caught by the kernels
   (MOE_ERR_RESIDENCY through moe_check); a failed copy returns MOE_ERR_CUDA,
   leaves the slot empty, and the next step recovers.
+* The optional CRC-32 check of host records: a wrong checksum refuses the
+  step that would upload the record, with the cache state unchanged.
 """
+import ctypes
 import os
 
 import numpy as np
@@ -177,4 +180,49 @@ def test_faults_are_caught_and_recovered():
     torch.cuda.synchronize()
     assert small.stats() == before and small.slots() == slots
     small.close()
+    dl.close()
+
+
+def test_record_checksums():
+    """moe_residency_verify, the optional CRC-32 payload check: with the true
+    checksums every step runs and matches the oracle; a wrong value for one
+    expert refuses the first step that uploads its record (MOE_ERR_RESIDENCY
+    naming the expert, cache state unchanged); switched off, that step runs."""
+    shape = synth.Shape(256, 16, 2, 128, 256)
+    hl, dl, cl = make(shape, 4, None, 4, max_tokens=2)
+    orc = hl.oracle()
+    L = moe.lib()
+    lay = moe.moe_record_layout()
+    assert L.moe_record_layout_of(shape.H, shape.F, ctypes.byref(lay)) == moe.MOE_OK
+    base = cl.host.data_ptr()
+    crc = np.array([L.moe_crc32(base + e * lay.stride, lay.bytes) for e in range(shape.E)], np.uint32)
+    assert L.moe_residency_verify(cl.handle, crc.ctypes.data) == moe.MOE_OK
+    x0 = np.stack([hidden_with_margin(orc, 17, 0, 0)])
+    got = host(cl.decode(bf16_tensor(x0, DEV)))
+    assert dl.check() == moe.MOE_OK, moe.last_error()
+    assert_oracle(got, 0, *orc.token(x0[0]))
+    # a token that needs a record not yet resident
+    resident = set(cl.slots())
+    for s in range(1, 64):
+        x1 = np.stack([hidden_with_margin(orc, 17, s, 0)])
+        need = [int(e) for e in orc.route(x1[0])[1] if int(e) not in resident]
+        if need:
+            break
+    else:
+        pytest.fail("no token needing a non-resident expert")
+    bad = crc.copy()
+    bad[need[0]] ^= 1
+    assert L.moe_residency_verify(cl.handle, bad.ctypes.data) == moe.MOE_OK  # resident records still match
+    before, slots = cl.stats(), cl.slots()
+    with pytest.raises(moe.MoEError) as ei:
+        cl.decode(bf16_tensor(x1, DEV))
+    assert ei.value.code == moe.MOE_ERR_RESIDENCY
+    assert f"expert {need[0]} " in str(ei.value)
+    torch.cuda.synchronize()
+    assert cl.stats() == before and cl.slots() == slots
+    assert L.moe_residency_verify(cl.handle, None) == moe.MOE_OK
+    got = host(cl.decode(bf16_tensor(x1, DEV)))
+    assert dl.check() == moe.MOE_OK, moe.last_error()
+    assert_oracle(got, 0, *orc.token(x1[0]))
+    cl.close()
     dl.close()
