@@ -10,7 +10,8 @@ C, fp64).  See ``oracle.c`` for the formulas and the pages each one follows:
 the TurboFieldfare page, sections "Belleği azaltan çalışma yapısı" (affine
 4-bit group-64 experts, 8-bit router) and "Token üretim süreci" (router,
 top-k, bounded LFU cache, shared expert, combine), and the WASTE page,
-section "Disk streaming mimarisi" (gate, up and down stored contiguously).
+sections "Disk streaming mimarisi" (gate, up and down stored contiguously)
+and "Önceden okuma ve router tahmini" (router lookahead into the cache).
 """
 from __future__ import annotations
 
@@ -80,6 +81,8 @@ def lib():
         L.orc_moe_token_dense.restype = i32
         L.orc_lfu_step.argtypes = [i32, i32, vp, vp, vp, vp, i32, ctypes.c_int64, vp, vp]
         L.orc_lfu_step.restype = i32
+        L.orc_lfu_lookahead.argtypes = [i32, i32, vp, vp, vp, vp, vp, vp, i32, vp, vp]
+        L.orc_lfu_lookahead.restype = i32
     return _lib
 
 
@@ -188,24 +191,61 @@ class Layer:
 
 
 class LFU:
-    """Replays the bounded LFU residency policy on an id stream (see oracle.c)."""
+    """Replays the bounded LFU residency policy on an id stream, with the
+    optional router lookahead between demand steps (see oracle.c).
+
+    Cumulative counters, in the library's terms: hits, misses, evictions,
+    lookahead_copies, lookahead_hits (demand hits on a record a lookahead
+    copied and no demand step had used yet)."""
 
     def __init__(self, n_slots: int, E: int):
         self.n_slots, self.E = n_slots, E
         self.slot_expert = np.full(n_slots, -1, np.int32)
         self.count = np.zeros(E, np.int64)
         self.last_use = np.zeros(E, np.int64)
+        self.pinned = np.zeros(E, np.uint8)   # lookahead pins, cleared by the next demand step
+        self.fresh = np.zeros(E, np.uint8)    # copied by a lookahead, not yet used
         self.step_no = 0
+        self.hits = self.misses = self.evictions = 0
+        self.lookahead_copies = self.lookahead_hits = 0
 
     def step(self, ids: np.ndarray):
-        """Returns (hit[k] bool, slot[k] int, misses)."""
+        """One demand step over the step's distinct ids (first-appearance
+        order).  Returns (hit[k] bool, slot[k] int, misses)."""
         ids = np.ascontiguousarray(ids, dtype=np.int32)
         k = ids.size
         hit = np.zeros(k, np.int32)
         slot = np.zeros(k, np.int32)
+        empty = int((self.slot_expert < 0).sum())
+        self.pinned[:] = 0
         self.step_no += 1
         m = lib().orc_lfu_step(self.n_slots, self.E, _p(self.slot_expert), _p(self.count),
                                _p(self.last_use), _p(ids), k, self.step_no, _p(hit), _p(slot))
         if m < 0:
             raise ValueError("more distinct experts in one step than slots")
+        self.lookahead_hits += int(sum(1 for e, h in zip(ids, hit) if h and self.fresh[e]))
+        self.fresh[ids] = 0
+        gone = np.ones(self.E, bool)
+        gone[self.slot_expert[self.slot_expert >= 0]] = False
+        self.fresh[gone] = 0
+        self.hits += int(hit.sum())
+        self.misses += m
+        self.evictions += m - min(m, empty)
         return hit.astype(bool), slot, m
+
+    def lookahead(self, pred: np.ndarray, n_ahead: int):
+        """A lookahead over predicted rankings pred[B][k] (each row in rank
+        order), taking each token's first n_ahead.  Returns (slot[] of the
+        visited predictions, -1 where dropped; copies; evictions)."""
+        pred = np.asarray(pred, dtype=np.int32)
+        if pred.ndim == 1:
+            pred = pred[None]
+        order = np.ascontiguousarray(pred[:, :n_ahead].T.reshape(-1))  # rank-major
+        slot = np.zeros(order.size, np.int32)
+        ev = ctypes.c_int(0)
+        c = lib().orc_lfu_lookahead(self.n_slots, self.E, _p(self.slot_expert), _p(self.count),
+                                    _p(self.last_use), _p(self.pinned), _p(self.fresh), _p(order),
+                                    int(order.size), _p(slot), ctypes.byref(ev))
+        self.lookahead_copies += c
+        self.evictions += ev.value
+        return slot, c, ev.value

@@ -334,3 +334,78 @@ int orc_lfu_step(int n_slots, int E, int *slot_expert, int64_t *count,
     }
     return misses;
 }
+
+/* ---- Router lookahead into the LFU cache ---------------------------------
+ * WASTE page, section "Önceden okuma ve router tahmini": before a layer's own
+ * hidden state exists, that layer's router is run on the hidden state one
+ * residual earlier, and the first few experts of the predicted ranking are
+ * read into the cache; the layer's own router still chooses the experts, so
+ * the output does not change, only which reads are demand misses.
+ * Readings where the page is silent:
+ *   * the predictions of a batch are visited rank-major (every token's first
+ *     choice, then every token's second, ...), repeats skipped;
+ *   * every visited expert, resident or not, is pinned before any slot is
+ *     chosen, and stays pinned until the layer's next demand step, so one
+ *     prediction never evicts another;
+ *   * a non-resident prediction takes the lowest empty slot, else evicts the
+ *     unpinned resident with the lowest (use count, last use, id), as a
+ *     demand miss does; when every slot is pinned it is dropped;
+ *   * use counts and last-use steps are not touched: only demand steps use
+ *     an expert.
+ * pred[n] are the predicted ids already in visiting order (repeats allowed).
+ * pinned[E] and fresh[E] are 0/1 arrays owned by the caller: pinned marks
+ * the lookahead pins (the caller clears them at the next demand step), fresh
+ * marks records this lookahead copied that no demand step has used yet.
+ * Writes slot[n] (the slot the prediction occupies, -1 if dropped) and
+ * *evictions; returns the number of records copied. */
+int orc_lfu_lookahead(int n_slots, int E, int *slot_expert, const int64_t *count,
+                      const int64_t *last_use, uint8_t *pinned, uint8_t *fresh,
+                      const int32_t *pred, int n, int *slot, int *evictions)
+{
+    int copies = 0;
+    *evictions = 0;
+    for (int i = 0; i < n; ++i)
+        pinned[pred[i]] = 1;
+    for (int i = 0; i < n; ++i) {
+        int e = pred[i], where = -1;
+        for (int s = 0; s < n_slots; ++s)
+            if (slot_expert[s] == e)
+                where = s;
+        if (where >= 0) {
+            slot[i] = where;
+            continue;
+        }
+        int victim = -1;
+        for (int s = 0; s < n_slots && victim < 0; ++s)
+            if (slot_expert[s] < 0)
+                victim = s;
+        if (victim < 0) {
+            for (int s = 0; s < n_slots; ++s) {
+                int r = slot_expert[s];
+                if (pinned[r])
+                    continue;
+                if (victim < 0) {
+                    victim = s;
+                    continue;
+                }
+                int v = slot_expert[victim];
+                if (count[r] < count[v] ||
+                    (count[r] == count[v] &&
+                     (last_use[r] < last_use[v] ||
+                      (last_use[r] == last_use[v] && r < v))))
+                    victim = s;
+            }
+            if (victim >= 0) {
+                fresh[slot_expert[victim]] = 0;
+                ++*evictions;
+            }
+        }
+        slot[i] = victim;
+        if (victim < 0)
+            continue; /* every slot pinned: dropped */
+        slot_expert[victim] = e;
+        fresh[e] = 1;
+        ++copies;
+    }
+    return copies;
+}

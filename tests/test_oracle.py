@@ -299,6 +299,76 @@ def test_lfu_invariants_random_stream():
     assert total_miss < 300 * k
 
 
+def test_lfu_lookahead_hand_trace():
+    rows = [[c.strip() for c in l.split("|")]
+            for l in open(os.path.join(GOLDEN, "lfu_lookahead_trace.txt"))
+            if l.strip() and not l.startswith("#")]
+    lfu = oracle.LFU(3, 6)
+    for r in rows:
+        before = (lfu.hits, lfu.misses, lfu.lookahead_copies, lfu.lookahead_hits, lfu.evictions)
+        counts = lfu.count.copy()
+        if r[1] == "D":
+            lfu.step(np.array(r[3].split(), np.int32))
+        else:
+            pred = np.array([t.split() for t in r[3].split(";")], np.int32)
+            lfu.lookahead(pred, int(r[2]))
+            assert np.array_equal(lfu.count, counts)          # no use counted
+        after = (lfu.hits, lfu.misses, lfu.lookahead_copies, lfu.lookahead_hits, lfu.evictions)
+        assert [a - b for a, b in zip(after, before)] == [int(t) for t in r[4:9]], f"row {r[0]}"
+        assert list(lfu.slot_expert) == [int(t) for t in r[9].split()], f"row {r[0]}"
+
+
+def test_lfu_lookahead_with_exact_predictions_moves_every_miss():
+    """A lookahead told exactly the next step's ids (one token, n = k) pins the
+    same experts the step pins and sees the same counts among the others, so
+    it must choose the very victims the demand step would: the cache ends in
+    the same state as without it, and every miss becomes a lookahead copy
+    that the step then hits."""
+    rng = np.random.default_rng(5)
+    n_slots, E, k = 8, 40, 4
+    plain, ahead = oracle.LFU(n_slots, E), oracle.LFU(n_slots, E)
+    for _ in range(300):
+        ids = rng.choice(E, size=k, replace=False).astype(np.int32)
+        plain.step(ids)
+        ahead.lookahead(ids[None], k)
+        hit, _, m = ahead.step(ids)
+        assert m == 0 and hit.all()
+        assert list(ahead.slot_expert) == list(plain.slot_expert)
+    assert ahead.lookahead_copies == plain.misses > 0
+    assert ahead.lookahead_hits == ahead.lookahead_copies
+    assert ahead.evictions == plain.evictions and ahead.misses == 0
+
+
+def test_lfu_lookahead_invariants_random_stream():
+    rng = np.random.default_rng(6)
+    n_slots, E, k = 6, 30, 3
+    lfu = oracle.LFU(n_slots, E)
+    for it in range(400):
+        if it % 2:
+            B, n = int(rng.integers(1, 4)), int(rng.integers(0, k + 1))
+            pred = np.stack([rng.choice(E, size=k, replace=False) for _ in range(B)]).astype(np.int32)
+            counts, pinned0 = lfu.count.copy(), lfu.pinned.copy()
+            slot, c, ev = lfu.lookahead(pred, n)
+            order = pred[:, :n].T.reshape(-1)
+            assert np.array_equal(lfu.count, counts)
+            assert all(lfu.pinned[e] for e in order) and (lfu.pinned >= pinned0).all()
+            for i, e in enumerate(order):
+                if slot[i] >= 0:
+                    assert lfu.slot_expert[slot[i]] == e       # resident where it says
+                else:                                          # dropped: no slot was free
+                    assert all(lfu.pinned[x] for x in lfu.slot_expert if x >= 0)
+                    assert (lfu.slot_expert >= 0).all()
+            assert ev <= c
+        else:
+            ids = rng.choice(E, size=k, replace=False).astype(np.int32)
+            hit, slot, m = lfu.step(ids)
+            assert not lfu.pinned.any()
+            assert all(lfu.slot_expert[slot[i]] == e for i, e in enumerate(ids))
+        live = [e for e in lfu.slot_expert if e >= 0]
+        assert len(set(live)) == len(live)
+        assert not any(lfu.fresh[e] for e in range(E) if e not in live)
+
+
 # ---- generator --------------------------------------------------------------------------
 
 def test_synth_bf16_rounding():
