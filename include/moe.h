@@ -209,16 +209,21 @@ typedef struct {
     uint64_t steps;      /* moe_residency_decode calls that reached the cache */
     uint64_t hits;       /* distinct experts of a step already resident */
     uint64_t misses;     /* distinct experts copied in */
-    uint64_t evictions;  /* misses that replaced a resident expert */
-    uint64_t bytes_h2d;  /* record bytes copied host -> device */
+    uint64_t evictions;  /* copies (misses or lookahead) that replaced a resident expert */
+    uint64_t bytes_h2d;  /* record bytes copied host -> device for misses */
+    uint64_t lookaheads;        /* moe_residency_lookahead calls that reached the cache */
+    uint64_t lookahead_copies;  /* records copied in by a lookahead */
+    uint64_t lookahead_hits;    /* hits on a record a lookahead copied, before any step used it */
+    uint64_t lookahead_bytes;   /* record bytes copied host -> device by lookaheads */
 } moe_residency_stats_t;
 
 /* Host-side fault injection for tests (no device fault is involved). */
 #define MOE_RESIDENCY_FAULT_NONE 0
 #define MOE_RESIDENCY_FAULT_TAG 1   /* next step uploads a wrong tag for one of its slots:
                                        the kernels latch MOE_ERR_RESIDENCY (moe_check) */
-#define MOE_RESIDENCY_FAULT_COPY 2  /* next step's first miss fails as if its copy had:
-                                       MOE_ERR_CUDA, the slot is left empty */
+#define MOE_RESIDENCY_FAULT_COPY 2  /* the next record copy (of a step or a lookahead) fails
+                                       as if the copy had: MOE_ERR_CUDA, the slot is left
+                                       empty */
 
 /* Bytes of the device slot pool for n_slots slots: the records at the layer's
  * record stride, then the slot tables.  0 for an invalid handle or n_slots
@@ -229,7 +234,7 @@ size_t moe_residency_pool_bytes(const moe_layer *layer, int32_t n_slots);
  * layer's E expert records at the record stride, read by the copies;
  * device_pool (device, 256-byte aligned, >= moe_residency_pool_bytes): slot
  * storage, owned by the caller, written only by this cache.  n_slots in
- * [top_k, n_experts].  Allocates two small pinned host buffers and two
+ * [top_k, n_experts].  Allocates small pinned host buffers and a few
  * events, freed by moe_residency_close.  The layer may have been opened with
  * expert_records = NULL. */
 int moe_residency_open(moe_layer *layer, const void *host_records, int32_t n_slots,
@@ -249,6 +254,35 @@ int moe_residency_open(moe_layer *layer, const void *host_records, int32_t n_slo
 int moe_residency_decode(moe_residency *res, const uint16_t *x, int32_t B, uint16_t *out_bf16,
                          float *out_f32, int32_t *ids, float *weights, void *workspace,
                          size_t workspace_bytes, void *main_stream, void *copy_stream);
+
+/* Router lookahead (WASTE page, section "Önceden okuma ve router tahmini":
+ * before a layer's own hidden state exists, its router is run on the hidden
+ * state one residual earlier and the first few predicted experts are read
+ * ahead; the layer's own router still chooses, so outputs do not change).
+ *   x: device bf16 [B][hidden], the earlier hidden state (e.g. the previous
+ *      layer's input); B in [0, max_tokens].
+ *   n_ahead in [0, top_k]: experts taken from the head of each token's
+ *      predicted ranking (0: no work).
+ *   ids, weights: device [B][top_k], the predicted routing (written).
+ *   workspace: a workspace of this layer (moe_workspace_init) that no kernel
+ *      running at the same time uses; moe_check it for device errors.
+ *   stream: where the router runs; the caller orders it after x is written.
+ *      The call blocks until the predicted ids are on the host.
+ *   copy_stream: where the records are copied.  The copies are ordered after
+ *      the previous moe_residency_decode's kernels and the previous
+ *      lookahead, whatever the streams; the next moe_residency_decode is
+ *      ordered after them.
+ * Policy: predictions are visited rank-major (every token's first, then
+ * every token's second, ...), repeats skipped; all are pinned until the next
+ * moe_residency_decode; a non-resident one takes a slot by the demand rule
+ * (only lookahead pins count) and is dropped when every slot is pinned; use
+ * counts and last-use steps are not changed.  Errors as for
+ * moe_residency_decode (MOE_ERR_RESIDENCY for an out-of-range id or a record
+ * failing its CRC-32 check, with the cache state unchanged; MOE_ERR_CUDA for a
+ * failed copy, whose slot is left empty). */
+int moe_residency_lookahead(moe_residency *res, const uint16_t *x, int32_t B, int32_t n_ahead,
+                            int32_t *ids, float *weights, void *workspace, size_t workspace_bytes,
+                            void *stream, void *copy_stream);
 
 /* Counters since open. */
 int moe_residency_stats(const moe_residency *res, moe_residency_stats_t *out);

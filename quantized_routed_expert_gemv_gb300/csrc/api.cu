@@ -282,7 +282,7 @@ extern "C" int moe_workspace_init(const moe_layer* L, void* ws, size_t bytes, vo
   return e ? cuda_fail(e, "moe_workspace_init: cudaMemsetAsync") : MOE_OK;
 }
 
-enum class Path { kDecode, kPrefill };
+enum class Path { kDecode, kPrefill, kRoute };  // kRoute: the router alone, no layer output
 
 // Validates one call and fills `a` (geometry and workspace; the records are
 // the layer's own unless the caller replaces them).  T == 0 is valid and
@@ -294,7 +294,8 @@ static int prepare(moe_layer* L, const uint16_t* x, int32_t T, uint16_t* ob, flo
   const int cap = path == Path::kPrefill ? std::min(128, (int)L->d.max_tokens) : (int)L->d.max_tokens;
   if (T < 0 || T > cap) return fail(MOE_ERR_ARG, "%s: token count %d outside [0, %d]", name, T, cap);
   if (T == 0) return MOE_OK;
-  if (!x || !ob || !ids || !wts || !ws) return fail(MOE_ERR_ARG, "%s: a required pointer is NULL", name);
+  if (!x || (!ob && path != Path::kRoute) || !ids || !wts || !ws)
+    return fail(MOE_ERR_ARG, "%s: a required pointer is NULL", name);
   if (!aligned(x, 16) || !aligned(ob, 16) || !aligned(of, 16) || !aligned(ids, 16) || !aligned(wts, 16))
     return fail(MOE_ERR_ALIGN, "%s: activation/output pointers must be 16-byte aligned", name);
   if (!aligned(ws, 256)) return fail(MOE_ERR_ALIGN, "%s: workspace must be 256-byte aligned", name);
@@ -456,6 +457,18 @@ int prepare_cached_decode(moe_layer* L, const uint16_t* x, int32_t B, uint16_t* 
   int rc = prepare(L, x, B, ob, of, ids, wts, ws, ws_bytes, Path::kDecode, false, a, name);
   if (rc || B == 0) return rc;
   a->records = pool, a->slot_of = slot_of, a->slot_tag = slot_tag, a->n_slots = n_slots;
+  a->prof_on = 0;
+  *single = B == 1 && plan_b1(*a, L->num_sms, L->smem_optin);
+  *num_sms = L->num_sms;
+  return MOE_OK;
+}
+
+// The router alone (ids and weights), for a routing predicted ahead of the
+// layer's own step; no output buffer is needed.
+int prepare_route(moe_layer* L, const uint16_t* x, int32_t B, int32_t* ids, float* wts, void* ws,
+                  size_t ws_bytes, LayerArgs* a, bool* single, int* num_sms, const char* name) {
+  int rc = prepare(L, x, B, nullptr, nullptr, ids, wts, ws, ws_bytes, Path::kRoute, false, a, name);
+  if (rc || B == 0) return rc;
   a->prof_on = 0;
   *single = B == 1 && plan_b1(*a, L->num_sms, L->smem_optin);
   *num_sms = L->num_sms;

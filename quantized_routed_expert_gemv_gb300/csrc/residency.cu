@@ -27,6 +27,20 @@
 // Every kernel that reads a routed record checks the slot's tag against the
 // expert it wants and latches MOE_ERR_RESIDENCY on a mismatch (moe_check).
 //
+// Router lookahead (WASTE page, section "Önceden okuma ve router tahmini":
+// before a layer's own hidden state exists, its router runs on the hidden
+// state one residual earlier and the first few predicted experts are read
+// ahead; the true router still picks the experts): moe_residency_lookahead
+// runs this layer's router on the earlier hidden state, pins the first
+// n_ahead predictions of each token (rank-major) until the next step and
+// copies the missing ones into slots chosen by the miss rule above, with no
+// use counted.  Ordering, whatever streams the caller gives:
+//   lookahead copies  after  the previous step's routed kernels (ev_done)
+//                            and the previous lookahead (ev_ahead);
+//   a step's copies   after  the previous lookahead (ev_ahead).
+// Slot-table images are pinned buffers used in turn; one is rewritten only
+// after its previous upload has completed.
+//
 // Optional payload check (WASTE page, section "Disk streaming mimarisi": a
 // crc32 of each record, off by default, worth running once on records of
 // uncertain origin): with moe_residency_verify, a record's CRC-32 is
@@ -35,6 +49,7 @@
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
+#include <initializer_list>
 #include <mutex>
 #include <new>
 #include <vector>
@@ -54,6 +69,8 @@ int prepare_cached_decode(moe_layer* L, const uint16_t* x, int32_t B, uint16_t* 
                           int32_t* ids, float* wts, void* ws, size_t ws_bytes, const uint8_t* pool,
                           const int32_t* slot_of, const int32_t* slot_tag, int n_slots, LayerArgs* a,
                           bool* single, int* num_sms, const char* name);
+int prepare_route(moe_layer* L, const uint16_t* x, int32_t B, int32_t* ids, float* wts, void* ws,
+                  size_t ws_bytes, LayerArgs* a, bool* single, int* num_sms, const char* name);
 cudaError_t launch_b1_router(const LayerArgs& a, int num_sms, cudaStream_t st);
 cudaError_t launch_b1_shared(const LayerArgs& a, int num_sms, cudaStream_t st);
 cudaError_t launch_b1_routed(const LayerArgs& a, int num_sms, cudaStream_t st);
@@ -64,6 +81,7 @@ cudaError_t launch_decode_experts(const LayerArgs& a, int num_sms, cudaStream_t 
 namespace {
 
 constexpr uint32_t kResMagic = 0x52657331u;  // "Res1"
+constexpr int kTabRing = 4;                  // pinned slot-table images used in turn
 
 size_t round256(size_t v) { return (v + 255) / 256 * 256; }
 
@@ -120,15 +138,25 @@ struct moe_residency {
   const uint8_t* host;        // pinned: E records at `stride`
   uint8_t* pool;              // device: n_slots records, then the slot tables
   int32_t* d_tables;          // device: slot_of[E] | slot_tag[n_slots]
-  int32_t* h_tables;          // pinned mirror uploaded each step
+  int32_t* h_tab[kTabRing];   // pinned images of the slot tables, uploaded in turn
+  cudaEvent_t ev_tab[kTabRing];
+  bool tab_used[kTabRing];
+  int tab_next;
   int32_t* h_ids;             // pinned: the step's ids [max_tokens][k]
-  cudaEvent_t ev_ids, ev_copy;
+  int32_t* h_pids;            // pinned: a lookahead's predicted ids [max_tokens][k]
+  cudaEvent_t ev_ids, ev_copy, ev_pids;
+  cudaEvent_t ev_done;        // main stream, after the last step's routed kernels
+  cudaEvent_t ev_ahead;       // copy stream, after the last lookahead's copies
   // cache state (host)
   std::vector<int32_t> slot_expert;  // [n_slots] expert held, -1 = empty
   std::vector<int32_t> slot_of;      // [E] slot holding the expert, -1 = not resident
   std::vector<int64_t> count, last_use;
   std::vector<int64_t> pinned_at;    // [E] step that pinned the expert
   std::vector<int32_t> order;        // the step's distinct experts, first-appearance order
+  std::vector<uint8_t> ahead;        // [E] pinned by a lookahead until the next step
+  std::vector<int32_t> ahead_list;   // the experts with ahead[] set
+  std::vector<uint8_t> fresh;        // [E] copied by a lookahead, not yet used by a step
+  std::vector<int32_t> pred;         // a lookahead's predictions, visiting order
   int64_t step;
   moe_residency_stats_t stats;
   int fault;
@@ -182,17 +210,29 @@ extern "C" int moe_residency_open(moe_layer* layer, const void* host_records, in
   R->count.assign(R->E, 0);
   R->last_use.assign(R->E, 0);
   R->pinned_at.assign(R->E, 0);
-  R->order.reserve(static_cast<size_t>(R->max_tokens) * R->k);
+  R->ahead.assign(R->E, 0);
+  R->fresh.assign(R->E, 0);
+  const size_t nid = static_cast<size_t>(R->max_tokens) * R->k;
+  R->order.reserve(nid);
+  R->ahead_list.reserve(nid);
+  R->pred.reserve(nid);
   const size_t tb = static_cast<size_t>(R->E + n_slots) * 4;
-  if ((e = cudaHostAlloc(&R->h_tables, tb, cudaHostAllocDefault)) ||
-      (e = cudaHostAlloc(&R->h_ids, static_cast<size_t>(R->max_tokens) * R->k * 4, cudaHostAllocDefault)) ||
+  e = cudaSuccess;
+  for (int i = 0; i < kTabRing && !e; ++i)
+    if (!(e = cudaHostAlloc(&R->h_tab[i], tb, cudaHostAllocDefault)))
+      e = cudaEventCreateWithFlags(&R->ev_tab[i], cudaEventDisableTiming);
+  if (e || (e = cudaHostAlloc(&R->h_ids, nid * 4, cudaHostAllocDefault)) ||
+      (e = cudaHostAlloc(&R->h_pids, nid * 4, cudaHostAllocDefault)) ||
       (e = cudaEventCreateWithFlags(&R->ev_ids, cudaEventDisableTiming)) ||
-      (e = cudaEventCreateWithFlags(&R->ev_copy, cudaEventDisableTiming))) {
+      (e = cudaEventCreateWithFlags(&R->ev_copy, cudaEventDisableTiming)) ||
+      (e = cudaEventCreateWithFlags(&R->ev_pids, cudaEventDisableTiming)) ||
+      (e = cudaEventCreateWithFlags(&R->ev_done, cudaEventDisableTiming)) ||
+      (e = cudaEventCreateWithFlags(&R->ev_ahead, cudaEventDisableTiming))) {
     destroy(R);
     return moe::report_cuda(e, "moe_residency_open: pinned buffers / events");
   }
-  for (int i = 0; i < R->E + n_slots; ++i) R->h_tables[i] = -1;
-  if ((e = cudaMemcpy(R->d_tables, R->h_tables, tb, cudaMemcpyHostToDevice))) {
+  for (int i = 0; i < R->E + n_slots; ++i) R->h_tab[0][i] = -1;
+  if ((e = cudaMemcpy(R->d_tables, R->h_tab[0], tb, cudaMemcpyHostToDevice))) {
     destroy(R);
     return moe::report_cuda(e, "moe_residency_open: slot tables");
   }
@@ -201,14 +241,16 @@ extern "C" int moe_residency_open(moe_layer* layer, const void* host_records, in
   return MOE_OK;
 }
 
-// Victim slot for a miss: the lowest empty slot, else the unpinned resident
-// with the lowest (count, last use, id); -1 if every slot is pinned.
-static int choose_slot(const moe_residency* R) {
+// Victim slot for a copy: the lowest empty slot, else the unpinned resident
+// with the lowest (count, last use, id); -1 if every slot is pinned.  A
+// step's experts are pinned during the step; a lookahead's predictions until
+// the next step (a lookahead sees only those pins).
+static int choose_slot(const moe_residency* R, bool lookahead) {
   int best = -1;
   for (int s = 0; s < R->n_slots; ++s) {
     const int e = R->slot_expert[s];
     if (e < 0) return s;
-    if (R->pinned_at[e] == R->step) continue;
+    if (R->ahead[e] || (!lookahead && R->pinned_at[e] == R->step)) continue;
     if (best < 0) {
       best = s;
       continue;
@@ -220,6 +262,25 @@ static int choose_slot(const moe_residency* R) {
     if (better) best = s;
   }
   return best;
+}
+
+// Uploads the host's slot tables to the device on st from the next pinned
+// image; fault_expert >= 0 plants a wrong tag for that expert's slot.
+static cudaError_t upload_tables(moe_residency* R, cudaStream_t st, int fault_expert) {
+  const int i = R->tab_next;
+  R->tab_next = (i + 1) % kTabRing;
+  cudaError_t e;
+  if (R->tab_used[i] && (e = cudaEventSynchronize(R->ev_tab[i]))) return e;
+  int32_t* h = R->h_tab[i];
+  std::memcpy(h, R->slot_of.data(), static_cast<size_t>(R->E) * 4);
+  std::memcpy(h + R->E, R->slot_expert.data(), static_cast<size_t>(R->n_slots) * 4);
+  if (fault_expert >= 0) h[R->E + R->slot_of[fault_expert]] = (fault_expert + 1) % R->E;
+  if ((e = cudaMemcpyAsync(R->d_tables, h, static_cast<size_t>(R->E + R->n_slots) * 4,
+                           cudaMemcpyHostToDevice, st)) ||
+      (e = cudaEventRecord(R->ev_tab[i], st)))
+    return e;
+  R->tab_used[i] = true;
+  return cudaSuccess;
 }
 
 extern "C" int moe_residency_decode(moe_residency* R, const uint16_t* x, int32_t B, uint16_t* out_bf16,
@@ -280,19 +341,24 @@ extern "C" int moe_residency_decode(moe_residency* R, const uint16_t* x, int32_t
   }
   R->step = step;
   for (int32_t ex : R->order) R->count[ex] += 1, R->last_use[ex] = step;
+  for (int32_t ex : R->ahead_list) R->ahead[ex] = 0;  // a lookahead's pins end at this step
+  R->ahead_list.clear();
 
-  // 3. misses: choose slots, copy records on the side stream
+  // 3. misses: choose slots, copy records on the side stream (after the
+  // previous lookahead's copies, which may have used another stream)
+  if ((e = cudaStreamWaitEvent(C, R->ev_ahead, 0))) return moe::report_cuda(e, "moe_residency_decode: order after the lookahead");
   const int fault = R->fault;
   bool fault_used = false;
-  uint64_t hits = 0, misses = 0, evictions = 0, bytes = 0;
+  uint64_t hits = 0, misses = 0, evictions = 0, bytes = 0, ahead_hits = 0;
   for (int32_t ex : R->order) {
     if (R->slot_of[ex] >= 0) {
       ++hits;
+      if (R->fresh[ex]) ++ahead_hits, R->fresh[ex] = 0;
       continue;
     }
-    const int s = choose_slot(R);  // never -1: distinct experts <= slots
+    const int s = choose_slot(R, false);  // never -1: distinct experts <= slots
     const int old = R->slot_expert[s];
-    if (old >= 0) R->slot_of[old] = -1, ++evictions;
+    if (old >= 0) R->slot_of[old] = -1, R->fresh[old] = 0, ++evictions;
     ++misses;
     if (fault == MOE_RESIDENCY_FAULT_COPY && !fault_used) {
       e = cudaErrorInvalidValue;  // host-side stand-in for a failed copy
@@ -305,7 +371,7 @@ extern "C" int moe_residency_decode(moe_residency* R, const uint16_t* x, int32_t
       // the slot's contents are unknown now: it holds nothing
       R->slot_expert[s] = -1;
       R->stats.steps += 1, R->stats.hits += hits, R->stats.misses += misses;
-      R->stats.evictions += evictions, R->stats.bytes_h2d += bytes;
+      R->stats.evictions += evictions, R->stats.bytes_h2d += bytes, R->stats.lookahead_hits += ahead_hits;
       if (fault_used) R->fault = MOE_RESIDENCY_FAULT_NONE;
       return moe::report_cuda(e, "moe_residency_decode: record copy");
     }
@@ -314,21 +380,100 @@ extern "C" int moe_residency_decode(moe_residency* R, const uint16_t* x, int32_t
   }
 
   // 4. slot tables (one small copy behind the records), then the routed part
-  std::memcpy(R->h_tables, R->slot_of.data(), static_cast<size_t>(R->E) * 4);
-  std::memcpy(R->h_tables + R->E, R->slot_expert.data(), static_cast<size_t>(R->n_slots) * 4);
+  int fault_expert = -1;
   if (fault == MOE_RESIDENCY_FAULT_TAG) {
-    const int32_t ex = R->order[0];
-    R->h_tables[R->E + R->slot_of[ex]] = (ex + 1) % R->E;  // this step's tag no longer matches
+    fault_expert = R->order[0];  // this step's tag for it no longer matches
     R->fault = MOE_RESIDENCY_FAULT_NONE;
   }
-  if ((e = cudaMemcpyAsync(R->d_tables, R->h_tables, static_cast<size_t>(R->E + R->n_slots) * 4,
-                           cudaMemcpyHostToDevice, C)) ||
-      (e = cudaEventRecord(R->ev_copy, C)) || (e = cudaStreamWaitEvent(M, R->ev_copy, 0)))
+  if ((e = upload_tables(R, C, fault_expert)) || (e = cudaEventRecord(R->ev_copy, C)) ||
+      (e = cudaStreamWaitEvent(M, R->ev_copy, 0)))
     return moe::report_cuda(e, "moe_residency_decode: slot tables");
   R->stats.steps += 1, R->stats.hits += hits, R->stats.misses += misses;
-  R->stats.evictions += evictions, R->stats.bytes_h2d += bytes;
+  R->stats.evictions += evictions, R->stats.bytes_h2d += bytes, R->stats.lookahead_hits += ahead_hits;
   e = single ? moe::launch_b1_routed(a, num_sms, M) : moe::launch_decode_experts(a, num_sms, M);
-  if (e) return moe::report_cuda(e, "moe_residency_decode: routed experts");
+  if (e || (e = cudaEventRecord(R->ev_done, M))) return moe::report_cuda(e, "moe_residency_decode: routed experts");
+  return MOE_OK;
+}
+
+extern "C" int moe_residency_lookahead(moe_residency* R, const uint16_t* x, int32_t B, int32_t n_ahead,
+                                       int32_t* ids, float* weights, void* workspace, size_t workspace_bytes,
+                                       void* stream, void* copy_stream) {
+  static const char* kName = "moe_residency_lookahead";
+  if (!res_valid(R)) return moe::report_error(MOE_ERR_ARG, "moe_residency_lookahead: invalid residency handle");
+  if (n_ahead < 0 || n_ahead > R->k)
+    return moe::report_error(MOE_ERR_ARG, "moe_residency_lookahead: n_ahead outside [0, top_k]");
+  moe::LayerArgs a;
+  bool single = false;
+  int num_sms = 0;
+  int rc = moe::prepare_route(R->layer, x, B, ids, weights, workspace, workspace_bytes, &a, &single, &num_sms, kName);
+  if (rc || B == 0 || n_ahead == 0) return rc;
+  cudaStream_t S = static_cast<cudaStream_t>(stream), C = static_cast<cudaStream_t>(copy_stream);
+  const size_t nid = static_cast<size_t>(B) * R->k;
+
+  // 1. the predicted routing, to the host
+  cudaError_t e = single ? moe::launch_b1_router(a, num_sms, S) : moe::launch_decode_router(a, num_sms, S);
+  if (e) return moe::report_cuda(e, "moe_residency_lookahead: router");
+  if ((e = cudaMemcpyAsync(R->h_pids, ids, nid * 4, cudaMemcpyDeviceToHost, S)) ||
+      (e = cudaEventRecord(R->ev_pids, S)) || (e = cudaEventSynchronize(R->ev_pids)))
+    return moe::report_cuda(e, "moe_residency_lookahead: predicted ids to host");
+
+  // 2. visiting order (rank-major), validated and, with checksums on,
+  // checked before any state changes
+  R->pred.clear();
+  for (int r = 0; r < n_ahead; ++r)
+    for (int t = 0; t < B; ++t) {
+      const int32_t ex = R->h_pids[static_cast<size_t>(t) * R->k + r];
+      if (ex < 0 || ex >= R->E)
+        return moe::report_error(MOE_ERR_RESIDENCY, "moe_residency_lookahead: the router returned an expert id out of range (see moe_check)");
+      R->pred.push_back(ex);
+    }
+  if (!R->crc_expect.empty()) {
+    for (int32_t ex : R->pred) {
+      if (R->slot_of[ex] >= 0 || R->crc_checked[ex]) continue;
+      const uint32_t got = moe_crc32(R->host + static_cast<size_t>(ex) * R->stride, R->rec_bytes);
+      if (got != R->crc_expect[ex]) {
+        char msg[160];
+        std::snprintf(msg, sizeof msg,
+                      "moe_residency_lookahead: host record of expert %d fails its CRC-32 check (0x%08x, expected 0x%08x)",
+                      static_cast<int>(ex), got, R->crc_expect[ex]);
+        return moe::report_error(MOE_ERR_RESIDENCY, msg);
+      }
+      R->crc_checked[ex] = 1;
+    }
+  }
+  for (int32_t ex : R->pred)
+    if (!R->ahead[ex]) R->ahead[ex] = 1, R->ahead_list.push_back(ex);
+
+  // 3. copies, after the last step's kernels and the last lookahead
+  if ((e = cudaStreamWaitEvent(C, R->ev_done, 0)) || (e = cudaStreamWaitEvent(C, R->ev_ahead, 0)))
+    return moe::report_cuda(e, "moe_residency_lookahead: order the copies");
+  uint64_t copies = 0, evictions = 0, bytes = 0;
+  for (int32_t ex : R->pred) {
+    if (R->slot_of[ex] >= 0) continue;  // resident (or copied by an earlier repeat)
+    const int s = choose_slot(R, true);
+    if (s < 0) continue;                // every slot pinned: dropped
+    const int old = R->slot_expert[s];
+    if (old >= 0) R->slot_of[old] = -1, R->fresh[old] = 0, ++evictions;
+    if (R->fault == MOE_RESIDENCY_FAULT_COPY) {
+      e = cudaErrorInvalidValue;  // host-side stand-in for a failed copy
+      R->fault = MOE_RESIDENCY_FAULT_NONE;
+    } else {
+      e = cudaMemcpyAsync(R->pool + static_cast<size_t>(s) * R->stride, R->host + static_cast<size_t>(ex) * R->stride,
+                          R->rec_bytes, cudaMemcpyHostToDevice, C);
+    }
+    if (e) {
+      R->slot_expert[s] = -1;  // contents unknown: the slot holds nothing
+      R->stats.lookaheads += 1, R->stats.lookahead_copies += copies;
+      R->stats.evictions += evictions, R->stats.lookahead_bytes += bytes;
+      return moe::report_cuda(e, "moe_residency_lookahead: record copy");
+    }
+    R->slot_expert[s] = ex, R->slot_of[ex] = s, R->fresh[ex] = 1;
+    ++copies, bytes += R->rec_bytes;
+  }
+  if (copies && ((e = upload_tables(R, C, -1)) || (e = cudaEventRecord(R->ev_ahead, C))))
+    return moe::report_cuda(e, "moe_residency_lookahead: slot tables");
+  R->stats.lookaheads += 1, R->stats.lookahead_copies += copies;
+  R->stats.evictions += evictions, R->stats.lookahead_bytes += bytes;
   return MOE_OK;
 }
 
@@ -375,10 +520,14 @@ extern "C" int moe_residency_set_fault(moe_residency* R, int32_t mode) {
 }
 
 static void destroy(moe_residency* R) {
-  if (R->ev_ids) cudaEventDestroy(R->ev_ids);
-  if (R->ev_copy) cudaEventDestroy(R->ev_copy);
-  if (R->h_tables) cudaFreeHost(R->h_tables);
+  for (cudaEvent_t ev : {R->ev_ids, R->ev_copy, R->ev_pids, R->ev_done, R->ev_ahead})
+    if (ev) cudaEventDestroy(ev);
+  for (int i = 0; i < kTabRing; ++i) {
+    if (R->ev_tab[i]) cudaEventDestroy(R->ev_tab[i]);
+    if (R->h_tab[i]) cudaFreeHost(R->h_tab[i]);
+  }
   if (R->h_ids) cudaFreeHost(R->h_ids);
+  if (R->h_pids) cudaFreeHost(R->h_pids);
   R->magic = 0;
   delete R;
 }

@@ -132,6 +132,7 @@ class CachedLayer:
         self.handle = moe.moe_residency_open(dl.handle, host_records.data_ptr(), n_slots,
                                              self.pool.data_ptr(), self.pool_bytes)
         self.copy_stream = torch.cuda.Stream(dl.device)
+        self.ahead_ws = None
 
     def decode(self, x: torch.Tensor, outs=None, stream=None):
         ob, of, ids, w = outs or self.dl.outputs(x.shape[0])
@@ -141,6 +142,31 @@ class CachedLayer:
                                  w.data_ptr(), self.dl.ws.data_ptr(), self.dl.ws_bytes, st,
                                  self.copy_stream.cuda_stream)
         return ob, of, ids, w
+
+    def lookahead(self, x: torch.Tensor, n_ahead: int, stream=None, copy_stream=None):
+        """Runs this layer's router on an earlier hidden state x and reads the
+        first n_ahead experts of each token's predicted ranking into the
+        cache (moe_residency_lookahead).  Uses a workspace of its own, so it
+        may run on another stream than the layer's steps.  Returns the
+        predicted (ids, weights) [B][k] on the device."""
+        dl = self.dl
+        st = stream if stream is not None else torch.cuda.current_stream(dl.device).cuda_stream
+        if self.ahead_ws is None:
+            self.ahead_ws = torch.empty(dl.ws_bytes, dtype=torch.uint8, device=dl.device)
+            moe.moe_workspace_init(dl.handle, self.ahead_ws.data_ptr(), dl.ws_bytes, st)
+            _, _, self.ahead_ids, self.ahead_w = dl.outputs(dl.desc.max_tokens)
+        B = x.shape[0]
+        moe.moe_residency_lookahead(self.handle, x.data_ptr(), B, n_ahead, self.ahead_ids.data_ptr(),
+                                    self.ahead_w.data_ptr(), self.ahead_ws.data_ptr(), dl.ws_bytes,
+                                    st, (copy_stream or self.copy_stream).cuda_stream)
+        return self.ahead_ids[:B], self.ahead_w[:B]
+
+    def check_lookahead(self, stream=None) -> int:
+        """moe_check of the lookahead workspace (0 if none was made)."""
+        if self.ahead_ws is None:
+            return moe.MOE_OK
+        st = stream if stream is not None else torch.cuda.current_stream(self.dl.device).cuda_stream
+        return moe.moe_check(self.dl.handle, self.ahead_ws.data_ptr(), st)
 
     def stats(self) -> dict:
         return moe.moe_residency_stats(self.handle)

@@ -45,7 +45,9 @@ class moe_layer_weights(ctypes.Structure):
 
 class moe_residency_stats_t(ctypes.Structure):
     _fields_ = [("steps", ctypes.c_uint64), ("hits", ctypes.c_uint64), ("misses", ctypes.c_uint64),
-                ("evictions", ctypes.c_uint64), ("bytes_h2d", ctypes.c_uint64)]
+                ("evictions", ctypes.c_uint64), ("bytes_h2d", ctypes.c_uint64),
+                ("lookaheads", ctypes.c_uint64), ("lookahead_copies", ctypes.c_uint64),
+                ("lookahead_hits", ctypes.c_uint64), ("lookahead_bytes", ctypes.c_uint64)]
 
 
 class MoEError(RuntimeError):
@@ -85,6 +87,7 @@ SIGNATURES = {
     "moe_decode_kernels": (_i32, [_vp, _i32]),
     "moe_residency_verify": (ctypes.c_int, [_vp, _vp]),
     "moe_crc32": (ctypes.c_uint32, [_vp, _sz]),
+    "moe_residency_lookahead": (ctypes.c_int, [_vp, _vp, _i32, _i32, _vp, _vp, _vp, _sz, _vp, _vp]),
 }
 
 
@@ -191,6 +194,12 @@ def moe_residency_decode(res, x, B, out_bf16, out_f32, ids, weights, ws, ws_byte
                          copy_stream=0) -> None:
     check(lib().moe_residency_decode(res, x, B, out_bf16, out_f32, ids, weights, ws, ws_bytes,
                                      main_stream, copy_stream), "moe_residency_decode")
+
+
+def moe_residency_lookahead(res, x, B, n_ahead, ids, weights, ws, ws_bytes, stream=0,
+                            copy_stream=0) -> None:
+    check(lib().moe_residency_lookahead(res, x, B, n_ahead, ids, weights, ws, ws_bytes, stream,
+                                        copy_stream), "moe_residency_lookahead")
 
 
 def moe_residency_stats(res: int) -> dict:

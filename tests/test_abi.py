@@ -133,6 +133,7 @@ def test_residency_and_noalloc_calls_reject_invalid_handles(L):
         assert L.moe_residency_slots(r, (ctypes.c_int32 * 4)(), 4) == moe.MOE_ERR_ARG
         assert L.moe_residency_set_fault(r, 1) == moe.MOE_ERR_ARG
         assert L.moe_residency_verify(r, None) == moe.MOE_ERR_ARG
+        assert L.moe_residency_lookahead(r, 0, 1, 6, 0, 0, 0, 0, None, None) == moe.MOE_ERR_ARG
         assert L.moe_decode_kernels(r, 1) == -1
         L.moe_residency_close(r)  # ignored
         assert L.moe_decode_noalloc(r, 0, 1, 0, 0, 0, 0, None) == moe.MOE_ERR_ARG

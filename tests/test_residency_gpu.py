@@ -13,6 +13,12 @@
   leaves the slot empty, and the next step recovers.
 * The optional CRC-32 check of host records: a wrong checksum refuses the
   step that would upload the record, with the cache state unchanged.
+* Router lookahead (moe_residency_lookahead): the hand-worked trace
+  (tests/golden/lfu_lookahead_trace.txt, its one-token rows) replayed with a
+  steered router; Zipf streams at B=1 and B=4, the lookahead on its own
+  streams in the second, whose slots and counters equal the oracle's replay
+  of the ids the GPU predicted and chose, with outputs unchanged; a failed
+  lookahead copy and a record failing its checksum.
 """
 import ctypes
 import os
@@ -224,5 +230,137 @@ def test_record_checksums():
     got = host(cl.decode(bf16_tensor(x1, DEV)))
     assert dl.check() == moe.MOE_OK, moe.last_error()
     assert_oracle(got, 0, *orc.token(x1[0]))
+    cl.close()
+    dl.close()
+
+
+def test_lookahead_hand_trace_on_gpu():
+    rows = [[c.strip() for c in l.split("|")]
+            for l in open(os.path.join(GOLDEN, "lfu_lookahead_trace.txt"))
+            if l.strip() and not l.startswith("#")]
+    rows = [r for r in rows if ";" not in r[3]]  # one-token rows: the router is steered per expert
+    assert len(rows) >= 8
+    shape = synth.Shape(64, 6, 2, 64, 64)
+    hl, dl, cl = make(shape, 5, np.zeros(6, np.float32), 3, max_tokens=1)
+    x = bf16_tensor(synth.hidden(5, 0, 0, 64)[None], DEV)
+    keys = ("hits", "misses", "lookahead_copies", "lookahead_hits", "evictions")
+    for r in rows[:8]:                                   # rows 1-8 run back to back
+        ids = [int(t) for t in r[3].split()]
+        beta = np.zeros(6, np.float32)
+        beta[ids[0]], beta[ids[1]] = 200.0, 100.0
+        dl.beta.copy_(torch.from_numpy(beta))
+        prev = cl.stats()
+        if r[1] == "D":
+            got = host(cl.decode(x))
+            assert list(got[2][0]) == ids
+            assert_close(got, host(dl.decode(x)))
+        else:
+            pids, _ = cl.lookahead(x, int(r[2]))
+            torch.cuda.synchronize()
+            assert list(pids.cpu().numpy()[0]) == ids
+        st = cl.stats()
+        assert [st[k] - prev[k] for k in keys] == [int(t) for t in r[4:9]], f"row {r[0]}"
+        assert cl.slots() == [int(t) for t in r[9].split()], f"row {r[0]}"
+    st = cl.stats()
+    rec = oracle.record_layout(64, 64)["bytes"]
+    assert st["lookaheads"] == sum(1 for r in rows[:8] if r[1] == "P")
+    assert st["lookahead_bytes"] == st["lookahead_copies"] * rec
+    assert st["bytes_h2d"] == st["misses"] * rec
+    assert dl.check() == moe.MOE_OK, moe.last_error()
+    assert cl.check_lookahead() == moe.MOE_OK, moe.last_error()
+    cl.close()
+    dl.close()
+
+
+@pytest.mark.parametrize("B,steps,n_slots,n_ahead,own_streams", [(1, 40, 8, 2, False),
+                                                                 (4, 16, 16, 2, True)])
+def test_lookahead_zipf_stream_matches_replay(B, steps, n_slots, n_ahead, own_streams):
+    shape = synth.Shape(256, 64, 4, 128, 256)
+    beta = synth.beta_zipf(4, 0, 64)
+    hl, dl, cl = make(shape, 7, beta, n_slots, max_tokens=B)
+    orc = hl.oracle()
+    lfu = oracle.LFU(n_slots, 64)
+    ls = torch.cuda.Stream(DEV) if own_streams else None
+    lc = torch.cuda.Stream(DEV) if own_streams else None
+    keys = ("hits", "misses", "evictions", "lookahead_copies", "lookahead_hits")
+    for s in range(steps):
+        # the "earlier" hidden state of the lookahead and the step's own
+        xp = bf16_tensor(np.stack([hidden_with_margin(orc, 21, s, t) for t in range(B)]), DEV)
+        xs = np.stack([hidden_with_margin(orc, 9, s, t) for t in range(B)])
+        x = bf16_tensor(xs, DEV)
+        if own_streams:
+            ls.wait_stream(torch.cuda.current_stream(DEV))
+            pids, _ = cl.lookahead(xp, n_ahead, stream=ls.cuda_stream, copy_stream=lc)
+            torch.cuda.current_stream(DEV).wait_stream(ls)
+        else:
+            pids, _ = cl.lookahead(xp, n_ahead)
+        pred = pids.cpu().numpy()
+        assert np.array_equal(pred, host(dl.decode(xp))[2])    # the layer's own router on xp
+        lfu.lookahead(pred, n_ahead)
+        assert cl.slots() == list(lfu.slot_expert)
+        got = host(cl.decode(x))
+        lfu.step(first_appearance(got[2]))
+        st = cl.stats()
+        assert [st[k] for k in keys] == [getattr(lfu, k) for k in keys]
+        assert cl.slots() == list(lfu.slot_expert)
+        assert_close(got, host(dl.decode(x)))
+        if s % 8 == 0 or s == steps - 1:
+            for t in range(B):
+                assert_oracle(got, t, *orc.token(xs[t]))
+    assert dl.check() == moe.MOE_OK, moe.last_error()
+    assert cl.check_lookahead() == moe.MOE_OK, moe.last_error()
+    st = cl.stats()
+    assert st["lookahead_copies"] > 0 and st["lookahead_hits"] >= 0 and st["lookaheads"] == steps
+    cl.close()
+    dl.close()
+
+
+def test_lookahead_faults():
+    """A lookahead copy that fails: MOE_ERR_CUDA, its slot left empty, and
+    the next step still matches the oracle.  A predicted record that fails
+    its CRC-32 check: MOE_ERR_RESIDENCY, cache state unchanged."""
+    shape = synth.Shape(256, 16, 2, 128, 256)
+    hl, dl, cl = make(shape, 3, None, 4, max_tokens=1)
+    orc = hl.oracle()
+    x0 = np.stack([hidden_with_margin(orc, 23, 0, 0)])
+    cl.set_fault(moe.MOE_RESIDENCY_FAULT_COPY)
+    with pytest.raises(moe.MoEError) as ei:
+        cl.lookahead(bf16_tensor(x0, DEV), 2)
+    assert ei.value.code == moe.MOE_ERR_CUDA
+    torch.cuda.synchronize()
+    assert cl.slots().count(-1) == 4
+    got = host(cl.decode(bf16_tensor(x0, DEV)))
+    assert dl.check() == moe.MOE_OK, moe.last_error()
+    assert_oracle(got, 0, *orc.token(x0[0]))
+    # checksums: a wrong value for a predicted, non-resident expert
+    L = moe.lib()
+    lay = moe.moe_record_layout()
+    assert L.moe_record_layout_of(shape.H, shape.F, ctypes.byref(lay)) == moe.MOE_OK
+    base = cl.host.data_ptr()
+    crc = np.array([L.moe_crc32(base + e * lay.stride, lay.bytes) for e in range(shape.E)], np.uint32)
+    resident = set(cl.slots())
+    for s in range(1, 64):
+        x1 = np.stack([hidden_with_margin(orc, 23, s, 0)])
+        need = [int(e) for e in orc.route(x1[0])[1] if int(e) not in resident]
+        if need:
+            break
+    else:
+        pytest.fail("no token needing a non-resident expert")
+    bad = crc.copy()
+    bad[need[0]] ^= 1
+    assert L.moe_residency_verify(cl.handle, bad.ctypes.data) == moe.MOE_OK
+    before, slots = cl.stats(), cl.slots()
+    with pytest.raises(moe.MoEError) as ei:
+        cl.lookahead(bf16_tensor(x1, DEV), 2)
+    assert ei.value.code == moe.MOE_ERR_RESIDENCY and f"expert {need[0]} " in str(ei.value)
+    assert cl.stats() == before and cl.slots() == slots
+    assert L.moe_residency_verify(cl.handle, crc.ctypes.data) == moe.MOE_OK
+    cl.lookahead(bf16_tensor(x1, DEV), 2)
+    got = host(cl.decode(bf16_tensor(x1, DEV)))
+    assert dl.check() == moe.MOE_OK, moe.last_error()
+    assert cl.check_lookahead() == moe.MOE_OK, moe.last_error()
+    assert_oracle(got, 0, *orc.token(x1[0]))
+    st = cl.stats()
+    assert st["lookahead_hits"] >= 1 and st["misses"] - before["misses"] == 0
     cl.close()
     dl.close()
