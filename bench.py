@@ -54,7 +54,10 @@ def parse_args():
                    help="only the prefill-chunk measurement (mid-prefill, T=128), one JSON object")
     p.add_argument("--streamed", action="store_true",
                    help="add the streamed-cache workload (4 large layers, experts in pinned host "
-                        "memory, 64 HBM slots per layer, 256 B=1 steps); needs ~51 GB of host RAM")
+                        "memory, 64 HBM slots per layer, 256 B=1 steps, with and without the "
+                        "router lookahead); needs ~51 GB of host RAM")
+    p.add_argument("--streamed-only", action="store_true",
+                   help="only the streamed-cache workload, one JSON object")
     a = p.parse_args()
     a.warmup = max(a.warmup, 3)
     return a
@@ -412,6 +415,12 @@ def run_ours(args, world, rank, local):
         if rank == 0:
             print(json.dumps({"prefill": res}), flush=True)
         return
+    if args.streamed_only:
+        stream = torch.cuda.Stream(device)
+        res = run_streamed(args, device, stream, _peaks().get("hbm_gbs", 6800.0))
+        if rank == 0:
+            print(json.dumps({"streamed": res}), flush=True)
+        return
     wl = synth.WORKLOADS[WORKLOAD]
     s = wl.shape
     if args.experts:
@@ -645,12 +654,49 @@ def h2d_bandwidth(torch, device, nbytes=1 << 30, reps=5) -> float:
     return best
 
 
+LOOKAHEAD_RHO = 0.9   # hidden-state correlation between consecutive layers (chained inputs)
+LOOKAHEAD_N = 6       # experts read ahead per token
+STREAMED_COUNTS = os.path.join(os.path.dirname(os.path.abspath(__file__)), "tests", "golden",
+                               "streamed_lfu_counts.txt")
+COUNT_KEYS = ("hits", "misses", "evictions", "lookahead_copies", "lookahead_hits")
+
+
+def streamed_expected() -> dict:
+    """{run: [[counter per COUNT_KEYS] per layer]} from the oracle's replay of
+    the streamed workload (tests/golden/make_streamed_lfu_counts.py)."""
+    out = {}
+    try:
+        for line in open(STREAMED_COUNTS):
+            if line.strip() and not line.startswith("#"):
+                f = [c.strip() for c in line.split("|")]
+                out.setdefault(f[0], []).append([int(v) for v in f[2:]])
+    except OSError:
+        pass
+    return out
+
+
+def replay_verdict(expected, st) -> str:
+    """'equal' when every layer's counters equal the oracle's replay."""
+    if not expected:
+        return "no stored replay"
+    diffs = [f"layer {l} {k}: {s[k]} vs {e[i]}" for l, (s, e) in enumerate(zip(st, expected))
+             for i, k in enumerate(COUNT_KEYS) if s[k] != e[i]]
+    return "equal" if not diffs and len(st) == len(expected) else "differs: " + "; ".join(diffs[:4])
+
+
 def run_streamed(args, device, stream, hbm_peak):
     """Streamed expert cache: 4 stacked layers of the large shape, all expert
     records in pinned host memory, 64 HBM slots per layer, router offsets
-    Zipf(1.1) per layer, 256 consecutive B=1 steps from a cold cache (hidden
-    states drawn per step and layer; layers are not chained).  Timed end to
-    end (the cache update waits on the router every layer)."""
+    Zipf(1.1) per layer, 256 consecutive B=1 steps from a cold cache, timed
+    end to end (the cache update waits on the router every layer).
+
+    Three runs: (1) hidden states drawn independently per step and layer;
+    (2) and (3) hidden states chained across layers (synth.hidden_chain,
+    rho = LOOKAHEAD_RHO), without and with the router lookahead: after layer
+    l's step is issued, layer l+1's router runs on layer l's hidden state on
+    a stream of its own and its first LOOKAHEAD_N experts are read ahead.
+    All layers share one copy stream, so lookahead copies queue behind the
+    demand copies issued before them."""
     import numpy as np
     import torch
 
@@ -666,53 +712,87 @@ def run_streamed(args, device, stream, hbm_peak):
         dls.append(DeviceLayer(s, wl.weight_seed, layer=l, beta=synth.beta_for(wl, l), max_tokens=1,
                                device=device, resident=False))
         hosts.append(pinned_records(s, wl.weight_seed, layer=l))
-    xs = bf16_tensor(np.stack([np.stack([synth.hidden(wl.input_seed, l, t, s.H)[None] for l in range(nl)])
-                               for t in range(steps)]), device)  # [steps][layers][1][H]
+    xs_ind = bf16_tensor(np.stack([np.stack([synth.hidden(wl.input_seed, l, t, s.H)[None] for l in range(nl)])
+                                   for t in range(steps)]), device)  # [steps][layers][1][H]
+    xs_chain = bf16_tensor(np.stack([synth.hidden_chain(wl.input_seed, t, s.H, nl, LOOKAHEAD_RHO)[:, None]
+                                     for t in range(steps)]), device)
     outs = [d.outputs(1) for d in dls]
+    copy = torch.cuda.Stream(device)
+    side = torch.cuda.Stream(device)
+    hbm_bytes = nl * steps * layer_step_bytes(s, 1, s.k, with_f32=True)["step"]
 
-    def run(n, caches):
+    def caches_new():
+        cs = [CachedLayer(dls[l], hosts[l], slots) for l in range(nl)]
+        for c in cs:
+            c.copy_stream = copy
+            c.prepare_lookahead(side.cuda_stream)
+        return cs
+
+    def run(n, caches, xs, ahead):
         with torch.cuda.stream(stream):
             for t in range(n):
                 for l in range(nl):
                     caches[l].decode(xs[t, l], outs[l], stream.cuda_stream)
+                    if ahead and l + 1 < nl:
+                        caches[l + 1].lookahead(xs[t, l], LOOKAHEAD_N, stream=side.cuda_stream)
 
-    warm = [CachedLayer(dls[l], hosts[l], slots) for l in range(nl)]
-    run(max(args.warmup, 3), warm)          # kernels and copies warmed on throwaway caches
-    torch.cuda.synchronize()
-    for c in warm:
-        c.close()
-    caches = [CachedLayer(dls[l], hosts[l], slots) for l in range(nl)]
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    t0 = time.perf_counter()
-    run(steps, caches)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    wall = time.perf_counter() - t0
-    ms = e0.elapsed_time(e1)
-    for d in dls:
-        assert d.check(stream.cuda_stream) == 0
-    st = [c.stats() for c in caches]
-    hits, misses = sum(x["hits"] for x in st), sum(x["misses"] for x in st)
-    h2d = sum(x["bytes_h2d"] for x in st)
-    hbm_bytes = nl * steps * layer_step_bytes(s, 1, s.k, with_f32=True)["step"]
-    bound_s = max(hbm_bytes / (hbm_peak * 1e9), h2d / (bw * 1e9))
-    for c in caches:
-        c.close()
+    expected = streamed_expected()
+
+    def measure(xs, ahead, run_name):
+        warm = caches_new()
+        run(max(args.warmup, 3), warm, xs, ahead)  # kernels and copies warmed on throwaway caches
+        torch.cuda.synchronize()
+        for c in warm:
+            c.close()
+        caches = caches_new()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        t0 = time.perf_counter()
+        run(steps, caches, xs, ahead)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+        ms = e0.elapsed_time(e1)
+        for d in dls:
+            assert d.check(stream.cuda_stream) == 0
+        for c in caches:
+            assert c.check_lookahead(stream.cuda_stream) == 0
+        st = [c.stats() for c in caches]
+        for c in caches:
+            c.close()
+
+        def tot(key, layers=range(nl)):
+            return sum(st[l][key] for l in layers)
+
+        hits, misses = tot("hits"), tot("misses")
+        h2d = tot("bytes_h2d") + tot("lookahead_bytes")
+        bound_s = max(hbm_bytes / (hbm_peak * 1e9), h2d / (bw * 1e9))
+        later = range(1, nl)
+        return {"oracle_replay": replay_verdict(expected.get(run_name), st),
+                "tokens_per_s": steps / (ms / 1e3), "ms_per_token": ms / steps, "wall_s": wall,
+                "hit_rate": hits / max(1, hits + misses), "hits": hits, "misses": misses,
+                "hit_rate_layers_1_on": tot("hits", later) / max(1, tot("hits", later) + tot("misses", later)),
+                "lookahead_copies": tot("lookahead_copies"), "lookahead_hits": tot("lookahead_hits"),
+                "bytes_h2d": h2d, "h2d_bytes_per_token": h2d / steps,
+                "h2d_gbs_achieved": h2d / (ms / 1e3) / 1e9,
+                "bound_ms_per_token": bound_s * 1e3 / steps,
+                "frac_of_bound": (bound_s * 1e3 / steps) / (ms / steps)}
+
+    base = measure(xs_ind, False, "independent")
+    chained_off = measure(xs_chain, False, "chained_off")
+    chained_on = measure(xs_chain, True, "chained_on")
     for d in dls:
         d.close()
     del hosts
-    return {"workload": f"large-streamed: {nl} layers of H={s.H} E={s.E} top-{s.k} F={s.F} Fs={s.Fs}, "
-                        f"{slots} HBM slots per layer, Zipf(1.1) router offsets, {steps} B=1 steps "
-                        "from a cold cache",
-            "tokens_per_s": steps / (ms / 1e3), "ms_per_token": ms / steps, "wall_s": wall,
-            "hit_rate": hits / max(1, hits + misses), "hits": hits, "misses": misses,
-            "bytes_h2d": h2d, "h2d_bytes_per_token": h2d / steps,
-            "h2d_gbs_achieved": h2d / (ms / 1e3) / 1e9, "h2d_gbs_probed": bw,
-            "hbm_bytes_per_token": hbm_bytes / steps,
-            "bound_ms_per_token": bound_s * 1e3 / steps,
-            "frac_of_bound": (bound_s * 1e3 / steps) / (ms / steps)}
+    res = {"workload": f"large-streamed: {nl} layers of H={s.H} E={s.E} top-{s.k} F={s.F} Fs={s.Fs}, "
+                       f"{slots} HBM slots per layer, Zipf(1.1) router offsets, {steps} B=1 steps "
+                       "from a cold cache",
+           "h2d_gbs_probed": bw, "hbm_bytes_per_token": hbm_bytes / steps}
+    res.update(base)
+    res["lookahead"] = {"inputs": f"hidden states chained across layers, rho={LOOKAHEAD_RHO}",
+                        "n_ahead": LOOKAHEAD_N, "off": chained_off, "on": chained_on}
+    return res
 
 
 def cpu_baseline(wl, s, target_s=15.0):

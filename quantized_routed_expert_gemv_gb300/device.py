@@ -151,15 +151,21 @@ class CachedLayer:
         predicted (ids, weights) [B][k] on the device."""
         dl = self.dl
         st = stream if stream is not None else torch.cuda.current_stream(dl.device).cuda_stream
-        if self.ahead_ws is None:
-            self.ahead_ws = torch.empty(dl.ws_bytes, dtype=torch.uint8, device=dl.device)
-            moe.moe_workspace_init(dl.handle, self.ahead_ws.data_ptr(), dl.ws_bytes, st)
-            _, _, self.ahead_ids, self.ahead_w = dl.outputs(dl.desc.max_tokens)
+        self.prepare_lookahead(st)
         B = x.shape[0]
         moe.moe_residency_lookahead(self.handle, x.data_ptr(), B, n_ahead, self.ahead_ids.data_ptr(),
                                     self.ahead_w.data_ptr(), self.ahead_ws.data_ptr(), dl.ws_bytes,
                                     st, (copy_stream or self.copy_stream).cuda_stream)
         return self.ahead_ids[:B], self.ahead_w[:B]
+
+    def prepare_lookahead(self, stream) -> None:
+        """Allocates the lookahead's workspace and predicted-routing buffers
+        (once); stream orders the workspace initialisation."""
+        if self.ahead_ws is None:
+            dl = self.dl
+            self.ahead_ws = torch.empty(dl.ws_bytes, dtype=torch.uint8, device=dl.device)
+            moe.moe_workspace_init(dl.handle, self.ahead_ws.data_ptr(), dl.ws_bytes, stream)
+            _, _, self.ahead_ids, self.ahead_w = dl.outputs(dl.desc.max_tokens)
 
     def check_lookahead(self, stream=None) -> int:
         """moe_check of the lookahead workspace (0 if none was made)."""

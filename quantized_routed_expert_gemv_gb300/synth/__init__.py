@@ -177,6 +177,22 @@ def hidden(seed: int, stream: int, token: int, H: int, attempt: int = 0) -> np.n
     return out
 
 
+def hidden_chain(seed: int, token: int, H: int, layers: int, rho: float) -> np.ndarray:
+    """Hidden states of one token at successive layers, bf16 bits
+    uint16[layers][H], standing in for a residual stream that each layer
+    changes only in part: x_0 = z_0 and x_{l+1} = bf16(f32(rho * x_l +
+    sqrt(1 - rho^2) * z_{l+1})), with z_l = hidden(seed, l, token, H).  Every
+    x_l stays ~ N(0, 1); rho = 0 gives the independent per-layer draws."""
+    out = np.empty((layers, H), np.uint16)
+    out[0] = hidden(seed, 0, token, H)
+    c = float(np.sqrt(max(0.0, 1.0 - rho * rho)))
+    for l in range(1, layers):
+        prev = bf16_bits_to_float(out[l - 1]).astype(np.float64)
+        z = bf16_bits_to_float(hidden(seed, l, token, H)).astype(np.float64)
+        out[l] = float_to_bf16_bits((rho * prev + c * z).astype(np.float32))
+    return out
+
+
 def uniforms(k: int, n: int) -> np.ndarray:
     out = np.empty(n, np.float64)
     lib().synth_fill_f64_uniform(k, out.ctypes.data, n)

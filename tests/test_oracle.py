@@ -379,6 +379,20 @@ def test_synth_bf16_rounding():
     assert synth.bf16_from_double(-0.75) == 0xBF40
 
 
+def test_synth_hidden_chain():
+    H = 4096
+    ind = synth.hidden_chain(3, 5, H, 4, 0.0)
+    for l in range(4):
+        assert np.array_equal(ind[l], synth.hidden(3, l, 5, H))   # rho = 0: independent draws
+    ch = synth.hidden_chain(3, 5, H, 4, 0.9)
+    assert np.array_equal(ch[0], ind[0])
+    xs = synth.bf16_bits_to_float(ch).astype(np.float64)
+    for l in range(4):
+        assert abs(xs[l].std() - 1.0) < 0.05
+    for l in range(1, 4):
+        assert abs(np.corrcoef(xs[l - 1], xs[l])[0, 1] - 0.9) < 0.02
+
+
 def test_synth_random_access_and_distributions():
     H, F = 256, 128
     buf = np.zeros((3, synth.record_stride(H, F)), np.uint8)
