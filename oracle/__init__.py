@@ -190,6 +190,26 @@ class Layer:
         return out, ids, p
 
 
+def waves(ids: np.ndarray, n_slots: int):
+    """Splits a step's tokens into waves of consecutive tokens whose distinct
+    experts fit the cache: a wave grows token by token while the union of
+    its tokens' ids has at most n_slots experts.  ids[B][k]; returns the
+    [t0, t1) bounds.  (The pages give a cache of fixed size and a router of
+    k experts per token, and no rule for a step that needs more; reading:
+    run it as several steps, tokens in order.)"""
+    ids = np.asarray(ids)
+    out, t0, have = [], 0, set()
+    for t in range(ids.shape[0]):
+        row = set(int(e) for e in ids[t])
+        if len(have | row) > n_slots:
+            out.append((t0, t))
+            t0, have = t, set()
+        have |= row
+    if ids.shape[0]:
+        out.append((t0, ids.shape[0]))
+    return out
+
+
 class LFU:
     """Replays the bounded LFU residency policy on an id stream, with the
     optional router lookahead between demand steps (see oracle.c).

@@ -299,6 +299,17 @@ def test_lfu_invariants_random_stream():
     assert total_miss < 300 * k
 
 
+def test_waves_hand_example():
+    # 4 slots, top-2.  Worked by hand: {0,1} then {1,2} -> 3 experts; {3,4}
+    # would make 5 -> new wave; {3,4} {4,5} {0,5} -> {0,3,4,5} = 4 fits; then
+    # {1,2} makes 6 -> new wave.
+    ids = np.array([[0, 1], [1, 2], [3, 4], [4, 5], [0, 5], [1, 2]])
+    assert oracle.waves(ids, 4) == [(0, 2), (2, 5), (5, 6)]
+    assert oracle.waves(ids, 6) == [(0, 6)]
+    assert oracle.waves(ids, 2) == [(0, 1), (1, 2), (2, 3), (3, 4), (4, 5), (5, 6)]
+    assert oracle.waves(ids[:0], 4) == []
+
+
 def test_lfu_lookahead_hand_trace():
     rows = [[c.strip() for c in l.split("|")]
             for l in open(os.path.join(GOLDEN, "lfu_lookahead_trace.txt"))
