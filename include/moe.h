@@ -206,7 +206,7 @@ const char *moe_last_error(void);
 typedef struct moe_residency moe_residency;
 
 typedef struct {
-    uint64_t steps;      /* moe_residency_decode calls that reached the cache */
+    uint64_t steps;      /* cache steps: one per moe_residency_decode call, one per wave */
     uint64_t hits;       /* distinct experts of a step already resident */
     uint64_t misses;     /* distinct experts copied in */
     uint64_t evictions;  /* copies (misses or lookahead) that replaced a resident expert */
@@ -247,8 +247,10 @@ int moe_residency_open(moe_layer *layer, const void *host_records, int32_t n_slo
  * host waits for the ids (this call blocks until the router has finished),
  * updates the cache and issues one cudaMemcpyAsync per miss and one for the
  * slot tables on copy_stream; main_stream waits for them, then runs the
- * routed experts and the combine.  MOE_ERR_RESIDENCY (returned) if a step
- * needs more distinct experts than there are slots or the router's ids are
+ * routed experts and the combine.  A call whose tokens need more distinct
+ * experts than there are slots runs as waves: consecutive tokens, each wave
+ * growing while its experts fit the slots, each a step of its own (its
+ * router runs again).  MOE_ERR_RESIDENCY (returned) if the router's ids are
  * out of range; the cache state is then unchanged.  Device-side tag
  * mismatches are latched and reported by moe_check. */
 int moe_residency_decode(moe_residency *res, const uint16_t *x, int32_t B, uint16_t *out_bf16,

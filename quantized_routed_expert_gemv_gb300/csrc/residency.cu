@@ -264,6 +264,27 @@ static int choose_slot(const moe_residency* R, bool lookahead) {
   return best;
 }
 
+// Where a step needs more distinct experts than there are slots, its tokens
+// run in waves: a wave grows token by token while the union of its tokens'
+// experts fits the slots.  Writes each wave's first token to starts.
+static void plan_waves(const moe_residency* R, int B, std::vector<int>* starts) {
+  std::vector<uint8_t> in(R->E, 0);
+  std::vector<int32_t> members;
+  starts->assign(1, 0);
+  for (int t = 0; t < B; ++t) {
+    const int32_t* row = R->h_ids + static_cast<size_t>(t) * R->k;
+    int add = 0;
+    for (int i = 0; i < R->k; ++i) add += in[row[i]] ? 0 : 1;
+    if (static_cast<int>(members.size()) + add > R->n_slots) {
+      for (int32_t e : members) in[e] = 0;
+      members.clear();
+      starts->push_back(t);
+    }
+    for (int i = 0; i < R->k; ++i)
+      if (!in[row[i]]) in[row[i]] = 1, members.push_back(row[i]);
+  }
+}
+
 // Uploads the host's slot tables to the device on st from the next pinned
 // image; fault_expert >= 0 plants a wrong tag for that expert's slot.
 static cudaError_t upload_tables(moe_residency* R, cudaStream_t st, int fault_expert) {
@@ -319,8 +340,21 @@ extern "C" int moe_residency_decode(moe_residency* R, const uint16_t* x, int32_t
     if (R->pinned_at[ex] != step) R->pinned_at[ex] = step, R->order.push_back(ex);
   }
   if (static_cast<int>(R->order.size()) > R->n_slots) {
+    // more experts than slots: waves of consecutive tokens, each a step of
+    // its own (its router runs again; a single token always fits)
     for (int32_t ex : R->order) R->pinned_at[ex] = R->step;  // leave the state as it was
-    return moe::report_error(MOE_ERR_RESIDENCY, "moe_residency_decode: the step needs more distinct experts than the cache has slots");
+    std::vector<int> starts;
+    plan_waves(R, B, &starts);
+    starts.push_back(B);
+    const size_t H = moe::layer_desc(R->layer)->hidden, k = R->k;
+    for (size_t w = 0; w + 1 < starts.size(); ++w) {
+      const int t0 = starts[w], n = starts[w + 1] - t0;
+      rc = moe_residency_decode(R, x + t0 * H, n, out_bf16 + t0 * H, out_f32 ? out_f32 + t0 * H : nullptr,
+                                ids + t0 * k, weights + t0 * k, workspace, workspace_bytes, main_stream,
+                                copy_stream);
+      if (rc) return rc;
+    }
+    return MOE_OK;
   }
   // optional payload check of records about to be uploaded for the first
   // time; a mismatch refuses the step before any state changes

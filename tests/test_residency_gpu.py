@@ -11,6 +11,8 @@
 * Host-side fault injection: a wrong slot tag is caught by the kernels
   (MOE_ERR_RESIDENCY through moe_check); a failed copy returns MOE_ERR_CUDA,
   leaves the slot empty, and the next step recovers.
+* A step needing more experts than slots runs as waves of consecutive
+  tokens, replayed exactly by the oracle.
 * The optional CRC-32 check of host records: a wrong checksum refuses the
   step that would upload the record, with the cache state unchanged.
 * Router lookahead (moe_residency_lookahead): the hand-worked trace
@@ -168,24 +170,39 @@ def test_faults_are_caught_and_recovered():
     assert dl.check() == moe.MOE_OK, moe.last_error()
     assert_oracle(got, 0, *orc.token(xs[2][0]))
     cl.close()
-    # more distinct experts in a step than slots (2 slots, 2 tokens of top-2):
-    # refused, state unchanged
-    small = CachedLayer(dl, cl.host, 2)
-    host(small.decode(bf16_tensor(xs[3], DEV)))
-    before, slots = small.stats(), small.slots()
-    for s in range(8):
-        x2 = np.stack([hidden_with_margin(orc, 14, s, t) for t in range(2)])
-        ids = host(dl.decode(bf16_tensor(x2, DEV)))[2]
-        if len(set(ids.reshape(-1).tolist())) > 2:
-            break
-    else:
-        pytest.fail("no pair of tokens with more than 2 distinct experts")
-    with pytest.raises(moe.MoEError) as ei:
-        small.decode(bf16_tensor(x2, DEV))
-    assert ei.value.code == moe.MOE_ERR_RESIDENCY
-    torch.cuda.synchronize()
-    assert small.stats() == before and small.slots() == slots
-    small.close()
+    dl.close()
+
+
+def test_waves_when_a_step_needs_more_experts_than_slots():
+    """A step whose tokens need more distinct experts than there are slots
+    runs as waves of consecutive tokens (each a cache step): slots and
+    counters equal the oracle's LFU replay of the waves oracle.waves cuts
+    from the GPU's ids; outputs equal moe_decode's and the oracle's."""
+    shape = synth.Shape(256, 64, 4, 128, 256)
+    beta = synth.beta_zipf(4, 0, 64)
+    B, n_slots = 8, 8
+    hl, dl, cl = make(shape, 9, beta, n_slots, max_tokens=B)
+    orc = hl.oracle()
+    lfu = oracle.LFU(n_slots, 64)
+    n_waves = 0
+    for s in range(6):
+        xs = np.stack([hidden_with_margin(orc, 31, s, t) for t in range(B)])
+        x = bf16_tensor(xs, DEV)
+        got = host(cl.decode(x))
+        ws = oracle.waves(got[2], n_slots)
+        assert len(ws) > 1
+        for t0, t1 in ws:
+            lfu.step(first_appearance(got[2][t0:t1]))
+        n_waves += len(ws)
+        st = cl.stats()
+        assert st["steps"] == n_waves
+        assert (st["hits"], st["misses"], st["evictions"]) == (lfu.hits, lfu.misses, lfu.evictions)
+        assert cl.slots() == list(lfu.slot_expert)
+        assert_close(got, host(dl.decode(x)))
+        for t in (0, B - 1):
+            assert_oracle(got, t, *orc.token(xs[t]))
+    assert dl.check() == moe.MOE_OK, moe.last_error()
+    cl.close()
     dl.close()
 
 
