@@ -49,7 +49,8 @@ class _Layer(ctypes.Structure):
                 ("shared_record", ctypes.c_void_p),
                 ("router_codes", ctypes.c_void_p),
                 ("router_sb", ctypes.c_void_p),
-                ("beta", ctypes.c_void_p)]
+                ("beta", ctypes.c_void_p),
+                ("codebooks", ctypes.c_void_p)]
 
 
 _lib = None
@@ -83,6 +84,11 @@ def lib():
         L.orc_lfu_step.restype = i32
         L.orc_lfu_lookahead.argtypes = [i32, i32, vp, vp, vp, vp, vp, vp, i32, vp, vp]
         L.orc_lfu_lookahead.restype = i32
+        L.orc_rvq_layout.argtypes = [i32, i32, ctypes.POINTER(_Layout)]
+        L.orc_dequant_rvq.argtypes = [vp, vp, i32, i32, i32]
+        L.orc_dequant_rvq.restype = d
+        L.orc_gemv_rvq.argtypes = [vp, vp, i32, i32, vp, vp]
+        L.orc_expert_rvq.argtypes = [vp, vp, i32, i32, vp, vp, vp]
     return _lib
 
 
@@ -116,6 +122,35 @@ def gemv4(codes: np.ndarray, sb: np.ndarray, rows: int, cols: int, x: np.ndarray
     return y
 
 
+def rvq_layout(H: int, F: int) -> dict:
+    """Byte layout of a 3-bit residual-VQ expert record (see oracle.c)."""
+    L = _Layout()
+    lib().orc_rvq_layout(H, F, ctypes.byref(L))
+    return {n: int(getattr(L, n)) for n, _ in _Layout._fields_}
+
+
+def dequant_rvq(codes: np.ndarray, cb: np.ndarray, cols: int, r: int, j: int) -> float:
+    """Weight (r, j) of an RVQ matrix; cb = one kind's codebooks [3][256][8] bf16."""
+    return lib().orc_dequant_rvq(_p(codes), _p(np.ascontiguousarray(cb, np.uint16)), cols, r, j)
+
+
+def gemv_rvq(codes: np.ndarray, cb: np.ndarray, rows: int, cols: int, x: np.ndarray) -> np.ndarray:
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    y = np.zeros(rows, np.float64)
+    lib().orc_gemv_rvq(_p(codes), _p(np.ascontiguousarray(cb, np.uint16)), rows, cols, _p(x), _p(y))
+    return y
+
+
+def expert_rvq(record: np.ndarray, codebooks: np.ndarray, H: int, F: int, x: np.ndarray) -> np.ndarray:
+    """y = W_d(silu(W_g x) * W_u x) for one RVQ record; codebooks [3][3][256][8] bf16."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    y = np.zeros(H, np.float64)
+    scr = np.zeros(3 * F, np.float64)
+    lib().orc_expert_rvq(_p(record), _p(np.ascontiguousarray(codebooks, np.uint16)), H, F, _p(x),
+                         _p(y), _p(scr))
+    return y
+
+
 def silu(z: float) -> float:
     return lib().orc_silu(z)
 
@@ -135,8 +170,11 @@ class Layer:
     missing experts are allowed as long as the token does not select them."""
 
     def __init__(self, H, E, k, F, Fs, records, shared_record, router_codes, router_sb,
-                 beta=None):
+                 beta=None, codebooks=None):
+        """codebooks: bf16 [3][3][256][8] for a layer of 3-bit residual-VQ
+        experts; None for 4-bit affine experts."""
         self.H, self.E, self.k, self.F, self.Fs = H, E, k, F, Fs
+        self._cb = None if codebooks is None else np.ascontiguousarray(codebooks, dtype=np.uint16)
         self._recs = dict(records)
         self._shared = shared_record
         self._rc = np.ascontiguousarray(router_codes, dtype=np.uint8)
@@ -150,7 +188,8 @@ class Layer:
                          ctypes.cast(self._ptrs, ctypes.POINTER(ctypes.c_void_p)),
                          None if shared_record is None else shared_record.ctypes.data,
                          self._rc.ctypes.data, self._rsb.ctypes.data,
-                         None if self._beta is None else self._beta.ctypes.data)
+                         None if self._beta is None else self._beta.ctypes.data,
+                         None if self._cb is None else self._cb.ctypes.data)
 
     def set_record(self, e: int, rec: np.ndarray):
         self._recs[e] = rec

@@ -43,6 +43,19 @@
  *          bf16 scale, bits 16..31 the bf16 bias;
  *   stride: total size rounded up to 4096 bytes.
  * Router: codes u8 [E][H] row-major, sb words [E][H/64] as above.
+ *
+ * Second expert format, 3-bit residual VQ -- WASTE page, section
+ * "Quantization ve doğruluk": each run of 8 weights along a row is the sum
+ * of one codeword from each of 3 stages, every stage a codebook of 256
+ * eight-value codewords, so 3 code bytes per 8 weights (3.00 bits/weight):
+ *     w[r][8b + i] = C1[q1(r,b)][i] + C2[q2(r,b)][i] + C3[q3(r,b)][i]
+ * Readings where the page is silent: the codebooks are per layer and matrix
+ * kind (gate, up, down), kept with the router rather than in the records
+ * (the page's codebooks sit outside the checksummed expert records);
+ * codewords are bf16; there is no scale or bias.  Record: [gate codes
+ * F x 3H/8][up codes F x 3H/8][down codes H x 3F/8], row-major, a row's
+ * blocks in order and each block's three stage bytes in stage order; stride
+ * rounded up to 4096.  Codebooks: bf16 [kind][stage][256][8].
  */
 #include <math.h>
 #include <stddef.h>
@@ -129,6 +142,41 @@ void orc_gemv4(const uint8_t *codes, const uint8_t *sb, int rows, int cols,
     }
 }
 
+/* ---- 3-bit residual VQ (second expert format) ----------------------------- */
+
+void orc_rvq_layout(int H, int F, orc_layout *L)
+{
+    uint64_t mat = (uint64_t)F * (uint64_t)H / 8u * 3u; /* gate, up or down codes */
+    L->gate_codes = 0;
+    L->up_codes = mat;
+    L->down_codes = 2 * mat;
+    L->bytes = 3 * mat;
+    L->gate_sb = L->up_sb = L->down_sb = L->bytes; /* no scale/bias words */
+    L->stride = (L->bytes + 4095u) / 4096u * 4096u;
+}
+
+/* Weight (r, j) of an RVQ matrix with `cols` inputs; cb is one kind's
+ * codebooks [3][256][8]. */
+double orc_dequant_rvq(const uint8_t *codes, const uint16_t *cb, int cols, int r, int j)
+{
+    const uint8_t *blk = codes + (size_t)r * ((size_t)cols / 8 * 3) + (size_t)(j / 8) * 3;
+    double w = 0.0;
+    for (int s = 0; s < 3; ++s)
+        w += orc_bf16_to_double(cb[((size_t)s * 256 + blk[s]) * 8 + (size_t)(j % 8)]);
+    return w;
+}
+
+void orc_gemv_rvq(const uint8_t *codes, const uint16_t *cb, int rows, int cols,
+                  const double *x, double *y)
+{
+    for (int r = 0; r < rows; ++r) {
+        double acc = 0.0;
+        for (int j = 0; j < cols; ++j)
+            acc += orc_dequant_rvq(codes, cb, cols, r, j) * x[j];
+        y[r] = acc;
+    }
+}
+
 /* ---- router, top-k, weights (steps 2-4) ---------------------------------- */
 
 void orc_router_logits(const uint8_t *codes, const uint8_t *sb, const float *beta,
@@ -186,6 +234,22 @@ void orc_expert(const uint8_t *rec, int H, int F, const double *x, double *y,
     orc_gemv4(rec + L.down_codes, rec + L.down_sb, H, F, h, y);
 }
 
+/* The same expert in the RVQ format; cbs = the layer's codebooks
+ * [gate, up, down][3][256][8]. */
+void orc_expert_rvq(const uint8_t *rec, const uint16_t *cbs, int H, int F, const double *x,
+                    double *y, double *scratch)
+{
+    orc_layout L;
+    orc_rvq_layout(H, F, &L);
+    const size_t kind = 3 * 256 * 8;
+    double *g = scratch, *u = scratch + F, *h = scratch + 2 * F;
+    orc_gemv_rvq(rec + L.gate_codes, cbs, F, H, x, g);
+    orc_gemv_rvq(rec + L.up_codes, cbs + kind, F, H, x, u);
+    for (int j = 0; j < F; ++j)
+        h[j] = orc_silu(g[j]) * u[j];
+    orc_gemv_rvq(rec + L.down_codes, cbs + 2 * kind, H, F, h, y);
+}
+
 /* ---- whole layer for one token (steps 1-6) ------------------------------- */
 
 typedef struct {
@@ -195,7 +259,17 @@ typedef struct {
     const uint8_t *router_codes;    /* [E][H] */
     const uint8_t *router_sb;       /* [E][H/64] words */
     const float *beta;              /* [E] or NULL */
+    const uint16_t *codebooks;      /* RVQ experts: [3][3][256][8] bf16; NULL: 4-bit affine */
 } orc_layer;
+
+static void layer_expert(const orc_layer *Ly, const uint8_t *rec, int F, const double *x,
+                         double *y, double *scratch)
+{
+    if (Ly->codebooks)
+        orc_expert_rvq(rec, Ly->codebooks, Ly->H, F, x, y, scratch);
+    else
+        orc_expert(rec, Ly->H, F, x, y, scratch);
+}
 
 /* Route one token: logits (E doubles), ids (k), p (k).  taken: E bytes. */
 void orc_route(const orc_layer *Ly, const uint16_t *x_bf16, double *xd,
@@ -220,7 +294,7 @@ int orc_moe_token(const orc_layer *Ly, const uint16_t *x_bf16, double *out,
     for (int r = 0; r < H; ++r)
         out[r] = 0.0;
     if (Ly->Fs > 0) {
-        orc_expert(Ly->shared_record, H, Ly->Fs, xd, y, scr);
+        layer_expert(Ly, Ly->shared_record, Ly->Fs, xd, y, scr);
         for (int r = 0; r < H; ++r)
             out[r] = y[r];
     }
@@ -228,7 +302,7 @@ int orc_moe_token(const orc_layer *Ly, const uint16_t *x_bf16, double *out,
         const uint8_t *rec = Ly->records[ids[i]];
         if (!rec)
             return -1;
-        orc_expert(rec, H, Ly->F, xd, y, scr);
+        layer_expert(Ly, rec, Ly->F, xd, y, scr);
         for (int r = 0; r < H; ++r)
             out[r] += p[i] * y[r];
     }
@@ -256,12 +330,12 @@ int orc_moe_token_dense(const orc_layer *Ly, const uint16_t *x_bf16, double *out
                 pe = p[i];
         if (!Ly->records[e])
             return -1;
-        orc_expert(Ly->records[e], H, Ly->F, xd, y, scr);
+        layer_expert(Ly, Ly->records[e], Ly->F, xd, y, scr);
         for (int r = 0; r < H; ++r)
             out[r] += pe * y[r];
     }
     if (Ly->Fs > 0) {
-        orc_expert(Ly->shared_record, H, Ly->Fs, xd, y, scr);
+        layer_expert(Ly, Ly->shared_record, Ly->Fs, xd, y, scr);
         for (int r = 0; r < H; ++r)
             out[r] += y[r];
     }

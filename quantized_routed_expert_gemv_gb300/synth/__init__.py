@@ -43,6 +43,14 @@ ROUTER_BIAS_SD = 0.05
 TAG_HIDDEN = 10
 TAG_BETA = 11
 TAG_PERM = 12
+TAG_RVQ_CODES = 13
+TAG_RVQ_CB = 14
+
+# 3-bit residual VQ experts: codeword values ~ N(0, sd) per stage, rounded to
+# bf16, each stage finer than the one before (the pages give no distribution;
+# these give weights of about the spread of the 4-bit experts' dequantised
+# values around their mean).
+RVQ_STAGE_SD = (0.05, 0.02, 0.01)
 
 
 def build(force: bool = False) -> str:
@@ -157,6 +165,54 @@ def fill_records(seed: int, layer: int, experts, H: int, F: int, out: np.ndarray
     else:
         with ThreadPoolExecutor(threads) as ex:
             list(ex.map(one, range(len(experts))))
+    return out
+
+
+def rvq_record_stride(H: int, F: int) -> int:
+    """Stride of a 3-bit residual-VQ record: 3 code bytes per 8 weights of
+    gate, up and down, rounded up to 4096 bytes."""
+    return (3 * (3 * F * H // 8) + 4095) // 4096 * 4096
+
+
+def rvq_expert_record(seed: int, layer: int, e: int, H: int, F: int, out: np.ndarray | None = None):
+    """One RVQ expert record (the shared expert uses e = E) as uint8[stride]:
+    uniform code bytes, zero padding."""
+    n, payload = rvq_record_stride(H, F), 3 * (3 * F * H // 8)
+    if out is None:
+        out = np.empty(n, np.uint8)
+    assert out.nbytes >= n and out.flags["C_CONTIGUOUS"]
+    lib().synth_fill_bytes(key(seed, TAG_RVQ_CODES, layer, e), out.ctypes.data, payload)
+    out[payload:n] = 0
+    return out
+
+
+def fill_rvq_records(seed: int, layer: int, experts, H: int, F: int, out: np.ndarray, threads=None):
+    """RVQ records of `experts` back to back into out (uint8, >= n*stride)."""
+    stride = rvq_record_stride(H, F)
+    experts = list(experts)
+    assert out.nbytes >= stride * len(experts)
+    flat = out.reshape(-1)
+
+    def one(i):
+        rvq_expert_record(seed, layer, experts[i], H, F, flat[i * stride:(i + 1) * stride])
+
+    threads = threads or min(32, os.cpu_count() or 1)
+    if len(experts) <= 1 or threads <= 1:
+        for i in range(len(experts)):
+            one(i)
+    else:
+        with ThreadPoolExecutor(threads) as ex:
+            list(ex.map(one, range(len(experts))))
+    return out
+
+
+def rvq_codebooks(seed: int, layer: int) -> np.ndarray:
+    """A layer's RVQ codebooks, bf16 bits uint16[3 kinds (gate, up, down)][3 stages][256][8]."""
+    out = np.empty((3, 3, 256, 8), np.uint16)
+    for kind in range(3):
+        for st in range(3):
+            lib().synth_fill_bf16_normal(key(seed, TAG_RVQ_CB, layer, kind, st), out[kind, st].ctypes.data,
+                                         256 * 8, 0.0, RVQ_STAGE_SD[st])
     return out
 
 

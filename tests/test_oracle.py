@@ -9,7 +9,8 @@ import pytest
 import torch
 
 import oracle
-from layers import (HostLayer, dense4, dense8, hidden_with_margin, identity_layer,
+from layers import (HostLayer, HostLayerRVQ, dense4, dense8, hidden_with_margin, identity_layer,
+                    identity_layer_rvq,
                     record_mats)
 from quantized_routed_expert_gemv_gb300 import synth
 
@@ -167,7 +168,7 @@ def test_router_logits_vs_numpy_dense():
 
 # ---- whole layer --------------------------------------------------------------------
 
-def _torch_layer(hl: HostLayer, x_bits):
+def _torch_layer(hl, x_bits):
     """The layer from library routines in float64: torch.matmul, F.silu,
     torch.softmax, torch.topk (stable ordering enforced by id tie-break)."""
     s = hl.shape
@@ -181,7 +182,7 @@ def _torch_layer(hl: HostLayer, x_bits):
     pr = pr / pr.sum()
 
     def ffn(rec, F):
-        Wg, Wu, Wd = (torch.tensor(m) for m in record_mats(rec, s.H, F))
+        Wg, Wu, Wd = (torch.tensor(m) for m in hl.mats(rec, F))
         return Wd @ (torch.nn.functional.silu(Wg @ xd) * (Wu @ xd))
 
     out = ffn(hl.shared, s.Fs) if s.Fs else torch.zeros(s.H, dtype=torch.float64)
@@ -230,6 +231,78 @@ def test_identity_expert_layer():
     scale = 1.0 + sum(p[i] * 2.0 ** -(int(ids[i]) % 3) for i in range(k))
     np.testing.assert_allclose(out, scale * x, rtol=1e-15, atol=0)
     assert abs(p.sum() - 1.0) < 1e-12
+
+
+# ---- 3-bit residual VQ ------------------------------------------------------------------
+
+def _rvq_golden():
+    cb = np.zeros((3, 256, 8), np.uint16)
+    rows, expect = {}, {}
+    for line in open(os.path.join(GOLDEN, "rvq_blocks.txt")):
+        f = line.split("|")[0].split()
+        if not f or f[0].startswith("#"):
+            continue
+        if f[0] == "cb":
+            cb[int(f[1]) - 1, int(f[2])] = [int(h, 16) for h in f[3:11]]
+        elif f[0] == "row":
+            rows[int(f[1])] = [int(v) for v in f[3:]]
+        elif f[0] == "expect":
+            expect[int(f[1])] = [float(v) for v in f[2:]]
+    codes = np.array([rows[r] for r in sorted(rows)], np.uint8)
+    W = np.array([expect[r] for r in sorted(expect)], np.float64)
+    return cb, codes, W
+
+
+def test_rvq_hand_blocks():
+    cb, codes, W = _rvq_golden()
+    rows, cols = W.shape
+    for r in range(rows):
+        for j in range(cols):
+            assert oracle.dequant_rvq(codes, cb, cols, r, j) == W[r, j], (r, j)
+    for j in range(cols):                                     # unit inputs pick columns
+        x = np.zeros(cols)
+        x[j] = 1.0
+        assert np.array_equal(oracle.gemv_rvq(codes, cb, rows, cols, x), W[:, j])
+    x = np.linspace(-1, 1, cols)
+    np.testing.assert_allclose(oracle.gemv_rvq(codes, cb, rows, cols, x), W @ x, rtol=1e-14)
+
+
+def test_rvq_layout():
+    for H, F in [(256, 128), (2048, 768), (7168, 2048), (64, 64)]:
+        L = oracle.rvq_layout(H, F)
+        assert L["up_codes"] == 3 * F * H // 8 and L["down_codes"] == 2 * L["up_codes"]
+        assert L["bytes"] == 9 * F * H // 8 and L["stride"] % 4096 == 0
+        assert L["stride"] == synth.rvq_record_stride(H, F)
+    # 3 bits per weight: three code bytes per 8 weights of each matrix
+    assert oracle.rvq_layout(7168, 2048)["bytes"] * 8 == 3 * 3 * 7168 * 2048
+
+
+def test_rvq_identity_layer():
+    records, shared, rc, rsb, cbs = identity_layer_rvq()
+    E, k, H = 8, 2, 64
+    lay = oracle.Layer(H, E, k, H, H, {e: records[e] for e in range(E)}, shared, rc, rsb,
+                       codebooks=cbs)
+    xs = synth.hidden(3, 0, 0, H)
+    xs[0] = synth.bf16_from_double(8.0)
+    out, ids, p = lay.token(xs)
+    x = synth.bf16_bits_to_float(xs).astype(np.float64)
+    scale = 1.0 + sum(p[i] * 2.0 ** -(int(ids[i]) % 3) for i in range(k))
+    np.testing.assert_allclose(out, scale * x, rtol=1e-15, atol=0)
+
+
+@pytest.mark.parametrize("shape", SMALL[:3], ids=lambda s: f"H{s.H}E{s.E}k{s.k}F{s.F}Fs{s.Fs}")
+def test_rvq_layer_vs_torch_float64(shape):
+    hl = HostLayerRVQ(shape, seed=2, beta=synth.beta_normal(2, 0, shape.E))
+    orc = hl.oracle()
+    for t in range(2):
+        x = synth.hidden(2, 99, t, shape.H)
+        out, ids, p = orc.token(x)
+        ref, rids, rp = _torch_layer(hl, x)
+        assert np.array_equal(ids, rids)
+        np.testing.assert_allclose(p, rp, rtol=1e-12)
+        assert np.abs(out - ref).max() <= 1e-12 * np.abs(ref).max()
+        dense, _, _ = orc.token(x, dense=True)
+        assert np.abs(out - dense).max() <= 1e-12 * np.abs(dense).max()
 
 
 def test_missing_selected_record_raises():
