@@ -58,6 +58,8 @@ def parse_args():
                         "router lookahead); needs ~51 GB of host RAM")
     p.add_argument("--streamed-only", action="store_true",
                    help="only the streamed-cache workload, one JSON object")
+    p.add_argument("--rvq-only", action="store_true",
+                   help="only the residual-VQ expert decode (large shape, B=1 and 4), one JSON object")
     a = p.parse_args()
     a.warmup = max(a.warmup, 3)
     return a
@@ -415,6 +417,12 @@ def run_ours(args, world, rank, local):
         if rank == 0:
             print(json.dumps({"prefill": res}), flush=True)
         return
+    if args.rvq_only:
+        stream = torch.cuda.Stream(device)
+        res = run_rvq(args, device, stream, _peaks().get("hbm_gbs", 6800.0))
+        if rank == 0:
+            print(json.dumps({"rvq": res}), flush=True)
+        return
     if args.streamed_only:
         stream = torch.cuda.Stream(device)
         res = run_streamed(args, device, stream, _peaks().get("hbm_gbs", 6800.0))
@@ -561,6 +569,7 @@ def run_ours(args, world, rank, local):
     dl.close()
     if not args.no_extras:
         out["prefill"] = run_prefill(args, device, stream, peak, peaks.get("bf16_tflops", 1900.0))
+        out["rvq"] = run_rvq(args, device, stream, peak)
     if args.streamed:
         out["streamed"] = run_streamed(args, device, stream, peak)
     if rank == 0:
@@ -793,6 +802,70 @@ def run_streamed(args, device, stream, hbm_peak):
     res["lookahead"] = {"inputs": f"hidden states chained across layers, rho={LOOKAHEAD_RHO}",
                         "n_ahead": LOOKAHEAD_N, "off": chained_off, "on": chained_on}
     return res
+
+
+def run_rvq(args, device, stream, hbm_peak):
+    """Decode on the large shape with 3-bit residual-VQ experts (WASTE page,
+    section "Quantization ve doğruluk"), B = 1 and 4, timed as replays of
+    CUDA graphs of GRAPH_STEPS consecutive steps like the main leg.
+    Algorithmic bytes per step: the code bytes of the distinct experts and
+    of the shared expert, the router, the codebooks once, the activations."""
+    import numpy as np
+    import torch
+
+    from quantized_routed_expert_gemv_gb300 import moe, synth
+    from quantized_routed_expert_gemv_gb300.device import DeviceLayer, bf16_tensor
+
+    wl = synth.WORKLOADS["large-decode"]
+    s = wl.shape
+    dl = DeviceLayer(s, wl.weight_seed, max_tokens=4, device=device, rvq=True)
+    rvq_bytes = lambda F: 3 * (3 * F * s.H // 8)
+    router = s.E * s.H + s.E * (s.H // 64) * 4
+    pool = max(GRAPH_STEPS, min(args.pool, 32))
+    K = 256
+    out = {"workload": f"large-decode with residual-VQ experts: H={s.H} E={s.E} top-{s.k} F={s.F} Fs={s.Fs}, "
+                       "3 code bytes per 8 weights, bf16 codebooks 3 x 3 x 256 x 8",
+           "gpu_launches_per_step": moe.lib().moe_decode_kernels(dl.handle, 1)}
+    for B in (1, 4):
+        xs = np.stack([np.stack([synth.hidden(wl.input_seed, 2000 + p, t, s.H) for t in range(B)])
+                       for p in range(pool)])
+        x = bf16_tensor(xs, device)
+        outs = dl.outputs(B)
+        distinct = []
+        with torch.cuda.stream(stream):
+            for p in range(pool):
+                dl.decode(x[p], outs, stream.cuda_stream)
+                stream.synchronize()
+                distinct.append(len(np.unique(outs[2].cpu().numpy())))
+        chunks = []
+        for c0 in range(0, pool - GRAPH_STEPS + 1, GRAPH_STEPS):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for p in range(c0, c0 + GRAPH_STEPS):
+                    dl.decode(x[p], outs, stream.cuda_stream)
+            chunks.append(g)
+        torch.cuda.synchronize()
+        for i in range(max(args.warmup, 3)):
+            chunks[i % len(chunks)].replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for i in range(K // GRAPH_STEPS):
+                chunks[i % len(chunks)].replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        assert dl.check(stream.cuda_stream) == moe.MOE_OK, moe.last_error()
+        ms = e0.elapsed_time(e1) / K
+        d = float(np.mean(distinct))
+        step_bytes = d * rvq_bytes(s.F) + rvq_bytes(s.Fs) + router + 3 * 3 * 256 * 8 * 2 + \
+            B * s.H * (2 + 2 + 4) + B * s.k * 8
+        gbs = step_bytes / (ms / 1e3) / 1e9
+        out[str(B)] = {"tokens_per_s": B / (ms / 1e3), "ms_per_step": ms, "distinct_experts": d,
+                       "bytes_per_step": step_bytes, "gbs": gbs, "frac_of_measured_hbm": gbs / hbm_peak}
+        del chunks
+    dl.close()
+    return out
 
 
 def cpu_baseline(wl, s, target_s=15.0):

@@ -62,8 +62,9 @@ enum {
 /* Shapes and quantisation of one layer.  Limits: hidden H in [64, 8192] and a
  * multiple of 64; n_experts E in [1, 1024]; top_k in [1, min(E, 32)]; ffn F
  * and shared_ffn Fs multiples of 64 in [64, 8192] (Fs = 0: no shared
- * expert); group must be 64, wbits 4, rbits 8; max_tokens in [1, 128] bounds
- * B for decode and T for prefill chunks. */
+ * expert); group must be 64; wbits 4 (affine experts, moe_record_layout) or
+ * 3 (residual-VQ experts, moe_rvq_record_layout_of); rbits 8; max_tokens in
+ * [1, 128] bounds B for decode and T for prefill chunks. */
 typedef struct moe_layer_desc {
     int32_t hidden;
     int32_t n_experts;
@@ -97,13 +98,20 @@ typedef struct moe_record_layout {
  *   shared_record:  one record with FFN width shared_ffn (NULL iff Fs == 0).
  *   router_codes:   uint8 [E][H], one 8-bit code per weight.
  *   router_sb:      uint32 [E][H/64] sb words as in moe_record_layout.
- *   router_logit_bias: float [E] added to the logits, or NULL for none. */
+ *   router_logit_bias: float [E] added to the logits, or NULL for none.
+ *   expert_codebooks: wbits = 3 only (NULL otherwise): bf16 [3][3][256][8],
+ *                   the layer's residual-VQ codebooks for gate, up and down,
+ *                   3 stages each, 256 codewords of 8 values (16-byte
+ *                   aligned).  WASTE page, section "Quantization ve
+ *                   doğruluk": each run of 8 weights along a row is the sum
+ *                   of one codeword per stage, named by 3 code bytes. */
 typedef struct moe_layer_weights {
     const void *expert_records;
     const void *shared_record;
     const uint8_t *router_codes;
     const uint32_t *router_sb;
     const float *router_logit_bias;
+    const uint16_t *expert_codebooks;
 } moe_layer_weights;
 
 typedef struct moe_layer moe_layer;
@@ -112,7 +120,16 @@ typedef struct moe_layer moe_layer;
  * Returns MOE_ERR_ARG for shapes outside the limits above. */
 int moe_record_layout_of(int32_t hidden, int32_t ffn, moe_record_layout *out);
 
-/* Stride in bytes of one expert record of width `ffn` (0 on bad shapes). */
+/* Record layout of a residual-VQ expert (wbits = 3): code bytes only,
+ *   [gate codes F x 3H/8][up codes F x 3H/8][down codes H x 3F/8]
+ * row-major; a row holds its blocks of 8 inputs in order, each block 3 bytes
+ * (the codeword index of stage 1, 2, 3).  The sb offsets equal `bytes` (no
+ * scale/bias words); `stride` is `bytes` rounded up to 4096.  Decode only:
+ * moe_prefill_chunk and the expert cache need wbits = 4. */
+int moe_rvq_record_layout_of(int32_t hidden, int32_t ffn, moe_record_layout *out);
+
+/* Stride in bytes of one expert record of width `ffn` in desc's format
+ * (0 on bad shapes). */
 size_t moe_expert_bytes(const moe_layer_desc *desc, int32_t ffn);
 
 /* Validates shapes and pointers, queries the device (must be sm_103) and

@@ -16,7 +16,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 SO = os.path.join(PKG, "libmoe.so")
-SOURCES = ["api.cu", "decode.cu", "decode_b1.cu", "prefill.cu", "residency.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "decode.cu", "decode_b1.cu", "prefill.cu", "residency.cu", "noalloc.cu", "rvq.cu"]
 HEADERS = ["common.cuh", "kernels.h", "tcgen05.cuh", "tma.cuh", "gemv.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", os.path.join(ROOT, "include")]

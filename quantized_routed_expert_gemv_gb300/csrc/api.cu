@@ -28,6 +28,9 @@ cudaError_t launch_prefill(const LayerArgs& a, const LayerMaps* maps, int num_sm
 cudaError_t build_layer_maps(const LayerArgs& a, LayerMaps* out);
 bool prefill_tc_ok(const LayerArgs& a, int T);
 size_t prefill_workspace_bytes(const LayerArgs& a, int T);
+size_t rvq_smem_need(const LayerArgs& a);
+cudaError_t set_rvq_attributes(int smem_optin);
+cudaError_t launch_decode_rvq(const LayerArgs& a, int num_sms, cudaStream_t st);
 }  // namespace moe
 
 using moe::LayerArgs;
@@ -81,15 +84,44 @@ static RecordOffsets offsets_of(int H, int F) {
   return o;
 }
 
+// 3-bit residual VQ (wbits = 3): code bytes only, 3 per 8 weights.
+static RecordOffsets rvq_offsets_of(int H, int F) {
+  RecordOffsets o;
+  const uint64_t mat = static_cast<uint64_t>(F) * static_cast<uint64_t>(H) / 8 * 3;
+  o.gate_codes = 0;
+  o.up_codes = mat;
+  o.down_codes = 2 * mat;
+  o.bytes = 3 * mat;
+  o.gate_sb = o.up_sb = o.down_sb = o.bytes;
+  o.stride = (o.bytes + 4095u) / 4096u * 4096u;
+  return o;
+}
+
+static RecordOffsets offsets_for(int wbits, int H, int F) {
+  return wbits == 3 ? rvq_offsets_of(H, F) : offsets_of(H, F);
+}
+
+static void copy_layout(const RecordOffsets& o, moe_record_layout* out) {
+  out->gate_codes = o.gate_codes, out->up_codes = o.up_codes, out->down_codes = o.down_codes;
+  out->gate_sb = o.gate_sb, out->up_sb = o.up_sb, out->down_sb = o.down_sb;
+  out->bytes = o.bytes, out->stride = o.stride;
+}
+
+extern "C" int moe_rvq_record_layout_of(int32_t hidden, int32_t ffn, moe_record_layout* out) {
+  if (!out) return fail(MOE_ERR_ARG, "moe_rvq_record_layout_of: out is NULL");
+  if (!dim_ok(hidden) || !dim_ok(ffn))
+    return fail(MOE_ERR_ARG, "moe_rvq_record_layout_of: hidden=%d ffn=%d must be multiples of 64 in [64, %d]",
+                hidden, ffn, moe::kMaxDim);
+  copy_layout(rvq_offsets_of(hidden, ffn), out);
+  return MOE_OK;
+}
+
 extern "C" int moe_record_layout_of(int32_t hidden, int32_t ffn, moe_record_layout* out) {
   if (!out) return fail(MOE_ERR_ARG, "moe_record_layout_of: out is NULL");
   if (!dim_ok(hidden) || !dim_ok(ffn))
     return fail(MOE_ERR_ARG, "moe_record_layout_of: hidden=%d ffn=%d must be multiples of 64 in [64, %d]",
                 hidden, ffn, moe::kMaxDim);
-  const RecordOffsets o = offsets_of(hidden, ffn);
-  out->gate_codes = o.gate_codes, out->up_codes = o.up_codes, out->down_codes = o.down_codes;
-  out->gate_sb = o.gate_sb, out->up_sb = o.up_sb, out->down_sb = o.down_sb;
-  out->bytes = o.bytes, out->stride = o.stride;
+  copy_layout(offsets_of(hidden, ffn), out);
   return MOE_OK;
 }
 
@@ -104,7 +136,8 @@ static int check_desc(const moe_layer_desc* d) {
   if (d->shared_ffn != 0 && !dim_ok(d->shared_ffn))
     return fail(MOE_ERR_ARG, "shared_ffn=%d: must be 0 or a multiple of 64 in [64, %d]", d->shared_ffn, moe::kMaxDim);
   if (d->group != 64) return fail(MOE_ERR_ARG, "group=%d: only 64 is supported", d->group);
-  if (d->wbits != 4) return fail(MOE_ERR_ARG, "wbits=%d: only 4 is supported", d->wbits);
+  if (d->wbits != 4 && d->wbits != 3)
+    return fail(MOE_ERR_ARG, "wbits=%d: 4 (affine, group 64) or 3 (residual VQ) are supported", d->wbits);
   if (d->rbits != 8) return fail(MOE_ERR_ARG, "rbits=%d: only 8 is supported", d->rbits);
   if (d->max_tokens < 1 || d->max_tokens > moe::kMaxTokens)
     return fail(MOE_ERR_ARG, "max_tokens=%d: must be in [1, %d]", d->max_tokens, moe::kMaxTokens);
@@ -113,7 +146,7 @@ static int check_desc(const moe_layer_desc* d) {
 
 extern "C" size_t moe_expert_bytes(const moe_layer_desc* desc, int32_t ffn) {
   if (!desc || !dim_ok(desc->hidden) || !dim_ok(ffn)) return 0;
-  return static_cast<size_t>(offsets_of(desc->hidden, ffn).stride);
+  return static_cast<size_t>(offsets_for(desc->wbits, desc->hidden, ffn).stride);
 }
 
 static LayerArgs base_args(const moe_layer* L) {
@@ -125,6 +158,7 @@ static LayerArgs base_args(const moe_layer* L) {
   a.rcodes = L->w.router_codes;
   a.rsb = L->w.router_sb;
   a.beta = L->w.router_logit_bias;
+  a.cbs = L->d.wbits == 3 ? L->w.expert_codebooks : nullptr;
   a.off_r = L->off_r, a.off_s = L->off_s;
   a.prof_on = L->prof_on;
   for (int i = 0; i < 4; ++i) a.prof[i] = L->prof_on ? static_cast<void*>(L->prof[i]) : nullptr;
@@ -145,6 +179,10 @@ extern "C" int moe_open(const moe_layer_desc* desc, const moe_layer_weights* w, 
     return fail(MOE_ERR_ALIGN, "moe_open: router pointers must be 16-byte aligned");
   if (!aligned(w->expert_records, 256) || !aligned(w->shared_record, 256))
     return fail(MOE_ERR_ALIGN, "moe_open: expert records must be 256-byte aligned");
+  if (desc->wbits == 3 && !w->expert_codebooks)
+    return fail(MOE_ERR_ARG, "moe_open: wbits=3 needs expert_codebooks");
+  if (!aligned(w->expert_codebooks, 16))
+    return fail(MOE_ERR_ALIGN, "moe_open: expert_codebooks must be 16-byte aligned");
 
   moe_layer* L = new (std::nothrow) moe_layer;
   if (!L) return fail(MOE_ERR_NOMEM, "moe_open: out of host memory");
@@ -153,8 +191,8 @@ extern "C" int moe_open(const moe_layer_desc* desc, const moe_layer_weights* w, 
   L->d = *desc;
   L->w = *w;
   const int H = desc->hidden, F = desc->ffn, Fs = desc->shared_ffn;
-  L->off_r = offsets_of(H, F);
-  L->off_s = Fs ? offsets_of(H, Fs) : RecordOffsets{};
+  L->off_r = offsets_for(desc->wbits, H, F);
+  L->off_s = Fs ? offsets_for(desc->wbits, H, Fs) : RecordOffsets{};
 
   cudaError_t e = cudaGetDevice(&L->device);
   if (e) {
@@ -174,18 +212,20 @@ extern "C" int moe_open(const moe_layer_desc* desc, const moe_layer_weights* w, 
                 dev, major, minor);
   }
   const LayerArgs a = base_args(L);
-  const size_t need = std::max(moe::decode_smem_need(a, L->num_sms), moe::prefill_smem_need(a, L->num_sms));
+  const bool rvq = desc->wbits == 3;
+  const size_t need = rvq ? moe::rvq_smem_need(a)
+                          : std::max(moe::decode_smem_need(a, L->num_sms), moe::prefill_smem_need(a, L->num_sms));
   if (need + 1024 > static_cast<size_t>(smem_optin)) {
     delete L;
     return fail(MOE_ERR_UNSUPPORTED, "moe_open: kernels need %zu B of shared memory, device allows %d",
                 need, smem_optin);
   }
   if ((e = moe::set_decode_attributes(smem_optin)) || (e = moe::set_b1_attributes(smem_optin)) ||
-      (e = moe::set_prefill_attributes(smem_optin))) {
+      (e = moe::set_prefill_attributes(smem_optin)) || (e = moe::set_rvq_attributes(smem_optin))) {
     delete L;
     return cuda_fail(e, "moe_open: cudaFuncSetAttribute");
   }
-  if ((e = moe::build_layer_maps(a, &L->maps))) {
+  if (!rvq && (e = moe::build_layer_maps(a, &L->maps))) {
     delete L;
     return cuda_fail(e, "moe_open: tensor maps of the code matrices");
   }
@@ -326,7 +366,11 @@ static int run(moe_layer* L, const uint16_t* x, int32_t T, uint16_t* ob, float* 
   if (rc || T == 0) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
-  if (path == Path::kPrefill) {
+  if (L->d.wbits == 3) {
+    // residual-VQ experts: their own decode kernels, any B; no chunked prefill
+    if (path == Path::kPrefill) return fail(MOE_ERR_ARG, "%s: prefill chunks need wbits=4 experts", name);
+    e = moe::launch_decode_rvq(a, L->num_sms, st);
+  } else if (path == Path::kPrefill) {
     e = moe::launch_prefill(a, &L->maps, L->num_sms, st);
   } else if (T == 1 && moe::plan_b1(a, L->num_sms, L->smem_optin)) {
     e = moe::launch_decode_b1(a, L->num_sms, st);
@@ -397,6 +441,7 @@ extern "C" int moe_decode_host(moe_layer* L, const uint16_t* x_host, int32_t B, 
 extern "C" int32_t moe_decode_kernels(const moe_layer* L, int32_t B) {
   if (!valid(L) || B < 0 || B > L->d.max_tokens) return -1;
   if (B == 0) return 0;
+  if (L->d.wbits == 3) return 3;  // router, gate|up, down + combine
   LayerArgs a = base_args(L);
   a.T = B;
   const int b1 = moe::plan_b1(a, L->num_sms, L->smem_optin) ? (a.f1_nst > 0 ? 2 : 3) : 0;

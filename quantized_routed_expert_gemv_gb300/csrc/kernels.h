@@ -91,6 +91,8 @@ struct LayerArgs {
   const uint8_t* rcodes;   // router codes [E][H]
   const uint32_t* rsb;     // router sb words [E][H/64]
   const float* beta;       // [E] or null
+  const uint16_t* cbs;     // 3-bit residual-VQ experts: codebooks [3 kinds][3 stages][256][8]
+                           // bf16 (kinds gate, up, down); null for 4-bit affine experts
   const int32_t* slot_of;  // [E] expert -> slot (residency) or null for identity
   const int32_t* slot_tag; // [n_slots] expert id held by each slot, or null
   int n_slots;             // slots of the pool when slot_of is set

@@ -182,6 +182,8 @@ extern "C" int moe_residency_open(moe_layer* layer, const void* host_records, in
   if (!d) return moe::report_error(MOE_ERR_ARG, "moe_residency_open: invalid layer handle");
   if (n_slots < 1 || n_slots > d->n_experts)
     return moe::report_error(MOE_ERR_ARG, "moe_residency_open: n_slots must be in [1, n_experts]");
+  if (d->wbits != 4)
+    return moe::report_error(MOE_ERR_ARG, "moe_residency_open: the expert cache needs a wbits=4 layer");
   if (n_slots < d->top_k)
     return moe::report_error(MOE_ERR_ARG, "moe_residency_open: fewer slots than top_k: a step could never fit");
   if (!host_records || !device_pool)

@@ -27,11 +27,17 @@ class DeviceLayer:
     def __init__(self, shape: synth.Shape, weight_seed: int, layer: int = 0, beta=None,
                  max_tokens: int = 16, device="cuda:0", chunk_records: int = 32,
                  host_records: np.ndarray | None = None, host_shared: np.ndarray | None = None,
-                 router=None, resident: bool = True):
+                 router=None, resident: bool = True, rvq: bool = False, codebooks=None):
+        """rvq: the experts are 3-bit residual-VQ records (wbits = 3) with the
+        layer's codebooks (synth.rvq_codebooks unless given)."""
         self.shape = s = shape
         self.device = torch.device(device)
         self.max_tokens = max_tokens
-        self.stride = synth.record_stride(s.H, s.F)
+        self.rvq = rvq
+        stride_of = synth.rvq_record_stride if rvq else synth.record_stride
+        fill = synth.fill_rvq_records if rvq else synth.fill_records
+        one = synth.rvq_expert_record if rvq else synth.expert_record
+        self.stride = stride_of(s.H, s.F)
         if resident:
             self.records = torch.empty(s.E * self.stride, dtype=torch.uint8, device=self.device)
             if host_records is not None:
@@ -42,14 +48,13 @@ class DeviceLayer:
                 view = pinned.numpy()
                 for e0 in range(0, s.E, n):
                     cnt = min(n, s.E - e0)
-                    synth.fill_records(weight_seed, layer, range(e0, e0 + cnt), s.H, s.F, view)
+                    fill(weight_seed, layer, range(e0, e0 + cnt), s.H, s.F, view)
                     self.records[e0 * self.stride:(e0 + cnt) * self.stride].copy_(
                         pinned[:cnt * self.stride])
         else:
             self.records = None
         if s.Fs:
-            sh = host_shared if host_shared is not None else synth.expert_record(
-                weight_seed, layer, s.E, s.H, s.Fs)
+            sh = host_shared if host_shared is not None else one(weight_seed, layer, s.E, s.H, s.Fs)
             self.shared = torch.from_numpy(np.ascontiguousarray(sh)).to(self.device)
         else:
             self.shared = None
@@ -58,12 +63,17 @@ class DeviceLayer:
         self.router_sb = torch.from_numpy(np.ascontiguousarray(rsb).view(np.int32)).to(self.device)
         self.beta = None if beta is None else torch.from_numpy(
             np.ascontiguousarray(beta, np.float32)).to(self.device)
-        self.desc = moe.desc(s.H, s.E, s.k, s.F, s.Fs, max_tokens=max_tokens)
+        self.codebooks = None
+        if rvq:
+            cb = codebooks if codebooks is not None else synth.rvq_codebooks(weight_seed, layer)
+            self.codebooks = torch.from_numpy(np.ascontiguousarray(cb, np.uint16).view(np.int16)).to(self.device)
+        self.desc = moe.desc(s.H, s.E, s.k, s.F, s.Fs, max_tokens=max_tokens, wbits=3 if rvq else 4)
         self.weights = moe.moe_layer_weights(
             self.records.data_ptr() if self.records is not None else None,
             self.shared.data_ptr() if self.shared is not None else None,
             self.router_codes.data_ptr(), self.router_sb.data_ptr(),
-            self.beta.data_ptr() if self.beta is not None else None)
+            self.beta.data_ptr() if self.beta is not None else None,
+            self.codebooks.data_ptr() if self.codebooks is not None else None)
         self.handle = moe.moe_open(self.desc, self.weights)
         self.ws_bytes = moe.moe_workspace_bytes(self.handle, max_tokens)
         self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=self.device)

@@ -40,7 +40,7 @@ class moe_record_layout(ctypes.Structure):
 class moe_layer_weights(ctypes.Structure):
     _fields_ = [("expert_records", ctypes.c_void_p), ("shared_record", ctypes.c_void_p),
                 ("router_codes", ctypes.c_void_p), ("router_sb", ctypes.c_void_p),
-                ("router_logit_bias", ctypes.c_void_p)]
+                ("router_logit_bias", ctypes.c_void_p), ("expert_codebooks", ctypes.c_void_p)]
 
 
 class moe_residency_stats_t(ctypes.Structure):
@@ -88,6 +88,7 @@ SIGNATURES = {
     "moe_residency_verify": (ctypes.c_int, [_vp, _vp]),
     "moe_crc32": (ctypes.c_uint32, [_vp, _sz]),
     "moe_residency_lookahead": (ctypes.c_int, [_vp, _vp, _i32, _i32, _vp, _vp, _vp, _sz, _vp, _vp]),
+    "moe_rvq_record_layout_of": (ctypes.c_int, [_i32, _i32, ctypes.POINTER(moe_record_layout)]),
 }
 
 

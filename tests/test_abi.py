@@ -48,6 +48,16 @@ def test_record_layout_matches_oracle(L, H, F):
     assert moe.moe_expert_bytes(d, F) == synth.record_stride(H, F)
 
 
+@pytest.mark.parametrize("H,F", [(256, 128), (2048, 768), (7168, 2048), (64, 64)])
+def test_rvq_record_layout_matches_oracle(L, H, F):
+    out = moe.moe_record_layout()
+    assert L.moe_rvq_record_layout_of(H, F, ctypes.byref(out)) == moe.MOE_OK
+    assert {n: int(getattr(out, n)) for n, _ in moe.moe_record_layout._fields_} == oracle.rvq_layout(H, F)
+    d = moe.desc(H, 8, 2, F, 0, wbits=3)
+    assert moe.moe_expert_bytes(d, F) == synth.rvq_record_stride(H, F)
+    assert L.moe_rvq_record_layout_of(H + 32, F, ctypes.byref(out)) == moe.MOE_ERR_ARG
+
+
 @pytest.mark.parametrize("H,F", [(0, 64), (96, 64), (64, 100), (8256, 64), (64, -64)])
 def test_record_layout_rejects_bad_shapes(L, H, F):
     out = moe.moe_record_layout()
@@ -64,7 +74,9 @@ def _weights(aligned=True):
 
 BAD_DESCS = [
     dict(hidden=100), dict(hidden=0), dict(n_experts=0), dict(n_experts=2000), dict(top_k=0),
-    dict(top_k=9), dict(ffn=65), dict(shared_ffn=10), dict(group=32), dict(wbits=3), dict(rbits=4),
+    dict(top_k=9), dict(ffn=65), dict(shared_ffn=10), dict(group=32), dict(wbits=5),
+    dict(wbits=3),  # residual-VQ experts without codebooks
+    dict(rbits=4),
     dict(max_tokens=0), dict(max_tokens=129),
 ]
 
