@@ -280,7 +280,13 @@ static size_t carve(const moe_layer* L, int T, moe::Workspace* ws, uint8_t* base
   const size_t o_xs = c.take(t * H * 2), o_obs = c.take(t * H * 2), o_ofs = c.take(t * H * 4);
   const size_t o_ids = c.take(t * k * 4), o_w = c.take(t * k * 4);
   LayerArgs a = base_args(L);
-  const size_t o_pf = c.take(moe::prefill_workspace_bytes(a, T));
+  // residual-VQ layers: per-slice partial sums of one token (slices of 256 inputs)
+  const bool rvq = L->d.wbits == 3;
+  const size_t Fm = std::max(F, Fs), slices_h = (H / 8 + 31) / 32, slices_f = (Fm / 8 + 31) / 32;
+  const size_t o_rg = c.take(rvq ? slices_h * (k + 1) * Fm * 4 : 0);
+  const size_t o_ru = c.take(rvq ? slices_h * (k + 1) * Fm * 4 : 0);
+  const size_t o_ry = c.take(rvq ? (k + 1) * slices_f * H * 4 : 0);
+  const size_t o_pf = c.take(rvq ? 0 : moe::prefill_workspace_bytes(a, T));
   if (ws && base) {
     ws->ctl = reinterpret_cast<unsigned*>(base + o_ctl);
     ws->hcnt = reinterpret_cast<unsigned*>(base + o_hcnt);
@@ -301,9 +307,12 @@ static size_t carve(const moe_layer* L, int T, moe::Workspace* ws, uint8_t* base
     ws->of_stage = reinterpret_cast<float*>(base + o_ofs);
     ws->ids_stage = reinterpret_cast<int32_t*>(base + o_ids);
     ws->w_stage = reinterpret_cast<float*>(base + o_w);
+    ws->rvq_g = rvq ? reinterpret_cast<float*>(base + o_rg) : nullptr;
+    ws->rvq_u = rvq ? reinterpret_cast<float*>(base + o_ru) : nullptr;
+    ws->rvq_y = rvq ? reinterpret_cast<float*>(base + o_ry) : nullptr;
   }
   if (prefill_off) *prefill_off = o_pf;
-  if (ws && base) ws->pf = moe::prefill_workspace_bytes(a, T) ? base + o_pf : nullptr;
+  if (ws && base) ws->pf = !rvq && moe::prefill_workspace_bytes(a, T) ? base + o_pf : nullptr;
   return c.off;
 }
 
@@ -441,7 +450,7 @@ extern "C" int moe_decode_host(moe_layer* L, const uint16_t* x_host, int32_t B, 
 extern "C" int32_t moe_decode_kernels(const moe_layer* L, int32_t B) {
   if (!valid(L) || B < 0 || B > L->d.max_tokens) return -1;
   if (B == 0) return 0;
-  if (L->d.wbits == 3) return 3;  // router, gate|up, down + combine
+  if (L->d.wbits == 3) return 1 + 4 * B;  // router; per token gate|up, SwiGLU, down, combine
   LayerArgs a = base_args(L);
   a.T = B;
   const int b1 = moe::plan_b1(a, L->num_sms, L->smem_optin) ? (a.f1_nst > 0 ? 2 : 3) : 0;

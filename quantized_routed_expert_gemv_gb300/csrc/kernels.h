@@ -55,6 +55,10 @@ struct Workspace {
   int32_t* ids_stage;    // [T][k]
   float* w_stage;        // [T][k]
   uint8_t* pf;           // prefill chunk scratch (tensor-core path), or null
+  float* rvq_g;          // residual-VQ layers, one token at a time: gate partial sums
+                         // [input slice][entry][max(F, Fs)]
+  float* rvq_u;          // up partial sums, same layout
+  float* rvq_y;          // down partial sums [entry][input slice of F][H]
 };
 
 // One token block of the prefill path: up to 64 tokens of one expert (or of
