@@ -37,7 +37,7 @@
 // use counted.  Ordering, whatever streams the caller gives:
 //   lookahead copies  after  the previous step's routed kernels (ev_done)
 //                            and the previous lookahead (ev_ahead);
-//   a step's copies   after  the previous lookahead (ev_ahead).
+//   a step's copies   after  the same two events.
 // Slot-table images are pinned buffers used in turn; one is rewritten only
 // after its previous upload has completed.
 //
@@ -380,9 +380,11 @@ extern "C" int moe_residency_decode(moe_residency* R, const uint16_t* x, int32_t
   for (int32_t ex : R->ahead_list) R->ahead[ex] = 0;  // a lookahead's pins end at this step
   R->ahead_list.clear();
 
-  // 3. misses: choose slots, copy records on the side stream (after the
-  // previous lookahead's copies, which may have used another stream)
-  if ((e = cudaStreamWaitEvent(C, R->ev_ahead, 0))) return moe::report_cuda(e, "moe_residency_decode: order after the lookahead");
+  // 3. misses: choose slots, copy records on the side stream, after the
+  // previous step's routed kernels and the previous lookahead's copies (both
+  // may have used other streams)
+  if ((e = cudaStreamWaitEvent(C, R->ev_done, 0)) || (e = cudaStreamWaitEvent(C, R->ev_ahead, 0)))
+    return moe::report_cuda(e, "moe_residency_decode: order the copies");
   const int fault = R->fault;
   bool fault_used = false;
   uint64_t hits = 0, misses = 0, evictions = 0, bytes = 0, ahead_hits = 0;
@@ -501,13 +503,16 @@ extern "C" int moe_residency_lookahead(moe_residency* R, const uint16_t* x, int3
       R->slot_expert[s] = -1;  // contents unknown: the slot holds nothing
       R->stats.lookaheads += 1, R->stats.lookahead_copies += copies;
       R->stats.evictions += evictions, R->stats.lookahead_bytes += bytes;
+      if (copies) cudaEventRecord(R->ev_ahead, C);  // the next step still orders after the copies issued
       return moe::report_cuda(e, "moe_residency_lookahead: record copy");
     }
     R->slot_expert[s] = ex, R->slot_of[ex] = s, R->fresh[ex] = 1;
     ++copies, bytes += R->rec_bytes;
   }
-  if (copies && ((e = upload_tables(R, C, -1)) || (e = cudaEventRecord(R->ev_ahead, C))))
+  if (copies && ((e = upload_tables(R, C, -1)) || (e = cudaEventRecord(R->ev_ahead, C)))) {
+    cudaEventRecord(R->ev_ahead, C);
     return moe::report_cuda(e, "moe_residency_lookahead: slot tables");
+  }
   R->stats.lookaheads += 1, R->stats.lookahead_copies += copies;
   R->stats.evictions += evictions, R->stats.lookahead_bytes += bytes;
   return MOE_OK;
