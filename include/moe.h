@@ -163,7 +163,8 @@ int moe_decode(moe_layer *layer, const uint16_t *x, int32_t B, uint16_t *out_bf1
 
 /* Prefill chunk of T tokens (1 <= T <= min(128, max_tokens)); same buffers and
  * semantics as moe_decode.  Expert work runs as a grouped GEMM on the 5th-gen
- * tensor cores (tcgen05, accumulators in tensor memory). */
+ * tensor cores (tcgen05, accumulators in tensor memory).  MOE_ERR_ARG on a
+ * wbits = 3 layer. */
 int moe_prefill_chunk(moe_layer *layer, const uint16_t *x, int32_t T, uint16_t *out_bf16,
                       float *out_f32, int32_t *ids, float *weights, void *workspace,
                       size_t workspace_bytes, void *stream);
@@ -188,8 +189,9 @@ int moe_check(const moe_layer *layer, void *workspace, void *stream);
  * 2 for one token on the fused single-token kernel (router, fused gate|up +
  * down), 3 where the single-token kernels are not fused, B times that for
  * batches run one token at a time, 5 for the tensor-core chunk kernels and 3
- * for the grouped kernels.  0 for B = 0; -1 on a bad handle or B outside
- * [0, max_tokens].  Host-only: no device work. */
+ * for the grouped kernels; 1 + 4B on a wbits = 3 layer (the router, then
+ * gate|up, SwiGLU, down and combine per token).  0 for B = 0; -1 on a bad
+ * handle or B outside [0, max_tokens].  Host-only: no device work. */
 int32_t moe_decode_kernels(const moe_layer *layer, int32_t B);
 
 /* Profiling hook.  With `events` pointing to four cudaEvent_t (passed as
@@ -253,7 +255,8 @@ size_t moe_residency_pool_bytes(const moe_layer *layer, int32_t n_slots);
  * storage, owned by the caller, written only by this cache.  n_slots in
  * [top_k, n_experts].  Allocates small pinned host buffers and a few
  * events, freed by moe_residency_close.  The layer may have been opened with
- * expert_records = NULL. */
+ * expert_records = NULL; it must hold wbits = 4 experts (MOE_ERR_ARG
+ * otherwise). */
 int moe_residency_open(moe_layer *layer, const void *host_records, int32_t n_slots,
                        void *device_pool, size_t device_pool_bytes, moe_residency **out);
 
