@@ -63,3 +63,28 @@ def test_reference_arm_under_torchrun_prints_once():
     assert rec["impl"] == "reference" and rec["unit"] == "tokens/s" and rec["value"] > 0
     assert rec["cpu_baseline"]["kind"] == "oracle"
     assert rec["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_streamed_replay_counts_and_verdict():
+    """The stored oracle replay of the streamed workload parses into every
+    run and layer, holds the policy's identities, and the verdict names the
+    first counter that differs."""
+    sys.path.insert(0, ROOT)
+    import bench
+    exp = bench.streamed_expected()
+    assert set(exp) == {"independent", "chained_off", "chained_on"}
+    for run, rows in exp.items():
+        assert len(rows) == 4
+        for l, (hits, misses, evictions, la_copies, la_hits) in enumerate(rows):
+            assert hits + misses == 256 * 16                    # 256 one-token steps, top-16
+            assert la_hits <= la_copies
+            if run != "chained_on" or l == 0:                   # no lookahead: misses fill
+                assert la_copies == 0                           # 64 empty slots, then evict
+                assert evictions == misses - 64
+    assert exp["independent"][0] == exp["chained_off"][0] == exp["chained_on"][0]  # layer 0 alike
+    st = [dict(zip(bench.COUNT_KEYS, r)) for r in exp["chained_on"]]
+    assert bench.replay_verdict(exp["chained_on"], st) == "equal"
+    st[2]["lookahead_hits"] += 1
+    v = bench.replay_verdict(exp["chained_on"], st)
+    assert v.startswith("differs") and "layer 2 lookahead_hits" in v
+    assert bench.replay_verdict(None, st) == "no stored replay"
