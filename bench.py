@@ -684,7 +684,7 @@ def streamed_expected() -> dict:
     return out
 
 
-def replay_verdict(expected, st) -> str:
+def replay_match(expected, st) -> str:
     """'equal' when every layer's counters equal the oracle's replay."""
     if not expected:
         return "no stored replay"
@@ -778,7 +778,7 @@ def run_streamed(args, device, stream, hbm_peak):
         h2d = tot("bytes_h2d") + tot("lookahead_bytes")
         bound_s = max(hbm_bytes / (hbm_peak * 1e9), h2d / (bw * 1e9))
         later = range(1, nl)
-        return {"oracle_replay": replay_verdict(expected.get(run_name), st),
+        return {"oracle_replay": replay_match(expected.get(run_name), st),
                 "tokens_per_s": steps / (ms / 1e3), "ms_per_token": ms / steps, "wall_s": wall,
                 "hit_rate": hits / max(1, hits + misses), "hits": hits, "misses": misses,
                 "hit_rate_layers_1_on": tot("hits", later) / max(1, tot("hits", later) + tot("misses", later)),

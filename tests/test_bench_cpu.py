@@ -65,9 +65,9 @@ def test_reference_arm_under_torchrun_prints_once():
     assert rec["e2e"]["h2d_bytes_per_step"] == 0
 
 
-def test_streamed_replay_counts_and_verdict():
+def test_streamed_replay_counts_and_comparison():
     """The stored oracle replay of the streamed workload parses into every
-    run and layer, holds the policy's identities, and the verdict names the
+    run and layer, holds the policy's identities, and the comparison names the
     first counter that differs."""
     sys.path.insert(0, ROOT)
     import bench
@@ -83,8 +83,8 @@ def test_streamed_replay_counts_and_verdict():
                 assert evictions == misses - 64
     assert exp["independent"][0] == exp["chained_off"][0] == exp["chained_on"][0]  # layer 0 alike
     st = [dict(zip(bench.COUNT_KEYS, r)) for r in exp["chained_on"]]
-    assert bench.replay_verdict(exp["chained_on"], st) == "equal"
+    assert bench.replay_match(exp["chained_on"], st) == "equal"
     st[2]["lookahead_hits"] += 1
-    v = bench.replay_verdict(exp["chained_on"], st)
+    v = bench.replay_match(exp["chained_on"], st)
     assert v.startswith("differs") and "layer 2 lookahead_hits" in v
-    assert bench.replay_verdict(None, st) == "no stored replay"
+    assert bench.replay_match(None, st) == "no stored replay"
