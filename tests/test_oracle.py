@@ -477,6 +477,25 @@ def test_synth_hidden_chain():
         assert abs(np.corrcoef(xs[l - 1], xs[l])[0, 1] - 0.9) < 0.02
 
 
+def test_synth_rvq_records_and_codebooks():
+    H, F = 256, 128
+    stride = synth.rvq_record_stride(H, F)
+    buf = np.zeros((3, stride), np.uint8)
+    synth.fill_rvq_records(11, 2, [5, 0, 7], H, F, buf)
+    assert np.array_equal(buf[2], synth.rvq_expert_record(11, 2, 7, H, F))   # random access
+    assert not np.array_equal(buf[0], buf[1])
+    payload = oracle.rvq_layout(H, F)["bytes"]
+    assert not buf[0, payload:].any()                                        # zero padding
+    counts = np.bincount(buf[0, :payload], minlength=256)
+    assert counts.min() > 0.6 * payload / 256                                # uniform codes
+    cb = synth.rvq_codebooks(11, 2)
+    assert cb.shape == (3, 3, 256, 8) and np.array_equal(cb, synth.rvq_codebooks(11, 2))
+    w = synth.bf16_bits_to_float(cb).astype(np.float64)
+    for st, sd in enumerate(synth.RVQ_STAGE_SD):
+        assert abs(w[:, st].std() - sd) < 0.1 * sd and abs(w[:, st].mean()) < 0.1 * sd
+    assert not np.array_equal(cb[0], cb[1]) and not np.array_equal(cb, synth.rvq_codebooks(11, 3))
+
+
 def test_synth_random_access_and_distributions():
     H, F = 256, 128
     buf = np.zeros((3, synth.record_stride(H, F)), np.uint8)
