@@ -15,6 +15,7 @@ and "Önceden okuma ve router tahmini" (router lookahead into the cache).
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import subprocess
@@ -26,12 +27,14 @@ _SO = os.path.join(_HERE, "liboracle.so")
 _SRC = os.path.join(_HERE, "oracle.c")
 
 
+GCC_FLAGS = ["-O2", "-std=c99", "-ffp-contract=off", "-fPIC", "-shared"]
+
+
 def build(force: bool = False) -> str:
     """Compile oracle.c into liboracle.so beside it (gcc, no FMA contraction)."""
     if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(_SRC):
         tmp = _SO + ".tmp"
-        subprocess.check_call(["gcc", "-O2", "-std=c99", "-ffp-contract=off", "-fPIC",
-                               "-shared", _SRC, "-o", tmp, "-lm"])
+        subprocess.check_call(["gcc", *GCC_FLAGS, _SRC, "-o", tmp, "-lm"])
         os.replace(tmp, _SO)
     return _SO
 
@@ -59,37 +62,54 @@ _lib = None
 def lib():
     global _lib
     if _lib is None:
-        _lib = ctypes.CDLL(build())
-        L = _lib
-        vp, i32, d = ctypes.c_void_p, ctypes.c_int, ctypes.c_double
-        L.orc_bf16_to_double.argtypes = [ctypes.c_uint16]
-        L.orc_bf16_to_double.restype = d
-        L.orc_record_layout.argtypes = [i32, i32, ctypes.POINTER(_Layout)]
-        L.orc_dequant4.argtypes = [vp, vp, i32, i32, i32]
-        L.orc_dequant4.restype = d
-        L.orc_dequant8.argtypes = [vp, vp, i32, i32, i32]
-        L.orc_dequant8.restype = d
-        L.orc_gemv4.argtypes = [vp, vp, i32, i32, vp, vp]
-        L.orc_router_logits.argtypes = [vp, vp, vp, i32, i32, vp, vp]
-        L.orc_topk.argtypes = [vp, i32, i32, vp, vp, vp]
-        L.orc_silu.argtypes = [d]
-        L.orc_silu.restype = d
-        L.orc_expert.argtypes = [vp, i32, i32, vp, vp, vp]
-        L.orc_route.argtypes = [ctypes.POINTER(_Layer), vp, vp, vp, vp, vp, vp]
-        L.orc_moe_token.argtypes = [ctypes.POINTER(_Layer), vp, vp, vp, vp, vp, vp]
-        L.orc_moe_token.restype = i32
-        L.orc_moe_token_dense.argtypes = [ctypes.POINTER(_Layer), vp, vp, vp, vp, vp, vp]
-        L.orc_moe_token_dense.restype = i32
-        L.orc_lfu_step.argtypes = [i32, i32, vp, vp, vp, vp, i32, ctypes.c_int64, vp, vp]
-        L.orc_lfu_step.restype = i32
-        L.orc_lfu_lookahead.argtypes = [i32, i32, vp, vp, vp, vp, vp, vp, i32, vp, vp]
-        L.orc_lfu_lookahead.restype = i32
-        L.orc_rvq_layout.argtypes = [i32, i32, ctypes.POINTER(_Layout)]
-        L.orc_dequant_rvq.argtypes = [vp, vp, i32, i32, i32]
-        L.orc_dequant_rvq.restype = d
-        L.orc_gemv_rvq.argtypes = [vp, vp, i32, i32, vp, vp]
-        L.orc_expert_rvq.argtypes = [vp, vp, i32, i32, vp, vp, vp]
+        _lib = _bind(ctypes.CDLL(build()))
     return _lib
+
+
+@contextlib.contextmanager
+def using_library(path: str):
+    """Binds this wrapper to another build of oracle.c for the duration (the
+    tests use it to run the pins against copies with a planted mistake)."""
+    global _lib
+    saved = lib()
+    _lib = _bind(ctypes.CDLL(path))
+    try:
+        yield
+    finally:
+        _lib = saved
+
+
+def _bind(L):
+    """Declares the argument and result types of the oracle's C functions."""
+    vp, i32, d = ctypes.c_void_p, ctypes.c_int, ctypes.c_double
+    L.orc_bf16_to_double.argtypes = [ctypes.c_uint16]
+    L.orc_bf16_to_double.restype = d
+    L.orc_record_layout.argtypes = [i32, i32, ctypes.POINTER(_Layout)]
+    L.orc_dequant4.argtypes = [vp, vp, i32, i32, i32]
+    L.orc_dequant4.restype = d
+    L.orc_dequant8.argtypes = [vp, vp, i32, i32, i32]
+    L.orc_dequant8.restype = d
+    L.orc_gemv4.argtypes = [vp, vp, i32, i32, vp, vp]
+    L.orc_router_logits.argtypes = [vp, vp, vp, i32, i32, vp, vp]
+    L.orc_topk.argtypes = [vp, i32, i32, vp, vp, vp]
+    L.orc_silu.argtypes = [d]
+    L.orc_silu.restype = d
+    L.orc_expert.argtypes = [vp, i32, i32, vp, vp, vp]
+    L.orc_route.argtypes = [ctypes.POINTER(_Layer), vp, vp, vp, vp, vp, vp]
+    L.orc_moe_token.argtypes = [ctypes.POINTER(_Layer), vp, vp, vp, vp, vp, vp]
+    L.orc_moe_token.restype = i32
+    L.orc_moe_token_dense.argtypes = [ctypes.POINTER(_Layer), vp, vp, vp, vp, vp, vp]
+    L.orc_moe_token_dense.restype = i32
+    L.orc_lfu_step.argtypes = [i32, i32, vp, vp, vp, vp, i32, ctypes.c_int64, vp, vp]
+    L.orc_lfu_step.restype = i32
+    L.orc_lfu_lookahead.argtypes = [i32, i32, vp, vp, vp, vp, vp, vp, i32, vp, vp]
+    L.orc_lfu_lookahead.restype = i32
+    L.orc_rvq_layout.argtypes = [i32, i32, ctypes.POINTER(_Layout)]
+    L.orc_dequant_rvq.argtypes = [vp, vp, i32, i32, i32]
+    L.orc_dequant_rvq.restype = d
+    L.orc_gemv_rvq.argtypes = [vp, vp, i32, i32, vp, vp]
+    L.orc_expert_rvq.argtypes = [vp, vp, i32, i32, vp, vp, vp]
+    return L
 
 
 def _p(a: np.ndarray):
