@@ -18,6 +18,7 @@ import test_oracle as pins
 from quantized_routed_expert_gemv_gb300 import synth
 
 HAND4 = [b for b in pins._golden_blocks() if b["bits"] == 4][0]
+HAND8 = [b for b in pins._golden_blocks() if b["bits"] == 8][0]
 
 # (name, text in oracle.c, replacement, pins that must notice: (function, args))
 MUTANTS = [
@@ -29,6 +30,10 @@ MUTANTS = [
      "    return s * (double)q + b;\n}\n\n/* Weight (r, j) of the 8-bit router",
      "    return s * (double)q - b;\n}\n\n/* Weight (r, j) of the 8-bit router",
      [(pins.test_dequant_hand_blocks, (HAND4,)), (pins.test_gemv_bias_term, ())]),
+    ("router (8-bit) bias dropped",
+     "    return s * (double)q + b;\n}\n\n/* y[r] = sum_j",
+     "    return s * (double)q;\n}\n\n/* y[r] = sum_j",
+     [(pins.test_dequant_hand_blocks, (HAND8,)), (pins.test_router_logits_vs_numpy_dense, ())]),
     ("GEMV input reversed",
      "acc += orc_dequant4(codes, sb, cols, r, j) * x[j];",
      "acc += orc_dequant4(codes, sb, cols, r, j) * x[cols - 1 - j];",
@@ -63,6 +68,10 @@ MUTANTS = [
      "cb[((size_t)s * 256 + blk[s]) * 8 + (size_t)(j % 8)]",
      "cb[((size_t)(2 - s) * 256 + blk[s]) * 8 + (size_t)(j % 8)]",
      [(pins.test_rvq_hand_blocks, ())]),
+    ("residual-VQ block taken from the element index",
+     "(size_t)(j / 8) * 3;",
+     "(size_t)(j % 8 % (cols / 8)) * 3;",
+     [(pins.test_rvq_hand_blocks, ())]),
     ("residual-VQ elements of a codeword reversed",
      "cb[((size_t)s * 256 + blk[s]) * 8 + (size_t)(j % 8)]",
      "cb[((size_t)s * 256 + blk[s]) * 8 + (size_t)(7 - j % 8)]",
@@ -70,6 +79,10 @@ MUTANTS = [
     ("LFU ties go to the higher id",
      "(last_use[e] == last_use[v] && e < v))))",
      "(last_use[e] == last_use[v] && e > v))))",
+     [(pins.test_lfu_hand_trace, ())]),
+    ("LFU counts not cumulative",
+     "        count[ids[i]] += 1;",
+     "        count[ids[i]] = 1;",
      [(pins.test_lfu_hand_trace, ())]),
     ("LFU ignores recency",
      "(count[e] == count[v] &&\n                     (last_use[e] < last_use[v] ||",
