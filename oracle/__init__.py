@@ -10,8 +10,9 @@ C, fp64).  See ``oracle.c`` for the formulas and the pages each one follows:
 the TurboFieldfare page, sections "Belleği azaltan çalışma yapısı" (affine
 4-bit group-64 experts, 8-bit router) and "Token üretim süreci" (router,
 top-k, bounded LFU cache, shared expert, combine), and the WASTE page,
-sections "Disk streaming mimarisi" (gate, up and down stored contiguously)
-and "Önceden okuma ve router tahmini" (router lookahead into the cache).
+sections "Disk streaming mimarisi" (gate, up and down stored contiguously),
+"Önceden okuma ve router tahmini" (router lookahead into the cache) and
+"Quantization ve doğruluk" (3-bit residual-VQ experts).
 """
 from __future__ import annotations
 
