@@ -171,7 +171,11 @@ int moe_prefill_chunk(moe_layer *layer, const uint16_t *x, int32_t T, uint16_t *
 
 /* moe_decode with HOST buffers: copies x in, runs the step, copies every
  * output back (out_f32_host may be NULL) and synchronises `stream` before it
- * returns.  Device staging lives in the workspace. */
+ * returns.  Device staging lives in the workspace; the outputs come back in
+ * one device-to-host copy into a page-locked host buffer of the layer
+ * (allocated by the layer's first moe_decode_host call, sized for
+ * max_tokens, freed by moe_close), then are copied to the caller's buffers.
+ * Calls on one layer from several threads are serialised by a lock. */
 int moe_decode_host(moe_layer *layer, const uint16_t *x_host, int32_t B,
                     uint16_t *out_bf16_host, float *out_f32_host, int32_t *ids_host,
                     float *weights_host, void *workspace, size_t workspace_bytes,
@@ -351,10 +355,11 @@ void moe_residency_close(moe_residency *res);
  * library, one per device.  The call itself allocates nothing.
  *
  * Limit: moe_workspace_bytes(layer, B) must be <= MOE_NOALLOC_SCRATCH_BYTES
- * (4 MiB: e.g. H=7168, E=512, top-16, F=Fs=2048 up to B=16); a larger B is
- * rejected with MOE_ERR_ARG before anything is launched, and moe_last_error()
- * says to use moe_decode with a caller-allocated workspace.  The layer's
- * device must be the current device (MOE_ERR_ARG otherwise).
+ * (4 MiB: for H=7168, E=512, top-16, F=Fs=2048 that is B <= 18); a larger B
+ * is rejected with MOE_ERR_ARG before anything is launched, and
+ * moe_last_error() says to use moe_decode with a caller-allocated
+ * workspace.  The layer's device must be the current device (MOE_ERR_ARG
+ * otherwise).
  *
  * First call per device: looks up the scratch's device address once (with
  * that device current) and zeroes the whole scratch on `stream`, ordered
@@ -362,20 +367,31 @@ void moe_residency_close(moe_residency *res);
  * completion counter, item claim counters, per-expert and per-row-tile
  * completion counters) must start at zero; every later step leaves them
  * ready for the next one.  Make this first call before any stream capture
- * begins.
+ * begins.  The looked-up address is kept for the life of the process: do not
+ * use this entry point on a device after cudaDeviceReset() of that device.
  *
  * All calls on one device share the one scratch: calls whose executions
  * overlap (different streams, different threads or different layers without
  * an ordering between them) race on it and give undefined results.  Issue
  * them on one stream, or order them with events.  Errors that device code
- * latches (a bounded wait that ran out) stay in the private scratch, which
- * moe_check cannot read; use moe_decode with an own workspace where that
- * status is needed.
+ * latches (a bounded wait that ran out) stay in the scratch until
+ * moe_check_noalloc reads and clears them.
  *
  * Pointers, alignment, sizes and return codes otherwise as moe_decode. */
 #define MOE_NOALLOC_SCRATCH_BYTES (4u << 20)
 int moe_decode_noalloc(moe_layer *layer, const uint16_t *x, int32_t B, uint16_t *out_bf16,
                        float *out_f32, int32_t *ids, float *weights, void *stream);
+
+/* moe_check for the static scratch of moe_decode_noalloc on the layer's
+ * device (which must be current): synchronises `stream`, reads the error
+ * word and returns MOE_OK, MOE_ERR_TIMEOUT, MOE_ERR_RESIDENCY or MOE_ERR_ARG
+ * as moe_check does; after an error it zeroes the scratch's persistent
+ * control block (error word, claim and completion counters that a step that
+ * gave up may leave mid-count), so later no-alloc steps start clean.
+ * MOE_OK when no no-alloc step has run on the device yet.  Allocates
+ * nothing; it synchronises, so it must not be called during stream
+ * capture.  The pages have no counterpart. */
+int moe_check_noalloc(const moe_layer *layer, void *stream);
 
 #ifdef __cplusplus
 }

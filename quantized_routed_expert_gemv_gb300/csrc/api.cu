@@ -7,6 +7,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
 
 #include <cuda_runtime.h>
@@ -61,6 +62,11 @@ struct moe_layer {
   cudaEvent_t prof[4];
   int prof_on;
   moe::LayerMaps maps;  // tiled-load descriptors of the code matrices (prefill)
+  // moe_decode_host: page-locked host buffer that the step's outputs land in
+  // with one copy (allocated by the first call, freed by moe_close)
+  std::mutex* host_mu;
+  uint8_t* host_out;
+  size_t host_out_bytes;
 };
 
 static bool aligned(const void* p, size_t a) {
@@ -229,6 +235,11 @@ extern "C" int moe_open(const moe_layer_desc* desc, const moe_layer_weights* w, 
     delete L;
     return cuda_fail(e, "moe_open: tensor maps of the code matrices");
   }
+  L->host_mu = new (std::nothrow) std::mutex;
+  if (!L->host_mu) {
+    delete L;
+    return fail(MOE_ERR_NOMEM, "moe_open: out of host memory");
+  }
   *out = L;
   return MOE_OK;
 }
@@ -236,6 +247,8 @@ extern "C" int moe_open(const moe_layer_desc* desc, const moe_layer_weights* w, 
 extern "C" void moe_close(moe_layer* L) {
   if (L && L->magic == kMagic) {
     L->magic = 0;
+    if (L->host_out) cudaFreeHost(L->host_out);
+    delete L->host_mu;
     delete L;
   }
 }
@@ -277,8 +290,10 @@ static size_t carve(const moe_layer* L, int T, moe::Workspace* ws, uint8_t* base
   const size_t o_ae = c.take(E * 4), o_ao = c.take(E * 4), o_ac = c.take(E * 4);
   const size_t o_pt = c.take(t * k * 4), o_ps = c.take(t * k * 4);
   const size_t o_h = c.take(t * k * F * 4), o_hs = c.take(t * Fs * 4);
-  const size_t o_xs = c.take(t * H * 2), o_obs = c.take(t * H * 2), o_ofs = c.take(t * H * 4);
-  const size_t o_ids = c.take(t * k * 4), o_w = c.take(t * k * 4);
+  // host-entry staging: the outputs back to back (bf16, ids, weights, then
+  // f32), so one device-to-host copy returns all of them
+  const size_t o_xs = c.take(t * H * 2), o_obs = c.take(t * H * 2);
+  const size_t o_ids = c.take(t * k * 4), o_w = c.take(t * k * 4), o_ofs = c.take(t * H * 4);
   LayerArgs a = base_args(L);
   // residual-VQ layers: per-slice partial sums of one token (slices of 256 inputs)
   const bool rvq = L->d.wbits == 3;
@@ -433,17 +448,41 @@ extern "C" int moe_decode_host(moe_layer* L, const uint16_t* x_host, int32_t B, 
   if (ws_bytes < need) return fail(MOE_ERR_ARG, "moe_decode_host: workspace too small (%zu < %zu)", ws_bytes, need);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const size_t H = L->d.hidden, k = L->d.top_k, b = static_cast<size_t>(B);
+  // The staging area holds bf16 out, ids, weights and f32 out back to back:
+  // one copy of [ob_stage, end) brings every requested output to the
+  // layer's page-locked buffer, from which they are handed out.
+  uint8_t* const s0 = reinterpret_cast<uint8_t*>(w.ob_stage);
+  const size_t o_ids = reinterpret_cast<uint8_t*>(w.ids_stage) - s0;
+  const size_t o_w = reinterpret_cast<uint8_t*>(w.w_stage) - s0;
+  const size_t o_f = reinterpret_cast<uint8_t*>(w.of_stage) - s0;
+  const size_t span = of_host ? o_f + b * H * 4 : o_w + b * k * 4;
+  std::lock_guard<std::mutex> lock(*L->host_mu);
+  if (L->host_out_bytes < span) {
+    // sized for the largest call of the layer once, so later calls reuse it
+    moe::Workspace wm;
+    carve(L, L->d.max_tokens, &wm, static_cast<uint8_t*>(ws), nullptr);
+    const size_t full = static_cast<size_t>(reinterpret_cast<uint8_t*>(wm.of_stage) -
+                                            reinterpret_cast<uint8_t*>(wm.ob_stage)) +
+                        static_cast<size_t>(L->d.max_tokens) * H * 4;
+    const size_t cap = std::max(span, full);
+    if (L->host_out) cudaFreeHost(L->host_out), L->host_out = nullptr, L->host_out_bytes = 0;
+    void* p = nullptr;
+    cudaError_t e = cudaHostAlloc(&p, cap, cudaHostAllocDefault);
+    if (e) return cuda_fail(e, "moe_decode_host: page-locked output buffer");
+    L->host_out = static_cast<uint8_t*>(p), L->host_out_bytes = cap;
+  }
   cudaError_t e = cudaMemcpyAsync(w.x_stage, x_host, b * H * 2, cudaMemcpyHostToDevice, st);
   if (e) return cuda_fail(e, "moe_decode_host: copy in");
   int rc = moe_decode(L, w.x_stage, B, w.ob_stage, of_host ? w.of_stage : nullptr, w.ids_stage, w.w_stage,
                       ws, ws_bytes, stream);
   if (rc) return rc;
-  if ((e = cudaMemcpyAsync(ob_host, w.ob_stage, b * H * 2, cudaMemcpyDeviceToHost, st)) ||
-      (of_host && (e = cudaMemcpyAsync(of_host, w.of_stage, b * H * 4, cudaMemcpyDeviceToHost, st))) ||
-      (e = cudaMemcpyAsync(ids_host, w.ids_stage, b * k * 4, cudaMemcpyDeviceToHost, st)) ||
-      (e = cudaMemcpyAsync(w_host, w.w_stage, b * k * 4, cudaMemcpyDeviceToHost, st)))
+  if ((e = cudaMemcpyAsync(L->host_out, s0, span, cudaMemcpyDeviceToHost, st)))
     return cuda_fail(e, "moe_decode_host: copy out");
   if ((e = cudaStreamSynchronize(st))) return cuda_fail(e, "moe_decode_host: synchronize");
+  std::memcpy(ob_host, L->host_out, b * H * 2);
+  std::memcpy(ids_host, L->host_out + o_ids, b * k * 4);
+  std::memcpy(w_host, L->host_out + o_w, b * k * 4);
+  if (of_host) std::memcpy(of_host, L->host_out + o_f, b * H * 4);
   return MOE_OK;
 }
 
@@ -460,21 +499,26 @@ extern "C" int32_t moe_decode_kernels(const moe_layer* L, int32_t B) {
   return 3;
 }
 
-extern "C" int moe_check(const moe_layer* L, void* ws, void* stream) {
-  if (!valid(L)) return fail(MOE_ERR_ARG, "moe_check: invalid layer handle");
-  if (!ws) return fail(MOE_ERR_ARG, "moe_check: workspace is NULL");
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
+// Reads the error word that device code latches at the start of workspace
+// `ws` after synchronising `st`; after an error, zeroes the persistent block.
+static int check_workspace(void* ws, cudaStream_t st, const char* name) {
   cudaError_t e = cudaStreamSynchronize(st);
-  if (e) return cuda_fail(e, "moe_check: synchronize");
+  if (e) return cuda_fail(e, name);
   unsigned bits = 0;
-  if ((e = cudaMemcpy(&bits, ws, 4, cudaMemcpyDeviceToHost))) return cuda_fail(e, "moe_check: read error word");
+  if ((e = cudaMemcpy(&bits, ws, 4, cudaMemcpyDeviceToHost))) return cuda_fail(e, name);
   if (bits == 0) return MOE_OK;
   // a step that gave up may leave claim and completion counters mid-count:
   // the whole persistent block goes back to zero with the error word
-  if ((e = cudaMemset(ws, 0, kPersistentBytes))) return cuda_fail(e, "moe_check: clear control block");
+  if ((e = cudaMemset(ws, 0, kPersistentBytes))) return cuda_fail(e, name);
   if (bits & moe::kErrTimeout) return fail(MOE_ERR_TIMEOUT, "device code gave up a bounded wait (bits 0x%x)", bits);
   if (bits & moe::kErrResidency) return fail(MOE_ERR_RESIDENCY, "an expert slot did not hold the routed expert (bits 0x%x)", bits);
   return fail(MOE_ERR_ARG, "device code clamped an out-of-range routing value (bits 0x%x)", bits);
+}
+
+extern "C" int moe_check(const moe_layer* L, void* ws, void* stream) {
+  if (!valid(L)) return fail(MOE_ERR_ARG, "moe_check: invalid layer handle");
+  if (!ws) return fail(MOE_ERR_ARG, "moe_check: workspace is NULL");
+  return check_workspace(ws, static_cast<cudaStream_t>(stream), "moe_check");
 }
 
 extern "C" int moe_set_profile_events(moe_layer* L, void* const* events) {
@@ -495,6 +539,7 @@ extern "C" const char* moe_last_error(void) { return g_err; }
 
 // Internal helpers for entry points defined in other translation units.
 namespace moe {
+int check_scratch(void* ws, cudaStream_t st, const char* name) { return check_workspace(ws, st, name); }
 int report_error(int code, const char* msg) { return fail(code, "%s", msg); }
 int report_cuda(cudaError_t e, const char* what) { return cuda_fail(e, what); }
 int layer_device(const moe_layer* L) { return valid(L) ? L->device : -1; }

@@ -22,6 +22,9 @@ MOE_ERR_RESIDENCY = -5
 MOE_ERR_NOMEM = -6
 MOE_ERR_UNSUPPORTED = -7
 
+# bytes of the static device scratch behind moe_decode_noalloc (include/moe.h)
+MOE_NOALLOC_SCRATCH_BYTES = 4 << 20
+
 ERROR_NAMES = {0: "MOE_OK", -1: "MOE_ERR_ARG", -2: "MOE_ERR_ALIGN", -3: "MOE_ERR_CUDA",
                -4: "MOE_ERR_TIMEOUT", -5: "MOE_ERR_RESIDENCY", -6: "MOE_ERR_NOMEM",
                -7: "MOE_ERR_UNSUPPORTED"}
@@ -84,6 +87,7 @@ SIGNATURES = {
     "moe_residency_set_fault": (ctypes.c_int, [_vp, _i32]),
     "moe_residency_close": (None, [_vp]),
     "moe_decode_noalloc": (ctypes.c_int, [_vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp]),
+    "moe_check_noalloc": (ctypes.c_int, [_vp, _vp]),
     "moe_decode_kernels": (_i32, [_vp, _i32]),
     "moe_residency_verify": (ctypes.c_int, [_vp, _vp]),
     "moe_crc32": (ctypes.c_uint32, [_vp, _sz]),
@@ -169,6 +173,12 @@ def moe_decode_noalloc(layer, x, B, out_bf16, out_f32, ids, weights, stream=0) -
     """moe_decode with the workspace in the library's static device scratch."""
     check(lib().moe_decode_noalloc(layer, x, B, out_bf16, out_f32, ids, weights, stream),
           "moe_decode_noalloc")
+
+
+def moe_check_noalloc(layer: int, stream: int = 0) -> int:
+    """Status of the static scratch of moe_decode_noalloc (moe_check's codes);
+    clears its control block after an error."""
+    return int(lib().moe_check_noalloc(layer, stream))
 
 
 def moe_set_profile_events(layer: int, events) -> None:

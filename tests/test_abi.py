@@ -149,6 +149,7 @@ def test_residency_and_noalloc_calls_reject_invalid_handles(L):
         assert L.moe_decode_kernels(r, 1) == -1
         L.moe_residency_close(r)  # ignored
         assert L.moe_decode_noalloc(r, 0, 1, 0, 0, 0, 0, None) == moe.MOE_ERR_ARG
+        assert L.moe_check_noalloc(r, None) == moe.MOE_ERR_ARG
     assert "invalid" in moe.last_error()
 
 

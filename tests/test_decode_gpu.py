@@ -74,6 +74,29 @@ def test_identity_expert_layer(T):
         np.testing.assert_allclose(of[t], scale * x, rtol=2e-6, atol=1e-30)
 
 
+@pytest.mark.parametrize("T", [1, 3])
+def test_identity_expert_layer_unclamped(T):
+    """The identity-expert layer on hidden states as drawn (no clamp): small
+    activations in a chunk with a large one are rounded by the fixed-point
+    path, so the closed form holds within the parity bar, not exactly."""
+    records, shared, rc, rsb = identity_layer()
+    E, k, H = 8, 2, 64
+    shape = synth.Shape(H, E, k, H, H)
+    dl = DeviceLayer(shape, 0, max_tokens=4, device=DEV, host_records=records, host_shared=shared,
+                     router=(rc, rsb))
+    lay = oracle.Layer(H, E, k, H, H, {e: records[e] for e in range(E)}, shared, rc, rsb)
+    xs = np.stack([synth.hidden(5, 0, t, H) for t in range(T)])
+    xs[:, 0] = synth.bf16_from_double(8.0)
+    of, ob, ids, w = run(dl, xs)
+    for t in range(T):
+        ref, rids, rp = lay.token(xs[t])
+        assert_token(t, of, ob, ids, w, ref, rids, rp)
+        x = synth.bf16_bits_to_float(xs[t]).astype(np.float64)
+        scale = 1.0 + sum(float(w[t, i]) * 2.0 ** -(int(ids[t, i]) % 3) for i in range(k))
+        closed = scale * x
+        assert np.abs(of[t] - closed).max() <= TOL_REL * np.abs(closed).max() + TOL_ABS
+
+
 # ---------------------------------------------------------------- small layers
 
 SMALL = [

@@ -13,6 +13,9 @@
   leaves the slot empty, and the next step recovers.
 * A step needing more experts than slots runs as waves of consecutive
   tokens, replayed exactly by the oracle.
+* The streamed workload's own layer shape (H=7168, F=Fs=2048, top-16,
+  Zipf(1.1) router offsets; E cut to 64, 24 slots): B=1 steps with
+  evictions and a B=4 step in waves, every output against the oracle.
 * The optional CRC-32 check of host records: a wrong checksum refuses the
   step that would upload the record, with the cache state unchanged.
 * Router lookahead (moe_residency_lookahead): the hand-worked trace
@@ -24,6 +27,7 @@
 """
 import ctypes
 import os
+from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 import pytest
@@ -379,5 +383,46 @@ def test_lookahead_faults():
     assert_oracle(got, 0, *orc.token(x1[0]))
     st = cl.stats()
     assert st["lookahead_hits"] >= 1 and st["misses"] - before["misses"] == 0
+    cl.close()
+    dl.close()
+
+
+def test_streamed_workload_shape_through_the_cache():
+    """The cache at the streamed workload's layer shape, where its kernels
+    run the large tile plan (gate|up of the shared expert during the copies,
+    then the routed gate|up and the down + combine).  E is cut to 64 and the
+    cache to 24 slots so that the layer fits a test (1.6 GB of records).
+    Six B=1 steps (two fill the cache, the rest evict) and one B=4 step (64
+    pairs over more distinct experts than slots: waves).  Every token of
+    every step: ids bit-exact, weights within 1e-5 and out_f32 within the
+    parity bar of the fp64 oracle; counters and slots equal the oracle's LFU
+    replay of the waves it cuts from the GPU's ids."""
+    E, n_slots = 64, 24
+    shape = synth.Shape(7168, E, 16, 2048, 2048)
+    beta = synth.beta_zipf(4, 0, E)
+    hl, dl, cl = make(shape, 4, beta, n_slots, max_tokens=4)
+    orc = hl.oracle()
+    lfu = oracle.LFU(n_slots, E)
+    n_waves = 0
+    with ThreadPoolExecutor(max_workers=8) as pool:   # the oracle's C code runs outside the GIL
+        for s, B in enumerate([1, 1, 1, 1, 1, 1, 4]):
+            xs = np.stack([hidden_with_margin(orc, 43, s, t) for t in range(B)])
+            refs = pool.map(orc.token, list(xs))
+            got = host(cl.decode(bf16_tensor(xs, DEV)))
+            assert dl.check() == moe.MOE_OK, moe.last_error()
+            for t, ref in enumerate(refs):
+                assert_oracle(got, t, *ref)
+            assert np.array_equal(got[0], synth.float_to_bf16_bits(got[1]))
+            ws = oracle.waves(got[2], n_slots)
+            for t0, t1 in ws:
+                lfu.step(first_appearance(got[2][t0:t1]))
+            n_waves += len(ws)
+            st = cl.stats()
+            assert st["steps"] == n_waves
+            assert (st["hits"], st["misses"], st["evictions"]) == (lfu.hits, lfu.misses, lfu.evictions)
+            assert cl.slots() == list(lfu.slot_expert)
+    st = cl.stats()
+    assert st["evictions"] > 0 and st["hits"] > 0 and n_waves > 7
+    assert st["bytes_h2d"] == st["misses"] * oracle.record_layout(shape.H, shape.F)["bytes"]
     cl.close()
     dl.close()
