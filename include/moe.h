@@ -191,20 +191,23 @@ int moe_check(const moe_layer *layer, void *workspace, void *stream);
 /* Number of kernels one moe_decode call with B tokens launches on this
  * layer, as its dispatch would choose them (with a workspace sized for B):
  * 2 for one token on the fused single-token kernel (router, fused gate|up +
- * down), 3 where the single-token kernels are not fused, B times that for
- * batches run one token at a time, 5 for the tensor-core chunk kernels and 3
- * for the grouped kernels; 1 + 4B on a wbits = 3 layer (the router, then
- * gate|up, SwiGLU, down and combine per token).  0 for B = 0; -1 on a bad
- * handle or B outside [0, max_tokens].  Host-only: no device work. */
+ * down), 3 where the single-token kernels are not fused; 3 for 2..16 tokens
+ * on the few-token fused kernel (router, fused kernel, combine); B times the
+ * single-token count for larger batches run one token at a time, 5 for the
+ * tensor-core chunk kernels and 3 for the grouped kernels; 4 on a wbits = 3
+ * layer (the router, then gate|up, down and combine for every token at
+ * once).  0 for B = 0; -1 on a bad handle or B outside [0, max_tokens].
+ * Host-only: no device work. */
 int32_t moe_decode_kernels(const moe_layer *layer, int32_t B);
 
 /* Profiling hook.  With `events` pointing to four cudaEvent_t (passed as
  * void*), later moe_decode / moe_prefill_chunk calls on this layer record
- * events[0] before the router kernel, events[1] before the gate|up (or
- * grouped-GEMM, or fused single-token) kernel, events[2] before the down
- * kernel (right after the fused kernel, which has none) and events[3] after
- * it, and launch without programmatic dependent launch so the intervals are
- * per kernel.  NULL switches the hook off.  The events stay caller-owned. */
+ * events[0] before the router kernel, events[1] before the first expert
+ * kernel (gate|up, the fused kernel or the grouped GEMM), events[2] before
+ * the second (down, the few-token combine, or right after the single-token
+ * fused kernel, which has none) and events[3] after the last, and launch
+ * without programmatic dependent launch so the intervals are per kernel.
+ * NULL switches the hook off.  The events stay caller-owned. */
 int moe_set_profile_events(moe_layer *layer, void *const *events);
 
 /* Thread-local description of the last error (never NULL). */
@@ -355,7 +358,7 @@ void moe_residency_close(moe_residency *res);
  * library, one per device.  The call itself allocates nothing.
  *
  * Limit: moe_workspace_bytes(layer, B) must be <= MOE_NOALLOC_SCRATCH_BYTES
- * (4 MiB: for H=7168, E=512, top-16, F=Fs=2048 that is B <= 18); a larger B
+ * (16 MiB: for H=7168, E=512, top-16, F=Fs=2048 that is B <= 31); a larger B
  * is rejected with MOE_ERR_ARG before anything is launched, and
  * moe_last_error() says to use moe_decode with a caller-allocated
  * workspace.  The layer's device must be the current device (MOE_ERR_ARG
@@ -378,7 +381,7 @@ void moe_residency_close(moe_residency *res);
  * moe_check_noalloc reads and clears them.
  *
  * Pointers, alignment, sizes and return codes otherwise as moe_decode. */
-#define MOE_NOALLOC_SCRATCH_BYTES (4u << 20)
+#define MOE_NOALLOC_SCRATCH_BYTES (16u << 20)
 int moe_decode_noalloc(moe_layer *layer, const uint16_t *x, int32_t B, uint16_t *out_bf16,
                        float *out_f32, int32_t *ids, float *weights, void *stream);
 

@@ -16,8 +16,9 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 SO = os.path.join(PKG, "libmoe.so")
-SOURCES = ["api.cu", "decode.cu", "decode_b1.cu", "prefill.cu", "residency.cu", "noalloc.cu", "rvq.cu"]
-HEADERS = ["common.cuh", "kernels.h", "tcgen05.cuh", "tma.cuh", "gemv.cuh"]
+SOURCES = ["api.cu", "decode.cu", "decode_b1.cu", "decode_bt.cu", "prefill.cu", "residency.cu", "noalloc.cu",
+           "rvq.cu"]
+HEADERS = ["common.cuh", "kernels.h", "tcgen05.cuh", "tma.cuh", "gemv.cuh", "fused.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", os.path.join(ROOT, "include")]
 

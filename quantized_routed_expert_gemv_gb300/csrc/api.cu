@@ -32,6 +32,10 @@ size_t prefill_workspace_bytes(const LayerArgs& a, int T);
 size_t rvq_smem_need(const LayerArgs& a);
 cudaError_t set_rvq_attributes(int smem_optin);
 cudaError_t launch_decode_rvq(const LayerArgs& a, int num_sms, cudaStream_t st);
+size_t rvq_partial_floats(int H, int k, int F, int Fs, int T, int which);
+bool plan_bt(LayerArgs& a, int num_sms, int smem_optin);
+cudaError_t set_bt_attributes(int smem_optin);
+cudaError_t launch_decode_bt(const LayerArgs& a, int num_sms, cudaStream_t st);
 }  // namespace moe
 
 using moe::LayerArgs;
@@ -227,7 +231,8 @@ extern "C" int moe_open(const moe_layer_desc* desc, const moe_layer_weights* w, 
                 need, smem_optin);
   }
   if ((e = moe::set_decode_attributes(smem_optin)) || (e = moe::set_b1_attributes(smem_optin)) ||
-      (e = moe::set_prefill_attributes(smem_optin)) || (e = moe::set_rvq_attributes(smem_optin))) {
+      (e = moe::set_prefill_attributes(smem_optin)) || (e = moe::set_rvq_attributes(smem_optin)) ||
+      (e = moe::set_bt_attributes(smem_optin))) {
     delete L;
     return cuda_fail(e, "moe_open: cudaFuncSetAttribute");
   }
@@ -260,8 +265,15 @@ extern "C" void moe_close(moe_layer* L) {
 // calls (kept at zero by the kernels, cleared by moe_check after a device
 // error); everything after them is per-call scratch.
 
+// The persistent control block: 64 control words, per-entry h counters (the
+// shared expert and up to kMaxExperts routed experts), per down row tile
+// counters (at most H / 8 tiles), each region rounded to 256 bytes.
+constexpr size_t round256(size_t v) { return (v + 255) / 256 * 256; }
+constexpr size_t kCtlBytes = round256(64 * 4);
+constexpr size_t kHcntBytes = round256((moe::kMaxExperts + 1) * 4);
+constexpr size_t kTcntBytes = round256(moe::kMaxDim / 8 * 4);
 // Bytes at the start of a workspace that persist between calls.
-constexpr size_t kPersistentBytes = 64 * 4 + 64 * 4 + moe::kMaxDim / 8 * 4;
+constexpr size_t kPersistentBytes = kCtlBytes + kHcntBytes + kTcntBytes;
 
 struct Carve {
   size_t off = 0;
@@ -277,14 +289,19 @@ static size_t carve(const moe_layer* L, int T, moe::Workspace* ws, uint8_t* base
   const size_t H = L->d.hidden, E = L->d.n_experts, k = L->d.top_k, F = L->d.ffn,
                Fs = L->d.shared_ffn, t = static_cast<size_t>(T);
   Carve c;
-  // persistent control block: 64 control words, per-entry h counters, per
-  // down row tile counters (at most H / 8 tiles)
-  const size_t o_ctl = c.take(64 * 4), o_hcnt = c.take(64 * 4), o_tcnt = c.take(moe::kMaxDim / 8 * 4);
-  // single-token fixed-point h: k routed rows of F and the shared row of Fs;
-  // per 32-value chunk 64 bytes of words and 4 group scales and sums (96 B)
-  const size_t hchunks = k * (F / 32) + Fs / 32;
+  const bool rvq = L->d.wbits == 3;
+  const size_t o_ctl = c.take(kCtlBytes), o_hcnt = c.take(kHcntBytes), o_tcnt = c.take(kTcntBytes);
+  // Fixed-point h of the fused kernels, per 32-value chunk 64 bytes of words
+  // and 4 group scales and sums (96 B): one token, a block per expert entry
+  // (k routed rows of F, the shared row of Fs); few tokens, a block per
+  // (expert, token) pair.  The few-token buffers are sized for
+  // min(T, kBtMaxTokens) tokens, so a workspace for T serves every smaller
+  // batch.
+  const size_t tb = rvq ? 0 : std::min(t, static_cast<size_t>(moe::kBtMaxTokens));
+  const size_t hchunks = std::max(k * (F / 32) + Fs / 32, tb * (k * (F / 32) + Fs / 32));
   const size_t o_hx = c.take(hchunks * 96);
-  const size_t o_yp = c.take((k + 1) * H * 4);
+  const size_t o_yp = c.take(std::max(k + 1, tb * (k + (Fs ? 1 : 0))) * H * 4);
+  const size_t o_xq = c.take(tb * (H / 32) * 72);
   const size_t o_log = c.take(t * E * 4);
   const size_t o_nact = c.take(16);
   const size_t o_ae = c.take(E * 4), o_ao = c.take(E * 4), o_ac = c.take(E * 4);
@@ -295,18 +312,17 @@ static size_t carve(const moe_layer* L, int T, moe::Workspace* ws, uint8_t* base
   const size_t o_xs = c.take(t * H * 2), o_obs = c.take(t * H * 2);
   const size_t o_ids = c.take(t * k * 4), o_w = c.take(t * k * 4), o_ofs = c.take(t * H * 4);
   LayerArgs a = base_args(L);
-  // residual-VQ layers: per-slice partial sums of one token (slices of 256 inputs)
-  const bool rvq = L->d.wbits == 3;
-  const size_t Fm = std::max(F, Fs), slices_h = (H / 8 + 31) / 32, slices_f = (Fm / 8 + 31) / 32;
-  const size_t o_rg = c.take(rvq ? slices_h * (k + 1) * Fm * 4 : 0);
-  const size_t o_ru = c.take(rvq ? slices_h * (k + 1) * Fm * 4 : 0);
-  const size_t o_ry = c.take(rvq ? (k + 1) * slices_f * H * 4 : 0);
+  // residual-VQ layers: per-slice partial sums of every token (slices of 256 inputs)
+  const size_t o_rg = c.take(rvq ? moe::rvq_partial_floats(H, k, F, Fs, T, 0) * 4 : 0);
+  const size_t o_ru = c.take(rvq ? moe::rvq_partial_floats(H, k, F, Fs, T, 1) * 4 : 0);
+  const size_t o_ry = c.take(rvq ? moe::rvq_partial_floats(H, k, F, Fs, T, 2) * 4 : 0);
   const size_t o_pf = c.take(rvq ? 0 : moe::prefill_workspace_bytes(a, T));
   if (ws && base) {
     ws->ctl = reinterpret_cast<unsigned*>(base + o_ctl);
     ws->hcnt = reinterpret_cast<unsigned*>(base + o_hcnt);
     ws->tcnt = reinterpret_cast<unsigned*>(base + o_tcnt);
     ws->ypart = reinterpret_cast<float*>(base + o_yp);
+    ws->xq = base + o_xq;
     ws->hx = base + o_hx;
     ws->logits = reinterpret_cast<float*>(base + o_log);
     ws->n_act = reinterpret_cast<int*>(base + o_nact);
@@ -383,6 +399,22 @@ static bool per_token_decode(const moe_layer* L, int T) {
   return T > 1 && T <= 64 && static_cast<long>(T) * L->d.top_k <= L->d.n_experts;
 }
 
+// Batches of 2..kBtMaxTokens tokens run the few-token fused kernel
+// (decode_bt.cu): the single-token weight stream with a token loop per item.
+static bool few_token_decode(const moe_layer* L, int T) {
+  return T >= 2 && T <= moe::kBtMaxTokens && L->d.wbits == 4;
+}
+
+// plan_bt on a copy of `a`'s geometry fields (the single-token plan must
+// hold too: the few-token kernel uses its row-lane mapping).
+static bool bt_planned(const moe_layer* L, LayerArgs& a) {
+  LayerArgs b = a;
+  if (!moe::plan_b1(b, L->num_sms, L->smem_optin)) return false;
+  if (!moe::plan_bt(b, L->num_sms, L->smem_optin)) return false;
+  a = b;
+  return true;
+}
+
 static int run(moe_layer* L, const uint16_t* x, int32_t T, uint16_t* ob, float* of, int32_t* ids,
                float* wts, void* ws, size_t ws_bytes, void* stream, Path path, const char* name) {
   LayerArgs a;
@@ -398,6 +430,10 @@ static int run(moe_layer* L, const uint16_t* x, int32_t T, uint16_t* ob, float* 
     e = moe::launch_prefill(a, &L->maps, L->num_sms, st);
   } else if (T == 1 && moe::plan_b1(a, L->num_sms, L->smem_optin)) {
     e = moe::launch_decode_b1(a, L->num_sms, st);
+  } else if (few_token_decode(L, T) && bt_planned(L, a)) {
+    // A few tokens: one pass over the step's experts, each expert's weights
+    // read once and applied to all of its tokens.
+    e = moe::launch_decode_bt(a, L->num_sms, st);
   } else if (per_token_decode(L, T) && moe::plan_b1(a, L->num_sms, L->smem_optin)) {
     // Few tokens over many experts: the tokens share almost no expert, so a
     // grouped pass reads nearly the same weight bytes as one single-token
@@ -489,11 +525,12 @@ extern "C" int moe_decode_host(moe_layer* L, const uint16_t* x_host, int32_t B, 
 extern "C" int32_t moe_decode_kernels(const moe_layer* L, int32_t B) {
   if (!valid(L) || B < 0 || B > L->d.max_tokens) return -1;
   if (B == 0) return 0;
-  if (L->d.wbits == 3) return 1 + 4 * B;  // router; per token gate|up, SwiGLU, down, combine
+  if (L->d.wbits == 3) return 4;  // router, gate|up, down, combine for every token at once
   LayerArgs a = base_args(L);
   a.T = B;
   const int b1 = moe::plan_b1(a, L->num_sms, L->smem_optin) ? (a.f1_nst > 0 ? 2 : 3) : 0;
   if (B == 1 && b1) return b1;
+  if (few_token_decode(L, B) && bt_planned(L, a)) return 3;
   if (per_token_decode(L, B) && b1) return B * b1;
   if (moe::prefill_tc_ok(a, B) && L->maps.valid) return 5;
   return 3;

@@ -75,6 +75,40 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const __grid_con
   const bool act = g < G && c < nchunk;
   float* red = rsm;  // [G][NT][kRouterRows][WPR]
 
+  if (blockIdx.x < a.xq_nconv) {
+    // The few-token fused kernel (decode_bt.cu) reads every token's
+    // activations in the fixed-point chunk form of gemv.cuh: CTAs below
+    // xq_nconv write them once ([T][4 kinds][C] words, then [T][C] (2^e,
+    // plain sum)) and count themselves done on ctl[10] (release).
+    const int C = H >> 5, n = T * C;
+    uint4* xw = reinterpret_cast<uint4*>(a.ws.xq);
+    float2* xs = reinterpret_cast<float2*>(a.ws.xq + static_cast<size_t>(T) * C * 64);
+    for (int i = blockIdx.x * kRouterThreads + tid; i < n; i += a.xq_nconv * kRouterThreads) {
+      const int t = i / C, c = i - t * C;
+      const uint4* v = reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(t) * H + c * 32);
+      float xv[32], sx = 0.f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint4 w4 = __ldg(v + j);
+        const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+        for (int b = 0; b < 4; ++b) xv[8 * j + 2 * b] = bf16lo(w[b]), xv[8 * j + 2 * b + 1] = bf16hi(w[b]);
+      }
+#pragma unroll
+      for (int m = 0; m < 32; ++m) sx += xv[m];
+      XChunk X;
+      const float scale = make_xchunk_own(xv, X);
+      xw[(static_cast<size_t>(t) * 4 + 0) * C + c] = make_uint4(X.eh[0], X.eh[1], X.eh[2], X.eh[3]);
+      xw[(static_cast<size_t>(t) * 4 + 1) * C + c] = make_uint4(X.el[0], X.el[1], X.el[2], X.el[3]);
+      xw[(static_cast<size_t>(t) * 4 + 2) * C + c] = make_uint4(X.oh[0], X.oh[1], X.oh[2], X.oh[3]);
+      xw[(static_cast<size_t>(t) * 4 + 3) * C + c] = make_uint4(X.ol[0], X.ol[1], X.ol[2], X.ol[3]);
+      xs[static_cast<size_t>(t) * C + c] = make_float2(scale, sx);
+    }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) red_add_release_gpu(&a.ws.ctl[10], 1u);
+  }
+
   // The grid is (row blocks of kRouterRows experts) x (token blocks): a CTA
   // loads its router rows once and walks its share of the token passes.
   const int RB = (E + kRouterRows - 1) / kRouterRows;
@@ -783,13 +817,18 @@ static cudaError_t mark(const LayerArgs& a, int i, cudaStream_t st) {
   return a.prof_on ? cudaEventRecord(static_cast<cudaEvent_t>(a.prof[i]), st) : cudaSuccess;
 }
 
-static cudaError_t launch_router_g(const LayerArgs& a, int num_sms, cudaStream_t st) {
-  const bool one = (a.T == 1);
-  const int nt = one ? 1 : 2;
+// Router grid: row blocks x token blocks.
+int decode_router_grid(const LayerArgs& a, int num_sms) {
+  const int nt = a.T == 1 ? 1 : 2;
   const int rb = (a.E + kRouterRows - 1) / kRouterRows;
   const int tp = nt * router_groups(a.H);  // tokens per pass of a CTA
   const int tb = std::max(1, std::min((a.T + tp - 1) / tp, (2 * num_sms) / rb));
-  const int rgrid = rb * tb;  // row blocks x token blocks
+  return rb * tb;
+}
+
+static cudaError_t launch_router_g(const LayerArgs& a, int num_sms, cudaStream_t st) {
+  const bool one = (a.T == 1);
+  const int rgrid = decode_router_grid(a, num_sms);
   const int kpl = a.E <= 128 ? 4 : a.E <= 256 ? 8 : a.E <= 512 ? 16 : 32;
   const void* fn;
   if (one)

@@ -12,6 +12,7 @@ constexpr int kMaxTokens = 128;  // decode B and prefill T cap
 constexpr int kMaxTopK = 32;
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxDim = 8192;    // H, F, Fs
+constexpr int kBtMaxTokens = 16; // largest batch of the few-token fused path (decode_bt.cu)
 constexpr int kConsumers = 256;  // consumer threads of the GEMV kernels (8 warps)
 constexpr int kStages = 4;       // bulk-copy pipeline depth
 constexpr int kStageTarget = 36 * 1024;  // bytes of weights per pipeline stage
@@ -31,15 +32,18 @@ struct RecordOffsets {
 // Device pointers into the caller's workspace (computed on the host).
 struct Workspace {
   unsigned* ctl;         // [0] error bits, [1] router done counter, [2] gate|up (or fused
-                         // single-token) item claims, [3] shared-only gate|up claims,
-                         // [8] fused single-token producers done claiming
-  unsigned* hcnt;        // single token, fused kernel: gate|up items done per expert entry
+                         // kernel) item claims, [3] shared-only gate|up claims, [8] fused
+                         // kernel producers done claiming, [10] router CTAs done writing xq
+  unsigned* hcnt;        // fused kernels: gate|up items done per expert entry [kMaxExperts + 1]
   unsigned* tcnt;        // single token, fused kernel: experts done per down row tile
   uint8_t* hx;           // single token: fixed-point h, one block of 96 * nc bytes per
                          // expert entry (nc chunks, starting at byte 96 * c0): [4 kinds]
                          // [nc] uint4 words (word i of a uint4 = 8-value group i of the
                          // chunk), then [nc] float4 group 2^e, then [nc] float4 group sums
-  float* ypart;          // single token, fused kernel: [entry][H] weighted down outputs
+  float* ypart;          // fused kernels: [entry][H] (one token) or [pair][H] (few tokens)
+                         // weighted down outputs
+  uint8_t* xq;           // few-token fused path: the tokens' fixed-point activation chunks,
+                         // [T][4 kinds][H/32] uint4 words, then [T][H/32] float2 (2^e, sum)
   float* logits;         // [T][E]
   int* n_act;            // number of distinct routed experts this step
   int* act_expert;       // [E] active expert ids, ascending
@@ -118,6 +122,7 @@ struct LayerArgs {
   int f1_rt, f1_stage, f1_nst; // fused single-token kernel: down rows per item, stage bytes
                                // and count (f1_nst == 0: not planned)
   PrefillPtrs pf;              // prefill chunk scratch (tensor-core path)
+  int xq_nconv;                // router CTAs that write ws.xq (0: none)
   int prof_on;                 // record prof[] events between kernels, no PDL
   void* prof[4];               // cudaEvent_t: before router / gate|up / down, after down
 };

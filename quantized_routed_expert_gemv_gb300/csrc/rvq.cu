@@ -12,20 +12,25 @@
 // The page's method: the dot product of the input with every codeword is
 // tabulated once per block of 8 inputs, and each row then costs three table
 // lookups and their sum per block, with no weight rebuilt.  Here the input is
-// cut into slices of 32 blocks (256 inputs); a CTA tabulates one slice,
-//   T[stage][block][code] = <codeword(stage, code), x_block>,
-// 96 KB per matrix kind in shared memory, and streams the code bytes of its
-// share of the rows, one row per thread, adding one table entry per stage
-// and block.  Partial sums per slice land in the workspace and small kernels
-// add them in a fixed order.  Per token:
-//   rvq_gateup_kernel   (slice, row part): gate and up partial sums of every
-//                       active expert and the shared expert
-//   rvq_swiglu_kernel   h = silu(sum g) * (sum u)
-//   rvq_down_kernel     (expert entry, slice of F, row part): down partials
+// cut into slices of 32 blocks (256 inputs) and a CTA tabulates one slice of
+// one matrix kind, 96 KB of shared memory laid out [stage][code][block]:
+// the 32 blocks of one (stage, code) fill one 128-byte row of the 32 banks.
+// Lane j of a warp owns block j of the slice for every row, so its lookups
+// always hit bank j and a warp's 32 lookups are one conflict-free wavefront
+// whatever the codes are (with lanes owning rows instead, the code decides
+// the bank and a lookup costs about 3.15 wavefronts).  Each lane reads its
+// block's 3 code bytes of a row straight from global memory; a warp takes 8
+// rows at a time and sums each row over its lanes with one 8-row butterfly.
+// Partial sums per slice land in the workspace; later kernels add them in a
+// fixed order.  One launch of each kernel serves every token of the step:
+//   rvq_gateup_kernel   (token, kind, slice, row part): gate or up partial
+//                       sums of the token's routed experts and the shared
+//                       expert; the table is built before the wait for the
+//                       router, so it overlaps the router
+//   rvq_down_kernel     (token, entry, slice of F, row part): h of the slice
+//                       from the gate|up partials (SwiGLU), its table, then
+//                       down partial sums
 //   rvq_combine_kernel  out = sum_i p_i y_i + y_shared, bf16 and f32
-// A lookup's index is the code byte, so the 32 lanes of a warp hit random
-// banks: about 3.5 shared-memory wavefronts per lookup instruction, which
-// bounds these kernels below the HBM rate.
 #include <algorithm>
 #include <cstdint>
 
@@ -40,231 +45,335 @@ cudaError_t launch_decode_router(const LayerArgs& a, int num_sms, cudaStream_t s
 
 namespace {
 
-constexpr int kRvqThreads = 256;
-constexpr int kTB = 32;          // blocks of 8 inputs per slice
-constexpr int kCodes = 256;      // codewords per stage
-constexpr int kKindWords = 3 * kCodes;
-constexpr int kTabFloats = 3 * kTB * kCodes;  // one kind's table of a slice
+constexpr int kRvqThreads = 512;          // 16 warps
+constexpr int kRvqWarps = kRvqThreads / 32;
+constexpr int kTB = 32;                   // blocks of 8 inputs per slice: one per lane
+constexpr int kCodes = 256;               // codewords per stage
+constexpr int kKindWords = 3 * kCodes;    // codewords of one matrix kind
+constexpr int kTabFloats = 3 * kCodes * kTB;  // one kind's table of a slice: [stage][code][block]
+constexpr int kBatch = 8;                 // rows a warp sums at once
 
-// Launch geometry of one token, the same on host and device.
+// Launch geometry, the same on host and device.
 struct RvqPlan {
-  int S, P, rpp;          // gate|up: input slices, row parts, rows per part
-  int Sdr, Sds, Sdm, Pd;  // down: slices of F, of Fs, their maximum; row parts
-  int rpd;                // down rows per part
+  int S;          // input slices of H (gate|up)
+  int R;          // gate|up rows of one token: k F + Fs
+  int P, rpp;     // gate|up row parts per (token, kind, slice); rows per part (multiple of 8)
+  int Sdr, Sds;   // down: slices of F and of Fs
+  int Sdm;        // their maximum
+  int Pd, rpd;    // down row parts per (token, entry, slice); rows per part (multiple of 8)
 };
 
 int cdiv(int a, int b) { return (a + b - 1) / b; }
 
 RvqPlan rvq_plan(const LayerArgs& a, int num_sms) {
   RvqPlan p;
-  const int R = a.k * a.F + a.Fs;
+  const int slots = 2 * num_sms;  // two CTAs per SM
+  p.R = a.k * a.F + a.Fs;
   p.S = cdiv(a.H / 8, kTB);
-  p.P = std::max(1, std::min(num_sms / p.S, cdiv(R, kRvqThreads)));  // one CTA per SM
-  p.rpp = cdiv(R, p.P);
+  p.P = std::max(1, std::min(slots / (2 * a.T * p.S), cdiv(p.R, kRvqWarps * kBatch)));
+  p.rpp = cdiv(cdiv(p.R, p.P), kBatch) * kBatch;
   p.Sdr = cdiv(a.F / 8, kTB);
   p.Sds = a.Fs ? cdiv(a.Fs / 8, kTB) : 0;
   p.Sdm = std::max(p.Sdr, p.Sds);
-  p.Pd = std::max(1, std::min(2 * num_sms / (a.k * p.Sdr + p.Sds), cdiv(a.H, kRvqThreads)));  // two per SM
-  p.rpd = cdiv(a.H, p.Pd);
+  const int units = a.T * (a.k + (a.Fs ? 1 : 0)) * p.Sdm;
+  p.Pd = std::max(1, std::min(slots / units, cdiv(a.H, kRvqWarps * kBatch)));
+  p.rpd = cdiv(cdiv(a.H, p.Pd), kBatch) * kBatch;
   return p;
 }
 
-size_t gateup_smem() { return (2 * kTabFloats + kTB * 8) * sizeof(float); }
-size_t down_smem() { return (kTabFloats + kTB * 8) * sizeof(float); }
+size_t rvq_table_smem() { return kTabFloats * sizeof(float) + 256 * sizeof(float); }
 
 __device__ __forceinline__ float rvq_silu(float g) { return g / (1.0f + expf(-g)); }
 
-// T[kind][stage][j][c] = <codeword(kind, stage, c), v[8j .. 8j+7]> for
-// nkinds kinds starting at book (bf16 codewords as uint4) and nb blocks.
-__device__ __forceinline__ void build_tables(const uint4* __restrict__ book, int nkinds,
-                                             const float* __restrict__ v, int nb, float* __restrict__ T) {
-  for (int q = threadIdx.x; q < nkinds * kKindWords; q += kRvqThreads) {
-    const int c = q % kCodes, ks = q / kCodes;  // ks = kind * 3 + stage
+// Lane j's entries T[stage][code][j] = <codeword(stage, code), v_j> of one
+// kind's codebooks (book: 768 codewords as uint4 of 8 bf16), v_j the lane's
+// 8 inputs; zero for lanes past the slice's nb blocks.  Warp w fills codes
+// w, w + 16, ...: the codeword is one broadcast load, each lane's store its
+// own bank.
+__device__ __forceinline__ void build_table(const uint4* __restrict__ book, const float (&v)[8], bool act,
+                                            float* __restrict__ T) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int q = warp; q < kKindWords; q += kRvqWarps) {
     const uint4 w = __ldg(book + q);
-    const float c0 = bf16lo(w.x), c1 = bf16hi(w.x), c2 = bf16lo(w.y), c3 = bf16hi(w.y);
-    const float c4 = bf16lo(w.z), c5 = bf16hi(w.z), c6 = bf16lo(w.w), c7 = bf16hi(w.w);
-    float* out = T + static_cast<size_t>(ks) * kTB * kCodes + c;
-    for (int j = 0; j < nb; ++j) {
-      const float* x = v + 8 * j;
-      float d = c0 * x[0];
-      d = fmaf(c1, x[1], d), d = fmaf(c2, x[2], d), d = fmaf(c3, x[3], d);
-      d = fmaf(c4, x[4], d), d = fmaf(c5, x[5], d), d = fmaf(c6, x[6], d), d = fmaf(c7, x[7], d);
-      out[j * kCodes] = d;
-    }
+    float d = bf16lo(w.x) * v[0];
+    d = fmaf(bf16hi(w.x), v[1], d), d = fmaf(bf16lo(w.y), v[2], d), d = fmaf(bf16hi(w.y), v[3], d);
+    d = fmaf(bf16lo(w.z), v[4], d), d = fmaf(bf16hi(w.z), v[5], d), d = fmaf(bf16lo(w.w), v[6], d);
+    d = fmaf(bf16hi(w.w), v[7], d);
+    T[q * kTB + lane] = act ? d : 0.f;
   }
 }
 
-// Sum over NB blocks and 3 stages of T[stage][j][code byte 3j + stage] for
-// one row's 3*NB code bytes (8-byte aligned).
-template <int NB>
-__device__ __forceinline__ float lookup_row(const uint8_t* __restrict__ codes, const float* __restrict__ T) {
-  constexpr int NW = 3 * NB / 8;
-  uint2 w[NW];
+// Sums 8 per-lane row partials over the warp; lane L ends with the total of
+// row L >> 2.
+__device__ __forceinline__ float rvq_bfly8(const float (&p)[8], int lane) {
+  const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+  float k[4];
 #pragma unroll
-  for (int i = 0; i < NW; ++i) w[i] = __ldg(reinterpret_cast<const uint2*>(codes) + i);
-  float acc[3] = {0.f, 0.f, 0.f};
+  for (int i = 0; i < 4; ++i) {
+    const float keep = b4 ? p[4 + i] : p[i], send = b4 ? p[i] : p[4 + i];
+    k[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 16);
+  }
+  float k2[2];
 #pragma unroll
-  for (int j = 0; j < NB; ++j)
-#pragma unroll
-    for (int s = 0; s < 3; ++s) {
-      const int n = 3 * j + s;
-      const uint32_t word = (n % 8) < 4 ? w[n / 8].x : w[n / 8].y;
-      acc[s] += T[(s * kTB + j) * kCodes + ((word >> (8 * (n % 4))) & 0xFFu)];
-    }
-  return (acc[0] + acc[1]) + acc[2];
+  for (int i = 0; i < 2; ++i) {
+    const float keep = b3 ? k[2 + i] : k[i], send = b3 ? k[i] : k[2 + i];
+    k2[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 8);
+  }
+  float v = b2 ? k2[1] : k2[0];
+  const float send = b2 ? k2[0] : k2[1];
+  v += __shfl_xor_sync(0xFFFFFFFFu, send, 4);
+  v += __shfl_xor_sync(0xFFFFFFFFu, v, 2);
+  v += __shfl_xor_sync(0xFFFFFFFFu, v, 1);
+  return v;
 }
 
-// Rows [r0, r1) of the gate|up matrices of every entry (entry-major: routed
-// entries' F rows in rank order, then the shared expert's Fs rows), over one
-// slice of the input.
-template <int NB>
-__device__ void gateup_rows(const LayerArgs& a, int t, int slice, int r0, int r1, const float* T) {
-  const int Fm = max(a.F, a.Fs);
-  const size_t row_bytes = static_cast<size_t>(a.H) / 8 * 3, o0 = static_cast<size_t>(slice) * kTB * 3;
-  for (int r = r0 + threadIdx.x; r < r1; r += kRvqThreads) {
-    int e, f;
-    const uint8_t* rec;
-    const RecordOffsets* off;
-    if (r < a.k * a.F) {
-      e = r / a.F, f = r - e * a.F, off = &a.off_r;
-      rec = a.records + static_cast<size_t>(a.ids[t * a.k + e]) * a.off_r.stride;
-    } else {
-      e = a.k, f = r - a.k * a.F, off = &a.off_s, rec = a.shared;
-    }
-    const size_t o = static_cast<size_t>(f) * row_bytes + o0;
-    const float g = lookup_row<NB>(rec + off->gate_codes + o, T);
-    const float u = lookup_row<NB>(rec + off->up_codes + o, T + kTabFloats);
-    const size_t idx = (static_cast<size_t>(slice) * (a.k + 1) + e) * Fm + f;
-    a.ws.rvq_g[idx] = g, a.ws.rvq_u[idx] = u;
+// Lane j's 3 code bytes of block j of 8 rows, whose slice chunks start at
+// row0 + i * row_bytes (8-byte aligned): the aligned 32-bit word holding
+// byte 3j and, for lanes whose bytes cross into the next word (j mod 4 in
+// {1, 2}), that word too; both stay inside the 96-byte chunk.
+struct CodeBatch {
+  uint32_t lo[kBatch], hi[kBatch];
+};
+
+__device__ __forceinline__ void load_codes(const uint8_t* row0, size_t row_bytes, int lane, bool act,
+                                           CodeBatch& c) {
+  const int w = (3 * lane) >> 2;
+  const bool two = ((lane & 3) == 1) || ((lane & 3) == 2);
+#pragma unroll
+  for (int i = 0; i < kBatch; ++i) {
+    const uint32_t* p = reinterpret_cast<const uint32_t*>(row0 + i * row_bytes) + w;
+    c.lo[i] = act ? __ldg(p) : 0u;
+    c.hi[i] = (act && two) ? __ldg(p + 1) : 0u;
   }
 }
 
-// grid S * P: CTA (slice, part)
-__global__ void __launch_bounds__(kRvqThreads, 1) rvq_gateup_kernel(const __grid_constant__ LayerArgs a,
-                                                                     const RvqPlan pl, int t) {
+// Per row of the batch: the sum of lane j's three table entries.
+__device__ __forceinline__ void lookup_batch(const CodeBatch& c, const float* __restrict__ T, int lane,
+                                             float (&acc)[kBatch]) {
+  const int sh = 8 * ((3 * lane) & 3);
+  const float* Tl = T + lane;
+#pragma unroll
+  for (int i = 0; i < kBatch; ++i) {
+    const uint32_t q = __funnelshift_r(c.lo[i], c.hi[i], sh);
+    const float t0 = Tl[(0 * kCodes + (q & 0xFFu)) * kTB];
+    const float t1 = Tl[(1 * kCodes + ((q >> 8) & 0xFFu)) * kTB];
+    const float t2 = Tl[(2 * kCodes + ((q >> 16) & 0xFFu)) * kTB];
+    acc[i] = (t0 + t1) + t2;
+  }
+}
+
+// Record of routed rank i of token t (through the cache's slot table when
+// there is one: a slot outside the pool or holding another expert latches
+// an error and is never read).
+__device__ __forceinline__ const uint8_t* rvq_routed_record(const LayerArgs& a, int t, int i) {
+  int e = a.ids[t * a.k + i];
+  if (e < 0 || e >= a.E) latch_error(&a.ws.ctl[0], kErrRange), e = 0;
+  int slot = e;
+  if (a.slot_of) {
+    slot = a.slot_of[e];
+    if (slot < 0 || slot >= a.n_slots) latch_error(&a.ws.ctl[0], kErrResidency), slot = 0;
+    else if (a.slot_tag && a.slot_tag[slot] != e) latch_error(&a.ws.ctl[0], kErrResidency);
+  }
+  return a.records + static_cast<size_t>(slot) * a.off_r.stride;
+}
+
+// Rows [r0, r1) of the CTA's row part, warp w taking batches w, w + 16, ...
+// row_chunk(r) is row r's slice chunk (8 consecutive rows share a matrix);
+// out(r) receives the row's partial sum.  The next batch's codes are loaded
+// while the current one is looked up.
+template <typename RowChunk, typename Out>
+__device__ __forceinline__ void stream_rows(int r0, int r1, size_t row_bytes, bool act, const float* T,
+                                            RowChunk row_chunk, Out out) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int rb = r0 + warp * kBatch;
+  if (rb >= r1) return;
+  CodeBatch cur, nxt;
+  load_codes(row_chunk(rb), row_bytes, lane, act, cur);
+  for (; rb < r1; rb += kRvqWarps * kBatch) {
+    const int rn = rb + kRvqWarps * kBatch;
+    if (rn < r1) load_codes(row_chunk(rn), row_bytes, lane, act, nxt);
+    float acc[kBatch];
+    lookup_batch(cur, T, lane, acc);
+    const float v = rvq_bfly8(acc, lane);
+    if ((lane & 3) == 0 && rb + (lane >> 2) < r1) out(rb + (lane >> 2), v);
+    cur = nxt;
+  }
+}
+
+// grid T * 2 * S * P: CTA (token, kind, slice, part), kind 0 gate, 1 up.
+// Partial sums to rvq_g (gate) / rvq_u (up) as [T][S][R].
+__global__ void __launch_bounds__(kRvqThreads, 2) rvq_gateup_kernel(const __grid_constant__ LayerArgs a,
+                                                                    const RvqPlan pl) {
   extern __shared__ __align__(16) float smem[];
-  float* T = smem;                   // [gate, up][3][kTB][256]
-  float* xs = smem + 2 * kTabFloats;  // the slice's inputs
-  const int slice = blockIdx.x % pl.S, part = blockIdx.x / pl.S;
-  const int b0 = slice * kTB, nb = min(kTB, a.H / 8 - b0);
-  const uint16_t* x = a.x + static_cast<size_t>(t) * a.H + 8 * b0;
-  for (int i = threadIdx.x; i < nb * 8; i += kRvqThreads) xs[i] = __uint_as_float(static_cast<uint32_t>(x[i]) << 16);
-  __syncthreads();
-  build_tables(reinterpret_cast<const uint4*>(a.cbs), 2, xs, nb, T);
-  __syncthreads();
-  const int R = a.k * a.F + a.Fs, r0 = part * pl.rpp, r1 = min(R, r0 + pl.rpp);
-  switch (nb) {  // a.H is a multiple of 64: whole slices, or a last one of 8, 16 or 24 blocks
-    case 32: gateup_rows<32>(a, t, slice, r0, r1, T); break;
-    case 24: gateup_rows<24>(a, t, slice, r0, r1, T); break;
-    case 16: gateup_rows<16>(a, t, slice, r0, r1, T); break;
-    default: gateup_rows<8>(a, t, slice, r0, r1, T); break;
+  float* T = smem;
+  int id = blockIdx.x;
+  const int p = id % pl.P;
+  id /= pl.P;
+  const int s = id % pl.S;
+  id /= pl.S;
+  const int kind = id & 1, t = id >> 1;
+  const int lane = threadIdx.x & 31;
+  const int b0 = s * kTB, nb = min(kTB, a.H / 8 - b0);
+  const bool act = lane < nb;
+  pdl_launch_dependents();
+  float v[8];
+  {
+    const uint4 w = act ? __ldg(reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(t) * a.H) + b0 + lane)
+                        : make_uint4(0, 0, 0, 0);
+    v[0] = bf16lo(w.x), v[1] = bf16hi(w.x), v[2] = bf16lo(w.y), v[3] = bf16hi(w.y);
+    v[4] = bf16lo(w.z), v[5] = bf16hi(w.z), v[6] = bf16lo(w.w), v[7] = bf16hi(w.w);
   }
+  build_table(reinterpret_cast<const uint4*>(a.cbs) + kind * kKindWords, v, act, T);
+  __syncthreads();
+  pdl_wait();  // the router's ids (routed rows), and the previous step's readers of the partials
+  const size_t row_bytes = static_cast<size_t>(a.H) / 8 * 3, o0 = static_cast<size_t>(s) * kTB * 3;
+  const int kF = a.k * a.F;
+  const size_t moff = kind ? a.off_r.up_codes : a.off_r.gate_codes;
+  const size_t soff = kind ? a.off_s.up_codes : a.off_s.gate_codes;
+  float* part = (kind ? a.ws.rvq_u : a.ws.rvq_g) + (static_cast<size_t>(t) * pl.S + s) * pl.R;
+  const int r0 = p * pl.rpp, r1 = min(pl.R, r0 + pl.rpp);
+  stream_rows(
+      r0, r1, row_bytes, act, T,
+      [&](int r) -> const uint8_t* {
+        if (r < kF) {
+          const int i = r / a.F, f = r - i * a.F;
+          return rvq_routed_record(a, t, i) + moff + static_cast<size_t>(f) * row_bytes + o0;
+        }
+        return a.shared + soff + static_cast<size_t>(r - kF) * row_bytes + o0;
+      },
+      [&](int r, float val) { part[r] = val; });
 }
 
-// grid ceil((k F + Fs) / 256): h of every entry from the slices' partial sums
-__global__ void __launch_bounds__(kRvqThreads) rvq_swiglu_kernel(const __grid_constant__ LayerArgs a,
-                                                                 const RvqPlan pl, int t) {
-  const int r = blockIdx.x * kRvqThreads + threadIdx.x;
-  if (r >= a.k * a.F + a.Fs) return;
-  const int Fm = max(a.F, a.Fs);
-  const int e = r < a.k * a.F ? r / a.F : a.k, f = r < a.k * a.F ? r - e * a.F : r - a.k * a.F;
-  float g = 0.f, u = 0.f;
-  for (int sl = 0; sl < pl.S; ++sl) {
-    const size_t idx = (static_cast<size_t>(sl) * (a.k + 1) + e) * Fm + f;
-    g += a.ws.rvq_g[idx], u += a.ws.rvq_u[idx];
-  }
-  const float h = rvq_silu(g) * u;
-  if (e < a.k) a.ws.h[(static_cast<size_t>(t) * a.k + e) * a.F + f] = h;
-  else a.ws.h_shared[static_cast<size_t>(t) * a.Fs + f] = h;
-}
-
-template <int NB>
-__device__ void down_rows(const LayerArgs& a, const uint8_t* codes, size_t row_bytes, int r0, int r1,
-                          float* y, const float* T) {
-  for (int r = r0 + threadIdx.x; r < r1; r += kRvqThreads)
-    y[r] = lookup_row<NB>(codes + static_cast<size_t>(r) * row_bytes, T);
-}
-
-// grid k * Sdr * Pd + Sds * Pd: CTA (entry, slice of the entry's F, row part)
+// grid T * (k + 1) * Sdm * Pd: CTA (token, entry, slice of the entry's
+// width, part); entry k is the shared expert.  h of the slice (SwiGLU of the
+// gate|up partials added over the input slices in order), its table, then
+// the down rows' partial sums to rvq_y as [T][k + 1][Sdm][H].
 __global__ void __launch_bounds__(kRvqThreads, 2) rvq_down_kernel(const __grid_constant__ LayerArgs a,
-                                                                  const RvqPlan pl, int t) {
+                                                                  const RvqPlan pl) {
   extern __shared__ __align__(16) float smem[];
-  float* T = smem;             // [3][kTB][256]
-  float* hs = smem + kTabFloats;
-  int e, slice, part, Fe;
-  const uint8_t* rec;
-  const RecordOffsets* off;
-  const float* h;
-  const int nr = a.k * pl.Sdr * pl.Pd;
-  if (static_cast<int>(blockIdx.x) < nr) {
-    const int per = pl.Sdr * pl.Pd, rem = blockIdx.x % per;
-    e = blockIdx.x / per, slice = rem % pl.Sdr, part = rem / pl.Sdr, Fe = a.F, off = &a.off_r;
-    rec = a.records + static_cast<size_t>(a.ids[t * a.k + e]) * a.off_r.stride;
-    h = a.ws.h + (static_cast<size_t>(t) * a.k + e) * a.F;
-  } else {
-    const int i = blockIdx.x - nr;
-    e = a.k, slice = i % pl.Sds, part = i / pl.Sds, Fe = a.Fs, off = &a.off_s, rec = a.shared;
-    h = a.ws.h_shared + static_cast<size_t>(t) * a.Fs;
+  float* T = smem;
+  float* hs = smem + kTabFloats;  // the slice's 256 h values
+  int id = blockIdx.x;
+  const int p = id % pl.Pd;
+  id /= pl.Pd;
+  const int sd = id % pl.Sdm;
+  id /= pl.Sdm;
+  const int e = id % (a.k + 1), t = id / (a.k + 1);
+  const bool sh = e == a.k;
+  if (sh && a.Fs == 0) return;
+  const int Fe = sh ? a.Fs : a.F;
+  if (sd >= (sh ? pl.Sds : pl.Sdr)) return;
+  const int lane = threadIdx.x & 31;
+  const int b0 = sd * kTB, nb = min(kTB, Fe / 8 - b0);
+  const bool act = lane < nb;
+  pdl_launch_dependents();
+  pdl_wait();  // the gate|up partials
+  // h of the slice: thread i takes value i >> 1 of kind i & 1 (gate, up)
+  const int rowb = sh ? a.k * a.F : e * a.F;
+  for (int i = threadIdx.x; i < 2 * 256; i += kRvqThreads) {
+    const int f = 8 * b0 + (i >> 1);
+    float sum = 0.f;
+    if (f < Fe) {
+      const float* src = ((i & 1) ? a.ws.rvq_u : a.ws.rvq_g) + static_cast<size_t>(t) * pl.S * pl.R + rowb + f;
+      for (int s = 0; s < pl.S; ++s) sum += __ldcg(src + static_cast<size_t>(s) * pl.R);
+    }
+    const float other = __shfl_xor_sync(0xFFFFFFFFu, sum, 1);
+    if ((i & 1) == 0) hs[i >> 1] = rvq_silu(sum) * other;
   }
-  const int b0 = slice * kTB, nb = min(kTB, Fe / 8 - b0);
-  for (int i = threadIdx.x; i < nb * 8; i += kRvqThreads) hs[i] = h[8 * b0 + i];
   __syncthreads();
-  build_tables(reinterpret_cast<const uint4*>(a.cbs) + 2 * kKindWords, 1, hs, nb, T);
+  float v[8];
+#pragma unroll
+  for (int m = 0; m < 8; ++m) v[m] = act ? hs[8 * lane + m] : 0.f;
+  build_table(reinterpret_cast<const uint4*>(a.cbs) + 2 * kKindWords, v, act, T);
   __syncthreads();
-  const size_t row_bytes = static_cast<size_t>(Fe) / 8 * 3;
-  const uint8_t* codes = rec + off->down_codes + static_cast<size_t>(b0) * 3;
-  float* y = a.ws.rvq_y + (static_cast<size_t>(e) * pl.Sdm + slice) * a.H;
-  const int r0 = part * pl.rpd, r1 = min(a.H, r0 + pl.rpd);
-  switch (nb) {
-    case 32: down_rows<32>(a, codes, row_bytes, r0, r1, y, T); break;
-    case 24: down_rows<24>(a, codes, row_bytes, r0, r1, y, T); break;
-    case 16: down_rows<16>(a, codes, row_bytes, r0, r1, y, T); break;
-    default: down_rows<8>(a, codes, row_bytes, r0, r1, y, T); break;
-  }
+  const size_t row_bytes = static_cast<size_t>(Fe) / 8 * 3, o0 = static_cast<size_t>(b0) * 3;
+  const uint8_t* codes = (sh ? a.shared + a.off_s.down_codes : rvq_routed_record(a, t, e) + a.off_r.down_codes) + o0;
+  float* y = a.ws.rvq_y + ((static_cast<size_t>(t) * (a.k + 1) + e) * pl.Sdm + sd) * a.H;
+  const int r0 = p * pl.rpd, r1 = min(a.H, r0 + pl.rpd);
+  stream_rows(
+      r0, r1, row_bytes, act, T, [&](int r) { return codes + static_cast<size_t>(r) * row_bytes; },
+      [&](int r, float val) { y[r] = val; });
 }
 
-// grid ceil(H / 256): out = sum_i p_i y_i + y_shared, entries in rank order
-__global__ void __launch_bounds__(kRvqThreads) rvq_combine_kernel(const __grid_constant__ LayerArgs a,
-                                                                  const RvqPlan pl, int t) {
-  const int r = blockIdx.x * kRvqThreads + threadIdx.x;
-  if (r >= a.H) return;
+// grid ceil(T H / 256): out = sum_i p_i y_i + y_shared, ranks in order, each
+// y the sum of its slices in order.
+__global__ void __launch_bounds__(256) rvq_combine_kernel(const __grid_constant__ LayerArgs a, const RvqPlan pl) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const size_t i = static_cast<size_t>(blockIdx.x) * 256 + threadIdx.x;
+  if (i >= static_cast<size_t>(a.T) * a.H) return;
+  const int t = static_cast<int>(i / a.H), r = static_cast<int>(i - static_cast<size_t>(t) * a.H);
+  const float* yt = a.ws.rvq_y + static_cast<size_t>(t) * (a.k + 1) * pl.Sdm * a.H + r;
   float acc = 0.f;
-  for (int i = 0; i < a.k; ++i) {
+  for (int e = 0; e < a.k; ++e) {
     float y = 0.f;
-    for (int sl = 0; sl < pl.Sdr; ++sl) y += a.ws.rvq_y[(static_cast<size_t>(i) * pl.Sdm + sl) * a.H + r];
-    acc = fmaf(a.weights[t * a.k + i], y, acc);
+    for (int sl = 0; sl < pl.Sdr; ++sl) y += __ldcg(yt + (static_cast<size_t>(e) * pl.Sdm + sl) * a.H);
+    acc = fmaf(a.weights[t * a.k + e], y, acc);
   }
   if (a.Fs) {
     float y = 0.f;
-    for (int sl = 0; sl < pl.Sds; ++sl) y += a.ws.rvq_y[(static_cast<size_t>(a.k) * pl.Sdm + sl) * a.H + r];
+    for (int sl = 0; sl < pl.Sds; ++sl) y += __ldcg(yt + (static_cast<size_t>(a.k) * pl.Sdm + sl) * a.H);
     acc += y;
   }
-  a.out_bf16[static_cast<size_t>(t) * a.H + r] = f32_to_bf16_rne(acc);
-  if (a.out_f32) a.out_f32[static_cast<size_t>(t) * a.H + r] = acc;
+  a.out_bf16[i] = f32_to_bf16_rne(acc);
+  if (a.out_f32) a.out_f32[i] = acc;
+}
+
+cudaError_t launch_rvq(const void* fn, int grid, int block, size_t smem, cudaStream_t st, bool pdl,
+                       const LayerArgs& a, const RvqPlan& pl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  void* args[] = {const_cast<LayerArgs*>(&a), const_cast<RvqPlan*>(&pl)};
+  return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+cudaError_t mark_rvq(const LayerArgs& a, int i, cudaStream_t st) {
+  return a.prof_on ? cudaEventRecord(static_cast<cudaEvent_t>(a.prof[i]), st) : cudaSuccess;
 }
 
 }  // namespace
 
-size_t rvq_smem_need(const LayerArgs&) { return std::max(gateup_smem(), down_smem()); }
+size_t rvq_smem_need(const LayerArgs&) { return rvq_table_smem(); }
 
-cudaError_t set_rvq_attributes(int smem_optin) {
-  cudaError_t e = cudaFuncSetAttribute(rvq_gateup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin);
-  return e ? e : cudaFuncSetAttribute(rvq_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin);
+// Bytes of the residual-VQ partial sums for T tokens: gate and up [T][S][R],
+// down [T][k + 1][Sdm][H] (the workspace carve).
+size_t rvq_partial_floats(int H, int k, int F, int Fs, int T, int which) {
+  const int S = cdiv(H / 8, kTB), R = k * F + Fs;
+  const int Sdm = std::max(cdiv(F / 8, kTB), Fs ? cdiv(Fs / 8, kTB) : 0);
+  return which < 2 ? static_cast<size_t>(T) * S * R : static_cast<size_t>(T) * (k + 1) * Sdm * H;
 }
 
+cudaError_t set_rvq_attributes(int smem_optin) {
+  (void)smem_optin;
+  const int bytes = static_cast<int>(rvq_table_smem());
+  cudaError_t e = cudaFuncSetAttribute(rvq_gateup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  return e ? e : cudaFuncSetAttribute(rvq_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+// The router, then gate|up, down and the combine for every token at once.
+// Profile events: before the router, before gate|up, before down, after the
+// combine.
 cudaError_t launch_decode_rvq(const LayerArgs& a, int num_sms, cudaStream_t st) {
-  cudaError_t e = launch_decode_router(a, num_sms, st);
-  if (e) return e;
+  const bool pdl = !a.prof_on;
   const RvqPlan pl = rvq_plan(a, num_sms);
-  const int R = a.k * a.F + a.Fs;
-  for (int t = 0; t < a.T; ++t) {
-    rvq_gateup_kernel<<<pl.S * pl.P, kRvqThreads, gateup_smem(), st>>>(a, pl, t);
-    rvq_swiglu_kernel<<<cdiv(R, kRvqThreads), kRvqThreads, 0, st>>>(a, pl, t);
-    rvq_down_kernel<<<a.k * pl.Sdr * pl.Pd + pl.Sds * pl.Pd, kRvqThreads, down_smem(), st>>>(a, pl, t);
-    rvq_combine_kernel<<<cdiv(a.H, kRvqThreads), kRvqThreads, 0, st>>>(a, pl, t);
-    if ((e = cudaGetLastError())) return e;
-  }
-  return cudaSuccess;
+  const int gu = a.T * 2 * pl.S * pl.P, dn = a.T * (a.k + 1) * pl.Sdm * pl.Pd;
+  const int cb = cdiv(a.T * a.H, 256);
+  cudaError_t e;
+  if ((e = mark_rvq(a, 0, st)) || (e = launch_decode_router(a, num_sms, st)) || (e = mark_rvq(a, 1, st)) ||
+      (e = launch_rvq((const void*)rvq_gateup_kernel, gu, kRvqThreads, rvq_table_smem(), st, pdl, a, pl)) ||
+      (e = mark_rvq(a, 2, st)) ||
+      (e = launch_rvq((const void*)rvq_down_kernel, dn, kRvqThreads, rvq_table_smem(), st, pdl, a, pl)) ||
+      (e = launch_rvq((const void*)rvq_combine_kernel, cb, 256, 0, st, pdl, a, pl)))
+    return e;
+  return mark_rvq(a, 3, st);
 }
 
 }  // namespace moe

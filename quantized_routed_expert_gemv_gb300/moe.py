@@ -23,7 +23,7 @@ MOE_ERR_NOMEM = -6
 MOE_ERR_UNSUPPORTED = -7
 
 # bytes of the static device scratch behind moe_decode_noalloc (include/moe.h)
-MOE_NOALLOC_SCRATCH_BYTES = 4 << 20
+MOE_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 ERROR_NAMES = {0: "MOE_OK", -1: "MOE_ERR_ARG", -2: "MOE_ERR_ALIGN", -3: "MOE_ERR_CUDA",
                -4: "MOE_ERR_TIMEOUT", -5: "MOE_ERR_RESIDENCY", -6: "MOE_ERR_NOMEM",

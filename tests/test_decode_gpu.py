@@ -141,6 +141,27 @@ def test_single_token_geometries(shape):
         assert_token(0, of, ob, ids, w, ref, rids, rp)
 
 
+@pytest.mark.parametrize("T", [2, 4, 5, 16])
+def test_few_tokens_sharing_every_expert(T):
+    """Logit offsets steer every token to the same k experts, so each routed
+    expert of the few-token kernel serves all T tokens (the most tokens an
+    item holds, up to 16) and the shared expert too; a second call on the
+    same workspace checks that the kernels left their counters at zero."""
+    shape = synth.Shape(1024, 40, 6, 448, 320)
+    beta = np.zeros(shape.E, np.float32)
+    beta[[3, 7, 11, 19, 23, 31]] = 50.0
+    hl = HostLayer(shape, seed=37, beta=beta)
+    orc = hl.oracle()
+    dl = device_from_host(hl)
+    for rep in range(2):
+        xs = draw_tokens(orc, 37, 5 + rep, T)
+        of, ob, ids, w = run(dl, xs)
+        assert set(np.unique(ids)) == {3, 7, 11, 19, 23, 31}
+        for t in range(T):
+            ref, rids, rp = orc.token(xs[t])
+            assert_token(t, of, ob, ids, w, ref, rids, rp)
+
+
 @pytest.mark.parametrize("outlier", [64.0, 4096.0])
 def test_activation_outliers(outlier):
     # One huge activation per token (as real hidden states have): the single-
@@ -309,13 +330,17 @@ def test_large_prefill_chunk(large):
 
 def test_decode_kernel_counts(large):
     """moe_decode_kernels follows the dispatch: one token runs the router and
-    the fused gate|up + down kernel; 16 tokens over 512 experts run 16 such
-    passes; 64 tokens (64 * 16 > 512) the five tensor-core chunk kernels."""
+    the fused gate|up + down kernel; 2..16 tokens the router, the few-token
+    fused kernel and the combine; 32 tokens over 512 experts one single-token
+    pass per token; 64 tokens (64 * 16 > 512) the five tensor-core chunk
+    kernels."""
     _, dl, _ = large
     L = moe.lib()
     assert L.moe_decode_kernels(dl.handle, 0) == 0
     assert L.moe_decode_kernels(dl.handle, 1) == 2
-    assert L.moe_decode_kernels(dl.handle, 16) == 32
+    for B in (2, 4, 16):
+        assert L.moe_decode_kernels(dl.handle, B) == 3
+    assert L.moe_decode_kernels(dl.handle, 32) == 64
     assert L.moe_decode_kernels(dl.handle, 64) == 5
     assert L.moe_decode_kernels(dl.handle, 129) == -1
     assert L.moe_decode_kernels(None, 1) == -1
