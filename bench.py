@@ -49,6 +49,8 @@ def parse_args():
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--batch", type=int, default=1)
     p.add_argument("--pool", type=int, default=64, help="distinct hidden-state batches rotated")
+    p.add_argument("--windows", type=int, default=5,
+                   help="timed windows of K steps each; the value is the median window")
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--experts", type=int, default=0,
                    help="shrink the routed-expert count (small layers for ncu captures only)")
@@ -364,7 +366,7 @@ def _frac(sl):
     return 1.0 - len(sl.plan) / sl._n_slices
 
 
-def config_dict(s, B):
+def config_dict(s, B, windows=1):
     return {"workload": f"{WORKLOAD}: H={s.H} E={s.E} top-{s.k} F={s.F} Fs={s.Fs}, "
                         f"4-bit affine group-64 experts, 8-bit router, all experts in HBM",
             "batch": B, "hidden": s.H, "experts": s.E, "top_k": s.k, "ffn": s.F,
@@ -372,7 +374,8 @@ def config_dict(s, B):
             "l2": "inputs larger than L2: >=425 MB of distinct weights per step, hidden "
                   "states rotated over a pool of distinct batches",
             "graphs": f"{GRAPH_STEPS} consecutive steps per CUDA graph replay (the remainder "
-                      "of K as one-step graphs); every step is a full layer call"}
+                      "of K as one-step graphs); every step is a full layer call",
+            "timing": f"{windows} timed windows of K steps; value from the median window"}
 
 
 # ----------------------------------------------------------------- our arm
@@ -380,30 +383,66 @@ def config_dict(s, B):
 GRAPH_STEPS = 16  # consecutive steps captured in one CUDA graph
 
 
-def time_graphs(torch, graphs, chunks, K, W, stream, world, device):
-    """W warm-up steps, then exactly K timed steps: K // GRAPH_STEPS replays
-    of the multi-step graphs (rotating over the pool) and the remainder as
-    single-step graphs; without multi-step graphs, K single-step replays."""
+def time_graphs(torch, graphs, chunks, K, W, stream, world, device, windows=1):
+    """W warm-up steps, then `windows` timed windows of exactly K steps each:
+    K // GRAPH_STEPS replays of the multi-step graphs (rotating over the
+    pool) and the remainder as single-step graphs; without multi-step graphs,
+    K single-step replays.  Every window is bracketed by a barrier and a
+    synchronize and timed with CUDA events on the launching stream.  Returns
+    (per-window ms over all ranks (max), t0, t1)."""
     for i in range(W):
         graphs[i % len(graphs)].replay()
     torch.cuda.synchronize()
-    barrier(world)
+    out = []
+    t_first = None
+    for w in range(windows):
+        barrier(world)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0 = time.time()
+        t_first = t0 if t_first is None else t_first
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            n_multi = K // GRAPH_STEPS if chunks else 0
+            for i in range(n_multi):
+                chunks[(i + w) % len(chunks)].replay()
+            for i in range(K - n_multi * GRAPH_STEPS):
+                graphs[i % len(graphs)].replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        t1 = time.time()
+        barrier(world)
+        out.append(max_over_ranks(world, e0.elapsed_time(e1), device))
+    return out, t_first, t1
+
+
+def window_stats(ms_list, K):
+    """Median window and the spread of the windows, per step."""
+    per = sorted(m / K for m in ms_list)
+    return {"ms_per_step": statistics.median(per), "windows": len(per),
+            "spread_ms_per_step": [per[0], per[-1]],
+            "spread_pct": 100.0 * (per[-1] - per[0]) / statistics.median(per)}
+
+
+def kernel_times(torch, moe, dl, x, outs, stream, pool, n=100):
+    """Per-kernel CUDA-event durations (ms) of the dispatch's kernels: the
+    profiling hook records events between them and launches without
+    programmatic dependent launch.  Returns the three intervals averaged."""
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    for e in evs:               # torch creates the CUDA event on its first record
+        e.record(stream)
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t0 = time.time()
+    moe.moe_set_profile_events(dl.handle, [e.cuda_event for e in evs])
+    sums = [0.0, 0.0, 0.0]
     with torch.cuda.stream(stream):
-        e0.record(stream)
-        n_multi = K // GRAPH_STEPS if chunks else 0
-        for i in range(n_multi):
-            chunks[i % len(chunks)].replay()
-        for i in range(K - n_multi * GRAPH_STEPS):
-            graphs[i % len(graphs)].replay()
-        e1.record(stream)
-    torch.cuda.synchronize()
-    t1 = time.time()
-    barrier(world)
-    ms = e0.elapsed_time(e1)
-    return max_over_ranks(world, ms, device), t0, t1
+        for i in range(n + 5):
+            dl.decode(x[i % pool], outs, stream.cuda_stream)
+            evs[3].synchronize()
+            if i >= 5:
+                for j in range(3):
+                    sums[j] += evs[j].elapsed_time(evs[j + 1])
+    moe.moe_set_profile_events(dl.handle, None)
+    return [v / n for v in sums]
 
 
 def run_ours(args, world, rank, local):
@@ -478,16 +517,39 @@ def run_ours(args, world, rank, local):
     clocks.start()
     time.sleep(0.3)
     main = None
+    peaks = _peaks()
+    peak = peaks.get("hbm_gbs", 6800.0)
+    peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
     for B in batches:
         xs, x, outs, graphs, chunks, distinct = make(B)
         K = args.steps if B == args.batch else min(args.steps, 2000)
-        ms, t0, t1 = time_graphs(torch, graphs, chunks, K, args.warmup, stream, world, device)
+        nwin = args.windows if B == args.batch else min(args.windows, 3)
+        ms_list, t0, t1 = time_graphs(torch, graphs, chunks, K, args.warmup, stream, world, device, nwin)
         assert dl.check(stream.cuda_stream) == moe.MOE_OK, moe.last_error()
+        st = window_stats(ms_list, K)
+        msps = st["ms_per_step"]
         nbytes = layer_step_bytes(s, B, distinct, with_f32=True)
-        r = {"tokens_per_s": B * K * world / (ms / 1e3), "ms_per_step": ms / K,
-             "distinct_experts": distinct, "bytes_per_step": nbytes["step"],
-             "layer_gbs": nbytes["step"] / (ms / K / 1e3) / 1e9}
+        r = {"tokens_per_s": B * world / (msps / 1e3), "ms_per_step": msps,
+             "windows": st["windows"], "spread_ms_per_step": st["spread_ms_per_step"],
+             "spread_pct": st["spread_pct"], "distinct_experts": distinct, "bytes_per_step": nbytes["step"],
+             "layer_gbs": nbytes["step"] / (msps / 1e3) / 1e9,
+             "gpu_launches_per_step": moe.lib().moe_decode_kernels(dl.handle, B)}
         r["layer_frac_of_8tbs"] = r["layer_gbs"] / NOMINAL_HBM_GBS
+        if not args.no_extras:
+            per = kernel_times(torch, moe, dl, x, outs, stream, args.pool, n=min(args.steps, 200))
+            # one token: the router, then the fused gate|up + down kernel (the
+            # third interval is empty); 2..16 tokens: the router, the few-token
+            # fused kernel, then the combine
+            fused = (B == 1 and per[2] < 0.1 * per[1]) or (2 <= B <= 16 and r["gpu_launches_per_step"] == 3)
+            key = "fused" if fused else "gateup"
+            kname = ("ffn_b1_kernel" if B == 1 else "ffn_bt_kernel") if fused else \
+                ("gateup_b1_kernel" if B == 1 else "gateup_kernel")
+            achieved = nbytes[key] / (per[1] / 1e3) / 1e9
+            r["kernel_ms"] = ({"router": per[0], "ffn": per[1]} if fused and B == 1 else
+                              {"router": per[0], "ffn": per[1], "combine": per[2]} if fused else
+                              {"router": per[0], "gateup": per[1], "down": per[2]})
+            r["kernel"] = {"name": kname, "algorithmic_bytes_per_launch": nbytes[key],
+                           "achieved_gbs": achieved, "frac_of_measured_hbm": achieved / peak}
         results[B] = r
         if B == args.batch:
             main = dict(r, K=K, t0=t0, t1=t1, xs=xs, x=x, outs=outs, nbytes=nbytes)
@@ -500,50 +562,28 @@ def run_ours(args, world, rank, local):
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": main["ms_per_step"],
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": DTYPE,
            "data": "synthetic (seeded SplitMix64 layer and hidden states)",
-           "config": config_dict(s, args.batch), "gpu_launches": moe.lib().moe_decode_kernels(dl.handle, args.batch) * args.steps,
+           "config": config_dict(s, args.batch, args.windows),
+           "gpu_launches": main["gpu_launches_per_step"] * args.steps * main["windows"],
+           "timing": {"windows": main["windows"], "steps_per_window": main["K"],
+                      "value_from": "median window", "spread_ms_per_step": main["spread_ms_per_step"],
+                      "spread_pct": main["spread_pct"]},
            "clocks": clk,
            "layer": {"gbs": main["layer_gbs"], "frac_of_8tbs": main["layer_frac_of_8tbs"],
                      "bytes_per_step": main["bytes_per_step"],
                      "distinct_experts": main["distinct_experts"]},
            "by_batch": {str(b): {k: v for k, v in r.items()} for b, r in results.items()}}
 
-    peaks = _peaks()
-    peak = peaks.get("hbm_gbs", 6800.0)
-    peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
-
     if not args.no_extras:
-        # per-kernel durations: events between the three kernels (no PDL overlap)
         B = args.batch
-        evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
-        for e in evs:               # torch creates the CUDA event on its first record
-            e.record(stream)
-        torch.cuda.synchronize()
-        moe.moe_set_profile_events(dl.handle, [e.cuda_event for e in evs])
-        Kp = min(args.steps, 200)
-        sums = [0.0, 0.0, 0.0]
-        x, outs = main["x"], main["outs"]
-        with torch.cuda.stream(stream):
-            for i in range(Kp + 5):
-                dl.decode(x[i % args.pool], outs, stream.cuda_stream)
-                evs[3].synchronize()
-                if i >= 5:
-                    for j in range(3):
-                        sums[j] += evs[j].elapsed_time(evs[j + 1])
-        moe.moe_set_profile_events(dl.handle, None)
-        per = [v / Kp for v in sums]
-        # one token runs the router, then one fused gate|up + down kernel
-        # (the second interval holds it, the third is empty)
-        fused = B == 1 and per[2] < 0.1 * per[1]
-        key = "fused" if fused else "gateup"
-        achieved = main["nbytes"][key] / (per[1] / 1e3) / 1e9
-        kname = "ffn_b1_kernel" if fused else ("gateup_b1_kernel" if B == 1 else "gateup_kernel")
-        out["roofline"] = {"bound": "hbm", "kernel": kname, "achieved": achieved,
-                           "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+        kern = main["kernel"]
+        fused = kern["name"] in ("ffn_b1_kernel", "ffn_bt_kernel")
+        out["roofline"] = {"bound": "hbm", "kernel": kern["name"], "achieved": kern["achieved_gbs"],
+                           "peak": peak, "unit": "GB/s", "frac": kern["achieved_gbs"] / peak,
                            "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)",
-                           "traffic": read_traffic() if fused else None,
-                           "algorithmic_bytes_per_launch": main["nbytes"][key],
-                           "kernel_ms": ({"router": per[0], "ffn": per[1]} if fused else
-                                         {"router": per[0], "gateup": per[1], "down": per[2]})}
+                           "traffic": read_traffic() if fused and B == 1 else None,
+                           "algorithmic_bytes_per_launch": kern["algorithmic_bytes_per_launch"],
+                           "kernel_ms": main["kernel_ms"]}
+        x, outs = main["x"], main["outs"]
 
         # end to end through the host-buffer entry point
         xs = main["xs"]
@@ -563,15 +603,19 @@ def run_ours(args, world, rank, local):
                                 hids.data_ptr(), hw.data_ptr(), dl.ws.data_ptr(), dl.ws_bytes,
                                 stream.cuda_stream)
         dt = max_over_ranks(world, time.perf_counter() - t0, device)
+        r256 = lambda v: (v + 255) // 256 * 256
         out["e2e"] = {"value": B * Ke * world / dt, "unit": "tokens/s",
                       "h2d_bytes_per_step": B * s.H * 2,
-                      "d2h_bytes_per_step": B * s.H * 2 + B * s.k * 8, "steps": Ke,
-                      "entry": "moe_decode_host (pinned host buffers, copies + sync per step)"}
+                      # one copy of the staged bf16 output, ids and weights (256-byte carve)
+                      "d2h_bytes_per_step": r256(B * s.H * 2) + r256(B * s.k * 4) + B * s.k * 4, "steps": Ke,
+                      "entry": "moe_decode_host (pinned host buffers, one copy in, one copy out, "
+                               "sync per step)"}
 
         if rank == 0 and world == 1:
             out["cpu_baseline"] = cpu_baseline(wl, s)
     dl.close()
     if not args.no_extras:
+        out["mid_decode"] = run_mid_decode(args, device, stream, peak, world)
         out["prefill"] = run_prefill(args, device, stream, peak, peaks.get("bf16_tflops", 1900.0))
         out["rvq"] = run_rvq(args, device, stream, peak)
     if args.streamed:
@@ -585,6 +629,71 @@ def _peaks() -> dict:
         return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
     except OSError:
         return {}
+
+
+MID_COPIES = 16  # layer copies the mid-decode leg rotates over
+
+
+def run_mid_decode(args, device, stream, hbm_peak, world):
+    """Decode on the mid layer (H=2048, E=128, top-8, F=768, Fs=2048) at
+    B = 1, 4 and 16.  One step reads ~28.6 MB at B=1, far less than L2 (129
+    MB), so consecutive steps rotate over MID_COPIES distinct copies of the
+    layer (synthetic layers 0..15, 3.6 GB): a copy comes back only after the
+    other fifteen steps have streamed ~430 MB (B=1) through L2, so each step
+    reads its weights from HBM.  Timed like the main leg (16-step graphs, one
+    step per copy, median of windows of K steps)."""
+    import torch
+
+    from quantized_routed_expert_gemv_gb300 import moe, synth
+    from quantized_routed_expert_gemv_gb300.device import DeviceLayer, bf16_tensor
+
+    wl = synth.WORKLOADS["mid-decode"]
+    s = wl.shape
+    dls = [DeviceLayer(s, wl.weight_seed, layer=l, max_tokens=16, device=device) for l in range(MID_COPIES)]
+    out = {"workload": f"mid-decode: H={s.H} E={s.E} top-{s.k} F={s.F} Fs={s.Fs}, {MID_COPIES} layer "
+                       "copies rotated step by step (each step reads HBM, not L2)"}
+    K = max(GRAPH_STEPS, min(args.steps, 1024) // GRAPH_STEPS * GRAPH_STEPS)
+    for B in (1, 4, 16):
+        npool = 2 * GRAPH_STEPS
+        x = bf16_tensor(np.stack([np.stack([synth.hidden(wl.input_seed, 3000 + p, t, s.H) for t in range(B)])
+                                  for p in range(npool)]), device)
+        outs = [d.outputs(B) for d in dls]
+        distinct = []
+        with torch.cuda.stream(stream):
+            for p in range(npool):
+                l = p % MID_COPIES
+                dls[l].decode(x[p], outs[l], stream.cuda_stream)
+                stream.synchronize()
+                distinct.append(len(np.unique(outs[l][2].cpu().numpy())))
+        chunks = []
+        for c0 in range(0, npool, GRAPH_STEPS):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for p in range(c0, c0 + GRAPH_STEPS):
+                    l = p % MID_COPIES
+                    dls[l].decode(x[p], outs[l], stream.cuda_stream)
+            chunks.append(g)
+        torch.cuda.synchronize()
+        ms_list, _, _ = time_graphs(torch, chunks, chunks, K, max(args.warmup, 3), stream, world, device,
+                                    min(args.windows, 3))
+        for d in dls:
+            assert d.check(stream.cuda_stream) == moe.MOE_OK, moe.last_error()
+        st = window_stats(ms_list, K)
+        d = float(np.mean(distinct))
+        nb = layer_step_bytes(s, B, d, with_f32=True)
+        per = kernel_times(torch, moe, dls[0], x, outs[0], stream, npool, n=50)
+        kb = nb["fused"]
+        out[str(B)] = {"tokens_per_s": B * world / (st["ms_per_step"] / 1e3), "ms_per_step": st["ms_per_step"],
+                       "spread_pct": st["spread_pct"], "distinct_experts": d, "bytes_per_step": nb["step"],
+                       "layer_gbs": nb["step"] / (st["ms_per_step"] / 1e3) / 1e9,
+                       "gpu_launches_per_step": moe.lib().moe_decode_kernels(dls[0].handle, B),
+                       "kernel_ms": per, "fused_kernel_gbs": kb / (per[1] / 1e3) / 1e9,
+                       "fused_kernel_frac_of_measured_hbm": kb / (per[1] / 1e3) / 1e9 / hbm_peak}
+        out[str(B)]["layer_frac_of_8tbs"] = out[str(B)]["layer_gbs"] / NOMINAL_HBM_GBS
+        del chunks
+    for d in dls:
+        d.close()
+    return out
 
 
 def run_prefill(args, device, stream, hbm_peak, bf16_peak):
@@ -620,7 +729,8 @@ def run_prefill(args, device, stream, hbm_peak, bf16_peak):
             dl.prefill(xs[p], outs, stream.cuda_stream)
         graphs.append(g)
     K = min(args.steps, 200)
-    ms, _, _ = time_graphs(torch, graphs, [], K, args.warmup, stream, 1, device)
+    ms_list, _, _ = time_graphs(torch, graphs, [], K, args.warmup, stream, 1, device, min(args.windows, 3))
+    ms = window_stats(ms_list, K)["ms_per_step"] * K
     assert dl.check(stream.cuda_stream) == moe.MOE_OK, moe.last_error()
     d = float(np.mean(distinct))
     rec = record_bytes_unpadded(s.H, s.F)
@@ -797,14 +907,34 @@ def run_streamed(args, device, stream, hbm_peak):
     chained_on = measure(xs_chain, True, "chained_on")
     for d in dls:
         d.close()
+    # the same layers with 3-bit residual-VQ expert records (same routers, so
+    # the same ids and cache counters; a miss copies 3 bits per weight)
+    dls.clear()
+    hosts.clear()
+    torch.cuda.synchronize()
+    for l in range(nl):
+        dls.append(DeviceLayer(s, wl.weight_seed, layer=l, beta=synth.beta_for(wl, l), max_tokens=1,
+                               device=device, resident=False, rvq=True))
+        hosts.append(pinned_records(s, wl.weight_seed, layer=l, rvq=True))
+    outs = [d.outputs(1) for d in dls]
+    hbm_bytes_4bit = hbm_bytes
+    rvq_bytes = lambda F: 3 * (3 * F * s.H // 8)
+    hbm_bytes = nl * steps * (s.k * rvq_bytes(s.F) + rvq_bytes(s.Fs) + s.E * s.H + s.E * (s.H // 64) * 4 +
+                              s.H * 8 + s.k * 8)
+    rvq_run = measure(xs_ind, False, "independent")
+    for d in dls:
+        d.close()
     del hosts
     res = {"workload": f"large-streamed: {nl} layers of H={s.H} E={s.E} top-{s.k} F={s.F} Fs={s.Fs}, "
                        f"{slots} HBM slots per layer, Zipf(1.1) router offsets, {steps} B=1 steps "
                        "from a cold cache",
-           "h2d_gbs_probed": bw, "hbm_bytes_per_token": hbm_bytes / steps}
+           "h2d_gbs_probed": bw, "hbm_bytes_per_token": hbm_bytes_4bit / steps}
     res.update(base)
     res["lookahead"] = {"inputs": f"hidden states chained across layers, rho={LOOKAHEAD_RHO}",
                         "n_ahead": LOOKAHEAD_N, "off": chained_off, "on": chained_on}
+    res["rvq_records"] = dict(rvq_run, records="3-bit residual-VQ experts (moe_rvq_record_layout_of), "
+                                               "independent inputs", 
+                              h2d_bytes_vs_4bit=rvq_run["bytes_h2d"] / max(1, base["bytes_h2d"]))
     return res
 
 
@@ -822,6 +952,8 @@ def run_rvq(args, device, stream, hbm_peak):
 
     wl = synth.WORKLOADS["large-decode"]
     s = wl.shape
+    if args.experts:
+        s = synth.Shape(s.H, args.experts, s.k, s.F, s.Fs)
     dl = DeviceLayer(s, wl.weight_seed, max_tokens=4, device=device, rvq=True)
     rvq_bytes = lambda F: 3 * (3 * F * s.H // 8)
     router = s.E * s.H + s.E * (s.H // 64) * 4

@@ -124,8 +124,9 @@ int moe_record_layout_of(int32_t hidden, int32_t ffn, moe_record_layout *out);
  *   [gate codes F x 3H/8][up codes F x 3H/8][down codes H x 3F/8]
  * row-major; a row holds its blocks of 8 inputs in order, each block 3 bytes
  * (the codeword index of stage 1, 2, 3).  The sb offsets equal `bytes` (no
- * scale/bias words); `stride` is `bytes` rounded up to 4096.  Decode only:
- * moe_prefill_chunk and the expert cache need wbits = 4. */
+ * scale/bias words); `stride` is `bytes` rounded up to 4096.  Decode and the
+ * expert cache (which copies these records); moe_prefill_chunk needs
+ * wbits = 4. */
 int moe_rvq_record_layout_of(int32_t hidden, int32_t ffn, moe_record_layout *out);
 
 /* Stride in bytes of one expert record of width `ffn` in desc's format
@@ -171,11 +172,17 @@ int moe_prefill_chunk(moe_layer *layer, const uint16_t *x, int32_t T, uint16_t *
 
 /* moe_decode with HOST buffers: copies x in, runs the step, copies every
  * output back (out_f32_host may be NULL) and synchronises `stream` before it
- * returns.  Device staging lives in the workspace; the outputs come back in
- * one device-to-host copy into a page-locked host buffer of the layer
- * (allocated by the layer's first moe_decode_host call, sized for
- * max_tokens, freed by moe_close), then are copied to the caller's buffers.
- * Calls on one layer from several threads are serialised by a lock. */
+ * returns.  Device staging lives in the workspace.  The layer keeps page-
+ * locked input and output buffers and a private stream (made by its first
+ * moe_decode_host call, sized for max_tokens, freed by moe_close): x goes
+ * through the input buffer, and the outputs come back in one device-to-
+ * host copy into the output buffer, then to the caller's buffers.  The
+ * first call for a given (workspace, B, out_f32_host set or not) runs plain
+ * launches and then captures the step (copy in, kernels, copy out) into a
+ * CUDA graph; later such calls replay it with one graph launch on `stream`
+ * (the layer keeps the last 4).  The profiling hook always takes plain
+ * launches.  Calls on one layer from several threads are serialised by a
+ * lock. */
 int moe_decode_host(moe_layer *layer, const uint16_t *x_host, int32_t B,
                     uint16_t *out_bf16_host, float *out_f32_host, int32_t *ids_host,
                     float *weights_host, void *workspace, size_t workspace_bytes,
@@ -262,8 +269,9 @@ size_t moe_residency_pool_bytes(const moe_layer *layer, int32_t n_slots);
  * storage, owned by the caller, written only by this cache.  n_slots in
  * [top_k, n_experts].  Allocates small pinned host buffers and a few
  * events, freed by moe_residency_close.  The layer may have been opened with
- * expert_records = NULL; it must hold wbits = 4 experts (MOE_ERR_ARG
- * otherwise). */
+ * expert_records = NULL.  A wbits = 3 layer's records are its residual-VQ
+ * records (moe_rvq_record_layout_of): a miss copies 3 bits per weight, and
+ * the codebooks stay resident with the router. */
 int moe_residency_open(moe_layer *layer, const void *host_records, int32_t n_slots,
                        void *device_pool, size_t device_pool_bytes, moe_residency **out);
 

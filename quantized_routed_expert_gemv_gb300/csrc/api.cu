@@ -66,11 +66,21 @@ struct moe_layer {
   cudaEvent_t prof[4];
   int prof_on;
   moe::LayerMaps maps;  // tiled-load descriptors of the code matrices (prefill)
-  // moe_decode_host: page-locked host buffer that the step's outputs land in
-  // with one copy (allocated by the first call, freed by moe_close)
+  // moe_decode_host: page-locked staging buffers for the inputs and the
+  // outputs (allocated by the first call, sized for max_tokens, freed by
+  // moe_close), a private stream and a few captured steps (copy in, kernels,
+  // copy out) replayed as CUDA graphs
   std::mutex* host_mu;
+  uint8_t* host_in;
   uint8_t* host_out;
   size_t host_out_bytes;
+  cudaStream_t host_st;
+  struct HostGraph {
+    void* ws;
+    int B, f32;
+    cudaGraphExec_t exec;
+  } hg[4];
+  int hg_next;
 };
 
 static bool aligned(const void* p, size_t a) {
@@ -252,6 +262,10 @@ extern "C" int moe_open(const moe_layer_desc* desc, const moe_layer_weights* w, 
 extern "C" void moe_close(moe_layer* L) {
   if (L && L->magic == kMagic) {
     L->magic = 0;
+    for (auto& g : L->hg)
+      if (g.exec) cudaGraphExecDestroy(g.exec);
+    if (L->host_st) cudaStreamDestroy(L->host_st);
+    if (L->host_in) cudaFreeHost(L->host_in);
     if (L->host_out) cudaFreeHost(L->host_out);
     delete L->host_mu;
     delete L;
@@ -294,12 +308,12 @@ static size_t carve(const moe_layer* L, int T, moe::Workspace* ws, uint8_t* base
   // Fixed-point h of the fused kernels, per 32-value chunk 64 bytes of words
   // and 4 group scales and sums (96 B): one token, a block per expert entry
   // (k routed rows of F, the shared row of Fs); few tokens, a block per
-  // (expert, token) pair.  The few-token buffers are sized for
+  // (expert, token) pair padded to 128-byte lines.  The few-token buffers are sized for
   // min(T, kBtMaxTokens) tokens, so a workspace for T serves every smaller
   // batch.
   const size_t tb = rvq ? 0 : std::min(t, static_cast<size_t>(moe::kBtMaxTokens));
-  const size_t hchunks = std::max(k * (F / 32) + Fs / 32, tb * (k * (F / 32) + Fs / 32));
-  const size_t o_hx = c.take(hchunks * 96);
+  const auto line128 = [](size_t v) { return (v + 127) / 128 * 128; };
+  const size_t o_hx = c.take(std::max((k * (F / 32) + Fs / 32) * 96, tb * (k * line128(3 * F) + line128(3 * Fs))));
   const size_t o_yp = c.take(std::max(k + 1, tb * (k + (Fs ? 1 : 0))) * H * 4);
   const size_t o_xq = c.take(tb * (H / 32) * 72);
   const size_t o_log = c.take(t * E * 4);
@@ -470,6 +484,47 @@ extern "C" int moe_prefill_chunk(moe_layer* L, const uint16_t* x, int32_t T, uin
              "moe_prefill_chunk");
 }
 
+// moe_decode_host's staging buffers and private stream, made once per layer.
+static int host_entry_setup(moe_layer* L, void* ws) {
+  if (L->host_out) return MOE_OK;
+  const size_t H = L->d.hidden, n = static_cast<size_t>(L->d.max_tokens);
+  moe::Workspace wm;
+  carve(L, L->d.max_tokens, &wm, static_cast<uint8_t*>(ws), nullptr);
+  const size_t out_bytes =
+      static_cast<size_t>(reinterpret_cast<uint8_t*>(wm.of_stage) - reinterpret_cast<uint8_t*>(wm.ob_stage)) +
+      n * H * 4;
+  void *pin = nullptr, *pout = nullptr;
+  cudaError_t e;
+  if ((e = cudaHostAlloc(&pin, n * H * 2, cudaHostAllocDefault)))
+    return cuda_fail(e, "moe_decode_host: page-locked input buffer");
+  if ((e = cudaHostAlloc(&pout, out_bytes, cudaHostAllocDefault))) {
+    cudaFreeHost(pin);
+    return cuda_fail(e, "moe_decode_host: page-locked output buffer");
+  }
+  if ((e = cudaStreamCreateWithFlags(&L->host_st, cudaStreamNonBlocking))) {
+    cudaFreeHost(pin), cudaFreeHost(pout);
+    L->host_st = nullptr;
+    return cuda_fail(e, "moe_decode_host: capture stream");
+  }
+  L->host_in = static_cast<uint8_t*>(pin), L->host_out = static_cast<uint8_t*>(pout), L->host_out_bytes = out_bytes;
+  return MOE_OK;
+}
+
+// Copy in, the step, copy out, on `st`, between the layer's staging buffers
+// and the workspace's.
+static int host_entry_step(moe_layer* L, int32_t B, bool f32, const moe::Workspace& w, void* ws, size_t ws_bytes,
+                           size_t span, cudaStream_t st) {
+  const size_t H = L->d.hidden;
+  cudaError_t e = cudaMemcpyAsync(w.x_stage, L->host_in, static_cast<size_t>(B) * H * 2, cudaMemcpyHostToDevice, st);
+  if (e) return cuda_fail(e, "moe_decode_host: copy in");
+  const int rc = moe_decode(L, w.x_stage, B, w.ob_stage, f32 ? w.of_stage : nullptr, w.ids_stage, w.w_stage, ws,
+                            ws_bytes, st);
+  if (rc) return rc;
+  if ((e = cudaMemcpyAsync(L->host_out, w.ob_stage, span, cudaMemcpyDeviceToHost, st)))
+    return cuda_fail(e, "moe_decode_host: copy out");
+  return MOE_OK;
+}
+
 extern "C" int moe_decode_host(moe_layer* L, const uint16_t* x_host, int32_t B, uint16_t* ob_host,
                                float* of_host, int32_t* ids_host, float* w_host, void* ws,
                                size_t ws_bytes, void* stream) {
@@ -491,34 +546,49 @@ extern "C" int moe_decode_host(moe_layer* L, const uint16_t* x_host, int32_t B, 
   const size_t o_ids = reinterpret_cast<uint8_t*>(w.ids_stage) - s0;
   const size_t o_w = reinterpret_cast<uint8_t*>(w.w_stage) - s0;
   const size_t o_f = reinterpret_cast<uint8_t*>(w.of_stage) - s0;
-  const size_t span = of_host ? o_f + b * H * 4 : o_w + b * k * 4;
+  const bool f32 = of_host != nullptr;
+  const size_t span = f32 ? o_f + b * H * 4 : o_w + b * k * 4;
   std::lock_guard<std::mutex> lock(*L->host_mu);
-  if (L->host_out_bytes < span) {
-    // sized for the largest call of the layer once, so later calls reuse it
-    moe::Workspace wm;
-    carve(L, L->d.max_tokens, &wm, static_cast<uint8_t*>(ws), nullptr);
-    const size_t full = static_cast<size_t>(reinterpret_cast<uint8_t*>(wm.of_stage) -
-                                            reinterpret_cast<uint8_t*>(wm.ob_stage)) +
-                        static_cast<size_t>(L->d.max_tokens) * H * 4;
-    const size_t cap = std::max(span, full);
-    if (L->host_out) cudaFreeHost(L->host_out), L->host_out = nullptr, L->host_out_bytes = 0;
-    void* p = nullptr;
-    cudaError_t e = cudaHostAlloc(&p, cap, cudaHostAllocDefault);
-    if (e) return cuda_fail(e, "moe_decode_host: page-locked output buffer");
-    L->host_out = static_cast<uint8_t*>(p), L->host_out_bytes = cap;
-  }
-  cudaError_t e = cudaMemcpyAsync(w.x_stage, x_host, b * H * 2, cudaMemcpyHostToDevice, st);
-  if (e) return cuda_fail(e, "moe_decode_host: copy in");
-  int rc = moe_decode(L, w.x_stage, B, w.ob_stage, of_host ? w.of_stage : nullptr, w.ids_stage, w.w_stage,
-                      ws, ws_bytes, stream);
+  int rc = host_entry_setup(L, ws);
   if (rc) return rc;
-  if ((e = cudaMemcpyAsync(L->host_out, s0, span, cudaMemcpyDeviceToHost, st)))
-    return cuda_fail(e, "moe_decode_host: copy out");
+  std::memcpy(L->host_in, x_host, b * H * 2);
+  // A step already captured for this workspace, batch and output set is
+  // replayed as one graph launch; otherwise the step runs as plain launches
+  // and is captured for the next call (every kernel has launched once by
+  // then).  The profiling hook always takes plain launches.
+  cudaGraphExec_t exec = nullptr;
+  if (!L->prof_on)
+    for (const auto& g : L->hg)
+      if (g.exec && g.ws == ws && g.B == B && g.f32 == (f32 ? 1 : 0)) exec = g.exec;
+  cudaError_t e;
+  if (exec) {
+    if ((e = cudaGraphLaunch(exec, st))) return cuda_fail(e, "moe_decode_host: graph launch");
+  } else {
+    if ((rc = host_entry_step(L, B, f32, w, ws, ws_bytes, span, st))) return rc;
+  }
   if ((e = cudaStreamSynchronize(st))) return cuda_fail(e, "moe_decode_host: synchronize");
   std::memcpy(ob_host, L->host_out, b * H * 2);
   std::memcpy(ids_host, L->host_out + o_ids, b * k * 4);
   std::memcpy(w_host, L->host_out + o_w, b * k * 4);
-  if (of_host) std::memcpy(of_host, L->host_out + o_f, b * H * 4);
+  if (f32) std::memcpy(of_host, L->host_out + o_f, b * H * 4);
+  if (!exec && !L->prof_on) {
+    // capture this step on the private stream; a failed capture only means
+    // later calls keep the plain launches
+    cudaGraph_t graph = nullptr;
+    cudaGraphExec_t ge = nullptr;
+    if (cudaStreamBeginCapture(L->host_st, cudaStreamCaptureModeThreadLocal) == cudaSuccess) {
+      const int crc = host_entry_step(L, B, f32, w, ws, ws_bytes, span, L->host_st);
+      const cudaError_t ce = cudaStreamEndCapture(L->host_st, &graph);
+      if (crc == MOE_OK && ce == cudaSuccess && graph && cudaGraphInstantiate(&ge, graph, 0) == cudaSuccess) {
+        auto& slot = L->hg[L->hg_next];
+        if (slot.exec) cudaGraphExecDestroy(slot.exec);
+        slot.ws = ws, slot.B = B, slot.f32 = f32 ? 1 : 0, slot.exec = ge;
+        L->hg_next = (L->hg_next + 1) % 4;
+      }
+      if (graph) cudaGraphDestroy(graph);
+    }
+    cudaGetLastError();  // a capture that failed leaves no sticky error behind
+  }
   return MOE_OK;
 }
 
@@ -594,7 +664,8 @@ int prepare_cached_decode(moe_layer* L, const uint16_t* x, int32_t B, uint16_t* 
   if (rc || B == 0) return rc;
   a->records = pool, a->slot_of = slot_of, a->slot_tag = slot_tag, a->n_slots = n_slots;
   a->prof_on = 0;
-  *single = B == 1 && plan_b1(*a, L->num_sms, L->smem_optin);
+  // residual-VQ layers run their own kernels (never the single-token split)
+  *single = L->d.wbits == 4 && B == 1 && plan_b1(*a, L->num_sms, L->smem_optin);
   *num_sms = L->num_sms;
   return MOE_OK;
 }
@@ -606,7 +677,7 @@ int prepare_route(moe_layer* L, const uint16_t* x, int32_t B, int32_t* ids, floa
   int rc = prepare(L, x, B, nullptr, nullptr, ids, wts, ws, ws_bytes, Path::kRoute, false, a, name);
   if (rc || B == 0) return rc;
   a->prof_on = 0;
-  *single = B == 1 && plan_b1(*a, L->num_sms, L->smem_optin);
+  *single = L->d.wbits == 4 && B == 1 && plan_b1(*a, L->num_sms, L->smem_optin);
   *num_sms = L->num_sms;
   return MOE_OK;
 }

@@ -39,6 +39,7 @@ constexpr int kBtWarps = 16;                     // consumer warps
 constexpr int kBtThreads = (kBtWarps + 3) * 32;  // + producer + two epilogue warps
 constexpr int kBtMaxStages = 8;
 constexpr int kBtCombineThreads = 256;
+constexpr int kBtVals = 8;  // values an epilogue lane gathers before the stage is released
 
 struct BtEnt {         // one expert entry of the step, as the producer and the consumers use it
   const uint8_t* rec;  // record base
@@ -66,11 +67,15 @@ __host__ __device__ inline BtSmem bt_smem(int nst, int stage, int nt, int n_ent_
 
 // Pairs: the shared expert's token t is pair t (t < nsh = B when there is a
 // shared expert); the router's grouped pair position q is pair nsh + q.
-// Pair P's fixed-point h block starts at chunk bt_c0(P) of the workspace's
-// h area: shared blocks of Fs/32 chunks first, then routed blocks of F/32.
-__device__ __forceinline__ int bt_c0(int P, int nsh, int Fs, int F) {
-  return P < nsh ? P * (Fs >> 5) : nsh * (Fs >> 5) + (P - nsh) * (F >> 5);
+// Pair P's fixed-point h block (96 bytes per 32-value chunk) starts at byte
+// bt_hoff(P) of the workspace's h area: shared blocks first, then routed
+// ones, each padded to whole 128-byte lines.
+__host__ __device__ inline size_t bt_hblock(int Fe) { return (static_cast<size_t>(3 * Fe) + 127) / 128 * 128; }
+__device__ __forceinline__ size_t bt_hoff(int P, int nsh, int Fs, int F) {
+  return P < nsh ? P * bt_hblock(Fs) : nsh * bt_hblock(Fs) + (P - nsh) * bt_hblock(F);
 }
+
+
 
 // Routing weight of pair P (1 for the shared expert's pairs).
 __device__ __forceinline__ float bt_weight(const LayerArgs& a, int P, int nsh) {
@@ -255,54 +260,73 @@ __global__ void __launch_bounds__(kBtThreads, 1) ffn_bt_kernel(const __grid_cons
       }
       const int code = s_code[s];
       if (code < 0) break;
-      if (!mbar_wait_sleep_warp(&pdone[s], ph)) {
-        if (lane == 0) latch_error(&a.ws.ctl[0], kErrTimeout);
-        break;
-      }
       const int gate = code & 1, e = code >> 20, tile = (code >> 1) & 0x7FFFF;
       const bool sh_row = has_sh && e == 0;
       const BtEnt en = tab[e];
       const int ntok = min(en.ntok, NT);
       const float* ws0 = wsum + static_cast<size_t>(s) * NT * NCW * 8;
-      if (gate) {
-        // per pair (token u of the entry) and item row j: SwiGLU of the
-        // gathered gate and up sums, published as fixed-point h groups (rth
-        // is a multiple of 8, so an 8-lane segment is one group of one pair)
-        const int Fe = sh_row ? a.Fs : a.F, nc = Fe >> 5, nv = ntok * rth;
-        for (int v0 = 0; v0 < nv; v0 += 32) {
-          const int v = v0 + lane;
-          const bool act = v < nv;
-          const int u = act ? v / rth : 0, j = act ? v - u * rth : 0;
-          const int rlj = j / RH, mj = j % RH;
-          float g = 0.f, up = 0.f;
-          if (act)
-            for (int w = 0; w < WC; ++w) {
-              const float* p = ws0 + (u * NCW + rlj * WC + w) * 8;
-              g += p[mj];
-              up += p[RH + mj];
-            }
-          publish_hgroup(a, bt_c0(en.pair0 + u, nsh, a.Fs, a.F), nc, tile * rth + j, silu1(g) * up, act, lane);
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
-        if (lane == 0) red_add_release_gpu(&a.ws.hcnt[e], 1u);
-      } else {
-        // per pair and item row: the weighted row sum, to the pair's row of ypart
-        const D1Geo& g = sh_row ? gs : gr;
-        const int nv = ntok * RTD;
-        for (int v0 = 0; v0 < nv; v0 += 32) {
-          const int v = v0 + lane;
+      // Lane u < ntok holds the routing weight of the item's pair u, loaded
+      // before the wait for the consumers' sums so its latency is hidden.
+      const float pw = (!gate && lane < ntok) ? bt_weight(a, en.pair0 + lane, nsh) : 1.f;
+      if (!mbar_wait_sleep_warp(&pdone[s], ph)) {
+        if (lane == 0) latch_error(&a.ws.ctl[0], kErrTimeout);
+        break;
+      }
+      // The values of the item (pair u, row) are gathered from the stage's
+      // row sums kBtVals per lane at a time; the stage is released as soon
+      // as the last round is gathered, and the stores follow.
+      const int rows = gate ? rth : RTD, nv = ntok * rows;
+      const D1Geo& g = sh_row ? gs : gr;
+      for (int r0 = 0; r0 < nv; r0 += 32 * kBtVals) {
+        float val[kBtVals];
+#pragma unroll
+        for (int i = 0; i < kBtVals; ++i) {
+          const int v = r0 + i * 32 + lane;
+          val[i] = 0.f;
           if (v < nv) {
-            const int u = v / RTD, r = v - u * RTD;
-            const int rl = r % g.NRL, m = r / g.NRL;
-            float y = 0.f;
-            for (int w = 0; w < g.WC; ++w) y += ws0[(u * NCW + rl * g.WC + w) * 8 + m];
-            const int P = en.pair0 + u;
-            a.ws.ypart[static_cast<size_t>(P) * H + static_cast<size_t>(tile) * RTD + r] = bt_weight(a, P, nsh) * y;
+            const int u = v / rows, r = v - u * rows;
+            if (gate) {
+              // SwiGLU of the gathered gate and up sums of row r
+              const int rlj = r / RH, mj = r % RH;
+              float gg = 0.f, up = 0.f;
+              for (int w = 0; w < WC; ++w) {
+                const float* p = ws0 + (u * NCW + rlj * WC + w) * 8;
+                gg += p[mj];
+                up += p[RH + mj];
+              }
+              val[i] = silu1(gg) * up;
+            } else {
+              const int rl = r % g.NRL, m = r / g.NRL;
+              float y = 0.f;
+              for (int w = 0; w < g.WC; ++w) y += ws0[(u * NCW + rl * g.WC + w) * 8 + m];
+              val[i] = y;
+            }
           }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
+        if (r0 + 32 * kBtVals >= nv && lane == 0) mbar_arrive(&empty[s]);  // the stage is free
+#pragma unroll
+        for (int i = 0; i < kBtVals; ++i) {
+          const int v0 = r0 + i * 32;
+          if (v0 >= nv) break;  // the same on every lane
+          const int v = v0 + lane;
+          const bool act = v < nv;
+          const int u = act ? v / rows : 0, r = act ? v - u * rows : 0;
+          if (gate) {
+            // fixed-point h groups (rth is a multiple of 8, so an 8-lane
+            // segment is one group of one pair)
+            publish_hgroup_at(a.ws.hx + bt_hoff(en.pair0 + u, nsh, a.Fs, a.F), (sh_row ? a.Fs : a.F) >> 5,
+                              tile * rth + r, val[i], act, lane);
+          } else {
+            const float p = __shfl_sync(kAll, pw, u);
+            if (act)
+              a.ws.ypart[static_cast<size_t>(en.pair0 + u) * H + static_cast<size_t>(tile) * RTD + r] = p * val[i];
+          }
+        }
+      }
+      if (gate) {
+        __syncwarp();
+        if (lane == 0) red_add_release_gpu(&a.ws.hcnt[e], 1u);
       }
     }
     return;
@@ -313,7 +337,7 @@ __global__ void __launch_bounds__(kBtThreads, 1) ffn_bt_kernel(const __grid_cons
   const bool gact = warp < NAW && col < C;  // this lane's column of a gate|up item
   const D1Geo gs = d1_geo(has_sh ? a.Fs : a.F, warp, lane), gr = d1_geo(a.F, warp, lane);
   // the router's fixed-point activations: words [T][4][C] uint4, then [T][C]
-  // (2^e, plain sum of the chunk)
+  // (2^e, plain sum of the chunk), read from L2 like the h blocks
   const uint4* xqw = reinterpret_cast<const uint4*>(a.ws.xq);
   const float2* xqs = reinterpret_cast<const float2*>(a.ws.xq + static_cast<size_t>(T) * C * 64);
   bool xready = false, abort = false;
@@ -383,7 +407,7 @@ __global__ void __launch_bounds__(kBtThreads, 1) ffn_bt_kernel(const __grid_cons
 #pragma unroll
         for (int m = 0; m < 8; ++m) part[m] = 0.f;
         if (g.act) {
-          const uint8_t* xb = a.ws.hx + static_cast<size_t>(bt_c0(en.pair0 + u, nsh, a.Fs, a.F)) * 96;
+          const uint8_t* xb = a.ws.hx + bt_hoff(en.pair0 + u, nsh, a.Fs, a.F);
           const uint4* xw = reinterpret_cast<const uint4*>(xb);
           XChunk Xh;
           const uint4 g0 = __ldcg(xw + 0 * nc + g.col), g1 = __ldcg(xw + 1 * nc + g.col),

@@ -110,8 +110,9 @@ __device__ __forceinline__ B1Entry b1_entry(const LayerArgs& a, int idx, int has
 // bytes, 2 and 3: the same for the odd elements) of group i of chunk c sits
 // at 32-bit word (K * nc + c) * 4 + i; the group's 2^e at float
 // 16 * nc + c * 4 + i and its plain sum at float 20 * nc + c * 4 + i.
-__device__ __forceinline__ void publish_hgroup(const LayerArgs& a, int c0, int nc, int f, float v, bool act,
-                                               int lane) {
+// publish_hgroup into the block that starts at blk_base (the chunk layout
+// above, any 16-byte aligned start).
+__device__ __forceinline__ void publish_hgroup_at(uint8_t* blk_base, int nc, int f, float v, bool act, int lane) {
   float amax = fabsf(v), sum = v;
 #pragma unroll
   for (int o = 4; o > 0; o >>= 1) {
@@ -136,7 +137,7 @@ __device__ __forceinline__ void publish_hgroup(const LayerArgs& a, int c0, int n
   }
   if (act && p < 4) {
     const int c = f >> 5, i = (f >> 3) & 3;
-    uint32_t* blk = reinterpret_cast<uint32_t*>(a.ws.hx + static_cast<size_t>(c0) * 96);
+    uint32_t* blk = reinterpret_cast<uint32_t*>(blk_base);
     blk[(p * nc + c) * 4 + i] = pack4(byte[0], byte[1], byte[2], byte[3]);
     if (p == 0) {
       float* f = reinterpret_cast<float*>(blk);
@@ -144,6 +145,11 @@ __device__ __forceinline__ void publish_hgroup(const LayerArgs& a, int c0, int n
       f[20 * nc + c * 4 + i] = sum;
     }
   }
+}
+
+__device__ __forceinline__ void publish_hgroup(const LayerArgs& a, int c0, int nc, int f, float v, bool act,
+                                               int lane) {
+  publish_hgroup_at(a.ws.hx + static_cast<size_t>(c0) * 96, nc, f, v, act, lane);
 }
 
 struct D1Geo {  // thread mapping for one expert width

@@ -63,6 +63,10 @@ constexpr unsigned kAllLanes = 0xFFFFFFFFu;
 constexpr int kBlkTokens = 64;     // tokens per block (N of the MMA <= 64)
 
 __host__ __device__ inline int round16(int v) { return (v + 15) & ~15; }
+// Chunks of 128 K whose accumulators share one 128-column TMEM buffer before
+// the epilogue drains it: each chunk adds two 64-K groups of np columns, so
+// blocks of up to 16 tokens drain every 4 chunks, up to 32 every 2.
+__host__ __device__ inline int unit_chunks(int np) { return np <= 16 ? 4 : np <= 32 ? 2 : 1; }
 __host__ __device__ inline int blocks_of(int cnt) { return (cnt + kBlkTokens - 1) / kBlkTokens; }
 __host__ __device__ inline int rows_of(int cnt) {  // packed rows of an entry with cnt tokens
   return (cnt / kBlkTokens) * kBlkTokens + round16(cnt % kBlkTokens);
@@ -258,7 +262,7 @@ constexpr int kNSA = 4;                  // A stages (in TMEM)
 
 constexpr int kCodesStage = 128 * 64;    // 128 rows x 64 B (128 codes)
 constexpr int kACols = 64;               // TMEM columns of one A stage: 128 bf16 per row
-constexpr int kTmemBufs = 2;             // accumulator buffers: 2 groups x 64 columns each
+constexpr int kTmemBufs = 2;             // accumulator buffers of 128 columns each
 constexpr int kACol0 = kTmemBufs * 128;  // A stages follow the accumulators
 constexpr int kTmemCols = 512;
 static_assert(kACol0 + kNSA * kACols <= kTmemCols, "TMEM columns");
@@ -403,7 +407,8 @@ __global__ void __maxnreg__(168)
   uint64_t* tm_empty = tm_full + kTmemBufs;
   uint64_t* gs_full = tm_empty + kTmemBufs;
   uint64_t* gs_empty = gs_full + kNSG;
-  uint32_t* s_taddr = reinterpret_cast<uint32_t*>(gs_empty + kNSG);
+  uint64_t* mma_done = gs_empty + kNSG;  // an issuer's own MMAs complete (abort path)
+  uint32_t* s_taddr = reinterpret_cast<uint32_t*>(mma_done + kMmaWarps);
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_taddr + 1);
   unsigned* err = &a.ws.ctl[0];
 
@@ -412,7 +417,10 @@ __global__ void __maxnreg__(168)
     for (int i = 0; i < kNSC<MODE>; ++i) mbar_init(&codes_full[i], 1), mbar_init(&codes_empty[i], kDqWarps);
     for (int i = 0; i < kNSA; ++i) mbar_init(&a_full[i], kDqWarps), mbar_init(&a_empty[i], 1);
     for (int i = 0; i < kNSB<MODE>; ++i) mbar_init(&b_full[i], 1), mbar_init(&b_empty[i], 1);
-    for (int i = 0; i < kTmemBufs; ++i) mbar_init(&tm_full[i], 1), mbar_init(&tm_empty[i], kEpiWarps);
+    // tm_full: one commit from each MMA issuer per drain unit (an issuer
+    // alone in a unit commits twice)
+    for (int i = 0; i < kTmemBufs; ++i) mbar_init(&tm_full[i], kMmaWarps), mbar_init(&tm_empty[i], kEpiWarps);
+    for (int i = 0; i < kMmaWarps; ++i) mbar_init(&mma_done[i], 1);
     for (int i = 0; i < kNSG; ++i) mbar_init(&gs_full[i], 1), mbar_init(&gs_empty[i], kEpiWarps);
     *s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -570,63 +578,80 @@ __global__ void __maxnreg__(168)
     // ------------------------------------------------------------ MMA issue
     // Two issuing threads: one thread can issue a tcgen05.mma only every
     // ~50 cycles, two together about every 30.  Issuer mi takes the chunks
-    // with index % 2 == mi; both track every ring.
+    // with index % 2 == mi; both track every ring.  The accumulators of the
+    // chunks of one drain unit share a TMEM buffer: chunk j of the unit puts
+    // its groups at columns (2j + gi) * np.
     const int mi = warp - kMmaWarp;
     if (lane == 0) {
-      RingPos pa, pb, pt;
-      int cc = 0, last = -1;
+      RingPos pa, pb;
+      int cc = 0, units = 0;
       bool stop = false;
       for (int it = blockIdx.x; it < n_items && !stop; it += gridDim.x) {
         PgItem I;
         if (!pg_item<MODE>(a, it, nblk, nsb, I)) break;
-        const int np = I.blk.np;
+        const int np = I.blk.np, U = unit_chunks(np);
         const uint32_t idesc = idesc_bf16_f32(128, np);
-        for (int c = 0; c < I.nch; ++c, ++cc, pa.next(kNSA), pb.next(kNSB<MODE>), pt.next(kTmemBufs)) {
-          if ((cc % kMmaWarps) != mi) continue;
-          if (!pg_wait(&a_full[pa.s], pa.ph, s_abort, err) || !pg_wait(&b_full[pb.s], pb.ph, s_abort, err) ||
-              (cc >= kTmemBufs && !pg_wait(&tm_empty[pt.s], pt.ph ^ 1u, s_abort, err))) {
-            stop = true;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t a0 = taddr + kACol0 + pa.s * kACols, b0 = smem_u32(s_b + pb.s * L.bstage);
-          // descriptor of the chunk's first K step; each next step adds
-          // np * 32 bytes to the start address field (units of 16 bytes)
-          const uint64_t bd0 = smem_desc(b0, np * 16, 128), bstep = static_cast<uint64_t>(np * 2);
-          const uint64_t bd_lo = smem_desc(b0 + np * 256, np * 16, 128);
-#pragma unroll
-          for (int gi = 0; gi < 2; ++gi) {
-            const uint32_t d = taddr + pt.s * 128 + gi * 64;
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const int kq = gi * 4 + kk;  // K = 16 per MMA: 8 TMEM columns of A
-              mma_bf16_ta(d, a0 + kq * 8, bd0 + kq * bstep, idesc, kk > 0 ? 1u : 0u);
-              if (MODE == 1) mma_bf16_ta(d, a0 + kq * 8, bd_lo + kq * bstep, idesc, 1u);
+        for (int u0 = 0; u0 < I.nch && !stop; u0 += U, ++units) {
+          const int ue = min(u0 + U, I.nch), buf = units % kTmemBufs;
+          const uint32_t uph = (units / kTmemBufs) & 1;
+          int mine = 0, others = 0;
+          for (int c = u0; c < ue; ++c, ++cc, pa.next(kNSA), pb.next(kNSB<MODE>)) {
+            if ((cc % kMmaWarps) != mi) {
+              ++others;
+              continue;
             }
+            if ((mine == 0 && units >= kTmemBufs && !pg_wait(&tm_empty[buf], uph ^ 1u, s_abort, err)) ||
+                !pg_wait(&a_full[pa.s], pa.ph, s_abort, err) || !pg_wait(&b_full[pb.s], pb.ph, s_abort, err)) {
+              stop = true;
+              break;
+            }
+            ++mine;
+            tc_fence_after();
+            const uint32_t a0 = taddr + kACol0 + pa.s * kACols, b0 = smem_u32(s_b + pb.s * L.bstage);
+            // descriptor of the chunk's first K step; each next step adds
+            // np * 32 bytes to the start address field (units of 16 bytes)
+            const uint64_t bd0 = smem_desc(b0, np * 16, 128), bstep = static_cast<uint64_t>(np * 2);
+            const uint64_t bd_lo = smem_desc(b0 + np * 256, np * 16, 128);
+#pragma unroll
+            for (int gi = 0; gi < 2; ++gi) {
+              const uint32_t d = taddr + buf * 128 + (2 * (c - u0) + gi) * np;
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                const int kq = gi * 4 + kk;  // K = 16 per MMA: 8 TMEM columns of A
+                mma_bf16_ta(d, a0 + kq * 8, bd0 + kq * bstep, idesc, kk > 0 ? 1u : 0u);
+                if (MODE == 1) mma_bf16_ta(d, a0 + kq * 8, bd_lo + kq * bstep, idesc, 1u);
+              }
+            }
+            mma_commit(smem_u32(&a_empty[pa.s]));
+            mma_commit(smem_u32(&b_empty[pb.s]));
           }
-          mma_commit(smem_u32(&a_empty[pa.s]));
-          mma_commit(smem_u32(&b_empty[pb.s]));
-          mma_commit(smem_u32(&tm_full[pt.s]));
-          last = cc;
+          if (stop) break;
+          if (mine > 0) {
+            mma_commit(smem_u32(&tm_full[buf]));
+            if (others == 0) mma_commit(smem_u32(&tm_full[buf]));
+          }
         }
       }
       // Normally the epilogue has consumed every accumulator (so every MMA
       // completed) before the final barrier; after an abort, this issuer's
-      // last chunk lands before TMEM is released.
-      if (*s_abort && last >= 0 && !mbar_wait(&tm_full[last % kTmemBufs], (last / kTmemBufs) & 1))
-        latch_error(err, kErrTimeout);
+      // MMAs land before TMEM is released.
+      if (*s_abort) {
+        mma_commit(smem_u32(&mma_done[mi]));
+        if (!mbar_wait(&mma_done[mi], 0)) latch_error(err, kErrTimeout);
+      }
     }
     __syncwarp();
   } else if (warp < kEpiWarps) {
     // ------------------------------------------------------------ epilogue
     const int q = warp;              // TMEM lane quarter
     const int row = q * 32 + lane;   // TMEM lane = A row of the item
-    RingPos pt, pg;
+    RingPos pg;
+    int units = 0;
     bool stop = false;
     for (int it = blockIdx.x; it < n_items && !stop; it += gridDim.x) {
       PgItem I;
       if (!pg_item<MODE>(a, it, nblk, nsb, I)) break;
-      const int np = I.blk.np;
+      const int np = I.blk.np, U = unit_chunks(np);
       const int G = I.K / 64;
       // this row's scale/bias words (the next chunk's pair is loaded one chunk ahead)
       const uint32_t* sbrow;
@@ -640,45 +665,55 @@ __global__ void __maxnreg__(168)
 #pragma unroll
       for (int j = 0; j < kBlkTokens; ++j) acc[j] = 0.f;
       uint2 sb_next = __ldg(reinterpret_cast<const uint2*>(sbrow));
-      for (int c = 0; c < I.nch; ++c, pt.next(kTmemBufs), pg.next(kNSG)) {
-        const uint32_t sbw[2] = {sb_next.x, sb_next.y};
-        if (c + 1 < I.nch) sb_next = __ldg(reinterpret_cast<const uint2*>(sbrow + 2 * c + 2));
+      for (int u0 = 0; u0 < I.nch && !stop; u0 += U, ++units) {
+        const int ue = min(u0 + U, I.nch), buf = units % kTmemBufs;
+        const uint32_t uph = (units / kTmemBufs) & 1;
         // the epilogue warps decide together, so the barriers below stay uniform
-        const bool ok = pg_wait_warp(&tm_full[pt.s], pt.ph, s_abort, err) &&
-                        pg_wait_warp(&gs_full[pg.s], pg.ph, s_abort, err);
-        if (named_bar_or(2, kEpiWarps * 32, !ok)) {
+        if (named_bar_or(2, kEpiWarps * 32, !pg_wait_warp(&tm_full[buf], uph, s_abort, err))) {
           stop = true;
           break;
         }
-        tc_fence_after();
+        for (int c = u0; c < ue; ++c, pg.next(kNSG)) {
+          const uint32_t sbw[2] = {sb_next.x, sb_next.y};
+          if (c + 1 < I.nch) sb_next = __ldg(reinterpret_cast<const uint2*>(sbrow + 2 * c + 2));
+          if (named_bar_or(2, kEpiWarps * 32, !pg_wait_warp(&gs_full[pg.s], pg.ph, s_abort, err))) {
+            stop = true;
+            break;
+          }
+          tc_fence_after();
 #pragma unroll
-        for (int gi = 0; gi < 2; ++gi) {
-          const uint32_t base = taddr + (static_cast<uint32_t>(q * 32) << 16) + pt.s * 128 + gi * 64;
-          const float s = bf16lo(sbw[gi]), b = bf16hi(sbw[gi]);
-          const float* gs = s_gs + pg.s * 2 * kBlkTokens + gi * np;
+          for (int gi = 0; gi < 2; ++gi) {
+            const uint32_t base =
+                taddr + (static_cast<uint32_t>(q * 32) << 16) + buf * 128 + (2 * (c - u0) + gi) * np;
+            const float s = bf16lo(sbw[gi]), b = bf16hi(sbw[gi]);
+            const float* gs = s_gs + pg.s * 2 * kBlkTokens + gi * np;
 #pragma unroll
-          for (int p = 0; p < kBlkTokens / 16; ++p)  // 16 columns per TMEM round trip
-            if (p * 16 < np) {
-              uint32_t d0[8], d1[8];
-              tmem_ld8(base + p * 16, d0);
-              tmem_ld8(base + p * 16 + 8, d1);
-              tmem_wait();
-              const float4 x0 = *reinterpret_cast<const float4*>(gs + p * 16);
-              const float4 x1 = *reinterpret_cast<const float4*>(gs + p * 16 + 4);
-              const float4 x2 = *reinterpret_cast<const float4*>(gs + p * 16 + 8);
-              const float4 x3 = *reinterpret_cast<const float4*>(gs + p * 16 + 12);
-              const float xs[16] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w,
-                                    x2.x, x2.y, x2.z, x2.w, x3.x, x3.y, x3.z, x3.w};
+            for (int p = 0; p < kBlkTokens / 16; ++p)  // 16 columns per TMEM round trip
+              if (p * 16 < np) {
+                uint32_t d0[8], d1[8];
+                tmem_ld8(base + p * 16, d0);
+                tmem_ld8(base + p * 16 + 8, d1);
+                tmem_wait();
+                const float4 x0 = *reinterpret_cast<const float4*>(gs + p * 16);
+                const float4 x1 = *reinterpret_cast<const float4*>(gs + p * 16 + 4);
+                const float4 x2 = *reinterpret_cast<const float4*>(gs + p * 16 + 8);
+                const float4 x3 = *reinterpret_cast<const float4*>(gs + p * 16 + 12);
+                const float xs[16] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w,
+                                      x2.x, x2.y, x2.z, x2.w, x3.x, x3.y, x3.z, x3.w};
 #pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                acc[p * 16 + j] = fmaf(s, __uint_as_float(d0[j]), fmaf(b, xs[j], acc[p * 16 + j]));
-                acc[p * 16 + 8 + j] = fmaf(s, __uint_as_float(d1[j]), fmaf(b, xs[8 + j], acc[p * 16 + 8 + j]));
+                for (int j = 0; j < 8; ++j) {
+                  acc[p * 16 + j] = fmaf(s, __uint_as_float(d0[j]), fmaf(b, xs[j], acc[p * 16 + j]));
+                  acc[p * 16 + 8 + j] = fmaf(s, __uint_as_float(d1[j]), fmaf(b, xs[8 + j], acc[p * 16 + 8 + j]));
+                }
               }
-            }
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&gs_empty[pg.s]);
         }
+        if (stop) break;
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&tm_empty[pt.s]), mbar_arrive(&gs_empty[pg.s]);
+        if (lane == 0) mbar_arrive(&tm_empty[buf]);
       }
       if (stop) break;
       if (MODE == 0) {

@@ -76,6 +76,7 @@ cudaError_t launch_b1_shared(const LayerArgs& a, int num_sms, cudaStream_t st);
 cudaError_t launch_b1_routed(const LayerArgs& a, int num_sms, cudaStream_t st);
 cudaError_t launch_decode_router(const LayerArgs& a, int num_sms, cudaStream_t st);
 cudaError_t launch_decode_experts(const LayerArgs& a, int num_sms, cudaStream_t st);
+cudaError_t launch_rvq_experts(const LayerArgs& a, int num_sms, cudaStream_t st);
 }  // namespace moe
 
 namespace {
@@ -182,8 +183,7 @@ extern "C" int moe_residency_open(moe_layer* layer, const void* host_records, in
   if (!d) return moe::report_error(MOE_ERR_ARG, "moe_residency_open: invalid layer handle");
   if (n_slots < 1 || n_slots > d->n_experts)
     return moe::report_error(MOE_ERR_ARG, "moe_residency_open: n_slots must be in [1, n_experts]");
-  if (d->wbits != 4)
-    return moe::report_error(MOE_ERR_ARG, "moe_residency_open: the expert cache needs a wbits=4 layer");
+
   if (n_slots < d->top_k)
     return moe::report_error(MOE_ERR_ARG, "moe_residency_open: fewer slots than top_k: a step could never fit");
   if (!host_records || !device_pool)
@@ -428,7 +428,9 @@ extern "C" int moe_residency_decode(moe_residency* R, const uint16_t* x, int32_t
     return moe::report_cuda(e, "moe_residency_decode: slot tables");
   R->stats.steps += 1, R->stats.hits += hits, R->stats.misses += misses;
   R->stats.evictions += evictions, R->stats.bytes_h2d += bytes, R->stats.lookahead_hits += ahead_hits;
-  e = single ? moe::launch_b1_routed(a, num_sms, M) : moe::launch_decode_experts(a, num_sms, M);
+  e = single ? moe::launch_b1_routed(a, num_sms, M)
+      : a.cbs ? moe::launch_rvq_experts(a, num_sms, M)  // residual-VQ records
+              : moe::launch_decode_experts(a, num_sms, M);
   if (e || (e = cudaEventRecord(R->ev_done, M))) return moe::report_cuda(e, "moe_residency_decode: routed experts");
   return MOE_OK;
 }

@@ -81,7 +81,10 @@ RvqPlan rvq_plan(const LayerArgs& a, int num_sms) {
   return p;
 }
 
+// The table, then 256 floats (the down kernel's h slice; the gate|up
+// kernel's record pointers of the routed ranks and the shared expert).
 size_t rvq_table_smem() { return kTabFloats * sizeof(float) + 256 * sizeof(float); }
+static_assert((kMaxTopK + 1) * sizeof(void*) <= 256 * sizeof(float), "record table");
 
 __device__ __forceinline__ float rvq_silu(float g) { return g / (1.0f + expf(-g)); }
 
@@ -147,17 +150,18 @@ __device__ __forceinline__ void load_codes(const uint8_t* row0, size_t row_bytes
   }
 }
 
-// Per row of the batch: the sum of lane j's three table entries.
+// Per row of the batch: the sum of lane j's three table entries.  Entry
+// (stage s, code c) of the lane sits c * 128 bytes into the stage's 32 KB.
 __device__ __forceinline__ void lookup_batch(const CodeBatch& c, const float* __restrict__ T, int lane,
                                              float (&acc)[kBatch]) {
   const int sh = 8 * ((3 * lane) & 3);
-  const float* Tl = T + lane;
+  const char* Tl = reinterpret_cast<const char*>(T + lane);
 #pragma unroll
   for (int i = 0; i < kBatch; ++i) {
     const uint32_t q = __funnelshift_r(c.lo[i], c.hi[i], sh);
-    const float t0 = Tl[(0 * kCodes + (q & 0xFFu)) * kTB];
-    const float t1 = Tl[(1 * kCodes + ((q >> 8) & 0xFFu)) * kTB];
-    const float t2 = Tl[(2 * kCodes + ((q >> 16) & 0xFFu)) * kTB];
+    const float t0 = *reinterpret_cast<const float*>(Tl + ((q << 7) & 0x7F80u));
+    const float t1 = *reinterpret_cast<const float*>(Tl + (kCodes * kTB * 4) + ((q >> 1) & 0x7F80u));
+    const float t2 = *reinterpret_cast<const float*>(Tl + (2 * kCodes * kTB * 4) + ((q >> 9) & 0x7F80u));
     acc[i] = (t0 + t1) + t2;
   }
 }
@@ -182,13 +186,14 @@ __device__ __forceinline__ const uint8_t* rvq_routed_record(const LayerArgs& a, 
 // out(r) receives the row's partial sum.  The next batch's codes are loaded
 // while the current one is looked up.
 template <typename RowChunk, typename Out>
-__device__ __forceinline__ void stream_rows(int r0, int r1, size_t row_bytes, bool act, const float* T,
+__device__ __forceinline__ void stream_rows(int r0, int r1, size_t row_bytes, int nbytes, bool act, const float* T,
                                             RowChunk row_chunk, Out out) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int rb = r0 + warp * kBatch;
   if (rb >= r1) return;
   CodeBatch cur, nxt;
   load_codes(row_chunk(rb), row_bytes, lane, act, cur);
+  (void)nbytes;
   for (; rb < r1; rb += kRvqWarps * kBatch) {
     const int rn = rb + kRvqWarps * kBatch;
     if (rn < r1) load_codes(row_chunk(rn), row_bytes, lane, act, nxt);
@@ -224,22 +229,22 @@ __global__ void __launch_bounds__(kRvqThreads, 2) rvq_gateup_kernel(const __grid
     v[4] = bf16lo(w.z), v[5] = bf16hi(w.z), v[6] = bf16lo(w.w), v[7] = bf16hi(w.w);
   }
   build_table(reinterpret_cast<const uint4*>(a.cbs) + kind * kKindWords, v, act, T);
-  __syncthreads();
   pdl_wait();  // the router's ids (routed rows), and the previous step's readers of the partials
   const size_t row_bytes = static_cast<size_t>(a.H) / 8 * 3, o0 = static_cast<size_t>(s) * kTB * 3;
+  // this kind's matrix of every routed rank, and of the shared expert (rank k)
+  const uint8_t** mat = reinterpret_cast<const uint8_t**>(smem + kTabFloats);
+  if (threadIdx.x < a.k)
+    mat[threadIdx.x] = rvq_routed_record(a, t, threadIdx.x) + (kind ? a.off_r.up_codes : a.off_r.gate_codes) + o0;
+  if (threadIdx.x == a.k && a.Fs) mat[a.k] = a.shared + (kind ? a.off_s.up_codes : a.off_s.gate_codes) + o0;
+  __syncthreads();
   const int kF = a.k * a.F;
-  const size_t moff = kind ? a.off_r.up_codes : a.off_r.gate_codes;
-  const size_t soff = kind ? a.off_s.up_codes : a.off_s.gate_codes;
   float* part = (kind ? a.ws.rvq_u : a.ws.rvq_g) + (static_cast<size_t>(t) * pl.S + s) * pl.R;
   const int r0 = p * pl.rpp, r1 = min(pl.R, r0 + pl.rpp);
   stream_rows(
-      r0, r1, row_bytes, act, T,
+      r0, r1, row_bytes, 3 * nb, act, T,
       [&](int r) -> const uint8_t* {
-        if (r < kF) {
-          const int i = r / a.F, f = r - i * a.F;
-          return rvq_routed_record(a, t, i) + moff + static_cast<size_t>(f) * row_bytes + o0;
-        }
-        return a.shared + soff + static_cast<size_t>(r - kF) * row_bytes + o0;
+        const int i = r < kF ? r / a.F : a.k, f = r < kF ? r - i * a.F : r - kF;
+        return mat[i] + static_cast<size_t>(f) * row_bytes;
       },
       [&](int r, float val) { part[r] = val; });
 }
@@ -291,7 +296,7 @@ __global__ void __launch_bounds__(kRvqThreads, 2) rvq_down_kernel(const __grid_c
   float* y = a.ws.rvq_y + ((static_cast<size_t>(t) * (a.k + 1) + e) * pl.Sdm + sd) * a.H;
   const int r0 = p * pl.rpd, r1 = min(a.H, r0 + pl.rpd);
   stream_rows(
-      r0, r1, row_bytes, act, T, [&](int r) { return codes + static_cast<size_t>(r) * row_bytes; },
+      r0, r1, row_bytes, 3 * nb, act, T, [&](int r) { return codes + static_cast<size_t>(r) * row_bytes; },
       [&](int r, float val) { y[r] = val; });
 }
 
@@ -358,20 +363,29 @@ cudaError_t set_rvq_attributes(int smem_optin) {
   return e ? e : cudaFuncSetAttribute(rvq_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
-// The router, then gate|up, down and the combine for every token at once.
-// Profile events: before the router, before gate|up, before down, after the
-// combine.
-cudaError_t launch_decode_rvq(const LayerArgs& a, int num_sms, cudaStream_t st) {
+// gate|up, down and the combine for every token at once, after a router
+// launch of the same step (the expert cache runs them after its copies).
+cudaError_t launch_rvq_experts(const LayerArgs& a, int num_sms, cudaStream_t st) {
   const bool pdl = !a.prof_on;
   const RvqPlan pl = rvq_plan(a, num_sms);
   const int gu = a.T * 2 * pl.S * pl.P, dn = a.T * (a.k + 1) * pl.Sdm * pl.Pd;
   const int cb = cdiv(a.T * a.H, 256);
   cudaError_t e;
-  if ((e = mark_rvq(a, 0, st)) || (e = launch_decode_router(a, num_sms, st)) || (e = mark_rvq(a, 1, st)) ||
-      (e = launch_rvq((const void*)rvq_gateup_kernel, gu, kRvqThreads, rvq_table_smem(), st, pdl, a, pl)) ||
+  if ((e = launch_rvq((const void*)rvq_gateup_kernel, gu, kRvqThreads, rvq_table_smem(), st, pdl, a, pl)) ||
       (e = mark_rvq(a, 2, st)) ||
       (e = launch_rvq((const void*)rvq_down_kernel, dn, kRvqThreads, rvq_table_smem(), st, pdl, a, pl)) ||
       (e = launch_rvq((const void*)rvq_combine_kernel, cb, 256, 0, st, pdl, a, pl)))
+    return e;
+  return cudaSuccess;
+}
+
+// The router, then gate|up, down and the combine for every token at once.
+// Profile events: before the router, before gate|up, before down, after the
+// combine.
+cudaError_t launch_decode_rvq(const LayerArgs& a, int num_sms, cudaStream_t st) {
+  cudaError_t e;
+  if ((e = mark_rvq(a, 0, st)) || (e = launch_decode_router(a, num_sms, st)) || (e = mark_rvq(a, 1, st)) ||
+      (e = launch_rvq_experts(a, num_sms, st)))
     return e;
   return mark_rvq(a, 3, st);
 }

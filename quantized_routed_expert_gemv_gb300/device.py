@@ -118,14 +118,16 @@ class DeviceLayer:
 
 
 def pinned_records(shape: synth.Shape, weight_seed: int, layer: int = 0,
-                   host_records: np.ndarray | None = None) -> torch.Tensor:
-    """All E expert records of a layer in page-locked host memory."""
-    stride = synth.record_stride(shape.H, shape.F)
+                   host_records: np.ndarray | None = None, rvq: bool = False) -> torch.Tensor:
+    """All E expert records of a layer in page-locked host memory (3-bit
+    residual-VQ records when rvq)."""
+    stride = (synth.rvq_record_stride if rvq else synth.record_stride)(shape.H, shape.F)
     t = torch.empty(shape.E * stride, dtype=torch.uint8, pin_memory=True)
     if host_records is not None:
         t.copy_(torch.from_numpy(np.ascontiguousarray(host_records).reshape(-1)))
     else:
-        synth.fill_records(weight_seed, layer, range(shape.E), shape.H, shape.F, t.numpy())
+        fill = synth.fill_rvq_records if rvq else synth.fill_records
+        fill(weight_seed, layer, range(shape.E), shape.H, shape.F, t.numpy())
     return t
 
 

@@ -235,6 +235,30 @@ def test_deterministic_and_host_entry_matches():
     assert np.array_equal(ids, a[2]) and np.array_equal(w, a[3])
 
 
+@pytest.mark.parametrize("B,f32", [(1, False), (1, True), (3, False)])
+def test_host_entry_replays_match_device_entry(B, f32):
+    """moe_decode_host over several calls with changing inputs: the first call
+    runs plain launches and captures the step, later ones replay the graph;
+    every call's outputs equal moe_decode's on the same inputs."""
+    shape = synth.Shape(1024, 40, 6, 448, 320)
+    hl = HostLayer(shape, seed=29)
+    orc = hl.oracle()
+    dl = device_from_host(hl)
+    for rep in range(4):
+        xs = draw_tokens(orc, 29, 40 + rep, B)
+        ref = run(dl, xs)
+        ob = np.zeros((B, shape.H), np.uint16)
+        of = np.zeros((B, shape.H), np.float32)
+        ids = np.zeros((B, shape.k), np.int32)
+        w = np.zeros((B, shape.k), np.float32)
+        moe.moe_decode_host(dl.handle, xs.ctypes.data, B, ob.ctypes.data, of.ctypes.data if f32 else None,
+                            ids.ctypes.data, w.ctypes.data, dl.ws.data_ptr(), dl.ws_bytes, None)
+        assert np.array_equal(ob, ref[1]) and np.array_equal(ids, ref[2]) and np.array_equal(w, ref[3])
+        if f32:
+            assert np.array_equal(of, ref[0])
+    assert dl.check() == moe.MOE_OK, moe.last_error()
+
+
 # ---------------------------------------------------------------- workloads
 
 @pytest.fixture(scope="module")

@@ -6,7 +6,10 @@ codebooks.  moe_decode on such a layer is compared element by element with
 the fp64 oracle (oracle.c, orc_expert_rvq) on seeded layers from tiny to the
 mid shape, with ragged tile counts, no shared expert, k = E and k = 1; the
 identity-expert layer in this format must give its closed form; prefill
-chunks and the expert cache refuse the format.
+chunks refuse the format.  Through the HBM expert cache (WASTE page, section
+"Disk streaming mimarisi": the 3-bit records are what is streamed), Zipf
+streams at B = 1 and 4 keep counters and slots equal to the oracle's LFU
+replay, copy 3 bits per weight per miss, and give the oracle's outputs.
 """
 import numpy as np
 import pytest
@@ -15,7 +18,7 @@ import torch
 import oracle
 from layers import HostLayerRVQ, hidden_with_margin, identity_layer_rvq
 from quantized_routed_expert_gemv_gb300 import moe, synth
-from quantized_routed_expert_gemv_gb300.device import DeviceLayer, bf16_bits, bf16_tensor
+from quantized_routed_expert_gemv_gb300.device import CachedLayer, DeviceLayer, bf16_bits, bf16_tensor
 
 pytestmark = pytest.mark.gpu
 
@@ -88,17 +91,55 @@ def test_rvq_identity_expert_layer(T):
     dl.close()
 
 
-def test_rvq_refuses_prefill_and_the_cache():
+def test_rvq_refuses_prefill():
     hl = HostLayerRVQ(synth.TINY, seed=1)
     dl = device_rvq(hl, 4)
     x = bf16_tensor(np.stack([synth.hidden(1, 0, t, synth.TINY.H) for t in range(2)]), DEV)
     with pytest.raises(moe.MoEError) as ei:
         dl.prefill(x)
     assert ei.value.code == moe.MOE_ERR_ARG and "wbits=4" in str(ei.value)
-    nbytes = moe.moe_residency_pool_bytes(dl.handle, 4)
-    pool = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+    dl.close()
+
+
+def first_appearance(ids):
+    seen, order = set(), []
+    for e in np.asarray(ids).reshape(-1):
+        if int(e) not in seen:
+            seen.add(int(e))
+            order.append(int(e))
+    return np.array(order, np.int32)
+
+
+@pytest.mark.parametrize("B,steps,n_slots", [(1, 24, 8), (4, 10, 16)])
+def test_rvq_records_through_the_cache(B, steps, n_slots):
+    shape = synth.Shape(256, 64, 4, 128, 256)
+    beta = synth.beta_zipf(4, 0, 64)
+    hl = HostLayerRVQ(shape, seed=8, beta=beta)
+    orc = hl.oracle()
+    dl = DeviceLayer(shape, 0, beta=beta, max_tokens=B, device=DEV, host_records=hl.records,
+                     host_shared=hl.shared, router=(hl.router_codes, hl.router_sb), rvq=True,
+                     codebooks=hl.codebooks)
     host = torch.empty(hl.records.nbytes, dtype=torch.uint8, pin_memory=True)
-    with pytest.raises(moe.MoEError) as ei:
-        moe.moe_residency_open(dl.handle, host.data_ptr(), 4, pool.data_ptr(), nbytes)
-    assert ei.value.code == moe.MOE_ERR_ARG
+    host.copy_(torch.from_numpy(hl.records.reshape(-1)))
+    cl = CachedLayer(dl, host, n_slots)
+    lfu = oracle.LFU(n_slots, shape.E)
+    rec_bytes = oracle.rvq_layout(shape.H, shape.F)["bytes"]
+    for s in range(steps):
+        xs = np.stack([hidden_with_margin(orc, 19, s, t) for t in range(B)])
+        ob, of, ids, w = cl.decode(bf16_tensor(xs, DEV))
+        torch.cuda.synchronize()
+        assert dl.check() == moe.MOE_OK, moe.last_error()
+        ids = ids.cpu().numpy()
+        for t0, t1 in oracle.waves(ids, n_slots):
+            lfu.step(first_appearance(ids[t0:t1]))
+        st = cl.stats()
+        assert (st["hits"], st["misses"], st["evictions"]) == (lfu.hits, lfu.misses, lfu.evictions)
+        assert st["bytes_h2d"] == st["misses"] * rec_bytes
+        assert cl.slots() == list(lfu.slot_expert)
+        got = (of.cpu().numpy(), bf16_bits(ob), ids, w.cpu().numpy())
+        for t in range(B):
+            assert_token(t, *got, *orc.token(xs[t]))
+    st = cl.stats()
+    assert st["evictions"] > 0 and st["hits"] > 0
+    cl.close()
     dl.close()
