@@ -64,6 +64,12 @@ def parse_args():
                         "router lookahead); needs ~51 GB of host RAM")
     p.add_argument("--streamed-only", action="store_true",
                    help="only the streamed-cache workload, one JSON object")
+    p.add_argument("--mid-only", action="store_true",
+                   help="only the mid-decode leg (B=1/4/16 over rotated layer copies), one JSON object")
+    p.add_argument("--mid-batch", type=int, default=0,
+                   help="mid-decode leg at this one batch size only (0: B = 1, 4 and 16)")
+    p.add_argument("--copies", type=int, default=16,
+                   help="mid-decode layer copies rotated step by step (fewer for ncu captures only)")
     p.add_argument("--rvq-only", action="store_true",
                    help="only the residual-VQ expert decode (large shape, B=1 and 4), one JSON object")
     a = p.parse_args()
@@ -466,6 +472,12 @@ def run_ours(args, world, rank, local):
         if rank == 0:
             print(json.dumps({"rvq": res}), flush=True)
         return
+    if args.mid_only:
+        stream = torch.cuda.Stream(device)
+        res = run_mid_decode(args, device, stream, _peaks().get("hbm_gbs", 6800.0), world)
+        if rank == 0:
+            print(json.dumps({"mid_decode": res}), flush=True)
+        return
     if args.streamed_only:
         stream = torch.cuda.Stream(device)
         res = run_streamed(args, device, stream, _peaks().get("hbm_gbs", 6800.0))
@@ -631,17 +643,17 @@ def _peaks() -> dict:
         return {}
 
 
-MID_COPIES = 16  # layer copies the mid-decode leg rotates over
 
 
 def run_mid_decode(args, device, stream, hbm_peak, world):
     """Decode on the mid layer (H=2048, E=128, top-8, F=768, Fs=2048) at
     B = 1, 4 and 16.  One step reads ~28.6 MB at B=1, far less than L2 (129
-    MB), so consecutive steps rotate over MID_COPIES distinct copies of the
+    MB), so consecutive steps rotate over 16 distinct copies of the
     layer (synthetic layers 0..15, 3.6 GB): a copy comes back only after the
     other fifteen steps have streamed ~430 MB (B=1) through L2, so each step
     reads its weights from HBM.  Timed like the main leg (16-step graphs, one
-    step per copy, median of windows of K steps)."""
+    step per copy, median of windows of K steps).  `--copies` lowers the
+    copy count for small ncu captures."""
     import torch
 
     from quantized_routed_expert_gemv_gb300 import moe, synth
@@ -649,11 +661,12 @@ def run_mid_decode(args, device, stream, hbm_peak, world):
 
     wl = synth.WORKLOADS["mid-decode"]
     s = wl.shape
-    dls = [DeviceLayer(s, wl.weight_seed, layer=l, max_tokens=16, device=device) for l in range(MID_COPIES)]
-    out = {"workload": f"mid-decode: H={s.H} E={s.E} top-{s.k} F={s.F} Fs={s.Fs}, {MID_COPIES} layer "
+    n_copies = max(1, min(args.copies, 16))
+    dls = [DeviceLayer(s, wl.weight_seed, layer=l, max_tokens=16, device=device) for l in range(n_copies)]
+    out = {"workload": f"mid-decode: H={s.H} E={s.E} top-{s.k} F={s.F} Fs={s.Fs}, {n_copies} layer "
                        "copies rotated step by step (each step reads HBM, not L2)"}
     K = max(GRAPH_STEPS, min(args.steps, 1024) // GRAPH_STEPS * GRAPH_STEPS)
-    for B in (1, 4, 16):
+    for B in ((args.mid_batch,) if args.mid_batch else (1, 4, 16)):
         npool = 2 * GRAPH_STEPS
         x = bf16_tensor(np.stack([np.stack([synth.hidden(wl.input_seed, 3000 + p, t, s.H) for t in range(B)])
                                   for p in range(npool)]), device)
@@ -661,7 +674,7 @@ def run_mid_decode(args, device, stream, hbm_peak, world):
         distinct = []
         with torch.cuda.stream(stream):
             for p in range(npool):
-                l = p % MID_COPIES
+                l = p % n_copies
                 dls[l].decode(x[p], outs[l], stream.cuda_stream)
                 stream.synchronize()
                 distinct.append(len(np.unique(outs[l][2].cpu().numpy())))
@@ -670,7 +683,7 @@ def run_mid_decode(args, device, stream, hbm_peak, world):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
                 for p in range(c0, c0 + GRAPH_STEPS):
-                    l = p % MID_COPIES
+                    l = p % n_copies
                     dls[l].decode(x[p], outs[l], stream.cuda_stream)
             chunks.append(g)
         torch.cuda.synchronize()
