@@ -488,8 +488,11 @@ static int bt_nrl(int Fe) {
 // Geometry of the few-token kernel for a.T tokens: gate|up items of R rows
 // per thread (8, else 4), down items of RTD rows (a divisor of H, a multiple
 // of 4 and of both widths' row-lanes, at most 8 rows per thread), and the
-// deepest ring the shared memory holds.  Prefers the larger items while the
-// ring keeps three stages.  False when no plan keeps two stages.
+// deepest ring the shared memory holds.  Takes the largest items that keep a
+// ring of three stages (a ring of two leaves one stage of copies in flight
+// per SM, too little to cover HBM latency at this SM's share of the
+// bandwidth); a ring of two only when no plan keeps three.  False when no
+// plan keeps two stages.
 bool plan_bt(LayerArgs& a, int num_sms, int smem_optin) {
   (void)num_sms;
   if (a.T < 2 || a.T > kBtMaxTokens) return false;
@@ -499,7 +502,7 @@ bool plan_bt(LayerArgs& a, int num_sms, int smem_optin) {
   const int Fm = std::max(a.F, a.Fs), nr = bt_nrl(a.F), ns = a.Fs ? bt_nrl(a.Fs) : nr;
   const int nt = bt_nt(a.T), has_sh = a.Fs > 0 ? 1 : 0;
   const int budget = smem_optin - 1024;
-  int best_nst = 0;
+  int fb_R = 0, fb_rt = 0, fb_sb = 0, fb_nst = 0;  // the first two-stage plan
   for (int R = 8; R >= 4; R -= 4) {
     const int rth = (R / 2) * nrl;
     if (rth % 8 || rth > 64 || a.F % rth || (a.Fs && a.Fs % rth)) continue;
@@ -511,14 +514,16 @@ bool plan_bt(LayerArgs& a, int num_sms, int smem_optin) {
       const int fixed = bt_smem(0, sb, nt, has_sh + std::min(a.E, a.T * a.k), has_sh * a.T + a.T * a.k).total;
       const int per = bt_smem(1, sb, nt, 0, 0).total - bt_smem(0, sb, nt, 0, 0).total;
       const int nst = std::min(kBtMaxStages, (budget - fixed) / per);
-      if (nst < 2 || nst <= best_nst) continue;
-      best_nst = nst;
-      a.gu_nrl = nrl, a.gu_rows = R, a.f1_rt = rt, a.f1_stage = sb, a.f1_nst = nst;
-      break;  // the largest down item for this R
+      if (nst >= 3) {
+        a.gu_nrl = nrl, a.gu_rows = R, a.f1_rt = rt, a.f1_stage = sb, a.f1_nst = nst;
+        return true;
+      }
+      if (nst == 2 && fb_nst == 0) fb_R = R, fb_rt = rt, fb_sb = sb, fb_nst = 2;
     }
-    if (best_nst >= 3) break;
   }
-  return best_nst >= 2;
+  if (fb_nst < 2) return false;
+  a.gu_nrl = nrl, a.gu_rows = fb_R, a.f1_rt = fb_rt, a.f1_stage = fb_sb, a.f1_nst = fb_nst;
+  return true;
 }
 
 cudaError_t set_bt_attributes(int smem_optin) {
