@@ -1010,8 +1010,15 @@ def run_rvq(args, device, stream, hbm_peak):
         step_bytes = d * rvq_bytes(s.F) + rvq_bytes(s.Fs) + router + 3 * 3 * 256 * 8 * 2 + \
             B * s.H * (2 + 2 + 4) + B * s.k * 8
         gbs = step_bytes / (ms / 1e3) / 1e9
+        # per kernel (events between launches, no programmatic dependent
+        # launch): the router, gate|up, then down + combine
+        per = kernel_times(torch, moe, dl, x, outs, stream, pool, n=50)
+        pair_bytes = B * s.k * rvq_bytes(s.F) + B * rvq_bytes(s.Fs)  # each token reads its own experts
         out[str(B)] = {"tokens_per_s": B / (ms / 1e3), "ms_per_step": ms, "distinct_experts": d,
-                       "bytes_per_step": step_bytes, "gbs": gbs, "frac_of_measured_hbm": gbs / hbm_peak}
+                       "bytes_per_step": step_bytes, "gbs": gbs, "frac_of_measured_hbm": gbs / hbm_peak,
+                       "kernel_ms": {"router": per[0], "gateup": per[1], "down_combine": per[2]},
+                       "expert_bytes_read": pair_bytes,
+                       "expert_gbs": pair_bytes / ((per[1] + per[2]) / 1e3) / 1e9}
         del chunks
     dl.close()
     return out

@@ -12,23 +12,31 @@
 // The page's method: the dot product of the input with every codeword is
 // tabulated once per block of 8 inputs, and each row then costs three table
 // lookups and their sum per block, with no weight rebuilt.  Here the input is
-// cut into slices of 32 blocks (256 inputs) and a CTA tabulates one slice of
-// one matrix kind, 96 KB of shared memory laid out [stage][code][block]:
-// the 32 blocks of one (stage, code) fill one 128-byte row of the 32 banks.
-// Lane j of a warp owns block j of the slice for every row, so its lookups
-// always hit bank j and a warp's 32 lookups are one conflict-free wavefront
-// whatever the codes are (with lanes owning rows instead, the code decides
-// the bank and a lookup costs about 3.15 wavefronts).  Each lane reads its
-// block's 3 code bytes of a row straight from global memory; a warp takes 8
-// rows at a time and sums each row over its lanes with one 8-row butterfly.
-// Partial sums per slice land in the workspace; later kernels add them in a
-// fixed order.  One launch of each kernel serves every token of the step:
-//   rvq_gateup_kernel   (token, kind, slice, row part): gate or up partial
-//                       sums of the token's routed experts and the shared
-//                       expert; the table is built before the wait for the
+// cut into slices of 64 blocks (512 inputs) and a CTA tabulates one slice of
+// one matrix kind: 192 KB of shared memory laid out [stage][code][block],
+// one 256-byte row per (stage, code).  Lane j owns two blocks of the slice
+// for every row, 2j and 2j + 1, and looks them up in turn: lanes 0-15 take
+// 2j first, lanes 16-31 2j + 1, so the first lookup of a warp hits the even
+// banks from its low half and the odd banks from its high half, the second
+// the other way round, and every lookup instruction is one conflict-free
+// wavefront whatever the codes are.  A lane's 6 code bytes of a row sit in
+// two aligned 32-bit words; one byte permute puts them in lookup order and
+// one more per lookup builds the table offset (stage << 16 | code << 8 |
+// 4 * block).  A warp takes 8 rows at a time and sums each row over its
+// lanes with one 8-row butterfly.  Partial sums per slice land in the
+// workspace; later kernels add them in a fixed order.
+//
+// Each kernel runs one CTA per SM over a flat list of 8-row batches of all
+// its units (a unit: one table, i.e. one token, matrix kind and slice), a
+// contiguous share of the list per CTA, so every SM gets the same number of
+// rows and builds at most a few tables.  One launch of each serves every
+// token of the step:
+//   rvq_gateup_kernel   units (token, kind, slice): gate or up partial sums of
+//                       the token's routed experts and the shared expert; the
+//                       CTA's first table is built before the wait for the
 //                       router, so it overlaps the router
-//   rvq_down_kernel     (token, entry, slice of F, row part): h of the slice
-//                       from the gate|up partials (SwiGLU), its table, then
+//   rvq_down_kernel     units (token, entry, slice of F): h of the slice from
+//                       the gate|up partials (SwiGLU), its table, then the
 //                       down partial sums
 //   rvq_combine_kernel  out = sum_i p_i y_i + y_shared, bf16 and f32
 #include <algorithm>
@@ -45,64 +53,87 @@ cudaError_t launch_decode_router(const LayerArgs& a, int num_sms, cudaStream_t s
 
 namespace {
 
-constexpr int kRvqThreads = 512;          // 16 warps
+constexpr int kRvqThreads = 512;            // 16 warps
 constexpr int kRvqWarps = kRvqThreads / 32;
-constexpr int kTB = 32;                   // blocks of 8 inputs per slice: one per lane
-constexpr int kCodes = 256;               // codewords per stage
-constexpr int kKindWords = 3 * kCodes;    // codewords of one matrix kind
-constexpr int kTabFloats = 3 * kCodes * kTB;  // one kind's table of a slice: [stage][code][block]
-constexpr int kBatch = 8;                 // rows a warp sums at once
+constexpr int kSB = 64;                     // blocks of 8 inputs per slice: two per lane
+constexpr int kCodes = 256;                 // codewords per stage
+constexpr int kKindWords = 3 * kCodes;      // codewords of one matrix kind
+constexpr int kRowBytes = kSB * 4;          // one (stage, code) row of the table
+constexpr int kTabBytes = 3 * kCodes * kRowBytes;  // 196,608: [stage][code][block]
+constexpr int kBatch = 8;                   // rows a warp sums at once
+constexpr int kChunkBytes = 3 * kSB;        // a row's code bytes of one slice
 
 // Launch geometry, the same on host and device.
 struct RvqPlan {
   int S;          // input slices of H (gate|up)
   int R;          // gate|up rows of one token: k F + Fs
-  int P, rpp;     // gate|up row parts per (token, kind, slice); rows per part (multiple of 8)
   int Sdr, Sds;   // down: slices of F and of Fs
   int Sdm;        // their maximum
-  int Pd, rpd;    // down row parts per (token, entry, slice); rows per part (multiple of 8)
+  int upt;        // down units of one token: k Sdr + Sds
+  long long gu_batches, dn_batches;  // 8-row batches of all units
+  int grid;       // CTAs of each kernel (one per SM)
 };
 
-int cdiv(int a, int b) { return (a + b - 1) / b; }
+__host__ __device__ inline int cdiv(int a, int b) { return (a + b - 1) / b; }
 
 RvqPlan rvq_plan(const LayerArgs& a, int num_sms) {
   RvqPlan p;
-  const int slots = 2 * num_sms;  // two CTAs per SM
   p.R = a.k * a.F + a.Fs;
-  p.S = cdiv(a.H / 8, kTB);
-  p.P = std::max(1, std::min(slots / (2 * a.T * p.S), cdiv(p.R, kRvqWarps * kBatch)));
-  p.rpp = cdiv(cdiv(p.R, p.P), kBatch) * kBatch;
-  p.Sdr = cdiv(a.F / 8, kTB);
-  p.Sds = a.Fs ? cdiv(a.Fs / 8, kTB) : 0;
+  p.S = cdiv(a.H / 8, kSB);
+  p.Sdr = cdiv(a.F / 8, kSB);
+  p.Sds = a.Fs ? cdiv(a.Fs / 8, kSB) : 0;
   p.Sdm = std::max(p.Sdr, p.Sds);
-  const int units = a.T * (a.k + (a.Fs ? 1 : 0)) * p.Sdm;
-  p.Pd = std::max(1, std::min(slots / units, cdiv(a.H, kRvqWarps * kBatch)));
-  p.rpd = cdiv(cdiv(a.H, p.Pd), kBatch) * kBatch;
+  p.upt = a.k * p.Sdr + p.Sds;
+  p.gu_batches = static_cast<long long>(a.T) * 2 * p.S * cdiv(p.R, kBatch);
+  p.dn_batches = static_cast<long long>(a.T) * p.upt * cdiv(a.H, kBatch);
+  p.grid = std::max(1, num_sms);
   return p;
 }
 
-// The table, then 256 floats (the down kernel's h slice; the gate|up
-// kernel's record pointers of the routed ranks and the shared expert).
-size_t rvq_table_smem() { return kTabFloats * sizeof(float) + 256 * sizeof(float); }
-static_assert((kMaxTopK + 1) * sizeof(void*) <= 256 * sizeof(float), "record table");
+// The table, then the matrix kind's codebooks (768 codewords, 12 KB), then
+// 2 KB: the down kernel's h slice (512 floats) or the gate|up kernel's record
+// pointers of the routed ranks and the shared expert.
+constexpr int kBookBytes = kKindWords * 16;
+size_t rvq_table_smem() { return kTabBytes + kBookBytes + 512 * sizeof(float); }
+static_assert((kMaxTopK + 1) * sizeof(void*) <= 512 * sizeof(float), "record table");
 
 __device__ __forceinline__ float rvq_silu(float g) { return g / (1.0f + expf(-g)); }
 
-// Lane j's entries T[stage][code][j] = <codeword(stage, code), v_j> of one
-// kind's codebooks (book: 768 codewords as uint4 of 8 bf16), v_j the lane's
-// 8 inputs; zero for lanes past the slice's nb blocks.  Warp w fills codes
-// w, w + 16, ...: the codeword is one broadcast load, each lane's store its
-// own bank.
-__device__ __forceinline__ void build_table(const uint4* __restrict__ book, const float (&v)[8], bool act,
-                                            float* __restrict__ T) {
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+// The same with a selector known at compile time (an immediate operand).
+template <uint32_t SEL>
+__device__ __forceinline__ uint32_t prmt_i(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "n"(SEL));
+  return d;
+}
+
+// The kind's 768 codewords (uint4 of 8 bf16 each) into shared memory, every
+// load of the CTA in flight at once; the caller synchronises before use.
+__device__ __forceinline__ void stage_book(const uint4* __restrict__ book, uint4* __restrict__ sbook) {
+  for (int q = threadIdx.x; q < kKindWords; q += kRvqThreads) sbook[q] = __ldg(book + q);
+}
+
+// Lane j's entries T[stage][code][2j], T[...][2j + 1] = <codeword(stage,
+// code), v_b> of one kind's codebooks (sbook: the 768 codewords in shared
+// memory), vA/vB the lane's two blocks of 8 inputs; zero for lanes past the
+// slice's nb blocks.  Warp w fills codewords w, w + 16, ...: the codeword is
+// one broadcast read, and the warp's 32 float2 stores fill one table row.
+__device__ __forceinline__ void build_table(const uint4* __restrict__ sbook, const float (&vA)[8],
+                                            const float (&vB)[8], bool act, uint8_t* __restrict__ T) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int q = warp; q < kKindWords; q += kRvqWarps) {
-    const uint4 w = __ldg(book + q);
-    float d = bf16lo(w.x) * v[0];
-    d = fmaf(bf16hi(w.x), v[1], d), d = fmaf(bf16lo(w.y), v[2], d), d = fmaf(bf16hi(w.y), v[3], d);
-    d = fmaf(bf16lo(w.z), v[4], d), d = fmaf(bf16hi(w.z), v[5], d), d = fmaf(bf16lo(w.w), v[6], d);
-    d = fmaf(bf16hi(w.w), v[7], d);
-    T[q * kTB + lane] = act ? d : 0.f;
+    const uint4 w = sbook[q];
+    const float c[8] = {bf16lo(w.x), bf16hi(w.x), bf16lo(w.y), bf16hi(w.y),
+                        bf16lo(w.z), bf16hi(w.z), bf16lo(w.w), bf16hi(w.w)};
+    float dA = c[0] * vA[0], dB = c[0] * vB[0];
+#pragma unroll
+    for (int m = 1; m < 8; ++m) dA = fmaf(c[m], vA[m], dA), dB = fmaf(c[m], vB[m], dB);
+    *reinterpret_cast<float2*>(T + q * kRowBytes + 8 * lane) = act ? make_float2(dA, dB) : make_float2(0.f, 0.f);
   }
 }
 
@@ -130,39 +161,76 @@ __device__ __forceinline__ float rvq_bfly8(const float (&p)[8], int lane) {
   return v;
 }
 
-// Lane j's 3 code bytes of block j of 8 rows, whose slice chunks start at
-// row0 + i * row_bytes (8-byte aligned): the aligned 32-bit word holding
-// byte 3j and, for lanes whose bytes cross into the next word (j mod 4 in
-// {1, 2}), that word too; both stay inside the 96-byte chunk.
-struct CodeBatch {
-  uint32_t lo[kBatch], hi[kBatch];
+// A lane's per-row constants.  Its 6 code bytes of a row (blocks 2j and
+// 2j + 1, 3 stage bytes each) start d = 6j mod 4 bytes into the aligned word
+// pair (w0, w1) at byte 4 * wo of the slice chunk.  sel_lo / sel_hi permute
+// them so that lo holds the first-looked-up block's 3 bytes and the other
+// block's first byte, hi the other block's last two; base[i] holds
+// stage << 16 | 4 * block for lookup i (first block's stages 0-2, then the
+// second block's).
+struct Lane {
+  int wo;
+  uint32_t sel_lo, sel_hi;
+  uint32_t base[6];
+  bool act;
 };
 
-__device__ __forceinline__ void load_codes(const uint8_t* row0, size_t row_bytes, int lane, bool act,
-                                           CodeBatch& c) {
-  const int w = (3 * lane) >> 2;
-  const bool two = ((lane & 3) == 1) || ((lane & 3) == 2);
+__device__ __forceinline__ Lane lane_consts(int lane, int nb) {
+  Lane L;
+  const int d = (6 * lane) & 3;
+  L.wo = (6 * lane) >> 2;
+  const bool hi16 = lane >= 16;
+  const int first = hi16 ? 2 * lane + 1 : 2 * lane, second = hi16 ? 2 * lane : 2 * lane + 1;
+  // bytes of block 2j: d .. d + 2; of block 2j + 1: d + 3 .. d + 5
+  const int f0 = hi16 ? d + 3 : d, s0 = hi16 ? d : d + 3;
+  L.sel_lo = static_cast<uint32_t>(f0 | (f0 + 1) << 4 | (f0 + 2) << 8 | s0 << 12);
+  L.sel_hi = static_cast<uint32_t>((s0 + 1) | (s0 + 2) << 4 | (s0 + 1) << 8 | (s0 + 1) << 12);
 #pragma unroll
-  for (int i = 0; i < kBatch; ++i) {
-    const uint32_t* p = reinterpret_cast<const uint32_t*>(row0 + i * row_bytes) + w;
-    c.lo[i] = act ? __ldg(p) : 0u;
-    c.hi[i] = (act && two) ? __ldg(p + 1) : 0u;
+  for (int st = 0; st < 3; ++st) {
+    L.base[st] = static_cast<uint32_t>(st << 16 | 4 * first);
+    L.base[3 + st] = static_cast<uint32_t>(st << 16 | 4 * second);
   }
+  L.act = 2 * lane < nb;
+  return L;
 }
 
-// Per row of the batch: the sum of lane j's three table entries.  Entry
-// (stage s, code c) of the lane sits c * 128 bytes into the stage's 32 KB.
-__device__ __forceinline__ void lookup_batch(const CodeBatch& c, const float* __restrict__ T, int lane,
-                                             float (&acc)[kBatch]) {
-  const int sh = 8 * ((3 * lane) & 3);
-  const char* Tl = reinterpret_cast<const char*>(T + lane);
+struct CodeBatch {
+  uint32_t w0[kBatch], w1[kBatch];
+};
+
+// Lane's code words of row i of a batch whose slice chunks start at row0 +
+// i * row_bytes.  Both words of a row go out together and through L1, so the
+// second one meets the first one's sectors on the SM.
+__device__ __forceinline__ void load_row(const uint8_t* row0, size_t row_bytes, const Lane& L, int i,
+                                         CodeBatch& c) {
+  const uint32_t* p = reinterpret_cast<const uint32_t*>(row0 + i * row_bytes) + L.wo;
+  c.w0[i] = L.act ? __ldca(p) : 0u;
+  c.w1[i] = L.act ? __ldca(p + 1) : 0u;
+}
+
+__device__ __forceinline__ void load_codes(const uint8_t* row0, size_t row_bytes, const Lane& L, CodeBatch& c) {
+#pragma unroll
+  for (int i = 0; i < kBatch; ++i) load_row(row0, row_bytes, L, i, c);
+}
+
+// Per row of the batch: the sum of the lane's six table entries.  Once a
+// row's words are used, the same registers take that row of the batch at
+// `next` (when there is one), so a warp keeps about two batches of code
+// loads in flight with one spare register set.
+__device__ __forceinline__ void lookup_batch(CodeBatch& c, const uint8_t* __restrict__ T, const Lane& L,
+                                             const uint8_t* next, size_t row_bytes, float (&acc)[kBatch]) {
 #pragma unroll
   for (int i = 0; i < kBatch; ++i) {
-    const uint32_t q = __funnelshift_r(c.lo[i], c.hi[i], sh);
-    const float t0 = *reinterpret_cast<const float*>(Tl + ((q << 7) & 0x7F80u));
-    const float t1 = *reinterpret_cast<const float*>(Tl + (kCodes * kTB * 4) + ((q >> 1) & 0x7F80u));
-    const float t2 = *reinterpret_cast<const float*>(Tl + (2 * kCodes * kTB * 4) + ((q >> 9) & 0x7F80u));
-    acc[i] = (t0 + t1) + t2;
+    const uint32_t lo = prmt(c.w0[i], c.w1[i], L.sel_lo), hi = prmt(c.w0[i], c.w1[i], L.sel_hi);
+    if (next) load_row(next, row_bytes, L, i, c);
+    // offset = stage << 16 | code << 8 | 4 * block: byte 0 and 2 from base, byte 1 the code
+    const float a0 = *reinterpret_cast<const float*>(T + prmt_i<0x7604u>(lo, L.base[0]));
+    const float a1 = *reinterpret_cast<const float*>(T + prmt_i<0x7614u>(lo, L.base[1]));
+    const float a2 = *reinterpret_cast<const float*>(T + prmt_i<0x7624u>(lo, L.base[2]));
+    const float b0 = *reinterpret_cast<const float*>(T + prmt_i<0x7634u>(lo, L.base[3]));
+    const float b1 = *reinterpret_cast<const float*>(T + prmt_i<0x7604u>(hi, L.base[4]));
+    const float b2 = *reinterpret_cast<const float*>(T + prmt_i<0x7614u>(hi, L.base[5]));
+    acc[i] = ((a0 + a1) + a2) + ((b0 + b1) + b2);
   }
 }
 
@@ -181,147 +249,241 @@ __device__ __forceinline__ const uint8_t* rvq_routed_record(const LayerArgs& a, 
   return a.records + static_cast<size_t>(slot) * a.off_r.stride;
 }
 
-// Rows [r0, r1) of the CTA's row part, warp w taking batches w, w + 16, ...
-// row_chunk(r) is row r's slice chunk (8 consecutive rows share a matrix);
-// out(r) receives the row's partial sum.  The next batch's codes are loaded
-// while the current one is looked up.
-template <typename RowChunk, typename Out>
-__device__ __forceinline__ void stream_rows(int r0, int r1, size_t row_bytes, int nbytes, bool act, const float* T,
-                                            RowChunk row_chunk, Out out) {
+// Batches [b0, b1) of a unit (rows 8 b .. 8 b + 7, clipped at nrows), warp
+// w taking b0 + w, b0 + w + 16, ...  Cur is a row cursor: at(b) places it on
+// batch b's first row, then next() steps it 16 batches on; ptr() is that
+// row's slice chunk (8 consecutive rows share a matrix).  out(r) receives
+// row r's partial sum.  Two register sets alternate: while one batch is
+// looked up its registers are refilled with the batch two ahead, and the
+// other set's loads (the next batch) are in flight.
+template <typename Cur, typename Out>
+__device__ __forceinline__ void stream_batches(long long b0, long long b1, int nrows, size_t row_bytes,
+                                               const Lane& L, const uint8_t* T, Cur cur, Out out) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  int rb = r0 + warp * kBatch;
-  if (rb >= r1) return;
-  CodeBatch cur, nxt;
-  load_codes(row_chunk(rb), row_bytes, lane, act, cur);
-  (void)nbytes;
-  for (; rb < r1; rb += kRvqWarps * kBatch) {
-    const int rn = rb + kRvqWarps * kBatch;
-    if (rn < r1) load_codes(row_chunk(rn), row_bytes, lane, act, nxt);
+  long long b = b0 + warp;
+  if (b >= b1) return;
+  constexpr int W = kRvqWarps;
+  CodeBatch A, B;
+  cur.at(static_cast<int>(b) * kBatch);
+  load_codes(cur.ptr(), row_bytes, L, A);
+  cur.next();
+  if (b + W < b1) load_codes(cur.ptr(), row_bytes, L, B);
+  cur.next();  // on batch b + 2W: the refill of the first set
+  auto one = [&](CodeBatch& c, long long bb) {
     float acc[kBatch];
-    lookup_batch(cur, T, lane, acc);
+    const uint8_t* next = bb + 2 * W < b1 ? cur.ptr() : nullptr;
+    lookup_batch(c, T, L, next, row_bytes, acc);
+    cur.next();
     const float v = rvq_bfly8(acc, lane);
-    if ((lane & 3) == 0 && rb + (lane >> 2) < r1) out(rb + (lane >> 2), v);
-    cur = nxt;
+    const int r = static_cast<int>(bb) * kBatch + (lane >> 2);
+    if ((lane & 3) == 0 && r < nrows) out(r, v);
+  };
+  for (;;) {
+    one(A, b);
+    if ((b += W) >= b1) break;
+    one(B, b);
+    if ((b += W) >= b1) break;
   }
 }
 
-// grid T * 2 * S * P: CTA (token, kind, slice, part), kind 0 gate, 1 up.
-// Partial sums to rvq_g (gate) / rvq_u (up) as [T][S][R].
-__global__ void __launch_bounds__(kRvqThreads, 2) rvq_gateup_kernel(const __grid_constant__ LayerArgs a,
+// Row cursor over the rows of one matrix (the down matrix of an entry).
+struct FlatCur {
+  const uint8_t* base;
+  size_t row_bytes;
+  int r;
+  __device__ __forceinline__ void at(int r0) { r = r0; }
+  __device__ __forceinline__ void next() { r += kRvqWarps * kBatch; }
+  __device__ __forceinline__ const uint8_t* ptr() const { return base + static_cast<size_t>(r) * row_bytes; }
+};
+
+// Row cursor over the gate (or up) rows of a token: k routed matrices of F
+// rows, then the shared expert's Fs rows (mat[i] the slice chunk of matrix
+// i's first row).  Steps without division once placed.
+struct GuCur {
+  const uint8_t* const* mat;
+  size_t row_bytes;
+  int k, F, Fs, i, f;
+  __device__ __forceinline__ void at(int r) {
+    i = r / F;
+    if (i > k) i = k;
+    f = r - i * F;
+    norm();
+  }
+  __device__ __forceinline__ void norm() {
+    while (i < k && f >= F) f -= F, ++i;
+  }
+  __device__ __forceinline__ void next() {
+    f += kRvqWarps * kBatch;
+    norm();
+  }
+  __device__ __forceinline__ const uint8_t* ptr() const {
+    // past the last row (no batch reads it): a valid address all the same
+    const int ii = i > k ? k : i, ff = (i == k && f >= Fs) ? 0 : f;
+    return mat[ii] + static_cast<size_t>(ff) * row_bytes;
+  }
+};
+
+// This CTA's share [lo, hi) of n batches over `grid` CTAs.
+__device__ __forceinline__ void cta_share(long long n, int grid, long long& lo, long long& hi) {
+  lo = n * blockIdx.x / grid;
+  hi = n * (blockIdx.x + 1) / grid;
+}
+
+// Units (token, kind, slice), kind 0 gate, 1 up, each cdiv(R, 8) batches of
+// the rows of the token's k routed experts then the shared expert.  Partial
+// sums to rvq_g (gate) / rvq_u (up) as [T][S][R].
+__global__ void __launch_bounds__(kRvqThreads, 1) rvq_gateup_kernel(const __grid_constant__ LayerArgs a,
                                                                     const RvqPlan pl) {
-  extern __shared__ __align__(16) float smem[];
-  float* T = smem;
-  int id = blockIdx.x;
-  const int p = id % pl.P;
-  id /= pl.P;
-  const int s = id % pl.S;
-  id /= pl.S;
-  const int kind = id & 1, t = id >> 1;
+  extern __shared__ __align__(16) uint8_t smem[];
+  uint8_t* T = smem;
+  uint4* sbook = reinterpret_cast<uint4*>(smem + kTabBytes);
+  const uint8_t** mat = reinterpret_cast<const uint8_t**>(smem + kTabBytes + kBookBytes);
   const int lane = threadIdx.x & 31;
-  const int b0 = s * kTB, nb = min(kTB, a.H / 8 - b0);
-  const bool act = lane < nb;
   pdl_launch_dependents();
-  float v[8];
-  {
-    const uint4 w = act ? __ldg(reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(t) * a.H) + b0 + lane)
-                        : make_uint4(0, 0, 0, 0);
-    v[0] = bf16lo(w.x), v[1] = bf16hi(w.x), v[2] = bf16lo(w.y), v[3] = bf16hi(w.y);
-    v[4] = bf16lo(w.z), v[5] = bf16hi(w.z), v[6] = bf16lo(w.w), v[7] = bf16hi(w.w);
-  }
-  build_table(reinterpret_cast<const uint4*>(a.cbs) + kind * kKindWords, v, act, T);
-  pdl_wait();  // the router's ids (routed rows), and the previous step's readers of the partials
-  const size_t row_bytes = static_cast<size_t>(a.H) / 8 * 3, o0 = static_cast<size_t>(s) * kTB * 3;
-  // this kind's matrix of every routed rank, and of the shared expert (rank k)
-  const uint8_t** mat = reinterpret_cast<const uint8_t**>(smem + kTabFloats);
-  if (threadIdx.x < a.k)
-    mat[threadIdx.x] = rvq_routed_record(a, t, threadIdx.x) + (kind ? a.off_r.up_codes : a.off_r.gate_codes) + o0;
-  if (threadIdx.x == a.k && a.Fs) mat[a.k] = a.shared + (kind ? a.off_s.up_codes : a.off_s.gate_codes) + o0;
-  __syncthreads();
-  const int kF = a.k * a.F;
-  float* part = (kind ? a.ws.rvq_u : a.ws.rvq_g) + (static_cast<size_t>(t) * pl.S + s) * pl.R;
-  const int r0 = p * pl.rpp, r1 = min(pl.R, r0 + pl.rpp);
-  stream_rows(
-      r0, r1, row_bytes, 3 * nb, act, T,
-      [&](int r) -> const uint8_t* {
-        const int i = r < kF ? r / a.F : a.k, f = r < kF ? r - i * a.F : r - kF;
-        return mat[i] + static_cast<size_t>(f) * row_bytes;
-      },
-      [&](int r, float val) { part[r] = val; });
-}
-
-// grid T * (k + 1) * Sdm * Pd: CTA (token, entry, slice of the entry's
-// width, part); entry k is the shared expert.  h of the slice (SwiGLU of the
-// gate|up partials added over the input slices in order), its table, then
-// the down rows' partial sums to rvq_y as [T][k + 1][Sdm][H].
-__global__ void __launch_bounds__(kRvqThreads, 2) rvq_down_kernel(const __grid_constant__ LayerArgs a,
-                                                                  const RvqPlan pl) {
-  extern __shared__ __align__(16) float smem[];
-  float* T = smem;
-  float* hs = smem + kTabFloats;  // the slice's 256 h values
-  int id = blockIdx.x;
-  const int p = id % pl.Pd;
-  id /= pl.Pd;
-  const int sd = id % pl.Sdm;
-  id /= pl.Sdm;
-  const int e = id % (a.k + 1), t = id / (a.k + 1);
-  const bool sh = e == a.k;
-  if (sh && a.Fs == 0) return;
-  const int Fe = sh ? a.Fs : a.F;
-  if (sd >= (sh ? pl.Sds : pl.Sdr)) return;
-  const int lane = threadIdx.x & 31;
-  const int b0 = sd * kTB, nb = min(kTB, Fe / 8 - b0);
-  const bool act = lane < nb;
-  pdl_launch_dependents();
-  pdl_wait();  // the gate|up partials
-  // h of the slice: thread i takes value i >> 1 of kind i & 1 (gate, up)
-  const int rowb = sh ? a.k * a.F : e * a.F;
-  for (int i = threadIdx.x; i < 2 * 256; i += kRvqThreads) {
-    const int f = 8 * b0 + (i >> 1);
-    float sum = 0.f;
-    if (f < Fe) {
-      const float* src = ((i & 1) ? a.ws.rvq_u : a.ws.rvq_g) + static_cast<size_t>(t) * pl.S * pl.R + rowb + f;
-      for (int s = 0; s < pl.S; ++s) sum += __ldcg(src + static_cast<size_t>(s) * pl.R);
-    }
-    const float other = __shfl_xor_sync(0xFFFFFFFFu, sum, 1);
-    if ((i & 1) == 0) hs[i >> 1] = rvq_silu(sum) * other;
-  }
-  __syncthreads();
-  float v[8];
+  const int nbu = cdiv(pl.R, kBatch);  // batches per unit
+  long long lo, hi;
+  cta_share(pl.gu_batches, gridDim.x, lo, hi);
+  const size_t row_bytes = static_cast<size_t>(a.H) / 8 * 3;
+  bool routed = false;
+  for (long long u = lo / nbu; u * nbu < hi; ++u) {
+    const int s = static_cast<int>(u % pl.S), kind = static_cast<int>((u / pl.S) & 1),
+              t = static_cast<int>(u / (2 * pl.S));
+    const int nb = min(kSB, a.H / 8 - s * kSB);
+    const Lane L = lane_consts(lane, nb);
+    float vA[8], vB[8];
+    {
+      const uint4* xp = reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(t) * a.H) + s * kSB + 2 * lane;
+      const uint4 wa = L.act ? __ldg(xp) : make_uint4(0, 0, 0, 0), wb = L.act ? __ldg(xp + 1) : make_uint4(0, 0, 0, 0);
+      const uint32_t A[4] = {wa.x, wa.y, wa.z, wa.w}, B[4] = {wb.x, wb.y, wb.z, wb.w};
 #pragma unroll
-  for (int m = 0; m < 8; ++m) v[m] = act ? hs[8 * lane + m] : 0.f;
-  build_table(reinterpret_cast<const uint4*>(a.cbs) + 2 * kKindWords, v, act, T);
-  __syncthreads();
-  const size_t row_bytes = static_cast<size_t>(Fe) / 8 * 3, o0 = static_cast<size_t>(b0) * 3;
-  const uint8_t* codes = (sh ? a.shared + a.off_s.down_codes : rvq_routed_record(a, t, e) + a.off_r.down_codes) + o0;
-  float* y = a.ws.rvq_y + ((static_cast<size_t>(t) * (a.k + 1) + e) * pl.Sdm + sd) * a.H;
-  const int r0 = p * pl.rpd, r1 = min(a.H, r0 + pl.rpd);
-  stream_rows(
-      r0, r1, row_bytes, 3 * nb, act, T, [&](int r) { return codes + static_cast<size_t>(r) * row_bytes; },
-      [&](int r, float val) { y[r] = val; });
+      for (int m = 0; m < 4; ++m) {
+        vA[2 * m] = bf16lo(A[m]), vA[2 * m + 1] = bf16hi(A[m]);
+        vB[2 * m] = bf16lo(B[m]), vB[2 * m + 1] = bf16hi(B[m]);
+      }
+    }
+    __syncthreads();  // the previous unit's lookups and table builders are done
+    stage_book(reinterpret_cast<const uint4*>(a.cbs) + kind * kKindWords, sbook);
+    __syncthreads();
+    build_table(sbook, vA, vB, L.act, T);
+    if (!routed) {
+      pdl_wait();  // the router's ids (routed rows), and the previous step's readers of the partials
+      routed = true;
+    }
+    // this kind's matrix of every routed rank, and of the shared expert (rank k)
+    const size_t o0 = static_cast<size_t>(s) * kChunkBytes;
+    if (threadIdx.x < a.k)
+      mat[threadIdx.x] = rvq_routed_record(a, t, threadIdx.x) + (kind ? a.off_r.up_codes : a.off_r.gate_codes) + o0;
+    if (threadIdx.x == a.k && a.Fs) mat[a.k] = a.shared + (kind ? a.off_s.up_codes : a.off_s.gate_codes) + o0;
+    __syncthreads();
+    float* part = (kind ? a.ws.rvq_u : a.ws.rvq_g) + (static_cast<size_t>(t) * pl.S + s) * pl.R;
+    const long long u0 = u * nbu;
+    GuCur gc;
+    gc.mat = mat, gc.row_bytes = row_bytes, gc.k = a.k, gc.F = a.F, gc.Fs = a.Fs;
+    stream_batches(max(lo, u0) - u0, min(hi, u0 + nbu) - u0, pl.R, row_bytes, L, T, gc,
+                   [&](int r, float val) { part[r] = val; });
+  }
+  if (!routed) pdl_wait();
 }
 
-// grid ceil(T H / 256): out = sum_i p_i y_i + y_shared, ranks in order, each
-// y the sum of its slices in order.
-__global__ void __launch_bounds__(256) rvq_combine_kernel(const __grid_constant__ LayerArgs a, const RvqPlan pl) {
+// Units (token, entry, slice of the entry's width): entry i < k routed rank
+// i (Sdr slices each), then the shared expert (Sds slices); each cdiv(H, 8)
+// batches of down rows.  h of the slice (SwiGLU of the gate|up partials
+// added over the input slices in order), its table, then the down rows'
+// partial sums to rvq_y as [T][k + 1][Sdm][H].
+__global__ void __launch_bounds__(kRvqThreads, 1) rvq_down_kernel(const __grid_constant__ LayerArgs a,
+                                                                  const RvqPlan pl) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  uint8_t* T = smem;
+  uint4* sbook = reinterpret_cast<uint4*>(smem + kTabBytes);
+  float* hs = reinterpret_cast<float*>(smem + kTabBytes + kBookBytes);  // the slice's 512 h values
+  const int lane = threadIdx.x & 31;
+  pdl_launch_dependents();
+  // the down codebooks are the same for every unit: staged once
+  stage_book(reinterpret_cast<const uint4*>(a.cbs) + 2 * kKindWords, sbook);
+  pdl_wait();  // the gate|up partials
+  const int nbu = cdiv(a.H, kBatch);
+  long long lo, hi;
+  cta_share(pl.dn_batches, gridDim.x, lo, hi);
+  for (long long u = lo / nbu; u * nbu < hi; ++u) {
+    const int t = static_cast<int>(u / pl.upt), rem = static_cast<int>(u % pl.upt);
+    const bool sh = rem >= a.k * pl.Sdr;
+    const int e = sh ? a.k : rem / pl.Sdr, sd = sh ? rem - a.k * pl.Sdr : rem % pl.Sdr;
+    const int Fe = sh ? a.Fs : a.F;
+    const int nb = min(kSB, Fe / 8 - sd * kSB);
+    const Lane L = lane_consts(lane, nb);
+    __syncthreads();  // the previous unit's lookups and h readers are done
+    // h of the slice: thread i takes value i of gate (sum over the S input
+    // slices in order) and the same value of up
+    const int rowb = sh ? a.k * a.F : e * a.F;
+    {
+      const int i = threadIdx.x, f = 8 * kSB * sd + i;
+      float g = 0.f, up = 0.f;
+      if (f < Fe) {
+        const size_t o = static_cast<size_t>(t) * pl.S * pl.R + rowb + f;
+#pragma unroll 8
+        for (int s = 0; s < pl.S; ++s) {
+          g += __ldcg(a.ws.rvq_g + o + static_cast<size_t>(s) * pl.R);
+          up += __ldcg(a.ws.rvq_u + o + static_cast<size_t>(s) * pl.R);
+        }
+      }
+      hs[i] = rvq_silu(g) * up;
+    }
+    __syncthreads();
+    float vA[8], vB[8];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) vA[m] = hs[16 * lane + m], vB[m] = hs[16 * lane + 8 + m];
+    build_table(sbook, vA, vB, L.act, T);
+    __syncthreads();
+    const size_t row_bytes = static_cast<size_t>(Fe) / 8 * 3, o0 = static_cast<size_t>(sd) * kChunkBytes;
+    const uint8_t* codes = (sh ? a.shared + a.off_s.down_codes : rvq_routed_record(a, t, e) + a.off_r.down_codes) + o0;
+    float* y = a.ws.rvq_y + ((static_cast<size_t>(t) * (a.k + 1) + e) * pl.Sdm + sd) * a.H;
+    const long long u0 = u * nbu;
+    FlatCur fc;
+    fc.base = codes, fc.row_bytes = row_bytes;
+    stream_batches(max(lo, u0) - u0, min(hi, u0 + nbu) - u0, a.H, row_bytes, L, T, fc,
+                   [&](int r, float val) { y[r] = val; });
+  }
+}
+
+// out = sum_i p_i y_i + y_shared, each y the sum of its slices in order.
+// A CTA takes 32 consecutive outputs of one token; its 8 warps split the
+// ranks (warp g: ranks g, g + 8, ..., the shared expert in warp 0), so each
+// thread has few dependent loads, and the warps' sums are added in warp
+// order: the same order for every launch.
+constexpr int kCombThreads = 256, kCombOut = 32, kCombGroups = kCombThreads / kCombOut;
+__global__ void __launch_bounds__(kCombThreads) rvq_combine_kernel(const __grid_constant__ LayerArgs a,
+                                                                   const RvqPlan pl) {
+  __shared__ float red[kCombGroups][kCombOut];
   pdl_launch_dependents();
   pdl_wait();
-  const size_t i = static_cast<size_t>(blockIdx.x) * 256 + threadIdx.x;
-  if (i >= static_cast<size_t>(a.T) * a.H) return;
-  const int t = static_cast<int>(i / a.H), r = static_cast<int>(i - static_cast<size_t>(t) * a.H);
-  const float* yt = a.ws.rvq_y + static_cast<size_t>(t) * (a.k + 1) * pl.Sdm * a.H + r;
+  const int per_t = (a.H + kCombOut - 1) / kCombOut;
+  const int t = blockIdx.x / per_t, r = (blockIdx.x % per_t) * kCombOut + (threadIdx.x & 31);
+  const int g = threadIdx.x >> 5;
   float acc = 0.f;
-  for (int e = 0; e < a.k; ++e) {
-    float y = 0.f;
-    for (int sl = 0; sl < pl.Sdr; ++sl) y += __ldcg(yt + (static_cast<size_t>(e) * pl.Sdm + sl) * a.H);
-    acc = fmaf(a.weights[t * a.k + e], y, acc);
+  if (r < a.H) {
+    const float* yt = a.ws.rvq_y + static_cast<size_t>(t) * (a.k + 1) * pl.Sdm * a.H + r;
+    for (int e = g; e < a.k; e += kCombGroups) {
+      const float* ye = yt + static_cast<size_t>(e) * pl.Sdm * a.H;
+      float y = 0.f;
+      for (int sl = 0; sl < pl.Sdr; ++sl) y += __ldcg(ye + static_cast<size_t>(sl) * a.H);
+      acc = fmaf(a.weights[t * a.k + e], y, acc);
+    }
+    if (g == 0 && a.Fs) {
+      const float* ye = yt + static_cast<size_t>(a.k) * pl.Sdm * a.H;
+      float y = 0.f;
+      for (int sl = 0; sl < pl.Sds; ++sl) y += __ldcg(ye + static_cast<size_t>(sl) * a.H);
+      acc += y;
+    }
   }
-  if (a.Fs) {
-    float y = 0.f;
-    for (int sl = 0; sl < pl.Sds; ++sl) y += __ldcg(yt + (static_cast<size_t>(a.k) * pl.Sdm + sl) * a.H);
-    acc += y;
+  red[g][threadIdx.x & 31] = acc;
+  __syncthreads();
+  if (g == 0 && r < a.H) {
+    float out = red[0][threadIdx.x];
+    for (int j = 1; j < kCombGroups; ++j) out += red[j][threadIdx.x];
+    const size_t i = static_cast<size_t>(t) * a.H + r;
+    a.out_bf16[i] = f32_to_bf16_rne(out);
+    if (a.out_f32) a.out_f32[i] = out;
   }
-  a.out_bf16[i] = f32_to_bf16_rne(acc);
-  if (a.out_f32) a.out_f32[i] = acc;
 }
 
 cudaError_t launch_rvq(const void* fn, int grid, int block, size_t smem, cudaStream_t st, bool pdl,
@@ -351,8 +513,8 @@ size_t rvq_smem_need(const LayerArgs&) { return rvq_table_smem(); }
 // Bytes of the residual-VQ partial sums for T tokens: gate and up [T][S][R],
 // down [T][k + 1][Sdm][H] (the workspace carve).
 size_t rvq_partial_floats(int H, int k, int F, int Fs, int T, int which) {
-  const int S = cdiv(H / 8, kTB), R = k * F + Fs;
-  const int Sdm = std::max(cdiv(F / 8, kTB), Fs ? cdiv(Fs / 8, kTB) : 0);
+  const int S = cdiv(H / 8, kSB), R = k * F + Fs;
+  const int Sdm = std::max(cdiv(F / 8, kSB), Fs ? cdiv(Fs / 8, kSB) : 0);
   return which < 2 ? static_cast<size_t>(T) * S * R : static_cast<size_t>(T) * (k + 1) * Sdm * H;
 }
 
@@ -368,13 +530,12 @@ cudaError_t set_rvq_attributes(int smem_optin) {
 cudaError_t launch_rvq_experts(const LayerArgs& a, int num_sms, cudaStream_t st) {
   const bool pdl = !a.prof_on;
   const RvqPlan pl = rvq_plan(a, num_sms);
-  const int gu = a.T * 2 * pl.S * pl.P, dn = a.T * (a.k + 1) * pl.Sdm * pl.Pd;
-  const int cb = cdiv(a.T * a.H, 256);
+  const int cb = a.T * cdiv(a.H, kCombOut);
   cudaError_t e;
-  if ((e = launch_rvq((const void*)rvq_gateup_kernel, gu, kRvqThreads, rvq_table_smem(), st, pdl, a, pl)) ||
+  if ((e = launch_rvq((const void*)rvq_gateup_kernel, pl.grid, kRvqThreads, rvq_table_smem(), st, pdl, a, pl)) ||
       (e = mark_rvq(a, 2, st)) ||
-      (e = launch_rvq((const void*)rvq_down_kernel, dn, kRvqThreads, rvq_table_smem(), st, pdl, a, pl)) ||
-      (e = launch_rvq((const void*)rvq_combine_kernel, cb, 256, 0, st, pdl, a, pl)))
+      (e = launch_rvq((const void*)rvq_down_kernel, pl.grid, kRvqThreads, rvq_table_smem(), st, pdl, a, pl)) ||
+      (e = launch_rvq((const void*)rvq_combine_kernel, cb, kCombThreads, 0, st, pdl, a, pl)))
     return e;
   return cudaSuccess;
 }
