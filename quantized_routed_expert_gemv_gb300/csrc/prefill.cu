@@ -142,6 +142,10 @@ __global__ void __launch_bounds__(kPackThreads) pf_pack_kernel(const __grid_cons
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, H = a.H;
   const bool shared = has_sh && j == 0;
   const int Fj = shared ? a.Fs : a.F;
+  const int cnt = entry_cnt(a, j, has_sh);
+  // slices past the entry's packed rows have nothing to do (slice 0 also
+  // writes the block table and the pair index)
+  if (slice > 0 && slice * 16 >= rows_of(cnt)) return;
 
   // prefix over the entries before j: blocks, packed rows, packed h elements
   __shared__ long long s_red[3][kPackThreads / 32];
@@ -163,7 +167,6 @@ __global__ void __launch_bounds__(kPackThreads) pf_pack_kernel(const __grid_cons
   long long nb0 = 0, row0 = 0, h0 = 0;
   for (int w = 0; w < kPackThreads / 32; ++w) nb0 += s_red[0][w], row0 += s_red[1][w], h0 += s_red[2][w];
 
-  const int cnt = entry_cnt(a, j, has_sh);
   const int nbj = blocks_of(cnt);
   const int expert = shared ? -1 : a.ws.act_expert[j - has_sh];
   const int pair0 = shared ? 0 : a.ws.act_off[j - has_sh];
@@ -774,14 +777,23 @@ __global__ void __maxnreg__(168)
 __global__ void __launch_bounds__(256) pf_combine_kernel(const __grid_constant__ LayerArgs a) {
   const int t = blockIdx.x, H = a.H, k = a.k;
   const bool has_sh = a.Fs > 0;
+  // the token's pair rows and weights, read once into shared memory
+  __shared__ int s_p[kMaxTopK];
+  __shared__ float s_w[kMaxTopK];
+  if (threadIdx.x < k) {
+    int p = a.pf.inv[t * k + threadIdx.x];
+    if (p < 0 || p >= a.T * k) p = 0;
+    s_p[threadIdx.x] = p;
+    s_w[threadIdx.x] = a.weights[t * k + threadIdx.x];
+  }
+  __syncthreads();
   for (int r4 = threadIdx.x; r4 < H / 4; r4 += blockDim.x) {
     float4 acc = has_sh ? reinterpret_cast<const float4*>(a.pf.y_sh + static_cast<size_t>(t) * H)[r4]
                         : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
     for (int i = 0; i < k; ++i) {
-      int p = a.pf.inv[t * k + i];
-      if (p < 0 || p >= a.T * k) p = 0;
-      const float w = a.weights[t * k + i];
-      const float4 y = reinterpret_cast<const float4*>(a.pf.y_pair + static_cast<size_t>(p) * H)[r4];
+      const float w = s_w[i];
+      const float4 y = reinterpret_cast<const float4*>(a.pf.y_pair + static_cast<size_t>(s_p[i]) * H)[r4];
       acc.x = fmaf(w, y.x, acc.x), acc.y = fmaf(w, y.y, acc.y);
       acc.z = fmaf(w, y.z, acc.z), acc.w = fmaf(w, y.w, acc.w);
     }
