@@ -53,15 +53,19 @@ def parse_args():
                    help="timed windows of K steps each; the value is the median window")
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--experts", type=int, default=0,
-                   help="shrink the routed-expert count (small layers for ncu captures only)")
+                   help="shrink the routed-expert count (small layers for ncu captures only; with "
+                        "--streamed-only also the slots, E/8, and the steps, --steps)")
     p.add_argument("--no-extras", action="store_true",
                    help="skip the B=4/16 lines, e2e, per-kernel and CPU-baseline passes")
     p.add_argument("--prefill-only", action="store_true",
                    help="only the prefill-chunk measurement (mid-prefill, T=128), one JSON object")
     p.add_argument("--streamed", action="store_true",
-                   help="add the streamed-cache workload (4 large layers, experts in pinned host "
+                   help="the streamed-cache workload (4 large layers, experts in pinned host "
                         "memory, 64 HBM slots per layer, 256 B=1 steps, with and without the "
-                        "router lookahead); needs ~51 GB of host RAM")
+                        "router lookahead; ~51 GB of host RAM) also with --no-extras; the default "
+                        "run includes it at N=1")
+    p.add_argument("--no-streamed", action="store_true",
+                   help="leave the streamed-cache workload out of the default run")
     p.add_argument("--streamed-only", action="store_true",
                    help="only the streamed-cache workload, one JSON object")
     p.add_argument("--mid-only", action="store_true",
@@ -490,7 +494,8 @@ def run_ours(args, world, rank, local):
         s = synth.Shape(s.H, args.experts, s.k, s.F, s.Fs)
     batches = [args.batch] if args.no_extras else sorted({args.batch, 1, 4, 16})
     maxB = max(batches)
-    dl = DeviceLayer(s, wl.weight_seed, max_tokens=maxB, device=device)
+    # the same layer also takes 128-token prefill chunks (the large-prefill line)
+    dl = DeviceLayer(s, wl.weight_seed, max_tokens=maxB if args.no_extras else max(maxB, 128), device=device)
     stream = torch.cuda.Stream(device)
 
     def make(B):
@@ -625,12 +630,18 @@ def run_ours(args, world, rank, local):
 
         if rank == 0 and world == 1:
             out["cpu_baseline"] = cpu_baseline(wl, s)
+        # a 128-token prefill chunk of this layer (no router offsets)
+        pl = time_prefill(args, dl, s, wl.input_seed, device, stream, peak, peaks.get("bf16_tflops", 1900.0))
+        out["prefill_large"] = dict({"workload": f"large-prefill: T=128 token chunks of the {WORKLOAD} layer "
+                                                 f"(H={s.H} E={s.E} top-{s.k} F={s.F} Fs={s.Fs})"}, **pl)
     dl.close()
     if not args.no_extras:
         out["mid_decode"] = run_mid_decode(args, device, stream, peak, world)
         out["prefill"] = run_prefill(args, device, stream, peak, peaks.get("bf16_tflops", 1900.0))
         out["rvq"] = run_rvq(args, device, stream, peak)
-    if args.streamed:
+    # the streamed cache holds ~51 GB of pinned host records per process:
+    # one replica only
+    if (args.streamed or not args.no_extras) and not args.no_streamed and world == 1:
         out["streamed"] = run_streamed(args, device, stream, peak)
     if rank == 0:
         print(json.dumps(out), flush=True)
@@ -716,16 +727,30 @@ def run_prefill(args, device, stream, hbm_peak, bf16_peak):
     Algorithmic bytes: every distinct selected expert's record, the shared
     record and the router once, plus the activations; flops: 2 x 3 x F x H
     per (token, expert) pair and 2 x 3 x Fs x H per token."""
-    import torch
-
-    from quantized_routed_expert_gemv_gb300 import moe, synth
-    from quantized_routed_expert_gemv_gb300.device import DeviceLayer, bf16_tensor
+    from quantized_routed_expert_gemv_gb300 import synth
+    from quantized_routed_expert_gemv_gb300.device import DeviceLayer
 
     wl = synth.WORKLOADS["mid-prefill"]
     s, T = wl.shape, 128
     dl = DeviceLayer(s, wl.weight_seed, beta=synth.beta_for(wl), max_tokens=T, device=device)
-    pool = 8
-    xs = [bf16_tensor(np.stack([synth.hidden(wl.input_seed, 2000 + p, t, s.H) for t in range(T)]), device)
+    res = time_prefill(args, dl, s, wl.input_seed, device, stream, hbm_peak, bf16_peak)
+    dl.close()
+    res = dict({"workload": f"mid-prefill: T={T} token chunks, H={s.H} E={s.E} top-{s.k} F={s.F} Fs={s.Fs}, "
+                           "per-expert logit offsets ~ N(0,1)"}, **res)
+    res["l2"] = "inputs larger than L2: ~344 MB of distinct weights per chunk"
+    return res
+
+
+def time_prefill(args, dl, s, input_seed, device, stream, hbm_peak, bf16_peak, T=128, pool=8):
+    """T-token chunks through `dl` on the tensor-core path, `pool` distinct
+    chunks replayed as CUDA graphs; the chunk time, bytes, flops and the
+    per-phase split (events around router + pack, gate|up, down + combine)."""
+    import torch
+
+    from quantized_routed_expert_gemv_gb300 import moe, synth
+    from quantized_routed_expert_gemv_gb300.device import bf16_tensor
+
+    xs = [bf16_tensor(np.stack([synth.hidden(input_seed, 2000 + p, t, s.H) for t in range(T)]), device)
           for p in range(pool)]
     outs = dl.outputs(T)
     graphs, distinct = [], []
@@ -764,14 +789,11 @@ def run_prefill(args, device, stream, hbm_peak, bf16_peak):
             for j in range(3):
                 sums[j] += evs[j].elapsed_time(evs[j + 1])
     moe.moe_set_profile_events(dl.handle, None)
-    dl.close()
-    return {"workload": f"mid-prefill: T={T} token chunks, H={s.H} E={s.E} top-{s.k} F={s.F} Fs={s.Fs}, "
-                        "per-expert logit offsets ~ N(0,1)",
-            "tokens_per_s": T / sec, "ms_per_chunk": sec * 1e3, "distinct_experts": d,
+    del graphs
+    return {"tokens_per_s": T / sec, "ms_per_chunk": sec * 1e3, "distinct_experts": d,
             "bytes_per_chunk": nbytes, "gbs": nbytes / sec / 1e9, "frac_of_measured_hbm": nbytes / sec / 1e9 / hbm_peak,
             "tflops": flops / sec / 1e12, "frac_of_bf16_peak": flops / sec / 1e12 / bf16_peak,
-            "phase_ms": {"router_pack": sums[0] / 20, "gateup": sums[1] / 20, "down_combine": sums[2] / 20},
-            "l2": "inputs larger than L2: ~344 MB of distinct weights per chunk"}
+            "phase_ms": {"router_pack": sums[0] / 20, "gateup": sums[1] / 20, "down_combine": sums[2] / 20}}
 
 
 def h2d_bandwidth(torch, device, nbytes=1 << 30, reps=5) -> float:
@@ -842,10 +864,14 @@ def run_streamed(args, device, stream, hbm_peak):
 
     wl = synth.WORKLOADS["large-streamed"]
     s, nl, slots, steps = wl.shape, wl.layers, 64, 256
+    if args.experts:  # a reduced copy for small captures: fewer experts, slots in proportion
+        s = synth.Shape(s.H, args.experts, s.k, s.F, s.Fs)
+        slots = max(s.k, args.experts // 8)
+        steps = min(steps, max(GRAPH_STEPS, args.steps))
     bw = h2d_bandwidth(torch, device)
     dls, hosts = [], []
     for l in range(nl):
-        dls.append(DeviceLayer(s, wl.weight_seed, layer=l, beta=synth.beta_for(wl, l), max_tokens=1,
+        dls.append(DeviceLayer(s, wl.weight_seed, layer=l, beta=synth.beta_for(wl, l)[:s.E], max_tokens=1,
                                device=device, resident=False))
         hosts.append(pinned_records(s, wl.weight_seed, layer=l))
     xs_ind = bf16_tensor(np.stack([np.stack([synth.hidden(wl.input_seed, l, t, s.H)[None] for l in range(nl)])
@@ -926,7 +952,7 @@ def run_streamed(args, device, stream, hbm_peak):
     hosts.clear()
     torch.cuda.synchronize()
     for l in range(nl):
-        dls.append(DeviceLayer(s, wl.weight_seed, layer=l, beta=synth.beta_for(wl, l), max_tokens=1,
+        dls.append(DeviceLayer(s, wl.weight_seed, layer=l, beta=synth.beta_for(wl, l)[:s.E], max_tokens=1,
                                device=device, resident=False, rvq=True))
         hosts.append(pinned_records(s, wl.weight_seed, layer=l, rvq=True))
     outs = [d.outputs(1) for d in dls]
