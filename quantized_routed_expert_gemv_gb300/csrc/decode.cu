@@ -818,17 +818,14 @@ static cudaError_t mark(const LayerArgs& a, int i, cudaStream_t st) {
 }
 
 // Router grid: row blocks x token blocks.
-// CTAs of the router: row blocks x token blocks.  The kernel takes 128
-// registers a thread, so one CTA fits an SM: a prefill chunk (many token
-// passes) stays within one wave, so no CTA waits for a second wave and no
-// router row is loaded twice; a few decode tokens may use two waves, which
-// halves each CTA's serial token passes.
+// CTAs of the router: row blocks x token blocks, up to two waves (the kernel
+// takes 128 registers a thread, one CTA per SM): more token blocks shorten
+// each CTA's serial token passes.
 int decode_router_grid(const LayerArgs& a, int num_sms) {
   const int nt = a.T == 1 ? 1 : 2;
   const int rb = (a.E + kRouterRows - 1) / kRouterRows;
   const int tp = nt * router_groups(a.H);  // tokens per pass of a CTA
-  const int waves = a.T > kBtMaxTokens ? 1 : 2;
-  const int tb = std::max(1, std::min((a.T + tp - 1) / tp, (waves * num_sms) / rb));
+  const int tb = std::max(1, std::min((a.T + tp - 1) / tp, (2 * num_sms) / rb));
   return rb * tb;
 }
 
