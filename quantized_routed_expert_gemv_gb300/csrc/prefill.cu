@@ -355,7 +355,10 @@ __device__ __forceinline__ bool pg_wait_warp(uint64_t* bar, uint32_t parity, vol
   return __all_sync(kAllLanes, pg_wait(bar, parity, abort, err)) != 0;
 }
 
-__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
+// SiLU with the fast exponential and division (a few ulp, far inside the
+// parity bound; the per-item SwiGLU of a whole tile is on the epilogue's
+// critical path here).  silu(64) = 64 exactly, as the identity layer needs.
+__device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
 // Asks L2 to fetch [p, p + bytes) (16-byte aligned, a multiple of 16 bytes).
 __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
@@ -667,7 +670,14 @@ __global__ void __maxnreg__(168)
       float acc[kBlkTokens];
 #pragma unroll
       for (int j = 0; j < kBlkTokens; ++j) acc[j] = 0.f;
-      uint2 sb_next = __ldg(reinterpret_cast<const uint2*>(sbrow));
+      // the row's scale/bias words of the next four chunks are in flight
+      // while a chunk is drained (an L2 round trip takes longer than one
+      // chunk's epilogue)
+      const uint2* sbp = reinterpret_cast<const uint2*>(sbrow);
+      uint2 sb0 = __ldg(sbp), sb1 = make_uint2(0, 0), sb2 = make_uint2(0, 0), sb3 = make_uint2(0, 0);
+      if (1 < I.nch) sb1 = __ldg(sbp + 1);
+      if (2 < I.nch) sb2 = __ldg(sbp + 2);
+      if (3 < I.nch) sb3 = __ldg(sbp + 3);
       for (int u0 = 0; u0 < I.nch && !stop; u0 += U, ++units) {
         const int ue = min(u0 + U, I.nch), buf = units % kTmemBufs;
         const uint32_t uph = (units / kTmemBufs) & 1;
@@ -677,8 +687,9 @@ __global__ void __maxnreg__(168)
           break;
         }
         for (int c = u0; c < ue; ++c, pg.next(kNSG)) {
-          const uint32_t sbw[2] = {sb_next.x, sb_next.y};
-          if (c + 1 < I.nch) sb_next = __ldg(reinterpret_cast<const uint2*>(sbrow + 2 * c + 2));
+          const uint32_t sbw[2] = {sb0.x, sb0.y};
+          sb0 = sb1, sb1 = sb2, sb2 = sb3;
+          if (c + 4 < I.nch) sb3 = __ldg(sbp + c + 4);
           if (named_bar_or(2, kEpiWarps * 32, !pg_wait_warp(&gs_full[pg.s], pg.ph, s_abort, err))) {
             stop = true;
             break;
@@ -728,29 +739,78 @@ __global__ void __maxnreg__(168)
             if (j < np) xr[j] = acc[j];
         }
         named_bar(1, kEpiWarps * 32);
-        if (q < 2) {
-          const int f = I.tile * 64 + row;  // row of h (F index)
-          const int cf = f >> 7, k8 = (f & 127) >> 3, pos = ((f & 7) >> 2) | ((f & 3) << 1);
+        if (q < 2) {  // h = silu(g) * u of the tile's 64 rows, into the exchange rows
           float* xr = s_x + row * kXPitch;
-          const size_t e0 = static_cast<size_t>(I.blk.hoff) + static_cast<size_t>(cf) * np * 128 + k8 * (np >> 3) * 64 + pos;
 #pragma unroll
           for (int n = 0; n < kBlkTokens; ++n)
-            if (n < np) {
-              const float h = silu_f(acc[n]) * xr[n];
-              xr[n] = h;
-              const uint16_t hi = f32_to_bf16_rne(h);
-              const uint16_t lo = f32_to_bf16_rne(h - __uint_as_float(static_cast<uint32_t>(hi) << 16));
-              const size_t e = e0 + (n >> 3) * 64 + (n & 7) * 8;
-              a.pf.hc_hi[e] = hi;
-              a.pf.hc_lo[e] = lo;
-            }
+            if (n < np) xr[n] = silu_f(acc[n]) * xr[n];
         }
         named_bar(1, kEpiWarps * 32);
-        // group sums of h over the tile's 64 rows (one group of the down GEMM)
-        if (tid < np) {
+        // The tile's h in the down GEMM's B layout (bf16 hi + lo): its 64
+        // rows are 8 k8 columns of one 128-K chunk, a contiguous run of
+        // 8 * np 16-byte core rows: core row (k8l, token n) holds rows
+        // 8 k8l + {0, 4, 1, 5, 2, 6, 3, 7} of token n.  Each thread builds
+        // whole core rows from the exchange and stores them as 16 bytes.
+        {
+          const int cf = I.tile >> 1, k80 = 8 * (I.tile & 1), r8n = np >> 3;
+          const size_t base = static_cast<size_t>(I.blk.hoff) + static_cast<size_t>(cf) * np * 128 +
+                              static_cast<size_t>(k80) * r8n * 64;
+          for (int u = tid; u < 8 * np; u += kEpiWarps * 32) {
+            const int k8l = u / np, n = u - k8l * np;
+            uint32_t hw[4], lw[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const float h0 = s_x[(8 * k8l + j) * kXPitch + n], h1 = s_x[(8 * k8l + 4 + j) * kXPitch + n];
+              const uint16_t a0 = f32_to_bf16_rne(h0), a1 = f32_to_bf16_rne(h1);
+              const uint16_t b0 = f32_to_bf16_rne(h0 - __uint_as_float(static_cast<uint32_t>(a0) << 16));
+              const uint16_t b1 = f32_to_bf16_rne(h1 - __uint_as_float(static_cast<uint32_t>(a1) << 16));
+              hw[j] = static_cast<uint32_t>(a0) | (static_cast<uint32_t>(a1) << 16);
+              lw[j] = static_cast<uint32_t>(b0) | (static_cast<uint32_t>(b1) << 16);
+            }
+            // core row (k8l, r8 = n / 8, n % 8) at element (k8l * r8n + n / 8) * 64 + (n % 8) * 8
+            const size_t e = base + (static_cast<size_t>(k8l) * r8n + (n >> 3)) * 64 + (n & 7) * 8;
+            *reinterpret_cast<uint4*>(a.pf.hc_hi + e) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            *reinterpret_cast<uint4*>(a.pf.hc_lo + e) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+          }
+        }
+        // group sums of h over the tile's 64 rows (one group of the down
+        // GEMM): eight threads per token, each over 8 rows, then a fixed
+        // butterfly (the same order every time)
+        {
+          const int n = tid >> 3, part = tid & 7;
           float sum = 0.f;
-          for (int r = 0; r < 64; ++r) sum += s_x[r * kXPitch + tid];
-          a.pf.sh[I.blk.hoff / 64 + I.tile * np + tid] = sum;
+          if (n < np)
+#pragma unroll
+            for (int r = 0; r < 8; ++r) sum += s_x[(8 * part + r) * kXPitch + n];
+          sum += __shfl_xor_sync(kAllLanes, sum, 1);
+          sum += __shfl_xor_sync(kAllLanes, sum, 2);
+          sum += __shfl_xor_sync(kAllLanes, sum, 4);
+          if (n < np && part == 0) a.pf.sh[I.blk.hoff / 64 + I.tile * np + n] = sum;
+          if (np > 16) {  // tokens 16 .. np - 1: a second round
+            const int n2 = n + 16;
+            float s2 = 0.f;
+            if (n2 < np)
+#pragma unroll
+              for (int r = 0; r < 8; ++r) s2 += s_x[(8 * part + r) * kXPitch + n2];
+            s2 += __shfl_xor_sync(kAllLanes, s2, 1);
+            s2 += __shfl_xor_sync(kAllLanes, s2, 2);
+            s2 += __shfl_xor_sync(kAllLanes, s2, 4);
+            if (n2 < np && part == 0) a.pf.sh[I.blk.hoff / 64 + I.tile * np + n2] = s2;
+            if (np > 32) {
+#pragma unroll
+              for (int rr = 2; rr < 4; ++rr) {
+                const int n3 = n + 16 * rr;
+                float s3 = 0.f;
+                if (n3 < np)
+#pragma unroll
+                  for (int r = 0; r < 8; ++r) s3 += s_x[(8 * part + r) * kXPitch + n3];
+                s3 += __shfl_xor_sync(kAllLanes, s3, 1);
+                s3 += __shfl_xor_sync(kAllLanes, s3, 2);
+                s3 += __shfl_xor_sync(kAllLanes, s3, 4);
+                if (n3 < np && part == 0) a.pf.sh[I.blk.hoff / 64 + I.tile * np + n3] = s3;
+              }
+            }
+          }
         }
         named_bar(1, kEpiWarps * 32);
       } else {
