@@ -686,44 +686,51 @@ __global__ void __maxnreg__(168)
           stop = true;
           break;
         }
+        // A failed wait inside the unit only marks the warp; the four
+        // epilogue warps agree at the unit's end, so no named barrier runs
+        // per chunk and the barriers after it stay uniform.
+        bool lost = false;
         for (int c = u0; c < ue; ++c, pg.next(kNSG)) {
           const uint32_t sbw[2] = {sb0.x, sb0.y};
           sb0 = sb1, sb1 = sb2, sb2 = sb3;
           if (c + 4 < I.nch) sb3 = __ldg(sbp + c + 4);
-          if (named_bar_or(2, kEpiWarps * 32, !pg_wait_warp(&gs_full[pg.s], pg.ph, s_abort, err))) {
-            stop = true;
-            break;
-          }
+          if (!lost && !pg_wait_warp(&gs_full[pg.s], pg.ph, s_abort, err)) lost = true;
           tc_fence_after();
+          const uint32_t base0 =
+              taddr + (static_cast<uint32_t>(q * 32) << 16) + buf * 128 + (2 * (c - u0)) * np;
+          const uint32_t base1 = base0 + np;
+          const float s0 = bf16lo(sbw[0]), b0 = bf16hi(sbw[0]), s1 = bf16lo(sbw[1]), b1 = bf16hi(sbw[1]);
+          const float* gs0 = s_gs + pg.s * 2 * kBlkTokens;
+          const float* gs1 = gs0 + np;
 #pragma unroll
-          for (int gi = 0; gi < 2; ++gi) {
-            const uint32_t base =
-                taddr + (static_cast<uint32_t>(q * 32) << 16) + buf * 128 + (2 * (c - u0) + gi) * np;
-            const float s = bf16lo(sbw[gi]), b = bf16hi(sbw[gi]);
-            const float* gs = s_gs + pg.s * 2 * kBlkTokens + gi * np;
+          for (int p = 0; p < kBlkTokens / 16; ++p)  // 16 columns of both groups per TMEM round trip
+            if (p * 16 < np) {
+              uint32_t d0[8], d1[8], e0[8], e1[8];
+              tmem_ld8(base0 + p * 16, d0);
+              tmem_ld8(base0 + p * 16 + 8, d1);
+              tmem_ld8(base1 + p * 16, e0);
+              tmem_ld8(base1 + p * 16 + 8, e1);
+              float xa[16], xb[16];
 #pragma unroll
-            for (int p = 0; p < kBlkTokens / 16; ++p)  // 16 columns per TMEM round trip
-              if (p * 16 < np) {
-                uint32_t d0[8], d1[8];
-                tmem_ld8(base + p * 16, d0);
-                tmem_ld8(base + p * 16 + 8, d1);
-                tmem_wait();
-                const float4 x0 = *reinterpret_cast<const float4*>(gs + p * 16);
-                const float4 x1 = *reinterpret_cast<const float4*>(gs + p * 16 + 4);
-                const float4 x2 = *reinterpret_cast<const float4*>(gs + p * 16 + 8);
-                const float4 x3 = *reinterpret_cast<const float4*>(gs + p * 16 + 12);
-                const float xs[16] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w,
-                                      x2.x, x2.y, x2.z, x2.w, x3.x, x3.y, x3.z, x3.w};
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                  acc[p * 16 + j] = fmaf(s, __uint_as_float(d0[j]), fmaf(b, xs[j], acc[p * 16 + j]));
-                  acc[p * 16 + 8 + j] = fmaf(s, __uint_as_float(d1[j]), fmaf(b, xs[8 + j], acc[p * 16 + 8 + j]));
-                }
+              for (int j = 0; j < 4; ++j) {
+                const float4 ua = *reinterpret_cast<const float4*>(gs0 + p * 16 + 4 * j);
+                const float4 ub = *reinterpret_cast<const float4*>(gs1 + p * 16 + 4 * j);
+                xa[4 * j] = ua.x, xa[4 * j + 1] = ua.y, xa[4 * j + 2] = ua.z, xa[4 * j + 3] = ua.w;
+                xb[4 * j] = ub.x, xb[4 * j + 1] = ub.y, xb[4 * j + 2] = ub.z, xb[4 * j + 3] = ub.w;
               }
-          }
+              tmem_wait();
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                float v = fmaf(s0, __uint_as_float(d0[j]), fmaf(b0, xa[j], acc[p * 16 + j]));
+                acc[p * 16 + j] = fmaf(s1, __uint_as_float(e0[j]), fmaf(b1, xb[j], v));
+                float w = fmaf(s0, __uint_as_float(d1[j]), fmaf(b0, xa[8 + j], acc[p * 16 + 8 + j]));
+                acc[p * 16 + 8 + j] = fmaf(s1, __uint_as_float(e1[j]), fmaf(b1, xb[8 + j], w));
+              }
+            }
           __syncwarp();
           if (lane == 0) mbar_arrive(&gs_empty[pg.s]);
         }
+        if (named_bar_or(2, kEpiWarps * 32, lost)) stop = true;
         if (stop) break;
         tc_fence_before();
         __syncwarp();
