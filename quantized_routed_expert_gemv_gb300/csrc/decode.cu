@@ -52,6 +52,11 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int la
 
 constexpr int kRouterThreads = 512;
 constexpr int kRouterRows = 4;  // rows in flight per iteration
+// control words of the multi-token router: per token block, row-block CTAs
+// done with its logits; token blocks done with their top-k
+constexpr int kCtlTopkDone = 15;
+constexpr int kCtlTokenBlock0 = 16;
+constexpr int kRouterMaxTokenBlocks = 48;  // ctl[16 .. 63]
 
 // Warp groups: a group of WPR = ceil(H / 512) warps covers a router row (its
 // thread c owns 16-byte chunk c, 16 activations); the block's G = 16 / WPR
@@ -191,22 +196,28 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const __grid_con
     __syncthreads();
   }
 
-  // ---- last CTA: top-k, weights, grouping --------------------------------
+  // ---- top-k per token block, then grouping by the last token block ------
+  // The last of the RB row-block CTAs of token block tb to finish its
+  // logits takes the top-k of the block's tokens (every logit of them is
+  // written by then); the last token block to finish its top-k groups every
+  // token's pairs by expert.  Both counters go back to zero in the CTA that
+  // completes them.
   __shared__ int s_last;
+  unsigned* const tb_done = &a.ws.ctl[kCtlTokenBlock0 + tb];
+  unsigned* const tk_done = &a.ws.ctl[kCtlTopkDone];
   __threadfence();
   __syncthreads();
-  if (tid == 0) s_last = (atomicAdd(&a.ws.ctl[1], 1u) == gridDim.x - 1);
+  if (tid == 0) s_last = (atomicAdd(tb_done, 1u) == static_cast<unsigned>(RB - 1));
   __syncthreads();
   if (!s_last) return;
   __threadfence();
+  if (tid == 0) *tb_done = 0u;
 
   unsigned* sel = reinterpret_cast<unsigned*>(rsm + NW * E);      // [E][4] token bitmasks
   int* s_off = reinterpret_cast<int*>(sel + 4 * E);               // [E] pair offsets
   int* s_ids = s_off + E;                                         // [T*k]
   int* s_scan = s_ids + kMaxTokens * kMaxTopK;                    // [2*NW] scan scratch
-
-  for (int i = tid; i < 4 * E; i += kRouterThreads) sel[i] = 0u;
-  __syncthreads();
+  const int t_lo = min(T, p_lo * TP), t_hi = min(T, p_hi * TP);  // this token block's tokens
 
   // One warp per token.  Lane l holds the keys of experts l, l+32, ... in
   // registers (a logit's IEEE bits mapped to an order-preserving unsigned;
@@ -218,11 +229,11 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const __grid_con
 #pragma unroll
     for (int s2 = 0; s2 < KPL; ++s2) {
       const int e = s2 * 32 + lane;
-      lnext[s2] = (t < T && e < E) ? __ldcg(a.ws.logits + static_cast<size_t>(t) * E + e) : 0.f;
+      lnext[s2] = (t < t_hi && e < E) ? __ldcg(a.ws.logits + static_cast<size_t>(t) * E + e) : 0.f;
     }
   };
-  load_logits(warp);
-  for (int t = warp; t < T; t += NW) {
+  load_logits(t_lo + warp);
+  for (int t = t_lo + warp; t < t_hi; t += NW) {
     uint32_t key[KPL];
 #pragma unroll
     for (int s2 = 0; s2 < KPL; ++s2) {
@@ -268,10 +279,27 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const __grid_con
     if (lane < k) {
       a.ids[t * k + lane] = myi;
       a.weights[t * k + lane] = ex / z;
-      s_ids[t * k + lane] = myi;
-      atomicOr(&sel[myi * 4 + (t >> 5)], 1u << (t & 31));
     }
     __syncwarp();
+  }
+
+  // the last token block: every token's ids are in; group the pairs
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = (atomicAdd(tk_done, 1u) == static_cast<unsigned>(TB - 1));
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  if (tid == 0) *tk_done = 0u;
+
+  for (int i = tid; i < 4 * E; i += kRouterThreads) sel[i] = 0u;
+  __syncthreads();
+  for (int p = tid; p < T * k; p += kRouterThreads) {
+    int e = __ldcg(a.ids + p);
+    if (e < 0 || e >= E) e = 0;  // (a range error was latched where it arose)
+    const int t = p / k;
+    s_ids[p] = e;
+    atomicOr(&sel[e * 4 + (t >> 5)], 1u << (t & 31));
   }
   __syncthreads();
 
@@ -321,7 +349,6 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const __grid_con
     a.ws.pair_token[pos] = t;
     a.ws.pair_slot[pos] = p;
   }
-  if (tid == 0) a.ws.ctl[1] = 0u;  // counter back to zero for the next call
 }
 
 // ============================================================================
@@ -825,7 +852,7 @@ int decode_router_grid(const LayerArgs& a, int num_sms) {
   const int nt = a.T == 1 ? 1 : 2;
   const int rb = (a.E + kRouterRows - 1) / kRouterRows;
   const int tp = nt * router_groups(a.H);  // tokens per pass of a CTA
-  const int tb = std::max(1, std::min((a.T + tp - 1) / tp, (2 * num_sms) / rb));
+  const int tb = std::max(1, std::min({(a.T + tp - 1) / tp, (2 * num_sms) / rb, kRouterMaxTokenBlocks}));
   return rb * tb;
 }
 
