@@ -50,6 +50,7 @@
 namespace moe {
 
 cudaError_t launch_decode_router(const LayerArgs& a, int num_sms, cudaStream_t st);
+cudaError_t launch_b1_router(const LayerArgs& a, int num_sms, cudaStream_t st);
 
 namespace {
 
@@ -540,12 +541,15 @@ cudaError_t launch_rvq_experts(const LayerArgs& a, int num_sms, cudaStream_t st)
   return cudaSuccess;
 }
 
-// The router, then gate|up, down and the combine for every token at once.
+// The router (the single-token one, with its block-wide top-k, for one
+// token), then gate|up, down and the combine for every token at once.
 // Profile events: before the router, before gate|up, before down, after the
 // combine.
 cudaError_t launch_decode_rvq(const LayerArgs& a, int num_sms, cudaStream_t st) {
   cudaError_t e;
-  if ((e = mark_rvq(a, 0, st)) || (e = launch_decode_router(a, num_sms, st)) || (e = mark_rvq(a, 1, st)) ||
+  if ((e = mark_rvq(a, 0, st)) ||
+      (e = a.T == 1 ? launch_b1_router(a, num_sms, st) : launch_decode_router(a, num_sms, st)) ||
+      (e = mark_rvq(a, 1, st)) ||
       (e = launch_rvq_experts(a, num_sms, st)))
     return e;
   return mark_rvq(a, 3, st);
