@@ -330,6 +330,27 @@ __device__ __forceinline__ void cta_share(long long n, int grid, long long& lo, 
   hi = n * (blockIdx.x + 1) / grid;
 }
 
+// With no more units than CTAs, every CTA takes a part of exactly one unit
+// (units split into G / U or G / U + 1 equal parts), so no CTA builds two
+// tables; otherwise the flat share.
+__device__ __forceinline__ void unit_share(int units, int nbu, int grid, long long& lo, long long& hi) {
+  if (units > grid) {
+    cta_share(static_cast<long long>(units) * nbu, grid, lo, hi);
+    return;
+  }
+  const int q = grid / units, r = grid % units, c = blockIdx.x;
+  int u, part, parts;
+  if (c < r * (q + 1)) {
+    u = c / (q + 1), part = c % (q + 1), parts = q + 1;
+  } else {
+    const int c2 = c - r * (q + 1);
+    u = r + c2 / q, part = c2 % q, parts = q;
+  }
+  const long long u0 = static_cast<long long>(u) * nbu;
+  lo = u0 + static_cast<long long>(nbu) * part / parts;
+  hi = u0 + static_cast<long long>(nbu) * (part + 1) / parts;
+}
+
 // Units (token, kind, slice), kind 0 gate, 1 up, each cdiv(R, 8) batches of
 // the rows of the token's k routed experts then the shared expert.  Partial
 // sums to rvq_g (gate) / rvq_u (up) as [T][S][R].
@@ -404,7 +425,7 @@ __global__ void __launch_bounds__(kRvqThreads, 1) rvq_down_kernel(const __grid_c
   pdl_wait();  // the gate|up partials
   const int nbu = cdiv(a.H, kBatch);
   long long lo, hi;
-  cta_share(pl.dn_batches, gridDim.x, lo, hi);
+  unit_share(a.T * pl.upt, nbu, gridDim.x, lo, hi);
   for (long long u = lo / nbu; u * nbu < hi; ++u) {
     const int t = static_cast<int>(u / pl.upt), rem = static_cast<int>(u % pl.upt);
     const bool sh = rem >= a.k * pl.Sdr;
