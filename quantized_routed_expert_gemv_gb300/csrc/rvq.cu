@@ -330,11 +330,12 @@ __device__ __forceinline__ void cta_share(long long n, int grid, long long& lo, 
   hi = n * (blockIdx.x + 1) / grid;
 }
 
-// With no more units than CTAs, every CTA takes a part of exactly one unit
-// (units split into G / U or G / U + 1 equal parts), so no CTA builds two
-// tables; otherwise the flat share.
+// With at least two CTAs per unit, every CTA takes a part of exactly one
+// unit (units split into G / U or G / U + 1 equal parts), so no CTA builds
+// two tables; otherwise (one part per unit would leave whole units to
+// single CTAs beside halves) the flat share.
 __device__ __forceinline__ void unit_share(int units, int nbu, int grid, long long& lo, long long& hi) {
-  if (units > grid) {
+  if (2 * units > grid) {
     cta_share(static_cast<long long>(units) * nbu, grid, lo, hi);
     return;
   }
@@ -364,7 +365,7 @@ __global__ void __launch_bounds__(kRvqThreads, 1) rvq_gateup_kernel(const __grid
   pdl_launch_dependents();
   const int nbu = cdiv(pl.R, kBatch);  // batches per unit
   long long lo, hi;
-  cta_share(pl.gu_batches, gridDim.x, lo, hi);
+  unit_share(a.T * 2 * pl.S, nbu, gridDim.x, lo, hi);
   const size_t row_bytes = static_cast<size_t>(a.H) / 8 * 3;
   bool routed = false;
   for (long long u = lo / nbu; u * nbu < hi; ++u) {
