@@ -635,14 +635,17 @@ def run_ours(args, world, rank, local):
         out["prefill_large"] = dict({"workload": f"large-prefill: T=128 token chunks of the {WORKLOAD} layer "
                                                  f"(H={s.H} E={s.E} top-{s.k} F={s.F} Fs={s.Fs})"}, **pl)
     dl.close()
-    if not args.no_extras:
-        out["mid_decode"] = run_mid_decode(args, device, stream, peak, world)
-        out["prefill"] = run_prefill(args, device, stream, peak, peaks.get("bf16_tflops", 1900.0))
-        out["rvq"] = run_rvq(args, device, stream, peak)
+    del x, outs
+    main.clear()
+    torch.cuda.empty_cache()
     # the streamed cache holds ~51 GB of pinned host records per process:
     # one replica only
     if (args.streamed or not args.no_extras) and not args.no_streamed and world == 1:
         out["streamed"] = run_streamed(args, device, stream, peak)
+    if not args.no_extras:
+        out["mid_decode"] = run_mid_decode(args, device, stream, peak, world)
+        out["prefill"] = run_prefill(args, device, stream, peak, peaks.get("bf16_tflops", 1900.0))
+        out["rvq"] = run_rvq(args, device, stream, peak)
     if rank == 0:
         print(json.dumps(out), flush=True)
 

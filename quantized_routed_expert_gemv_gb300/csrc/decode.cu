@@ -870,8 +870,18 @@ static cudaError_t launch_router_g(const LayerArgs& a, int num_sms, cudaStream_t
   return launch_ex(fn, dim3(rgrid), dim3(kRouterThreads), router_smem_bytes(a.E), st, false, a);
 }
 
+// The grouped kernels with 4 tokens per pass have 7 consumer warps, one
+// 32-chunk column block of a row each: rows of at most 7 x 32 x 32 = 7168
+// values.  A wider hidden or FFN row takes the one-token-per-pass variants
+// (16 and 8 consumer warps, rows up to 8192), which loop over an expert's
+// tokens for any batch.
+static bool grouped_one(const LayerArgs& a) {
+  constexpr int kWide = 7 * 32 * 32;
+  return a.T == 1 || a.H > kWide || std::max(a.F, a.Fs) > kWide;
+}
+
 static cudaError_t launch_experts_g(LayerArgs& a, int num_sms, cudaStream_t st, bool pdl) {
-  const bool one = (a.T == 1);
+  const bool one = grouped_one(a);
   cudaError_t e;
   if (one)
     e = launch_ex((const void*)gateup_kernel<1, 16>, dim3(num_sms), dim3(17 * 32),
@@ -897,14 +907,14 @@ cudaError_t launch_decode_router(const LayerArgs& a, int num_sms, cudaStream_t s
 
 cudaError_t launch_decode_experts(const LayerArgs& in, int num_sms, cudaStream_t st) {
   LayerArgs a = in;
-  const bool one = (a.T == 1);
+  const bool one = grouped_one(a);
   plan_decode(a, num_sms, one ? 16 : 7, one ? 8 : 7, one ? 1 : 4);
   return launch_experts_g(a, num_sms, st, false);
 }
 
 cudaError_t launch_decode(const LayerArgs& in, int num_sms, cudaStream_t st) {
   LayerArgs a = in;
-  const bool one = (a.T == 1);
+  const bool one = grouped_one(a);
   const bool pdl = !a.prof_on;
   plan_decode(a, num_sms, one ? 16 : 7, one ? 8 : 7, one ? 1 : 4);
   cudaError_t e;

@@ -105,3 +105,32 @@ def test_identity_experts_closed_form():
         # every product and partial sum is exact until the final fp32 combine
         np.testing.assert_allclose(of[t], scale * x, rtol=2e-6, atol=1e-30)
     dl.close()
+
+
+def test_wide_hidden_router_token_blocks():
+    """H = 8192 with E = 8: a router row spans 16 warps, so a token pass holds
+    2 tokens and a 128-token chunk has 64 passes over 2 row blocks of 4
+    experts.  The router then runs at its cap of 48 token blocks, some of
+    them two passes long; the last row-block CTA of each token block takes
+    that block's top-k and the last token block groups every pair.  Every
+    token's ids and weights are checked against the oracle's routing, and
+    sampled outputs against the oracle."""
+    shape = synth.Shape(8192, 8, 2, 128, 128)
+    hl = HostLayer(shape, 12, beta=synth.beta_normal(12, 0, 8))
+    orc = hl.oracle()
+    T = 128
+    xs = np.stack([hidden_with_margin(orc, 47, 0, t) for t in range(T)])
+    for prefill, n in ((True, T), (False, 16)):
+        dl = DeviceLayer(shape, 0, beta=hl.beta, max_tokens=128, device=DEV, host_records=hl.records,
+                         host_shared=hl.shared, router=(hl.router_codes, hl.router_sb))
+        of, ob, ids, w = run(dl, xs[:n], prefill)
+        for t in range(n):
+            _, rids, rp = orc.route(xs[t])
+            assert np.array_equal(ids[t], rids), (prefill, t, ids[t], rids)
+            assert np.abs(w[t] - rp).max() <= P_TOL
+        assert np.array_equal(ob, synth.float_to_bf16_bits(of))
+        for t in (0, n // 2, n - 1):
+            r, _, _ = orc.token(xs[t])
+            err = np.abs(of[t].astype(np.float64) - r).max()
+            assert err <= TOL_REL * np.abs(r).max() + TOL_ABS, (prefill, t, err)
+        dl.close()
