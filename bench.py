@@ -488,6 +488,8 @@ def run_ours(args, world, rank, local):
         if rank == 0:
             print(json.dumps({"streamed": res}), flush=True)
         return
+    streamed = (args.streamed or not args.no_extras) and not args.no_streamed and world == 1
+    st_hosts = streamed_hosts(args) if streamed else None
     wl = synth.WORKLOADS[WORKLOAD]
     s = wl.shape
     if args.experts:
@@ -640,8 +642,9 @@ def run_ours(args, world, rank, local):
     torch.cuda.empty_cache()
     # the streamed cache holds ~51 GB of pinned host records per process:
     # one replica only
-    if (args.streamed or not args.no_extras) and not args.no_streamed and world == 1:
-        out["streamed"] = run_streamed(args, device, stream, peak)
+    if streamed:
+        out["streamed"] = run_streamed(args, device, stream, peak, st_hosts)
+        st_hosts = None
     if not args.no_extras:
         out["mid_decode"] = run_mid_decode(args, device, stream, peak, world)
         out["prefill"] = run_prefill(args, device, stream, peak, peaks.get("bf16_tflops", 1900.0))
@@ -845,7 +848,28 @@ def replay_match(expected, st) -> str:
     return "equal" if not diffs and len(st) == len(expected) else "differs: " + "; ".join(diffs[:4])
 
 
-def run_streamed(args, device, stream, hbm_peak):
+def streamed_shape(args):
+    """(workload, shape, layers, slots, steps) of the streamed-cache leg."""
+    from quantized_routed_expert_gemv_gb300 import synth
+    wl = synth.WORKLOADS["large-streamed"]
+    s, nl, slots, steps = wl.shape, wl.layers, 64, 256
+    if args.experts:  # a reduced copy for small captures: fewer experts, slots in proportion
+        s = synth.Shape(s.H, args.experts, s.k, s.F, s.Fs)
+        slots = max(s.k, args.experts // 8)
+        steps = min(steps, max(GRAPH_STEPS, args.steps))
+    return wl, s, nl, slots, steps
+
+
+def streamed_hosts(args):
+    """The streamed leg's expert records in page-locked host memory, one
+    tensor per layer (~51 GB at the full shape).  Made before the other legs
+    so the host pages are taken while host memory is still unfragmented."""
+    from quantized_routed_expert_gemv_gb300.device import pinned_records
+    wl, s, nl, _, _ = streamed_shape(args)
+    return [pinned_records(s, wl.weight_seed, layer=l) for l in range(nl)]
+
+
+def run_streamed(args, device, stream, hbm_peak, hosts=None):
     """Streamed expert cache: 4 stacked layers of the large shape, all expert
     records in pinned host memory, 64 HBM slots per layer, router offsets
     Zipf(1.1) per layer, 256 consecutive B=1 steps from a cold cache, timed
@@ -865,18 +889,14 @@ def run_streamed(args, device, stream, hbm_peak):
     from quantized_routed_expert_gemv_gb300.device import CachedLayer, DeviceLayer, bf16_tensor, \
         pinned_records
 
-    wl = synth.WORKLOADS["large-streamed"]
-    s, nl, slots, steps = wl.shape, wl.layers, 64, 256
-    if args.experts:  # a reduced copy for small captures: fewer experts, slots in proportion
-        s = synth.Shape(s.H, args.experts, s.k, s.F, s.Fs)
-        slots = max(s.k, args.experts // 8)
-        steps = min(steps, max(GRAPH_STEPS, args.steps))
+    wl, s, nl, slots, steps = streamed_shape(args)
     bw = h2d_bandwidth(torch, device)
-    dls, hosts = [], []
+    dls = []
+    if hosts is None:
+        hosts = streamed_hosts(args)
     for l in range(nl):
         dls.append(DeviceLayer(s, wl.weight_seed, layer=l, beta=synth.beta_for(wl, l)[:s.E], max_tokens=1,
                                device=device, resident=False))
-        hosts.append(pinned_records(s, wl.weight_seed, layer=l))
     xs_ind = bf16_tensor(np.stack([np.stack([synth.hidden(wl.input_seed, l, t, s.H)[None] for l in range(nl)])
                                    for t in range(steps)]), device)  # [steps][layers][1][H]
     xs_chain = bf16_tensor(np.stack([synth.hidden_chain(wl.input_seed, t, s.H, nl, LOOKAHEAD_RHO)[:, None]
