@@ -63,6 +63,11 @@ constexpr int kRowBytes = kSB * 4;          // one (stage, code) row of the tabl
 constexpr int kTabBytes = 3 * kCodes * kRowBytes;  // 196,608: [stage][code][block]
 constexpr int kBatch = 8;                   // rows a warp sums at once
 constexpr int kChunkBytes = 3 * kSB;        // a row's code bytes of one slice
+// The shared address at which dynamic shared memory starts in a kernel with
+// no static shared memory on this part (after the CTA's reserved 1 KB).  The
+// lookups of a table there carry its address as an immediate; a table at
+// any other address takes the same lookups with one add each.
+constexpr int kDynSmemBase = 1024;
 
 // Launch geometry, the same on host and device.
 struct RvqPlan {
@@ -180,6 +185,8 @@ __device__ __forceinline__ Lane lane_consts(int lane, int nb) {
   Lane L;
   const int d = (6 * lane) & 3;
   L.wo = (6 * lane) >> 2;
+  L.act = 2 * lane < nb;
+  if (!L.act) L.wo = 0;  // reads valid bytes of the row; its table entries are zero
   const bool hi16 = lane >= 16;
   const int first = hi16 ? 2 * lane + 1 : 2 * lane, second = hi16 ? 2 * lane : 2 * lane + 1;
   // bytes of block 2j: d .. d + 2; of block 2j + 1: d + 3 .. d + 5
@@ -191,47 +198,96 @@ __device__ __forceinline__ Lane lane_consts(int lane, int nb) {
     L.base[st] = static_cast<uint32_t>(st << 16 | 4 * first);
     L.base[3 + st] = static_cast<uint32_t>(st << 16 | 4 * second);
   }
-  L.act = 2 * lane < nb;
   return L;
 }
 
 struct CodeBatch {
   uint32_t w0[kBatch], w1[kBatch];
+  const uint8_t* row0;  // the batch's first slice chunk
 };
 
 // Lane's code words of row i of a batch whose slice chunks start at row0 +
 // i * row_bytes.  Both words of a row go out together and through L1, so the
-// second one meets the first one's sectors on the SM.
+// second one meets the first one's sectors on the SM.  Every lane loads
+// (a lane past the slice's blocks reads the row's first word pair), so the
+// loads need no predicate.
 __device__ __forceinline__ void load_row(const uint8_t* row0, size_t row_bytes, const Lane& L, int i,
                                          CodeBatch& c) {
   const uint32_t* p = reinterpret_cast<const uint32_t*>(row0 + i * row_bytes) + L.wo;
-  c.w0[i] = L.act ? __ldca(p) : 0u;
-  c.w1[i] = L.act ? __ldca(p + 1) : 0u;
+  c.w0[i] = __ldca(p);
+  c.w1[i] = __ldca(p + 1);
 }
 
 __device__ __forceinline__ void load_codes(const uint8_t* row0, size_t row_bytes, const Lane& L, CodeBatch& c) {
+  c.row0 = row0;
 #pragma unroll
   for (int i = 0; i < kBatch; ++i) load_row(row0, row_bytes, L, i, c);
 }
 
-// Per row of the batch: the sum of the lane's six table entries.  Once a
-// row's words are used, the same registers take that row of the batch at
-// `next` (when there is one), so a warp keeps about two batches of code
-// loads in flight with one spare register set.
-__device__ __forceinline__ void lookup_batch(CodeBatch& c, const uint8_t* __restrict__ T, const Lane& L,
-                                             const uint8_t* next, size_t row_bytes, float (&acc)[kBatch]) {
+// One table entry at shared offset `off` from the table.  kBase >= 0: the
+// table's shared address, known at compile time, goes into the load as an
+// immediate; otherwise tb is added.
+template <int kBase>
+__device__ __forceinline__ float tab(uint32_t off, uint32_t tb) {
+  float v;
+  if constexpr (kBase >= 0)
+    asm volatile("ld.shared.f32 %0, [%1+%2];" : "=f"(v) : "r"(off), "n"(kBase));
+  else
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(off + tb));
+  return v;
+}
+
+__device__ __forceinline__ unsigned long long pack2(float lo, float hi) {
+  unsigned long long d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+  return d;
+}
+__device__ __forceinline__ unsigned long long add2(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// Row i's six lookups, packed with row i + 1's (lane-wise pairs of f32).
+template <int kBase>
+__device__ __forceinline__ void lookup_row(uint32_t lo, uint32_t hi, const Lane& L, uint32_t tb, float (&v)[6]) {
+  // offset = stage << 16 | code << 8 | 4 * block: byte 0 and 2 from base, byte 1 the code
+  v[0] = tab<kBase>(prmt_i<0x7604u>(lo, L.base[0]), tb);
+  v[1] = tab<kBase>(prmt_i<0x7614u>(lo, L.base[1]), tb);
+  v[2] = tab<kBase>(prmt_i<0x7624u>(lo, L.base[2]), tb);
+  v[3] = tab<kBase>(prmt_i<0x7634u>(lo, L.base[3]), tb);
+  v[4] = tab<kBase>(prmt_i<0x7604u>(hi, L.base[4]), tb);
+  v[5] = tab<kBase>(prmt_i<0x7614u>(hi, L.base[5]), tb);
+}
+
+// Per row of the batch: the sum of the lane's six table entries, two rows
+// at a time in packed f32 pairs (each row's sum in the order ((a0 + a1) +
+// a2) + ((b0 + b1) + b2)).  Once a row's words are used, the same registers
+// take that row of the batch at `next`, so a warp keeps about two batches of
+// code loads in flight with one spare register set.  With no batch left to
+// fetch, `next` is the batch's own rows again (cached, and never looked up),
+// which keeps the loop free of branches.
+template <int kBase>
+__device__ __forceinline__ void lookup_batch(CodeBatch& c, uint32_t tb, const Lane& L, const uint8_t* next,
+                                             size_t row_bytes, float (&acc)[kBatch]) {
+  c.row0 = next;
 #pragma unroll
-  for (int i = 0; i < kBatch; ++i) {
-    const uint32_t lo = prmt(c.w0[i], c.w1[i], L.sel_lo), hi = prmt(c.w0[i], c.w1[i], L.sel_hi);
-    if (next) load_row(next, row_bytes, L, i, c);
-    // offset = stage << 16 | code << 8 | 4 * block: byte 0 and 2 from base, byte 1 the code
-    const float a0 = *reinterpret_cast<const float*>(T + prmt_i<0x7604u>(lo, L.base[0]));
-    const float a1 = *reinterpret_cast<const float*>(T + prmt_i<0x7614u>(lo, L.base[1]));
-    const float a2 = *reinterpret_cast<const float*>(T + prmt_i<0x7624u>(lo, L.base[2]));
-    const float b0 = *reinterpret_cast<const float*>(T + prmt_i<0x7634u>(lo, L.base[3]));
-    const float b1 = *reinterpret_cast<const float*>(T + prmt_i<0x7604u>(hi, L.base[4]));
-    const float b2 = *reinterpret_cast<const float*>(T + prmt_i<0x7614u>(hi, L.base[5]));
-    acc[i] = ((a0 + a1) + a2) + ((b0 + b1) + b2);
+  for (int i = 0; i < kBatch; i += 2) {
+    float v[6], w[6];
+    {
+      const uint32_t lo = prmt(c.w0[i], c.w1[i], L.sel_lo), hi = prmt(c.w0[i], c.w1[i], L.sel_hi);
+      load_row(next, row_bytes, L, i, c);
+      lookup_row<kBase>(lo, hi, L, tb, v);
+    }
+    {
+      const uint32_t lo = prmt(c.w0[i + 1], c.w1[i + 1], L.sel_lo), hi = prmt(c.w0[i + 1], c.w1[i + 1], L.sel_hi);
+      load_row(next, row_bytes, L, i + 1, c);
+      lookup_row<kBase>(lo, hi, L, tb, w);
+    }
+    const unsigned long long a = add2(add2(pack2(v[0], w[0]), pack2(v[1], w[1])), pack2(v[2], w[2]));
+    const unsigned long long b = add2(add2(pack2(v[3], w[3]), pack2(v[4], w[4])), pack2(v[5], w[5]));
+    const unsigned long long r = add2(a, b);
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(acc[i]), "=f"(acc[i + 1]) : "l"(r));
   }
 }
 
@@ -256,14 +312,27 @@ __device__ __forceinline__ const uint8_t* rvq_routed_record(const LayerArgs& a, 
 // row's slice chunk (8 consecutive rows share a matrix).  out(r) receives
 // row r's partial sum.  Two register sets alternate: while one batch is
 // looked up its registers are refilled with the batch two ahead, and the
-// other set's loads (the next batch) are in flight.
-template <typename Cur, typename Out>
-__device__ __forceinline__ void stream_batches(long long b0, long long b1, int nrows, size_t row_bytes,
-                                               const Lane& L, const uint8_t* T, Cur cur, Out out) {
+// other set's loads (the next batch) are in flight.  A second cursor runs
+// kPfAhead batches ahead and prefetches their chunks into L2 (a chunk of
+// `chunk` bytes spans at most two 128-byte lines: lane 2i takes row i's
+// first byte, lane 2i + 1 the byte 128 on, clipped to the chunk).
+constexpr int kPfAhead = 4;
+template <int kBase, typename Cur, typename Out>
+__device__ __forceinline__ void stream_batches(long long b0, long long b1, int nrows, size_t row_bytes, int chunk,
+                                               const Lane& L, uint32_t tb, Cur cur, Out out) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   long long b = b0 + warp;
   if (b >= b1) return;
   constexpr int W = kRvqWarps;
+  const size_t pf_off = static_cast<size_t>(lane >> 1) * row_bytes + ((lane & 1) ? min(128, chunk - 1) : 0);
+  Cur pf = cur;
+  auto prefetch = [&](long long bb) {  // pf on batch bb
+    if (bb < b1 && lane < 2 * kBatch) asm volatile("prefetch.global.L2 [%0];" ::"l"(pf.ptr() + pf_off));
+    pf.next();
+  };
+  pf.at(static_cast<int>(b + 2 * W) * kBatch);
+#pragma unroll
+  for (int j = 2; j < kPfAhead; ++j) prefetch(b + j * W);
   CodeBatch A, B;
   cur.at(static_cast<int>(b) * kBatch);
   load_codes(cur.ptr(), row_bytes, L, A);
@@ -272,8 +341,9 @@ __device__ __forceinline__ void stream_batches(long long b0, long long b1, int n
   cur.next();  // on batch b + 2W: the refill of the first set
   auto one = [&](CodeBatch& c, long long bb) {
     float acc[kBatch];
-    const uint8_t* next = bb + 2 * W < b1 ? cur.ptr() : nullptr;
-    lookup_batch(c, T, L, next, row_bytes, acc);
+    prefetch(bb + kPfAhead * W);
+    const uint8_t* next = bb + 2 * W < b1 ? cur.ptr() : c.row0;
+    lookup_batch<kBase>(c, tb, L, next, row_bytes, acc);
     cur.next();
     const float v = rvq_bfly8(acc, lane);
     const int r = static_cast<int>(bb) * kBatch + (lane >> 2);
@@ -359,6 +429,7 @@ __global__ void __launch_bounds__(kRvqThreads, 1) rvq_gateup_kernel(const __grid
                                                                     const RvqPlan pl) {
   extern __shared__ __align__(16) uint8_t smem[];
   uint8_t* T = smem;
+  const uint32_t tb = static_cast<uint32_t>(__cvta_generic_to_shared(T));
   uint4* sbook = reinterpret_cast<uint4*>(smem + kTabBytes);
   const uint8_t** mat = reinterpret_cast<const uint8_t**>(smem + kTabBytes + kBookBytes);
   const int lane = threadIdx.x & 31;
@@ -402,8 +473,11 @@ __global__ void __launch_bounds__(kRvqThreads, 1) rvq_gateup_kernel(const __grid
     const long long u0 = u * nbu;
     GuCur gc;
     gc.mat = mat, gc.row_bytes = row_bytes, gc.k = a.k, gc.F = a.F, gc.Fs = a.Fs;
-    stream_batches(max(lo, u0) - u0, min(hi, u0 + nbu) - u0, pl.R, row_bytes, L, T, gc,
-                   [&](int r, float val) { part[r] = val; });
+    const auto out = [&](int r, float val) { part[r] = val; };
+    if (tb == kDynSmemBase)
+      stream_batches<kDynSmemBase>(max(lo, u0) - u0, min(hi, u0 + nbu) - u0, pl.R, row_bytes, 3 * nb, L, tb, gc, out);
+    else
+      stream_batches<-1>(max(lo, u0) - u0, min(hi, u0 + nbu) - u0, pl.R, row_bytes, 3 * nb, L, tb, gc, out);
   }
   if (!routed) pdl_wait();
 }
@@ -417,6 +491,7 @@ __global__ void __launch_bounds__(kRvqThreads, 1) rvq_down_kernel(const __grid_c
                                                                   const RvqPlan pl) {
   extern __shared__ __align__(16) uint8_t smem[];
   uint8_t* T = smem;
+  const uint32_t tb = static_cast<uint32_t>(__cvta_generic_to_shared(T));
   uint4* sbook = reinterpret_cast<uint4*>(smem + kTabBytes);
   float* hs = reinterpret_cast<float*>(smem + kTabBytes + kBookBytes);  // the slice's 512 h values
   const int lane = threadIdx.x & 31;
@@ -463,8 +538,11 @@ __global__ void __launch_bounds__(kRvqThreads, 1) rvq_down_kernel(const __grid_c
     const long long u0 = u * nbu;
     FlatCur fc;
     fc.base = codes, fc.row_bytes = row_bytes;
-    stream_batches(max(lo, u0) - u0, min(hi, u0 + nbu) - u0, a.H, row_bytes, L, T, fc,
-                   [&](int r, float val) { y[r] = val; });
+    const auto out = [&](int r, float val) { y[r] = val; };
+    if (tb == kDynSmemBase)
+      stream_batches<kDynSmemBase>(max(lo, u0) - u0, min(hi, u0 + nbu) - u0, a.H, row_bytes, 3 * nb, L, tb, fc, out);
+    else
+      stream_batches<-1>(max(lo, u0) - u0, min(hi, u0 + nbu) - u0, a.H, row_bytes, 3 * nb, L, tb, fc, out);
   }
 }
 
