@@ -341,6 +341,28 @@ __global__ void __launch_bounds__(kBtThreads, 1) ffn_bt_kernel(const __grid_cons
   const uint4* xqw = reinterpret_cast<const uint4*>(a.ws.xq);
   const float2* xqs = reinterpret_cast<const float2*>(a.ws.xq + static_cast<size_t>(T) * C * 64);
   bool xready = false, abort = false;
+  // Token t's activations of this lane's column into L1 ahead of their use.
+  // The router writes them before it counts itself done and they do not
+  // change for the rest of the grid, so once the count has been acquired
+  // they are read through L1 (one token's 72 bytes a column fit beside the
+  // next one's prefetch).
+  const auto prefetch_x = [&](int t) {
+    if (!gact || !xready) return;
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      asm volatile("prefetch.global.L1 [%0];" ::"l"(xqw + (static_cast<size_t>(t) * 4 + k) * C + col));
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(xqs + static_cast<size_t>(t) * C + col));
+  };
+  // The next ring position's first token, when its weights are already in
+  // and it is a gate|up item.
+  const auto prefetch_next = [&](const RingPos& at) {
+    RingPos nx = at;
+    nx.next(NST);
+    if (!mbar_test_wait(&full[nx.s], nx.ph)) return;
+    const int c2 = s_code[nx.s];
+    if (c2 < 0 || !(c2 & 1)) return;
+    prefetch_x(s_tok[tab[c2 >> 20].pair0]);
+  };
 
   RingPos pos;
   for (;; pos.next(NST)) {
@@ -373,11 +395,13 @@ __global__ void __launch_bounds__(kBtThreads, 1) ffn_bt_kernel(const __grid_cons
         for (int m = 0; m < R; ++m) part[m] = 0.f;
         if (gact && !abort) {
           XChunk X;
-          const uint4 k0 = __ldcg(xqw + (static_cast<size_t>(t) * 4 + 0) * C + col);
-          const uint4 k1 = __ldcg(xqw + (static_cast<size_t>(t) * 4 + 1) * C + col);
-          const uint4 k2 = __ldcg(xqw + (static_cast<size_t>(t) * 4 + 2) * C + col);
-          const uint4 k3 = __ldcg(xqw + (static_cast<size_t>(t) * 4 + 3) * C + col);
-          const float2 ss = __ldcg(xqs + static_cast<size_t>(t) * C + col);
+          const uint4 k0 = __ldca(xqw + (static_cast<size_t>(t) * 4 + 0) * C + col);
+          const uint4 k1 = __ldca(xqw + (static_cast<size_t>(t) * 4 + 1) * C + col);
+          const uint4 k2 = __ldca(xqw + (static_cast<size_t>(t) * 4 + 2) * C + col);
+          const uint4 k3 = __ldca(xqw + (static_cast<size_t>(t) * 4 + 3) * C + col);
+          const float2 ss = __ldca(xqs + static_cast<size_t>(t) * C + col);
+          if (u + 1 < ntok) prefetch_x(s_tok[en.pair0 + u + 1]);
+          else prefetch_next(pos);
           X.eh[0] = k0.x, X.eh[1] = k0.y, X.eh[2] = k0.z, X.eh[3] = k0.w;
           X.el[0] = k1.x, X.el[1] = k1.y, X.el[2] = k1.z, X.el[3] = k1.w;
           X.oh[0] = k2.x, X.oh[1] = k2.y, X.oh[2] = k2.z, X.oh[3] = k2.w;
@@ -414,6 +438,7 @@ __global__ void __launch_bounds__(kBtThreads, 1) ffn_bt_kernel(const __grid_cons
                       g2 = __ldcg(xw + 2 * nc + g.col), g3 = __ldcg(xw + 3 * nc + g.col);
           const float4 sc4 = __ldcg(reinterpret_cast<const float4*>(xb + 64 * nc) + g.col);
           const float4 sm4 = __ldcg(reinterpret_cast<const float4*>(xb + 80 * nc) + g.col);
+          if (u + 1 == ntok) prefetch_next(pos);
           Xh.eh[0] = g0.x, Xh.eh[1] = g0.y, Xh.eh[2] = g0.z, Xh.eh[3] = g0.w;
           Xh.el[0] = g1.x, Xh.el[1] = g1.y, Xh.el[2] = g1.z, Xh.el[3] = g1.w;
           Xh.oh[0] = g2.x, Xh.oh[1] = g2.y, Xh.oh[2] = g2.z, Xh.oh[3] = g2.w;
