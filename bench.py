@@ -622,13 +622,12 @@ def run_ours(args, world, rank, local):
                                 hids.data_ptr(), hw.data_ptr(), dl.ws.data_ptr(), dl.ws_bytes,
                                 stream.cuda_stream)
         dt = max_over_ranks(world, time.perf_counter() - t0, device)
-        r256 = lambda v: (v + 255) // 256 * 256
         out["e2e"] = {"value": B * Ke * world / dt, "unit": "tokens/s",
                       "h2d_bytes_per_step": B * s.H * 2,
-                      # one copy of the staged bf16 output, ids and weights (256-byte carve)
-                      "d2h_bytes_per_step": r256(B * s.H * 2) + r256(B * s.k * 4) + B * s.k * 4, "steps": Ke,
-                      "entry": "moe_decode_host (pinned host buffers, one copy in, one copy out, "
-                               "sync per step)"}
+                      # bf16 output, ids and weights, written by the kernels into mapped host memory
+                      "d2h_bytes_per_step": B * s.H * 2 + 2 * B * s.k * 4, "steps": Ke,
+                      "entry": "moe_decode_host (pinned host buffers: one copy in; the kernels write the "
+                               "outputs, ids and weights into the layer's mapped output buffer; sync per step)"}
 
         if rank == 0 and world == 1:
             out["cpu_baseline"] = cpu_baseline(wl, s)

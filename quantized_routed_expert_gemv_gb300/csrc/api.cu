@@ -68,11 +68,13 @@ struct moe_layer {
   moe::LayerMaps maps;  // tiled-load descriptors of the code matrices (prefill)
   // moe_decode_host: page-locked staging buffers for the inputs and the
   // outputs (allocated by the first call, sized for max_tokens, freed by
-  // moe_close), a private stream and a few captured steps (copy in, kernels,
-  // copy out) replayed as CUDA graphs
+  // moe_close), a private stream and a few captured steps (copy in, kernels)
+  // replayed as CUDA graphs.  The output buffer is mapped: the kernels write
+  // the outputs, ids and weights straight into it (host_out_dev).
   std::mutex* host_mu;
   uint8_t* host_in;
   uint8_t* host_out;
+  uint8_t* host_out_dev;
   size_t host_out_bytes;
   cudaStream_t host_st;
   struct HostGraph {
@@ -429,11 +431,15 @@ static bool bt_planned(const moe_layer* L, LayerArgs& a) {
   return true;
 }
 
+// ids_host / w_host: optional copies of ids and weights in mapped host
+// memory, written by the router beside the device ones.
 static int run(moe_layer* L, const uint16_t* x, int32_t T, uint16_t* ob, float* of, int32_t* ids,
-               float* wts, void* ws, size_t ws_bytes, void* stream, Path path, const char* name) {
+               float* wts, void* ws, size_t ws_bytes, void* stream, Path path, const char* name,
+               int32_t* ids_host = nullptr, float* w_host = nullptr) {
   LayerArgs a;
   const int rc = prepare(L, x, T, ob, of, ids, wts, ws, ws_bytes, path, true, &a, name);
   if (rc || T == 0) return rc;
+  a.ids_host = ids_host, a.weights_host = ids_host ? w_host : nullptr;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (L->d.wbits == 3) {
@@ -458,6 +464,7 @@ static int run(moe_layer* L, const uint16_t* x, int32_t T, uint16_t* ob, float* 
       const size_t H = L->d.hidden, k = L->d.top_k;
       b.T = 1, b.x = x + t * H, b.out_bf16 = ob + t * H, b.out_f32 = of ? of + t * H : nullptr;
       b.ids = ids + t * k, b.weights = wts + t * k;
+      if (ids_host) b.ids_host = ids_host + t * k, b.weights_host = w_host + t * k;
       b.prof_on = t == 0 ? a.prof_on : 0;  // the profiling hook times the first token's kernels
       e = moe::launch_decode_b1(b, L->num_sms, st);
     }
@@ -497,9 +504,14 @@ static int host_entry_setup(moe_layer* L, void* ws) {
   cudaError_t e;
   if ((e = cudaHostAlloc(&pin, n * H * 2, cudaHostAllocDefault)))
     return cuda_fail(e, "moe_decode_host: page-locked input buffer");
-  if ((e = cudaHostAlloc(&pout, out_bytes, cudaHostAllocDefault))) {
+  if ((e = cudaHostAlloc(&pout, out_bytes, cudaHostAllocMapped))) {
     cudaFreeHost(pin);
     return cuda_fail(e, "moe_decode_host: page-locked output buffer");
+  }
+  void* pout_dev = nullptr;
+  if ((e = cudaHostGetDevicePointer(&pout_dev, pout, 0))) {
+    cudaFreeHost(pin), cudaFreeHost(pout);
+    return cuda_fail(e, "moe_decode_host: device address of the output buffer");
   }
   if ((e = cudaStreamCreateWithFlags(&L->host_st, cudaStreamNonBlocking))) {
     cudaFreeHost(pin), cudaFreeHost(pout);
@@ -507,22 +519,24 @@ static int host_entry_setup(moe_layer* L, void* ws) {
     return cuda_fail(e, "moe_decode_host: capture stream");
   }
   L->host_in = static_cast<uint8_t*>(pin), L->host_out = static_cast<uint8_t*>(pout), L->host_out_bytes = out_bytes;
+  L->host_out_dev = static_cast<uint8_t*>(pout_dev);
   return MOE_OK;
 }
 
-// Copy in, the step, copy out, on `st`, between the layer's staging buffers
-// and the workspace's.
+// Copy in, then the step, on `st`.  The outputs land in the layer's mapped
+// output buffer, at the offsets the workspace's output staging area has:
+// the kernels write the bf16 (and f32) outputs there, and the router writes
+// ids and weights both to the workspace (which the expert kernels read) and
+// there.  No copy out: the host reads the buffer after the synchronisation.
 static int host_entry_step(moe_layer* L, int32_t B, bool f32, const moe::Workspace& w, void* ws, size_t ws_bytes,
-                           size_t span, cudaStream_t st) {
+                           size_t o_ids, size_t o_w, size_t o_f, cudaStream_t st) {
   const size_t H = L->d.hidden;
   cudaError_t e = cudaMemcpyAsync(w.x_stage, L->host_in, static_cast<size_t>(B) * H * 2, cudaMemcpyHostToDevice, st);
   if (e) return cuda_fail(e, "moe_decode_host: copy in");
-  const int rc = moe_decode(L, w.x_stage, B, w.ob_stage, f32 ? w.of_stage : nullptr, w.ids_stage, w.w_stage, ws,
-                            ws_bytes, st);
-  if (rc) return rc;
-  if ((e = cudaMemcpyAsync(L->host_out, w.ob_stage, span, cudaMemcpyDeviceToHost, st)))
-    return cuda_fail(e, "moe_decode_host: copy out");
-  return MOE_OK;
+  uint8_t* const hd = L->host_out_dev;
+  return run(L, w.x_stage, B, reinterpret_cast<uint16_t*>(hd), f32 ? reinterpret_cast<float*>(hd + o_f) : nullptr,
+             w.ids_stage, w.w_stage, ws, ws_bytes, st, Path::kDecode, "moe_decode_host",
+             reinterpret_cast<int32_t*>(hd + o_ids), reinterpret_cast<float*>(hd + o_w));
 }
 
 extern "C" int moe_decode_host(moe_layer* L, const uint16_t* x_host, int32_t B, uint16_t* ob_host,
@@ -547,7 +561,6 @@ extern "C" int moe_decode_host(moe_layer* L, const uint16_t* x_host, int32_t B, 
   const size_t o_w = reinterpret_cast<uint8_t*>(w.w_stage) - s0;
   const size_t o_f = reinterpret_cast<uint8_t*>(w.of_stage) - s0;
   const bool f32 = of_host != nullptr;
-  const size_t span = f32 ? o_f + b * H * 4 : o_w + b * k * 4;
   std::lock_guard<std::mutex> lock(*L->host_mu);
   int rc = host_entry_setup(L, ws);
   if (rc) return rc;
@@ -564,7 +577,7 @@ extern "C" int moe_decode_host(moe_layer* L, const uint16_t* x_host, int32_t B, 
   if (exec) {
     if ((e = cudaGraphLaunch(exec, st))) return cuda_fail(e, "moe_decode_host: graph launch");
   } else {
-    if ((rc = host_entry_step(L, B, f32, w, ws, ws_bytes, span, st))) return rc;
+    if ((rc = host_entry_step(L, B, f32, w, ws, ws_bytes, o_ids, o_w, o_f, st))) return rc;
   }
   if ((e = cudaStreamSynchronize(st))) return cuda_fail(e, "moe_decode_host: synchronize");
   std::memcpy(ob_host, L->host_out, b * H * 2);
@@ -577,7 +590,7 @@ extern "C" int moe_decode_host(moe_layer* L, const uint16_t* x_host, int32_t B, 
     cudaGraph_t graph = nullptr;
     cudaGraphExec_t ge = nullptr;
     if (cudaStreamBeginCapture(L->host_st, cudaStreamCaptureModeThreadLocal) == cudaSuccess) {
-      const int crc = host_entry_step(L, B, f32, w, ws, ws_bytes, span, L->host_st);
+      const int crc = host_entry_step(L, B, f32, w, ws, ws_bytes, o_ids, o_w, o_f, L->host_st);
       const cudaError_t ce = cudaStreamEndCapture(L->host_st, &graph);
       if (crc == MOE_OK && ce == cudaSuccess && graph && cudaGraphInstantiate(&ge, graph, 0) == cudaSuccess) {
         auto& slot = L->hg[L->hg_next];

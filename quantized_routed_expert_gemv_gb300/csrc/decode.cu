@@ -279,6 +279,7 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const __grid_con
     if (lane < k) {
       a.ids[t * k + lane] = myi;
       a.weights[t * k + lane] = ex / z;
+      if (a.ids_host) a.ids_host[t * k + lane] = myi, a.weights_host[t * k + lane] = ex / z;
     }
     __syncwarp();
   }

@@ -146,7 +146,10 @@ __device__ __forceinline__ void topk_block_b1(const LayerArgs& a, uint64_t (*lis
   const float lmax = __shfl_sync(kAll, myl, 0);
   const float ex = (lane < k) ? expf(myl - lmax) : 0.f;
   const float z = warp_add(ex);
-  if (lane < k) a.ids[lane] = myi, a.weights[lane] = ex / z;
+  if (lane < k) {
+    a.ids[lane] = myi, a.weights[lane] = ex / z;
+    if (a.ids_host) a.ids_host[lane] = myi, a.weights_host[lane] = ex / z;
+  }
   // grouping for one token: active experts in ascending id, one pair each;
   // the sort carries each expert's position in ids[] in the low 5 bits
   const uint32_t s = warp_sort_asc32(lane < k ? (static_cast<uint32_t>(myi) << 5) | lane : 0xFFFFFFFFu, lane);

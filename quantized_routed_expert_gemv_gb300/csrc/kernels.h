@@ -109,6 +109,8 @@ struct LayerArgs {
   float* out_f32;          // [T][H] or null
   int32_t* ids;            // [T][k]
   float* weights;          // [T][k]
+  int32_t* ids_host;       // [T][k] copies of ids and weights in mapped page-locked host
+  float* weights_host;     // memory (the router writes both), or null
   Workspace ws;
   RecordOffsets off_r, off_s;  // layouts for F and Fs
   // per-launch geometry (plan_decode / plan_prefill)
