@@ -739,18 +739,28 @@ __global__ void __maxnreg__(168)
       if (stop) break;
       if (MODE == 0) {
         // SwiGLU: up rows (64..127, warps 2-3) hand their values to the gate rows
+        // (np is a multiple of 16: one test per 16 tokens, so each block of
+        // 16 is straight-line code whose exponentials and divisions overlap)
         if (q >= 2) {
           float* xr = s_x + ((q - 2) * 32 + lane) * kXPitch;
 #pragma unroll
-          for (int j = 0; j < kBlkTokens; ++j)
-            if (j < np) xr[j] = acc[j];
+          for (int j0 = 0; j0 < kBlkTokens; j0 += 16)
+            if (j0 < np)
+#pragma unroll
+              for (int j = j0; j < j0 + 16; ++j) xr[j] = acc[j];
         }
         named_bar(1, kEpiWarps * 32);
         if (q < 2) {  // h = silu(g) * u of the tile's 64 rows, into the exchange rows
           float* xr = s_x + row * kXPitch;
 #pragma unroll
-          for (int n = 0; n < kBlkTokens; ++n)
-            if (n < np) xr[n] = silu_f(acc[n]) * xr[n];
+          for (int n0 = 0; n0 < kBlkTokens; n0 += 16)
+            if (n0 < np) {
+              float u[16];
+#pragma unroll
+              for (int j = 0; j < 16; ++j) u[j] = xr[n0 + j];
+#pragma unroll
+              for (int j = 0; j < 16; ++j) xr[n0 + j] = silu_f(acc[n0 + j]) * u[j];
+            }
         }
         named_bar(1, kEpiWarps * 32);
         // The tile's h in the down GEMM's B layout (bf16 hi + lo): its 64
