@@ -345,9 +345,13 @@ __global__ void __launch_bounds__(kBtThreads, 1) ffn_bt_kernel(const __grid_cons
   // The router writes them before it counts itself done and they do not
   // change for the rest of the grid, so once the count has been acquired
   // they are read through L1 (one token's 72 bytes a column fit beside the
-  // next one's prefetch).
+  // next one's prefetch).  Only for rows of at least 4096 values: there
+  // the L2 round trip at the start of a token's pass is the larger cost
+  // (H = 7168, B = 4: 302 -> 295 us per step); at H = 2048 the added
+  // instructions cost more than they hide (B = 4 and 16: 2-4% slower).
+  const bool xpf = C >= 128;
   const auto prefetch_x = [&](int t) {
-    if (!gact || !xready) return;
+    if (!xpf || !gact || !xready) return;
 #pragma unroll
     for (int k = 0; k < 4; ++k)
       asm volatile("prefetch.global.L1 [%0];" ::"l"(xqw + (static_cast<size_t>(t) * 4 + k) * C + col));
@@ -356,6 +360,7 @@ __global__ void __launch_bounds__(kBtThreads, 1) ffn_bt_kernel(const __grid_cons
   // The next ring position's first token, when its weights are already in
   // and it is a gate|up item.
   const auto prefetch_next = [&](const RingPos& at) {
+    if (!xpf) return;
     RingPos nx = at;
     nx.next(NST);
     if (!mbar_test_wait(&full[nx.s], nx.ph)) return;
