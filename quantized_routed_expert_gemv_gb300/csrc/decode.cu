@@ -284,14 +284,19 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const __grid_con
     __syncwarp();
   }
 
-  // the last token block: every token's ids are in; group the pairs
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) s_last = (atomicAdd(tk_done, 1u) == static_cast<unsigned>(TB - 1));
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  if (tid == 0) *tk_done = 0u;
+  // the last token block: every token's ids are in; group the pairs (with
+  // one token block this CTA took every token's top-k itself)
+  if (TB > 1) {
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_last = (atomicAdd(tk_done, 1u) == static_cast<unsigned>(TB - 1));
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    if (tid == 0) *tk_done = 0u;
+  } else {
+    __syncthreads();
+  }
 
   for (int i = tid; i < 4 * E; i += kRouterThreads) sel[i] = 0u;
   __syncthreads();
@@ -849,10 +854,14 @@ static cudaError_t mark(const LayerArgs& a, int i, cudaStream_t st) {
 // CTAs of the router: row blocks x token blocks, up to two waves (the kernel
 // takes 128 registers a thread, one CTA per SM): more token blocks shorten
 // each CTA's serial token passes.
+// Decode batches of up to 16 tokens take one token block: one wave of CTAs
+// (a second wave started up to 9 us late at E = 512) and one CTA for every
+// token's top-k and the grouping, with no second completion count.
 int decode_router_grid(const LayerArgs& a, int num_sms) {
   const int nt = a.T == 1 ? 1 : 2;
   const int rb = (a.E + kRouterRows - 1) / kRouterRows;
   const int tp = nt * router_groups(a.H);  // tokens per pass of a CTA
+  if (a.T <= 16) return rb;
   const int tb = std::max(1, std::min({(a.T + tp - 1) / tp, (2 * num_sms) / rb, kRouterMaxTokenBlocks}));
   return rb * tb;
 }
