@@ -323,8 +323,10 @@ static size_t carve(const moe_layer* L, int T, moe::Workspace* ws, uint8_t* base
   const size_t o_ae = c.take(E * 4), o_ao = c.take(E * 4), o_ac = c.take(E * 4);
   const size_t o_pt = c.take(t * k * 4), o_ps = c.take(t * k * 4);
   const size_t o_h = c.take(t * k * F * 4), o_hs = c.take(t * Fs * 4);
-  // host-entry staging: the outputs back to back (bf16, ids, weights, then
-  // f32), so one device-to-host copy returns all of them
+  // host-entry staging: x, then the outputs back to back (bf16, ids,
+  // weights, then f32).  The same offsets lay out the layer's mapped output
+  // buffer, which the kernels write; the ids and weights here are the device
+  // copies the expert kernels read.
   const size_t o_xs = c.take(t * H * 2), o_obs = c.take(t * H * 2);
   const size_t o_ids = c.take(t * k * 4), o_w = c.take(t * k * 4), o_ofs = c.take(t * H * 4);
   LayerArgs a = base_args(L);
