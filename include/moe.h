@@ -174,15 +174,17 @@ int moe_prefill_chunk(moe_layer *layer, const uint16_t *x, int32_t T, uint16_t *
  * output back (out_f32_host may be NULL) and synchronises `stream` before it
  * returns.  Device staging lives in the workspace.  The layer keeps page-
  * locked input and output buffers and a private stream (made by its first
- * moe_decode_host call, sized for max_tokens, freed by moe_close): x goes
- * through the input buffer and one host-to-device copy; the output buffer
- * is mapped into the device's address space, and the kernels write the
- * outputs there directly (the router writes ids and weights both to the
- * workspace and there), from where they go to the caller's buffers after
- * the synchronisation.  The first call for a given (workspace, B,
- * out_f32_host set or not) runs plain launches and then captures the step
- * (copy in, kernels) into a CUDA graph; later such calls replay it with one
- * graph launch on `stream` (the layer keeps the last 4).  The profiling hook always takes plain
+ * moe_decode_host call, sized for max_tokens, freed by moe_close).  Both
+ * buffers are mapped into the device's address space: x goes through the
+ * input buffer, from which a small kernel copies it into the workspace (a
+ * single-token router overlaps that copy as its programmatic dependent);
+ * the kernels write the outputs into the output buffer directly (the router
+ * writes ids and weights both to the workspace and there), from where they
+ * go to the caller's buffers after the synchronisation.  The first call for
+ * a given (workspace, B, out_f32_host set or not) runs plain launches and
+ * then captures the step (copy kernel, layer kernels) into a CUDA graph;
+ * later such calls replay it with one graph launch on `stream` (the layer
+ * keeps the last 4).  The profiling hook always takes plain
  * launches.  Calls on one layer from several threads are serialised by a
  * lock. */
 int moe_decode_host(moe_layer *layer, const uint16_t *x_host, int32_t B,

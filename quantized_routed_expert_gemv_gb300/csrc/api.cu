@@ -23,6 +23,7 @@ cudaError_t set_decode_attributes(int smem_optin);
 cudaError_t set_b1_attributes(int smem_optin);
 bool plan_b1(LayerArgs& a, int num_sms, int smem_optin);
 cudaError_t launch_decode_b1(const LayerArgs& a, int num_sms, cudaStream_t st);
+cudaError_t launch_stage_x(const void* src, void* dst, size_t bytes, cudaStream_t st);
 cudaError_t launch_decode(const LayerArgs& a, int num_sms, cudaStream_t st);
 cudaError_t set_prefill_attributes(int smem_optin);
 cudaError_t launch_prefill(const LayerArgs& a, const LayerMaps* maps, int num_sms, cudaStream_t st);
@@ -73,6 +74,7 @@ struct moe_layer {
   // the outputs, ids and weights straight into it (host_out_dev).
   std::mutex* host_mu;
   uint8_t* host_in;
+  uint8_t* host_in_dev;
   uint8_t* host_out;
   uint8_t* host_out_dev;
   size_t host_out_bytes;
@@ -434,14 +436,17 @@ static bool bt_planned(const moe_layer* L, LayerArgs& a) {
 }
 
 // ids_host / w_host: optional copies of ids and weights in mapped host
-// memory, written by the router beside the device ones.
+// memory, written by the router beside the device ones.  x_pdl: x is being
+// written by the kernel launched just before this call (the host entry's
+// staging kernel), which a single-token router may overlap.
 static int run(moe_layer* L, const uint16_t* x, int32_t T, uint16_t* ob, float* of, int32_t* ids,
                float* wts, void* ws, size_t ws_bytes, void* stream, Path path, const char* name,
-               int32_t* ids_host = nullptr, float* w_host = nullptr) {
+               int32_t* ids_host = nullptr, float* w_host = nullptr, bool x_pdl = false) {
   LayerArgs a;
   const int rc = prepare(L, x, T, ob, of, ids, wts, ws, ws_bytes, path, true, &a, name);
   if (rc || T == 0) return rc;
   a.ids_host = ids_host, a.weights_host = ids_host ? w_host : nullptr;
+  a.x_pdl = x_pdl ? 1 : 0;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (L->d.wbits == 3) {
@@ -467,6 +472,7 @@ static int run(moe_layer* L, const uint16_t* x, int32_t T, uint16_t* ob, float* 
       b.T = 1, b.x = x + t * H, b.out_bf16 = ob + t * H, b.out_f32 = of ? of + t * H : nullptr;
       b.ids = ids + t * k, b.weights = wts + t * k;
       if (ids_host) b.ids_host = ids_host + t * k, b.weights_host = w_host + t * k;
+      b.x_pdl = t == 0 ? a.x_pdl : 0;  // later tokens follow the previous token's kernels
       b.prof_on = t == 0 ? a.prof_on : 0;  // the profiling hook times the first token's kernels
       e = moe::launch_decode_b1(b, L->num_sms, st);
     }
@@ -504,16 +510,16 @@ static int host_entry_setup(moe_layer* L, void* ws) {
       n * H * 4;
   void *pin = nullptr, *pout = nullptr;
   cudaError_t e;
-  if ((e = cudaHostAlloc(&pin, n * H * 2, cudaHostAllocDefault)))
+  if ((e = cudaHostAlloc(&pin, n * H * 2, cudaHostAllocMapped)))
     return cuda_fail(e, "moe_decode_host: page-locked input buffer");
   if ((e = cudaHostAlloc(&pout, out_bytes, cudaHostAllocMapped))) {
     cudaFreeHost(pin);
     return cuda_fail(e, "moe_decode_host: page-locked output buffer");
   }
-  void* pout_dev = nullptr;
-  if ((e = cudaHostGetDevicePointer(&pout_dev, pout, 0))) {
+  void *pin_dev = nullptr, *pout_dev = nullptr;
+  if ((e = cudaHostGetDevicePointer(&pin_dev, pin, 0)) || (e = cudaHostGetDevicePointer(&pout_dev, pout, 0))) {
     cudaFreeHost(pin), cudaFreeHost(pout);
-    return cuda_fail(e, "moe_decode_host: device address of the output buffer");
+    return cuda_fail(e, "moe_decode_host: device address of a page-locked buffer");
   }
   if ((e = cudaStreamCreateWithFlags(&L->host_st, cudaStreamNonBlocking))) {
     cudaFreeHost(pin), cudaFreeHost(pout);
@@ -522,23 +528,28 @@ static int host_entry_setup(moe_layer* L, void* ws) {
   }
   L->host_in = static_cast<uint8_t*>(pin), L->host_out = static_cast<uint8_t*>(pout), L->host_out_bytes = out_bytes;
   L->host_out_dev = static_cast<uint8_t*>(pout_dev);
+  L->host_in_dev = static_cast<uint8_t*>(pin_dev);
   return MOE_OK;
 }
 
-// Copy in, then the step, on `st`.  The outputs land in the layer's mapped
-// output buffer, at the offsets the workspace's output staging area has:
-// the kernels write the bf16 (and f32) outputs there, and the router writes
-// ids and weights both to the workspace (which the expert kernels read) and
-// there.  No copy out: the host reads the buffer after the synchronisation.
+// Copy in, then the step, on `st`.  A small kernel copies x from the mapped
+// input buffer into the workspace; a single-token router is launched as its
+// programmatic dependent, so the router's launch and weight loads overlap the
+// copy (other paths follow it in plain stream order).  The outputs land in
+// the layer's mapped output buffer, at the offsets the workspace's output
+// staging area has: the kernels write the bf16 (and f32) outputs there, and
+// the router writes ids and weights both to the workspace (which the expert
+// kernels read) and there.  No copy out: the host reads the buffer after the
+// synchronisation.
 static int host_entry_step(moe_layer* L, int32_t B, bool f32, const moe::Workspace& w, void* ws, size_t ws_bytes,
                            size_t o_ids, size_t o_w, size_t o_f, cudaStream_t st) {
   const size_t H = L->d.hidden;
-  cudaError_t e = cudaMemcpyAsync(w.x_stage, L->host_in, static_cast<size_t>(B) * H * 2, cudaMemcpyHostToDevice, st);
+  cudaError_t e = moe::launch_stage_x(L->host_in_dev, w.x_stage, static_cast<size_t>(B) * H * 2, st);
   if (e) return cuda_fail(e, "moe_decode_host: copy in");
   uint8_t* const hd = L->host_out_dev;
   return run(L, w.x_stage, B, reinterpret_cast<uint16_t*>(hd), f32 ? reinterpret_cast<float*>(hd + o_f) : nullptr,
              w.ids_stage, w.w_stage, ws, ws_bytes, st, Path::kDecode, "moe_decode_host",
-             reinterpret_cast<int32_t*>(hd + o_ids), reinterpret_cast<float*>(hd + o_w));
+             reinterpret_cast<int32_t*>(hd + o_ids), reinterpret_cast<float*>(hd + o_w), true);
 }
 
 extern "C" int moe_decode_host(moe_layer* L, const uint16_t* x_host, int32_t B, uint16_t* ob_host,

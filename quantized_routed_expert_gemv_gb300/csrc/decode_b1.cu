@@ -169,7 +169,6 @@ constexpr int kR1Rows = 4;  // rows per CTA pass: 128 CTAs for 512 experts (the 
 
 __global__ void __launch_bounds__(kR1Threads) router_b1_kernel(const __grid_constant__ LayerArgs a) {
   extern __shared__ __align__(16) float rsm[];
-  pdl_launch_dependents();
   if (blockIdx.x == 0 && threadIdx.x == 0) a.ws.ctl[3] = 0u;  // shared-only gate|up claims
   const int H = a.H, E = a.E;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -191,6 +190,11 @@ __global__ void __launch_bounds__(kR1Threads) router_b1_kernel(const __grid_cons
     }
   };
   load_rows(blockIdx.x * kR1Rows);  // weight rows in flight before the activations
+  // When x is staged by the kernel before this one (x_pdl), wait for it; the
+  // dependents (which read x too) are released only after that, so they see
+  // x complete.  Launched in plain stream order, the wait returns at once.
+  pdl_wait();
+  pdl_launch_dependents();
 
   // token chunk: 16 bf16 activations, pre-scaled per byte position
   float2 X[8];
@@ -1241,7 +1245,24 @@ static cudaError_t mark1(const LayerArgs& a, int i, cudaStream_t st) {
 
 static cudaError_t launch_router1(const LayerArgs& a, int num_sms, cudaStream_t st) {
   const int rgrid = std::max(1, std::min((a.E + kR1Rows - 1) / kR1Rows, 2 * num_sms));
-  return launch1((const void*)router_b1_kernel, rgrid, kR1Threads, router_b1_smem_bytes(a.E), st, false, a);
+  return launch1((const void*)router_b1_kernel, rgrid, kR1Threads, router_b1_smem_bytes(a.E), st,
+                 a.x_pdl != 0 && !a.prof_on, a);
+}
+
+// Copies n16 16-byte words from src (mapped page-locked host memory) to dst
+// (device).  It releases its dependents at once: a single-token router
+// launched after it loads its weight rows meanwhile and waits for the copy
+// before it reads x.
+__global__ void __launch_bounds__(256) stage_x_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, int n16) {
+  pdl_launch_dependents();
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += gridDim.x * blockDim.x) dst[i] = src[i];
+}
+
+cudaError_t launch_stage_x(const void* src, void* dst, size_t bytes, cudaStream_t st) {
+  const int n16 = static_cast<int>(bytes / 16);
+  const int grid = std::max(1, std::min(8, (n16 + 255) / 256));
+  stage_x_kernel<<<grid, 256, 0, st>>>(static_cast<const uint4*>(src), static_cast<uint4*>(dst), n16);
+  return cudaGetLastError();
 }
 
 static cudaError_t launch_gateup1(const LayerArgs& a, int part, int num_sms, cudaStream_t st, bool pdl) {

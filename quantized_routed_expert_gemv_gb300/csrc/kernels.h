@@ -125,6 +125,9 @@ struct LayerArgs {
                                // and count (f1_nst == 0: not planned)
   PrefillPtrs pf;              // prefill chunk scratch (tensor-core path)
   int xq_nconv;                // router CTAs that write ws.xq (0: none)
+  int x_pdl;                   // x is written by the kernel launched just before the single-
+                               // token router (the host entry's staging kernel): the router is
+                               // its programmatic dependent and waits for it before reading x
   int prof_on;                 // record prof[] events between kernels, no PDL
   void* prof[4];               // cudaEvent_t: before router / gate|up / down, after down
 };
