@@ -627,8 +627,9 @@ def run_ours(args, world, rank, local):
                       "h2d_bytes_per_step": B * s.H * 2,
                       # bf16 output, ids and weights, written by the kernels into mapped host memory
                       "d2h_bytes_per_step": B * s.H * 2 + 2 * B * s.k * 4, "steps": Ke,
-                      "entry": "moe_decode_host (pinned host buffers: one copy in; the kernels write the "
-                               "outputs, ids and weights into the layer's mapped output buffer; sync per step)"}
+                      "entry": "moe_decode_host (pinned host buffers: a kernel copies x from the layer's mapped "
+                               "input buffer; the kernels write the outputs, ids and weights into its mapped "
+                               "output buffer; sync per step)"}
 
         if rank == 0 and world == 1:
             out["cpu_baseline"] = cpu_baseline(wl, s)
