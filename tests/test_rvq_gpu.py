@@ -143,3 +143,31 @@ def test_rvq_records_through_the_cache(B, steps, n_slots):
     assert st["evictions"] > 0 and st["hits"] > 0
     cl.close()
     dl.close()
+
+
+@pytest.mark.parametrize("B", [1, 3])
+def test_rvq_host_entry_matches_device_entry(B):
+    """moe_decode_host on a 3-bit layer over several calls with changing
+    inputs (the first call plain, later ones replaying the captured step:
+    x staged by a kernel that the single-token router overlaps, outputs
+    written into mapped host memory) equals moe_decode on the same inputs,
+    and the oracle."""
+    shape = synth.Shape(320, 16, 4, 192, 128)
+    hl = HostLayerRVQ(shape, seed=12, beta=synth.beta_normal(12, 0, shape.E))
+    orc = hl.oracle()
+    dl = device_rvq(hl, 4)
+    for rep in range(4):
+        xs = np.stack([hidden_with_margin(orc, 12, rep, t) for t in range(B)])
+        of, ob, ids, w = run(dl, xs)
+        hob = np.zeros((B, shape.H), np.uint16)
+        hof = np.zeros((B, shape.H), np.float32)
+        hids = np.zeros((B, shape.k), np.int32)
+        hw = np.zeros((B, shape.k), np.float32)
+        moe.moe_decode_host(dl.handle, xs.ctypes.data, B, hob.ctypes.data, hof.ctypes.data, hids.ctypes.data,
+                            hw.ctypes.data, dl.ws.data_ptr(), dl.ws_bytes, None)
+        assert np.array_equal(hob, ob) and np.array_equal(hof, of)
+        assert np.array_equal(hids, ids) and np.array_equal(hw, w)
+        for t in range(B):
+            assert_token(t, hof, hob, hids, hw, *orc.token(xs[t]))
+    assert dl.check() == moe.MOE_OK, moe.last_error()
+    dl.close()
