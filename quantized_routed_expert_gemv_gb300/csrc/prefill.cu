@@ -335,6 +335,52 @@ __device__ __forceinline__ bool pg_item(const LayerArgs& a, int it, int nblk, in
   return true;
 }
 
+// Order of a CTA's items.  The shared expert's items (the first S of the
+// list) each cost several routed items: blocks of up to 64 tokens against
+// about 16, and in the down GEMM K = Fs against F.  With S < G CTAs, CTA
+// c < S takes shared item c first and then sits out the first K rounds of
+// the routed items, which the other G - S CTAs share; every routed item is
+// still taken exactly once.  An item's cost is modelled as its 128-K chunks
+// x (tokens + 16), and K is the rounded cost ratio minus one.  Every role
+// of a CTA walks the same sequence.
+struct PgSched {
+  int S, R, G, K;
+};
+
+template <int MODE>
+__device__ __forceinline__ PgSched pg_sched_of(const LayerArgs& a, int nblk, int nsb) {
+  PgSched p;
+  p.G = static_cast<int>(gridDim.x);
+  p.S = nsb * (MODE == 0 ? a.Fs / 64 : a.H / 128);
+  p.R = (nblk - nsb) * (MODE == 0 ? a.F / 64 : a.H / 128);
+  p.K = 0;
+  if (p.S > 0 && p.S < p.G && p.R > 0) {
+    const int np_s = min(kBlkTokens, round16(a.T));
+    const int nch_s = (MODE == 0 ? a.H : a.Fs) / 128, nch_r = (MODE == 0 ? a.H : a.F) / 128;
+    const int w = (nch_s * (np_s + 16) + nch_r * 16) / (nch_r * 32);
+    p.K = max(0, min(w - 1, p.R / (p.G - p.S)));
+  }
+  return p;
+}
+
+// Item index of CTA c's j-th item, -1 past its last.
+__device__ __forceinline__ int pg_next(const PgSched& p, int c, int j) {
+  long long r;
+  if (p.K == 0) {
+    r = c + static_cast<long long>(j) * p.G;
+    return r < p.S + p.R ? static_cast<int>(r) : -1;
+  }
+  if (c < p.S) {
+    if (j == 0) return c;
+    r = static_cast<long long>(p.K) * (p.G - p.S) + static_cast<long long>(j - 1) * p.G + c;
+  } else if (j < p.K) {
+    r = static_cast<long long>(j) * (p.G - p.S) + (c - p.S);
+  } else {
+    r = static_cast<long long>(p.K) * (p.G - p.S) + static_cast<long long>(j - p.K) * p.G + c;
+  }
+  return r < p.R ? p.S + static_cast<int>(r) : -1;
+}
+
 // Waits for a phase; gives up (and tells every other role through `abort`)
 // after the bounded limit or when another role already gave up.
 __device__ __forceinline__ bool pg_wait(uint64_t* bar, uint32_t parity, volatile int* abort, unsigned* err) {
@@ -441,7 +487,8 @@ __global__ void __maxnreg__(168)
   nblk = max(0, nblk);
   nsb = min(max(0, nsb), nblk);
   const int H = a.H;
-  const int n_items = MODE == 0 ? nsb * (a.Fs / 64) + (nblk - nsb) * (a.F / 64) : nblk * (H / 128);
+  const PgSched ps = pg_sched_of<MODE>(a, nblk, nsb);
+  const int cta = static_cast<int>(blockIdx.x);
 
   if (warp == kProdWarp) {
     // ------------------------------------------------------------ codes
@@ -449,14 +496,14 @@ __global__ void __maxnreg__(168)
     RingPos pc, pg;
     int issued = 0;
     bool stop = false;
-    for (int it = blockIdx.x; it < n_items && !stop; it += gridDim.x) {
+    for (int j = 0, it; !stop && (it = pg_next(ps, cta, j)) >= 0; ++j) {
       PgItem I;
       if (!pg_item<MODE>(a, it, nblk, nsb, I)) break;
       if (lane == 0) {  // this item's rows (first item only) and the next item's, into L2
         PgItem J;
-        if (it == blockIdx.x) prefetch_item<MODE>(I, H);
-        if (it + static_cast<int>(gridDim.x) < n_items && pg_item<MODE>(a, it + gridDim.x, nblk, nsb, J))
-          prefetch_item<MODE>(J, H);
+        if (j == 0) prefetch_item<MODE>(I, H);
+        const int itn = pg_next(ps, cta, j + 1);
+        if (itn >= 0 && pg_item<MODE>(a, itn, nblk, nsb, J)) prefetch_item<MODE>(J, H);
       }
       const int np = I.blk.np;
       const float* gsum = MODE == 0 ? a.pf.sx + static_cast<size_t>(I.blk.xrow) * (H / 64) : a.pf.sh + I.blk.hoff / 64;
@@ -500,7 +547,7 @@ __global__ void __maxnreg__(168)
     const int dw = warp - kDqWarp0, t = dw * 32 + lane;
     RingPos pc, pa;
     int cc = 0;
-    for (int it = blockIdx.x; it < n_items && !*s_abort; it += gridDim.x) {
+    for (int j = 0, it; !*s_abort && (it = pg_next(ps, cta, j)) >= 0; ++j) {
       PgItem I;
       if (!pg_item<MODE>(a, it, nblk, nsb, I)) break;
       bool stop = false;
@@ -552,7 +599,7 @@ __global__ void __maxnreg__(168)
       RingPos pb;
       int issued = 0;
       bool stop = false;
-      for (int it = blockIdx.x; it < n_items && !stop; it += gridDim.x) {
+      for (int j = 0, it; !stop && (it = pg_next(ps, cta, j)) >= 0; ++j) {
         PgItem I;
         if (!pg_item<MODE>(a, it, nblk, nsb, I)) break;
         const int np = I.blk.np;
@@ -592,7 +639,7 @@ __global__ void __maxnreg__(168)
       RingPos pa, pb;
       int cc = 0, units = 0;
       bool stop = false;
-      for (int it = blockIdx.x; it < n_items && !stop; it += gridDim.x) {
+      for (int j = 0, it; !stop && (it = pg_next(ps, cta, j)) >= 0; ++j) {
         PgItem I;
         if (!pg_item<MODE>(a, it, nblk, nsb, I)) break;
         const int np = I.blk.np, U = unit_chunks(np);
@@ -654,7 +701,7 @@ __global__ void __maxnreg__(168)
     RingPos pg;
     int units = 0;
     bool stop = false;
-    for (int it = blockIdx.x; it < n_items && !stop; it += gridDim.x) {
+    for (int j = 0, it; !stop && (it = pg_next(ps, cta, j)) >= 0; ++j) {
       PgItem I;
       if (!pg_item<MODE>(a, it, nblk, nsb, I)) break;
       const int np = I.blk.np, U = unit_chunks(np);
