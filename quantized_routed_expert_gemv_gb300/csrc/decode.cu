@@ -80,15 +80,18 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const __grid_con
   const bool act = g < G && c < nchunk;
   float* red = rsm;  // [G][NT][kRouterRows][WPR]
 
-  if (blockIdx.x < a.xq_nconv) {
+  // The last xq_nconv CTAs convert the tokens; the ones before them compute
+  // the logits, so the top-k never waits for a conversion.
+  const int nlog = static_cast<int>(gridDim.x) - a.xq_nconv;
+  if (static_cast<int>(blockIdx.x) >= nlog) {
     // The few-token fused kernel (decode_bt.cu) reads every token's
-    // activations in the fixed-point chunk form of gemv.cuh: CTAs below
-    // xq_nconv write them once ([T][4 kinds][C] words, then [T][C] (2^e,
-    // plain sum)) and count themselves done on ctl[10] (release).
-    const int C = H >> 5, n = T * C;
+    // activations in the fixed-point chunk form of gemv.cuh: these CTAs
+    // write them once ([T][4 kinds][C] words, then [T][C] (2^e, plain sum))
+    // and count themselves done on ctl[10] (release).
+    const int C = H >> 5, n = T * C, ci = static_cast<int>(blockIdx.x) - nlog;
     uint4* xw = reinterpret_cast<uint4*>(a.ws.xq);
     float2* xs = reinterpret_cast<float2*>(a.ws.xq + static_cast<size_t>(T) * C * 64);
-    for (int i = blockIdx.x * kRouterThreads + tid; i < n; i += a.xq_nconv * kRouterThreads) {
+    for (int i = ci * kRouterThreads + tid; i < n; i += a.xq_nconv * kRouterThreads) {
       const int t = i / C, c = i - t * C;
       const uint4* v = reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(t) * H + c * 32);
       float xv[32], sx = 0.f;
@@ -112,12 +115,13 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const __grid_con
     __threadfence();
     __syncthreads();
     if (tid == 0) red_add_release_gpu(&a.ws.ctl[10], 1u);
+    return;
   }
 
-  // The grid is (row blocks of kRouterRows experts) x (token blocks): a CTA
-  // loads its router rows once and walks its share of the token passes.
+  // The logits grid is (row blocks of kRouterRows experts) x (token blocks):
+  // a CTA loads its router rows once and walks its share of the token passes.
   const int RB = (E + kRouterRows - 1) / kRouterRows;
-  const int TB = max(1, static_cast<int>(gridDim.x) / RB);
+  const int TB = max(1, nlog / RB);
   const int rb = blockIdx.x % RB, tb = blockIdx.x / RB;
   const int er0 = rb * kRouterRows;
   const int TP = NT * G;  // tokens per pass
@@ -877,7 +881,8 @@ static cudaError_t launch_router_g(const LayerArgs& a, int num_sms, cudaStream_t
   else
     fn = kpl == 4 ? (const void*)router_kernel<2, 4> : kpl == 8 ? (const void*)router_kernel<2, 8>
        : kpl == 16 ? (const void*)router_kernel<2, 16> : (const void*)router_kernel<2, 32>;
-  return launch_ex(fn, dim3(rgrid), dim3(kRouterThreads), router_smem_bytes(a.E), st, false, a);
+  // the conversion CTAs (few-token fused path) follow the logits CTAs
+  return launch_ex(fn, dim3(rgrid + a.xq_nconv), dim3(kRouterThreads), router_smem_bytes(a.E), st, false, a);
 }
 
 // The grouped kernels with 4 tokens per pass have 7 consumer warps, one
