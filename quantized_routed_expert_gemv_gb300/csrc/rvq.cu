@@ -26,10 +26,11 @@
 // lanes with one 8-row butterfly.  Partial sums per slice land in the
 // workspace; later kernels add them in a fixed order.
 //
-// Each kernel runs one CTA per SM over a flat list of 8-row batches of all
-// its units (a unit: one table, i.e. one token, matrix kind and slice), a
-// contiguous share of the list per CTA, so every SM gets the same number of
-// rows and builds at most a few tables.  One launch of each serves every
+// Each kernel runs one CTA per SM over the 8-row batches of all its units (a
+// unit: one table, i.e. one token, matrix kind and slice).  With at least two
+// CTAs per unit every CTA takes a contiguous part of one unit and builds one
+// table; otherwise the flat list of batches is cut into equal contiguous
+// shares and a CTA builds a few tables.  One launch of each serves every
 // token of the step:
 //   rvq_gateup_kernel   units (token, kind, slice): gate or up partial sums of
 //                       the token's routed experts and the shared expert; the
