@@ -7,10 +7,10 @@
 // the step is the single-token step's weight stream (the fused kernel of
 // decode_b1.cu) with a short token loop per item:
 //
-// router_kernel    (decode.cu) logits, top-k and the grouping by expert; its
-//                  first CTAs also write every token's activations in the
-//                  fixed-point chunk form of gemv.cuh once, and count
-//                  themselves done on a control word.
+// router_kernel    (decode.cu) logits, top-k and the grouping by expert;
+//                  CTAs of its own (after the logits CTAs) write every
+//                  token's activations in the fixed-point chunk form of
+//                  gemv.cuh once, and count themselves done on a control word.
 // ffn_bt_kernel    one persistent kernel over one claimed item list:
 //                  gate|up items (rth gate + rth up rows of one expert) and
 //                  down items (RTD rows of H of one expert's down matrix),
@@ -593,7 +593,8 @@ static cudaError_t mark_bt(const LayerArgs& a, int i, cudaStream_t st) {
 int decode_router_grid(const LayerArgs& a, int num_sms);
 cudaError_t launch_decode_router(const LayerArgs& a, int num_sms, cudaStream_t st);
 
-// Number of router CTAs that convert the tokens to fixed point.
+// Number of router CTAs that convert the tokens to fixed point (launched
+// after the logits CTAs).
 int bt_nconv(const LayerArgs& a, int num_sms) {
   const int chunks = a.T * (a.H / 32);
   return std::max(1, std::min(decode_router_grid(a, num_sms), (chunks + 511) / 512));

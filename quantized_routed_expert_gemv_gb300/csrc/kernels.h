@@ -124,7 +124,7 @@ struct LayerArgs {
   int f1_rt, f1_stage, f1_nst; // fused single-token kernel: down rows per item, stage bytes
                                // and count (f1_nst == 0: not planned)
   PrefillPtrs pf;              // prefill chunk scratch (tensor-core path)
-  int xq_nconv;                // router CTAs that write ws.xq (0: none)
+  int xq_nconv;                // router CTAs after the logits CTAs that write ws.xq (0: none)
   int x_pdl;                   // x is written by the kernel launched just before the single-
                                // token router (the host entry's staging kernel): the router is
                                // its programmatic dependent and waits for it before reading x
